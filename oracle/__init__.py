@@ -1,0 +1,276 @@
+"""ctypes binding of the plain-C CPU oracle (``dspark_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: imported by the test suite, the smoke check and the
+benchmark's CPU-baseline leg, never by the product library.  The oracle shares
+no code with the CUDA path; the only module both sides read is the seeded
+input generator.
+
+``build()`` compiles the C source with gcc (``-O2 -ffp-contract=off``, no
+fused multiply-add, single thread).  All wrappers take and return numpy
+arrays.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dspark_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libdspark_oracle.so")
+
+# status bits (same values as the library's device status word)
+ST_CAPACITY = 1
+ST_TOKEN_RANGE = 2
+ST_NAN_LOGIT = 4
+ST_BAD_INPUT = 8
+ST_BAD_LEN = 16
+ST_BAD_COST = 32
+ST_INFEASIBLE = 64
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/libdspark_oracle.so``."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _P(t):
+    return ctypes.POINTER(t)
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            f32p, f64p, i32p, u8p, u16p = (_P(ctypes.c_float), _P(ctypes.c_double),
+                                           _P(ctypes.c_int32), _P(ctypes.c_uint8),
+                                           _P(ctypes.c_uint16))
+            ci, cf, cd, cl = ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_int64
+            L.orc_sts.argtypes = [cf, cf]
+            L.orc_sts.restype = cf
+            L.orc_survival.argtypes = [f32p, f32p, ci, ci, cf, f32p, f32p, i32p]
+            L.orc_survival.restype = None
+            L.orc_plan_from_survivals.argtypes = [f32p, ci, ci, cf, ci, ci, ci, ci, ci, i32p, f64p,
+                                                  cd, cd, i32p, i32p, f64p, f64p, f64p, u8p, i32p]
+            L.orc_plan_from_survivals.restype = ci
+            L.orc_plan.argtypes = [f32p, f32p, ci, ci, cf, ci, ci, ci, ci, ci, i32p, f64p, cd, cd,
+                                   f32p, i32p, i32p, f64p, i32p]
+            L.orc_plan.restype = ci
+            L.orc_pack.argtypes = [i32p, i32p, i32p, i32p, ci, ci, i32p, ci, ci, i32p, i32p, i32p,
+                                   i32p, i32p, i32p, i32p]
+            L.orc_pack.restype = None
+            L.orc_argmax_rows_f32.argtypes = [f32p, cl, ci, ci, i32p, i32p]
+            L.orc_argmax_rows_f32.restype = None
+            L.orc_argmax_rows_bf16.argtypes = [u16p, cl, ci, ci, i32p, i32p]
+            L.orc_argmax_rows_bf16.restype = None
+            L.orc_greedy_finalize.argtypes = [i32p, ci, i32p, i32p, i32p, ci, ci, ci, i32p, i32p,
+                                              i32p, i32p, i32p, i32p]
+            L.orc_greedy_finalize.restype = None
+            L.orc_cap_finalize.argtypes = [i32p, i32p, i32p, i32p, ci, ci, ci, i32p, i32p, i32p,
+                                           i32p, i32p, i32p, i32p, i32p]
+            L.orc_cap_finalize.restype = None
+            _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray | None, ctype):
+    if a is None:
+        return ctypes.cast(None, ctypes.POINTER(ctype))
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ------------------------------------------------------------------ planner
+
+def sts(z: float, T: float) -> float:
+    return float(lib().orc_sts(ctypes.c_float(z), ctypes.c_float(T)))
+
+
+def survival(z, T, eps):
+    """Returns (s_raw, s_out, status) for confidence logits z [B, gamma]."""
+    z = _c(z, np.float32)
+    T = _c(T, np.float32)
+    B, g = z.shape
+    s_raw = np.empty((B, g), np.float32)
+    s_out = np.empty((B, g), np.float32)
+    st = np.zeros(1, np.int32)
+    lib().orc_survival(_ptr(z, ctypes.c_float), _ptr(T, ctypes.c_float), B, g, float(eps),
+                       _ptr(s_raw, ctypes.c_float), _ptr(s_out, ctypes.c_float),
+                       _ptr(st, ctypes.c_int32))
+    return s_raw, s_out, int(st[0])
+
+
+class PlanResult(dict):
+    __getattr__ = dict.__getitem__
+
+
+def plan_from_survivals(s_raw, eps, min_len, max_len, forced, kind, M, val, bias=0.0, alpha=0.0):
+    s_raw = _c(s_raw, np.float32)
+    B, g = s_raw.shape
+    M = _c(M, np.int32)
+    val = _c(val, np.float64)
+    lens = np.empty(B, np.int32)
+    budget = np.zeros(1, np.int32)
+    tt = np.zeros(2, np.float64)
+    tau = np.zeros(B * g + 1, np.float64)
+    theta = np.zeros(B * g + 1, np.float64)
+    feas = np.zeros(B * g + 1, np.uint8)
+    st = np.zeros(1, np.int32)
+    n_kept = lib().orc_plan_from_survivals(
+        _ptr(s_raw, ctypes.c_float), B, g, float(eps), int(min_len), int(max_len), int(forced),
+        int(kind), int(M.size), _ptr(M, ctypes.c_int32), _ptr(val, ctypes.c_double), float(bias),
+        float(alpha), _ptr(lens, ctypes.c_int32), _ptr(budget, ctypes.c_int32),
+        _ptr(tt, ctypes.c_double), _ptr(tau, ctypes.c_double), _ptr(theta, ctypes.c_double),
+        _ptr(feas, ctypes.c_uint8), _ptr(st, ctypes.c_int32))
+    return PlanResult(verify_lens=lens, budget=int(budget[0]), tau=float(tt[0]),
+                      theta=float(tt[1]), tau_curve=tau[:n_kept + 1],
+                      theta_curve=theta[:n_kept + 1], feasible=feas[:n_kept + 1].astype(bool),
+                      n_kept=int(n_kept), status=int(st[0]))
+
+
+def plan(z, T, eps, min_len, max_len, forced, kind, M, val, bias=0.0, alpha=0.0):
+    z = _c(z, np.float32)
+    T = _c(T, np.float32)
+    B, g = z.shape
+    M = _c(M, np.int32)
+    val = _c(val, np.float64)
+    s = np.empty((B, g), np.float32)
+    lens = np.empty(B, np.int32)
+    budget = np.zeros(1, np.int32)
+    tt = np.zeros(2, np.float64)
+    st = np.zeros(1, np.int32)
+    n_kept = lib().orc_plan(
+        _ptr(z, ctypes.c_float), _ptr(T, ctypes.c_float), B, g, float(eps), int(min_len),
+        int(max_len), int(forced), int(kind), int(M.size), _ptr(M, ctypes.c_int32),
+        _ptr(val, ctypes.c_double), float(bias), float(alpha), _ptr(s, ctypes.c_float),
+        _ptr(lens, ctypes.c_int32), _ptr(budget, ctypes.c_int32), _ptr(tt, ctypes.c_double),
+        _ptr(st, ctypes.c_int32))
+    return PlanResult(survivals=s, verify_lens=lens, budget=int(budget[0]), tau=float(tt[0]),
+                      theta=float(tt[1]), n_kept=int(n_kept), status=int(st[0]))
+
+
+def plan_step(step):
+    """Run the planner on a ``workloads.StepInputs``."""
+    w, c = step.workload, step.cost
+    return plan(step.conf_logits, step.sts_temps, w.survival_eps, w.min_verify_len, w.max_len,
+                w.forced_budget, c.kind, c.M, c.val, c.bias_ms, c.alpha_ms)
+
+
+# --------------------------------------------------------------------- pack
+
+def pack(anchor, draft, prefix, lens, tiers, capacity, sentinel=-7):
+    anchor, prefix, lens = _c(anchor, np.int32), _c(prefix, np.int32), _c(lens, np.int32)
+    draft = _c(draft, np.int32)
+    tiers = _c(tiers, np.int32)
+    B, g = draft.shape
+    outs = [np.full(capacity, sentinel, np.int32) for _ in range(4)]
+    cu = np.empty(B + 1, np.int32)
+    totals = np.zeros(2, np.int32)
+    st = np.zeros(1, np.int32)
+    lib().orc_pack(_ptr(anchor, ctypes.c_int32), _ptr(draft, ctypes.c_int32),
+                   _ptr(prefix, ctypes.c_int32), _ptr(lens, ctypes.c_int32), B, g,
+                   _ptr(tiers if tiers.size else np.zeros(1, np.int32), ctypes.c_int32),
+                   int(tiers.size), int(capacity), *[_ptr(o, ctypes.c_int32) for o in outs],
+                   _ptr(cu, ctypes.c_int32), _ptr(totals, ctypes.c_int32),
+                   _ptr(st, ctypes.c_int32))
+    return PlanResult(ids=outs[0], pos=outs[1], req=outs[2], src=outs[3], cu_seqlens=cu,
+                      total=int(totals[0]), padded=int(totals[1]), status=int(st[0]))
+
+
+# ------------------------------------------------------------------- accept
+
+def argmax_rows(logits, V=None, rows=None, dtype=None):
+    """Row argmax; ``logits`` is float32 [rows, ld] or uint16 bf16 bits."""
+    logits = np.ascontiguousarray(logits)
+    n, ld = logits.shape
+    V = ld if V is None else V
+    rows = n if rows is None else rows
+    am = np.zeros(max(rows, 1), np.int32)
+    st = np.zeros(1, np.int32)
+    if logits.dtype == np.float32:
+        lib().orc_argmax_rows_f32(_ptr(logits, ctypes.c_float), ld, V, rows,
+                                  _ptr(am, ctypes.c_int32), _ptr(st, ctypes.c_int32))
+    elif logits.dtype == np.uint16:
+        lib().orc_argmax_rows_bf16(_ptr(logits, ctypes.c_uint16), ld, V, rows,
+                                   _ptr(am, ctypes.c_int32), _ptr(st, ctypes.c_int32))
+    else:
+        raise TypeError(logits.dtype)
+    return am[:rows], int(st[0])
+
+
+def greedy_finalize(am, rows, cu, draft, prefix, V):
+    draft = _c(draft, np.int32)
+    B, g = draft.shape
+    am = _c(am if len(am) else np.zeros(1, np.int32), np.int32)
+    cu = _c(cu, np.int32)
+    prefix = _c(prefix, np.int32)
+    o = [np.empty(B, np.int32) for _ in range(4)]
+    out = np.empty((B, g + 1), np.int32)
+    st = np.zeros(1, np.int32)
+    lib().orc_greedy_finalize(_ptr(am, ctypes.c_int32), int(rows), _ptr(cu, ctypes.c_int32),
+                              _ptr(draft, ctypes.c_int32), _ptr(prefix, ctypes.c_int32), B, g,
+                              int(V), *[_ptr(x, ctypes.c_int32) for x in o],
+                              _ptr(out, ctypes.c_int32), _ptr(st, ctypes.c_int32))
+    return PlanResult(num_accepted=o[0], bonus=o[1], commit_lens=o[2], new_seq_lens=o[3],
+                      out_tokens=out, status=int(st[0]))
+
+
+def greedy_accept(logits, V, cu, draft, prefix, max_rows=None):
+    """Compact-mode accept: argmax of rows [0, min(cu[B], max_rows)), then
+    the per-request first mismatch, finalize and out tokens."""
+    cu = _c(cu, np.int32)
+    B = cu.size - 1
+    max_rows = logits.shape[0] if max_rows is None else max_rows
+    want = int(cu[B])
+    status = 0
+    rows = max(0, min(want, max_rows))
+    if want > max_rows:
+        status |= ST_CAPACITY
+    am, st = argmax_rows(logits, V=V, rows=rows)
+    fin = greedy_finalize(am, rows, cu, draft, prefix, V)
+    fin["argmax"] = am
+    fin["status"] = fin.status | st | status
+    return fin
+
+
+def cap_accept(logits, V, lens, draft, prefix):
+    draft = _c(draft, np.int32)
+    B, g = draft.shape
+    am, st = argmax_rows(logits, V=V, rows=B * (g + 1))
+    lens = _c(lens, np.int32)
+    prefix = _c(prefix, np.int32)
+    o = [np.empty(B, np.int32) for _ in range(5)]
+    out = np.empty((B, g + 1), np.int32)
+    totals = np.zeros(2, np.int32)
+    st2 = np.zeros(1, np.int32)
+    lib().orc_cap_finalize(_ptr(am, ctypes.c_int32), _ptr(lens, ctypes.c_int32),
+                           _ptr(draft, ctypes.c_int32), _ptr(prefix, ctypes.c_int32), B, g,
+                           int(V), *[_ptr(x, ctypes.c_int32) for x in o[:4]],
+                           _ptr(out, ctypes.c_int32), _ptr(o[4], ctypes.c_int32),
+                           _ptr(totals, ctypes.c_int32), _ptr(st2, ctypes.c_int32))
+    return PlanResult(argmax=am, num_accepted=o[0], bonus=o[1], commit_lens=o[2],
+                      new_seq_lens=o[3], out_tokens=out, ceiling=o[4],
+                      sum_commit=int(totals[0]), sum_ceiling=int(totals[1]),
+                      status=st | int(st2[0]))

@@ -1,0 +1,434 @@
+/*
+ * dspark_oracle.c -- plain, slow, single-threaded CPU oracle for the DSpark
+ * verify planner, ragged verify pack and greedy / cap-accept.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this file.  The product path (the CUDA
+ * library) never links, calls or executes it, and it shares no code, header,
+ * table or helper with that path.
+ *
+ * Every function restates a definition from the pages it cites, in the order
+ * the pages give the steps, with no blocking, fusion or reordering:
+ *
+ *   [AVS]   "DSpark 自适应 Verify 怎样分配候选预算" (DSpark adaptive verify:
+ *           how the candidate budget is allocated), akiyangdev.github.io
+ *   [ROUND] "DeepSeek-V4 DSpark一轮 Draft、Verify、Accept 与 Commit" (one
+ *           DSpark round: draft, verify, accept and commit), akiyangdev.github.io
+ *   [SGL]   "DSpark接入SGLang：用置信度驱动可变长度验证" (DSpark in SGLang:
+ *           confidence-driven variable-length verify), yingzheng.com review
+ *   [TUT]   charlestar.github.io tutorial "DSpark confidence-scheduled
+ *           speculative decoding"
+ *
+ * Arithmetic: STS division and the survival product in IEEE fp32 (the
+ * planner's tensors are fp32 on the pages), the sigmoid in fp64 rounded once
+ * to fp32, the tau prefix sum and theta in fp64.  Build with
+ * -ffp-contract=off so that no multiply-add is fused.
+ *
+ * Readings of points the pages leave open (each also listed in the design
+ * notes):
+ *   R1 sigmoid precision: c = (float)(1 / (1 + exp(-(double)t))).
+ *   R2 depths k >= max_verify_len-1 cannot be verified and are not budget
+ *      candidates.
+ *   R3 tau is summed in fp64; with every kept survival >= 2^-14 and
+ *      B + B*gamma <= 2^16 every partial sum is exact.
+ *   R4 1-D SPS lookup below the first sample uses sample 0; additive lookup
+ *      above the largest tier is infeasible; an entry whose SPS or total step
+ *      time is not a positive finite number is infeasible and flagged.
+ *   R5 argmax ties go to the smaller budget; a forced budget is clipped to
+ *      the largest in-range budget.
+ *   R6 clamps to [min_verify_len, max_verify_len] are applied after the
+ *      top-b selection.
+ *   R7 argmax over a logits row: the lowest index of the largest non-NaN
+ *      value, -0 equal to +0; a row with no value above -inf returns 0.
+ *   R8 out_tokens[r][gamma] is -1 before the bonus scatter; pad rows carry
+ *      id 0, position 0, request -1, source -1.
+ *
+ * Parity pins: every function below is pinned in the oracle's CPU tests
+ * against the pages' worked examples, closed forms or brute force.
+ */
+
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* status flags (the library's device status word uses the same bit values,
+ * which are part of the call interface) */
+#define ORC_ST_CAPACITY    1
+#define ORC_ST_TOKEN_RANGE 2
+#define ORC_ST_NAN_LOGIT   4
+#define ORC_ST_BAD_INPUT   8
+#define ORC_ST_BAD_LEN     16
+#define ORC_ST_BAD_COST    32
+#define ORC_ST_INFEASIBLE  64
+
+/* ------------------------------------------------------------------ STS */
+
+/* One STS-calibrated conditional confidence: c = sigmoid(z / T).
+ * [AVS] §二 "STS 更像运行时语义桥" (runtime formula c_i = sigmoid(z_i / T_i)). */
+float orc_sts(float z, float T)
+{
+    float t = z / T;                               /* fp32 IEEE division */
+    double c = 1.0 / (1.0 + exp(-(double)t));      /* reading R1 */
+    return (float)c;
+}
+
+/* Prefix survivals S_k = prod_{i<=k} c_i per request, in sequential order.
+ * [AVS] §一 (same-request survival is a cumulative product) and §二 (S_k);
+ * [TUT] "接受是一件前缀事件" (prefix survival table).
+ * s_raw receives the product itself; s_out the product with values below
+ * survival_eps set to 0 ([AVS] §三, sixth deviation: eps treats tiny
+ * survivals as 0). */
+void orc_survival(const float *z, const float *T, int B, int gamma, float eps,
+                  float *s_raw, float *s_out, int *status)
+{
+    for (int k = 0; k < gamma; ++k)
+        if (!(T[k] > 0.0f)) *status |= ORC_ST_BAD_INPUT;
+    for (int r = 0; r < B; ++r) {
+        float run = 0.0f;
+        for (int k = 0; k < gamma; ++k) {
+            float zk = z[(size_t)r * gamma + k];
+            if (zk != zk) *status |= ORC_ST_BAD_INPUT;
+            float c = orc_sts(zk, T[k]);
+            run = (k == 0) ? c : run * c;
+            s_raw[(size_t)r * gamma + k] = run;
+            s_out[(size_t)r * gamma + k] = (run >= eps) ? run : 0.0f;
+        }
+    }
+}
+
+/* ---------------------------------------------------------------- plan */
+
+typedef struct { float s; int k; int r; } orc_cand;
+
+/* Global order of candidates: survival descending; equal survivals go to the
+ * earlier position, then to the lower request id.  [AVS] §一 (sort from high
+ * to low; ties prefer the earlier position, then the request number). */
+static int orc_cand_cmp(const void *a, const void *b)
+{
+    const orc_cand *x = (const orc_cand *)a, *y = (const orc_cand *)b;
+    if (x->s > y->s) return -1;
+    if (x->s < y->s) return 1;
+    if (x->k != y->k) return x->k < y->k ? -1 : 1;
+    if (x->r != y->r) return x->r < y->r ? -1 : 1;
+    return 0;
+}
+
+/* theta(b) for one budget.  [AVS] §一: 1-D table theta = tau(b) * SPS(B+b);
+ * additive table theta = tau(b) / T(B, B+b).  [AVS] §四 "1D SpsCostTable"
+ * (floor lookup, no interpolation) and "Additive SPS" (T = bias + alpha(B) +
+ * theta(M)); [TUT] "调度器要比较期望收益与边际成本" (M = bs + K).
+ * Returns 1 if b is feasible and writes theta; sets *bad when the entry used
+ * holds an invalid value (reading R4). */
+static int orc_theta(double tau, int B, int b, int kind, int n, const int32_t *M,
+                     const double *val, double bias, double alpha, double *theta, int *bad)
+{
+    long Mv = (long)B + b;
+    if (kind == 0) {
+        int j = -1;
+        for (int i = 0; i < n; ++i)
+            if (M[i] <= Mv) j = i;
+        if (j < 0) j = 0;
+        double sps = val[j];
+        if (!(sps > 0.0) || !isfinite(sps)) { *bad = 1; return 0; }
+        *theta = tau * sps;
+        return 1;
+    } else {
+        int j = -1;
+        for (int i = 0; i < n; ++i)
+            if (M[i] >= Mv) { j = i; break; }
+        if (j < 0) return 0;                       /* above the largest tier */
+        double T = (bias + alpha) + val[j];
+        if (!(T > 0.0) || !isfinite(T)) { *bad = 1; return 0; }
+        *theta = tau / T;
+        return 1;
+    }
+}
+
+/* Budget choice and ScheduleVerifyLensTopk from given survivals (s_raw as
+ * produced by orc_survival, i.e. before the eps zeroing).
+ *   [AVS] §一: tau(b) = B + sum_{i<=b} s_i over survivals sorted descending;
+ *   budget = argmax_b theta(b); ScheduleVerifyLensTopk hands the budget to
+ *   requests by the same order; verify_len = root + selected candidates,
+ *   bounded by min/max_verify_len and survival_eps.
+ * tau_curve / theta_curve / feasible (each of size B*gamma+1) and n_kept are
+ * optional diagnostics.  Returns the number of kept candidates. */
+int orc_plan_from_survivals(const float *s_raw, int B, int gamma, float eps, int min_len,
+                            int max_len, int forced, int kind, int n, const int32_t *M,
+                            const double *val, double bias, double alpha, int32_t *verify_lens,
+                            int32_t *budget_out, double *tau_theta, double *tau_curve,
+                            double *theta_curve, uint8_t *feasible_curve, int *status)
+{
+    size_t NT = (size_t)B * gamma;
+    orc_cand *cand = (orc_cand *)malloc(sizeof(orc_cand) * (NT ? NT : 1));
+    double *tau = (double *)malloc(sizeof(double) * (NT + 1));
+    double *theta = (double *)malloc(sizeof(double) * (NT + 1));
+    uint8_t *feas = (uint8_t *)malloc(NT + 1);
+    int32_t *cnt = (int32_t *)calloc((size_t)B, sizeof(int32_t));
+
+    /* candidates: s >= eps (eps drop) and a verifiable depth (reading R2) */
+    int N = 0;
+    for (int r = 0; r < B; ++r)
+        for (int k = 0; k < gamma; ++k) {
+            float s = s_raw[(size_t)r * gamma + k];
+            if (k < max_len - 1 && s >= eps) {
+                cand[N].s = s; cand[N].k = k; cand[N].r = r; ++N;
+            }
+        }
+    qsort(cand, (size_t)N, sizeof(orc_cand), orc_cand_cmp);
+
+    /* tau(b) = B + sum of the b largest survivals, fp64, sequential (R3) */
+    tau[0] = (double)B;
+    for (int b = 1; b <= N; ++b) tau[b] = tau[b - 1] + (double)cand[b - 1].s;
+
+    /* the cost table must list strictly ascending M */
+    int table_ok = n >= 1;
+    for (int i = 1; i < n; ++i)
+        if (!(M[i] > M[i - 1])) table_ok = 0;
+    if (!table_ok) *status |= ORC_ST_BAD_COST;
+
+    int bad = 0;
+    for (int b = 0; b <= N; ++b) {
+        theta[b] = 0.0;
+        feas[b] = table_ok ? (uint8_t)orc_theta(tau[b], B, b, kind, n, M, val, bias, alpha,
+                                                &theta[b], &bad)
+                           : 0;
+    }
+    if (bad) *status |= ORC_ST_BAD_COST;
+
+    int budget;
+    if (forced < 0) {
+        double best = -INFINITY;
+        budget = -1;
+        for (int b = 0; b <= N; ++b)
+            if (feas[b] && theta[b] > best) { best = theta[b]; budget = b; }
+        if (budget < 0) { budget = 0; *status |= ORC_ST_INFEASIBLE; }
+    } else {
+        long b_hi = N;
+        if (kind == 1 && n >= 1) {
+            long top = (long)M[n - 1] - B;
+            if (top < b_hi) b_hi = top;
+        }
+        if (!table_ok) b_hi = -1;
+        if (b_hi < 0) { budget = 0; *status |= ORC_ST_INFEASIBLE; }
+        else budget = forced < b_hi ? forced : (int)b_hi;
+    }
+
+    for (int i = 0; i < budget; ++i) cnt[cand[i].r] += 1;
+    for (int r = 0; r < B; ++r) {
+        int len = 1 + cnt[r];
+        if (len < min_len) len = min_len;
+        if (len > max_len) len = max_len;
+        verify_lens[r] = len;
+    }
+    *budget_out = budget;
+    tau_theta[0] = tau[budget];
+    tau_theta[1] = feas[budget] ? theta[budget] : 0.0;
+
+    if (tau_curve) memcpy(tau_curve, tau, sizeof(double) * (size_t)(N + 1));
+    if (theta_curve) memcpy(theta_curve, theta, sizeof(double) * (size_t)(N + 1));
+    if (feasible_curve) memcpy(feasible_curve, feas, (size_t)(N + 1));
+
+    free(cand); free(tau); free(theta); free(feas); free(cnt);
+    return N;
+}
+
+/* The whole planner: STS + survival, then budget and verify_lens. */
+int orc_plan(const float *z, const float *T, int B, int gamma, float eps, int min_len,
+             int max_len, int forced, int kind, int n, const int32_t *M, const double *val,
+             double bias, double alpha, float *survivals, int32_t *verify_lens,
+             int32_t *budget, double *tau_theta, int *status)
+{
+    size_t NT = (size_t)B * gamma;
+    float *s_raw = (float *)malloc(sizeof(float) * (NT ? NT : 1));
+    orc_survival(z, T, B, gamma, eps, s_raw, survivals, status);
+    int N = orc_plan_from_survivals(s_raw, B, gamma, eps, min_len, max_len, forced, kind, n, M,
+                                    val, bias, alpha, verify_lens, budget, tau_theta, NULL, NULL,
+                                    NULL, status);
+    free(s_raw);
+    return N;
+}
+
+/* ---------------------------------------------------------------- pack */
+
+/* Front-pack each request's anchor + selected draft prefix into compact
+ * verify rows with cu_seqlens, then round the packed total up to the
+ * smallest captured graph tier.
+ *   [ROUND] §三 (verify ids = [anchor, draft...]; compact ragged layout;
+ *   BuildRaggedVerifyWindow / compact_verify_ids), §四 (positions of the
+ *   verify window); [AVS] §六 (cu_seqlens_q = [0, 2, 3, 7] for lens
+ *   [2, 1, 4]); [SGL] "Ragged verify" (front-pack, round to the nearest
+ *   captured tier); [TUT] "变长批次如何与 CUDA Graph 共存" (37 -> 40 etc.).
+ * Row cu[r]+j: id = anchor[r] for j = 0, else draft[r][j-1];
+ * position = prefix_lens[r] + j; request = r; source = r*(gamma+1) + j. */
+void orc_pack(const int32_t *anchor, const int32_t *draft, const int32_t *prefix,
+              const int32_t *lens, int B, int gamma, const int32_t *tiers, int n_tiers,
+              int capacity, int32_t *ids, int32_t *pos, int32_t *req, int32_t *src,
+              int32_t *cu, int32_t *totals, int *status)
+{
+    cu[0] = 0;
+    for (int r = 0; r < B; ++r) {
+        int L = lens[r];
+        if (L < 1 || L > gamma + 1) {
+            *status |= ORC_ST_BAD_LEN;
+            L = L < 1 ? 1 : gamma + 1;
+        }
+        cu[r + 1] = cu[r] + L;
+        for (int j = 0; j < L; ++j) {
+            int dst = cu[r] + j;
+            if (dst >= capacity) { *status |= ORC_ST_CAPACITY; continue; }
+            ids[dst] = (j == 0) ? anchor[r] : draft[(size_t)r * gamma + (j - 1)];
+            pos[dst] = prefix[r] + j;
+            req[dst] = r;
+            src[dst] = r * (gamma + 1) + j;
+        }
+    }
+    int total = cu[B];
+    int padded = total;
+    if (n_tiers > 0) {
+        int found = 0;
+        for (int i = 0; i < n_tiers; ++i)
+            if (tiers[i] >= total) { padded = tiers[i]; found = 1; break; }
+        if (!found) *status |= ORC_ST_CAPACITY;
+    }
+    for (int i = total; i < padded; ++i) {
+        if (i >= capacity) { *status |= ORC_ST_CAPACITY; break; }
+        ids[i] = 0; pos[i] = 0; req[i] = -1; src[i] = -1;
+    }
+    totals[0] = total;
+    totals[1] = padded;
+}
+
+/* -------------------------------------------------------------- accept */
+
+static float orc_bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* target_predict = argmax(target_logits) per row ([ROUND] §五 "Greedy"),
+ * with the tie and NaN conventions of reading R7. */
+void orc_argmax_rows_f32(const float *x, int64_t ld, int V, int rows, int32_t *am, int *status)
+{
+    for (int i = 0; i < rows; ++i) {
+        const float *row = x + (size_t)i * (size_t)ld;
+        float best = -INFINITY;
+        int idx = 0;
+        for (int v = 0; v < V; ++v) {
+            float f = row[v];
+            if (f != f) { *status |= ORC_ST_NAN_LOGIT; continue; }
+            if (f > best) { best = f; idx = v; }
+        }
+        am[i] = idx;
+    }
+}
+
+void orc_argmax_rows_bf16(const uint16_t *x, int64_t ld, int V, int rows, int32_t *am, int *status)
+{
+    for (int i = 0; i < rows; ++i) {
+        const uint16_t *row = x + (size_t)i * (size_t)ld;
+        float best = -INFINITY;
+        int idx = 0;
+        for (int v = 0; v < V; ++v) {
+            float f = orc_bf16_to_f32(row[v]);
+            if (f != f) { *status |= ORC_ST_NAN_LOGIT; continue; }
+            if (f > best) { best = f; idx = v; }
+        }
+        am[i] = idx;
+    }
+}
+
+static void orc_check_tokens(const int32_t *draft, int B, int gamma, int V, int *status)
+{
+    for (size_t i = 0; i < (size_t)B * gamma; ++i)
+        if (draft[i] < 0 || draft[i] >= V) { *status |= ORC_ST_TOKEN_RANGE; return; }
+}
+
+/* Shared tail of both accept modes for one request: given the accepted draft
+ * count and the bonus, FinalizeAcceptLens and BuildOutTokens.
+ *   [ROUND] §五: commit_lens = correct_len + 1; new_seq_lens = prefix_lens +
+ *   commit_lens; out_tokens[:, :gamma] = drafts, then the bonus is scattered
+ *   at column correct_len. */
+static void orc_finish(int r, int correct, int bonus_tok, const int32_t *draft,
+                       const int32_t *prefix, int gamma, int32_t *num_acc, int32_t *bonus,
+                       int32_t *commit, int32_t *new_seq, int32_t *out)
+{
+    num_acc[r] = correct;
+    bonus[r] = bonus_tok;
+    commit[r] = correct + 1;
+    if (new_seq) new_seq[r] = prefix[r] + correct + 1;
+    for (int j = 0; j < gamma; ++j) out[(size_t)r * (gamma + 1) + j] = draft[(size_t)r * gamma + j];
+    out[(size_t)r * (gamma + 1) + gamma] = -1;
+    out[(size_t)r * (gamma + 1) + correct] = bonus_tok;
+}
+
+/* Compact-mode greedy accept over argmax rows of the packed window.
+ *   [ROUND] §五 "Greedy": correct_len counts the leading drafts equal to the
+ *   target chain's argmax; bonus is the prediction of the last valid input
+ *   row; no acceptance past the first mismatch ([AVS] §二, prefix_mask;
+ *   [TUT] "一次推测解码究竟节省了什么").
+ * Request r owns packed rows [cu[r], cu[r+1]); L = cu[r+1]-cu[r] rows verify
+ * L-1 drafts.  A request whose range is empty, longer than gamma+1 or past
+ * `rows` is flagged BAD_LEN and gets correct 0, bonus -1, commit 0. */
+void orc_greedy_finalize(const int32_t *am, int rows, const int32_t *cu, const int32_t *draft,
+                         const int32_t *prefix, int B, int gamma, int V, int32_t *num_acc,
+                         int32_t *bonus, int32_t *commit, int32_t *new_seq, int32_t *out,
+                         int *status)
+{
+    orc_check_tokens(draft, B, gamma, V, status);
+    for (int r = 0; r < B; ++r) {
+        int lo = cu[r], hi = cu[r + 1], L = hi - lo;
+        if (lo < 0 || hi > rows || L < 1 || L > gamma + 1) {
+            *status |= ORC_ST_BAD_LEN;
+            num_acc[r] = 0; bonus[r] = -1; commit[r] = 0;
+            if (new_seq) new_seq[r] = prefix[r];
+            for (int j = 0; j < gamma; ++j)
+                out[(size_t)r * (gamma + 1) + j] = draft[(size_t)r * gamma + j];
+            out[(size_t)r * (gamma + 1) + gamma] = -1;
+            continue;
+        }
+        int correct = L - 1;
+        for (int j = 0; j < L - 1; ++j)
+            if (am[lo + j] != draft[(size_t)r * gamma + j]) { correct = j; break; }
+        orc_finish(r, correct, am[lo + correct], draft, prefix, gamma, num_acc, bonus, commit,
+                   new_seq, out);
+    }
+}
+
+/* cap-accept: the full block is verified (rows r*(gamma+1)+j), the raw
+ * acceptance is the ceiling, and only the window commits:
+ * capped = min(raw, verify_len - 1).
+ *   [AVS] §三 "Cap 本身也没有破坏这个推导" and §五 "cap-accept" (lens
+ *   [2,1,4] at width 4 cap the drafts to [1,0,3]); [SGL] "三种 verify mode"
+ *   (same commits as compact, exposes the acceptance ceiling).
+ * totals[0] = sum of commit_lens, totals[1] = sum of (ceiling + 1). */
+void orc_cap_finalize(const int32_t *am, const int32_t *lens, const int32_t *draft,
+                      const int32_t *prefix, int B, int gamma, int V, int32_t *num_acc,
+                      int32_t *bonus, int32_t *commit, int32_t *new_seq, int32_t *out,
+                      int32_t *ceiling, int32_t *totals, int *status)
+{
+    orc_check_tokens(draft, B, gamma, V, status);
+    int sum_commit = 0, sum_ceiling = 0;
+    for (int r = 0; r < B; ++r) {
+        int base = r * (gamma + 1);
+        int raw = gamma;
+        for (int j = 0; j < gamma; ++j)
+            if (am[base + j] != draft[(size_t)r * gamma + j]) { raw = j; break; }
+        int len = lens[r];
+        if (len < 1 || len > gamma + 1) {
+            *status |= ORC_ST_BAD_LEN;
+            len = len < 1 ? 1 : gamma + 1;
+        }
+        int capped = raw < len - 1 ? raw : len - 1;
+        orc_finish(r, capped, am[base + capped], draft, prefix, gamma, num_acc, bonus, commit,
+                   new_seq, out);
+        ceiling[r] = raw;
+        sum_commit += capped + 1;
+        sum_ceiling += raw + 1;
+    }
+    totals[0] = sum_commit;
+    totals[1] = sum_ceiling;
+}

@@ -1,0 +1,448 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: values the
+pages print for a worked example (fixtures under tests/golden, each with its
+citation), closed forms, hand-derived table lookups, library routines for
+special cases (numpy's first-occurrence argmax, float32 accumulate) and brute
+force over every prefix-respecting allocation on tiny inputs.
+"""
+
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+from conftest import golden
+from confidence_scheduled_speculative_gb300 import workloads as wl
+
+EPS_MIN = 2.0 ** -14
+
+
+# ----------------------------------------------------------------------- STS
+
+def test_sts_closed_forms(orc):
+    # sigmoid(0) = 1/2 for any temperature
+    for T in (0.5, 1.0, 3.0):
+        assert orc.sts(0.0, T) == 0.5
+    ln3 = float(np.float32(math.log(3.0)))
+    # sigmoid(ln 3) = 3/4; dividing by T (not multiplying) keeps 3/4 at z=2ln3, T=2
+    assert abs(orc.sts(ln3, 1.0) - 0.75) < 1e-7
+    assert abs(orc.sts(2 * ln3, 2.0) - 0.75) < 1e-7
+    assert abs(orc.sts(ln3 / 2, 0.5) - 0.75) < 1e-7
+    # sign: sigmoid(-ln 3) = 1/4
+    assert abs(orc.sts(-ln3, 1.0) - 0.25) < 1e-7
+    # saturation
+    assert orc.sts(40.0, 1.0) == 1.0
+    assert 0.0 <= orc.sts(-120.0, 1.0) < 1e-30
+
+
+def test_sts_symmetry(orc):
+    rng = np.random.default_rng(3)
+    for z in rng.normal(0, 4, size=200).astype(np.float32):
+        a, b = orc.sts(float(z), 1.0), orc.sts(float(-z), 1.0)
+        assert abs((a + b) - 1.0) <= 2 * np.spacing(np.float32(1.0))
+
+
+def test_survival_pages_example(orc):
+    g = golden("planner_example.json")
+    z = wl.confidence_logits_for(np.array(g["confidences"]))
+    s_raw, s_out, st = orc.survival(z, np.ones(2, np.float32), 1e-4)
+    assert st == 0
+    np.testing.assert_allclose(s_raw, np.array(g["survivals"]), atol=1e-6, rtol=0)
+    np.testing.assert_array_equal(s_raw, s_out)
+
+
+def test_survival_table_of_tutorial(orc):
+    g = golden("survival_table.json")
+    c = np.array(g["c"])[None, :]
+    s_raw, _, _ = orc.survival(wl.confidence_logits_for(c), np.ones(c.shape[1], np.float32), 1e-4)
+    half = 0.5 * 10.0 ** -g["printed_decimals"]
+    for k, printed in enumerate(g["S_printed"]):
+        if k == g["slip_index"]:
+            # the page prints 0.665; the exact product 0.92*0.88*0.82 = 0.663872
+            assert abs(s_raw[0, k] - g["slip_exact"]) < 1e-6
+            assert abs(s_raw[0, k] - printed) > half
+        else:
+            assert abs(s_raw[0, k] - printed) <= half + 1e-6, (k, s_raw[0, k], printed)
+
+
+def test_survival_is_sequential_float32_product(orc):
+    rng = np.random.default_rng(11)
+    z = rng.normal(1.0, 1.5, size=(37, 9)).astype(np.float32)
+    T = (1.0 + 0.07 * np.arange(9)).astype(np.float32)
+    s_raw, _, _ = orc.survival(z, T, 1e-4)
+    c = np.array([[orc.sts(float(z[r, k]), float(T[k])) for k in range(9)] for r in range(37)],
+                 dtype=np.float32)
+    ref = np.multiply.accumulate(c, axis=1, dtype=np.float32)
+    np.testing.assert_array_equal(s_raw, ref)
+    # non-increasing per request
+    assert np.all(np.diff(s_raw, axis=1) <= 0)
+
+
+def test_eps_drop(orc):
+    z = np.full((3, 6), -2.0, np.float32)  # c ~ 0.119: survival falls below 1e-4 at depth 4
+    s_raw, s_out, _ = orc.survival(z, np.ones(6, np.float32), 1e-4)
+    keep = s_raw >= np.float32(1e-4)
+    assert keep[:, 0].all() and not keep[:, -1].any()
+    np.testing.assert_array_equal(s_out[keep], s_raw[keep])
+    assert np.all(s_out[~keep] == 0.0)
+
+
+def test_bad_temperature_is_flagged(orc):
+    _, _, st = orc.survival(np.zeros((1, 2), np.float32), np.array([1.0, 0.0], np.float32), 1e-4)
+    assert st & orc.ST_BAD_INPUT
+
+
+# -------------------------------------------------------------- planner
+
+def _f32(a):
+    return np.array(a, dtype=np.float32)
+
+
+def test_pages_example_allocation(orc):
+    g = golden("planner_example.json")
+    s = _f32(g["survivals"])
+    r = orc.plan_from_survivals(s, EPS_MIN, 1, 3, g["extra_budget"], wl.COST_SPS_1D, [1], [1.0])
+    assert r.budget == 2
+    assert list(r.verify_lens) == g["verify_lens"]
+    assert abs(r.tau - g["tau"]) < 1e-6
+    assert abs(r.tau_curve[3] - g["tau_budget3"]) < 1e-6
+
+
+def test_pages_example_budget_choice(orc):
+    """3.62 / 1 ms = 3620 beats 4.22 / 1.4 ms ~ 3014, so the 2-row budget wins."""
+    g = golden("planner_example.json")
+    s = _f32(g["survivals"])
+    B = 2
+    # 1-D SPS table over M = B + b: 1 ms at b=2, 1.4 ms at b=3, slow elsewhere
+    M = np.arange(B, B + 5, dtype=np.int32)
+    sps = np.array([1.0, 1.0, 1000.0 / g["step_ms"]["2"], 1000.0 / g["step_ms"]["3"], 1.0])
+    r = orc.plan_from_survivals(s, EPS_MIN, 1, 3, -1, wl.COST_SPS_1D, M, sps)
+    assert r.budget == g["chosen_budget"]
+    assert abs(r.theta - g["throughput"]["2"]) < 1e-6 * g["throughput"]["2"]
+    assert abs(r.theta_curve[3] - g["throughput"]["3"]) < g["throughput_b3_tolerance"]
+    assert list(r.verify_lens) == g["verify_lens"]
+
+
+def test_tie_order_depth_then_request(orc):
+    # two identical requests: ties go to the lower request id
+    s = _f32([[0.5, 0.25], [0.5, 0.25]])
+    lens = lambda b, s=s: list(orc.plan_from_survivals(s, EPS_MIN, 1, 3, b, 0, [1], [1.0]).verify_lens)
+    assert lens(1) == [2, 1]
+    assert lens(2) == [2, 2]
+    assert lens(3) == [3, 2]
+    # a depth-1 candidate of request 0 ties depth-0 candidates: earlier depth first
+    s2 = _f32([[0.5, 0.5], [0.5, 0.1]])
+    assert list(orc.plan_from_survivals(s2, EPS_MIN, 1, 3, 2, 0, [1], [1.0]).verify_lens) == [2, 2]
+    # equal depth, three requests
+    s3 = _f32([[0.3], [0.3], [0.3]])
+    assert list(orc.plan_from_survivals(s3, EPS_MIN, 1, 2, 2, 0, [1], [1.0]).verify_lens) == [2, 2, 1]
+
+
+def _best_sums_brute_force(s, eps, max_len):
+    """max over prefix-respecting allocations of the survival sum, per total b."""
+    B, g = s.shape
+    kept = [int(np.sum((s[r] >= eps) & (np.arange(g) < max_len - 1))) for r in range(B)]
+    best = {}
+    for alloc in itertools.product(*[range(k + 1) for k in kept]):
+        b = sum(alloc)
+        tot = sum(float(s[r, k]) for r in range(B) for k in range(alloc[r]))
+        if tot > best.get(b, -1.0):
+            best[b] = tot
+    return best, kept
+
+
+@pytest.mark.parametrize("seed", range(120))
+def test_brute_force_tiny(orc, seed):
+    rng = np.random.default_rng(1000 + seed)
+    B = int(rng.integers(1, 5))
+    g = int(rng.integers(1, 5))
+    # conditional confidences from a small set so that exact ties occur
+    c = rng.choice(np.array([1.0, 0.8, 0.5, 0.25, 0.125, 0.9], np.float32), size=(B, g))
+    s = np.multiply.accumulate(c, axis=1, dtype=np.float32)
+    eps = float(np.float32(rng.choice([EPS_MIN, 0.05, 0.2])))
+    max_len = int(rng.integers(1, g + 2))
+    n_tab = int(rng.integers(1, 6))
+    M = np.sort(rng.choice(np.arange(1, B + B * g + 3), size=n_tab, replace=False)).astype(np.int32)
+    sps = rng.uniform(0.5, 3.0, size=n_tab)
+    r = orc.plan_from_survivals(s, eps, 1, max_len, -1, wl.COST_SPS_1D, M, sps)
+    best, kept = _best_sums_brute_force(s, eps, max_len)
+    assert r.n_kept == sum(kept)
+    # tau(b) - B is the best achievable survival sum with b extra rows, exactly
+    for b in range(r.n_kept + 1):
+        assert r.tau_curve[b] - B == best[b], (b, r.tau_curve[b], best[b])
+    # the budget is the first maximiser of theta (numpy's first-occurrence argmax)
+    th = np.where(r.feasible, r.theta_curve, -np.inf)
+    assert r.budget == int(np.argmax(th))
+    # the allocation at the budget is prefix-respecting and optimal
+    alloc = r.verify_lens - 1
+    assert alloc.sum() == r.budget
+    assert all(0 <= alloc[q] <= kept[q] for q in range(B))
+    got = sum(float(s[q, k]) for q in range(B) for k in range(alloc[q]))
+    assert got == best[r.budget]
+
+
+def test_cost_lookup_1d_floor(orc):
+    s = _f32([[0.5, 0.25], [0.5, 0.25]])  # sorted 0.5 0.5 0.25 0.25 -> tau 2 2.5 3 3.25 3.5
+    # samples at M=4 (100 steps/s) and M=6 (50 steps/s); M < 4 uses sample 0
+    r = orc.plan_from_survivals(s, EPS_MIN, 1, 3, -1, wl.COST_SPS_1D, [4, 6], [100.0, 50.0])
+    np.testing.assert_array_equal(r.tau_curve, [2.0, 2.5, 3.0, 3.25, 3.5])
+    np.testing.assert_allclose(r.theta_curve, [200.0, 250.0, 300.0, 325.0, 175.0], rtol=1e-15)
+    assert r.budget == 3
+    assert list(r.verify_lens) == [3, 2]
+
+
+def test_cost_lookup_additive_ceil_tier(orc):
+    s = _f32([[0.5, 0.25], [0.5, 0.25]])
+    # T = bias + alpha + cost(ceil_tier(M)): M<=3 -> 0.5+0.5+1 = 2 ms; M in 4..5 -> 4 ms; M>5 infeasible
+    r = orc.plan_from_survivals(s, EPS_MIN, 1, 3, -1, wl.COST_ADDITIVE, [3, 5], [1.0, 3.0],
+                                bias=0.5, alpha=0.5)
+    np.testing.assert_allclose(r.theta_curve[:4], [1.0, 1.25, 0.75, 0.8125], rtol=1e-15)
+    assert list(r.feasible) == [True, True, True, True, False]
+    assert r.budget == 1 and abs(r.theta - 1.25) < 1e-15
+    # a forced budget is clipped to the largest in-range budget (M <= 5 -> b <= 3)
+    f = orc.plan_from_survivals(s, EPS_MIN, 1, 3, 4, wl.COST_ADDITIVE, [3, 5], [1.0, 3.0],
+                                bias=0.5, alpha=0.5)
+    assert f.budget == 3 and list(f.verify_lens) == [3, 2]
+
+
+def test_invalid_cost_and_infeasible(orc):
+    s = _f32([[0.5, 0.25]])
+    r = orc.plan_from_survivals(s, EPS_MIN, 1, 3, -1, wl.COST_SPS_1D, [1, 2], [0.0, 5.0])
+    assert r.status & orc.ST_BAD_COST
+    assert not r.feasible[0] and r.feasible[1]
+    # every budget above the largest tier: infeasible, budget 0
+    q = orc.plan_from_survivals(_f32([[0.5], [0.5], [0.5]]), EPS_MIN, 1, 2, -1,
+                                wl.COST_ADDITIVE, [2], [1.0], bias=1.0)
+    assert q.status & orc.ST_INFEASIBLE and q.budget == 0 and list(q.verify_lens) == [1, 1, 1]
+
+
+def test_min_verify_len_clamp(orc):
+    s = _f32([[0.9, 0.8, 0.7], [0.1, 0.01, 0.001]])
+    r = orc.plan_from_survivals(s, EPS_MIN, 2, 4, 2, 0, [1], [1.0])
+    assert list(r.verify_lens) == [3, 2]  # request 1 raised to the minimum of 2
+    # max_verify_len bounds both the candidates and the lens
+    r2 = orc.plan_from_survivals(s, EPS_MIN, 1, 2, 3, 0, [1], [1.0])
+    assert list(r2.verify_lens) == [2, 2] and r2.n_kept == 2
+
+
+def test_plan_invariants_on_workloads(orc):
+    for w in (wl.TINY, wl.QWEN, wl.DSV4, wl.MIXED):
+        step = wl.make_step(w, seed=0)
+        r = orc.plan_step(step)
+        lens = r.verify_lens
+        assert np.all(lens >= w.min_verify_len) and np.all(lens <= w.max_len)
+        assert lens.sum() == w.B + r.budget  # min_verify_len = 1
+        assert np.all(np.diff(r.survivals, axis=1) <= 0)
+        assert r.status == 0
+
+
+# ------------------------------------------------------------------ pack
+
+def test_pack_cu_seqlens(orc):
+    for ex in golden("pack_examples.json")["cu_seqlens"]:
+        lens = np.array(ex["verify_lens"], np.int32)
+        B, g = len(lens), int(lens.max())
+        p = orc.pack(np.zeros(B), np.zeros((B, g)), np.zeros(B), lens, [], 64)
+        assert list(p.cu_seqlens) == ex["cu_seqlens"]
+        assert p.total == p.padded == ex["rows"]
+
+
+def test_pack_layout_of_the_page(orc):
+    ex = golden("pack_examples.json")["packed_layout"]
+    lens = np.array(ex["verify_lens"], np.int32)
+    gamma = 3
+    # token of request q (letter) at chain position j is encoded 100*(q+1)+j
+    anchor = np.array([100 * (q + 1) for q in range(3)], np.int32)
+    draft = np.array([[100 * (q + 1) + j for j in range(1, gamma + 1)] for q in range(3)], np.int32)
+    prefix = np.array([10, 20, 30], np.int32)
+    p = orc.pack(anchor, draft, prefix, lens, [], 12)
+    names = [f"{'ABC'[t // 100 - 1]}{t % 100}" for t in p.ids[:p.total]]
+    assert names == ex["rows"]
+    assert list(p.req[:7]) == [0, 0, 1, 2, 2, 2, 2]
+    assert list(p.pos[:7]) == [10, 11, 20, 30, 31, 32, 33]
+    assert list(p.src[:7]) == [0, 1, 4, 8, 9, 10, 11]
+    assert np.all(p.ids[7:] == -7)  # rows past the packed total are not touched
+
+
+def test_pack_tier_round_up(orc):
+    for ex in golden("pack_examples.json")["tiers"]:
+        for total, padded in ex["total_to_padded"]:
+            lens = np.ones(total, np.int32)
+            p = orc.pack(np.arange(total), np.zeros((total, 1)), np.zeros(total), lens,
+                         ex["tiers"], 128)
+            assert p.total == total and p.padded == padded
+            assert np.all(p.req[total:padded] == -1) and np.all(p.src[total:padded] == -1)
+            assert np.all(p.ids[total:padded] == 0) and np.all(p.pos[total:padded] == 0)
+            assert np.all(p.req[padded:] == -7)
+            if "padding" in ex:
+                assert padded - total == ex["padding"]
+
+
+def test_pack_capacity_and_bad_len(orc):
+    p = orc.pack(np.zeros(2), np.zeros((2, 3)), np.zeros(2), [4, 4], [], 6)
+    assert p.status & orc.ST_CAPACITY and p.total == 8
+    q = orc.pack(np.zeros(2), np.zeros((2, 3)), np.zeros(2), [0, 9], [], 16)
+    assert q.status & orc.ST_BAD_LEN and list(q.cu_seqlens) == [0, 1, 5]
+    r = orc.pack(np.zeros(3), np.zeros((3, 3)), np.zeros(3), [4, 4, 4], [8], 16)
+    assert r.status & orc.ST_CAPACITY and r.padded == 12
+
+
+# ---------------------------------------------------------------- accept
+
+_TOK = {"A": 11, "B": 12, "C": 13, "D": 14, "E": 15, "X": 5, "Y": 6, "Z": 7}
+
+
+def _one_hot_rows(tokens, V, rng):
+    x = rng.normal(0, 1, size=(len(tokens), V)).astype(np.float32)
+    for i, t in enumerate(tokens):
+        x[i, t] += 8.0
+    return x
+
+
+def test_greedy_accept_page_example(orc):
+    ex = golden("accept_examples.json")
+    rng = np.random.default_rng(5)
+    for key in ("greedy", "all_accepted"):
+        e = ex[key]
+        draft = np.array([[_TOK[t] for t in e["drafts"]]], np.int32)
+        logits = _one_hot_rows([_TOK[t] for t in e["target_chain"]], 32, rng)
+        cu = np.array([0, 5], np.int32)
+        fin = orc.greedy_accept(logits, 32, cu, draft, np.array([10], np.int32))
+        assert fin.num_accepted[0] == e["correct_len"]
+        assert fin.commit_lens[0] == e["commit_len"]
+        assert fin.status == 0
+        if "bonus" in e:
+            assert fin.bonus[0] == _TOK[e["bonus"]]
+            valid = fin.out_tokens[0, :fin.commit_lens[0]]
+            assert [t for t in valid] == [_TOK[t] for t in e["valid_output"]]
+    f = ex["finalize"]
+    fin = orc.greedy_accept(_one_hot_rows([11, 12, 5], 32, rng), 32, np.array([0, 3], np.int32),
+                            np.array([[11, 12, 13, 14]], np.int32),
+                            np.array([f["prefix_len"]], np.int32))
+    assert fin.commit_lens[0] == f["commit_len"] and fin.new_seq_lens[0] == f["new_seq_len"]
+
+
+def test_no_recovery_after_first_mismatch(orc):
+    rng = np.random.default_rng(6)
+    draft = np.array([[11, 12, 13, 14]], np.int32)
+    # the target matches drafts 0, 2 and 3 but not 1: only one draft is accepted
+    logits = _one_hot_rows([11, 5, 13, 14, 15], 32, rng)
+    fin = orc.greedy_accept(logits, 32, np.array([0, 5], np.int32), draft, np.zeros(1, np.int32))
+    assert fin.num_accepted[0] == 1 and fin.bonus[0] == 5 and fin.commit_lens[0] == 2
+    assert list(fin.out_tokens[0]) == [11, 5, 13, 14, -1]
+
+
+def test_cap_accept_page_example(orc):
+    e = golden("accept_examples.json")["cap_accept"]
+    gamma = e["width"] - 1
+    B = len(e["verify_lens"])
+    rng = np.random.default_rng(7)
+    draft = rng.integers(0, 32, size=(B, gamma)).astype(np.int32)
+    chain = [int(draft[r, j]) if j < gamma else 3 for r in range(B) for j in range(gamma + 1)]
+    logits = _one_hot_rows(chain, 32, rng)
+    assert logits.shape[0] == e["target_rows"]
+    cap = orc.cap_accept(logits, 32, np.array(e["verify_lens"], np.int32), draft,
+                         np.zeros(B, np.int32))
+    assert list(cap.num_accepted) == e["draft_caps"]
+    assert list(cap.ceiling) == [gamma] * B
+    assert list(cap.commit_lens) == [c + 1 for c in e["draft_caps"]]
+    assert cap.sum_commit == sum(c + 1 for c in e["draft_caps"])
+    assert cap.sum_ceiling == B * (gamma + 1)
+
+
+def test_argmax_special_cases(orc):
+    V = 64
+    am, st = orc.argmax_rows(np.zeros((3, V), np.float32))
+    assert list(am) == [0, 0, 0] and st == 0
+    rng = np.random.default_rng(8)
+    x = rng.normal(size=(50, V)).astype(np.float32)
+    x[5, 7] = x[5, 40] = 9.0  # tie: lowest index
+    am, _ = orc.argmax_rows(x)
+    np.testing.assert_array_equal(am, np.argmax(x, axis=1))
+    assert am[5] == 7
+    # bf16 rows agree with numpy's argmax of the decoded values
+    b = wl.to_bf16_bits(rng.normal(size=(40, 300)).astype(np.float32))
+    am, _ = orc.argmax_rows(b)
+    np.testing.assert_array_equal(am, np.argmax(wl.bf16_bits_to_f32(b), axis=1))
+    # -0 equals +0; NaN is skipped and flagged; a row with nothing above -inf gives 0
+    z = np.array([[-1.0, -0.0, 0.0, -2.0]], np.float32)
+    assert orc.argmax_rows(z)[0][0] == 1
+    n = np.array([[np.nan, 1.0, 2.0, np.nan]], np.float32)
+    am, st = orc.argmax_rows(n)
+    assert am[0] == 2 and st & orc.ST_NAN_LOGIT
+    m = np.array([[np.nan, -np.inf, -np.inf]], np.float32)
+    assert orc.argmax_rows(m)[0][0] == 0
+    # ld > V: trailing columns are ignored
+    y = np.zeros((2, 8), np.float32)
+    y[:, 6] = 5.0
+    y[:, 2] = 1.0
+    assert list(orc.argmax_rows(y, V=5)[0]) == [2, 2]
+
+
+def test_greedy_bad_ranges_and_tokens(orc):
+    rng = np.random.default_rng(9)
+    logits = _one_hot_rows([1, 2, 3], 16, rng)
+    draft = np.array([[1, 2], [3, 99]], np.int32)
+    fin = orc.greedy_accept(logits, 16, np.array([0, 3, 3], np.int32), draft,
+                            np.array([4, 5], np.int32))
+    assert fin.status & orc.ST_BAD_LEN and fin.status & orc.ST_TOKEN_RANGE
+    assert fin.num_accepted[1] == 0 and fin.bonus[1] == -1 and fin.commit_lens[1] == 0
+    assert fin.new_seq_lens[1] == 5
+    # rows beyond max_rows: capacity flag, the request past them is a bad range
+    fin2 = orc.greedy_accept(logits, 16, np.array([0, 2, 4], np.int32),
+                             np.array([[1, 2], [3, 4]], np.int32), np.zeros(2, np.int32))
+    assert fin2.status & orc.ST_CAPACITY and fin2.status & orc.ST_BAD_LEN
+
+
+def test_compact_equals_cap_accept(orc):
+    """Compact and cap-accept commit the same tokens (the review page's mode
+    table); the compact window is the gather of the strided rows."""
+    for seed in range(3):
+        step = wl.make_step(wl.TINY, seed=seed)
+        r = orc.plan_step(step)
+        strided = wl.strided_logits(step)
+        p = orc.pack(step.anchor, step.draft, step.prefix_lens, r.verify_lens, step.tiers,
+                     step.capacity)
+        compact = strided[p.src[:p.total]]
+        g = orc.greedy_accept(compact, step.V, p.cu_seqlens, step.draft, step.prefix_lens)
+        c = orc.cap_accept(strided, step.V, r.verify_lens, step.draft, step.prefix_lens)
+        for key in ("num_accepted", "bonus", "commit_lens", "new_seq_lens", "out_tokens"):
+            np.testing.assert_array_equal(g[key], c[key], err_msg=key)
+        assert np.all(c.ceiling >= c.num_accepted)
+
+
+def test_expected_commit_equals_tau(orc):
+    """E[sum(commit_lens)] = B + sum of the selected survivals when the survival
+    estimates are the true prefix probabilities (adaptive verify page, section
+    三, expectation by linearity)."""
+    B, gamma, V = 48, 6, 256
+    c = np.array([0.95, 0.9, 0.85, 0.8, 0.7, 0.6])
+    w = wl.Workload("expectation", B=B, gamma=gamma, V=V, logits_dtype="fp32")
+    z = np.tile(wl.confidence_logits_for(c[None, :]), (B, 1))
+    res = orc.plan(z, np.ones(gamma, np.float32), 1e-4, 1, gamma + 1, 150, 0, [1], [1.0])
+    commits, n_steps = [], 160
+    for seed in range(n_steps):
+        rng = np.random.default_rng(seed)
+        step = wl.StepInputs(workload=w, seed=seed, conf_logits=z,
+                             sts_temps=np.ones(gamma, np.float32),
+                             draft=rng.integers(0, V, size=(B, gamma)).astype(np.int32),
+                             anchor=np.zeros(B, np.int32), prefix_lens=np.zeros(B, np.int32),
+                             match_prob=np.tile(c, (B, 1)), cost=None, tiers=np.zeros(0, np.int32),
+                             capacity=B * (gamma + 1))
+        cap = orc.cap_accept(wl.strided_logits(step), V, res.verify_lens, step.draft,
+                             step.prefix_lens)
+        commits.append(cap.sum_commit)
+    mean = float(np.mean(commits))
+    sem = float(np.std(commits)) / math.sqrt(n_steps)
+    assert abs(mean - res.tau) < 4.5 * sem + 1e-3, (mean, res.tau, sem)
+
+
+def test_budget_theta_tie_goes_to_smaller_budget(orc):
+    # tau = 2, 2.5, 2.75; SPS 5, 4, 3 -> theta = 10, 10, 8.25 (exact in fp64)
+    s = _f32([[0.5], [0.25]])
+    r = orc.plan_from_survivals(s, EPS_MIN, 1, 2, -1, wl.COST_SPS_1D, [2, 3, 4], [5.0, 4.0, 3.0])
+    np.testing.assert_array_equal(r.theta_curve, [10.0, 10.0, 8.25])
+    assert r.budget == int(np.argmax(r.theta_curve)) == 0
+    assert list(r.verify_lens) == [1, 1]
