@@ -1,0 +1,455 @@
+"""Benchmark of the DSpark verify hot path on GB300: plan + pack + greedy
+accept steps/s at B=256, gamma=16, V=129280 (bf16 target logits), compact
+mode, and the accept kernel's HBM bandwidth against the measured peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own batch
+of B requests (weak scaling, no data-path collective); the elapsed time is
+the maximum over ranks.
+
+A step = dspark_plan + dspark_pack_verify + dspark_greedy_accept over one
+batch, with every input resident in HBM when the timed region starts.  The
+target logits of the packed rows (~2048 rows x 129280 x 2 B = 529 MB) are
+larger than the 129 MB L2, so each step streams them from HBM.  ``e2e``
+times the same step through ``engine.run_host``: inputs from pinned host
+memory, the packed total read back (the host needs it to run the verify
+window), the packed rows' logits copied host -> device, results read back.
+
+--impl reference times the CPU oracle (the reference arm of this build) on
+the host cores with the same metric and workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "plan+pack+accept steps/s at B=256 gamma=16 V=129280; accept HBM GB/s % of peak"
+UNIT = "steps/s"
+KERNELS_PER_STEP = 5  # survival, budget, pack, argmax, greedy finalize
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dsv4_like")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-cap", action="store_true")
+    ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def ncu_traffic(workload: str):
+    """Per-launch DRAM bytes of the accept kernel from the committed ncu
+    summary, if one was taken for the current kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get(workload)
+    except (OSError, ValueError):
+        return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [ln.strip().split(",") for ln in self.file if ln.strip()]
+        os.unlink(self.file.name)
+        sm, mx, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def oracle_step_timing(step, compact, budget_s, max_steps=None, row_fraction=1.0):
+    """Time the CPU oracle on the workload: the full planner and pack, and
+    the accept over a sample of the packed rows.  Returns the full-step rate
+    estimated as 1 / (t_plan_pack + rows * t_per_row)."""
+    import oracle
+    oracle.build()
+    w = step.workload
+    rows = compact.shape[0]
+    n_rows = max(1, int(round(rows * row_fraction)))
+    t_pp, t_acc, rows_done, steps = 0.0, 0.0, 0, 0
+    start = time.perf_counter()
+    cursor = 0
+    while True:
+        t0 = time.perf_counter()
+        r = oracle.plan_step(step)
+        p = oracle.pack(step.anchor, step.draft, step.prefix_lens, r.verify_lens, step.tiers,
+                        step.capacity)
+        t1 = time.perf_counter()
+        lo = cursor % rows
+        hi = min(rows, lo + n_rows)
+        am, _ = oracle.argmax_rows(compact[lo:hi], V=w.V)
+        full_am = np.zeros(rows, np.int32)
+        full_am[lo:hi] = am
+        oracle.greedy_finalize(full_am, rows, p.cu_seqlens, step.draft, step.prefix_lens, w.V)
+        t2 = time.perf_counter()
+        cursor = hi
+        t_pp += t1 - t0
+        t_acc += t2 - t1
+        rows_done += hi - lo
+        steps += 1
+        if time.perf_counter() - start >= budget_s or (max_steps and steps >= max_steps):
+            break
+    per_step = t_pp / steps + rows * (t_acc / rows_done)
+    return {"value": 1.0 / per_step, "steps": steps, "t_plan_pack_ms": 1e3 * t_pp / steps,
+            "t_accept_row_us": 1e6 * t_acc / rows_done, "rows_sampled": rows_done,
+            "elapsed_s": time.perf_counter() - start}
+
+
+def make_inputs(name: str, seed: int):
+    from confidence_scheduled_speculative_gb300 import workloads as wl
+    step = wl.make_step(wl.WORKLOADS[name], seed=seed)
+    strided = wl.strided_logits(step)  # [B*(gamma+1), V] bf16 bits
+    return step, strided
+
+
+def cpu_info():
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part", "processor name")):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "model": model}
+
+
+# ---------------------------------------------------------------- reference
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from confidence_scheduled_speculative_gb300 import workloads as wl
+    step = wl.make_step(wl.WORKLOADS[args.workload], seed=args.seed)
+    import oracle
+    r = oracle.plan_step(step)
+    p = oracle.pack(step.anchor, step.draft, step.prefix_lens, r.verify_lens, step.tiers,
+                    step.capacity)
+    rows = [(int(s) // (step.gamma + 1), int(s) % (step.gamma + 1)) for s in p.src[:p.total]]
+    compact = wl.target_rows(step, rows)
+    # bound the whole run to about two minutes: each timed step processes the
+    # planner, the pack and a slice of the packed rows
+    k = max(1, args.steps)
+    est = oracle_step_timing(step, compact, budget_s=3.0)
+    full_step_s = 1.0 / est["value"]
+    per_step_budget = min(full_step_s, 120.0 / (k + max(3, args.warmup)))
+    frac = max(1.0 / compact.shape[0],
+               min(1.0, (per_step_budget - est["t_plan_pack_ms"] / 1e3) / max(full_step_s, 1e-9)))
+    oracle_step_timing(step, compact, budget_s=0.0, max_steps=max(3, args.warmup),
+                       row_fraction=frac)
+    res = oracle_step_timing(step, compact, budget_s=1e9, max_steps=k, row_fraction=frac)
+    sample = (f"{res['steps']} oracle steps: full planner + pack each step, accept over "
+              f"{res['rows_sampled']} of {compact.shape[0]}*{res['steps']} packed rows "
+              f"(fraction {frac:.4f} per step); full-step rate = 1/(t_plan_pack + rows*t_row)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": res["value"], "unit": UNIT,
+        "n_gpus": args.gpus, "steps": res["steps"], "warmup": max(3, args.warmup),
+        "ms_per_step": 1e3 / res["value"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.workload} B={step.B} gamma={step.gamma} V={step.V} compact",
+                   "seed": args.seed},
+        "cpu_baseline": {"value": res["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample, "host": cpu_info()},
+        "e2e": {"value": res["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    emit(line, args)
+
+
+def emit(line, args):
+    s = json.dumps(line)
+    print(s, flush=True)
+    if args.out:
+        with open(args.out, "a") as f:
+            f.write(s + "\n")
+
+
+# --------------------------------------------------------------------- ours
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from confidence_scheduled_speculative_gb300 import api
+    from confidence_scheduled_speculative_gb300 import build as _b
+    from confidence_scheduled_speculative_gb300.engine import (HostStepIO, StepConfig, VerifyStep,
+                                                               run_host)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    _b.build()
+    api.load()
+
+    step, strided = make_inputs(args.workload, args.seed + rank)
+    w = step.workload
+    vs = VerifyStep(StepConfig.from_step(step), dev)
+    vs.load_inputs(step)
+    vs.plan()
+    vs.pack()
+    torch.cuda.synchronize()
+    total, padded = (int(x) for x in vs.totals.cpu())
+    strided_dev = torch.from_numpy(strided.view(np.int16)).to(dev).view(torch.bfloat16)
+    compact = strided_dev.index_select(0, vs.packed_src[:total].long()).contiguous()
+    accept_bytes = total * w.V * w.elem_bytes
+
+    plan_fn, pack_fn, acc_fn = vs.bind_compact(compact)
+    stream = torch.cuda.current_stream()
+
+    def one_step():
+        plan_fn()
+        pack_fn()
+        acc_fn()
+
+    warm = max(3, args.warmup)
+    vs.status.zero_()
+    for _ in range(warm):
+        one_step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, accept bracketed by events on its stream
+    K = max(1, args.steps)
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_start.record(stream)
+    for i in range(K):
+        plan_fn()
+        pack_fn()
+        ev_a[i].record(stream)
+        acc_fn()
+        ev_b[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    accept_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    status = int(vs.status.item())
+
+    # ---- breakdown (outside the timed region): per call on the same stream
+    n_b = min(K, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_b)]
+    for e in evs:
+        e[0].record(stream)
+        plan_fn()
+        e[1].record(stream)
+        pack_fn()
+        e[2].record(stream)
+        acc_fn()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    br = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
+                   for e in evs]) * 1e3
+
+    # ---- cap-accept over the full strided block (secondary)
+    cap = None
+    if not args.no_cap:
+        n_c = min(K, 200)
+        ce = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_c)]
+        for _ in range(3):
+            vs.cap_accept(strided_dev, write_argmax=False)
+        for e in ce:
+            e[0].record(stream)
+            vs.cap_accept(strided_dev, write_argmax=False)
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        cap_us = float(np.median([a.elapsed_time(b) for a, b in ce])) * 1e3
+        cap_bytes = w.strided_rows * w.V * w.elem_bytes
+        tot = vs.cap_totals.cpu().tolist()
+        cap = {"accept_us": cap_us, "rows": w.strided_rows,
+               "hbm_gbs": cap_bytes / (cap_us * 1e-6) / 1e9,
+               "sum_commit": tot[0], "sum_ceiling_plus1": tot[1]}
+
+    # ---- end to end from pinned host buffers
+    io = HostStepIO(vs)
+    io.fill(step)
+    host_logits = torch.empty((total, w.V), dtype=torch.bfloat16, pin_memory=True)
+    host_logits.copy_(compact)
+    e2e_dev = torch.empty_like(compact)
+    for _ in range(3):
+        run_host(vs, io, host_logits, e2e_dev)
+    n_e = max(1, min(args.e2e_steps, K))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    logit_bytes = 0
+    for _ in range(n_e):
+        logit_bytes = run_host(vs, io, host_logits, e2e_dev)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_ok = (np.array_equal(io.out_tokens.numpy(), vs.out_tokens.cpu().numpy())
+              and int(io.status.item()) == 0)
+
+    # ---- CPU oracle baseline (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        host_compact = strided[vs.packed_src[:total].cpu().numpy()]
+        res = oracle_step_timing(step, host_compact, budget_s=args.cpu_seconds)
+        cpu = {"value": res["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": (f"{res['steps']} oracle steps in {res['elapsed_s']:.1f} s: full "
+                          f"planner + pack each, accept over {res['rows_sampled']} packed rows "
+                          f"in total; full-step rate = 1/(t_plan_pack + {total}*t_row)"),
+               "t_plan_pack_ms": res["t_plan_pack_ms"], "t_accept_row_us": res["t_accept_row_us"],
+               "host": cpu_info()}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = load_peaks()
+    acc_us = float(np.mean(accept_ms)) * 1e3
+    achieved = accept_bytes / (acc_us * 1e-6) / 1e9
+    ms_per_step = elapsed_ms / K
+    value = world * K / (elapsed_ms / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": warm, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name} B={w.B} gamma={w.gamma} V={w.V} compact",
+                   "B": w.B, "gamma": w.gamma, "V": w.V, "mode": "compact",
+                   "packed_rows": total, "padded_rows": padded, "seed": args.seed,
+                   "l2": f"inputs larger than L2: {accept_bytes / 1e6:.1f} MB of logits per step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "kernel": "dspark_greedy_accept (argmax + finalize)",
+                     "bytes_per_launch": accept_bytes,
+                     "traffic": ncu_traffic(w.name)},
+        "e2e": {"value": world * n_e / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": io.h2d_input_bytes() + logit_bytes,
+                "d2h_bytes_per_step": io.d2h_output_bytes(), "steps": n_e,
+                "matches_device_path": bool(e2e_ok)},
+        "cpu_baseline": cpu,
+        "gpu_launches": KERNELS_PER_STEP * K,
+        "clocks": clocks,
+        "breakdown_us": {"plan": float(np.median(br[:, 0])), "pack": float(np.median(br[:, 1])),
+                         "accept": float(np.median(br[:, 2])),
+                         "accept_timed_mean": acc_us, "step_timed_mean": 1e3 * ms_per_step},
+        "cap_accept": cap,
+        "status": status,
+    }
+    emit(line, args)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

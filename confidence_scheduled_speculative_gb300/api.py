@@ -1,0 +1,236 @@
+"""Thin Python binding of libdspark.so (include/dspark.h).
+
+Argument marshalling only: every function here forwards device pointers,
+sizes and the current CUDA stream to the C entry point of the same name, and
+raises :class:`DsparkError` on a non-zero return code.  PyTorch provides the
+device buffers and the stream; every step of the computation runs in the
+library's CUDA kernels.  There is no fallback: if the library is missing the
+import of a function raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+DSPARK_OK = 0
+DSPARK_ERR_INVALID_ARG = -1
+DSPARK_ERR_WORKSPACE = -2
+DSPARK_ERR_CUDA = -3
+DSPARK_ERR_UNSUPPORTED = -4
+
+STATUS_CAPACITY = 1
+STATUS_TOKEN_RANGE = 2
+STATUS_NAN_LOGIT = 4
+STATUS_BAD_INPUT = 8
+STATUS_BAD_LEN = 16
+STATUS_BAD_COST = 32
+STATUS_INFEASIBLE = 64
+
+COST_SPS_1D = 0
+COST_ADDITIVE = 1
+DTYPE_BF16 = 0
+DTYPE_F32 = 1
+MAX_TIERS = 64
+
+
+class DsparkError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {dspark_strerror(code)} ({code})")
+        self.code = code
+
+
+class dspark_plan_params(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("gamma", ctypes.c_int32),
+                ("survival_eps", ctypes.c_float), ("min_verify_len", ctypes.c_int32),
+                ("max_verify_len", ctypes.c_int32), ("forced_budget", ctypes.c_int32)]
+
+
+class dspark_cost_table(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("n", ctypes.c_int32), ("M", ctypes.c_void_p),
+                ("val", ctypes.c_void_p), ("bias_ms", ctypes.c_double),
+                ("alpha_ms", ctypes.c_double)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+_VP, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+
+_SIGS = {
+    "dspark_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "dspark_version": (ctypes.c_int, []),
+    "dspark_plan_workspace_bytes": (_SZ, [_I32, _I32]),
+    "dspark_plan": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(dspark_plan_params),
+                                   ctypes.POINTER(dspark_cost_table), _VP, _VP, _VP, _VP, _VP,
+                                   _SZ, _VP, _VP]),
+    "dspark_pack_verify": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _I32,
+                                          ctypes.POINTER(ctypes.c_int32), _I32, _I32, _VP, _VP,
+                                          _VP, _VP, _VP, _VP, _VP, _VP]),
+    "dspark_accept_workspace_bytes": (_SZ, [_I32, _I32]),
+    "dspark_greedy_accept": (ctypes.c_int, [_VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP, _I32,
+                                            _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP,
+                                            _VP]),
+    "dspark_cap_accept": (ctypes.c_int, [_VP, _I32, _I64, _I32, _VP, _VP, _VP, _I32, _I32, _VP,
+                                         _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load libdspark.so; raise if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"libdspark.so not found at {path}: build it first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _p(t: torch.Tensor | None, dtype: torch.dtype | None = None, name: str = "") -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != DSPARK_OK:
+        raise DsparkError(fn, rc)
+
+
+# ------------------------------------------------------------------- calls
+
+def dspark_strerror(code: int) -> str:
+    return load().dspark_strerror(int(code)).decode()
+
+
+def dspark_version() -> int:
+    return int(load().dspark_version())
+
+
+def dspark_plan_workspace_bytes(B: int, gamma: int) -> int:
+    return int(load().dspark_plan_workspace_bytes(B, gamma))
+
+
+def dspark_accept_workspace_bytes(max_rows: int, V: int) -> int:
+    return int(load().dspark_accept_workspace_bytes(max_rows, V))
+
+
+def dspark_plan(conf_logits, sts_temps, *, B, gamma, survival_eps, min_verify_len,
+                max_verify_len, forced_budget, cost_kind, cost_M, cost_val, bias_ms=0.0,
+                alpha_ms=0.0, survivals, verify_lens, budget, tau_theta, status,
+                workspace=None, stream=None) -> None:
+    """Planner: STS survivals -> budget -> verify_lens (all outputs on device)."""
+    params = dspark_plan_params(B, gamma, survival_eps, min_verify_len, max_verify_len,
+                                forced_budget)
+    cost = dspark_cost_table(cost_kind, int(cost_M.numel()), _p(cost_M, torch.int32, "cost_M"),
+                             _p(cost_val, torch.float64, "cost_val"), bias_ms, alpha_ms)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().dspark_plan(
+        _p(conf_logits, torch.float32, "conf_logits"), _p(sts_temps, torch.float32, "sts_temps"),
+        ctypes.byref(params), ctypes.byref(cost), _p(survivals, torch.float32, "survivals"),
+        _p(verify_lens, torch.int32, "verify_lens"), _p(budget, torch.int32, "budget"),
+        _p(tau_theta, torch.float64, "tau_theta"), _p(workspace), ws_bytes,
+        _p(status, torch.int32, "status"), _stream(stream))
+    _check("dspark_plan", rc)
+
+
+def dspark_pack_verify(anchor, draft, prefix_lens, verify_lens, *, B, gamma, tiers, capacity,
+                       packed_ids, packed_pos, packed_req, packed_src, cu_seqlens, totals,
+                       status, stream=None) -> None:
+    """Front-pack the verify rows; ``tiers`` is a host sequence of ints."""
+    tiers = [int(t) for t in tiers]
+    arr = (ctypes.c_int32 * max(1, len(tiers)))(*tiers)
+    rc = load().dspark_pack_verify(
+        _p(anchor, torch.int32, "anchor"), _p(draft, torch.int32, "draft"),
+        _p(prefix_lens, torch.int32, "prefix_lens"), _p(verify_lens, torch.int32, "verify_lens"),
+        B, gamma, arr, len(tiers), capacity, _p(packed_ids, torch.int32, "packed_ids"),
+        _p(packed_pos, torch.int32, "packed_pos"), _p(packed_req, torch.int32, "packed_req"),
+        _p(packed_src, torch.int32, "packed_src"), _p(cu_seqlens, torch.int32, "cu_seqlens"),
+        _p(totals, torch.int32, "totals"), _p(status, torch.int32, "status"), _stream(stream))
+    _check("dspark_pack_verify", rc)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    raise ValueError(f"logits: expected bfloat16 or float32, got {t.dtype}")
+
+
+def _logits_ptr(logits: torch.Tensor, V: int) -> tuple[int, int]:
+    if not logits.is_cuda or logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits: expected a 2-D CUDA tensor with unit column stride")
+    if logits.size(1) < V:
+        raise ValueError("logits: fewer columns than V")
+    return logits.data_ptr(), logits.stride(0)
+
+
+def dspark_greedy_accept(logits, *, V, cu_seqlens, draft, prefix_lens, B, gamma, num_accepted,
+                         bonus, commit_lens, out_tokens, workspace, status, argmax=None,
+                         new_seq_lens=None, max_rows=None, stream=None) -> None:
+    """Compact-mode greedy accept over the packed rows of ``logits``."""
+    ptr, ld = _logits_ptr(logits, V)
+    max_rows = logits.size(0) if max_rows is None else max_rows
+    rc = load().dspark_greedy_accept(
+        ptr, _dtype_code(logits), ld, V, max_rows, _p(cu_seqlens, torch.int32, "cu_seqlens"),
+        _p(draft, torch.int32, "draft"), _p(prefix_lens, torch.int32, "prefix_lens"), B, gamma,
+        _p(argmax, torch.int32, "argmax"), _p(num_accepted, torch.int32, "num_accepted"),
+        _p(bonus, torch.int32, "bonus"), _p(commit_lens, torch.int32, "commit_lens"),
+        _p(new_seq_lens, torch.int32, "new_seq_lens"), _p(out_tokens, torch.int32, "out_tokens"),
+        _p(workspace), workspace.numel() * workspace.element_size(),
+        _p(status, torch.int32, "status"), _stream(stream))
+    _check("dspark_greedy_accept", rc)
+
+
+def dspark_cap_accept(logits, *, V, verify_lens, draft, prefix_lens, B, gamma, num_accepted,
+                      bonus, commit_lens, out_tokens, ceiling, totals, workspace, status,
+                      argmax=None, new_seq_lens=None, stream=None) -> None:
+    """cap-accept over the strided [B*(gamma+1), V] verify rows."""
+    ptr, ld = _logits_ptr(logits, V)
+    rc = load().dspark_cap_accept(
+        ptr, _dtype_code(logits), ld, V, _p(verify_lens, torch.int32, "verify_lens"),
+        _p(draft, torch.int32, "draft"), _p(prefix_lens, torch.int32, "prefix_lens"), B, gamma,
+        _p(argmax, torch.int32, "argmax"), _p(num_accepted, torch.int32, "num_accepted"),
+        _p(bonus, torch.int32, "bonus"), _p(commit_lens, torch.int32, "commit_lens"),
+        _p(new_seq_lens, torch.int32, "new_seq_lens"), _p(out_tokens, torch.int32, "out_tokens"),
+        _p(ceiling, torch.int32, "ceiling"), _p(totals, torch.int32, "totals"), _p(workspace),
+        workspace.numel() * workspace.element_size(), _p(status, torch.int32, "status"),
+        _stream(stream))
+    _check("dspark_cap_accept", rc)
+
+
+def workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A device byte buffer usable as a workspace (256-byte aligned by the
+    caching allocator)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")

@@ -1,0 +1,498 @@
+// accept.cu -- greedy accept (compact mode) and cap-accept on sm_103a.
+//
+// Pages (by title and section):
+//   [ROUND] "DeepSeek-V4 DSpark一轮 Draft、Verify、Accept 与 Commit", §五
+//           (AcceptGreedy: target_predict = argmax(target_logits); correct_len
+//           counts the leading drafts equal to the target chain; bonus comes
+//           from the last valid input row; FinalizeAcceptLens: commit_lens =
+//           correct_len + 1, new_seq_lens = prefix_lens + commit_lens;
+//           BuildOutTokens: copy the drafts, scatter the bonus at correct_len)
+//   [AVS]   "DSpark 自适应 Verify 怎样分配候选预算", §三 (capped_correct_len =
+//           min(raw_correct_len, verify_len - 1)), §五 "cap-accept"
+//   [SGL]   "DSpark接入SGLang：用置信度驱动可变长度验证", "三种 verify mode"
+//           (cap-accept commits what compact commits and exposes the
+//           full-verify acceptance ceiling)
+//
+// The argmax over the vocabulary is the whole cost: rows * V * 2 bytes of
+// bf16 read once from HBM.  It is a streaming reduction, not a contraction,
+// so no tensor cores: the design goal is HBM bandwidth.
+//
+// argmax_kernel  persistent grid of (SMs x kCtasPerSm) CTAs.  The rows are
+//   flattened into 16-byte chunks and cut into one equal contiguous range per
+//   CTA, so every CTA streams the same number of bytes whatever the ragged
+//   row count (which only the device knows: cu_seqlens[B]).  A CTA's range
+//   crosses at most a few row boundaries; for each (CTA c, row r) piece it
+//   writes one partial (max, lowest index) to slot c + r, which is unique
+//   because c + r increases by at least one from one piece to the next.
+//   Inner loop: kUnroll independent 16-byte non-allocating loads per thread
+//   in flight, then a packed bf16x2 max over the 8 values of each chunk
+//   (NaN-propagating); only when that max beats the running best (or is NaN)
+//   does the thread walk the chunk element by element, so the common path
+//   costs about one instruction per element.
+// finalize kernels  one warp per request, lane j = verify row j: combine the
+//   partials of the row, compare with draft j, ballot the mismatches; the
+//   first set bit is correct_len (no acceptance after the first mismatch).
+
+#include "dspark_common.cuh"
+
+#include <cuda_bf16.h>
+
+namespace dspark {
+
+constexpr int kArgmaxThreads = 256;
+constexpr int kCtasPerSm = 4;
+constexpr int kUnroll = 8;
+constexpr int kMaxCtas = 4096;
+constexpr int kFinalWarps = 8;
+
+struct Partial {
+    float v;
+    int i;
+};
+
+struct ArgmaxArgs {
+    const void *logits;
+    long long ld;
+    int V;
+    int rows_host;           // used when rows_dev is null
+    const int32_t *rows_dev;  // cu_seqlens + B (compact mode)
+    int max_rows;
+    Partial *partial;
+    int32_t *status;
+    int32_t *zero_totals;  // cap-accept totals, zeroed here before the finalize adds
+};
+
+__device__ __forceinline__ int device_rows(const int32_t *rows_dev, int rows_host, int max_rows) {
+    if (!rows_dev) return rows_host;
+    const int r = *rows_dev;
+    return r < 0 ? 0 : (r > max_rows ? max_rows : r);
+}
+
+__device__ __forceinline__ uint4 ld_stream16(const uint4 *p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void take(float f, int idx, float &best, int &bidx, bool &nan) {
+    if (f != f) nan = true;
+    else if (f > best) {
+        best = f;
+        bidx = idx;
+    }
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <typename T>
+struct Elem;
+template <>
+struct Elem<__nv_bfloat16> {
+    static constexpr int kPerChunk = 8;
+    __device__ static float load(const __nv_bfloat16 *p) {
+        return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(p)) << 16);
+    }
+    __device__ static void chunk(const uint4 &v, int base, float &best, int &bidx, bool &nan) {
+        __nv_bfloat162 a, b, c, d;
+        *reinterpret_cast<uint32_t *>(&a) = v.x;
+        *reinterpret_cast<uint32_t *>(&b) = v.y;
+        *reinterpret_cast<uint32_t *>(&c) = v.z;
+        *reinterpret_cast<uint32_t *>(&d) = v.w;
+        const __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+        if (!(__low2float(m) <= best) || !(__high2float(m) <= best)) {
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                take(bf16_lo(w[q]), base + 2 * q, best, bidx, nan);
+                take(bf16_hi(w[q]), base + 2 * q + 1, best, bidx, nan);
+            }
+        }
+    }
+};
+template <>
+struct Elem<float> {
+    static constexpr int kPerChunk = 4;
+    __device__ static float load(const float *p) { return __ldg(p); }
+    __device__ static void chunk(const uint4 &v, int base, float &best, int &bidx, bool &nan) {
+        const float f0 = __uint_as_float(v.x), f1 = __uint_as_float(v.y);
+        const float f2 = __uint_as_float(v.z), f3 = __uint_as_float(v.w);
+        if (!(f0 <= best) || !(f1 <= best) || !(f2 <= best) || !(f3 <= best)) {
+            take(f0, base, best, bidx, nan);
+            take(f1, base + 1, best, bidx, nan);
+            take(f2, base + 2, best, bidx, nan);
+            take(f3, base + 3, best, bidx, nan);
+        }
+    }
+};
+
+// Scan chunks [c0, c1) of one row.  VEC: 16-byte chunks (the last one of a
+// row may be partial and is read element-wise); otherwise one element per
+// chunk.
+template <typename T, bool VEC>
+__device__ __forceinline__ void scan_row(const T *row, int c0, int c1, int full, int V,
+                                         float &best, int &bidx, bool &nan) {
+    constexpr int EPC = VEC ? Elem<T>::kPerChunk : 1;
+    const int step = kUnroll * kArgmaxThreads;
+    if (VEC) {
+        const uint4 *row4 = reinterpret_cast<const uint4 *>(row);
+        for (int c = c0 + (int)threadIdx.x; c < c1; c += step) {
+            uint4 v[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int cc = c + u * kArgmaxThreads;
+                if (cc < c1 && cc < full) v[u] = ld_stream16(row4 + cc);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int cc = c + u * kArgmaxThreads;
+                if (cc < c1) {
+                    if (cc < full) {
+                        Elem<T>::chunk(v[u], cc * EPC, best, bidx, nan);
+                    } else {
+                        for (int e = cc * EPC; e < V; ++e) take(Elem<T>::load(row + e), e, best, bidx, nan);
+                    }
+                }
+            }
+        }
+    } else {
+        for (int c = c0 + (int)threadIdx.x; c < c1; c += step) {
+            float f[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int cc = c + u * kArgmaxThreads;
+                f[u] = cc < c1 ? Elem<T>::load(row + cc) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int cc = c + u * kArgmaxThreads;
+                if (cc < c1) take(f[u], cc, best, bidx, nan);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+    return v > bv || (v == bv && i < bi);
+}
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kArgmaxThreads, kCtasPerSm) argmax_kernel(ArgmaxArgs a) {
+    __shared__ float red_v[kArgmaxThreads / 32];
+    __shared__ int red_i[kArgmaxThreads / 32];
+    constexpr int EPC = VEC ? Elem<T>::kPerChunk : 1;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+    pdl_trigger();
+    pdl_wait();  // cu_seqlens / logits come from the kernels before
+    const int rows = device_rows(a.rows_dev, a.rows_host, a.max_rows);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (a.rows_dev && *a.rows_dev > a.max_rows) flag(a.status, DSPARK_STATUS_CAPACITY);
+        if (a.zero_totals) {
+            a.zero_totals[0] = 0;
+            a.zero_totals[1] = 0;
+        }
+    }
+    const int cpr = (a.V + EPC - 1) / EPC;
+    const int full = a.V / EPC;
+    const long long W = (long long)rows * cpr;
+    const long long per = (W + gridDim.x - 1) / gridDim.x;
+    const long long q0 = (long long)blockIdx.x * per;
+    const long long q1 = min(q0 + per, W);
+    bool nan = false;
+    for (long long q = q0; q < q1;) {
+        const int r = (int)(q / cpr);
+        const int c0 = (int)(q - (long long)r * cpr);
+        const long long seg_end = min(q1, (long long)(r + 1) * cpr);
+        const int c1 = c0 + (int)(seg_end - q);
+        const T *row = reinterpret_cast<const T *>(a.logits) + (long long)r * a.ld;
+        float best = -INFINITY;
+        int bidx = c0 * EPC;
+        scan_row<T, VEC>(row, c0, c1, full, a.V, best, bidx, nan);
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+            const float ov = __shfl_down_sync(kFullMask, best, d);
+            const int oi = __shfl_down_sync(kFullMask, bidx, d);
+            if (better(ov, oi, best, bidx)) {
+                best = ov;
+                bidx = oi;
+            }
+        }
+        if (lane == 0) {
+            red_v[warp] = best;
+            red_i[warp] = bidx;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float bv = red_v[0];
+            int bi = red_i[0];
+            for (int w = 1; w < kArgmaxThreads / 32; ++w)
+                if (better(red_v[w], red_i[w], bv, bi)) {
+                    bv = red_v[w];
+                    bi = red_i[w];
+                }
+            a.partial[blockIdx.x + r] = Partial{bv, bi};
+        }
+        __syncthreads();
+        q = seg_end;
+    }
+    if (__syncthreads_or(nan) && threadIdx.x == 0) flag(a.status, DSPARK_STATUS_NAN_LOGIT);
+}
+
+struct FinalArgs {
+    int rows_host;
+    const int32_t *rows_dev;
+    int max_rows, V, epc, grid;
+    const Partial *partial;
+    const int32_t *cu;    // greedy: cu_seqlens [B+1]
+    const int32_t *lens;  // cap: verify_lens [B]
+    const int32_t *draft, *prefix;
+    int B, gamma;
+    int32_t *argmax, *num_acc, *bonus, *commit, *new_seq, *out, *ceiling, *totals, *status;
+};
+
+__device__ __forceinline__ int row_argmax(const Partial *partial, int row, long long cpr,
+                                          long long per) {
+    const long long q_first = (long long)row * cpr;
+    const int c_lo = (int)(q_first / per), c_hi = (int)((q_first + cpr - 1) / per);
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+    for (int c = c_lo; c <= c_hi; ++c) {
+        const Partial p = partial[c + row];
+        if (better(p.v, p.i, bv, bi)) {
+            bv = p.v;
+            bi = p.i;
+        }
+    }
+    return bi;
+}
+
+// per-row argmax output (every row < rows), grid-stride over all threads
+__device__ __forceinline__ void write_argmax(const FinalArgs &a, int rows, long long cpr, long long per) {
+    if (!a.argmax || per <= 0) return;
+    const int nthreads = gridDim.x * blockDim.x;
+    for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < rows; row += nthreads)
+        a.argmax[row] = row_argmax(a.partial, row, cpr, per);
+}
+
+// BuildOutTokens and FinalizeAcceptLens for request r (lane 0 writes the scalars)
+__device__ __forceinline__ void finish(const FinalArgs &a, int r, int lane, int correct, int bon,
+                                       int dj) {
+    const int g = a.gamma;
+    if (lane == 0) {
+        a.num_acc[r] = correct;
+        a.bonus[r] = bon;
+        a.commit[r] = correct + 1;
+        if (a.new_seq) a.new_seq[r] = a.prefix[r] + correct + 1;
+    }
+    if (lane < g) a.out[(size_t)r * (g + 1) + lane] = (lane == correct) ? bon : dj;
+    else if (lane == g) a.out[(size_t)r * (g + 1) + g] = (g == correct) ? bon : -1;
+}
+
+__global__ void __launch_bounds__(kFinalWarps * 32) greedy_finalize_kernel(FinalArgs a) {
+    pdl_wait();
+    const int rows = device_rows(a.rows_dev, a.rows_host, a.max_rows);
+    const long long cpr = (a.V + a.epc - 1) / a.epc;
+    const long long W = (long long)rows * cpr;
+    const long long per = (W + a.grid - 1) / a.grid;
+    write_argmax(a, rows, cpr, per);
+
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * kFinalWarps + (threadIdx.x >> 5);
+    if (r >= a.B) return;  // warp-uniform
+    const int g = a.gamma;
+    const int dj = lane < g ? a.draft[(size_t)r * g + lane] : -1;
+    if (__any_sync(kFullMask, lane < g && (dj < 0 || dj >= a.V)) && lane == 0)
+        flag(a.status, DSPARK_STATUS_TOKEN_RANGE);
+    const int lo = a.cu[r], hi = a.cu[r + 1], L = hi - lo;
+    if (lo < 0 || hi > rows || L < 1 || L > g + 1) {
+        if (lane == 0) {
+            a.num_acc[r] = 0;
+            a.bonus[r] = -1;
+            a.commit[r] = 0;
+            if (a.new_seq) a.new_seq[r] = a.prefix[r];
+            flag(a.status, DSPARK_STATUS_BAD_LEN);
+        }
+        if (lane < g) a.out[(size_t)r * (g + 1) + lane] = dj;
+        else if (lane == g) a.out[(size_t)r * (g + 1) + g] = -1;
+        return;
+    }
+    const int am = lane < L ? row_argmax(a.partial, lo + lane, cpr, per) : 0;
+    const unsigned mism = __ballot_sync(kFullMask, lane < L - 1 && am != dj);
+    const int correct = mism ? __ffs(mism) - 1 : L - 1;
+    const int bon = __shfl_sync(kFullMask, am, correct);
+    finish(a, r, lane, correct, bon, dj);
+}
+
+__global__ void __launch_bounds__(kFinalWarps * 32) cap_finalize_kernel(FinalArgs a) {
+    __shared__ int sums[2];
+    pdl_wait();
+    const int rows = a.rows_host;
+    const long long cpr = (a.V + a.epc - 1) / a.epc;
+    const long long W = (long long)rows * cpr;
+    const long long per = (W + a.grid - 1) / a.grid;
+    write_argmax(a, rows, cpr, per);
+    if (threadIdx.x == 0) sums[0] = sums[1] = 0;
+    __syncthreads();
+
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * kFinalWarps + (threadIdx.x >> 5);
+    const int g = a.gamma;
+    if (r < a.B) {
+        const int dj = lane < g ? a.draft[(size_t)r * g + lane] : -1;
+        if (__any_sync(kFullMask, lane < g && (dj < 0 || dj >= a.V)) && lane == 0)
+            flag(a.status, DSPARK_STATUS_TOKEN_RANGE);
+        const int base = r * (g + 1);
+        const int am = lane <= g ? row_argmax(a.partial, base + lane, cpr, per) : 0;
+        const unsigned mism = __ballot_sync(kFullMask, lane < g && am != dj);
+        const int raw = mism ? __ffs(mism) - 1 : g;
+        int len = a.lens[r];
+        if (len < 1 || len > g + 1) {
+            if (lane == 0) flag(a.status, DSPARK_STATUS_BAD_LEN);
+            len = len < 1 ? 1 : g + 1;
+        }
+        const int capped = min(raw, len - 1);
+        const int bon = __shfl_sync(kFullMask, am, capped);
+        finish(a, r, lane, capped, bon, dj);
+        if (lane == 0) {
+            a.ceiling[r] = raw;
+            atomicAdd(&sums[0], capped + 1);
+            atomicAdd(&sums[1], raw + 1);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        atomicAdd(&a.totals[0], sums[0]);
+        atomicAdd(&a.totals[1], sums[1]);
+    }
+}
+
+int argmax_grid() {
+    const int g = sm_count() * kCtasPerSm;
+    return g < 1 ? 1 : (g > kMaxCtas ? kMaxCtas : g);
+}
+
+template <typename T>
+cudaError_t launch_argmax(const ArgmaxArgs &a, bool vec, int grid, cudaStream_t s) {
+    if (vec) return launch_pdl(argmax_kernel<T, true>, dim3(grid), dim3(kArgmaxThreads), 0, s, a);
+    return launch_pdl(argmax_kernel<T, false>, dim3(grid), dim3(kArgmaxThreads), 0, s, a);
+}
+
+int run_accept(const void *logits, int dtype, long long ld, int V, int max_rows, int rows_host,
+               const int32_t *rows_dev, FinalArgs f, bool cap, void *ws, size_t ws_bytes,
+               cudaStream_t s) {
+    if (!ws || ws_bytes < dspark_accept_workspace_bytes(max_rows, V) || !aligned(ws, 256))
+        return DSPARK_ERR_WORKSPACE;
+    const size_t esize = dtype == DSPARK_DTYPE_BF16 ? 2 : 4;
+    const bool vec = aligned(logits, 16) && ((ld * (long long)esize) % 16 == 0);
+    const int grid = argmax_grid();
+    ArgmaxArgs a;
+    a.logits = logits;
+    a.ld = ld;
+    a.V = V;
+    a.rows_host = rows_host;
+    a.rows_dev = rows_dev;
+    a.max_rows = max_rows;
+    a.partial = static_cast<Partial *>(ws);
+    a.status = f.status;
+    a.zero_totals = cap ? f.totals : nullptr;
+    cudaError_t e = dtype == DSPARK_DTYPE_BF16 ? launch_argmax<__nv_bfloat16>(a, vec, grid, s)
+                                               : launch_argmax<float>(a, vec, grid, s);
+    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+    f.rows_host = rows_host;
+    f.rows_dev = rows_dev;
+    f.max_rows = max_rows;
+    f.V = V;
+    f.epc = vec ? (int)(16 / esize) : 1;
+    f.grid = grid;
+    f.partial = a.partial;
+    const int fgrid = (f.B + kFinalWarps - 1) / kFinalWarps;
+    e = cap ? launch_pdl(cap_finalize_kernel, dim3(fgrid), dim3(kFinalWarps * 32), 0, s, f)
+            : launch_pdl(greedy_finalize_kernel, dim3(fgrid), dim3(kFinalWarps * 32), 0, s, f);
+    return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+int check_common(const void *logits, int dtype, long long ld, int V, const int32_t *draft,
+                 const int32_t *prefix, int B, int gamma, const int32_t *num_acc,
+                 const int32_t *bonus, const int32_t *commit, const int32_t *new_seq,
+                 const int32_t *out, const int32_t *status) {
+    if (!logits || !draft || !num_acc || !bonus || !commit || !out || !status)
+        return DSPARK_ERR_INVALID_ARG;
+    if (new_seq && !prefix) return DSPARK_ERR_INVALID_ARG;
+    if (dtype != DSPARK_DTYPE_BF16 && dtype != DSPARK_DTYPE_F32) return DSPARK_ERR_INVALID_ARG;
+    if (B < 1 || gamma < 1 || gamma > 31 || V < 1 || ld < V) return DSPARK_ERR_INVALID_ARG;
+    return DSPARK_OK;
+}
+
+}  // namespace dspark
+
+using namespace dspark;
+
+extern "C" size_t dspark_accept_workspace_bytes(int32_t max_rows, int32_t V) {
+    (void)V;
+    if (max_rows < 0) max_rows = 0;
+    const size_t n = (size_t)kMaxCtas + (size_t)max_rows + 1;
+    return (n * sizeof(Partial) + 255) & ~size_t(255);
+}
+
+extern "C" int dspark_greedy_accept(const void *logits, int32_t dtype, int64_t ld, int32_t V,
+                                    int32_t max_rows, const int32_t *cu_seqlens,
+                                    const int32_t *draft, const int32_t *prefix_lens, int32_t B,
+                                    int32_t gamma, int32_t *argmax, int32_t *num_accepted,
+                                    int32_t *bonus, int32_t *commit_lens, int32_t *new_seq_lens,
+                                    int32_t *out_tokens, void *workspace, size_t workspace_bytes,
+                                    int32_t *status, void *stream) {
+    int rc = check_common(logits, dtype, ld, V, draft, prefix_lens, B, gamma, num_accepted, bonus,
+                          commit_lens, new_seq_lens, out_tokens, status);
+    if (rc != DSPARK_OK) return rc;
+    if (!cu_seqlens || max_rows < 0) return DSPARK_ERR_INVALID_ARG;
+    FinalArgs f = {};
+    f.cu = cu_seqlens;
+    f.draft = draft;
+    f.prefix = prefix_lens;
+    f.B = B;
+    f.gamma = gamma;
+    f.argmax = argmax;
+    f.num_acc = num_accepted;
+    f.bonus = bonus;
+    f.commit = commit_lens;
+    f.new_seq = new_seq_lens;
+    f.out = out_tokens;
+    f.status = status;
+    return run_accept(logits, dtype, ld, V, max_rows, 0, cu_seqlens + B, f, false, workspace,
+                      workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int dspark_cap_accept(const void *logits, int32_t dtype, int64_t ld, int32_t V,
+                                 const int32_t *verify_lens, const int32_t *draft,
+                                 const int32_t *prefix_lens, int32_t B, int32_t gamma,
+                                 int32_t *argmax, int32_t *num_accepted, int32_t *bonus,
+                                 int32_t *commit_lens, int32_t *new_seq_lens, int32_t *out_tokens,
+                                 int32_t *ceiling, int32_t *totals, void *workspace,
+                                 size_t workspace_bytes, int32_t *status, void *stream) {
+    int rc = check_common(logits, dtype, ld, V, draft, prefix_lens, B, gamma, num_accepted, bonus,
+                          commit_lens, new_seq_lens, out_tokens, status);
+    if (rc != DSPARK_OK) return rc;
+    if (!verify_lens || !ceiling || !totals) return DSPARK_ERR_INVALID_ARG;
+    if ((long long)B * (gamma + 1) > 0x7FFFFFFF) return DSPARK_ERR_INVALID_ARG;
+    const int rows = B * (gamma + 1);
+    FinalArgs f = {};
+    f.lens = verify_lens;
+    f.draft = draft;
+    f.prefix = prefix_lens;
+    f.B = B;
+    f.gamma = gamma;
+    f.argmax = argmax;
+    f.num_acc = num_accepted;
+    f.bonus = bonus;
+    f.commit = commit_lens;
+    f.new_seq = new_seq_lens;
+    f.out = out_tokens;
+    f.ceiling = ceiling;
+    f.totals = totals;
+    f.status = status;
+    return run_accept(logits, dtype, ld, V, rows, rows, nullptr, f, true, workspace,
+                      workspace_bytes, static_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,108 @@
+// dspark_common.cuh -- device helpers and host plumbing shared by the
+// library's translation units (plan.cu, pack.cu, accept.cu, api.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// Set a status bit from device code.  Kernels never trap: every condition a
+// kernel can detect is reported here and the host decides.
+__device__ __forceinline__ void flag(int32_t *status, int bit) { atomicOr(status, bit); }
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start before its predecessor finishes;
+// it must wait here before touching the predecessor's outputs.  Without the
+// attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Block-wide exclusive scan over blockDim.x threads (a multiple of 32, at
+// most 1024).  `warp_tot` is shared scratch of at least 32 entries.  Returns
+// the exclusive prefix of `v`; *total receives the block total.  Contains
+// __syncthreads(): every thread of the block must call it.
+template <typename T>
+__device__ T block_exclusive_scan(T v, T *warp_tot, T *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    T incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        T o = __shfl_up_sync(kFullMask, incl, d);
+        if (lane >= d) incl += o;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        T w = lane < nwarps ? warp_tot[lane] : T(0);
+        T wi = w;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            T o = __shfl_up_sync(kFullMask, wi, d);
+            if (lane >= d) wi += o;
+        }
+        if (lane < nwarps) warp_tot[lane] = wi - w;  // exclusive warp offsets
+        if (lane == 31) warp_tot[32] = wi;            // block total
+    }
+    __syncthreads();
+    T res = warp_tot[warp] + incl - v;
+    *total = warp_tot[32];
+    __syncthreads();
+    return res;
+}
+
+// Block-wide sum (all threads receive it).  `scratch` >= 33 entries.
+template <typename T>
+__device__ T block_sum(T v, T *scratch) {
+    T total;
+    block_exclusive_scan<T>(v, scratch, &total);
+    return total;
+}
+
+}  // namespace dspark
+
+// ---------------------------------------------------------------- host side
+namespace dspark {
+
+// Streaming multiprocessor count of the current device (cached per device).
+int sm_count();
+
+// Raise a kernel's dynamic shared-memory limit once per device.
+cudaError_t ensure_smem(const void *kernel, int bytes, int slot);
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Launch with the programmatic stream-serialization attribute so that the
+// kernel's prologue overlaps its predecessor on the stream (the kernel calls
+// pdl_wait() before reading what the predecessor wrote).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+}  // namespace dspark

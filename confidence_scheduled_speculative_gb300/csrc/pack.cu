@@ -1,0 +1,161 @@
+// pack.cu -- ragged verify pack on sm_103a.
+//
+// Pages (by title and section):
+//   [ROUND] "DeepSeek-V4 DSpark一轮 Draft、Verify、Accept 与 Commit", §三
+//           (verify ids = [anchor, draft tokens]; compact ragged layout built
+//           by BuildRaggedVerifyWindow / compact_verify_ids), §四 (verify
+//           positions)
+//   [AVS]   "DSpark 自适应 Verify 怎样分配候选预算", §五 (compact rows
+//           A0 A1 | B0 | C0 C1 C2 C3), §六 (cu_seqlens_q = [0,2,3,7])
+//   [SGL]   "DSpark接入SGLang：用置信度驱动可变长度验证", "Ragged verify"
+//           (front-pack into a compact buffer, round the total up to the
+//           nearest captured tier)
+//
+// One warp per request, lane j = row j of the request (gamma+1 <= 32).  Each
+// CTA covers 32 requests; it obtains the packed offset of its first request
+// from a block-wide sum of the preceding lengths (B is at most a few
+// thousand, so every CTA re-reading verify_lens is cheaper than a separate
+// scan kernel), and the packed total from the same pass, which it needs for
+// the pad rows.
+
+#include "dspark_common.cuh"
+
+namespace dspark {
+
+constexpr int kPackThreads = 1024;
+constexpr int kPackReqPerCta = kPackThreads / 32;
+
+struct TierArgs {
+    int n;
+    int32_t t[DSPARK_MAX_TIERS];
+};
+
+__device__ __forceinline__ int clamp_len(int L, int gamma, bool &bad) {
+    if (L < 1 || L > gamma + 1) {
+        bad = true;
+        return L < 1 ? 1 : gamma + 1;
+    }
+    return L;
+}
+
+__global__ void __launch_bounds__(kPackThreads)
+pack_kernel(const int32_t *__restrict__ anchor, const int32_t *__restrict__ draft,
+            const int32_t *__restrict__ prefix, const int32_t *__restrict__ lens, int B, int gamma,
+            TierArgs tiers, int capacity, int32_t *__restrict__ ids, int32_t *__restrict__ pos,
+            int32_t *__restrict__ req, int32_t *__restrict__ src, int32_t *__restrict__ cu,
+            int32_t *__restrict__ totals, int32_t *__restrict__ status) {
+    __shared__ int scan32[40];
+    __shared__ int offs[kPackReqPerCta];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r0 = blockIdx.x * kPackReqPerCta;
+
+    pdl_trigger();
+    pdl_wait();  // verify_lens may come from the planner just before
+
+    // lengths of all requests: total, and the sum before this CTA's first request
+    int tot_local = 0, pre_local = 0;
+    bool bad = false;
+    for (int r = tid; r < B; r += kPackThreads) {
+        const int L = clamp_len(lens[r], gamma, bad);
+        tot_local += L;
+        if (r < r0) pre_local += L;
+    }
+    const int total = block_sum<int>(tot_local, scan32);
+    const int before = block_sum<int>(pre_local, scan32);
+    if (__syncthreads_or(bad) && tid == 0 && blockIdx.x == 0) flag(status, DSPARK_STATUS_BAD_LEN);
+
+    // offsets of this CTA's 32 requests
+    if (warp == 0) {
+        const int r = r0 + lane;
+        bool b2 = false;
+        const int L = r < B ? clamp_len(lens[r], gamma, b2) : 0;
+        int incl = L;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(kFullMask, incl, d);
+            if (lane >= d) incl += o;
+        }
+        offs[lane] = before + incl - L;
+    }
+    __syncthreads();
+
+    const int r = r0 + warp;
+    bool over = false;
+    if (r < B) {
+        bool b3 = false;
+        const int L = clamp_len(lens[r], gamma, b3);
+        const int off = offs[warp];
+        if (lane == 0) cu[r + 1] = off + L;
+        if (lane < L) {
+            const int dst = off + lane;
+            if (dst < capacity) {
+                ids[dst] = lane == 0 ? anchor[r] : draft[(size_t)r * gamma + lane - 1];
+                pos[dst] = prefix[r] + lane;
+                req[dst] = r;
+                src[dst] = r * (gamma + 1) + lane;
+            } else {
+                over = true;
+            }
+        }
+    }
+
+    // graph-tier round-up and pad rows
+    int padded = total;
+    bool no_tier = false;
+    if (tiers.n > 0) {
+        no_tier = true;
+        for (int i = 0; i < tiers.n; ++i)
+            if (tiers.t[i] >= total) {
+                padded = tiers.t[i];
+                no_tier = false;
+                break;
+            }
+    }
+    const int pad_end = min(padded, capacity);
+    for (int i = total + blockIdx.x * kPackThreads + tid; i < pad_end; i += gridDim.x * kPackThreads) {
+        ids[i] = 0;
+        pos[i] = 0;
+        req[i] = -1;
+        src[i] = -1;
+    }
+    if (blockIdx.x == 0 && tid == 0) {
+        cu[0] = 0;
+        totals[0] = total;
+        totals[1] = padded;
+        if (no_tier || padded > capacity) over = true;
+    }
+    if (__syncthreads_or(over) && tid == 0) flag(status, DSPARK_STATUS_CAPACITY);
+}
+
+}  // namespace dspark
+
+using namespace dspark;
+
+extern "C" int dspark_pack_verify(const int32_t *anchor, const int32_t *draft,
+                                  const int32_t *prefix_lens, const int32_t *verify_lens, int32_t B,
+                                  int32_t gamma, const int32_t *host_tiers, int32_t n_tiers,
+                                  int32_t capacity, int32_t *packed_ids, int32_t *packed_pos,
+                                  int32_t *packed_req, int32_t *packed_src, int32_t *cu_seqlens,
+                                  int32_t *totals, int32_t *status, void *stream) {
+    if (!anchor || !draft || !prefix_lens || !verify_lens || !packed_ids || !packed_pos ||
+        !packed_req || !packed_src || !cu_seqlens || !totals || !status)
+        return DSPARK_ERR_INVALID_ARG;
+    if (B < 1 || gamma < 1 || gamma > 31 || capacity < 0) return DSPARK_ERR_INVALID_ARG;
+    if ((long long)B * (gamma + 1) > 0x7FFFFFFF) return DSPARK_ERR_INVALID_ARG;
+    if (n_tiers < 0 || n_tiers > DSPARK_MAX_TIERS || (n_tiers > 0 && !host_tiers))
+        return DSPARK_ERR_INVALID_ARG;
+    TierArgs t;
+    t.n = n_tiers;
+    for (int i = 0; i < n_tiers; ++i) {
+        t.t[i] = host_tiers[i];
+        if (i > 0 && !(t.t[i] > t.t[i - 1])) return DSPARK_ERR_INVALID_ARG;
+    }
+    for (int i = n_tiers; i < DSPARK_MAX_TIERS; ++i) t.t[i] = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int grid = (B + kPackReqPerCta - 1) / kPackReqPerCta;
+    if (launch_pdl(pack_kernel, dim3(grid), dim3(kPackThreads), 0, s, anchor, draft, prefix_lens,
+                   verify_lens, B, gamma, t, capacity, packed_ids, packed_pos, packed_req,
+                   packed_src, cu_seqlens, totals, status) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    return DSPARK_OK;
+}

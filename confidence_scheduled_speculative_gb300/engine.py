@@ -1,0 +1,277 @@
+"""Device buffers for one planner + pack + accept step, and the calls that
+run it.
+
+``VerifyStep`` owns every device buffer a DSpark decode step needs on the
+verify side (planner outputs, packed window, accept outputs, workspaces and
+the cost table), allocated once through PyTorch, and enqueues the C-ABI
+calls on one stream.  It adds no computation of its own: the numbers all
+come from the library's kernels.
+
+``run_host`` is the end-to-end entry a caller with host buffers uses: it
+copies the step's inputs from pinned host memory, runs the planner and the
+pack, reads back the packed totals (the host needs them to pick the verify
+graph tier), copies the target logits of the packed rows, runs the accept
+and reads the results back.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+from . import api
+
+
+@dataclasses.dataclass
+class StepConfig:
+    B: int
+    gamma: int
+    V: int
+    logits_dtype: torch.dtype
+    survival_eps: float
+    min_verify_len: int
+    max_verify_len: int
+    forced_budget: int
+    cost_kind: int
+    cost_M: np.ndarray
+    cost_val: np.ndarray
+    bias_ms: float
+    alpha_ms: float
+    tiers: tuple
+    capacity: int
+
+    @classmethod
+    def from_step(cls, step) -> "StepConfig":
+        """Build from a ``workloads.StepInputs``."""
+        w, c = step.workload, step.cost
+        return cls(B=w.B, gamma=w.gamma, V=w.V,
+                   logits_dtype=torch.bfloat16 if w.logits_dtype == "bf16" else torch.float32,
+                   survival_eps=w.survival_eps, min_verify_len=w.min_verify_len,
+                   max_verify_len=w.max_len, forced_budget=w.forced_budget, cost_kind=c.kind,
+                   cost_M=np.asarray(c.M, np.int32), cost_val=np.asarray(c.val, np.float64),
+                   bias_ms=c.bias_ms, alpha_ms=c.alpha_ms,
+                   tiers=tuple(int(t) for t in step.tiers), capacity=int(step.capacity))
+
+
+class VerifyStep:
+    """All device state of one verify-side step for a fixed configuration."""
+
+    def __init__(self, cfg: StepConfig, device: str | torch.device = "cuda"):
+        self.cfg = cfg
+        self.device = torch.device(device)
+        B, g, cap = cfg.B, cfg.gamma, cfg.capacity
+        i32 = dict(dtype=torch.int32, device=self.device)
+        f32 = dict(dtype=torch.float32, device=self.device)
+        self.conf_logits = torch.zeros((B, g), **f32)
+        self.sts_temps = torch.ones(g, **f32)
+        self.anchor = torch.zeros(B, **i32)
+        self.draft = torch.zeros((B, g), **i32)
+        self.prefix_lens = torch.zeros(B, **i32)
+        self.cost_M = torch.as_tensor(cfg.cost_M, dtype=torch.int32, device=self.device)
+        self.cost_val = torch.as_tensor(cfg.cost_val, dtype=torch.float64, device=self.device)
+        # planner outputs
+        self.survivals = torch.zeros((B, g), **f32)
+        self.verify_lens = torch.zeros(B, **i32)
+        self.budget = torch.zeros(1, **i32)
+        self.tau_theta = torch.zeros(2, dtype=torch.float64, device=self.device)
+        self.status = torch.zeros(1, **i32)
+        # pack outputs
+        self.packed_ids = torch.zeros(cap, **i32)
+        self.packed_pos = torch.zeros(cap, **i32)
+        self.packed_req = torch.zeros(cap, **i32)
+        self.packed_src = torch.zeros(cap, **i32)
+        self.cu_seqlens = torch.zeros(B + 1, **i32)
+        self.totals = torch.zeros(2, **i32)
+        # accept outputs
+        rows_max = max(cap, B * (g + 1))
+        self.argmax = torch.zeros(rows_max, **i32)
+        self.num_accepted = torch.zeros(B, **i32)
+        self.bonus = torch.zeros(B, **i32)
+        self.commit_lens = torch.zeros(B, **i32)
+        self.new_seq_lens = torch.zeros(B, **i32)
+        self.out_tokens = torch.zeros((B, g + 1), **i32)
+        self.ceiling = torch.zeros(B, **i32)
+        self.cap_totals = torch.zeros(2, **i32)
+        self.accept_ws = api.workspace(api.dspark_accept_workspace_bytes(rows_max, cfg.V),
+                                       self.device)
+        self.plan_ws = None
+        nb = api.dspark_plan_workspace_bytes(B, g)
+        if nb:
+            self.plan_ws = api.workspace(nb, self.device)
+
+    # ------------------------------------------------------------- inputs
+    def load_inputs(self, step) -> None:
+        """Copy a ``workloads.StepInputs``'s planner/pack inputs to the device."""
+        self.conf_logits.copy_(torch.from_numpy(step.conf_logits))
+        self.sts_temps.copy_(torch.from_numpy(step.sts_temps))
+        self.anchor.copy_(torch.from_numpy(step.anchor))
+        self.draft.copy_(torch.from_numpy(step.draft))
+        self.prefix_lens.copy_(torch.from_numpy(step.prefix_lens))
+
+    # -------------------------------------------------------------- calls
+    def plan(self, stream=None) -> None:
+        c = self.cfg
+        api.dspark_plan(self.conf_logits, self.sts_temps, B=c.B, gamma=c.gamma,
+                        survival_eps=c.survival_eps, min_verify_len=c.min_verify_len,
+                        max_verify_len=c.max_verify_len, forced_budget=c.forced_budget,
+                        cost_kind=c.cost_kind, cost_M=self.cost_M, cost_val=self.cost_val,
+                        bias_ms=c.bias_ms, alpha_ms=c.alpha_ms, survivals=self.survivals,
+                        verify_lens=self.verify_lens, budget=self.budget,
+                        tau_theta=self.tau_theta, status=self.status, workspace=self.plan_ws,
+                        stream=stream)
+
+    def pack(self, stream=None) -> None:
+        c = self.cfg
+        api.dspark_pack_verify(self.anchor, self.draft, self.prefix_lens, self.verify_lens,
+                               B=c.B, gamma=c.gamma, tiers=c.tiers, capacity=c.capacity,
+                               packed_ids=self.packed_ids, packed_pos=self.packed_pos,
+                               packed_req=self.packed_req, packed_src=self.packed_src,
+                               cu_seqlens=self.cu_seqlens, totals=self.totals,
+                               status=self.status, stream=stream)
+
+    def greedy_accept(self, logits: torch.Tensor, write_argmax: bool = True, stream=None) -> None:
+        c = self.cfg
+        api.dspark_greedy_accept(logits, V=c.V, cu_seqlens=self.cu_seqlens, draft=self.draft,
+                                 prefix_lens=self.prefix_lens, B=c.B, gamma=c.gamma,
+                                 num_accepted=self.num_accepted, bonus=self.bonus,
+                                 commit_lens=self.commit_lens, out_tokens=self.out_tokens,
+                                 workspace=self.accept_ws, status=self.status,
+                                 argmax=self.argmax if write_argmax else None,
+                                 new_seq_lens=self.new_seq_lens, stream=stream)
+
+    def cap_accept(self, logits: torch.Tensor, write_argmax: bool = True, stream=None) -> None:
+        c = self.cfg
+        api.dspark_cap_accept(logits, V=c.V, verify_lens=self.verify_lens, draft=self.draft,
+                              prefix_lens=self.prefix_lens, B=c.B, gamma=c.gamma,
+                              num_accepted=self.num_accepted, bonus=self.bonus,
+                              commit_lens=self.commit_lens, out_tokens=self.out_tokens,
+                              ceiling=self.ceiling, totals=self.cap_totals,
+                              workspace=self.accept_ws, status=self.status,
+                              argmax=self.argmax if write_argmax else None,
+                              new_seq_lens=self.new_seq_lens, stream=stream)
+
+    def compact_step(self, logits: torch.Tensor, stream=None) -> None:
+        """plan -> pack -> greedy accept, enqueued back to back (5 kernels)."""
+        self.plan(stream)
+        self.pack(stream)
+        self.greedy_accept(logits, write_argmax=False, stream=stream)
+
+    def bind_compact(self, logits: torch.Tensor, stream=None):
+        """Marshal the three calls of a compact step once; returns
+        (plan, pack, accept) zero-argument callables that re-issue the same
+        C calls with the same device pointers (for tight timing loops)."""
+        lib = api.load()
+        c = self.cfg
+        s = api._stream(stream)
+        p = lambda t: None if t is None else t.data_ptr()
+        self._params = api.dspark_plan_params(c.B, c.gamma, c.survival_eps, c.min_verify_len,
+                                              c.max_verify_len, c.forced_budget)
+        self._cost = api.dspark_cost_table(c.cost_kind, int(self.cost_M.numel()),
+                                           p(self.cost_M), p(self.cost_val), c.bias_ms,
+                                           c.alpha_ms)
+        self._tiers = (api.ctypes.c_int32 * max(1, len(c.tiers)))(*c.tiers)
+        plan_args = (p(self.conf_logits), p(self.sts_temps), api.ctypes.byref(self._params),
+                     api.ctypes.byref(self._cost), p(self.survivals), p(self.verify_lens),
+                     p(self.budget), p(self.tau_theta), p(self.plan_ws),
+                     0 if self.plan_ws is None else self.plan_ws.numel(), p(self.status), s)
+        pack_args = (p(self.anchor), p(self.draft), p(self.prefix_lens), p(self.verify_lens),
+                     c.B, c.gamma, self._tiers, len(c.tiers), c.capacity, p(self.packed_ids),
+                     p(self.packed_pos), p(self.packed_req), p(self.packed_src),
+                     p(self.cu_seqlens), p(self.totals), p(self.status), s)
+        ptr, ld = api._logits_ptr(logits, c.V)
+        acc_args = (ptr, api._dtype_code(logits), ld, c.V, logits.size(0), p(self.cu_seqlens),
+                    p(self.draft), p(self.prefix_lens), c.B, c.gamma, None,
+                    p(self.num_accepted), p(self.bonus), p(self.commit_lens),
+                    p(self.new_seq_lens), p(self.out_tokens), p(self.accept_ws),
+                    self.accept_ws.numel(), p(self.status), s)
+
+        def call(fn, args, name):
+            def run():
+                rc = fn(*args)
+                if rc != api.DSPARK_OK:
+                    raise api.DsparkError(name, rc)
+            return run
+
+        return (call(lib.dspark_plan, plan_args, "dspark_plan"),
+                call(lib.dspark_pack_verify, pack_args, "dspark_pack_verify"),
+                call(lib.dspark_greedy_accept, acc_args, "dspark_greedy_accept"))
+
+    # ------------------------------------------------------- host round trip
+    def result(self) -> dict:
+        """Copy every output to host numpy arrays (synchronises)."""
+        torch.cuda.synchronize(self.device)
+        names = ["survivals", "verify_lens", "budget", "tau_theta", "status", "packed_ids",
+                 "packed_pos", "packed_req", "packed_src", "cu_seqlens", "totals", "argmax",
+                 "num_accepted", "bonus", "commit_lens", "new_seq_lens", "out_tokens", "ceiling",
+                 "cap_totals"]
+        return {n: getattr(self, n).cpu().numpy() for n in names}
+
+
+class HostStepIO:
+    """Pinned host buffers for the end-to-end path (``run_host``)."""
+
+    def __init__(self, vs: VerifyStep):
+        c = vs.cfg
+        pin = dict(pin_memory=True)
+        self.conf_logits = torch.zeros((c.B, c.gamma), dtype=torch.float32, **pin)
+        self.sts_temps = torch.zeros(c.gamma, dtype=torch.float32, **pin)
+        self.anchor = torch.zeros(c.B, dtype=torch.int32, **pin)
+        self.draft = torch.zeros((c.B, c.gamma), dtype=torch.int32, **pin)
+        self.prefix_lens = torch.zeros(c.B, dtype=torch.int32, **pin)
+        self.totals = torch.zeros(2, dtype=torch.int32, **pin)
+        self.out_tokens = torch.zeros((c.B, c.gamma + 1), dtype=torch.int32, **pin)
+        self.commit_lens = torch.zeros(c.B, dtype=torch.int32, **pin)
+        self.new_seq_lens = torch.zeros(c.B, dtype=torch.int32, **pin)
+        self.verify_lens = torch.zeros(c.B, dtype=torch.int32, **pin)
+        self.status = torch.zeros(1, dtype=torch.int32, **pin)
+
+    def fill(self, step) -> None:
+        self.conf_logits.copy_(torch.from_numpy(step.conf_logits))
+        self.sts_temps.copy_(torch.from_numpy(step.sts_temps))
+        self.anchor.copy_(torch.from_numpy(step.anchor))
+        self.draft.copy_(torch.from_numpy(step.draft))
+        self.prefix_lens.copy_(torch.from_numpy(step.prefix_lens))
+
+    def h2d_input_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in
+                   (self.conf_logits, self.sts_temps, self.anchor, self.draft, self.prefix_lens))
+
+    def d2h_output_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in
+                   (self.totals, self.out_tokens, self.commit_lens, self.new_seq_lens,
+                    self.verify_lens, self.status))
+
+
+def run_host(vs: VerifyStep, io: HostStepIO, host_logits: torch.Tensor,
+             dev_logits: torch.Tensor, stream=None) -> int:
+    """One end-to-end compact step from pinned host buffers.
+
+    ``host_logits`` (pinned, [rows, V]) holds the target logits of the packed
+    rows in packed order, standing in for the verify forward's output;
+    ``dev_logits`` is the device buffer they are copied into.  Returns the
+    number of logits bytes copied host -> device.
+    """
+    s = torch.cuda.current_stream() if stream is None else stream
+    with torch.cuda.stream(s):
+        vs.conf_logits.copy_(io.conf_logits, non_blocking=True)
+        vs.sts_temps.copy_(io.sts_temps, non_blocking=True)
+        vs.anchor.copy_(io.anchor, non_blocking=True)
+        vs.draft.copy_(io.draft, non_blocking=True)
+        vs.prefix_lens.copy_(io.prefix_lens, non_blocking=True)
+        vs.status.zero_()
+        vs.plan(s)
+        vs.pack(s)
+        io.totals.copy_(vs.totals, non_blocking=True)
+        s.synchronize()  # the host needs the packed total to run the verify window
+        rows = int(io.totals[0])
+        dev_logits[:rows].copy_(host_logits[:rows], non_blocking=True)
+        vs.greedy_accept(dev_logits, write_argmax=False, stream=s)
+        io.out_tokens.copy_(vs.out_tokens, non_blocking=True)
+        io.commit_lens.copy_(vs.commit_lens, non_blocking=True)
+        io.new_seq_lens.copy_(vs.new_seq_lens, non_blocking=True)
+        io.verify_lens.copy_(vs.verify_lens, non_blocking=True)
+        io.status.copy_(vs.status, non_blocking=True)
+        s.synchronize()
+    return rows * host_logits.stride(0) * host_logits.element_size()

@@ -1,0 +1,230 @@
+/*
+ * dspark.h -- C ABI of the GB300 (sm_103a) DSpark verify planner, ragged
+ * verify pack and greedy / cap-accept library (libdspark.so).
+ *
+ * Pages cited below (by title and section):
+ *   [AVS]   "DSpark 自适应 Verify 怎样分配候选预算" -- DSpark adaptive
+ *           verify: how the candidate budget is allocated
+ *   [ROUND] "DeepSeek-V4 DSpark一轮 Draft、Verify、Accept 与 Commit" -- one
+ *           DSpark round: draft, verify, accept and commit
+ *   [SGL]   "DSpark接入SGLang：用置信度驱动可变长度验证" -- DSpark in SGLang
+ *   [TUT]   charlestar.github.io tutorial "DSpark confidence-scheduled
+ *           speculative decoding"
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer is DEVICE memory unless its comment says "host".
+ *   - The caller owns every buffer; the library allocates nothing.  Scratch
+ *     comes from a caller-provided device workspace whose size the matching
+ *     *_workspace_bytes() function returns (256-byte aligned pointer).
+ *   - All work is enqueued asynchronously on `stream` (a cudaStream_t passed
+ *     as void*; NULL = the legacy default stream).  No call synchronises the
+ *     host; every result, including the budget, stays in device memory.
+ *   - Return value: DSPARK_OK or a negative DSPARK_ERR_* code.  Argument
+ *     checks happen on the host before anything is enqueued, so a rejected
+ *     call has no effect on the device.
+ *   - `status` (device int32[1], zeroed by the caller) collects
+ *     DSPARK_STATUS_* bits that the kernels OR in for conditions only the
+ *     device can see.  Kernels never trap, assert or spin.
+ *   - Calls are stateless and thread-safe; concurrent calls must not share
+ *     workspaces.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DSPARK_API __attribute__((visibility("default")))
+#else
+#define DSPARK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- errors */
+#define DSPARK_OK               0
+#define DSPARK_ERR_INVALID_ARG (-1) /* null pointer, size or range violation */
+#define DSPARK_ERR_WORKSPACE   (-2) /* workspace missing, too small or misaligned */
+#define DSPARK_ERR_CUDA        (-3) /* a CUDA launch or attribute call failed */
+#define DSPARK_ERR_UNSUPPORTED (-4) /* outside the supported envelope (see each call) */
+
+/* device status bits (OR-ed into *status) */
+#define DSPARK_STATUS_CAPACITY    1  /* a row count exceeded the buffer's capacity */
+#define DSPARK_STATUS_TOKEN_RANGE 2  /* a draft token outside [0, V) */
+#define DSPARK_STATUS_NAN_LOGIT   4  /* a NaN in a target-logits row (NaN never wins the argmax) */
+#define DSPARK_STATUS_BAD_INPUT   8  /* a NaN confidence logit or a temperature that is not > 0 */
+#define DSPARK_STATUS_BAD_LEN     16 /* a verify length / cu_seqlens range outside [1, gamma+1] */
+#define DSPARK_STATUS_BAD_COST    32 /* cost table not ascending, or a non-positive / non-finite cost used */
+#define DSPARK_STATUS_INFEASIBLE  64 /* no budget in range: budget set to 0 */
+
+/* Message for a DSPARK_ERR_* code (static string). */
+DSPARK_API const char *dspark_strerror(int code);
+
+/* Library version: major*10000 + minor*100 + patch. */
+DSPARK_API int dspark_version(void);
+
+/* ---------------------------------------------------------------- planner */
+
+#define DSPARK_COST_SPS_1D   0
+#define DSPARK_COST_ADDITIVE 1
+
+/* Planner parameters (host struct).  [AVS] §一: ScheduleVerifyLensTopk is
+ * bounded by min_verify_len, max_verify_len and survival_eps. */
+typedef struct {
+    int32_t B;              /* requests in this planner decision, >= 1 */
+    int32_t gamma;          /* draft tokens per request, 1..31 */
+    float survival_eps;     /* candidates with survival < eps are dropped; in [2^-14, 1] */
+    int32_t min_verify_len; /* 1 <= min <= max */
+    int32_t max_verify_len; /* <= gamma + 1; depths >= max-1 are never candidates */
+    int32_t forced_budget;  /* < 0: budget = argmax theta; >= 0: this budget, clipped to range */
+} dspark_plan_params;
+
+/* Step-cost table (host struct pointing at DEVICE arrays M[n], val[n]).
+ *   DSPARK_COST_SPS_1D ([AVS] §一 and §四 "1D SpsCostTable"):
+ *     theta(b) = tau(b) * SPS(B + b); SPS is a floor lookup -- the sample
+ *     with the largest M_j <= B + b, sample 0 below the first -- with no
+ *     interpolation.  val = steps per second, must be > 0.
+ *   DSPARK_COST_ADDITIVE ([AVS] §一/§四 "Additive SPS"; [TUT] T(bs,K)):
+ *     theta(b) = tau(b) / T, T = (bias_ms + alpha_ms) + val[j] with j the
+ *     smallest graph tier M_j >= B + b; budgets above the largest tier are
+ *     infeasible.  alpha_ms is alpha(B) already evaluated for this B.
+ *   M must be strictly ascending (else DSPARK_STATUS_BAD_COST, all budgets
+ *   infeasible).  A used entry whose SPS or T is not a positive finite
+ *   number is infeasible and flagged DSPARK_STATUS_BAD_COST. */
+typedef struct {
+    int32_t kind;          /* DSPARK_COST_SPS_1D or DSPARK_COST_ADDITIVE */
+    int32_t n;             /* entries, >= 1 */
+    const int32_t *M;      /* device [n]: total verify rows (1-D) or graph tiers (additive) */
+    const double *val;     /* device [n]: SPS (steps/s) or token-side cost theta(M) in ms */
+    double bias_ms;        /* additive only */
+    double alpha_ms;       /* additive only */
+} dspark_cost_table;
+
+/* Device scratch of one planner call.  Currently 0: the planner keeps its
+ * whole state in one CTA's shared memory (hence B*gamma <= 24576). */
+DSPARK_API size_t dspark_plan_workspace_bytes(int32_t B, int32_t gamma);
+
+/* The verify planner.  [AVS] §一 (budget by survival, tau, theta, argmax,
+ * ScheduleVerifyLensTopk), §二 (STS c = sigmoid(z / T), S_k = prod c);
+ * [ROUND] §三 (resolve_verify_token_budget, schedule_layout).
+ *   conf_logits  [B, gamma] fp32 row-major: confidence-head logits z
+ *   sts_temps    [gamma] fp32: per-depth STS temperature T_k > 0
+ *   p, cost      host structs (above); cost->M / cost->val are device arrays
+ *   survivals    out [B, gamma] fp32: S_k = prod_{i<=k} sigmoid(z_i / T_i),
+ *                fp32 sequential product, 0 where S_k < eps
+ *   verify_lens  out [B] int32: 1 (root) + candidates selected for the
+ *                request, clamped to [min_verify_len, max_verify_len]
+ *   budget       out [1] int32: extra verify rows b (argmax or forced)
+ *   tau_theta    out [2] fp64: tau(budget) = B + sum of the budget largest
+ *                survivals (exact), theta(budget) (0 if the budget is infeasible)
+ * Candidates are ordered by survival descending, then depth ascending,
+ * then request id ascending; theta ties go to the smaller budget.
+ * Errors: INVALID_ARG (null pointer, B < 1, min/max out of order, cost n < 1
+ * or unknown kind); UNSUPPORTED (gamma > 31, B*(gamma+1) > 65536,
+ * B*gamma > 24576, eps outside [2^-14, 1]); CUDA.  Device flags: BAD_INPUT,
+ * BAD_COST, INFEASIBLE.  The workspace arguments are reserved (pass NULL, 0). */
+DSPARK_API int dspark_plan(const float *conf_logits, const float *sts_temps,
+                const dspark_plan_params *p /* host */, const dspark_cost_table *cost /* host */,
+                float *survivals, int32_t *verify_lens, int32_t *budget, double *tau_theta,
+                void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
+
+/* ------------------------------------------------------------------ pack */
+
+#define DSPARK_MAX_TIERS 64
+
+/* Front-pack the verify rows and round the total up to a graph tier.
+ * [ROUND] §三 (verify ids = [anchor, drafts]; BuildRaggedVerifyWindow /
+ * compact_verify_ids), §四 (verify positions); [AVS] §六 (cu_seqlens_q with
+ * a leading 0); [SGL] "Ragged verify"; [TUT] "变长批次如何与 CUDA Graph 共存".
+ *   anchor [B], draft [B, gamma], prefix_lens [B], verify_lens [B]: int32
+ *   host_tiers   host [n_tiers] ascending graph tiers (n_tiers <= 64; 0 = no
+ *                rounding)
+ *   capacity     rows available in each packed_* buffer
+ *   packed_ids/pos/req/src  out [capacity] int32.  Row cu[r]+j (j < len_r):
+ *                id = anchor[r] (j = 0) or draft[r][j-1]; pos = prefix_lens[r]
+ *                + j; req = r; src = r*(gamma+1) + j (row in the strided
+ *                [B, gamma+1] layout).  Rows [total, padded) are pad rows
+ *                (0, 0, -1, -1); rows >= padded are not written.
+ *   cu_seqlens   out [B+1] int32, cu[0] = 0
+ *   totals       out [2] int32: {total, padded}
+ * A length outside [1, gamma+1] is clamped and flagged BAD_LEN; rows past
+ * capacity are dropped and flagged CAPACITY, as is a total above the
+ * largest tier (then padded = total).
+ * Errors: INVALID_ARG (null pointer, B < 1, gamma outside 1..31, capacity
+ * < 0, n_tiers outside 0..64, tiers not ascending); CUDA. */
+DSPARK_API int dspark_pack_verify(const int32_t *anchor, const int32_t *draft, const int32_t *prefix_lens,
+                       const int32_t *verify_lens, int32_t B, int32_t gamma,
+                       const int32_t *host_tiers /* host */, int32_t n_tiers, int32_t capacity,
+                       int32_t *packed_ids, int32_t *packed_pos, int32_t *packed_req,
+                       int32_t *packed_src, int32_t *cu_seqlens, int32_t *totals,
+                       int32_t *status, void *stream);
+
+/* ---------------------------------------------------------------- accept */
+
+#define DSPARK_DTYPE_BF16 0
+#define DSPARK_DTYPE_F32  1
+
+/* Scratch of one accept call over at most max_rows rows. */
+DSPARK_API size_t dspark_accept_workspace_bytes(int32_t max_rows, int32_t V);
+
+/* Compact-mode greedy accept.  [ROUND] §五 "Greedy" (target_predict =
+ * argmax(target_logits); correct_len = leading drafts equal to the target
+ * chain; bonus from the last valid input row; no acceptance past the first
+ * mismatch), FinalizeAcceptLens and BuildOutTokens.
+ *   logits       [max_rows, ld] bf16 or fp32 (dtype), row stride ld >= V
+ *                elements; 16-byte aligned base and ld*elem % 16 == 0 take
+ *                the vector path, anything else a scalar path
+ *   cu_seqlens   [B+1]: request r owns packed rows [cu[r], cu[r+1]); rows
+ *                = min(cu[B], max_rows) rows are read (CAPACITY if cu[B] >
+ *                max_rows)
+ *   draft        [B, gamma]; prefix_lens [B] (may be NULL iff new_seq_lens is)
+ *   argmax       out [max_rows] (nullable): argmax of every row < rows --
+ *                lowest index of the largest non-NaN value, -0 == +0, 0 for
+ *                a row with nothing above -inf
+ *   num_accepted out [B]: correct_len = first j < L-1 with argmax(row
+ *                cu[r]+j) != draft[r][j], else L-1 (L = cu[r+1]-cu[r])
+ *   bonus        out [B]: argmax of row cu[r] + correct_len
+ *   commit_lens  out [B]: correct_len + 1
+ *   new_seq_lens out [B] (nullable): prefix_lens + commit_lens
+ *   out_tokens   out [B, gamma+1]: drafts, -1 in column gamma, then the
+ *                bonus written at column correct_len
+ * A request whose range is empty, longer than gamma+1 or beyond rows gets
+ * correct 0, bonus -1, commit 0 (flag BAD_LEN).  Device flags also:
+ * TOKEN_RANGE, NAN_LOGIT, CAPACITY.
+ * Errors: INVALID_ARG (null pointer, B < 1, gamma outside 1..31, V < 1,
+ * ld < V, max_rows < 0, unknown dtype, new_seq_lens without prefix_lens);
+ * WORKSPACE; CUDA. */
+DSPARK_API int dspark_greedy_accept(const void *logits, int32_t dtype, int64_t ld, int32_t V,
+                         int32_t max_rows, const int32_t *cu_seqlens, const int32_t *draft,
+                         const int32_t *prefix_lens, int32_t B, int32_t gamma, int32_t *argmax,
+                         int32_t *num_accepted, int32_t *bonus, int32_t *commit_lens,
+                         int32_t *new_seq_lens, int32_t *out_tokens, void *workspace,
+                         size_t workspace_bytes, int32_t *status, void *stream);
+
+/* cap-accept: verify the full block, commit only the window.  [AVS] §三
+ * (capped_correct_len = min(raw_correct_len, verify_len - 1)), §五
+ * "cap-accept"; [SGL] "三种 verify mode" (commits equal compact's and the
+ * full-verify acceptance ceiling is exposed).
+ *   logits       [B*(gamma+1), ld] strided verify rows, row r*(gamma+1)+j
+ *   verify_lens  [B] (clamped to [1, gamma+1], flag BAD_LEN)
+ *   outputs as dspark_greedy_accept, with L = gamma+1 for the raw count:
+ *   num_accepted = capped; bonus = argmax of row r*(gamma+1) + capped
+ *   ceiling      out [B]: raw correct_len over the full block
+ *   totals       out [2] int32: {sum commit_lens, sum (ceiling + 1)}
+ * Errors as dspark_greedy_accept. */
+DSPARK_API int dspark_cap_accept(const void *logits, int32_t dtype, int64_t ld, int32_t V,
+                      const int32_t *verify_lens, const int32_t *draft,
+                      const int32_t *prefix_lens, int32_t B, int32_t gamma, int32_t *argmax,
+                      int32_t *num_accepted, int32_t *bonus, int32_t *commit_lens,
+                      int32_t *new_seq_lens, int32_t *out_tokens, int32_t *ceiling,
+                      int32_t *totals, void *workspace, size_t workspace_bytes,
+                      int32_t *status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

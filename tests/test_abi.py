@@ -1,0 +1,138 @@
+"""The C-ABI library builds, loads and exports every symbol include/*.h
+declares; host-side argument checks return their error codes.  No call here
+reaches the GPU: each rejected call returns before anything is enqueued."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: rejected before any CUDA call
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from confidence_scheduled_speculative_gb300 import build
+    try:
+        path = build.build()
+    except RuntimeError as e:  # pragma: no cover - toolkit missing
+        pytest.skip(str(e))
+    return ctypes.CDLL(path)
+
+
+def declared_symbols():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        with open(h) as f:
+            text = f.read()
+        names += re.findall(r"DSPARK_API[^;(]*?\b(dspark_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_four_calls():
+    names = declared_symbols()
+    for n in ("dspark_plan", "dspark_pack_verify", "dspark_greedy_accept", "dspark_cap_accept"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror_and_version(lib):
+    lib.dspark_strerror.restype = ctypes.c_char_p
+    assert lib.dspark_strerror(0) == b"ok"
+    assert b"invalid" in lib.dspark_strerror(-1)
+    assert b"workspace" in lib.dspark_strerror(-2)
+    assert lib.dspark_version() >= 100
+
+
+class Params(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("gamma", ctypes.c_int32), ("eps", ctypes.c_float),
+                ("min_len", ctypes.c_int32), ("max_len", ctypes.c_int32),
+                ("forced", ctypes.c_int32)]
+
+
+class Cost(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("n", ctypes.c_int32), ("M", ctypes.c_void_p),
+                ("val", ctypes.c_void_p), ("bias", ctypes.c_double), ("alpha", ctypes.c_double)]
+
+
+def _plan(lib, p, c, null_out=False):
+    f = lib.dspark_plan
+    f.restype = ctypes.c_int
+    out = None if null_out else FAKE
+    return f(FAKE, FAKE, ctypes.byref(p), ctypes.byref(c), FAKE, out, FAKE, FAKE, None,
+             ctypes.c_size_t(0), FAKE, None)
+
+
+def test_plan_argument_checks(lib):
+    good = dict(B=4, gamma=4, eps=1e-4, min_len=1, max_len=5, forced=-1)
+    cost = Cost(0, 3, FAKE.value, FAKE.value, 0.0, 0.0)
+    assert _plan(lib, Params(**good), cost, null_out=True) == -1
+    assert _plan(lib, Params(**{**good, "B": 0}), cost) == -1
+    assert _plan(lib, Params(**{**good, "gamma": 32}), cost) == -4
+    assert _plan(lib, Params(**{**good, "eps": 1e-6}), cost) == -4
+    assert _plan(lib, Params(**{**good, "eps": 2.0}), cost) == -4
+    assert _plan(lib, Params(**{**good, "eps": float("nan")}), cost) == -1
+    assert _plan(lib, Params(**{**good, "min_len": 3, "max_len": 2}), cost) == -1
+    assert _plan(lib, Params(**{**good, "max_len": 6}), cost) == -1
+    assert _plan(lib, Params(**{**good, "B": 2048, "gamma": 16}), cost) == -4  # 2048*17 > 2^16
+    assert _plan(lib, Params(**{**good, "B": 1600, "gamma": 16}), cost) == -4  # > 24576 candidates
+    assert _plan(lib, Params(**good), Cost(2, 3, FAKE.value, FAKE.value, 0, 0)) == -1
+    assert _plan(lib, Params(**good), Cost(0, 0, FAKE.value, FAKE.value, 0, 0)) == -1
+    assert _plan(lib, Params(**good), Cost(1, 3, None, FAKE.value, 0, 0)) == -1
+    lib.dspark_plan_workspace_bytes.restype = ctypes.c_size_t
+    assert lib.dspark_plan_workspace_bytes(256, 16) == 0
+
+
+def test_pack_argument_checks(lib):
+    f = lib.dspark_pack_verify
+    f.restype = ctypes.c_int
+    tiers = (ctypes.c_int32 * 65)(*range(1, 66))
+
+    def call(B=4, gamma=4, n_tiers=0, cap=16, t=tiers, first=FAKE):
+        return f(first, FAKE, FAKE, FAKE, B, gamma, t, n_tiers, cap, FAKE, FAKE, FAKE, FAKE,
+                 FAKE, FAKE, FAKE, None)
+
+    assert call(first=None) == -1
+    assert call(B=0) == -1
+    assert call(gamma=32) == -1
+    assert call(cap=-1) == -1
+    assert call(n_tiers=65) == -1
+    bad = (ctypes.c_int32 * 3)(8, 4, 16)
+    assert call(n_tiers=3, t=bad) == -1
+
+
+def test_accept_argument_checks(lib):
+    g = lib.dspark_greedy_accept
+    g.restype = ctypes.c_int
+    lib.dspark_accept_workspace_bytes.restype = ctypes.c_size_t
+    need = lib.dspark_accept_workspace_bytes(100, 1000)
+    assert need >= 100 * 8 and need % 256 == 0
+
+    def call(dtype=0, ld=1024, V=1000, max_rows=100, ws_bytes=None, new_seq=None, prefix=FAKE,
+             ws=FAKE):
+        wb = need if ws_bytes is None else ws_bytes
+        return g(FAKE, dtype, ctypes.c_int64(ld), V, max_rows, FAKE, FAKE, prefix, 4, 4, None,
+                 FAKE, FAKE, FAKE, new_seq, FAKE, ws, ctypes.c_size_t(wb), FAKE, None)
+
+    assert call(dtype=2) == -1
+    assert call(ld=999) == -1
+    assert call(V=0) == -1
+    assert call(max_rows=-1) == -1
+    assert call(new_seq=FAKE, prefix=None) == -1
+    assert call(ws_bytes=need - 8) == -2
+    assert call(ws=None) == -2
+    assert call(ws=ctypes.c_void_p(0x10010)) == -2  # not 256-byte aligned
+    c = lib.dspark_cap_accept
+    c.restype = ctypes.c_int
+    assert c(FAKE, 0, ctypes.c_int64(1024), 1000, FAKE, FAKE, FAKE, 4, 4, None, FAKE, FAKE,
+             FAKE, None, FAKE, None, FAKE, FAKE, ctypes.c_size_t(need), FAKE, None) == -1

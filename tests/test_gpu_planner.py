@@ -1,0 +1,215 @@
+"""GPU parity of the planner (dspark_plan) and the pack (dspark_pack_verify)
+against the CPU oracle, element by element on the same seeded inputs,
+through the C-ABI.  Discrete outputs are compared bit-exactly; survivals,
+tau and theta too (the arithmetic is defined to give identical floats)."""
+
+import numpy as np
+import pytest
+import torch
+
+from confidence_scheduled_speculative_gb300 import workloads as wl
+from gpu_helpers import compare_plan, oracle_plan, require_gpu, run_plan_pack
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return require_gpu()
+
+
+def _pack_ref(orc, step, lens, sentinel):
+    return orc.pack(step.anchor, step.draft, step.prefix_lens, lens, step.tiers, step.capacity,
+                    sentinel=sentinel)
+
+
+def _check_pack(tag, gpu, ref, cap):
+    tot = ref.total
+    np.testing.assert_array_equal(gpu["cu_seqlens"], ref.cu_seqlens, err_msg=f"{tag} cu")
+    assert list(gpu["totals"]) == [ref.total, ref.padded], tag
+    n = min(max(ref.padded, tot), cap)
+    for k in ("ids", "pos", "req", "src"):
+        np.testing.assert_array_equal(gpu["packed_" + k][:n], ref[k][:n], err_msg=f"{tag} {k}")
+
+
+CASES = ([("tiny", s, None) for s in range(6)] + [("qwen_like", s, None) for s in range(3)]
+         + [("dsv4_like", s, None) for s in range(3)] + [("mixed", s, None) for s in range(4)]
+         + [("stress", 0, f) for f in (None, 0, 1024, 8192, 16384)])
+
+
+@pytest.mark.parametrize("name,seed,forced", CASES)
+def test_plan_and_pack_workloads(dev, orc, name, seed, forced):
+    step = wl.make_step(wl.WORKLOADS[name], seed=seed)
+    vs, g = run_plan_pack(dev, step, forced)
+    ref = oracle_plan(orc, step, forced)
+    strict = compare_plan(f"{name}/{seed}/{forced}", g, ref, step.B, step.gamma,
+                          step.workload.min_verify_len)
+    assert int(g["status"][0]) == ref.status
+    if strict:
+        # the pack consumes the GPU's verify_lens, equal to the oracle's here
+        p = _pack_ref(orc, step, ref.verify_lens, sentinel=0)
+        _check_pack(name, g, p, step.capacity)
+
+
+def _random_problem(rng):
+    while True:
+        gamma = int(rng.integers(1, 32))
+        B = int(rng.integers(1, 48))
+        if B * (gamma + 1) <= 65536:
+            break
+    mu, sd = rng.uniform(-1, 4), rng.uniform(0.1, 3)
+    z = rng.normal(mu, sd, size=(B, gamma)).astype(np.float32)
+    if rng.random() < 0.4:  # exact ties: repeat some requests
+        k = int(rng.integers(1, B + 1))
+        z[rng.integers(0, B, size=k)] = z[int(rng.integers(0, B))]
+    if rng.random() < 0.2:  # saturated confidences: survivals of exactly 1.0
+        z[:, : max(1, gamma // 2)] = 40.0
+    T = rng.uniform(0.5, 2.0, size=gamma).astype(np.float32)
+    if rng.random() < 0.3:
+        T[:] = 1.0
+    eps = float(np.float32(rng.choice([2.0 ** -14, 1e-4, 0.01, 0.2])))
+    max_len = int(rng.integers(1, gamma + 2))
+    min_len = int(rng.integers(1, max_len + 1)) if rng.random() < 0.3 else 1
+    kind = int(rng.integers(0, 2))
+    n = int(rng.integers(1, 12))
+    hi = B + B * gamma + 6
+    M = np.sort(rng.choice(np.arange(1, hi + 1), size=min(n, hi), replace=False)).astype(np.int32)
+    val = (rng.uniform(100, 1000, M.size) if kind == 0 else rng.uniform(0.01, 3.0, M.size))
+    if rng.random() < 0.1:
+        val[int(rng.integers(0, M.size))] = 0.0 if kind == 0 else -100.0
+    forced = -1 if rng.random() < 0.6 else int(rng.integers(0, B * gamma + 4))
+    bias, alpha = float(rng.uniform(0, 2)), float(rng.uniform(0, 1))
+    return dict(B=B, gamma=gamma, z=z, T=T, eps=eps, min_len=min_len, max_len=max_len,
+                kind=kind, M=M, val=val, forced=forced, bias=bias, alpha=alpha)
+
+
+def _gpu_plan(dev, P):
+    from confidence_scheduled_speculative_gb300 import api
+    B, g = P["B"], P["gamma"]
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = dict(survivals=torch.zeros((B, g), dtype=torch.float32, device=dev),
+               verify_lens=torch.zeros(B, **i32), budget=torch.zeros(1, **i32),
+               tau_theta=torch.zeros(2, dtype=torch.float64, device=dev),
+               status=torch.zeros(1, **i32))
+    api.dspark_plan(torch.from_numpy(P["z"]).to(dev), torch.from_numpy(P["T"]).to(dev), B=B,
+                    gamma=g, survival_eps=P["eps"], min_verify_len=P["min_len"],
+                    max_verify_len=P["max_len"], forced_budget=P["forced"], cost_kind=P["kind"],
+                    cost_M=torch.from_numpy(P["M"]).to(dev),
+                    cost_val=torch.from_numpy(P["val"]).to(dev), bias_ms=P["bias"],
+                    alpha_ms=P["alpha"], **out)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+@pytest.mark.parametrize("seed", range(150))
+def test_plan_random(dev, orc, seed):
+    rng = np.random.default_rng(70000 + seed)
+    P = _random_problem(rng)
+    g = _gpu_plan(dev, P)
+    ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"], P["kind"],
+                   P["M"], P["val"], P["bias"], P["alpha"])
+    if compare_plan(f"random/{seed}", g, ref, P["B"], P["gamma"], P["min_len"]):
+        assert int(g["status"][0]) == ref.status
+
+
+def test_plan_edge_cases(dev, orc):
+    cases = []
+    # every survival below eps: budget 0, all lens = min
+    cases.append(dict(B=3, gamma=4, z=np.full((3, 4), -12.0, np.float32), T=np.ones(4, np.float32),
+                      eps=0.01, min_len=1, max_len=5, kind=0, M=np.array([1], np.int32),
+                      val=np.array([5.0]), forced=-1, bias=0.0, alpha=0.0))
+    # B = 1, gamma = 1
+    cases.append(dict(B=1, gamma=1, z=np.array([[2.0]], np.float32), T=np.ones(1, np.float32),
+                      eps=1e-4, min_len=1, max_len=2, kind=1, M=np.array([1, 2], np.int32),
+                      val=np.array([1.0, 1.1]), forced=-1, bias=0.5, alpha=0.1))
+    # gamma = 31, many identical requests (ties everywhere)
+    z = np.tile(np.linspace(4, -1, 31, dtype=np.float32), (40, 1))
+    cases.append(dict(B=40, gamma=31, z=z, T=np.ones(31, np.float32), eps=1e-4, min_len=1,
+                      max_len=32, kind=0, M=np.arange(40, 40 + 40 * 31 + 1, dtype=np.int32),
+                      val=1.0 / (1e-3 + 2e-6 * np.arange(40, 40 + 40 * 31 + 1)), forced=-1,
+                      bias=0.0, alpha=0.0))
+    # additive table whose largest tier is below B: infeasible
+    cases.append(dict(B=8, gamma=3, z=np.ones((8, 3), np.float32), T=np.ones(3, np.float32),
+                      eps=1e-4, min_len=2, max_len=4, kind=1, M=np.array([4], np.int32),
+                      val=np.array([1.0]), forced=-1, bias=1.0, alpha=0.0))
+    # cost table not ascending, forced budget
+    cases.append(dict(B=4, gamma=4, z=np.ones((4, 4), np.float32), T=np.ones(4, np.float32),
+                      eps=1e-4, min_len=1, max_len=5, kind=0, M=np.array([5, 5, 9], np.int32),
+                      val=np.array([1.0, 2.0, 3.0]), forced=3, bias=0.0, alpha=0.0))
+    # NaN confidence and a zero temperature
+    zn = np.ones((4, 4), np.float32)
+    zn[1, 2] = np.nan
+    Tz = np.ones(4, np.float32)
+    Tz[3] = 0.0
+    cases.append(dict(B=4, gamma=4, z=zn, T=Tz, eps=1e-4, min_len=1, max_len=5, kind=0,
+                      M=np.array([1], np.int32), val=np.array([3.0]), forced=-1, bias=0.0,
+                      alpha=0.0))
+    # the largest planner (24576 candidates)
+    rng = np.random.default_rng(5)
+    cases.append(dict(B=1536, gamma=16, z=rng.normal(1, 1.5, (1536, 16)).astype(np.float32),
+                      T=np.ones(16, np.float32), eps=1e-4, min_len=1, max_len=17, kind=1,
+                      M=(2 ** np.arange(10, 16)).astype(np.int32),
+                      val=0.001 * 2.0 ** np.arange(10, 16), forced=-1, bias=2.0, alpha=7.68))
+    for i, P in enumerate(cases):
+        g = _gpu_plan(dev, P)
+        ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"],
+                       P["kind"], P["M"], P["val"], P["bias"], P["alpha"])
+        assert compare_plan(f"edge/{i}", g, ref, P["B"], P["gamma"], P["min_len"]), i
+        assert int(g["status"][0]) == ref.status, (i, int(g["status"][0]), ref.status)
+
+
+def _gpu_pack(dev, anchor, draft, prefix, lens, tiers, cap, sentinel):
+    from confidence_scheduled_speculative_gb300 import api
+    B, g = draft.shape
+    i32 = dict(dtype=torch.int32, device=dev)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    outs = [torch.full((max(cap, 1),), sentinel, **i32) for _ in range(4)]
+    cu = torch.full((B + 1,), sentinel, **i32)
+    totals = torch.zeros(2, **i32)
+    status = torch.zeros(1, **i32)
+    api.dspark_pack_verify(t(anchor), t(draft), t(prefix), t(lens), B=B, gamma=g, tiers=tiers,
+                           capacity=cap, packed_ids=outs[0], packed_pos=outs[1],
+                           packed_req=outs[2], packed_src=outs[3], cu_seqlens=cu, totals=totals,
+                           status=status)
+    torch.cuda.synchronize()
+    names = ["ids", "pos", "req", "src"]
+    res = {n: o.cpu().numpy()[:cap] for n, o in zip(names, outs)}
+    res.update(cu_seqlens=cu.cpu().numpy(), totals=totals.cpu().numpy(),
+               status=int(status.cpu()[0]))
+    return res
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_pack_random(dev, orc, seed):
+    rng = np.random.default_rng(90000 + seed)
+    gamma = int(rng.integers(1, 32))
+    B = int(rng.integers(1, 300))
+    lens = rng.integers(1, gamma + 2, size=B).astype(np.int32)
+    if rng.random() < 0.2:
+        lens[rng.integers(0, B)] = int(rng.choice([0, -3, gamma + 2]))
+    total = int(np.clip(lens, 1, gamma + 1).sum())
+    tiers = []
+    if rng.random() < 0.6:
+        tiers = sorted(set(int(x) for x in rng.integers(1, 2 * total + 2, size=int(rng.integers(1, 8)))))
+    cap = int(rng.choice([total + 64, total, max(0, total - 5), 2 * total + 2]))
+    anchor = rng.integers(0, 1000, B)
+    draft = rng.integers(0, 1000, (B, gamma))
+    prefix = rng.integers(0, 5000, B)
+    g = _gpu_pack(dev, anchor, draft, prefix, lens, tiers, cap, sentinel=-9)
+    r = orc.pack(anchor, draft, prefix, lens, tiers, cap, sentinel=-9)
+    np.testing.assert_array_equal(g["cu_seqlens"], r.cu_seqlens)
+    assert list(g["totals"]) == [r.total, r.padded]
+    for k in ("ids", "pos", "req", "src"):
+        np.testing.assert_array_equal(g[k], r[k][:cap], err_msg=k)  # incl. untouched rows
+    assert g["status"] == r.status
+
+
+def test_pack_page_layout_on_gpu(dev, orc):
+    lens = np.array([2, 1, 4], np.int32)
+    anchor = np.array([100, 200, 300])
+    draft = np.array([[101, 102, 103], [201, 202, 203], [301, 302, 303]])
+    g = _gpu_pack(dev, anchor, draft, np.array([10, 20, 30]), lens, [40, 64, 80], 64, -9)
+    assert list(g["cu_seqlens"]) == [0, 2, 3, 7]
+    assert list(g["ids"][:7]) == [100, 101, 200, 300, 301, 302, 303]
+    assert list(g["totals"]) == [7, 40]
+    assert np.all(g["req"][7:40] == -1) and np.all(g["req"][40:] == -9)
