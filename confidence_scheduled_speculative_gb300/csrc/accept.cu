@@ -25,10 +25,12 @@
 //   writes one partial (max, lowest index) to slot c + r, which is unique
 //   because c + r increases by at least one from one piece to the next.
 //   Inner loop: kUnroll independent 16-byte non-allocating loads per thread
-//   in flight, then a packed bf16x2 max over the 8 values of each chunk
-//   (NaN-propagating); only when that max beats the running best (or is NaN)
-//   does the thread walk the chunk element by element, so the common path
-//   costs about one instruction per element.
+//   in flight; each chunk is reduced by a packed bf16x2 NaN-propagating max
+//   (5 instructions for 8 values) and folded into a running (max, first
+//   chunk holding it) with one compare and two selects -- no divergent
+//   per-element path.  After the block reduction the winning chunk is read
+//   once more to find the first element equal to the max (-0 == +0).  A
+//   chunk holding a NaN takes a rare path that skips the NaN and flags it.
 // finalize kernels  one warp per request, lane j = verify row j: combine the
 //   partials of the row, compare with draft j, ballot the mismatches; the
 //   first set bit is correct_len (no acceptance after the first mismatch).
@@ -95,87 +97,129 @@ struct Elem<__nv_bfloat16> {
     __device__ static float load(const __nv_bfloat16 *p) {
         return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(p)) << 16);
     }
-    __device__ static void chunk(const uint4 &v, int base, float &best, int &bidx, bool &nan) {
+    __device__ static float at(const uint4 &v, int e) {
+        const uint32_t w = e < 2 ? v.x : (e < 4 ? v.y : (e < 6 ? v.z : v.w));
+        return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+    }
+    // Largest value of the chunk; NaN if the chunk holds a NaN.  Packed
+    // bf16x2 NaN-propagating max: 5 instructions for 8 values.
+    __device__ static float chunk_max(const uint4 &v) {
         __nv_bfloat162 a, b, c, d;
         *reinterpret_cast<uint32_t *>(&a) = v.x;
         *reinterpret_cast<uint32_t *>(&b) = v.y;
         *reinterpret_cast<uint32_t *>(&c) = v.z;
         *reinterpret_cast<uint32_t *>(&d) = v.w;
-        const __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
-        if (!(__low2float(m) <= best) || !(__high2float(m) <= best)) {
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                take(bf16_lo(w[q]), base + 2 * q, best, bidx, nan);
-                take(bf16_hi(w[q]), base + 2 * q + 1, best, bidx, nan);
-            }
-        }
+        __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+        const uint32_t mw = *reinterpret_cast<uint32_t *>(&m);
+        __nv_bfloat162 sw;
+        *reinterpret_cast<uint32_t *>(&sw) = __byte_perm(mw, 0u, 0x1032);
+        m = __hmax2_nan(m, sw);
+        return bf16_lo(*reinterpret_cast<uint32_t *>(&m));
     }
 };
 template <>
 struct Elem<float> {
     static constexpr int kPerChunk = 4;
     __device__ static float load(const float *p) { return __ldg(p); }
-    __device__ static void chunk(const uint4 &v, int base, float &best, int &bidx, bool &nan) {
+    __device__ static float at(const uint4 &v, int e) {
+        const uint32_t w = e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
+        return __uint_as_float(w);
+    }
+    __device__ static float chunk_max(const uint4 &v) {
         const float f0 = __uint_as_float(v.x), f1 = __uint_as_float(v.y);
         const float f2 = __uint_as_float(v.z), f3 = __uint_as_float(v.w);
-        if (!(f0 <= best) || !(f1 <= best) || !(f2 <= best) || !(f3 <= best)) {
-            take(f0, base, best, bidx, nan);
-            take(f1, base + 1, best, bidx, nan);
-            take(f2, base + 2, best, bidx, nan);
-            take(f3, base + 3, best, bidx, nan);
-        }
+        const bool nan = (f0 != f0) | (f1 != f1) | (f2 != f2) | (f3 != f3);
+        return nan ? __uint_as_float(0x7FC00000u) : fmaxf(fmaxf(f0, f1), fmaxf(f2, f3));
     }
 };
 
-// Scan chunks [c0, c1) of one row.  VEC: 16-byte chunks (the last one of a
-// row may be partial and is read element-wise); otherwise one element per
-// chunk.
-template <typename T, bool VEC>
-__device__ __forceinline__ void scan_row(const T *row, int c0, int c1, int full, int V,
-                                         float &best, int &bidx, bool &nan) {
-    constexpr int EPC = VEC ? Elem<T>::kPerChunk : 1;
-    const int step = kUnroll * kArgmaxThreads;
-    if (VEC) {
-        const uint4 *row4 = reinterpret_cast<const uint4 *>(row);
-        for (int c = c0 + (int)threadIdx.x; c < c1; c += step) {
-            uint4 v[kUnroll];
+// Largest non-NaN value of a chunk that holds a NaN (rare path).
+template <typename T>
+__device__ __noinline__ float chunk_max_nonnan(uint4 v) {
+    float m = -INFINITY;
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int cc = c + u * kArgmaxThreads;
-                if (cc < c1 && cc < full) v[u] = ld_stream16(row4 + cc);
-            }
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int cc = c + u * kArgmaxThreads;
-                if (cc < c1) {
-                    if (cc < full) {
-                        Elem<T>::chunk(v[u], cc * EPC, best, bidx, nan);
-                    } else {
-                        for (int e = cc * EPC; e < V; ++e) take(Elem<T>::load(row + e), e, best, bidx, nan);
-                    }
-                }
-            }
-        }
-    } else {
-        for (int c = c0 + (int)threadIdx.x; c < c1; c += step) {
-            float f[kUnroll];
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int cc = c + u * kArgmaxThreads;
-                f[u] = cc < c1 ? Elem<T>::load(row + cc) : 0.0f;
-            }
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int cc = c + u * kArgmaxThreads;
-                if (cc < c1) take(f[u], cc, best, bidx, nan);
-            }
-        }
+    for (int e = 0; e < Elem<T>::kPerChunk; ++e) {
+        const float f = Elem<T>::at(v, e);
+        if (f > m) m = f;
     }
+    return m;
+}
+
+// One chunk into the running (best value, first chunk holding it).  The
+// element index is recovered once per row segment, so the common path is
+// branch-free: compare, two selects.
+template <typename T>
+__device__ __forceinline__ void chunk_step(const uint4 &v, int cc, float &best, int &bchunk,
+                                           bool &nan) {
+    float m = Elem<T>::chunk_max(v);
+    if (m != m) {
+        nan = true;
+        m = chunk_max_nonnan<T>(v);
+    }
+    const bool up = m > best;
+    best = up ? m : best;
+    bchunk = up ? cc : bchunk;
+}
+
+// Scan the full 16-byte chunks [c0, c1) of one row.
+template <typename T>
+__device__ __forceinline__ void scan_chunks(const uint4 *row4, int c0, int c1, float &best,
+                                            int &bchunk, bool &nan) {
+    int c = c0 + (int)threadIdx.x;
+    for (; c + (kUnroll - 1) * kArgmaxThreads < c1; c += kUnroll * kArgmaxThreads) {
+        uint4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream16(row4 + c + u * kArgmaxThreads);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) chunk_step<T>(v[u], c + u * kArgmaxThreads, best, bchunk, nan);
+    }
+    for (; c < c1; c += kArgmaxThreads) chunk_step<T>(ld_stream16(row4 + c), c, best, bchunk, nan);
+}
+
+// Scalar scan of elements [e0, e1) (unaligned rows).
+template <typename T>
+__device__ __forceinline__ void scan_scalar(const T *row, int e0, int e1, float &best, int &bidx,
+                                            bool &nan) {
+    int e = e0 + (int)threadIdx.x;
+    for (; e + (kUnroll - 1) * kArgmaxThreads < e1; e += kUnroll * kArgmaxThreads) {
+        float f[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) f[u] = Elem<T>::load(row + e + u * kArgmaxThreads);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) take(f[u], e + u * kArgmaxThreads, best, bidx, nan);
+    }
+    for (; e < e1; e += kArgmaxThreads) take(Elem<T>::load(row + e), e, best, bidx, nan);
 }
 
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
     return v > bv || (v == bv && i < bi);
+}
+
+// Block-wide (max value, lowest index); the result is valid in thread 0.
+__device__ __forceinline__ void block_best(float &best, int &bidx, float *red_v, int *red_i) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+        const float ov = __shfl_down_sync(kFullMask, best, d);
+        const int oi = __shfl_down_sync(kFullMask, bidx, d);
+        if (better(ov, oi, best, bidx)) {
+            best = ov;
+            bidx = oi;
+        }
+    }
+    if (lane == 0) {
+        red_v[warp] = best;
+        red_i[warp] = bidx;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kArgmaxThreads / 32; ++w)
+            if (better(red_v[w], red_i[w], best, bidx)) {
+                best = red_v[w];
+                bidx = red_i[w];
+            }
+    }
+    __syncthreads();
 }
 
 template <typename T, bool VEC>
@@ -183,7 +227,6 @@ __global__ void __launch_bounds__(kArgmaxThreads, kCtasPerSm) argmax_kernel(Argm
     __shared__ float red_v[kArgmaxThreads / 32];
     __shared__ int red_i[kArgmaxThreads / 32];
     constexpr int EPC = VEC ? Elem<T>::kPerChunk : 1;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
     pdl_trigger();
     pdl_wait();  // cu_seqlens / logits come from the kernels before
@@ -195,8 +238,8 @@ __global__ void __launch_bounds__(kArgmaxThreads, kCtasPerSm) argmax_kernel(Argm
             a.zero_totals[1] = 0;
         }
     }
-    const int cpr = (a.V + EPC - 1) / EPC;
-    const int full = a.V / EPC;
+    const int cpr = (a.V + EPC - 1) / EPC;  // chunks per row, the last one maybe partial
+    const int full = a.V / EPC;             // full chunks per row
     const long long W = (long long)rows * cpr;
     const long long per = (W + gridDim.x - 1) / gridDim.x;
     const long long q0 = (long long)blockIdx.x * per;
@@ -209,33 +252,32 @@ __global__ void __launch_bounds__(kArgmaxThreads, kCtasPerSm) argmax_kernel(Argm
         const int c1 = c0 + (int)(seg_end - q);
         const T *row = reinterpret_cast<const T *>(a.logits) + (long long)r * a.ld;
         float best = -INFINITY;
-        int bidx = c0 * EPC;
-        scan_row<T, VEC>(row, c0, c1, full, a.V, best, bidx, nan);
+        int bidx;
+        if (VEC) {
+            int bchunk = c0;
+            scan_chunks<T>(reinterpret_cast<const uint4 *>(row), c0, min(c1, full), best, bchunk,
+                           nan);
+            block_best(best, bchunk, red_v, red_i);  // lowest chunk holding the max
+            if (threadIdx.x == 0) {
+                bidx = c0 * EPC;
+                if (best > -INFINITY) {
+                    // first element of that chunk equal to the max (-0 == +0)
+                    const uint4 v = ld_stream16(reinterpret_cast<const uint4 *>(row) + bchunk);
+                    bidx = bchunk * EPC + EPC - 1;
 #pragma unroll
-        for (int d = 16; d > 0; d >>= 1) {
-            const float ov = __shfl_down_sync(kFullMask, best, d);
-            const int oi = __shfl_down_sync(kFullMask, bidx, d);
-            if (better(ov, oi, best, bidx)) {
-                best = ov;
-                bidx = oi;
-            }
-        }
-        if (lane == 0) {
-            red_v[warp] = best;
-            red_i[warp] = bidx;
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float bv = red_v[0];
-            int bi = red_i[0];
-            for (int w = 1; w < kArgmaxThreads / 32; ++w)
-                if (better(red_v[w], red_i[w], bv, bi)) {
-                    bv = red_v[w];
-                    bi = red_i[w];
+                    for (int e = EPC - 1; e >= 0; --e)
+                        if (Elem<T>::at(v, e) == best) bidx = bchunk * EPC + e;
                 }
-            a.partial[blockIdx.x + r] = Partial{bv, bi};
+                // the row's partial last chunk, element by element
+                for (int e = full * EPC; c1 > full && e < a.V; ++e)
+                    take(Elem<T>::load(row + e), e, best, bidx, nan);
+            }
+        } else {
+            bidx = c0;
+            scan_scalar<T>(row, c0, c1, best, bidx, nan);
+            block_best(best, bidx, red_v, red_i);
         }
-        __syncthreads();
+        if (threadIdx.x == 0) a.partial[blockIdx.x + r] = Partial{best, bidx};
         q = seg_end;
     }
     if (__syncthreads_or(nan) && threadIdx.x == 0) flag(a.status, DSPARK_STATUS_NAN_LOGIT);
@@ -292,6 +334,10 @@ __device__ __forceinline__ void finish(const FinalArgs &a, int r, int lane, int 
 }
 
 __global__ void __launch_bounds__(kFinalWarps * 32) greedy_finalize_kernel(FinalArgs a) {
+    const int rq = blockIdx.x * kFinalWarps + (threadIdx.x >> 5);
+    const int ln = threadIdx.x & 31;
+    // drafts are step inputs: fetch them while the argmax finishes
+    const int dj = (rq < a.B && ln < a.gamma) ? __ldg(a.draft + (size_t)rq * a.gamma + ln) : -1;
     pdl_wait();
     const int rows = device_rows(a.rows_dev, a.rows_host, a.max_rows);
     const long long cpr = (a.V + a.epc - 1) / a.epc;
@@ -299,11 +345,10 @@ __global__ void __launch_bounds__(kFinalWarps * 32) greedy_finalize_kernel(Final
     const long long per = (W + a.grid - 1) / a.grid;
     write_argmax(a, rows, cpr, per);
 
-    const int lane = threadIdx.x & 31;
-    const int r = blockIdx.x * kFinalWarps + (threadIdx.x >> 5);
+    const int lane = ln;
+    const int r = rq;
     if (r >= a.B) return;  // warp-uniform
     const int g = a.gamma;
-    const int dj = lane < g ? a.draft[(size_t)r * g + lane] : -1;
     if (__any_sync(kFullMask, lane < g && (dj < 0 || dj >= a.V)) && lane == 0)
         flag(a.status, DSPARK_STATUS_TOKEN_RANGE);
     const int lo = a.cu[r], hi = a.cu[r + 1], L = hi - lo;
@@ -328,6 +373,9 @@ __global__ void __launch_bounds__(kFinalWarps * 32) greedy_finalize_kernel(Final
 
 __global__ void __launch_bounds__(kFinalWarps * 32) cap_finalize_kernel(FinalArgs a) {
     __shared__ int sums[2];
+    const int rq = blockIdx.x * kFinalWarps + (threadIdx.x >> 5);
+    const int ln = threadIdx.x & 31;
+    const int dj0 = (rq < a.B && ln < a.gamma) ? __ldg(a.draft + (size_t)rq * a.gamma + ln) : -1;
     pdl_wait();
     const int rows = a.rows_host;
     const long long cpr = (a.V + a.epc - 1) / a.epc;
@@ -337,11 +385,11 @@ __global__ void __launch_bounds__(kFinalWarps * 32) cap_finalize_kernel(FinalArg
     if (threadIdx.x == 0) sums[0] = sums[1] = 0;
     __syncthreads();
 
-    const int lane = threadIdx.x & 31;
-    const int r = blockIdx.x * kFinalWarps + (threadIdx.x >> 5);
+    const int lane = ln;
+    const int r = rq;
     const int g = a.gamma;
     if (r < a.B) {
-        const int dj = lane < g ? a.draft[(size_t)r * g + lane] : -1;
+        const int dj = dj0;
         if (__any_sync(kFullMask, lane < g && (dj < 0 || dj >= a.V)) && lane == 0)
             flag(a.status, DSPARK_STATUS_TOKEN_RANGE);
         const int base = r * (g + 1);

@@ -12,17 +12,17 @@
 //           nearest captured tier)
 //
 // One warp per request, lane j = row j of the request (gamma+1 <= 32).  Each
-// CTA covers 32 requests; it obtains the packed offset of its first request
-// from a block-wide sum of the preceding lengths (B is at most a few
-// thousand, so every CTA re-reading verify_lens is cheaper than a separate
-// scan kernel), and the packed total from the same pass, which it needs for
-// the pad rows.
+// CTA covers 8 requests; it obtains the packed offset of its first request
+// and the packed total (needed for the pad rows) from one block scan over
+// all lengths (B is at most a few thousand, so every CTA re-reading
+// verify_lens is cheaper than a separate scan kernel).  Token ids and
+// positions are fetched before waiting on the planner.
 
 #include "dspark_common.cuh"
 
 namespace dspark {
 
-constexpr int kPackThreads = 1024;
+constexpr int kPackThreads = 256;
 constexpr int kPackReqPerCta = kPackThreads / 32;
 
 struct TierArgs {
@@ -44,53 +44,60 @@ pack_kernel(const int32_t *__restrict__ anchor, const int32_t *__restrict__ draf
             TierArgs tiers, int capacity, int32_t *__restrict__ ids, int32_t *__restrict__ pos,
             int32_t *__restrict__ req, int32_t *__restrict__ src, int32_t *__restrict__ cu,
             int32_t *__restrict__ totals, int32_t *__restrict__ status) {
-    __shared__ int scan32[40];
+    __shared__ long long scan64[40];
     __shared__ int offs[kPackReqPerCta];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r0 = blockIdx.x * kPackReqPerCta;
+    const int r = r0 + warp;
 
     pdl_trigger();
-    pdl_wait();  // verify_lens may come from the planner just before
-
-    // lengths of all requests: total, and the sum before this CTA's first request
-    int tot_local = 0, pre_local = 0;
-    bool bad = false;
-    for (int r = tid; r < B; r += kPackThreads) {
-        const int L = clamp_len(lens[r], gamma, bad);
-        tot_local += L;
-        if (r < r0) pre_local += L;
+    // token ids and prefix lengths are step inputs (not written by the
+    // planner): fetch them while the planner finishes
+    int tok = 0, pre = 0;
+    if (r < B) {
+        pre = __ldg(prefix + r);
+        if (lane == 0) tok = __ldg(anchor + r);
+        else if (lane <= gamma) tok = __ldg(draft + (size_t)r * gamma + lane - 1);
     }
-    const int total = block_sum<int>(tot_local, scan32);
-    const int before = block_sum<int>(pre_local, scan32);
+    pdl_wait();  // verify_lens come from the planner
+
+    // total packed rows and the rows before this CTA's first request, in one
+    // block scan of (total << 32 | before)
+    long long both = 0;
+    bool bad = false;
+    for (int q = tid; q < B; q += kPackThreads) {
+        const long long L = clamp_len(__ldg(lens + q), gamma, bad);
+        both += (L << 32) | (q < r0 ? L : 0);
+    }
+    long long sum;
+    block_exclusive_scan<long long>(both, scan64, &sum);
+    const int total = (int)(sum >> 32), before = (int)(sum & 0xFFFFFFFFll);
     if (__syncthreads_or(bad) && tid == 0 && blockIdx.x == 0) flag(status, DSPARK_STATUS_BAD_LEN);
 
-    // offsets of this CTA's 32 requests
+    bool b2 = false;
+    const int L = r < B ? clamp_len(__ldg(lens + r), gamma, b2) : 0;
     if (warp == 0) {
-        const int r = r0 + lane;
-        bool b2 = false;
-        const int L = r < B ? clamp_len(lens[r], gamma, b2) : 0;
-        int incl = L;
+        bool b3 = false;
+        const int Lw = (r0 + lane < B && lane < kPackReqPerCta) ? clamp_len(__ldg(lens + r0 + lane), gamma, b3) : 0;
+        int incl = Lw;
 #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
+        for (int d = 1; d < kPackReqPerCta; d <<= 1) {
             const int o = __shfl_up_sync(kFullMask, incl, d);
             if (lane >= d) incl += o;
         }
-        offs[lane] = before + incl - L;
+        if (lane < kPackReqPerCta) offs[lane] = before + incl - Lw;
     }
     __syncthreads();
 
-    const int r = r0 + warp;
     bool over = false;
     if (r < B) {
-        bool b3 = false;
-        const int L = clamp_len(lens[r], gamma, b3);
         const int off = offs[warp];
         if (lane == 0) cu[r + 1] = off + L;
         if (lane < L) {
             const int dst = off + lane;
             if (dst < capacity) {
-                ids[dst] = lane == 0 ? anchor[r] : draft[(size_t)r * gamma + lane - 1];
-                pos[dst] = prefix[r] + lane;
+                ids[dst] = tok;
+                pos[dst] = pre + lane;
                 req[dst] = r;
                 src[dst] = r * (gamma + 1) + lane;
             } else {

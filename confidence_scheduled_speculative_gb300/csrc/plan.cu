@@ -46,15 +46,14 @@
 
 namespace dspark {
 
-constexpr int kSurvThreads = 256;
+constexpr int kSurvThreads = 64;  // 2 requests per CTA: spreads the fp64 sigmoids over many SMs
 constexpr int kBudgetThreads = 1024;
 constexpr int kBudgetWarps = kBudgetThreads / 32;
 constexpr int kRadixBits = 7;
 constexpr int kRadix = 1 << kRadixBits;
 constexpr int kRadixPasses = 4;             // 28 bits >= the 27-bit keys
 constexpr int kHistStride = kRadix + 1;     // pad: fewer bank conflicts in the scan
-constexpr int kMaxCandidates = 24576;       // B*gamma limit of the one-CTA planner
-constexpr int kMaxItemsPerThread = kMaxCandidates / kBudgetThreads;  // 24
+constexpr int kMaxCandidates = 16384;       // B*gamma limit of the one-CTA planner
 constexpr uint32_t kOneBits = 0x3F800000u;  // bits of 1.0f
 constexpr uint32_t kDroppedKey = 0x07FFFFFFu;
 constexpr int kMinExpBiased = 113;          // 2^-14: the smallest allowed eps
@@ -122,19 +121,25 @@ __device__ __forceinline__ long long fixed_of_key(uint32_t key) {
     return mant << (e - kMinExpBiased);
 }
 
+// inverse of fixed_of_key for a kept survival
+__device__ __forceinline__ uint32_t key_of_fixed(long long m) {
+    const float s = (float)(__ll2double_rn(m) * 0x1p-37);  // exact
+    return kOneBits - __float_as_uint(s);
+}
+
 __device__ __forceinline__ double tau_of(int B, long long P) {
     return __ll2double_rn(((long long)B << 37) + P) * 0x1p-37;  // exact
 }
 
-// Shared-memory layout of the budget kernel.
+// Shared-memory header of the budget kernel; the key and prefix arrays follow.
 struct BudgetSmem {
     uint32_t hist[kBudgetWarps * kHistStride];
     long long scan64[40];
     int scan32[40];
     double best_theta[kBudgetWarps];
     int best_b[kBudgetWarps];
-    int n_kept, budget, e_star, table_bad;
-    float v_star;
+    int budget, e_star, table_bad;
+    uint32_t key_star;
     uint32_t key_or, key_and;
 };
 
@@ -142,42 +147,47 @@ __device__ __forceinline__ bool theta_better(double ta, int ba, double tb, int b
     return ta > tb || (ta == tb && ba < bb);
 }
 
-// Stable LSD radix sort of N 28-bit keys; returns the buffer holding the
-// sorted keys (A or Bf).  Items are assigned warp-contiguously: warp w owns
-// [w*ipw, (w+1)*ipw) and handles it in rounds of 32 consecutive items, so a
-// key's rank inside its warp (earlier rounds, then lower lanes) plus the
-// (digit-major, warp-minor) histogram prefix is a stable position.
-__device__ uint32_t *radix_sort(uint32_t *A, uint32_t *Bf, int N, BudgetSmem &sm) {
+// Stable LSD radix sort of N 28-bit keys, IPT keys per thread.  Warp w owns
+// items [w*32*IPT, (w+1)*32*IPT) and ranks them in rounds of 32 consecutive
+// items, so (earlier rounds, lower lanes) before it within the warp plus the
+// (digit-major, warp-minor) histogram prefix is a stable position.  The first
+// executed pass reads `src` (left intact) and writes A; later passes
+// alternate A and Bf.  Passes whose digit is the same for every key are
+// skipped.  Returns the buffer that holds the sorted keys.
+template <int IPT>
+__device__ const uint32_t *radix_sort(const uint32_t *src, uint32_t *A, uint32_t *Bf, int N,
+                                      BudgetSmem &sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int ipt = (N + kBudgetThreads - 1) / kBudgetThreads;
-    const int ipw = ipt * 32;
     const unsigned lt = lanemask_lt();
-    uint32_t *src = A, *dst = Bf;
     const uint32_t varying = sm.key_or ^ sm.key_and;
+    uint32_t *dst = A;
+    const int base_idx = warp * 32 * IPT + lane;
     for (int pass = 0; pass < kRadixPasses; ++pass) {
         const int shift = pass * kRadixBits;
-        if (((varying >> shift) & (kRadix - 1)) == 0) continue;  // digit constant: skip
+        if (((varying >> shift) & (kRadix - 1)) == 0) continue;
         for (int i = tid; i < kBudgetWarps * kHistStride; i += kBudgetThreads) sm.hist[i] = 0;
-        __syncthreads();
-        uint32_t *h = sm.hist + warp * kHistStride;
-        int rank[kMaxItemsPerThread];
+        uint32_t key[IPT];
 #pragma unroll
-        for (int i = 0; i < kMaxItemsPerThread; ++i) {
-            if (i < ipt) {
-                const int idx = warp * ipw + i * 32 + lane;
-                const bool valid = idx < N;
-                const uint32_t d = valid ? (src[idx] >> shift) & (kRadix - 1) : 0xFFFFu;
-                const unsigned peers = __match_any_sync(kFullMask, d);
-                const uint32_t base = valid ? h[d] : 0u;
-                __syncwarp();
-                if (valid && lane == __ffs(peers) - 1) h[d] = base + __popc(peers);
-                __syncwarp();
-                rank[i] = (int)base + __popc(peers & lt);
-            }
+        for (int i = 0; i < IPT; ++i) {
+            const int idx = base_idx + i * 32;
+            key[i] = idx < N ? src[idx] : 0u;
         }
         __syncthreads();
-        // exclusive scan of the histogram in (digit, warp) order
-        {
+        uint32_t *h = sm.hist + warp * kHistStride;
+        int rank[IPT];
+#pragma unroll
+        for (int i = 0; i < IPT; ++i) {
+            const bool valid = base_idx + i * 32 < N;
+            const uint32_t d = valid ? (key[i] >> shift) & (kRadix - 1) : 0xFFFFu;
+            const unsigned peers = __match_any_sync(kFullMask, d);
+            const uint32_t base = valid ? h[d] : 0u;
+            __syncwarp();
+            if (valid && lane == __ffs(peers) - 1) h[d] = base + __popc(peers);
+            __syncwarp();
+            rank[i] = (int)base + __popc(peers & lt);
+        }
+        __syncthreads();
+        {   // exclusive scan of the histogram in (digit, warp) order
             const int d = tid >> 3, w0 = (tid & 7) * 4;
             uint32_t v[4], local = 0;
 #pragma unroll
@@ -195,84 +205,98 @@ __device__ uint32_t *radix_sort(uint32_t *A, uint32_t *Bf, int N, BudgetSmem &sm
         }
         __syncthreads();
 #pragma unroll
-        for (int i = 0; i < kMaxItemsPerThread; ++i) {
-            if (i < ipt) {
-                const int idx = warp * ipw + i * 32 + lane;
-                if (idx < N) {
-                    const uint32_t key = src[idx];
-                    const uint32_t d = (key >> shift) & (kRadix - 1);
-                    dst[h[d] + rank[i]] = key;
-                }
-            }
-        }
+        for (int i = 0; i < IPT; ++i)
+            if (base_idx + i * 32 < N) dst[h[(key[i] >> shift) & (kRadix - 1)] + rank[i]] = key[i];
         __syncthreads();
-        uint32_t *t = src;
         src = dst;
-        dst = t;
+        dst = (dst == A) ? Bf : A;
     }
     return src;
 }
 
+template <int IPT>
 __global__ void __launch_bounds__(kBudgetThreads, 1) budget_kernel(PlanArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     BudgetSmem &sm = *reinterpret_cast<BudgetSmem *>(smem_raw);
-    unsigned char *buf = smem_raw + ((sizeof(BudgetSmem) + 15) & ~size_t(15));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = a.B, G = a.gamma, N = a.N;
+    // U: unsorted keys in (depth, request) order e = k*B + r; A/Bf: sort
+    // buffers; P (prefix sums, N+1 int64) overlays A..Bf once sorted.
+    uint32_t *U = reinterpret_cast<uint32_t *>(smem_raw + ((sizeof(BudgetSmem) + 15) & ~size_t(15)));
+    const int Nu = (N + 3) & ~3;
+    uint32_t *A = U + Nu;
+    uint32_t *Bf = A + Nu;
+    long long *P = reinterpret_cast<long long *>(A);
+    const CostArgs &c = a.cost;
 
     pdl_trigger();
+    // the cost table is written before the step: fetch it while waiting
+    int Mj = 0, Mprev = 0, Mnext = 0;
+    double vj = 0.0;
+    if (tid < c.n) {
+        Mj = __ldg(c.M + tid);
+        vj = __ldg(c.val + tid);
+        if (tid > 0) Mprev = __ldg(c.M + tid - 1);
+        if (tid < c.n - 1) Mnext = __ldg(c.M + tid + 1);
+    }
     if (tid == 0) {
         sm.key_or = 0u;
         sm.key_and = 0xFFFFFFFFu;
-        sm.table_bad = 0;
     }
     pdl_wait();  // survivals come from survival_kernel
-    __syncthreads();
 
-    // (1) keys in depth-major order e = k*B + r (coalesced reads of [B, gamma])
-    uint32_t *A = reinterpret_cast<uint32_t *>(buf);
-    uint32_t *Bf = A + N;
+    // (1) keys (coalesced reads of the row-major survivals)
     int kept_local = 0;
     uint32_t kor = 0u, kand = 0xFFFFFFFFu;
-    for (int i = tid; i < N; i += kBudgetThreads) {
-        const int r = i / G, k = i - r * G;
-        const float s = a.surv[i];
-        const bool kept = (k < a.max_len - 1) && (s >= a.eps);
-        const uint32_t key = key_of(s, kept);
-        A[k * B + r] = key;
-        kept_local += kept ? 1 : 0;
-        kor |= key;
-        kand &= key;
+    {
+        float sv[IPT];
+#pragma unroll
+        for (int q = 0; q < IPT; ++q) {
+            const int i = q * kBudgetThreads + tid;
+            sv[q] = i < N ? a.surv[i] : 0.0f;
+        }
+#pragma unroll
+        for (int q = 0; q < IPT; ++q) {
+            const int i = q * kBudgetThreads + tid;
+            if (i < N) {
+                const int r = i / G, k = i - r * G;
+                const bool kept = (k < a.max_len - 1) && (sv[q] >= a.eps);
+                const uint32_t key = key_of(sv[q], kept);
+                U[k * B + r] = key;
+                kept_local += kept ? 1 : 0;
+                kor |= key;
+                kand &= key;
+            }
+        }
     }
     kor = __reduce_or_sync(kFullMask, kor);
     kand = __reduce_and_sync(kFullMask, kand);
+    __syncthreads();  // key_or / key_and initialised
     if (lane == 0) {
         atomicOr(&sm.key_or, kor);
         atomicAnd(&sm.key_and, kand);
     }
-    const int n_kept = block_sum<int>(kept_local, sm.scan32);  // contains __syncthreads
+    const int n_kept = block_sum<int>(kept_local, sm.scan32);  // syncs
 
     // (2) sort
-    const uint32_t *sorted = radix_sort(A, Bf, N, sm);
+    const uint32_t *sorted = radix_sort<IPT>(U, A, Bf, N, sm);
 
-    // (3) P[i] = sum of the i largest survivals, fixed point 2^-37 (P[0] = 0)
-    const int ipt = (N + kBudgetThreads - 1) / kBudgetThreads;
-    long long *P = reinterpret_cast<long long *>(buf);
+    // (3) P[i] = sum of the i largest survivals in units of 2^-37 (P[0] = 0)
     {
-        uint32_t kreg[kMaxItemsPerThread];
+        uint32_t kreg[IPT];
         long long local = 0;
 #pragma unroll
-        for (int i = 0; i < kMaxItemsPerThread; ++i) {
-            const int idx = tid * ipt + i;
-            kreg[i] = (i < ipt && idx < N) ? sorted[idx] : kDroppedKey;
+        for (int i = 0; i < IPT; ++i) {
+            const int idx = tid * IPT + i;
+            kreg[i] = idx < N ? sorted[idx] : kDroppedKey;
             local += fixed_of_key(kreg[i]);
         }
         long long tot;
-        long long run = block_exclusive_scan<long long>(local, sm.scan64, &tot);  // syncs: reads done
+        long long run = block_exclusive_scan<long long>(local, sm.scan64, &tot);  // reads done
 #pragma unroll
-        for (int i = 0; i < kMaxItemsPerThread; ++i) {
-            const int idx = tid * ipt + i;
-            if (i < ipt && idx < N) {
+        for (int i = 0; i < IPT; ++i) {
+            const int idx = tid * IPT + i;
+            if (idx < N) {
                 run += fixed_of_key(kreg[i]);
                 P[idx + 1] = run;
             }
@@ -281,24 +305,29 @@ __global__ void __launch_bounds__(kBudgetThreads, 1) budget_kernel(PlanArgs a) {
     }
     __syncthreads();
 
-    // (4) theta at the right end of every table entry's range of budgets
-    const CostArgs &c = a.cost;
+    // (4) theta at the last budget of every table entry's range of M = B + b
     const long long Bl = B;
     long long b_top = n_kept;  // largest in-range budget
-    if (c.kind == DSPARK_COST_ADDITIVE) b_top = min(b_top, (long long)c.M[c.n - 1] - Bl);
+    if (c.kind == DSPARK_COST_ADDITIVE) b_top = min(b_top, (long long)__ldg(c.M + c.n - 1) - Bl);
+    const double fixed_cost = __dadd_rn(c.bias, c.alpha);
     double my_theta = -INFINITY;
     int my_b = 0x7FFFFFFF;
     bool my_bad_cost = false, my_bad_table = false;
-    const double fixed_cost = __dadd_rn(c.bias, c.alpha);
     for (int j = tid; j < c.n; j += kBudgetThreads) {
-        if (j > 0 && !(c.M[j] > c.M[j - 1])) my_bad_table = true;
+        if (j >= kBudgetThreads) {
+            Mj = __ldg(c.M + j);
+            vj = __ldg(c.val + j);
+            Mprev = __ldg(c.M + j - 1);
+            Mnext = j < c.n - 1 ? __ldg(c.M + j + 1) : 0;
+        }
+        if (j > 0 && !(Mj > Mprev)) my_bad_table = true;
         long long loM, hiM;
         if (c.kind == DSPARK_COST_SPS_1D) {
-            loM = (j == 0) ? LLONG_MIN / 4 : (long long)c.M[j];
-            hiM = (j == c.n - 1) ? LLONG_MAX / 4 : (long long)c.M[j + 1] - 1;
+            loM = (j == 0) ? LLONG_MIN / 4 : (long long)Mj;
+            hiM = (j == c.n - 1) ? LLONG_MAX / 4 : (long long)Mnext - 1;
         } else {
-            loM = (j == 0) ? LLONG_MIN / 4 : (long long)c.M[j - 1] + 1;
-            hiM = (long long)c.M[j];
+            loM = (j == 0) ? LLONG_MIN / 4 : (long long)Mprev + 1;
+            hiM = (long long)Mj;
         }
         const long long blo = max(loM - Bl, 0LL);
         const long long bhi = min(hiM - Bl, b_top);
@@ -307,11 +336,10 @@ __global__ void __launch_bounds__(kBudgetThreads, 1) budget_kernel(PlanArgs a) {
         const double tau = tau_of(B, P[b]);
         double theta;
         if (c.kind == DSPARK_COST_SPS_1D) {
-            const double sps = c.val[j];
-            if (!(sps > 0.0) || !isfinite(sps)) { my_bad_cost = true; continue; }
-            theta = __dmul_rn(tau, sps);
+            if (!(vj > 0.0) || !isfinite(vj)) { my_bad_cost = true; continue; }
+            theta = __dmul_rn(tau, vj);
         } else {
-            const double Tm = __dadd_rn(fixed_cost, c.val[j]);
+            const double Tm = __dadd_rn(fixed_cost, vj);
             if (!(Tm > 0.0) || !isfinite(Tm)) { my_bad_cost = true; continue; }
             theta = __ddiv_rn(tau, Tm);
         }
@@ -320,7 +348,6 @@ __global__ void __launch_bounds__(kBudgetThreads, 1) budget_kernel(PlanArgs a) {
             my_b = b;
         }
     }
-    // block argmax (theta desc, b asc)
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) {
         const double ot = __shfl_down_sync(kFullMask, my_theta, d);
@@ -336,122 +363,119 @@ __global__ void __launch_bounds__(kBudgetThreads, 1) budget_kernel(PlanArgs a) {
     }
     const int any_bad_cost = __syncthreads_or(my_bad_cost);
     const int any_bad_table = __syncthreads_or(my_bad_table);
-    if (tid == 0) {
-        double bt = -INFINITY;
-        int bb = 0x7FFFFFFF;
-        for (int w = 0; w < kBudgetWarps; ++w)
-            if (theta_better(sm.best_theta[w], sm.best_b[w], bt, bb)) {
-                bt = sm.best_theta[w];
-                bb = sm.best_b[w];
+    if (warp == 0) {
+        double bt = sm.best_theta[lane];
+        int bb = sm.best_b[lane];
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+            const double ot = __shfl_down_sync(kFullMask, bt, d);
+            const int ob = __shfl_down_sync(kFullMask, bb, d);
+            if (theta_better(ot, ob, bt, bb)) {
+                bt = ot;
+                bb = ob;
             }
-        int st = 0;
-        if (any_bad_cost || any_bad_table) st |= DSPARK_STATUS_BAD_COST;
-        int budget;
-        double theta_out = 0.0;
-        if (a.forced < 0) {
-            if (any_bad_table || bb == 0x7FFFFFFF) {
-                budget = 0;
-                st |= DSPARK_STATUS_INFEASIBLE;
-            } else {
-                budget = bb;
-                theta_out = bt;
-            }
-        } else {
-            const long long bh = any_bad_table ? -1 : b_top;
-            if (bh < 0) {
-                budget = 0;
-                st |= DSPARK_STATUS_INFEASIBLE;
-            } else {
-                budget = (int)min((long long)a.forced, bh);
-                // theta at the forced budget: the entry that covers M = B + budget
-                const long long Mv = Bl + budget;
-                int j = -1;
-                if (c.kind == DSPARK_COST_SPS_1D) {
-                    for (int i = 0; i < c.n; ++i)
-                        if (c.M[i] <= Mv) j = i;
-                    if (j < 0) j = 0;
-                    const double sps = c.val[j];
-                    if (sps > 0.0 && isfinite(sps)) theta_out = __dmul_rn(tau_of(B, P[budget]), sps);
+        }
+        if (lane == 0) {
+            int st = (any_bad_cost || any_bad_table) ? DSPARK_STATUS_BAD_COST : 0;
+            int budget;
+            double theta_out = 0.0;
+            if (a.forced < 0) {
+                if (any_bad_table || bb == 0x7FFFFFFF) {
+                    budget = 0;
+                    st |= DSPARK_STATUS_INFEASIBLE;
                 } else {
-                    for (int i = c.n - 1; i >= 0; --i)
-                        if (c.M[i] >= Mv) j = i;
-                    if (j >= 0) {
-                        const double Tm = __dadd_rn(fixed_cost, c.val[j]);
-                        if (Tm > 0.0 && isfinite(Tm))
-                            theta_out = __ddiv_rn(tau_of(B, P[budget]), Tm);
+                    budget = bb;
+                    theta_out = bt;
+                }
+            } else {
+                const long long bh = any_bad_table ? -1 : b_top;
+                if (bh < 0) {
+                    budget = 0;
+                    st |= DSPARK_STATUS_INFEASIBLE;
+                } else {
+                    budget = (int)min((long long)a.forced, bh);
+                    // theta at the forced budget: binary search for the entry covering B + budget
+                    const long long Mv = Bl + budget;
+                    int lo = 0, hi = c.n;  // first index with M > Mv (1-D) / M >= Mv (additive)
+                    while (lo < hi) {
+                        const int mid = (lo + hi) >> 1;
+                        const long long Mm = __ldg(c.M + mid);
+                        const bool right = (c.kind == DSPARK_COST_SPS_1D) ? (Mm > Mv) : (Mm >= Mv);
+                        if (right) hi = mid;
+                        else lo = mid + 1;
+                    }
+                    if (c.kind == DSPARK_COST_SPS_1D) {
+                        const int j = lo > 0 ? lo - 1 : 0;
+                        const double sps = __ldg(c.val + j);
+                        if (sps > 0.0 && isfinite(sps)) theta_out = __dmul_rn(tau_of(B, P[budget]), sps);
+                    } else if (lo < c.n) {
+                        const double Tm = __dadd_rn(fixed_cost, __ldg(c.val + lo));
+                        if (Tm > 0.0 && isfinite(Tm)) theta_out = __ddiv_rn(tau_of(B, P[budget]), Tm);
                     }
                 }
             }
-        }
-        if (st) flag(a.status, st);
-        sm.budget = budget;
-        sm.n_kept = n_kept;
-        a.budget[0] = budget;
-        a.tau_theta[0] = tau_of(B, P[budget]);
-        a.tau_theta[1] = theta_out;
-        // the budget-th survival v* and how many candidates lie strictly above it
-        if (budget > 0) {
-            const long long mstar = P[budget] - P[budget - 1];
-            int lo = 0, hi = budget - 1;
-            while (lo < hi) {  // first index whose value equals v* (values descend)
-                const int mid = (lo + hi) >> 1;
-                if (P[mid + 1] - P[mid] > mstar) lo = mid + 1;
-                else hi = mid;
-            }
-            sm.e_star = budget - lo;  // ties to take, temporarily
-            sm.v_star = (float)(__ll2double_rn(mstar) * 0x1p-37);
-        } else {
-            sm.e_star = 0;
-            sm.v_star = INFINITY;
+            if (st) flag(a.status, st);
+            sm.budget = budget;
+            sm.key_star = budget > 0 ? key_of_fixed(P[budget] - P[budget - 1]) : 0u;
+            a.budget[0] = budget;
+            a.tau_theta[0] = tau_of(B, P[budget]);
+            a.tau_theta[1] = theta_out;
         }
     }
     __syncthreads();
 
-    // (6) the m-th tied candidate in (depth, request) order: e = k*B + r
+    // (5) ScheduleVerifyLensTopk: candidates strictly above the budget-th
+    // survival, plus the first m ties at it in (depth, request) order
     const int budget = sm.budget;
-    const float vstar = sm.v_star;
-    const int m_ties = sm.e_star;
-    __syncthreads();
+    const uint32_t kstar = sm.key_star;
+    int e_star = -1;
     if (budget > 0) {
-        int cnt = 0;
-        const int e0 = tid * ipt, e1 = min(e0 + ipt, N);
-        for (int e = e0; e < e1; ++e) {
-            const int k = e / B, r = e - k * B;
-            const float s = a.surv[(size_t)r * G + k];
-            cnt += (k < a.max_len - 1 && s >= a.eps && s == vstar) ? 1 : 0;
+        int gt = 0, tie = 0;
+#pragma unroll
+        for (int i = 0; i < IPT; ++i) {
+            const int e = tid * IPT + i;
+            const uint32_t key = e < N ? U[e] : kDroppedKey;
+            gt += key < kstar ? 1 : 0;
+            tie += key == kstar ? 1 : 0;
         }
         int total;
-        int before = block_exclusive_scan<int>(cnt, sm.scan32, &total);
-        if (before < m_ties && m_ties <= before + cnt) {
-            for (int e = e0; e < e1; ++e) {
-                const int k = e / B, r = e - k * B;
-                const float s = a.surv[(size_t)r * G + k];
-                if (k < a.max_len - 1 && s >= a.eps && s == vstar) {
-                    if (++before == m_ties) {
-                        sm.e_star = e;
-                        break;
-                    }
-                }
+        const int excl = block_exclusive_scan<int>((gt << 15) | tie, sm.scan32, &total);
+        const int m = budget - (total >> 15);  // ties to take (>= 1)
+        int before = excl & 0x7FFF;
+        if (before < m && m <= before + tie) {
+#pragma unroll
+            for (int i = 0; i < IPT; ++i) {
+                const int e = tid * IPT + i;
+                if (e < N && U[e] == kstar && ++before == m) sm.e_star = e;
             }
         }
         __syncthreads();
+        e_star = sm.e_star;
     }
-    const int e_star = sm.e_star;
+    const int kmax = min(G, a.max_len - 1);
     for (int r = tid; r < B; r += kBudgetThreads) {
         int cnt = 0;
-        if (budget > 0) {
-            for (int k = 0; k < G && k < a.max_len - 1; ++k) {
-                const float s = a.surv[(size_t)r * G + k];
-                if (!(s >= a.eps)) break;  // survivals do not increase along a request
-                if (s > vstar || (s == vstar && k * B + r <= e_star)) ++cnt;
-            }
+        for (int k = 0; k < kmax; ++k) {
+            const int e = k * B + r;
+            const uint32_t key = U[e];
+            cnt += (key < kstar || (key == kstar && e <= e_star)) ? 1 : 0;
         }
         a.verify_lens[r] = min(max(1 + cnt, a.min_len), a.max_len);
     }
 }
 
 size_t budget_smem_bytes(int N) {
-    return ((sizeof(BudgetSmem) + 15) & ~size_t(15)) + (size_t)8 * (N + 1);
+    const size_t Nu = (size_t)((N + 3) & ~3);
+    return ((sizeof(BudgetSmem) + 15) & ~size_t(15)) + 12 * Nu + 16;
+}
+
+template <int IPT>
+cudaError_t launch_budget(const PlanArgs &a, cudaStream_t s) {
+    const size_t smem = budget_smem_bytes(a.N);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(budget_kernel<IPT>),
+                                (int)budget_smem_bytes(IPT * kBudgetThreads), IPT);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(budget_kernel<IPT>, dim3(1), dim3(kBudgetThreads), smem, s, a);
 }
 
 }  // namespace dspark
@@ -508,11 +532,13 @@ extern "C" int dspark_plan(const float *conf_logits, const float *sts_temps,
     a.budget = budget;
     a.tau_theta = tau_theta;
     a.status = status;
-    const size_t smem = budget_smem_bytes(N);
-    if (ensure_smem(reinterpret_cast<const void *>(budget_kernel), (int)budget_smem_bytes(kMaxCandidates), 0) !=
-        cudaSuccess)
-        return DSPARK_ERR_CUDA;
-    if (launch_pdl(budget_kernel, dim3(1), dim3(kBudgetThreads), smem, s, a) != cudaSuccess)
-        return DSPARK_ERR_CUDA;
+    const int ipt = (N + kBudgetThreads - 1) / kBudgetThreads;
+    cudaError_t e;
+    if (ipt <= 1) e = launch_budget<1>(a, s);
+    else if (ipt <= 2) e = launch_budget<2>(a, s);
+    else if (ipt <= 4) e = launch_budget<4>(a, s);
+    else if (ipt <= 8) e = launch_budget<8>(a, s);
+    else e = launch_budget<16>(a, s);
+    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
     return DSPARK_OK;
 }

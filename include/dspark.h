@@ -104,7 +104,7 @@ typedef struct {
 } dspark_cost_table;
 
 /* Device scratch of one planner call.  Currently 0: the planner keeps its
- * whole state in one CTA's shared memory (hence B*gamma <= 24576). */
+ * whole state in one CTA's shared memory (hence B*gamma <= 16384). */
 DSPARK_API size_t dspark_plan_workspace_bytes(int32_t B, int32_t gamma);
 
 /* The verify planner.  [AVS] §一 (budget by survival, tau, theta, argmax,
@@ -124,7 +124,7 @@ DSPARK_API size_t dspark_plan_workspace_bytes(int32_t B, int32_t gamma);
  * then request id ascending; theta ties go to the smaller budget.
  * Errors: INVALID_ARG (null pointer, B < 1, min/max out of order, cost n < 1
  * or unknown kind); UNSUPPORTED (gamma > 31, B*(gamma+1) > 65536,
- * B*gamma > 24576, eps outside [2^-14, 1]); CUDA.  Device flags: BAD_INPUT,
+ * B*gamma > 16384, eps outside [2^-14, 1]); CUDA.  Device flags: BAD_INPUT,
  * BAD_COST, INFEASIBLE.  The workspace arguments are reserved (pass NULL, 0). */
 DSPARK_API int dspark_plan(const float *conf_logits, const float *sts_temps,
                 const dspark_plan_params *p /* host */, const dspark_cost_table *cost /* host */,

@@ -85,7 +85,7 @@ def test_plan_argument_checks(lib):
     assert _plan(lib, Params(**{**good, "min_len": 3, "max_len": 2}), cost) == -1
     assert _plan(lib, Params(**{**good, "max_len": 6}), cost) == -1
     assert _plan(lib, Params(**{**good, "B": 2048, "gamma": 16}), cost) == -4  # 2048*17 > 2^16
-    assert _plan(lib, Params(**{**good, "B": 1600, "gamma": 16}), cost) == -4  # > 24576 candidates
+    assert _plan(lib, Params(**{**good, "B": 1025, "gamma": 16}), cost) == -4  # > 16384 candidates
     assert _plan(lib, Params(**good), Cost(2, 3, FAKE.value, FAKE.value, 0, 0)) == -1
     assert _plan(lib, Params(**good), Cost(0, 0, FAKE.value, FAKE.value, 0, 0)) == -1
     assert _plan(lib, Params(**good), Cost(1, 3, None, FAKE.value, 0, 0)) == -1

@@ -144,12 +144,23 @@ def test_plan_edge_cases(dev, orc):
     cases.append(dict(B=4, gamma=4, z=zn, T=Tz, eps=1e-4, min_len=1, max_len=5, kind=0,
                       M=np.array([1], np.int32), val=np.array([3.0]), forced=-1, bias=0.0,
                       alpha=0.0))
-    # the largest planner (24576 candidates)
+    # the largest planner (16380 candidates, odd B)
     rng = np.random.default_rng(5)
-    cases.append(dict(B=1536, gamma=16, z=rng.normal(1, 1.5, (1536, 16)).astype(np.float32),
-                      T=np.ones(16, np.float32), eps=1e-4, min_len=1, max_len=17, kind=1,
+    cases.append(dict(B=1365, gamma=12, z=rng.normal(1, 1.5, (1365, 12)).astype(np.float32),
+                      T=np.ones(12, np.float32), eps=1e-4, min_len=1, max_len=13, kind=1,
                       M=(2 ** np.arange(10, 16)).astype(np.int32),
-                      val=0.001 * 2.0 ** np.arange(10, 16), forced=-1, bias=2.0, alpha=7.68))
+                      val=0.001 * 2.0 ** np.arange(10, 16), forced=-1, bias=2.0, alpha=6.825))
+    # a dense 1-D table with more than 1024 entries, forced budget
+    cases.append(dict(B=300, gamma=9, z=rng.normal(2, 1, (300, 9)).astype(np.float32),
+                      T=np.ones(9, np.float32), eps=1e-3, min_len=1, max_len=10, kind=0,
+                      M=np.arange(300, 300 + 2701, dtype=np.int32),
+                      val=1.0 / (2e-3 + 3e-6 * np.arange(300, 300 + 2701)), forced=1500,
+                      bias=0.0, alpha=0.0))
+    cases.append(dict(B=300, gamma=9, z=rng.normal(2, 1, (300, 9)).astype(np.float32),
+                      T=np.ones(9, np.float32), eps=1e-3, min_len=1, max_len=10, kind=0,
+                      M=np.arange(300, 300 + 2701, dtype=np.int32),
+                      val=1.0 / (2e-3 + 3e-6 * np.arange(300, 300 + 2701)), forced=-1,
+                      bias=0.0, alpha=0.0))
     for i, P in enumerate(cases):
         g = _gpu_plan(dev, P)
         ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"],
