@@ -148,8 +148,9 @@ def dspark_accept_workspace_bytes(max_rows: int, V: int) -> int:
 def dspark_plan(conf_logits, sts_temps, *, B, gamma, survival_eps, min_verify_len,
                 max_verify_len, forced_budget, cost_kind, cost_M, cost_val, bias_ms=0.0,
                 alpha_ms=0.0, survivals, verify_lens, budget, tau_theta, status,
-                workspace=None, stream=None) -> None:
-    """Planner: STS survivals -> budget -> verify_lens (all outputs on device)."""
+                workspace, stream=None) -> None:
+    """Planner: STS survivals -> budget -> verify_lens (all outputs on device).
+    ``workspace``: a device byte buffer of dspark_plan_workspace_bytes(B, gamma)."""
     params = dspark_plan_params(B, gamma, survival_eps, min_verify_len, max_verify_len,
                                 forced_budget)
     cost = dspark_cost_table(cost_kind, int(cost_M.numel()), _p(cost_M, torch.int32, "cost_M"),

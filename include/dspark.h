@@ -103,8 +103,8 @@ typedef struct {
     double alpha_ms;       /* additive only */
 } dspark_cost_table;
 
-/* Device scratch of one planner call.  Currently 0: the planner keeps its
- * whole state in one CTA's shared memory (hence B*gamma <= 16384). */
+/* Device scratch of one planner call: about 12 * B * gamma + 256 bytes
+ * (candidate ranks, the sorted survivals and a completion counter). */
 DSPARK_API size_t dspark_plan_workspace_bytes(int32_t B, int32_t gamma);
 
 /* The verify planner.  [AVS] §一 (budget by survival, tau, theta, argmax,
@@ -124,8 +124,9 @@ DSPARK_API size_t dspark_plan_workspace_bytes(int32_t B, int32_t gamma);
  * then request id ascending; theta ties go to the smaller budget.
  * Errors: INVALID_ARG (null pointer, B < 1, min/max out of order, cost n < 1
  * or unknown kind); UNSUPPORTED (gamma > 31, B*(gamma+1) > 65536,
- * B*gamma > 16384, eps outside [2^-14, 1]); CUDA.  Device flags: BAD_INPUT,
- * BAD_COST, INFEASIBLE.  The workspace arguments are reserved (pass NULL, 0). */
+ * B*gamma > 16384, eps outside [2^-14, 1]); WORKSPACE (missing, smaller than
+ * dspark_plan_workspace_bytes(B, gamma) or not 256-byte aligned); CUDA.
+ * Device flags: BAD_INPUT, BAD_COST, INFEASIBLE. */
 DSPARK_API int dspark_plan(const float *conf_logits, const float *sts_temps,
                 const dspark_plan_params *p /* host */, const dspark_cost_table *cost /* host */,
                 float *survivals, int32_t *verify_lens, int32_t *budget, double *tau_theta,

@@ -90,7 +90,15 @@ def test_plan_argument_checks(lib):
     assert _plan(lib, Params(**good), Cost(0, 0, FAKE.value, FAKE.value, 0, 0)) == -1
     assert _plan(lib, Params(**good), Cost(1, 3, None, FAKE.value, 0, 0)) == -1
     lib.dspark_plan_workspace_bytes.restype = ctypes.c_size_t
-    assert lib.dspark_plan_workspace_bytes(256, 16) == 0
+    need = lib.dspark_plan_workspace_bytes(256, 16)
+    assert need >= 12 * 256 * 16 and need % 256 == 0
+    # a missing or short planner workspace is rejected before any launch
+    f = lib.dspark_plan
+    assert f(FAKE, FAKE, ctypes.byref(Params(**good)), ctypes.byref(cost), FAKE, FAKE, FAKE,
+             FAKE, None, ctypes.c_size_t(0), FAKE, None) == -2
+    assert f(FAKE, FAKE, ctypes.byref(Params(**{**good, "B": 256, "gamma": 16, "max_len": 17})),
+             ctypes.byref(cost), FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_size_t(need - 256), FAKE,
+             None) == -2
 
 
 def test_pack_argument_checks(lib):

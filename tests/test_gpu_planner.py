@@ -91,12 +91,13 @@ def _gpu_plan(dev, P):
                verify_lens=torch.zeros(B, **i32), budget=torch.zeros(1, **i32),
                tau_theta=torch.zeros(2, dtype=torch.float64, device=dev),
                status=torch.zeros(1, **i32))
+    ws = api.workspace(api.dspark_plan_workspace_bytes(B, g), dev)
     api.dspark_plan(torch.from_numpy(P["z"]).to(dev), torch.from_numpy(P["T"]).to(dev), B=B,
                     gamma=g, survival_eps=P["eps"], min_verify_len=P["min_len"],
                     max_verify_len=P["max_len"], forced_budget=P["forced"], cost_kind=P["kind"],
                     cost_M=torch.from_numpy(P["M"]).to(dev),
                     cost_val=torch.from_numpy(P["val"]).to(dev), bias_ms=P["bias"],
-                    alpha_ms=P["alpha"], **out)
+                    alpha_ms=P["alpha"], workspace=ws, **out)
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in out.items()}
 
