@@ -60,22 +60,34 @@ constexpr uint32_t kDroppedKey = 0x07FFFFFFu;
 constexpr int kMinExpBiased = 113;          // 2^-14: the smallest allowed eps
 constexpr int kNoRank = 0x7FFFFFFF;
 
+// Cost tables with at most this many entries take the sparse path: every
+// CTA adds the survivals ranked below each candidate budget into one
+// accumulator per candidate, so no prefix scan is needed.
+constexpr int kMaxSparse = 64;
+
 // Planner scratch in the caller's workspace.
 struct PlanScratch {
-    unsigned int ticket;  // CTAs of rank_kernel done (zeroed by survival_kernel)
-    unsigned int pad[63];
-    // followed by: int32 rank[N] | int64 sorted[N] | int64 prefix[N+1]
+    unsigned int ticket;  // CTAs of rank_kernel done
+    unsigned int pad0;
+    unsigned long long acc[kMaxSparse + 1];  // sparse path: P at each candidate (+ forced budget)
+    unsigned int pad1[62];
+    // followed by: int32 rank[N] | int64 sorted[N] | int64 prefix[N+1] |
+    // int32 count[B][kMaxSparse+1] (sparse path: selected candidates of
+    // request r at each candidate budget)
 };
 
-__host__ __device__ inline size_t plan_rank_offset() { return sizeof(PlanScratch); }
+__host__ __device__ inline size_t plan_rank_offset() { return (sizeof(PlanScratch) + 255) & ~size_t(255); }
 __host__ __device__ inline size_t plan_sorted_offset(int N) {
     return plan_rank_offset() + (((size_t)N * 4 + 15) & ~size_t(15));
 }
 __host__ __device__ inline size_t plan_prefix_offset(int N) {
     return plan_sorted_offset(N) + (size_t)N * 8;
 }
-__host__ __device__ inline size_t plan_scratch_bytes(int N) {
-    return plan_prefix_offset(N) + (size_t)(N + 1) * 8;
+__host__ __device__ inline size_t plan_count_offset(int N) {
+    return (plan_prefix_offset(N) + (size_t)(N + 1) * 8 + 15) & ~size_t(15);
+}
+__host__ __device__ inline size_t plan_scratch_bytes(int B, int N) {
+    return plan_count_offset(N) + (size_t)B * (kMaxSparse + 1) * 4;
 }
 
 template <typename T>
@@ -90,10 +102,17 @@ survival_kernel(const float *__restrict__ z, const float *__restrict__ T, int B,
                 float eps, float *__restrict__ s_out, int32_t *__restrict__ status,
                 PlanScratch *__restrict__ scratch) {
     pdl_trigger();
-    if (blockIdx.x == 0 && threadIdx.x == 0) scratch->ticket = 0u;
+    if (blockIdx.x == 0) {  // reset the rank kernel's ticket and accumulators
+        for (int j = threadIdx.x; j <= kMaxSparse; j += blockDim.x) scratch->acc[j] = 0ull;
+        if (threadIdx.x == 0) scratch->ticket = 0u;
+    }
     const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (r >= B) return;  // warp-uniform
+    {   // reset this request's per-candidate counts (sparse path of rank_kernel)
+        int32_t *cnt = scratch_at<int32_t>(scratch, plan_count_offset(B * gamma)) + (size_t)r * (kMaxSparse + 1);
+        for (int j = lane; j <= kMaxSparse; j += 32) cnt[j] = 0;
+    }
     const bool active = lane < gamma;
     float c = 1.0f;
     bool bad = false;
@@ -128,6 +147,7 @@ struct CostArgs {
 struct PlanArgs {
     const float *surv;  // [B, gamma], eps-zeroed survivals
     int B, gamma, N;
+    int P2;  // gamma rounded up to a power of two (run length in shared memory)
     float eps;
     int min_len, max_len, forced;
     CostArgs cost;
@@ -163,57 +183,121 @@ __device__ __forceinline__ bool cand_better(long long ka, int ba, long long kb, 
     return ka > kb || (ka == kb && ba < bb);
 }
 
-// number of keys < key in a sorted run of length G (<= 31): 5 probes
-__device__ __forceinline__ int run_lower_bound(const uint32_t *run, int G, uint32_t key) {
+// Number of keys < key in a run of P2 keys (a power of two), padded past
+// gamma with the largest key: log2(P2) + 1 branch-free probes.
+__device__ __forceinline__ int run_lower_bound(const uint32_t *run, int P2, uint32_t key) {
     int pos = 0;
-#pragma unroll
-    for (int step = 16; step > 0; step >>= 1) {
-        const int p = pos + step;
-        if (p <= G && run[p - 1] < key) pos = p;
-    }
-    return pos;
+    for (int step = P2 >> 1; step > 0; step >>= 1) pos += (run[pos + step - 1] < key) ? step : 0;
+    return pos + ((run[pos] < key) ? 1 : 0);
 }
 
-// Shared state of the rank kernel's last CTA.
-struct FinalSmem {
+// Shared state of the rank kernel.
+struct RankSmem {
     long long scan64[40];
     int scan32[40];
     long long best_key[kRankWarps];
     int best_b[kRankWarps];
-    int budget, last;
+    int cand_b[kMaxSparse + 1];                 // candidate budget of each table entry (-1: none)
+    unsigned long long acc_s[kMaxSparse + 1];   // this CTA's part of each candidate's prefix
+    double val_s[kMaxSparse];                   // sparse path: the cost table values
+    int budget, last, n_kept, sparse;
+    long long b_top;
 };
 
-__device__ void finish_plan(const PlanArgs &a, int n_kept, FinalSmem &sm);
+__device__ void finish_plan(const PlanArgs &a, RankSmem &sm);
 
-// Keys live in shared memory request-major with an odd row stride, so the
-// 32 lanes of a warp probing 32 different runs hit 32 different banks.
-__host__ __device__ inline int run_stride(int G) { return G | 1; }
+// The range of budgets whose M = B + b uses table entry j, clipped to
+// [0, b_top]; returns its last budget, or -1 if the range is empty.
+__device__ __forceinline__ int entry_last_budget(const CostArgs &c, int j, int Mj, int Mprev,
+                                                 int Mnext, long long Bl, long long b_top) {
+    long long loM, hiM;
+    if (c.kind == DSPARK_COST_SPS_1D) {
+        loM = (j == 0) ? LLONG_MIN / 4 : (long long)Mj;
+        hiM = (j == c.n - 1) ? LLONG_MAX / 4 : (long long)Mnext - 1;
+    } else {
+        loM = (j == 0) ? LLONG_MIN / 4 : (long long)Mprev + 1;
+        hiM = (long long)Mj;
+    }
+    const long long blo = max(loM - Bl, 0LL);
+    const long long bhi = min(hiM - Bl, b_top);
+    return blo > bhi ? -1 : (int)bhi;
+}
+
+// Keys live in shared memory request-major, each run padded to P2 keys with
+// the largest key and laid out with an odd stride, so the 32 lanes of a warp
+// probing 32 different runs hit 32 different banks.
+__host__ __device__ inline int run_stride(int P2) { return P2 + 1; }
 
 __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    FinalSmem &sm = *reinterpret_cast<FinalSmem *>(smem_raw);
-    uint32_t *K = reinterpret_cast<uint32_t *>(smem_raw + ((sizeof(FinalSmem) + 15) & ~size_t(15)));
+    RankSmem &sm = *reinterpret_cast<RankSmem *>(smem_raw);
+    uint32_t *K = reinterpret_cast<uint32_t *>(smem_raw + ((sizeof(RankSmem) + 15) & ~size_t(15)));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int B = a.B, G = a.gamma, N = a.N, S = run_stride(G);
+    const int B = a.B, G = a.gamma, N = a.N, P2 = a.P2, S = run_stride(P2);
+    const CostArgs &c = a.cost;
     int32_t *rank_out = scratch_at<int32_t>(a.scratch, plan_rank_offset());
     long long *sorted = scratch_at<long long>(a.scratch, plan_sorted_offset(N));
 
     pdl_trigger();
+    // the cost table is written before the step: fetch it while waiting
+    int Mj = 0, Mprev = 0, Mnext = 0;
+    const bool sparse = c.n <= kMaxSparse;
+    double vj = 0.0;
+    if (sparse && tid < c.n) {
+        Mj = __ldg(c.M + tid);
+        Mprev = tid > 0 ? __ldg(c.M + tid - 1) : 0;
+        Mnext = tid < c.n - 1 ? __ldg(c.M + tid + 1) : 0;
+        vj = __ldg(c.val + tid);
+    }
+    const int Mlast = __ldg(c.M + c.n - 1);
     pdl_wait();  // survivals come from survival_kernel
 
-    // every CTA holds all keys: run r = K[r*S .. r*S + G)
+    // every CTA holds all keys: run r = K[r*S .. r*S + P2)
     int kept_local = 0;
-    for (int i = tid; i < N; i += kRankThreads) {
-        const float s = a.surv[i];
-        const int r = i / G;
-        const int k = i - r * G;
-        const bool kept = (k < a.max_len - 1) && (s >= a.eps);
-        K[r * S + k] = key_of(s, kept);
-        kept_local += kept ? 1 : 0;
+    for (int i0 = tid; i0 < N; i0 += 4 * kRankThreads) {
+        float sv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * kRankThreads;
+            sv[u] = i < N ? a.surv[i] : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * kRankThreads;
+            if (i < N) {
+                const int r = i / G;
+                const int k = i - r * G;
+                const bool kept = (k < a.max_len - 1) && (sv[u] >= a.eps);
+                K[r * S + k] = key_of(sv[u], kept);
+                kept_local += kept ? 1 : 0;
+            }
+        }
+    }
+    const int pad = P2 - G;
+    for (int j = tid; j < B * pad; j += kRankThreads) {
+        const int r = j / pad;
+        K[r * S + G + (j - r * pad)] = kDroppedKey;
+    }
+    const int n_kept = block_sum<int>(kept_local, sm.scan32);  // syncs
+    long long b_top = n_kept;  // largest in-range budget
+    if (c.kind == DSPARK_COST_ADDITIVE) b_top = min(b_top, (long long)Mlast - (long long)B);
+    if (sparse) {
+        if (tid < c.n) {
+            sm.cand_b[tid] = entry_last_budget(c, tid, Mj, Mprev, Mnext, B, b_top);
+            sm.val_s[tid] = vj;
+        }
+        if (tid == c.n) sm.cand_b[tid] = (a.forced >= 0 && b_top >= 0) ? (int)min((long long)a.forced, b_top) : -1;
+        if (tid <= c.n) sm.acc_s[tid] = 0ull;
+    }
+    if (tid == 0) {
+        sm.n_kept = n_kept;
+        sm.b_top = b_top;
+        sm.sparse = sparse ? 1 : 0;
     }
     __syncthreads();
 
     // ranks: one warp per candidate, lanes over the other requests' runs
+    unsigned long long my_acc[3] = {0ull, 0ull, 0ull};  // candidates lane, lane+32, lane+64
     const int nwarps = gridDim.x * kRankWarps;
     for (int x = blockIdx.x * kRankWarps + warp; x < N; x += nwarps) {
         const int r = x / G;
@@ -224,51 +308,86 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
             continue;
         }
         int cnt = 0;
-        for (int q = lane; q < B; q += 32) {
-            const uint32_t *run = K + q * S;
-            int lb = run_lower_bound(run, G, key);
-            // keys equal to this one in run q sit at depths lb, lb+1, ...;
-            // those at a smaller depth, or at the same depth of a lower
-            // request, come first (order: survival desc, depth, request)
-            const int lim = k + (q < r ? 1 : 0);
-            int c = lb;
-            for (int d = lb; d < lim && d < G && run[d] == key; ++d) ++c;
-            cnt += (q == r) ? 0 : c;
+        // four runs per lane at a time, so their probe chains overlap
+        for (int q0 = lane; q0 < B; q0 += 4 * 32) {
+            int lb[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int q = q0 + 32 * u;
+                lb[u] = q < B ? run_lower_bound(K + q * S, P2, key) : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int q = q0 + 32 * u;
+                if (q >= B || q == r) continue;
+                // keys equal to this one in run q sit at depths lb, lb+1, ...;
+                // those at a smaller depth, or at the same depth of a lower
+                // request, come first (order: survival desc, depth, request)
+                const uint32_t *run = K + q * S;
+                const int lim = k + (q < r ? 1 : 0);
+                int cq = lb[u];
+                for (int d = lb[u]; d < lim && run[d] == key; ++d) ++cq;
+                cnt += cq;
+            }
         }
 #pragma unroll
         for (int d = 16; d > 0; d >>= 1) cnt += __shfl_xor_sync(kFullMask, cnt, d);
+        const int rk = k + cnt;  // own request: exactly the k shallower depths come first
+        const long long m = fixed_of_key(key);
         if (lane == 0) {
-            const int rk = k + cnt;  // own request: exactly the k shallower depths come first
             rank_out[x] = rk;
-            sorted[rk] = fixed_of_key(key);
+            sorted[rk] = m;
+        }
+        if (sparse) {
+            int32_t *cnt_r = scratch_at<int32_t>(a.scratch, plan_count_offset(N)) + (size_t)r * (kMaxSparse + 1);
+#pragma unroll
+            for (int t = 0; t < 3; ++t) {
+                const int j = lane + 32 * t;
+                if (j <= c.n && rk < sm.cand_b[j]) {
+                    my_acc[t] += (unsigned long long)m;
+                    atomicAdd(cnt_r + j, 1);
+                }
+            }
         }
     }
+    if (sparse) {
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+            const int j = lane + 32 * t;
+            if (j <= c.n && my_acc[t] != 0ull) atomicAdd(&sm.acc_s[j], my_acc[t]);
+        }
+        __syncthreads();
+        if (tid <= c.n && sm.acc_s[tid] != 0ull) atomicAdd(&a.scratch->acc[tid], sm.acc_s[tid]);
+    }
 
-    // the last CTA to finish completes the plan
+    // the last CTA to finish completes the plan: the ranks, sorted values,
+    // counts and accumulator adds are made visible before the ticket
+    __threadfence();
     __syncthreads();
     if (tid == 0) {
-        __threadfence();
         const unsigned t = atomicAdd(&a.scratch->ticket, 1u);
         sm.last = (t == gridDim.x - 1) ? 1 : 0;
     }
     __syncthreads();
     if (!sm.last) return;
     __threadfence();
-    const int n_kept = block_sum<int>(kept_local, sm.scan32);
-    finish_plan(a, n_kept, sm);
+    finish_plan(a, sm);
 }
 
-__device__ void finish_plan(const PlanArgs &a, int n_kept, FinalSmem &sm) {
+__device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = a.B, G = a.gamma;
     const CostArgs &c = a.cost;
+    const int n_kept = sm.n_kept;
+    const long long b_top = sm.b_top;
+    const bool sparse = sm.sparse != 0;
     const int32_t *rank_in = scratch_at<int32_t>(a.scratch, plan_rank_offset());
     const long long *sorted = scratch_at<long long>(a.scratch, plan_sorted_offset(a.N));
     long long *P = scratch_at<long long>(a.scratch, plan_prefix_offset(a.N));
 
-    // (a) P[i] = sum of the i largest survivals in units of 2^-37 (P[0] = 0),
-    // a blocked scan written to the workspace
-    {
+    // (a) dense tables: P[i] = sum of the i largest survivals in units of
+    // 2^-37 (P[0] = 0), a blocked scan written to the workspace
+    if (!sparse) {
         const int per = (n_kept + kRankThreads - 1) / kRankThreads;
         const int lo = tid * per, hi = min(lo + per, n_kept);
         long long local = 0;
@@ -280,36 +399,26 @@ __device__ void finish_plan(const PlanArgs &a, int n_kept, FinalSmem &sm) {
             P[i + 1] = run;
         }
         if (tid == 0) P[0] = 0;
+        __syncthreads();
     }
-    __syncthreads();
 
     // (b) theta at the last budget of every table entry's range of M = B + b
-    const long long Bl = B;
-    long long b_top = n_kept;  // largest in-range budget
-    if (c.kind == DSPARK_COST_ADDITIVE) b_top = min(b_top, (long long)__ldg(c.M + c.n - 1) - Bl);
+    if (sparse && tid <= c.n) sm.acc_s[tid] = __ldcg(&a.scratch->acc[tid]);
+    if (sparse) __syncthreads();
     const double fixed_cost = __dadd_rn(c.bias, c.alpha);
     long long my_key = -1;
     int my_b = 0x7FFFFFFF;
     bool my_bad_cost = false, my_bad_table = false;
     for (int j = tid; j < c.n; j += kRankThreads) {
         const int Mj = __ldg(c.M + j);
-        const double vj = __ldg(c.val + j);
+        const double vj = sparse ? sm.val_s[j] : __ldg(c.val + j);
         const int Mprev = j > 0 ? __ldg(c.M + j - 1) : 0;
         const int Mnext = j < c.n - 1 ? __ldg(c.M + j + 1) : 0;
         if (j > 0 && !(Mj > Mprev)) my_bad_table = true;
-        long long loM, hiM;
-        if (c.kind == DSPARK_COST_SPS_1D) {
-            loM = (j == 0) ? LLONG_MIN / 4 : (long long)Mj;
-            hiM = (j == c.n - 1) ? LLONG_MAX / 4 : (long long)Mnext - 1;
-        } else {
-            loM = (j == 0) ? LLONG_MIN / 4 : (long long)Mprev + 1;
-            hiM = (long long)Mj;
-        }
-        const long long blo = max(loM - Bl, 0LL);
-        const long long bhi = min(hiM - Bl, b_top);
-        if (blo > bhi) continue;
-        const int b = (int)bhi;
-        const double tau = tau_of(B, __ldcg(P + b));
+        const int b = sparse ? sm.cand_b[j] : entry_last_budget(c, j, Mj, Mprev, Mnext, B, b_top);
+        if (b < 0) continue;
+        const long long Pb = sparse ? (long long)sm.acc_s[j] : __ldcg(P + b);
+        const double tau = tau_of(B, Pb);
         double theta;
         if (c.kind == DSPARK_COST_SPS_1D) {
             if (!(vj > 0.0) || !isfinite(vj)) { my_bad_cost = true; continue; }
@@ -356,6 +465,7 @@ __device__ void finish_plan(const PlanArgs &a, int n_kept, FinalSmem &sm) {
         if (lane == 0) {
             int st = (any_bad_cost || any_bad_table) ? DSPARK_STATUS_BAD_COST : 0;
             int budget;
+            long long Pbud = 0;
             double theta_out = 0.0;
             if (a.forced < 0) {
                 if (any_bad_table || bb == 0x7FFFFFFF) {
@@ -372,30 +482,59 @@ __device__ void finish_plan(const PlanArgs &a, int n_kept, FinalSmem &sm) {
                     st |= DSPARK_STATUS_INFEASIBLE;
                 } else {
                     budget = (int)min((long long)a.forced, bh);
-                    // theta at the forced budget: binary search for the entry covering B + budget
-                    const long long Mv = Bl + budget;
-                    int lo = 0, hi = c.n;  // first index with M > Mv (1-D) / M >= Mv (additive)
-                    while (lo < hi) {
-                        const int mid = (lo + hi) >> 1;
-                        const long long Mm = __ldg(c.M + mid);
-                        const bool right = (c.kind == DSPARK_COST_SPS_1D) ? (Mm > Mv) : (Mm >= Mv);
-                        if (right) hi = mid;
-                        else lo = mid + 1;
-                    }
-                    if (c.kind == DSPARK_COST_SPS_1D) {
-                        const int j = lo > 0 ? lo - 1 : 0;
-                        const double sps = __ldg(c.val + j);
-                        if (sps > 0.0 && isfinite(sps)) theta_out = __dmul_rn(tau_of(B, __ldcg(P + budget)), sps);
-                    } else if (lo < c.n) {
-                        const double Tm = __dadd_rn(fixed_cost, __ldg(c.val + lo));
-                        if (Tm > 0.0 && isfinite(Tm)) theta_out = __ddiv_rn(tau_of(B, __ldcg(P + budget)), Tm);
-                    }
+                }
+            }
+            // P at the budget: the candidate's accumulator (sparse) or the scan
+            if (budget > 0) {
+                if (!sparse) {
+                    Pbud = __ldcg(P + budget);
+                } else if (a.forced >= 0) {
+                    Pbud = (long long)sm.acc_s[c.n];
+                } else {
+                    for (int j = 0; j < c.n; ++j)
+                        if (sm.cand_b[j] == budget) {
+                            Pbud = (long long)sm.acc_s[j];
+                            break;
+                        }
+                }
+            }
+            if (a.forced >= 0 && budget == (int)min((long long)a.forced, b_top) && b_top >= 0 &&
+                !any_bad_table) {
+                // theta at the forced budget: the entry covering M = B + budget
+                const long long Mv = (long long)B + budget;
+                int lo = 0, hi = c.n;  // first index with M > Mv (1-D) / M >= Mv (additive)
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    const long long Mm = __ldg(c.M + mid);
+                    const bool right = (c.kind == DSPARK_COST_SPS_1D) ? (Mm > Mv) : (Mm >= Mv);
+                    if (right) hi = mid;
+                    else lo = mid + 1;
+                }
+                if (c.kind == DSPARK_COST_SPS_1D) {
+                    const int j = lo > 0 ? lo - 1 : 0;
+                    const double sps = __ldg(c.val + j);
+                    if (sps > 0.0 && isfinite(sps)) theta_out = __dmul_rn(tau_of(B, Pbud), sps);
+                } else if (lo < c.n) {
+                    const double Tm = __dadd_rn(fixed_cost, __ldg(c.val + lo));
+                    if (Tm > 0.0 && isfinite(Tm)) theta_out = __ddiv_rn(tau_of(B, Pbud), Tm);
                 }
             }
             if (st) flag(a.status, st);
             sm.budget = budget;
+            // sparse path: the entry whose counts hold the selection
+            int slot = -1;
+            if (sparse && budget > 0) {
+                if (a.forced >= 0) slot = c.n;
+                else
+                    for (int j = 0; j < c.n; ++j)
+                        if (sm.cand_b[j] == budget) {
+                            slot = j;
+                            break;
+                        }
+            }
+            sm.last = slot;
             a.budget[0] = budget;
-            a.tau_theta[0] = tau_of(B, __ldcg(P + budget));
+            a.tau_theta[0] = tau_of(B, Pbud);
             a.tau_theta[1] = theta_out;
         }
     }
@@ -403,17 +542,39 @@ __device__ void finish_plan(const PlanArgs &a, int n_kept, FinalSmem &sm) {
 
     // (d) a request's selected candidates are its ranks below the budget
     const int budget = sm.budget;
+    const int slot = sm.last;
     const int kmax = min(G, a.max_len - 1);
+    const int32_t *counts = scratch_at<int32_t>(a.scratch, plan_count_offset(a.N));
     for (int r = tid; r < B; r += kRankThreads) {
         int cnt = 0;
+        if (sparse) {
+            cnt = slot >= 0 ? __ldcg(counts + (size_t)r * (kMaxSparse + 1) + slot) : 0;
+        } else {
 #pragma unroll 8
-        for (int k = 0; k < kmax; ++k) cnt += __ldcg(rank_in + r * G + k) < budget ? 1 : 0;
+            for (int k = 0; k < kmax; ++k) cnt += __ldcg(rank_in + r * G + k) < budget ? 1 : 0;
+        }
         a.verify_lens[r] = min(max(1 + cnt, a.min_len), a.max_len);
     }
 }
 
-size_t rank_smem_bytes(int B, int G) {
-    return ((sizeof(FinalSmem) + 15) & ~size_t(15)) + (size_t)4 * B * run_stride(G);
+size_t rank_smem_bytes(int B, int P2) {
+    return ((sizeof(RankSmem) + 15) & ~size_t(15)) + (size_t)4 * B * run_stride(P2);
+}
+
+int pow2_at_least(int g) {
+    int p = 1;
+    while (p < g) p <<= 1;
+    return p;
+}
+
+// largest shared-memory request over every (B, gamma) with B*gamma <= kMaxCandidates
+size_t rank_smem_max() {
+    size_t m = 0;
+    for (int g = 1; g <= 31; ++g) {
+        const size_t v = rank_smem_bytes(kMaxCandidates / g, pow2_at_least(g));
+        m = v > m ? v : m;
+    }
+    return m;
 }
 
 }  // namespace dspark
@@ -422,7 +583,7 @@ using namespace dspark;
 
 extern "C" size_t dspark_plan_workspace_bytes(int32_t B, int32_t gamma) {
     if (B < 1 || gamma < 1) return 256;
-    return (plan_scratch_bytes(B * gamma) + 255) & ~size_t(255);
+    return (plan_scratch_bytes(B, B * gamma) + 255) & ~size_t(255);
 }
 
 extern "C" int dspark_plan(const float *conf_logits, const float *sts_temps,
@@ -472,9 +633,9 @@ extern "C" int dspark_plan(const float *conf_logits, const float *sts_temps,
     a.tau_theta = tau_theta;
     a.status = status;
     a.scratch = scratch;
-    const size_t smem = rank_smem_bytes(B, G);
-    if (ensure_smem(reinterpret_cast<const void *>(rank_kernel), (int)rank_smem_bytes(kMaxCandidates / 2, 2), 0) !=
-        cudaSuccess)
+    a.P2 = pow2_at_least(G);
+    const size_t smem = rank_smem_bytes(B, a.P2);
+    if (ensure_smem(reinterpret_cast<const void *>(rank_kernel), (int)rank_smem_max(), 0) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     // about one warp per candidate, at most one CTA per SM
     int grid = (N + kRankWarps - 1) / kRankWarps;
