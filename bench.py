@@ -71,15 +71,23 @@ def load_peaks():
 
 
 def ncu_traffic(workload: str):
-    """Per-launch DRAM bytes of the accept kernel from the committed ncu
-    summary, if one was taken for the current kernel."""
+    """Per-launch DRAM bytes (read + write) of the accept kernel from the
+    committed ncu summary, or None when no capture exists for this workload
+    or the kernel sources changed since it was taken."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            d = json.load(f)
-        return d.get(workload)
+            d = json.load(f).get(workload)
     except (OSError, ValueError):
         return None
+    if not d:
+        return None
+    h = hashlib.sha256()
+    for rel in ("csrc/accept.cu", "csrc/dspark_common.cuh"):
+        with open(os.path.join(ROOT, "confidence_scheduled_speculative_gb300", rel), "rb") as f:
+            h.update(f.read())
+    return d["bytes_per_launch"] if h.hexdigest() == d.get("sources_sha256") else None
 
 
 class ClockSampler:
