@@ -78,6 +78,9 @@ _SIGS = {
                                             _VP]),
     "dspark_cap_accept": (ctypes.c_int, [_VP, _I32, _I64, _I32, _VP, _VP, _VP, _I32, _I32, _VP,
                                          _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
+    "dspark_greedy_accept_static": (ctypes.c_int, [_VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP,
+                                                   _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                                   _VP]),
 }
 
 
@@ -235,3 +238,25 @@ def workspace(nbytes: int, device=None) -> torch.Tensor:
     """A device byte buffer usable as a workspace (256-byte aligned by the
     caching allocator)."""
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+STATIC_MAX_ROWS = 32768
+
+
+def dspark_greedy_accept_static(logits, *, V, cu_seqlens, draft, prefix_lens, B, gamma,
+                                num_accepted, bonus, commit_lens, out_tokens, status,
+                                argmax=None, new_seq_lens=None, max_rows=None,
+                                stream=None) -> None:
+    """dspark_greedy_accept for callers that cannot allocate device memory:
+    the scratch is a library-owned device array (at most STATIC_MAX_ROWS
+    rows).  Calls that overlap on the GPU race on that array."""
+    ptr, ld = _logits_ptr(logits, V)
+    max_rows = logits.size(0) if max_rows is None else max_rows
+    rc = load().dspark_greedy_accept_static(
+        ptr, _dtype_code(logits), ld, V, max_rows, _p(cu_seqlens, torch.int32, "cu_seqlens"),
+        _p(draft, torch.int32, "draft"), _p(prefix_lens, torch.int32, "prefix_lens"), B, gamma,
+        _p(argmax, torch.int32, "argmax"), _p(num_accepted, torch.int32, "num_accepted"),
+        _p(bonus, torch.int32, "bonus"), _p(commit_lens, torch.int32, "commit_lens"),
+        _p(new_seq_lens, torch.int32, "new_seq_lens"), _p(out_tokens, torch.int32, "out_tokens"),
+        _p(status, torch.int32, "status"), _stream(stream))
+    _check("dspark_greedy_accept_static", rc)

@@ -37,6 +37,8 @@
 
 #include "dspark_common.cuh"
 
+#include <atomic>
+
 #include <cuda_bf16.h>
 
 namespace dspark {
@@ -543,4 +545,103 @@ extern "C" int dspark_cap_accept(const void *logits, int32_t dtype, int64_t ld, 
     f.status = status;
     return run_accept(logits, dtype, ld, V, rows, rows, nullptr, f, true, workspace,
                       workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------- allocation-free variant
+//
+// dspark_greedy_accept_static: the same compact-mode greedy accept, for
+// callers that cannot allocate device memory -- for example code running
+// inside a captured or replayed graph whose allocator is frozen, an embedding
+// that only hands over tensors it owns, or a runtime that forbids cudaMalloc
+// after start-up.  Its scratch (the per-CTA partials of the argmax) lives in
+// the file-scope array below instead of a caller workspace.  Every GPU that
+// loads this library holds the array (about 300 KB) until the process exits.
+
+namespace dspark {
+
+constexpr int kStaticMaxRows = 32768;  // largest max_rows the static scratch serves
+
+static __device__ __align__(256) Partial g_static_partials[kMaxCtas + kStaticMaxRows + 1];
+
+namespace {
+constexpr int kMaxStaticDevices = 64;
+std::atomic<Partial *> g_static_ptr[kMaxStaticDevices];
+}  // namespace
+
+// Device address of g_static_partials on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is taken
+// once per device with cudaGetSymbolAddress (which also loads this module
+// on that device).
+static cudaError_t static_partials(Partial **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxStaticDevices) return cudaErrorInvalidDevice;
+    Partial *p = g_static_ptr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_static_partials);
+        if (e != cudaSuccess) return e;
+        g_static_ptr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return cudaSuccess;
+}
+
+}  // namespace dspark
+
+extern "C" int dspark_greedy_accept_static(const void *logits, int32_t dtype, int64_t ld,
+                                           int32_t V, int32_t max_rows,
+                                           const int32_t *cu_seqlens, const int32_t *draft,
+                                           const int32_t *prefix_lens, int32_t B, int32_t gamma,
+                                           int32_t *argmax, int32_t *num_accepted,
+                                           int32_t *bonus, int32_t *commit_lens,
+                                           int32_t *new_seq_lens, int32_t *out_tokens,
+                                           int32_t *status, void *stream) {
+    int rc = check_common(logits, dtype, ld, V, draft, prefix_lens, B, gamma, num_accepted, bonus,
+                          commit_lens, new_seq_lens, out_tokens, status);
+    if (rc != DSPARK_OK) return rc;
+    if (!cu_seqlens || max_rows < 0) return DSPARK_ERR_INVALID_ARG;
+    if (max_rows > kStaticMaxRows) return DSPARK_ERR_UNSUPPORTED;
+    Partial *partial = nullptr;
+    if (static_partials(&partial) != cudaSuccess) return DSPARK_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t esize = dtype == DSPARK_DTYPE_BF16 ? 2 : 4;
+    const bool vec = aligned(logits, 16) && ((ld * (long long)esize) % 16 == 0);
+    const int grid = argmax_grid();
+    ArgmaxArgs a;
+    a.logits = logits;
+    a.ld = ld;
+    a.V = V;
+    a.rows_host = 0;
+    a.rows_dev = cu_seqlens + B;
+    a.max_rows = max_rows;
+    a.partial = partial;  // every slot the finalize reads is written first: no clearing needed
+    a.status = status;
+    a.zero_totals = nullptr;
+    cudaError_t e = dtype == DSPARK_DTYPE_BF16 ? launch_argmax<__nv_bfloat16>(a, vec, grid, s)
+                                               : launch_argmax<float>(a, vec, grid, s);
+    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+    FinalArgs f = {};
+    f.rows_host = 0;
+    f.rows_dev = cu_seqlens + B;
+    f.max_rows = max_rows;
+    f.V = V;
+    f.epc = vec ? (int)(16 / esize) : 1;
+    f.grid = grid;
+    f.partial = partial;
+    f.cu = cu_seqlens;
+    f.draft = draft;
+    f.prefix = prefix_lens;
+    f.B = B;
+    f.gamma = gamma;
+    f.argmax = argmax;
+    f.num_acc = num_accepted;
+    f.bonus = bonus;
+    f.commit = commit_lens;
+    f.new_seq = new_seq_lens;
+    f.out = out_tokens;
+    f.status = status;
+    const int fgrid = (B + kFinalWarps - 1) / kFinalWarps;
+    e = launch_pdl(greedy_finalize_kernel, dim3(fgrid), dim3(kFinalWarps * 32), 0, s, f);
+    return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }

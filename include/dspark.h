@@ -224,6 +224,35 @@ DSPARK_API int dspark_cap_accept(const void *logits, int32_t dtype, int64_t ld, 
                       int32_t *totals, void *workspace, size_t workspace_bytes,
                       int32_t *status, void *stream);
 
+/* ------------------------------------------------ allocation-free accept */
+
+#define DSPARK_STATIC_MAX_ROWS 32768
+
+/* dspark_greedy_accept without a workspace.  The pages have no counterpart:
+ * this exists for callers that cannot allocate device memory (code running
+ * while a graph's memory is frozen, embeddings that only pass in buffers they
+ * own, runtimes that forbid cudaMalloc after start-up).
+ *   Arguments, outputs and device flags are those of dspark_greedy_accept,
+ *   minus workspace / workspace_bytes.
+ *   Scratch: a file-scope device array of (4096 + 32768 + 1) * 8 bytes
+ *   (~300 KB) that every GPU loading this library holds until the process
+ *   exits.  max_rows may be at most DSPARK_STATIC_MAX_ROWS (else
+ *   DSPARK_ERR_UNSUPPORTED, nothing enqueued).
+ *   The first call on a device looks up the array's device address with
+ *   cudaGetSymbolAddress (and so loads the module on that device); make that
+ *   first call on each device before any stream capture.
+ *   Every call shares the one array: calls whose kernels may overlap on the
+ *   GPU (different streams without ordering) race on it.  The array keeps the
+ *   last call's contents; nothing in it needs clearing, because every slot a
+ *   call reads is written earlier in the same call.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+DSPARK_API int dspark_greedy_accept_static(const void *logits, int32_t dtype, int64_t ld, int32_t V,
+                         int32_t max_rows, const int32_t *cu_seqlens, const int32_t *draft,
+                         const int32_t *prefix_lens, int32_t B, int32_t gamma, int32_t *argmax,
+                         int32_t *num_accepted, int32_t *bonus, int32_t *commit_lens,
+                         int32_t *new_seq_lens, int32_t *out_tokens, int32_t *status,
+                         void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -144,3 +144,12 @@ def test_accept_argument_checks(lib):
     c.restype = ctypes.c_int
     assert c(FAKE, 0, ctypes.c_int64(1024), 1000, FAKE, FAKE, FAKE, 4, 4, None, FAKE, FAKE,
              FAKE, None, FAKE, None, FAKE, FAKE, ctypes.c_size_t(need), FAKE, None) == -1
+
+
+def test_static_accept_rejects_rows_beyond_its_maximum(lib):
+    f = lib.dspark_greedy_accept_static
+    f.restype = ctypes.c_int
+    assert f(FAKE, 0, ctypes.c_int64(1024), 1000, 32769, FAKE, FAKE, FAKE, 4, 4, None, FAKE, FAKE,
+             FAKE, None, FAKE, FAKE, None) == -4
+    assert f(FAKE, 0, ctypes.c_int64(1024), 1000, -1, FAKE, FAKE, FAKE, 4, 4, None, FAKE, FAKE,
+             FAKE, None, FAKE, FAKE, None) == -1
