@@ -235,9 +235,11 @@ def dspark_cap_accept(logits, *, V, verify_lens, draft, prefix_lens, B, gamma, n
 
 
 def workspace(nbytes: int, device=None) -> torch.Tensor:
-    """A device byte buffer usable as a workspace (256-byte aligned by the
-    caching allocator)."""
-    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+    """A zero-filled device byte buffer usable as a workspace (256-byte
+    aligned by the caching allocator).  The planner's workspace must start
+    out zero; the accept workspaces need not, but zeroing is done once, at
+    allocation, off the step."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
 
 
 STATIC_MAX_ROWS = 32768

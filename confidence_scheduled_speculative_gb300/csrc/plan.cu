@@ -65,16 +65,28 @@ constexpr int kNoRank = 0x7FFFFFFF;
 // accumulator per candidate, so no prefix scan is needed.
 constexpr int kMaxSparse = 64;
 
+// The select path ranks candidates inside the top-11-bit bins of their keys:
+// survival_kernel counts the kept keys (and adds their fixed-point
+// survivals) per bin, select_kernel reads and clears the bins.
+constexpr int kHistShift = 16;               // bin = key >> 16 of a 27-bit key
+constexpr int kHistBins = 2048;              // kept keys use bins 0..1792
+
 // Planner scratch in the caller's workspace.
 struct PlanScratch {
     unsigned int ticket;  // CTAs of rank_kernel done
     unsigned int pad0;
     unsigned long long acc[kMaxSparse + 1];  // sparse path: P at each candidate (+ forced budget)
-    unsigned int pad1[62];
+    unsigned int pad1[124];
+    // select path: kept keys per top bin and their fixed-point survival sums;
+    // zero between calls (select_kernel clears what survival_kernel added)
+    unsigned int hcount[kHistBins];
+    unsigned long long hsum[kHistBins];
     // followed by: int32 rank[N] | int64 sorted[N] | int64 prefix[N+1] |
     // int32 count[B][kMaxSparse+1] (sparse path: selected candidates of
     // request r at each candidate budget)
 };
+static_assert(offsetof(PlanScratch, hcount) % 16 == 0 && offsetof(PlanScratch, hsum) % 16 == 0,
+              "histogram rows are read as 16-byte vectors");
 
 __host__ __device__ inline size_t plan_rank_offset() { return (sizeof(PlanScratch) + 255) & ~size_t(255); }
 __host__ __device__ inline size_t plan_sorted_offset(int N) {
@@ -95,12 +107,27 @@ __device__ __forceinline__ T *scratch_at(PlanScratch *sc, size_t off) {
     return reinterpret_cast<T *>(reinterpret_cast<unsigned char *>(sc) + off);
 }
 
+// Keys order the candidates: a kept survival s in [2^-14, 1] maps to
+// bits(1.0f) - bits(s), a 27-bit integer that grows as s shrinks; dropped
+// candidates map to the largest 27-bit value.
+__device__ __forceinline__ uint32_t key_of(float s, bool kept) {
+    return kept ? (kOneBits - __float_as_uint(s)) : kDroppedKey;
+}
+
+// survival of a kept key as an exact multiple of 2^-37
+__device__ __forceinline__ long long fixed_of_key(uint32_t key) {
+    const uint32_t bits = kOneBits - key;
+    const uint32_t e = bits >> 23;
+    const long long mant = (long long)((bits & 0x7FFFFFu) | 0x800000u);
+    return mant << (e - kMinExpBiased);
+}
+
 // ------------------------------------------------------------- survival
 
 __global__ void __launch_bounds__(kSurvThreads)
 survival_kernel(const float *__restrict__ z, const float *__restrict__ T, int B, int gamma,
-                float eps, float *__restrict__ s_out, int32_t *__restrict__ status,
-                PlanScratch *__restrict__ scratch) {
+                float eps, int kmax, bool bin_keys, float *__restrict__ s_out,
+                int32_t *__restrict__ status, PlanScratch *__restrict__ scratch) {
     pdl_trigger();
     if (blockIdx.x == 0) {  // reset the rank kernel's ticket and accumulators
         for (int j = threadIdx.x; j <= kMaxSparse; j += blockDim.x) scratch->acc[j] = 0ull;
@@ -133,6 +160,11 @@ survival_kernel(const float *__restrict__ z, const float *__restrict__ T, int B,
     }
     if (active) s_out[(size_t)r * gamma + lane] = (s >= eps) ? s : 0.0f;
     if (__any_sync(kFullMask, bad) && lane == 0) flag(status, DSPARK_STATUS_BAD_INPUT);
+    if (bin_keys && active && lane < kmax && s >= eps) {  // select path: bin the kept key
+        const uint32_t key = key_of(s, true);
+        atomicAdd(&scratch->hcount[key >> kHistShift], 1u);
+        atomicAdd(&scratch->hsum[key >> kHistShift], (unsigned long long)fixed_of_key(key));
+    }
 }
 
 // ---------------------------------------------------------------- rank
@@ -156,18 +188,6 @@ struct PlanArgs {
     int32_t *status;
     PlanScratch *scratch;
 };
-
-__device__ __forceinline__ uint32_t key_of(float s, bool kept) {
-    return kept ? (kOneBits - __float_as_uint(s)) : kDroppedKey;
-}
-
-// survival of a kept key as an exact multiple of 2^-37
-__device__ __forceinline__ long long fixed_of_key(uint32_t key) {
-    const uint32_t bits = kOneBits - key;
-    const uint32_t e = bits >> 23;
-    const long long mant = (long long)((bits & 0x7FFFFFu) | 0x800000u);
-    return mant << (e - kMinExpBiased);
-}
 
 // tau = (B * 2^37 + P) * 2^-37 as an fp64 built with integer operations:
 // the value is below 2^53 units, so it is exactly representable.
@@ -577,6 +597,557 @@ size_t rank_smem_max() {
     return m;
 }
 
+// ------------------------------------------------------------- select
+//
+// Cost tables with at most kMaxSelect entries (the graph-tier tables) need
+// tau only at a handful of candidate budgets b_j (the last budget of each
+// entry's range, and the forced budget), so one CTA finds, for every b_j at
+// once, the b_j-th candidate of the global order and the fixed-point sum of
+// the survivals up to it:
+//   (1) survival_kernel has counted the kept keys per top-11-bit bin; a
+//       block scan of the 2048 bins and a 32-way search per candidate give
+//       the bin holding its threshold and its rank inside that bin;
+//   (2) inside the bins, candidates order by the composite C = key*2^14 + e
+//       with e = k*B + r (depth-major position: key ascending is survival
+//       descending, then depth, then request), unique per candidate.  The
+//       candidates of the marked bins are gathered; when they are few, each
+//       one's rank among them is counted directly, otherwise four radix
+//       passes over C's low 30 bits (8, 8, 7, 7 bits) find each threshold;
+//   (3) theta at every candidate and the budget, as in rank_kernel;
+//   (4) a request's survivals never increase with depth, so its C grows with
+//       depth and its selected candidates are those up to its first C above
+//       C*: the thread holding that position writes the verify length.
+// Each thread holds IPT consecutive candidates of the request-major order.
+
+constexpr int kMaxSelect = 16;
+constexpr int kSelSlots = kMaxSelect + 1;  // table entries + the forced budget
+constexpr int kSelThreads = 1024;
+constexpr int kRadixBins = 256;
+constexpr int kGather = 512;  // gathered candidates ranked by counting
+constexpr unsigned long long kNoComposite = ~0ull;
+
+struct SelSmem {
+    unsigned int cum[kHistBins];                       // inclusive key counts by top bin
+    unsigned long long csum[kHistBins];                // fixed-point sums of the bins before
+    unsigned int H[2][kSelSlots][kRadixBins];          // radix pass counts (two buffers)
+    unsigned long long part[kSelSlots][32];            // per-warp partial sums (radix path)
+    unsigned long long LC[kGather], LF[kGather];       // gathered composites and survivals
+    unsigned long long SC[kGather], SF[kGather];       // the same in composite order
+    unsigned int binmask[kHistBins / 32];              // top bins holding some threshold
+    uint32_t lastkey[kSelThreads];                     // last key of each thread's candidates
+    unsigned int wc[32];
+    unsigned long long ws[32];
+    unsigned long long prefix[kSelSlots];  // high bits of C*_j fixed so far (radix path)
+    unsigned long long psum[kSelSlots];    // fixed-point survivals before the current prefix
+    unsigned long long P[kSelSlots];       // fixed-point sum of the b_j largest survivals
+    unsigned long long cthr[kSelSlots];    // C*_j
+    int cand_b[kSelSlots];                 // candidate budget (-1: entry unused)
+    int rem[kSelSlots];                    // rank still to find under the prefix (1-based)
+    int dbin[kSelSlots];                   // top bin holding C*_j
+    int hcnt[kSelSlots];                   // candidates in that bin
+    double val_s[kMaxSelect];
+    double div_s[kMaxSelect];              // theta divisor T of entry j (additive tables)
+    int ok_s[kMaxSelect];                  // entry j's SPS or T is a positive finite number
+    int32_t M_s[kMaxSelect];
+    int n_gather, bad_table;
+    unsigned long long cstar;  // C* of the chosen budget (kNoComposite: none)
+};
+
+__device__ __forceinline__ unsigned long long composite(uint32_t key, int e) {
+    return ((unsigned long long)key << 14) | (unsigned)e;
+}
+
+__device__ __forceinline__ void zero_rows(unsigned int (*H)[kRadixBins], int rows) {
+    uint4 *h = reinterpret_cast<uint4 *>(&H[0][0]);
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < rows * kRadixBins / 4; i += kSelThreads) h[i] = z;
+}
+
+// Four radix passes over the low 30 bits of C for every active slot (rem >=
+// 1, prefix = its top bin), then the fixed-point survivals of its bin below
+// C*_j; leaves P[j] and cthr[j].  Used when many candidates share the marked
+// bins.  Only 32-bit shared atomics: equal digits are common here (ties), and
+// same-address 64-bit shared additions serialise badly.
+template <int IPT>
+__device__ void radix_thresholds(const PlanArgs &a, SelSmem &sm, const uint32_t (&key)[IPT],
+                                 int r0, int k0, int nc) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = a.B, G = a.gamma;
+    zero_rows(sm.H[0], nc);
+    if (warp < nc && lane == 0) sm.prefix[warp] = (unsigned long long)sm.dbin[warp];
+    __syncthreads();
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+        const int sh = pass == 0 ? 22 : pass == 1 ? 14 : pass == 2 ? 7 : 0;
+        const int w = pass < 2 ? 8 : 7;
+        const int cur = pass & 1;
+        // the histogram row of slot `warp`: the first active slot with its prefix
+        int myrow = -1;
+        if (warp < nc && sm.rem[warp] >= 1) {
+            const unsigned long long pw = sm.prefix[warp];
+            for (int j = 0; j <= warp; ++j)
+                if (sm.rem[j] >= 1 && sm.prefix[j] == pw) {
+                    myrow = j;
+                    break;
+                }
+        }
+        {   // this thread's candidates in order; equal (row, digit) runs add at once
+            int run_row = -1;
+            unsigned run_d = 0u, run_c = 0u;
+            int r = r0, k = k0;
+#pragma unroll
+            for (int u = 0; u < IPT; ++u) {
+                const uint32_t kk = key[u];
+                const uint32_t bin = kk >> kHistShift;
+                if (kk != kDroppedKey && ((sm.binmask[bin >> 5] >> (bin & 31)) & 1u)) {
+                    const unsigned long long C = composite(kk, k * B + r);
+                    const unsigned long long hi = C >> (sh + w);
+                    int row = -1;
+                    for (int j = 0; j < nc; ++j)
+                        if (sm.rem[j] >= 1 && sm.prefix[j] == hi) {
+                            row = j;
+                            break;
+                        }
+                    if (row >= 0) {
+                        const unsigned dg = (unsigned)(C >> sh) & ((1u << w) - 1u);
+                        if (row == run_row && dg == run_d) {
+                            ++run_c;
+                        } else {
+                            if (run_row >= 0) atomicAdd(&sm.H[cur][run_row][run_d], run_c);
+                            run_row = row;
+                            run_d = dg;
+                            run_c = 1u;
+                        }
+                    }
+                }
+                if (++k == G) {
+                    k = 0;
+                    ++r;
+                }
+            }
+            if (run_row >= 0) atomicAdd(&sm.H[cur][run_row][run_d], run_c);
+        }
+        __syncthreads();
+        // warp j: the digit where the running count reaches rem_j.  Meanwhile
+        // the other buffer is cleared.
+        if (myrow >= 0) {
+            const int per = (1 << w) / 32;
+            const unsigned *hc = sm.H[cur][myrow];
+            unsigned local = 0u;
+            for (int q = 0; q < per; ++q) local += hc[lane * per + q];
+            unsigned incl = local;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const unsigned o = __shfl_up_sync(kFullMask, incl, d);
+                if (lane >= d) incl += o;
+            }
+            const int want = sm.rem[warp];
+            const int fl = __ffs(__ballot_sync(kFullMask, (int)incl >= want)) - 1;
+            if (lane == fl) {
+                int run = (int)(incl - local);
+                int dg = lane * per;
+                for (int q = 0; q < per; ++q) {
+                    const int cnt = (int)hc[lane * per + q];
+                    if (run + cnt >= want) {
+                        dg = lane * per + q;
+                        break;
+                    }
+                    run += cnt;
+                }
+                sm.prefix[warp] = (sm.prefix[warp] << w) | (unsigned long long)dg;
+                sm.rem[warp] = want - run;
+            }
+        }
+        if (pass < 3) zero_rows(sm.H[cur ^ 1], nc);
+        __syncthreads();
+    }
+    // the prefix is now C*_j; add the survivals of its bin below it: per-warp
+    // partial sums, then warp j adds its 32 partials
+    for (int j = 0; j < nc; ++j) {
+        if (sm.cand_b[j] < 1) continue;  // uniform
+        const unsigned long long cj = sm.prefix[j];
+        const uint32_t dj = (uint32_t)sm.dbin[j];
+        unsigned long long acc = 0ull;
+        int r = r0, k = k0;
+#pragma unroll
+        for (int u = 0; u < IPT; ++u) {
+            const uint32_t kk = key[u];
+            if (kk != kDroppedKey && (kk >> kHistShift) == dj && composite(kk, k * B + r) < cj)
+                acc += (unsigned long long)fixed_of_key(kk);
+            if (++k == G) {
+                k = 0;
+                ++r;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFullMask, acc, o);
+        if (lane == 0) sm.part[j][warp] = acc;
+    }
+    __syncthreads();
+    if (warp < nc && sm.cand_b[warp] >= 1) {
+        unsigned long long acc = sm.part[warp][lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFullMask, acc, o);
+        if (lane == 0) {
+            sm.cthr[warp] = sm.prefix[warp];
+            sm.P[warp] = sm.psum[warp] + acc +
+                         (unsigned long long)fixed_of_key((uint32_t)(sm.prefix[warp] >> 14));
+        }
+    }
+}
+
+template <int IPT>
+__global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    SelSmem &sm = *reinterpret_cast<SelSmem *>(smem_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = a.B, G = a.gamma, N = a.N;
+    const int kmax = a.max_len - 1;
+    const CostArgs &c = a.cost;
+    const int nc = c.n + 1;
+    const int i0 = tid * IPT;
+    const int r0 = i0 / G, k0 = i0 - r0 * G;  // request and depth of this thread's first candidate
+
+    pdl_trigger();
+    // while the survivals are computed: warp j fetches cost entry j (for its
+    // budget range); warp 0 fetches entry `lane` and prepares its theta
+    // divisor, so that only the product or quotient is left for later
+    int Mj = 0, Mprev = 0, Mnext = 0;
+    if (warp < c.n) {
+        Mj = __ldg(c.M + warp);
+        Mprev = warp > 0 ? __ldg(c.M + warp - 1) : 0;
+        Mnext = warp < c.n - 1 ? __ldg(c.M + warp + 1) : 0;
+    }
+    const int Mlast = __ldg(c.M + c.n - 1);
+    if (warp == 0) {
+        bool bad_entry = false;
+        if (lane < c.n) {
+            const int m = __ldg(c.M + lane);
+            const double v = __ldg(c.val + lane);
+            bad_entry = lane > 0 && !(m > __ldg(c.M + lane - 1));
+            double Tm = 0.0;
+            bool ok;
+            if (c.kind == DSPARK_COST_SPS_1D) {
+                ok = v > 0.0 && isfinite(v);
+            } else {
+                Tm = __dadd_rn(__dadd_rn(c.bias, c.alpha), v);
+                ok = Tm > 0.0 && isfinite(Tm);
+            }
+            sm.val_s[lane] = v;
+            sm.div_s[lane] = Tm;
+            sm.ok_s[lane] = ok ? 1 : 0;
+            sm.M_s[lane] = m;
+        }
+        const bool bt = __any_sync(kFullMask, bad_entry);
+        if (lane == 0) sm.bad_table = bt ? 1 : 0;
+    }
+    if (tid < kHistBins / 32) sm.binmask[tid] = 0u;
+    if (tid == 0) sm.n_gather = 0;
+    pdl_wait();  // survivals and bins come from survival_kernel
+
+    // (1) this thread's two bins, cleared for the next call; its keys
+    unsigned int h0, h1;
+    unsigned long long s0, s1;
+    {
+        uint2 *hc = reinterpret_cast<uint2 *>(a.scratch->hcount) + tid;
+        ulonglong2 *hs = reinterpret_cast<ulonglong2 *>(a.scratch->hsum) + tid;
+        const uint2 cv = *hc;
+        const ulonglong2 sv = *hs;
+        h0 = cv.x;
+        h1 = cv.y;
+        s0 = sv.x;
+        s1 = sv.y;
+        *hc = make_uint2(0u, 0u);
+        *hs = make_ulonglong2(0ull, 0ull);
+    }
+    uint32_t key[IPT];
+    {
+        float sv[IPT];
+#pragma unroll
+        for (int u = 0; u < IPT; ++u) sv[u] = i0 + u < N ? a.surv[i0 + u] : 0.0f;
+        int k = k0;
+#pragma unroll
+        for (int u = 0; u < IPT; ++u) {
+            key[u] = key_of(sv[u], i0 + u < N && k < kmax && sv[u] >= a.eps);
+            if (++k == G) k = 0;
+        }
+        sm.lastkey[tid] = key[IPT - 1];
+    }
+    // block scan of the bins: inclusive counts, exclusive sums
+    int n_kept;
+    {
+        unsigned ci = h0 + h1;
+        unsigned long long si = s0 + s1;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const unsigned oc = __shfl_up_sync(kFullMask, ci, d);
+            const unsigned long long os = __shfl_up_sync(kFullMask, si, d);
+            if (lane >= d) {
+                ci += oc;
+                si += os;
+            }
+        }
+        if (lane == 31) {
+            sm.wc[warp] = ci;
+            sm.ws[warp] = si;
+        }
+        __syncthreads();
+        // every warp scans the 32 warp totals itself (no second barrier)
+        const unsigned w = sm.wc[lane];
+        const unsigned long long wsum = sm.ws[lane];
+        unsigned wi = w;
+        unsigned long long wsi = wsum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const unsigned oc = __shfl_up_sync(kFullMask, wi, d);
+            const unsigned long long os = __shfl_up_sync(kFullMask, wsi, d);
+            if (lane >= d) {
+                wi += oc;
+                wsi += os;
+            }
+        }
+        n_kept = (int)__shfl_sync(kFullMask, wi, 31);
+        const unsigned wex = __shfl_sync(kFullMask, wi - w, warp);
+        const unsigned long long wsex = __shfl_sync(kFullMask, wsi - wsum, warp);
+        const unsigned cex = wex + ci - (h0 + h1);
+        const unsigned long long sex = wsex + si - (s0 + s1);
+        sm.cum[2 * tid] = cex + h0;
+        sm.cum[2 * tid + 1] = cex + h0 + h1;
+        sm.csum[2 * tid] = sex;
+        sm.csum[2 * tid + 1] = sex + s0;
+    }
+    __syncthreads();
+    long long b_top = n_kept;  // largest in-range budget
+    if (c.kind == DSPARK_COST_ADDITIVE) b_top = min(b_top, (long long)Mlast - (long long)B);
+
+    // warp j: candidate budget b_j, the top bin holding its threshold and
+    // its rank inside the bin
+    if (warp < nc) {
+        int b;
+        if (warp < c.n) b = entry_last_budget(c, warp, Mj, Mprev, Mnext, B, b_top);
+        else b = (a.forced >= 0 && b_top >= 0) ? (int)min((long long)a.forced, b_top) : -1;
+        int rem = 0, d = 0, cnt = 0;
+        unsigned long long ps = 0ull;
+        if (b >= 1) {  // b <= n_kept = cum[2047]
+            const unsigned ub = (unsigned)b;
+            // lane 31 always votes (cum[2047] = n_kept >= b); the clamps only keep
+            // the indices inside the table
+            const int l1 = max(__ffs(__ballot_sync(kFullMask, sm.cum[64 * lane + 63] >= ub)) - 1, 0);
+            const int base = 64 * l1;
+            const int l2 = max(__ffs(__ballot_sync(kFullMask, sm.cum[base + 2 * lane + 1] >= ub)) - 1, 0);
+            d = base + 2 * l2;
+            if (sm.cum[d] < ub) ++d;
+            const int before = d > 0 ? (int)sm.cum[d - 1] : 0;
+            rem = b - before;
+            cnt = (int)sm.cum[d] - before;
+            ps = sm.csum[d];
+            if (lane == 0) atomicOr(&sm.binmask[d >> 5], 1u << (d & 31));
+        }
+        if (lane == 0) {
+            sm.cand_b[warp] = b;
+            sm.rem[warp] = rem;
+            sm.dbin[warp] = d;
+            sm.hcnt[warp] = cnt;
+            sm.psum[warp] = ps;
+            sm.P[warp] = 0ull;
+            sm.cthr[warp] = kNoComposite;
+        }
+    }
+    __syncthreads();
+
+    // (2) gather the candidates of the marked bins (order irrelevant)
+    {
+        int r = r0, k = k0;
+#pragma unroll
+        for (int u = 0; u < IPT; ++u) {
+            const uint32_t kk = key[u];
+            const uint32_t bin = kk >> kHistShift;
+            const bool take = kk != kDroppedKey && ((sm.binmask[bin >> 5] >> (bin & 31)) & 1u);
+            const unsigned vote = __ballot_sync(kFullMask, take);
+            if (vote) {
+                int base = 0;
+                if (lane == 0) base = atomicAdd(&sm.n_gather, __popc(vote));
+                base = __shfl_sync(kFullMask, base, 0);
+                const int pos = base + __popc(vote & lanemask_lt());
+                if (take && pos < kGather) {
+                    sm.LC[pos] = composite(kk, k * B + r);
+                    sm.LF[pos] = (unsigned long long)fixed_of_key(kk);
+                }
+            }
+            if (++k == G) {
+                k = 0;
+                ++r;
+            }
+        }
+    }
+    __syncthreads();
+    const int m = sm.n_gather;
+    if (m <= kGather) {
+        // rank of each gathered candidate among all gathered ones
+        for (int i = tid; i < m; i += kSelThreads) {
+            const unsigned long long ci = sm.LC[i];
+            int pos = 0;
+            for (int y = 0; y < m; ++y) pos += sm.LC[y] < ci ? 1 : 0;
+            sm.SC[pos] = ci;
+            sm.SF[pos] = sm.LF[i];
+        }
+        __syncthreads();
+        // warp j: its bin starts after the gathered candidates of the marked
+        // bins below it; C*_j is the rem_j-th of its bin
+        if (warp < nc) {
+            const int d = sm.dbin[warp], rem = sm.rem[warp];
+            if (rem >= 1) {
+                int below = 0;
+                if (lane < nc) {
+                    const int dl = sm.dbin[lane];
+                    bool first = sm.rem[lane] >= 1 && dl < d;
+                    for (int i = 0; i < lane && first; ++i)
+                        if (sm.rem[i] >= 1 && sm.dbin[i] == dl) first = false;
+                    below = first ? sm.hcnt[lane] : 0;
+                }
+                const int start = __reduce_add_sync(kFullMask, below);
+                unsigned long long part = 0ull;
+                for (int q = lane; q < rem; q += 32) part += sm.SF[start + q];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFullMask, part, o);
+                if (lane == 0) {
+                    sm.cthr[warp] = sm.SC[start + rem - 1];
+                    sm.P[warp] = sm.psum[warp] + part;
+                }
+            }
+        }
+    } else {
+        radix_thresholds<IPT>(a, sm, key, r0, k0, nc);
+    }
+    __syncthreads();
+
+    // (3) theta at every candidate (all in warp 0) and the budget
+    if (warp == 0) {
+        long long my_key = -1;
+        int my_b = 0x7FFFFFFF;
+        bool bad_cost = false;
+        if (lane < c.n) {
+            const int b = sm.cand_b[lane];
+            if (b >= 0) {
+                if (!sm.ok_s[lane]) {
+                    bad_cost = true;
+                } else {
+                    const double tau = tau_of(B, b == 0 ? 0 : (long long)sm.P[lane]);
+                    const double theta = c.kind == DSPARK_COST_SPS_1D
+                                             ? __dmul_rn(tau, sm.val_s[lane])
+                                             : __ddiv_rn(tau, sm.div_s[lane]);
+                    my_key = __double_as_longlong(theta);
+                    my_b = b;
+                }
+            }
+        }
+        // first maximiser: theta >= 0, so its bits order like the values;
+        // +1 leaves 0 for "no candidate"; ties go to the smaller budget
+        {
+            const unsigned long long uk = my_key >= 0 ? (unsigned long long)my_key + 1ull : 0ull;
+            const unsigned hi = (unsigned)(uk >> 32), lo = (unsigned)uk;
+            const unsigned mhi = __reduce_max_sync(kFullMask, hi);
+            const unsigned mlo = __reduce_max_sync(kFullMask, hi == mhi ? lo : 0u);
+            const bool top = hi == mhi && lo == mlo;
+            my_b = (int)__reduce_min_sync(kFullMask, top ? (unsigned)my_b : 0x7FFFFFFFu);
+            my_key = (long long)((((unsigned long long)mhi << 32) | mlo) - 1ull);
+        }
+        const bool any_bad_cost = __any_sync(kFullMask, bad_cost);
+        if (lane == 0) {
+            const bool bad_table = sm.bad_table != 0;
+            int st = (any_bad_cost || bad_table) ? DSPARK_STATUS_BAD_COST : 0;
+            int budget = 0, slot = -1;
+            double theta_out = 0.0;
+            if (a.forced < 0) {
+                if (bad_table || my_b == 0x7FFFFFFF) {
+                    st |= DSPARK_STATUS_INFEASIBLE;
+                } else {
+                    budget = my_b;
+                    theta_out = __longlong_as_double(my_key);
+                    for (int j = 0; j < c.n; ++j)
+                        if (sm.cand_b[j] == budget) {
+                            slot = j;
+                            break;
+                        }
+                }
+            } else if (bad_table || b_top < 0) {
+                st |= DSPARK_STATUS_INFEASIBLE;
+            } else {
+                budget = sm.cand_b[c.n];
+                slot = c.n;
+                const double tau = tau_of(B, budget == 0 ? 0 : (long long)sm.P[slot]);
+                // theta at the forced budget: the entry covering M = B + budget
+                const long long Mv = (long long)B + budget;
+                int j = -1;
+                if (c.kind == DSPARK_COST_SPS_1D) {
+                    for (int i = 0; i < c.n; ++i)
+                        if ((long long)sm.M_s[i] <= Mv) j = i;
+                    if (j < 0) j = 0;
+                    const double sps = sm.val_s[j];
+                    if (sps > 0.0 && isfinite(sps)) theta_out = __dmul_rn(tau, sps);
+                } else {
+                    for (int i = c.n - 1; i >= 0; --i)
+                        if ((long long)sm.M_s[i] >= Mv) j = i;
+                    if (j >= 0) {
+                        const double Tm = __dadd_rn(__dadd_rn(c.bias, c.alpha), sm.val_s[j]);
+                        if (Tm > 0.0 && isfinite(Tm)) theta_out = __ddiv_rn(tau, Tm);
+                    }
+                }
+            }
+            const bool chosen = budget > 0 && slot >= 0;
+            if (st) flag(a.status, st);
+            sm.cstar = chosen ? sm.cthr[slot] : kNoComposite;
+            a.budget[0] = budget;
+            a.tau_theta[0] = tau_of(B, chosen ? (long long)sm.P[slot] : 0);
+            a.tau_theta[1] = theta_out;
+        }
+    }
+    __syncthreads();
+
+    // (4) ScheduleVerifyLensTopk: request r selects its candidates with
+    // C <= C*, a prefix of its depths; the thread holding the first depth
+    // past that prefix (or the last depth) writes 1 + its length, clamped
+    const unsigned long long cstar = sm.cstar;
+    {
+        int r = r0, k = k0;
+        bool prev_in = false;  // the previous depth of the same request is selected
+        if (tid > 0 && k0 > 0) {
+            const uint32_t pk = sm.lastkey[tid - 1];
+            prev_in = cstar != kNoComposite && pk != kDroppedKey &&
+                      composite(pk, (k0 - 1) * B + r0) <= cstar;
+        }
+#pragma unroll
+        for (int u = 0; u < IPT; ++u) {
+            if (i0 + u < N) {
+                const uint32_t kk = key[u];
+                const bool in = cstar != kNoComposite && kk != kDroppedKey &&
+                                composite(kk, k * B + r) <= cstar;
+                int len = -1;
+                if (!in && (k == 0 || prev_in)) len = k;  // first depth not selected
+                if (in && k == G - 1) len = G;            // every depth selected
+                if (len >= 0) a.verify_lens[r] = min(max(1 + len, a.min_len), a.max_len);
+                prev_in = in;
+            }
+            if (++k == G) {
+                k = 0;
+                ++r;
+                prev_in = false;
+            }
+        }
+    }
+}
+
+size_t select_smem_bytes() { return sizeof(SelSmem); }
+
+template <int IPT>
+cudaError_t launch_select(const PlanArgs &a, cudaStream_t s) {
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(select_kernel<IPT>),
+                                (int)select_smem_bytes(),
+                                IPT == 1 ? 1 : IPT == 2 ? 2 : IPT == 4 ? 3 : IPT == 8 ? 4 : 5);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(select_kernel<IPT>, dim3(1), dim3(kSelThreads), select_smem_bytes(), s, a);
+}
+
 }  // namespace dspark
 
 using namespace dspark;
@@ -614,8 +1185,10 @@ extern "C" int dspark_plan(const float *conf_logits, const float *sts_temps,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     PlanScratch *scratch = static_cast<PlanScratch *>(workspace);
     const int sblocks = (B * 32 + kSurvThreads - 1) / kSurvThreads;
+    const bool select = cost->n <= kMaxSelect;  // few candidate budgets: one-CTA select
     survival_kernel<<<sblocks, kSurvThreads, 0, s>>>(conf_logits, sts_temps, B, G,
-                                                     p->survival_eps, survivals, status, scratch);
+                                                     p->survival_eps, p->max_verify_len - 1,
+                                                     select, survivals, status, scratch);
     if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
 
     PlanArgs a;
@@ -633,6 +1206,20 @@ extern "C" int dspark_plan(const float *conf_logits, const float *sts_temps,
     a.tau_theta = tau_theta;
     a.status = status;
     a.scratch = scratch;
+    if (select) {
+        const int ipt = (N + kSelThreads - 1) / kSelThreads;
+        cudaError_t e;
+        if (ipt <= 1) e = launch_select<1>(a, s);
+        else if (ipt <= 2) e = launch_select<2>(a, s);
+        else if (ipt <= 4) e = launch_select<4>(a, s);
+        else if (ipt <= 8) e = launch_select<8>(a, s);
+        else e = launch_select<16>(a, s);
+        if (e == cudaSuccess) return DSPARK_OK;
+        // the bins survival_kernel filled must not reach the next call
+        cudaMemsetAsync(&scratch->hcount[0], 0,
+                        sizeof(scratch->hcount) + sizeof(scratch->hsum), s);
+        return DSPARK_ERR_CUDA;
+    }
     a.P2 = pow2_at_least(G);
     const size_t smem = rank_smem_bytes(B, a.P2);
     if (ensure_smem(reinterpret_cast<const void *>(rank_kernel), (int)rank_smem_max(), 0) != cudaSuccess)

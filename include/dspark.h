@@ -103,8 +103,14 @@ typedef struct {
     double alpha_ms;       /* additive only */
 } dspark_cost_table;
 
-/* Device scratch of one planner call: about 12 * B * gamma + 256 bytes
- * (candidate ranks, the sorted survivals and a completion counter). */
+/* Device scratch of one planner call: about 12 * B * gamma + 26 KB
+ * (candidate ranks, the sorted survivals, a completion counter and a
+ * 2048-bin histogram of the survivals).  The workspace must be zero-filled
+ * once before its first dspark_plan call (cudaMemset); every call that
+ * returns DSPARK_OK leaves the histogram zero again, and a call that
+ * returns DSPARK_ERR_CUDA after launching clears it on the stream, so the
+ * buffer can be passed unchanged to the next call.  Do not reuse it for
+ * other data between planner calls. */
 DSPARK_API size_t dspark_plan_workspace_bytes(int32_t B, int32_t gamma);
 
 /* The verify planner.  [AVS] §一 (budget by survival, tau, theta, argmax,

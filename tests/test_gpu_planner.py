@@ -3,6 +3,8 @@ against the CPU oracle, element by element on the same seeded inputs,
 through the C-ABI.  Discrete outputs are compared bit-exactly; survivals,
 tau and theta too (the arithmetic is defined to give identical floats)."""
 
+import zlib
+
 import numpy as np
 import pytest
 import torch
@@ -111,6 +113,85 @@ def test_plan_random(dev, orc, seed):
                    P["M"], P["val"], P["bias"], P["alpha"])
     if compare_plan(f"random/{seed}", g, ref, P["B"], P["gamma"], P["min_len"]):
         assert int(g["status"][0]) == ref.status
+
+
+def _select_case(name):
+    """Problems for the few-entry-table planner whose threshold bins hold few
+    candidates (ranked by counting) or thousands of equal survivals (radix
+    passes, ties resolved by depth then request)."""
+    rng = np.random.default_rng(zlib.crc32(name.encode()))
+    dsv4_M = np.array([256, 512, 1024, 2048, 4096], np.int32)
+    dsv4_val = np.array([0.512, 1.024, 2.048, 4.096, 8.192])
+    base = dict(T=np.ones(16, np.float32), eps=1e-4, min_len=1, max_len=17, kind=1, M=dsv4_M,
+                val=dsv4_val, forced=-1, bias=1.5, alpha=2.56)
+    if name == "all_ones":          # every survival exactly 1.0: one bin of 4096
+        return dict(base, B=256, gamma=16, z=np.full((256, 16), 40.0, np.float32))
+    if name == "all_ones_forced":
+        return dict(base, B=256, gamma=16, z=np.full((256, 16), 40.0, np.float32), forced=1001)
+    if name == "half_saturated":    # depths < 8 at 1.0, the rest spread
+        z = rng.normal(1.5, 1.0, (256, 16)).astype(np.float32)
+        z[:, :8] = 40.0
+        return dict(base, B=256, gamma=16, z=z)
+    if name == "identical_requests":  # 1000 equal survivals per depth
+        z = np.tile(rng.normal(2.0, 1.0, 16).astype(np.float32), (1000, 1))
+        return dict(base, B=1000, gamma=16, z=z, kind=0, M=np.array([1000, 3000, 9000], np.int32),
+                    val=np.array([90.0, 60.0, 25.0]))
+    if name == "identical_forced":
+        z = np.tile(rng.normal(2.0, 1.0, 16).astype(np.float32), (1000, 1))
+        return dict(base, B=1000, gamma=16, z=z, kind=0, M=np.array([1000, 3000, 9000], np.int32),
+                    val=np.array([90.0, 60.0, 25.0]), forced=4321)
+    if name == "large_spread":      # 12000 candidates, 16 per thread
+        z = rng.normal(1.0, 1.5, (600, 20)).astype(np.float32)
+        z[rng.integers(0, 600, 200)] = z[7]
+        return dict(base, B=600, gamma=20, z=z, T=np.full(20, 1.3, np.float32), max_len=21,
+                    M=np.array([600, 1024, 2048, 4096, 8192, 12600], np.int32),
+                    val=np.array([0.5, 0.9, 1.8, 3.5, 7.0, 11.0]))
+    if name == "sixteen_entries":   # the largest table the select path takes
+        z = rng.normal(1.0, 1.2, (512, 16)).astype(np.float32)
+        M = np.linspace(512, 512 * 17, 16).astype(np.int32)
+        return dict(base, B=512, gamma=16, z=z, kind=0, M=M, val=1.0 / (1e-3 + 2e-6 * M))
+    raise KeyError(name)
+
+
+@pytest.mark.parametrize("name", ["all_ones", "all_ones_forced", "half_saturated",
+                                  "identical_requests", "identical_forced", "large_spread",
+                                  "sixteen_entries"])
+def test_plan_select_bins(dev, orc, name):
+    P = _select_case(name)
+    g = _gpu_plan(dev, P)
+    ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"], P["kind"],
+                   P["M"], P["val"], P["bias"], P["alpha"])
+    assert compare_plan(f"select/{name}", g, ref, P["B"], P["gamma"], P["min_len"])
+    assert int(g["status"][0]) == ref.status
+
+
+def test_plan_workspace_reused_across_shapes(dev, orc):
+    """One zero-filled workspace serves calls of different shapes in a row:
+    each call leaves the survival bins it used cleared."""
+    from confidence_scheduled_speculative_gb300 import api
+    names = ["half_saturated", "large_spread", "all_ones", "identical_forced", "half_saturated"]
+    big = max(api.dspark_plan_workspace_bytes(_select_case(n)["B"], _select_case(n)["gamma"])
+              for n in names)
+    ws = api.workspace(big, dev)
+    for n in names:
+        P = _select_case(n)
+        B, gm = P["B"], P["gamma"]
+        i32 = dict(dtype=torch.int32, device=dev)
+        out = dict(survivals=torch.zeros((B, gm), dtype=torch.float32, device=dev),
+                   verify_lens=torch.zeros(B, **i32), budget=torch.zeros(1, **i32),
+                   tau_theta=torch.zeros(2, dtype=torch.float64, device=dev),
+                   status=torch.zeros(1, **i32))
+        api.dspark_plan(torch.from_numpy(P["z"]).to(dev), torch.from_numpy(P["T"]).to(dev), B=B,
+                        gamma=gm, survival_eps=P["eps"], min_verify_len=P["min_len"],
+                        max_verify_len=P["max_len"], forced_budget=P["forced"],
+                        cost_kind=P["kind"], cost_M=torch.from_numpy(P["M"]).to(dev),
+                        cost_val=torch.from_numpy(P["val"]).to(dev), bias_ms=P["bias"],
+                        alpha_ms=P["alpha"], workspace=ws, **out)
+        torch.cuda.synchronize()
+        g = {k: v.cpu().numpy() for k, v in out.items()}
+        ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"],
+                       P["kind"], P["M"], P["val"], P["bias"], P["alpha"])
+        assert compare_plan(f"reuse/{n}", g, ref, B, gm, P["min_len"])
 
 
 def test_plan_edge_cases(dev, orc):
