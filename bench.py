@@ -39,7 +39,6 @@ if ROOT not in sys.path:
 
 METRIC = "plan+pack+accept steps/s at B=256 gamma=16 V=129280; accept HBM GB/s % of peak"
 UNIT = "steps/s"
-KERNELS_PER_STEP = 5  # survival, budget, pack, argmax, greedy finalize
 
 
 def parse():
@@ -54,6 +53,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-cap", action="store_true")
+    ap.add_argument("--separate-plan-pack", action="store_true",
+                    help="issue dspark_plan and dspark_pack_verify instead of dspark_plan_pack")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
     return ap.parse_args()
 
@@ -290,12 +291,16 @@ def run_ours(args):
     compact = strided_dev.index_select(0, vs.packed_src[:total].long()).contiguous()
     accept_bytes = total * w.V * w.elem_bytes
 
-    plan_fn, pack_fn, acc_fn = vs.bind_compact(compact)
+    plan_pack_fn, plan_fn, pack_fn, acc_fn = vs.bind_compact(compact)
     stream = torch.cuda.current_stream()
 
+    if args.separate_plan_pack:
+        def plan_pack_fn():
+            plan_fn()
+            pack_fn()
+
     def one_step():
-        plan_fn()
-        pack_fn()
+        plan_pack_fn()
         acc_fn()
 
     warm = max(3, args.warmup)
@@ -306,6 +311,7 @@ def run_ours(args):
 
     # ---- timed region: K steps, accept bracketed by events on its stream
     K = max(1, args.steps)
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -321,8 +327,8 @@ def run_ours(args):
     sampler.start()
     t_start.record(stream)
     for i in range(K):
-        plan_fn()
-        pack_fn()
+        ev_s[i].record(stream)
+        plan_pack_fn()
         ev_a[i].record(stream)
         acc_fn()
         ev_b[i].record(stream)
@@ -333,26 +339,33 @@ def run_ours(args):
     clocks = sampler.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
     accept_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
+    step_us = np.array([ev_s[i].elapsed_time(ev_s[i + 1]) for i in range(K - 1)] +
+                       [ev_s[K - 1].elapsed_time(t_end)]) * 1e3
     if world > 1:
         t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
     status = int(vs.status.item())
 
-    # ---- breakdown (outside the timed region): per call on the same stream
+    # ---- breakdown (outside the timed region): per call on the same stream,
+    # the fused plan+pack and, for reference, the two separate calls
     n_b = min(K, 200)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_b)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_b)]
     for e in evs:
         e[0].record(stream)
-        plan_fn()
+        plan_pack_fn()
         e[1].record(stream)
-        pack_fn()
-        e[2].record(stream)
         acc_fn()
+        e[2].record(stream)
+        plan_fn()
         e[3].record(stream)
+        pack_fn()
+        e[4].record(stream)
+        acc_fn()
+        e[5].record(stream)
     torch.cuda.synchronize()
-    br = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
-                   for e in evs]) * 1e3
+    br = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3]),
+                    e[3].elapsed_time(e[4])] for e in evs]) * 1e3
 
     # ---- cap-accept over the full strided block (secondary)
     cap = None
@@ -426,6 +439,7 @@ def run_ours(args):
         "config": {"workload": f"{w.name} B={w.B} gamma={w.gamma} V={w.V} compact",
                    "B": w.B, "gamma": w.gamma, "V": w.V, "mode": "compact",
                    "packed_rows": total, "padded_rows": padded, "seed": args.seed,
+                   "plan_pack": "separate calls" if args.separate_plan_pack else "dspark_plan_pack",
                    "l2": f"inputs larger than L2: {accept_bytes / 1e6:.1f} MB of logits per step",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -438,10 +452,15 @@ def run_ours(args):
                 "d2h_bytes_per_step": io.d2h_output_bytes(), "steps": n_e,
                 "matches_device_path": bool(e2e_ok)},
         "cpu_baseline": cpu,
-        "gpu_launches": KERNELS_PER_STEP * K,
+        "gpu_launches": (5 if args.separate_plan_pack else vs.kernels_per_step) * K,
         "clocks": clocks,
-        "breakdown_us": {"plan": float(np.median(br[:, 0])), "pack": float(np.median(br[:, 1])),
-                         "accept": float(np.median(br[:, 2])),
+        "step_us": {"p10": float(np.percentile(step_us, 10)),
+                    "p50": float(np.percentile(step_us, 50)),
+                    "p90": float(np.percentile(step_us, 90))},
+        "breakdown_us": {"plan_pack": float(np.median(br[:, 0])),
+                         "accept": float(np.median(br[:, 1])),
+                         "plan_alone": float(np.median(br[:, 2])),
+                         "pack_alone": float(np.median(br[:, 3])),
                          "accept_timed_mean": acc_us, "step_timed_mean": 1e3 * ms_per_step},
         "cap_accept": cap,
         "status": status,

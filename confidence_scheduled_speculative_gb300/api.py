@@ -72,6 +72,10 @@ _SIGS = {
     "dspark_pack_verify": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _I32,
                                           ctypes.POINTER(ctypes.c_int32), _I32, _I32, _VP, _VP,
                                           _VP, _VP, _VP, _VP, _VP, _VP]),
+    "dspark_plan_pack": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(dspark_plan_params),
+                                        ctypes.POINTER(dspark_cost_table), _VP, _VP, _VP, _VP,
+                                        _VP, _VP, _VP, ctypes.POINTER(ctypes.c_int32), _I32, _I32,
+                                        _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
     "dspark_accept_workspace_bytes": (_SZ, [_I32, _I32]),
     "dspark_greedy_accept": (ctypes.c_int, [_VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP, _I32,
                                             _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP,
@@ -182,6 +186,35 @@ def dspark_pack_verify(anchor, draft, prefix_lens, verify_lens, *, B, gamma, tie
         _p(packed_src, torch.int32, "packed_src"), _p(cu_seqlens, torch.int32, "cu_seqlens"),
         _p(totals, torch.int32, "totals"), _p(status, torch.int32, "status"), _stream(stream))
     _check("dspark_pack_verify", rc)
+
+
+def dspark_plan_pack(conf_logits, sts_temps, anchor, draft, prefix_lens, *, B, gamma,
+                     survival_eps, min_verify_len, max_verify_len, forced_budget, cost_kind,
+                     cost_M, cost_val, bias_ms=0.0, alpha_ms=0.0, tiers, capacity, survivals,
+                     verify_lens, budget, tau_theta, packed_ids, packed_pos, packed_req,
+                     packed_src, cu_seqlens, totals, status, workspace, stream=None) -> None:
+    """dspark_plan then dspark_pack_verify on its verify_lens, in fewer launches
+    (the pack runs inside the planner's last kernel for tables of <= 16
+    entries)."""
+    params = dspark_plan_params(B, gamma, survival_eps, min_verify_len, max_verify_len,
+                                forced_budget)
+    cost = dspark_cost_table(cost_kind, int(cost_M.numel()), _p(cost_M, torch.int32, "cost_M"),
+                             _p(cost_val, torch.float64, "cost_val"), bias_ms, alpha_ms)
+    tiers = [int(t) for t in tiers]
+    arr = (ctypes.c_int32 * max(1, len(tiers)))(*tiers)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().dspark_plan_pack(
+        _p(conf_logits, torch.float32, "conf_logits"), _p(sts_temps, torch.float32, "sts_temps"),
+        ctypes.byref(params), ctypes.byref(cost), _p(survivals, torch.float32, "survivals"),
+        _p(verify_lens, torch.int32, "verify_lens"), _p(budget, torch.int32, "budget"),
+        _p(tau_theta, torch.float64, "tau_theta"), _p(anchor, torch.int32, "anchor"),
+        _p(draft, torch.int32, "draft"), _p(prefix_lens, torch.int32, "prefix_lens"), arr,
+        len(tiers), capacity, _p(packed_ids, torch.int32, "packed_ids"),
+        _p(packed_pos, torch.int32, "packed_pos"), _p(packed_req, torch.int32, "packed_req"),
+        _p(packed_src, torch.int32, "packed_src"), _p(cu_seqlens, torch.int32, "cu_seqlens"),
+        _p(totals, torch.int32, "totals"), _p(workspace), ws_bytes,
+        _p(status, torch.int32, "status"), _stream(stream))
+    _check("dspark_plan_pack", rc)
 
 
 def _dtype_code(t: torch.Tensor) -> int:

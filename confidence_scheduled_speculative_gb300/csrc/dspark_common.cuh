@@ -65,6 +65,24 @@ __device__ T block_exclusive_scan(T v, T *warp_tot, T *total) {
     return res;
 }
 
+// Graph tiers of the verify window (ascending), passed by value.
+struct TierArgs {
+    int n;
+    int32_t t[DSPARK_MAX_TIERS];
+};
+
+// The packed total rounded up to the smallest tier >= total ([SGL] "Ragged
+// verify"); no tiers: the total itself.  *no_tier is set when every tier is
+// below the total (the window cannot be replayed; flagged as CAPACITY).
+__device__ __forceinline__ int tier_round_up(const TierArgs &tiers, int total, bool *no_tier) {
+    *no_tier = false;
+    if (tiers.n <= 0) return total;
+    for (int i = 0; i < tiers.n; ++i)
+        if (tiers.t[i] >= total) return tiers.t[i];
+    *no_tier = true;
+    return total;
+}
+
 // Block-wide sum (all threads receive it).  `scratch` >= 33 entries.
 template <typename T>
 __device__ T block_sum(T v, T *scratch) {
@@ -80,6 +98,17 @@ namespace dspark {
 
 // Streaming multiprocessor count of the current device (cached per device).
 int sm_count();
+
+// Host-side check and copy of a tier list (ascending, at most
+// DSPARK_MAX_TIERS); false when it is invalid.
+bool load_tiers(const int32_t *host_tiers, int32_t n_tiers, TierArgs *out);
+
+// The pack kernel on `stream` (pack.cu), launched after the planner with
+// programmatic serialization.
+cudaError_t launch_pack(const int32_t *anchor, const int32_t *draft, const int32_t *prefix,
+                        const int32_t *lens, int B, int gamma, const TierArgs &tiers,
+                        int capacity, int32_t *ids, int32_t *pos, int32_t *req, int32_t *src,
+                        int32_t *cu, int32_t *totals, int32_t *status, cudaStream_t stream);
 
 // Raise a kernel's dynamic shared-memory limit once per device.
 cudaError_t ensure_smem(const void *kernel, int bytes, int slot);

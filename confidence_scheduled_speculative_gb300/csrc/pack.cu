@@ -25,11 +25,6 @@ namespace dspark {
 constexpr int kPackThreads = 256;
 constexpr int kPackReqPerCta = kPackThreads / 32;
 
-struct TierArgs {
-    int n;
-    int32_t t[DSPARK_MAX_TIERS];
-};
-
 __device__ __forceinline__ int clamp_len(int L, int gamma, bool &bad) {
     if (L < 1 || L > gamma + 1) {
         bad = true;
@@ -107,17 +102,8 @@ pack_kernel(const int32_t *__restrict__ anchor, const int32_t *__restrict__ draf
     }
 
     // graph-tier round-up and pad rows
-    int padded = total;
-    bool no_tier = false;
-    if (tiers.n > 0) {
-        no_tier = true;
-        for (int i = 0; i < tiers.n; ++i)
-            if (tiers.t[i] >= total) {
-                padded = tiers.t[i];
-                no_tier = false;
-                break;
-            }
-    }
+    bool no_tier;
+    const int padded = tier_round_up(tiers, total, &no_tier);
     const int pad_end = min(padded, capacity);
     for (int i = total + blockIdx.x * kPackThreads + tid; i < pad_end; i += gridDim.x * kPackThreads) {
         ids[i] = 0;
@@ -132,6 +118,27 @@ pack_kernel(const int32_t *__restrict__ anchor, const int32_t *__restrict__ draf
         if (no_tier || padded > capacity) over = true;
     }
     if (__syncthreads_or(over) && tid == 0) flag(status, DSPARK_STATUS_CAPACITY);
+}
+
+bool load_tiers(const int32_t *host_tiers, int32_t n_tiers, TierArgs *out) {
+    if (n_tiers < 0 || n_tiers > DSPARK_MAX_TIERS || (n_tiers > 0 && !host_tiers)) return false;
+    out->n = n_tiers;
+    for (int i = 0; i < n_tiers; ++i) {
+        out->t[i] = host_tiers[i];
+        if (i > 0 && !(out->t[i] > out->t[i - 1])) return false;
+    }
+    for (int i = n_tiers; i < DSPARK_MAX_TIERS; ++i) out->t[i] = 0;
+    return true;
+}
+
+cudaError_t launch_pack(const int32_t *anchor, const int32_t *draft, const int32_t *prefix,
+                        const int32_t *lens, int B, int gamma, const TierArgs &tiers,
+                        int capacity, int32_t *ids, int32_t *pos, int32_t *req, int32_t *src,
+                        int32_t *cu, int32_t *totals, int32_t *status, cudaStream_t stream) {
+    const int grid = (B + kPackReqPerCta - 1) / kPackReqPerCta;
+    return launch_pdl(pack_kernel, dim3(grid), dim3(kPackThreads), 0, stream, anchor, draft,
+                      prefix, lens, B, gamma, tiers, capacity, ids, pos, req, src, cu, totals,
+                      status);
 }
 
 }  // namespace dspark
@@ -149,20 +156,11 @@ extern "C" int dspark_pack_verify(const int32_t *anchor, const int32_t *draft,
         return DSPARK_ERR_INVALID_ARG;
     if (B < 1 || gamma < 1 || gamma > 31 || capacity < 0) return DSPARK_ERR_INVALID_ARG;
     if ((long long)B * (gamma + 1) > 0x7FFFFFFF) return DSPARK_ERR_INVALID_ARG;
-    if (n_tiers < 0 || n_tiers > DSPARK_MAX_TIERS || (n_tiers > 0 && !host_tiers))
-        return DSPARK_ERR_INVALID_ARG;
     TierArgs t;
-    t.n = n_tiers;
-    for (int i = 0; i < n_tiers; ++i) {
-        t.t[i] = host_tiers[i];
-        if (i > 0 && !(t.t[i] > t.t[i - 1])) return DSPARK_ERR_INVALID_ARG;
-    }
-    for (int i = n_tiers; i < DSPARK_MAX_TIERS; ++i) t.t[i] = 0;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int grid = (B + kPackReqPerCta - 1) / kPackReqPerCta;
-    if (launch_pdl(pack_kernel, dim3(grid), dim3(kPackThreads), 0, s, anchor, draft, prefix_lens,
-                   verify_lens, B, gamma, t, capacity, packed_ids, packed_pos, packed_req,
-                   packed_src, cu_seqlens, totals, status) != cudaSuccess)
+    if (!load_tiers(host_tiers, n_tiers, &t)) return DSPARK_ERR_INVALID_ARG;
+    if (launch_pack(anchor, draft, prefix_lens, verify_lens, B, gamma, t, capacity, packed_ids,
+                    packed_pos, packed_req, packed_src, cu_seqlens, totals, status,
+                    static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     return DSPARK_OK;
 }

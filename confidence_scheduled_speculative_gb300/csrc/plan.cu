@@ -176,6 +176,16 @@ struct CostArgs {
     double bias, alpha;
 };
 
+// Pack of the verify window fused into select_kernel (dspark_plan_pack):
+// the arguments of dspark_pack_verify, verify_lens being the planner's.
+struct PackArgs {
+    bool on;
+    const int32_t *anchor, *draft, *prefix;
+    TierArgs tiers;
+    int capacity;
+    int32_t *ids, *pos, *req, *src, *cu, *totals;
+};
+
 struct PlanArgs {
     const float *surv;  // [B, gamma], eps-zeroed survivals
     int B, gamma, N;
@@ -187,6 +197,7 @@ struct PlanArgs {
     double *tau_theta;
     int32_t *status;
     PlanScratch *scratch;
+    PackArgs pk;
 };
 
 // tau = (B * 2^37 + P) * 2^-37 as an fp64 built with integer operations:
@@ -626,17 +637,26 @@ constexpr int kRadixBins = 256;
 constexpr int kGather = 512;  // gathered candidates ranked by counting
 constexpr unsigned long long kNoComposite = ~0ull;
 
+constexpr int kStage = 24576;  // int32 step inputs the fused pack stages in shared memory
+
 struct SelSmem {
-    unsigned int cum[kHistBins];                       // inclusive key counts by top bin
-    unsigned long long csum[kHistBins];                // fixed-point sums of the bins before
-    unsigned int H[2][kSelSlots][kRadixBins];          // radix pass counts (two buffers)
-    unsigned long long part[kSelSlots][32];            // per-warp partial sums (radix path)
-    unsigned long long LC[kGather], LF[kGather];       // gathered composites and survivals
-    unsigned long long SC[kGather], SF[kGather];       // the same in composite order
+    union {
+        struct {  // steps (1)-(2)
+            unsigned int cum[kHistBins];                       // inclusive key counts by top bin
+            unsigned long long csum[kHistBins];                // fixed-point sums of the bins before
+            unsigned int H[2][kSelSlots][kRadixBins];          // radix pass counts (two buffers)
+            unsigned long long part[kSelSlots][32];            // per-warp partial sums (radix path)
+            unsigned long long LC[kGather], LF[kGather];       // gathered composites and survivals
+            unsigned long long SC[kGather], SF[kGather];       // the same in composite order
+        };
+        int lens_s[kMaxCandidates];  // steps (4)-(5): verify length, then first packed row
+    };
+    int32_t stage[kStage];  // fused pack: anchor [B] | prefix_lens [B] | draft [B, gamma]
     unsigned int binmask[kHistBins / 32];              // top bins holding some threshold
     uint32_t lastkey[kSelThreads];                     // last key of each thread's candidates
     unsigned int wc[32];
     unsigned long long ws[32];
+    int scan32[40];
     unsigned long long prefix[kSelSlots];  // high bits of C*_j fixed so far (radix path)
     unsigned long long psum[kSelSlots];    // fixed-point survivals before the current prefix
     unsigned long long P[kSelSlots];       // fixed-point sum of the b_j largest survivals
@@ -796,6 +816,173 @@ __device__ void radix_thresholds(const PlanArgs &a, SelSmem &sm, const uint32_t 
     }
 }
 
+// Step (5) of select_kernel when the pack is fused: the ragged verify window
+// of dspark_pack_verify from the lengths in shared memory ([ROUND] §三,
+// [AVS] §五-§六, [SGL] "Ragged verify"): cu_seqlens = exclusive scan of the
+// lengths, row cu[r]+j = (j == 0 ? anchor[r] : draft[r][j-1]) at position
+// prefix[r]+j, rounded up to the smallest graph tier with pad rows
+// (id 0, position 0, request -1, source -1).  A block scan gives each
+// request its first row; then each thread writes whole packed rows (stores
+// coalesced across the warp), reading anchor / prefix / draft from the copy
+// staged in shared memory before the dependency wait (when B*(gamma+2) <=
+// kStage).  The planner's lengths are always in [1, gamma+1].
+__device__ __forceinline__ void select_pack(const PlanArgs &a, SelSmem &sm, bool staged) {
+    const int tid = threadIdx.x;
+    const int B = a.B, G = a.gamma, capacity = a.pk.capacity;
+    const int32_t *__restrict__ anchor = a.pk.anchor;
+    const int32_t *__restrict__ draft = a.pk.draft;
+    const int32_t *__restrict__ prefix = a.pk.prefix;
+    int32_t *__restrict__ ids = a.pk.ids;
+    int32_t *__restrict__ pos = a.pk.pos;
+    int32_t *__restrict__ req = a.pk.req;
+    int32_t *__restrict__ src = a.pk.src;
+    int32_t *__restrict__ cu = a.pk.cu;
+    const int per = (B + kSelThreads - 1) / kSelThreads;
+    const int q0 = min(tid * per, B), q1 = min(q0 + per, B);
+    int mine = 0;
+    for (int q = q0; q < q1; ++q) mine += sm.lens_s[q];
+    int total;
+    int off = block_exclusive_scan<int>(mine, sm.scan32, &total);
+    // lens_s becomes the first packed row of each request (strictly
+    // increasing: every length is >= 1)
+    for (int q = q0; q < q1; ++q) {
+        const int L = sm.lens_s[q];
+        sm.lens_s[q] = off;
+        cu[q + 1] = off + L;
+        off += L;
+    }
+    bool no_tier;
+    const int padded = tier_round_up(a.pk.tiers, total, &no_tier);
+    __syncthreads();
+    // one packed row per thread (coalesced stores); its request by binary
+    // search over the first rows
+    const int rows = min(total, capacity);
+    for (int dst = tid; dst < rows; dst += kSelThreads) {
+        int lo = 0, hi = B - 1;  // the last request whose first row is <= dst
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (sm.lens_s[mid] <= dst) lo = mid;
+            else hi = mid - 1;
+        }
+        const int j = dst - sm.lens_s[lo];
+        int tok, pre;
+        if (staged) {
+            tok = j == 0 ? sm.stage[lo] : sm.stage[2 * B + lo * G + j - 1];
+            pre = sm.stage[B + lo];
+        } else {
+            tok = j == 0 ? __ldg(anchor + lo) : __ldg(draft + (size_t)lo * G + j - 1);
+            pre = __ldg(prefix + lo);
+        }
+        ids[dst] = tok;
+        pos[dst] = pre + j;
+        req[dst] = lo;
+        src[dst] = lo * (G + 1) + j;
+    }
+    const int pad_end = min(padded, capacity);
+    for (int i = total + tid; i < pad_end; i += kSelThreads) {
+        ids[i] = 0;
+        pos[i] = 0;
+        req[i] = -1;
+        src[i] = -1;
+    }
+    if (tid == 0) {
+        cu[0] = 0;
+        a.pk.totals[0] = total;
+        a.pk.totals[1] = padded;
+        if (total > capacity || no_tier || padded > capacity) flag(a.status, DSPARK_STATUS_CAPACITY);
+    }
+}
+
+// Step (3) of select_kernel, run by warp 0: theta at every candidate budget,
+// the first maximiser (or the forced budget) and the plan's scalar outputs.
+// Kept out of line so that the compiler schedules it on its own.
+__device__ __noinline__ void select_theta(const PlanArgs &a, SelSmem &sm, long long b_top) {
+    // arguments into registers first (the output stores could alias them)
+    const int lane = threadIdx.x & 31;
+    const int B = a.B, n = a.cost.n, kind = a.cost.kind, forced = a.forced;
+    const double bias = a.cost.bias, alpha = a.cost.alpha;
+    int32_t *budget_out = a.budget, *status = a.status;
+    double *tau_theta = a.tau_theta;
+    long long my_key = -1;
+    int my_b = 0x7FFFFFFF;
+    bool bad_cost = false;
+    if (lane < n) {
+        const int b = sm.cand_b[lane];
+        if (b >= 0) {
+            if (!sm.ok_s[lane]) {
+                bad_cost = true;
+            } else {
+                const double tau = tau_of(B, b == 0 ? 0 : (long long)sm.P[lane]);
+                const double theta = kind == DSPARK_COST_SPS_1D
+                                         ? __dmul_rn(tau, sm.val_s[lane])
+                                         : __ddiv_rn(tau, sm.div_s[lane]);
+                my_key = __double_as_longlong(theta);
+                my_b = b;
+            }
+        }
+    }
+    // first maximiser: theta >= 0, so its bits order like the values;
+    // +1 leaves 0 for "no candidate"; ties go to the smaller budget
+    {
+        const unsigned long long uk = my_key >= 0 ? (unsigned long long)my_key + 1ull : 0ull;
+        const unsigned hi = (unsigned)(uk >> 32), lo = (unsigned)uk;
+        const unsigned mhi = __reduce_max_sync(kFullMask, hi);
+        const unsigned mlo = __reduce_max_sync(kFullMask, hi == mhi ? lo : 0u);
+        const bool top = hi == mhi && lo == mlo;
+        my_b = (int)__reduce_min_sync(kFullMask, top ? (unsigned)my_b : 0x7FFFFFFFu);
+        my_key = (long long)((((unsigned long long)mhi << 32) | mlo) - 1ull);
+    }
+    const bool any_bad_cost = __any_sync(kFullMask, bad_cost);
+    if (lane == 0) {
+        const bool bad_table = sm.bad_table != 0;
+        int st = (any_bad_cost || bad_table) ? DSPARK_STATUS_BAD_COST : 0;
+        int budget = 0, slot = -1;
+        double theta_out = 0.0;
+        if (forced < 0) {
+            if (bad_table || my_b == 0x7FFFFFFF) {
+                st |= DSPARK_STATUS_INFEASIBLE;
+            } else {
+                budget = my_b;
+                theta_out = __longlong_as_double(my_key);
+                for (int j = 0; j < n; ++j)
+                    if (sm.cand_b[j] == budget) {
+                        slot = j;
+                        break;
+                    }
+            }
+        } else if (bad_table || b_top < 0) {
+            st |= DSPARK_STATUS_INFEASIBLE;
+        } else {
+            budget = sm.cand_b[n];
+            slot = n;
+            const double tau = tau_of(B, budget == 0 ? 0 : (long long)sm.P[slot]);
+            // theta at the forced budget: the entry covering M = B + budget
+            const long long Mv = (long long)B + budget;
+            int j = -1;
+            if (kind == DSPARK_COST_SPS_1D) {
+                for (int i = 0; i < n; ++i)
+                    if ((long long)sm.M_s[i] <= Mv) j = i;
+                if (j < 0) j = 0;
+                const double sps = sm.val_s[j];
+                if (sps > 0.0 && isfinite(sps)) theta_out = __dmul_rn(tau, sps);
+            } else {
+                for (int i = n - 1; i >= 0; --i)
+                    if ((long long)sm.M_s[i] >= Mv) j = i;
+                if (j >= 0) {
+                    const double Tm = __dadd_rn(__dadd_rn(bias, alpha), sm.val_s[j]);
+                    if (Tm > 0.0 && isfinite(Tm)) theta_out = __ddiv_rn(tau, Tm);
+                }
+            }
+        }
+        const bool chosen = budget > 0 && slot >= 0;
+        if (st) flag(status, st);
+        sm.cstar = chosen ? sm.cthr[slot] : kNoComposite;
+        budget_out[0] = budget;
+        tau_theta[0] = tau_of(B, chosen ? (long long)sm.P[slot] : 0);
+        tau_theta[1] = theta_out;
+    }
+}
+
 template <int IPT>
 __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -843,6 +1030,16 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
     }
     if (tid < kHistBins / 32) sm.binmask[tid] = 0u;
     if (tid == 0) sm.n_gather = 0;
+    // the fused pack's step inputs are not written by the planner: stage
+    // them now, while the survivals are computed
+    const bool staged = a.pk.on && (long long)B * (G + 2) <= kStage;
+    if (staged) {
+        for (int i = tid; i < B; i += kSelThreads) {
+            sm.stage[i] = __ldg(a.pk.anchor + i);
+            sm.stage[B + i] = __ldg(a.pk.prefix + i);
+        }
+        for (int i = tid; i < N; i += kSelThreads) sm.stage[2 * B + i] = __ldg(a.pk.draft + i);
+    }
     pdl_wait();  // survivals and bins come from survival_kernel
 
     // (1) this thread's two bins, cleared for the next call; its keys
@@ -1022,86 +1219,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
     __syncthreads();
 
     // (3) theta at every candidate (all in warp 0) and the budget
-    if (warp == 0) {
-        long long my_key = -1;
-        int my_b = 0x7FFFFFFF;
-        bool bad_cost = false;
-        if (lane < c.n) {
-            const int b = sm.cand_b[lane];
-            if (b >= 0) {
-                if (!sm.ok_s[lane]) {
-                    bad_cost = true;
-                } else {
-                    const double tau = tau_of(B, b == 0 ? 0 : (long long)sm.P[lane]);
-                    const double theta = c.kind == DSPARK_COST_SPS_1D
-                                             ? __dmul_rn(tau, sm.val_s[lane])
-                                             : __ddiv_rn(tau, sm.div_s[lane]);
-                    my_key = __double_as_longlong(theta);
-                    my_b = b;
-                }
-            }
-        }
-        // first maximiser: theta >= 0, so its bits order like the values;
-        // +1 leaves 0 for "no candidate"; ties go to the smaller budget
-        {
-            const unsigned long long uk = my_key >= 0 ? (unsigned long long)my_key + 1ull : 0ull;
-            const unsigned hi = (unsigned)(uk >> 32), lo = (unsigned)uk;
-            const unsigned mhi = __reduce_max_sync(kFullMask, hi);
-            const unsigned mlo = __reduce_max_sync(kFullMask, hi == mhi ? lo : 0u);
-            const bool top = hi == mhi && lo == mlo;
-            my_b = (int)__reduce_min_sync(kFullMask, top ? (unsigned)my_b : 0x7FFFFFFFu);
-            my_key = (long long)((((unsigned long long)mhi << 32) | mlo) - 1ull);
-        }
-        const bool any_bad_cost = __any_sync(kFullMask, bad_cost);
-        if (lane == 0) {
-            const bool bad_table = sm.bad_table != 0;
-            int st = (any_bad_cost || bad_table) ? DSPARK_STATUS_BAD_COST : 0;
-            int budget = 0, slot = -1;
-            double theta_out = 0.0;
-            if (a.forced < 0) {
-                if (bad_table || my_b == 0x7FFFFFFF) {
-                    st |= DSPARK_STATUS_INFEASIBLE;
-                } else {
-                    budget = my_b;
-                    theta_out = __longlong_as_double(my_key);
-                    for (int j = 0; j < c.n; ++j)
-                        if (sm.cand_b[j] == budget) {
-                            slot = j;
-                            break;
-                        }
-                }
-            } else if (bad_table || b_top < 0) {
-                st |= DSPARK_STATUS_INFEASIBLE;
-            } else {
-                budget = sm.cand_b[c.n];
-                slot = c.n;
-                const double tau = tau_of(B, budget == 0 ? 0 : (long long)sm.P[slot]);
-                // theta at the forced budget: the entry covering M = B + budget
-                const long long Mv = (long long)B + budget;
-                int j = -1;
-                if (c.kind == DSPARK_COST_SPS_1D) {
-                    for (int i = 0; i < c.n; ++i)
-                        if ((long long)sm.M_s[i] <= Mv) j = i;
-                    if (j < 0) j = 0;
-                    const double sps = sm.val_s[j];
-                    if (sps > 0.0 && isfinite(sps)) theta_out = __dmul_rn(tau, sps);
-                } else {
-                    for (int i = c.n - 1; i >= 0; --i)
-                        if ((long long)sm.M_s[i] >= Mv) j = i;
-                    if (j >= 0) {
-                        const double Tm = __dadd_rn(__dadd_rn(c.bias, c.alpha), sm.val_s[j]);
-                        if (Tm > 0.0 && isfinite(Tm)) theta_out = __ddiv_rn(tau, Tm);
-                    }
-                }
-            }
-            const bool chosen = budget > 0 && slot >= 0;
-            if (st) flag(a.status, st);
-            sm.cstar = chosen ? sm.cthr[slot] : kNoComposite;
-            a.budget[0] = budget;
-            a.tau_theta[0] = tau_of(B, chosen ? (long long)sm.P[slot] : 0);
-            a.tau_theta[1] = theta_out;
-        }
-    }
+    if (warp == 0) select_theta(a, sm, b_top);
     __syncthreads();
 
     // (4) ScheduleVerifyLensTopk: request r selects its candidates with
@@ -1125,7 +1243,11 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
                 int len = -1;
                 if (!in && (k == 0 || prev_in)) len = k;  // first depth not selected
                 if (in && k == G - 1) len = G;            // every depth selected
-                if (len >= 0) a.verify_lens[r] = min(max(1 + len, a.min_len), a.max_len);
+                if (len >= 0) {
+                    const int L = min(max(1 + len, a.min_len), a.max_len);
+                    a.verify_lens[r] = L;
+                    sm.lens_s[r] = L;
+                }
                 prev_in = in;
             }
             if (++k == G) {
@@ -1134,6 +1256,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
                 prev_in = false;
             }
         }
+    }
+    if (a.pk.on) {
+        __syncthreads();
+        select_pack(a, sm, staged);
     }
 }
 
@@ -1157,11 +1283,13 @@ extern "C" size_t dspark_plan_workspace_bytes(int32_t B, int32_t gamma) {
     return (plan_scratch_bytes(B, B * gamma) + 255) & ~size_t(255);
 }
 
-extern "C" int dspark_plan(const float *conf_logits, const float *sts_temps,
-                           const dspark_plan_params *p, const dspark_cost_table *cost,
-                           float *survivals, int32_t *verify_lens, int32_t *budget,
-                           double *tau_theta, void *workspace, size_t workspace_bytes,
-                           int32_t *status, void *stream) {
+namespace {
+
+// Argument checks of dspark_plan; DSPARK_OK when the call may proceed.
+int check_plan(const float *conf_logits, const float *sts_temps, const dspark_plan_params *p,
+               const dspark_cost_table *cost, float *survivals, int32_t *verify_lens,
+               int32_t *budget, double *tau_theta, void *workspace, size_t workspace_bytes,
+               int32_t *status) {
     if (!conf_logits || !sts_temps || !p || !cost || !survivals || !verify_lens || !budget ||
         !tau_theta || !status)
         return DSPARK_ERR_INVALID_ARG;
@@ -1177,12 +1305,19 @@ extern "C" int dspark_plan(const float *conf_logits, const float *sts_temps,
     if (cost->kind != DSPARK_COST_SPS_1D && cost->kind != DSPARK_COST_ADDITIVE)
         return DSPARK_ERR_INVALID_ARG;
     if (cost->n < 1 || !cost->M || !cost->val) return DSPARK_ERR_INVALID_ARG;
-    const int B = p->B, G = p->gamma, N = B * G;
-    if (!workspace || workspace_bytes < dspark_plan_workspace_bytes(B, G) ||
+    if (!workspace || workspace_bytes < dspark_plan_workspace_bytes(p->B, p->gamma) ||
         !aligned(workspace, 256))
         return DSPARK_ERR_WORKSPACE;
+    return DSPARK_OK;
+}
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+// The planner's launches; with pk->on the select path also packs the
+// verify window, and the rank path is followed by the pack kernel.
+int run_plan(const float *conf_logits, const float *sts_temps, const dspark_plan_params *p,
+             const dspark_cost_table *cost, float *survivals, int32_t *verify_lens,
+             int32_t *budget, double *tau_theta, void *workspace, int32_t *status,
+             const PackArgs &pk, cudaStream_t s) {
+    const int B = p->B, G = p->gamma, N = B * G;
     PlanScratch *scratch = static_cast<PlanScratch *>(workspace);
     const int sblocks = (B * 32 + kSurvThreads - 1) / kSurvThreads;
     const bool select = cost->n <= kMaxSelect;  // few candidate budgets: one-CTA select
@@ -1196,6 +1331,7 @@ extern "C" int dspark_plan(const float *conf_logits, const float *sts_temps,
     a.B = B;
     a.gamma = G;
     a.N = N;
+    a.P2 = pow2_at_least(G);
     a.eps = p->survival_eps;
     a.min_len = p->min_verify_len;
     a.max_len = p->max_verify_len;
@@ -1206,6 +1342,7 @@ extern "C" int dspark_plan(const float *conf_logits, const float *sts_temps,
     a.tau_theta = tau_theta;
     a.status = status;
     a.scratch = scratch;
+    a.pk = pk;
     if (select) {
         const int ipt = (N + kSelThreads - 1) / kSelThreads;
         cudaError_t e;
@@ -1220,7 +1357,7 @@ extern "C" int dspark_plan(const float *conf_logits, const float *sts_temps,
                         sizeof(scratch->hcount) + sizeof(scratch->hsum), s);
         return DSPARK_ERR_CUDA;
     }
-    a.P2 = pow2_at_least(G);
+    a.pk.on = false;
     const size_t smem = rank_smem_bytes(B, a.P2);
     if (ensure_smem(reinterpret_cast<const void *>(rank_kernel), (int)rank_smem_max(), 0) != cudaSuccess)
         return DSPARK_ERR_CUDA;
@@ -1229,5 +1366,57 @@ extern "C" int dspark_plan(const float *conf_logits, const float *sts_temps,
     grid = grid < 1 ? 1 : (grid > sm_count() ? sm_count() : grid);
     if (launch_pdl(rank_kernel, dim3(grid), dim3(kRankThreads), smem, s, a) != cudaSuccess)
         return DSPARK_ERR_CUDA;
+    if (pk.on && launch_pack(pk.anchor, pk.draft, pk.prefix, verify_lens, B, G, pk.tiers,
+                             pk.capacity, pk.ids, pk.pos, pk.req, pk.src, pk.cu, pk.totals,
+                             status, s) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
     return DSPARK_OK;
+}
+
+}  // namespace
+
+extern "C" int dspark_plan(const float *conf_logits, const float *sts_temps,
+                           const dspark_plan_params *p, const dspark_cost_table *cost,
+                           float *survivals, int32_t *verify_lens, int32_t *budget,
+                           double *tau_theta, void *workspace, size_t workspace_bytes,
+                           int32_t *status, void *stream) {
+    const int rc = check_plan(conf_logits, sts_temps, p, cost, survivals, verify_lens, budget,
+                              tau_theta, workspace, workspace_bytes, status);
+    if (rc != DSPARK_OK) return rc;
+    PackArgs pk = {};
+    pk.on = false;
+    return run_plan(conf_logits, sts_temps, p, cost, survivals, verify_lens, budget, tau_theta,
+                    workspace, status, pk, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int dspark_plan_pack(const float *conf_logits, const float *sts_temps,
+                                const dspark_plan_params *p, const dspark_cost_table *cost,
+                                float *survivals, int32_t *verify_lens, int32_t *budget,
+                                double *tau_theta, const int32_t *anchor, const int32_t *draft,
+                                const int32_t *prefix_lens, const int32_t *host_tiers,
+                                int32_t n_tiers, int32_t capacity, int32_t *packed_ids,
+                                int32_t *packed_pos, int32_t *packed_req, int32_t *packed_src,
+                                int32_t *cu_seqlens, int32_t *totals, void *workspace,
+                                size_t workspace_bytes, int32_t *status, void *stream) {
+    const int rc = check_plan(conf_logits, sts_temps, p, cost, survivals, verify_lens, budget,
+                              tau_theta, workspace, workspace_bytes, status);
+    if (rc != DSPARK_OK) return rc;
+    if (!anchor || !draft || !prefix_lens || !packed_ids || !packed_pos || !packed_req ||
+        !packed_src || !cu_seqlens || !totals || capacity < 0)
+        return DSPARK_ERR_INVALID_ARG;
+    PackArgs pk = {};
+    if (!load_tiers(host_tiers, n_tiers, &pk.tiers)) return DSPARK_ERR_INVALID_ARG;
+    pk.on = true;
+    pk.anchor = anchor;
+    pk.draft = draft;
+    pk.prefix = prefix_lens;
+    pk.capacity = capacity;
+    pk.ids = packed_ids;
+    pk.pos = packed_pos;
+    pk.req = packed_req;
+    pk.src = packed_src;
+    pk.cu = cu_seqlens;
+    pk.totals = totals;
+    return run_plan(conf_logits, sts_temps, p, cost, survivals, verify_lens, budget, tau_theta,
+                    workspace, status, pk, static_cast<cudaStream_t>(stream));
 }

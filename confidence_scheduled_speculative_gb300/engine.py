@@ -131,6 +131,30 @@ class VerifyStep:
                                cu_seqlens=self.cu_seqlens, totals=self.totals,
                                status=self.status, stream=stream)
 
+    def plan_pack(self, stream=None) -> None:
+        """plan then pack in fewer launches (dspark_plan_pack)."""
+        c = self.cfg
+        api.dspark_plan_pack(self.conf_logits, self.sts_temps, self.anchor, self.draft,
+                             self.prefix_lens, B=c.B, gamma=c.gamma,
+                             survival_eps=c.survival_eps, min_verify_len=c.min_verify_len,
+                             max_verify_len=c.max_verify_len, forced_budget=c.forced_budget,
+                             cost_kind=c.cost_kind, cost_M=self.cost_M, cost_val=self.cost_val,
+                             bias_ms=c.bias_ms, alpha_ms=c.alpha_ms, tiers=c.tiers,
+                             capacity=c.capacity, survivals=self.survivals,
+                             verify_lens=self.verify_lens, budget=self.budget,
+                             tau_theta=self.tau_theta, packed_ids=self.packed_ids,
+                             packed_pos=self.packed_pos, packed_req=self.packed_req,
+                             packed_src=self.packed_src, cu_seqlens=self.cu_seqlens,
+                             totals=self.totals, status=self.status, workspace=self.plan_ws,
+                             stream=stream)
+
+    @property
+    def kernels_per_step(self) -> int:
+        """Kernels one compact step launches: survival + select (with the
+        pack) + argmax + finalize for tables of <= 16 entries, else
+        survival + rank + pack + argmax + finalize."""
+        return 4 if len(self.cfg.cost_M) <= 16 else 5
+
     def greedy_accept(self, logits: torch.Tensor, write_argmax: bool = True, stream=None) -> None:
         c = self.cfg
         api.dspark_greedy_accept(logits, V=c.V, cu_seqlens=self.cu_seqlens, draft=self.draft,
@@ -153,15 +177,15 @@ class VerifyStep:
                               new_seq_lens=self.new_seq_lens, stream=stream)
 
     def compact_step(self, logits: torch.Tensor, stream=None) -> None:
-        """plan -> pack -> greedy accept, enqueued back to back (5 kernels)."""
-        self.plan(stream)
-        self.pack(stream)
+        """plan + pack -> greedy accept, enqueued back to back."""
+        self.plan_pack(stream)
         self.greedy_accept(logits, write_argmax=False, stream=stream)
 
     def bind_compact(self, logits: torch.Tensor, stream=None):
-        """Marshal the three calls of a compact step once; returns
-        (plan, pack, accept) zero-argument callables that re-issue the same
-        C calls with the same device pointers (for tight timing loops)."""
+        """Marshal the calls of a compact step once; returns zero-argument
+        callables (plan_pack, plan, pack, accept) that re-issue the same C
+        calls with the same device pointers (for tight timing loops);
+        plan_pack is plan then pack in fewer launches."""
         lib = api.load()
         c = self.cfg
         s = api._stream(stream)
@@ -180,6 +204,11 @@ class VerifyStep:
                      c.B, c.gamma, self._tiers, len(c.tiers), c.capacity, p(self.packed_ids),
                      p(self.packed_pos), p(self.packed_req), p(self.packed_src),
                      p(self.cu_seqlens), p(self.totals), p(self.status), s)
+        plan_pack_args = (plan_args[:8] + (p(self.anchor), p(self.draft), p(self.prefix_lens),
+                                           self._tiers, len(c.tiers), c.capacity,
+                                           p(self.packed_ids), p(self.packed_pos),
+                                           p(self.packed_req), p(self.packed_src),
+                                           p(self.cu_seqlens), p(self.totals)) + plan_args[8:])
         ptr, ld = api._logits_ptr(logits, c.V)
         acc_args = (ptr, api._dtype_code(logits), ld, c.V, logits.size(0), p(self.cu_seqlens),
                     p(self.draft), p(self.prefix_lens), c.B, c.gamma, None,
@@ -194,7 +223,8 @@ class VerifyStep:
                     raise api.DsparkError(name, rc)
             return run
 
-        return (call(lib.dspark_plan, plan_args, "dspark_plan"),
+        return (call(lib.dspark_plan_pack, plan_pack_args, "dspark_plan_pack"),
+                call(lib.dspark_plan, plan_args, "dspark_plan"),
                 call(lib.dspark_pack_verify, pack_args, "dspark_pack_verify"),
                 call(lib.dspark_greedy_accept, acc_args, "dspark_greedy_accept"))
 
@@ -261,8 +291,7 @@ def run_host(vs: VerifyStep, io: HostStepIO, host_logits: torch.Tensor,
         vs.draft.copy_(io.draft, non_blocking=True)
         vs.prefix_lens.copy_(io.prefix_lens, non_blocking=True)
         vs.status.zero_()
-        vs.plan(s)
-        vs.pack(s)
+        vs.plan_pack(s)
         io.totals.copy_(vs.totals, non_blocking=True)
         s.synchronize()  # the host needs the packed total to run the verify window
         rows = int(io.totals[0])

@@ -169,6 +169,24 @@ DSPARK_API int dspark_pack_verify(const int32_t *anchor, const int32_t *draft, c
                        int32_t *packed_src, int32_t *cu_seqlens, int32_t *totals,
                        int32_t *status, void *stream);
 
+/* dspark_plan followed by dspark_pack_verify on the planner's verify_lens,
+ * in fewer launches: for cost tables of at most 16 entries the planner's
+ * last kernel also packs the window (one launch and one dependency wait
+ * fewer per step); denser tables run the two calls' kernels back to back.
+ * Arguments and outputs are those of the two calls (the planner's
+ * workspace, which must be zero-filled once, serves both); the pages'
+ * planner and pack are the same two steps ([AVS] §一, §五-§六; [ROUND]
+ * §三).  Errors: those of dspark_plan, then of dspark_pack_verify's
+ * arguments (checked before anything is launched). */
+DSPARK_API int dspark_plan_pack(const float *conf_logits, const float *sts_temps,
+                     const dspark_plan_params *p /* host */, const dspark_cost_table *cost /* host */,
+                     float *survivals, int32_t *verify_lens, int32_t *budget, double *tau_theta,
+                     const int32_t *anchor, const int32_t *draft, const int32_t *prefix_lens,
+                     const int32_t *host_tiers /* host */, int32_t n_tiers, int32_t capacity,
+                     int32_t *packed_ids, int32_t *packed_pos, int32_t *packed_req,
+                     int32_t *packed_src, int32_t *cu_seqlens, int32_t *totals,
+                     void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
+
 /* ---------------------------------------------------------------- accept */
 
 #define DSPARK_DTYPE_BF16 0

@@ -153,3 +153,28 @@ def test_static_accept_rejects_rows_beyond_its_maximum(lib):
              FAKE, None, FAKE, FAKE, None) == -4
     assert f(FAKE, 0, ctypes.c_int64(1024), 1000, -1, FAKE, FAKE, FAKE, 4, 4, None, FAKE, FAKE,
              FAKE, None, FAKE, FAKE, None) == -1
+
+
+def test_plan_pack_argument_checks(lib):
+    f = lib.dspark_plan_pack
+    f.restype = ctypes.c_int
+    good = dict(B=4, gamma=4, eps=1e-4, min_len=1, max_len=5, forced=-1)
+    cost = Cost(1, 3, FAKE.value, FAKE.value, 0.0, 0.0)
+    lib.dspark_plan_workspace_bytes.restype = ctypes.c_size_t
+    need = lib.dspark_plan_workspace_bytes(4, 4)
+    tiers = (ctypes.c_int32 * 3)(8, 16, 32)
+    bad_tiers = (ctypes.c_int32 * 3)(8, 4, 32)
+
+    def call(p=good, anchor=FAKE, t=tiers, n_t=3, cap=16, ws=FAKE, wsb=need, cu=FAKE):
+        return f(FAKE, FAKE, ctypes.byref(Params(**p)), ctypes.byref(cost), FAKE, FAKE, FAKE, FAKE,
+                 anchor, FAKE, FAKE, t, n_t, cap, FAKE, FAKE, FAKE, FAKE, cu, FAKE, ws,
+                 ctypes.c_size_t(wsb), FAKE, None)
+
+    assert call(p={**good, "gamma": 32}) == -4       # planner checks first
+    assert call(ws=None) == -2
+    assert call(wsb=need - 256) == -2
+    assert call(anchor=None) == -1                   # then the pack's
+    assert call(cu=None) == -1
+    assert call(cap=-1) == -1
+    assert call(t=bad_tiers) == -1
+    assert call(n_t=65) == -1

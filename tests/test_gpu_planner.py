@@ -306,3 +306,106 @@ def test_pack_page_layout_on_gpu(dev, orc):
     assert list(g["ids"][:7]) == [100, 101, 200, 300, 301, 302, 303]
     assert list(g["totals"]) == [7, 40]
     assert np.all(g["req"][7:40] == -1) and np.all(g["req"][40:] == -9)
+
+
+# ------------------------------------------------- fused plan + pack (one entry point)
+
+def _fused(dev, P, anchor, prefix, draft, tiers, cap, sentinel=-9):
+    from confidence_scheduled_speculative_gb300 import api
+    B, g = P["B"], P["gamma"]
+    i32 = dict(dtype=torch.int32, device=dev)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    out = dict(survivals=torch.zeros((B, g), dtype=torch.float32, device=dev),
+               verify_lens=torch.zeros(B, **i32), budget=torch.zeros(1, **i32),
+               tau_theta=torch.zeros(2, dtype=torch.float64, device=dev),
+               status=torch.zeros(1, **i32))
+    pk = {k: torch.full((max(cap, 1),), sentinel, **i32) for k in ("ids", "pos", "req", "src")}
+    cu = torch.full((B + 1,), sentinel, **i32)
+    totals = torch.full((2,), sentinel, **i32)
+    ws = api.workspace(api.dspark_plan_workspace_bytes(B, g), dev)
+    api.dspark_plan_pack(torch.from_numpy(P["z"]).to(dev), torch.from_numpy(P["T"]).to(dev),
+                         t(anchor), t(draft), t(prefix), B=B, gamma=g, survival_eps=P["eps"],
+                         min_verify_len=P["min_len"], max_verify_len=P["max_len"],
+                         forced_budget=P["forced"], cost_kind=P["kind"],
+                         cost_M=torch.from_numpy(P["M"]).to(dev),
+                         cost_val=torch.from_numpy(P["val"]).to(dev), bias_ms=P["bias"],
+                         alpha_ms=P["alpha"], tiers=tiers, capacity=cap,
+                         packed_ids=pk["ids"], packed_pos=pk["pos"], packed_req=pk["req"],
+                         packed_src=pk["src"], cu_seqlens=cu, totals=totals, workspace=ws, **out)
+    torch.cuda.synchronize()
+    res = {k: v.cpu().numpy() for k, v in out.items()}
+    res.update({k: v.cpu().numpy()[:cap] for k, v in pk.items()})
+    res.update(cu_seqlens=cu.cpu().numpy(), totals=totals.cpu().numpy())
+    return res
+
+
+def _pack_inputs(rng, B, g, total_hint):
+    anchor = rng.integers(0, 1 << 20, B).astype(np.int32)
+    draft = rng.integers(0, 1 << 20, (B, g)).astype(np.int32)
+    prefix = rng.integers(1, 8192, B).astype(np.int32)
+    mode = rng.integers(0, 4)
+    if mode == 0:
+        tiers = []
+    elif mode == 1:  # every tier below the total: flagged, padded = total
+        tiers = [1, 2]
+    else:
+        tiers = sorted(set(int(x) for x in rng.integers(1, 2 * total_hint + 3, size=int(rng.integers(1, 8)))))
+    cap = int(rng.integers(0, 2 * total_hint + 4)) if rng.random() < 0.3 else 2 * total_hint + 8
+    return anchor, prefix, draft, tiers, cap
+
+
+@pytest.mark.parametrize("seed", range(80))
+def test_plan_pack_fused_random(dev, orc, seed):
+    """dspark_plan_pack equals the oracle's planner followed by its pack,
+    including untouched rows past the window, capacity overflow and tier
+    lists with no tier above the total; tables of more than 16 entries take
+    the separate kernels."""
+    rng = np.random.default_rng(90000 + seed)
+    P = _random_problem(rng)
+    if seed % 5 == 4:  # a dense 1-D table: rank path, then the pack kernel
+        B, g = P["B"], P["gamma"]
+        P["kind"] = 0
+        P["M"] = np.arange(B, B + max(B * g + 2, 40), dtype=np.int32)
+        P["val"] = 1.0 / (1e-3 + 2e-6 * P["M"])
+    B, g = P["B"], P["gamma"]
+    anchor, prefix, draft, tiers, cap = _pack_inputs(rng, B, g, B * (g + 1))
+    got = _fused(dev, P, anchor, prefix, draft, tiers, cap)
+    ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"], P["kind"],
+                   P["M"], P["val"], P["bias"], P["alpha"])
+    if not compare_plan(f"fused/{seed}", got, ref, B, g, P["min_len"]):
+        return  # a logged near tie: the pack below would see other lengths
+    pr = orc.pack(anchor, draft, prefix, ref.verify_lens, tiers, cap, sentinel=-9)
+    np.testing.assert_array_equal(got["cu_seqlens"], pr.cu_seqlens)
+    assert list(got["totals"]) == [pr.total, pr.padded]
+    for k in ("ids", "pos", "req", "src"):
+        np.testing.assert_array_equal(got[k], pr[k][:cap], err_msg=k)
+    assert int(got["status"][0]) == (ref.status | pr.status)
+
+
+@pytest.mark.parametrize("name,seed,forced", CASES)
+def test_plan_pack_fused_matches_separate_calls(dev, name, seed, forced):
+    """On every workload the fused call gives the two calls' outputs bit for bit."""
+    from confidence_scheduled_speculative_gb300.engine import StepConfig, VerifyStep
+    step = wl.make_step(wl.WORKLOADS[name], seed=seed)
+    cfg = StepConfig.from_step(step)
+    if forced is not None:
+        cfg.forced_budget = forced
+    res = []
+    for fused in (False, True):
+        vs = VerifyStep(cfg, dev)
+        vs.load_inputs(step)
+        for t in (vs.packed_ids, vs.packed_pos, vs.packed_req, vs.packed_src):
+            t.fill_(-3)
+        vs.status.zero_()
+        if fused:
+            vs.plan_pack()
+        else:
+            vs.plan()
+            vs.pack()
+        torch.cuda.synchronize()
+        r = vs.result()
+        r["packed_all"] = np.stack([t.cpu().numpy() for t in (vs.packed_ids, vs.packed_pos,
+                                                                vs.packed_req, vs.packed_src)])
+        res.append(r)
+    for k in res[0]:
+        np.testing.assert_array_equal(np.asarray(res[1][k]), np.asarray(res[0][k]), err_msg=k)
