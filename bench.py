@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--no-cap", action="store_true")
     ap.add_argument("--separate-plan-pack", action="store_true",
                     help="issue dspark_plan and dspark_pack_verify instead of dspark_plan_pack")
+    ap.add_argument("--event-every", type=int, default=16,
+                    help="bracket the accept call with events on every n-th timed step")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
     return ap.parse_args()
 
@@ -309,11 +311,17 @@ def run_ours(args):
         one_step()
     torch.cuda.synchronize()
 
-    # ---- timed region: K steps, accept bracketed by events on its stream
+    # ---- timed region: K steps.  An event at every step boundary (between
+    # an accept and the next survival kernel, which is not launched early
+    # anyway); every event_every-th step also brackets its accept call, which
+    # keeps that call from launching before the planner finishes -- those
+    # steps give the accept duration and are left out of the step percentiles.
     K = max(1, args.steps)
+    every = max(1, args.event_every)
+    sampled = list(range(0, K, every))
     ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_a = {i: torch.cuda.Event(enable_timing=True) for i in sampled}
+    ev_b = {i: torch.cuda.Event(enable_timing=True) for i in sampled}
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     uuid = None
     try:
@@ -329,18 +337,23 @@ def run_ours(args):
     for i in range(K):
         ev_s[i].record(stream)
         plan_pack_fn()
-        ev_a[i].record(stream)
-        acc_fn()
-        ev_b[i].record(stream)
+        if i % every == 0:
+            ev_a[i].record(stream)
+            acc_fn()
+            ev_b[i].record(stream)
+        else:
+            acc_fn()
     t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
-    accept_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
-    step_us = np.array([ev_s[i].elapsed_time(ev_s[i + 1]) for i in range(K - 1)] +
-                       [ev_s[K - 1].elapsed_time(t_end)]) * 1e3
+    accept_ms = [ev_a[i].elapsed_time(ev_b[i]) for i in sampled]
+    step_all = np.array([ev_s[i].elapsed_time(ev_s[i + 1]) for i in range(K - 1)] +
+                        [ev_s[K - 1].elapsed_time(t_end)]) * 1e3
+    clean = [i for i in range(K) if i % every != 0] or list(range(K))
+    step_us = step_all[clean]
     if world > 1:
         t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -366,6 +379,16 @@ def run_ours(args):
     torch.cuda.synchronize()
     br = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3]),
                     e[3].elapsed_time(e[4])] for e in evs]) * 1e3
+    # accept calls back to back (each launched while the previous one runs):
+    # the accept's own duration without the launch gap a bracketing event adds
+    n_acc = min(K, 200)
+    b2b = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    b2b[0].record(stream)
+    for _ in range(n_acc):
+        acc_fn()
+    b2b[1].record(stream)
+    torch.cuda.synchronize()
+    acc_b2b_us = b2b[0].elapsed_time(b2b[1]) * 1e3 / n_acc
 
     # ---- cap-accept over the full strided block (secondary)
     cap = None
@@ -452,7 +475,7 @@ def run_ours(args):
                 "d2h_bytes_per_step": io.d2h_output_bytes(), "steps": n_e,
                 "matches_device_path": bool(e2e_ok)},
         "cpu_baseline": cpu,
-        "gpu_launches": (5 if args.separate_plan_pack else vs.kernels_per_step) * K,
+        "gpu_launches": vs.kernels_per_step(args.separate_plan_pack) * K,
         "clocks": clocks,
         "step_us": {"p10": float(np.percentile(step_us, 10)),
                     "p50": float(np.percentile(step_us, 50)),
@@ -461,7 +484,9 @@ def run_ours(args):
                          "accept": float(np.median(br[:, 1])),
                          "plan_alone": float(np.median(br[:, 2])),
                          "pack_alone": float(np.median(br[:, 3])),
-                         "accept_timed_mean": acc_us, "step_timed_mean": 1e3 * ms_per_step},
+                         "accept_timed_mean": acc_us, "step_timed_mean": 1e3 * ms_per_step,
+                         "accept_back_to_back": acc_b2b_us,
+                         "accept_back_to_back_gbs": accept_bytes / (acc_b2b_us * 1e-6) / 1e9},
         "cap_accept": cap,
         "status": status,
     }

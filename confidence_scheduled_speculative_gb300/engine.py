@@ -148,12 +148,12 @@ class VerifyStep:
                              totals=self.totals, status=self.status, workspace=self.plan_ws,
                              stream=stream)
 
-    @property
-    def kernels_per_step(self) -> int:
-        """Kernels one compact step launches: survival + select (with the
-        pack) + argmax + finalize for tables of <= 16 entries, else
-        survival + rank + pack + argmax + finalize."""
-        return 4 if len(self.cfg.cost_M) <= 16 else 5
+    def kernels_per_step(self, separate_plan_pack: bool = False) -> int:
+        """Kernels one compact step launches: survival + select (the pack
+        inside) for tables of <= 16 entries, else survival + rank + pack
+        (separate calls add the pack kernel); then argmax + finalize."""
+        select = len(self.cfg.cost_M) <= 16
+        return (3 if (separate_plan_pack or not select) else 2) + 2
 
     def greedy_accept(self, logits: torch.Tensor, write_argmax: bool = True, stream=None) -> None:
         c = self.cfg

@@ -26,7 +26,9 @@ def dev():
     return require_gpu()
 
 
-def _gpu_greedy(dev, logits_dev, V, cu, draft, prefix, max_rows=None):
+def _gpu_greedy(dev, logits_dev, V, cu, draft, prefix, max_rows=None, with_argmax=True, ws=None):
+    """Compact greedy accept through the C ABI, with or without the per-row
+    argmax output."""
     from confidence_scheduled_speculative_gb300 import api
     B, g = draft.shape
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
@@ -37,13 +39,14 @@ def _gpu_greedy(dev, logits_dev, V, cu, draft, prefix, max_rows=None):
              out_tokens=torch.full((B, g + 1), -5, **i32))
     am = torch.full((max(rows_cap, 1),), -5, **i32)
     st = torch.zeros(1, **i32)
-    ws = api.workspace(api.dspark_accept_workspace_bytes(rows_cap, V), dev)
+    if ws is None:
+        ws = api.workspace(api.dspark_accept_workspace_bytes(rows_cap, V), dev)
     api.dspark_greedy_accept(logits_dev, V=V, cu_seqlens=t(cu), draft=t(draft),
                              prefix_lens=t(prefix), B=B, gamma=g, workspace=ws, status=st,
-                             argmax=am, max_rows=rows_cap, **o)
+                             argmax=am if with_argmax else None, max_rows=rows_cap, **o)
     torch.cuda.synchronize()
     res = {k: v.cpu().numpy() for k, v in o.items()}
-    res["argmax"] = am.cpu().numpy()
+    res["argmax"] = am.cpu().numpy() if with_argmax else None
     res["status"] = int(st.cpu()[0])
     return res
 
@@ -72,7 +75,8 @@ def _gpu_cap(dev, logits_dev, V, lens, draft, prefix):
 
 
 def _cmp_greedy(tag, g, r, rows):
-    np.testing.assert_array_equal(g["argmax"][:rows], r.argmax[:rows], err_msg=f"{tag} argmax")
+    if g["argmax"] is not None:
+        np.testing.assert_array_equal(g["argmax"][:rows], r.argmax[:rows], err_msg=f"{tag} argmax")
     for k in OUT_KEYS:
         np.testing.assert_array_equal(g[k], r[k], err_msg=f"{tag} {k}")
     assert g["status"] == r.status, (tag, g["status"], r.status)
@@ -94,8 +98,9 @@ def _plant(rng, x, rows_peaks, V):
             x[row, col] = 9.0
 
 
+@pytest.mark.parametrize("with_argmax", [True, False], ids=["argmax-out", "no-argmax-out"])
 @pytest.mark.parametrize("seed", range(40))
-def test_greedy_random_small(dev, orc, seed):
+def test_greedy_random_small(dev, orc, seed, with_argmax):
     rng = np.random.default_rng(123000 + seed)
     dtype = "fp32" if seed % 2 else "bf16"
     V = int(rng.choice([1024, 1001, 517, 4096, 33, 8, 1]))
@@ -115,12 +120,13 @@ def test_greedy_random_small(dev, orc, seed):
                 peaks.append((int(cu[r]) + j, int(draft[r, j])))
     _plant(rng, x, peaks, V)
     prefix = rng.integers(0, 9000, size=B).astype(np.int32)
-    g = _gpu_greedy(dev, to_dev_logits(x, dev), V, cu, draft, prefix)
+    g = _gpu_greedy(dev, to_dev_logits(x, dev), V, cu, draft, prefix, with_argmax=with_argmax)
     r = orc.greedy_accept(np.ascontiguousarray(x), V, cu, draft, prefix)
     _cmp_greedy(f"small/{seed}", g, r, rows)
 
 
-def test_argmax_edge_rows(dev, orc):
+@pytest.mark.parametrize("with_argmax", [True, False], ids=["argmax-out", "no-argmax-out"])
+def test_argmax_edge_rows(dev, orc, with_argmax):
     rng = np.random.default_rng(77)
     V, gamma = 129280, 3
     rows = 12
@@ -151,14 +157,17 @@ def test_argmax_edge_rows(dev, orc):
     prefix = np.zeros(3, np.int32)
     for dtype in ("fp32", "bf16"):
         xx = x if dtype == "fp32" else wl.to_bf16_bits(x)
-        g = _gpu_greedy(dev, to_dev_logits(xx, dev), V, cu, draft, prefix)
+        g = _gpu_greedy(dev, to_dev_logits(xx, dev), V, cu, draft, prefix,
+                        with_argmax=with_argmax)
         r = orc.greedy_accept(np.ascontiguousarray(xx), V, cu, draft, prefix)
         _cmp_greedy(f"edge/{dtype}", g, r, rows)
-        assert g["argmax"][2] == 5000 and g["argmax"][5] == 16 and g["argmax"][4] == 99
+        if with_argmax:
+            assert g["argmax"][2] == 5000 and g["argmax"][5] == 16 and g["argmax"][4] == 99
         assert g["status"] & 4
 
 
-def test_unaligned_and_capacity(dev, orc):
+@pytest.mark.parametrize("with_argmax", [True, False], ids=["argmax-out", "no-argmax-out"])
+def test_unaligned_and_capacity(dev, orc, with_argmax):
     rng = np.random.default_rng(78)
     V, gamma, B = 3001, 5, 6
     lens = np.array([6, 1, 3, 6, 2, 4])
@@ -171,20 +180,28 @@ def test_unaligned_and_capacity(dev, orc):
     dev_big = to_dev_logits(big, dev)
     view = dev_big.view(-1)[1:1 + cu[-1] * (V + 1)].view(cu[-1], V + 1)
     host_view = big.reshape(-1)[1:1 + cu[-1] * (V + 1)].reshape(cu[-1], V + 1)
-    g = _gpu_greedy(dev, view, V, cu, draft, prefix)
+    kw = dict(with_argmax=with_argmax)
+    g = _gpu_greedy(dev, view, V, cu, draft, prefix, **kw)
     r = orc.greedy_accept(np.ascontiguousarray(host_view), V, cu, draft, prefix)
     _cmp_greedy("unaligned", g, r, int(cu[-1]))
     # fewer rows available than cu[B]: CAPACITY, requests past them are bad ranges
-    g2 = _gpu_greedy(dev, view, V, cu, draft, prefix, max_rows=10)
+    g2 = _gpu_greedy(dev, view, V, cu, draft, prefix, max_rows=10, **kw)
     r2 = orc.greedy_accept(np.ascontiguousarray(host_view), V, cu, draft, prefix, max_rows=10)
     _cmp_greedy("capacity", g2, r2, 10)
     assert g2["status"] & 1 and g2["status"] & 16
     # a decreasing cu_seqlens entry is a bad range
     cu_bad = cu.copy()
     cu_bad[3] = cu_bad[2] - 1
-    g3 = _gpu_greedy(dev, view, V, cu_bad, draft, prefix)
+    g3 = _gpu_greedy(dev, view, V, cu_bad, draft, prefix, **kw)
     r3 = orc.greedy_accept(np.ascontiguousarray(host_view), V, cu_bad, draft, prefix)
     _cmp_greedy("bad-cu", g3, r3, int(cu_bad[-1]))
+    # negative start, empty request, and a request longer than gamma + 1
+    for i, cu_b in enumerate(([-1, 6, 7, 10, 16, 18, 22], [0, 6, 6, 9, 15, 17, 21],
+                              [0, 6, 7, 10, 20, 21, 22])):
+        cu_b = np.array(cu_b, np.int32)
+        g4 = _gpu_greedy(dev, view, V, cu_b, draft, prefix, **kw)
+        r4 = orc.greedy_accept(np.ascontiguousarray(host_view), V, cu_b, draft, prefix)
+        _cmp_greedy(f"bad-cu/{i}", g4, r4, max(int(cu_b[-1]), 0))
 
 
 @pytest.mark.parametrize("seed", range(16))
@@ -243,6 +260,14 @@ def test_step_workloads_full_size(dev, orc, name):
     for k in OUT_KEYS:
         np.testing.assert_array_equal(gg[k], rg[k], err_msg=k)
     assert int(gg["status"][0]) == rg.status == 0
+    # the benchmark's call: no per-row argmax output
+    for t in (vs.num_accepted, vs.bonus, vs.commit_lens, vs.new_seq_lens, vs.out_tokens):
+        t.fill_(-9)
+    vs.greedy_accept(compact_dev, write_argmax=False)
+    gf = vs.result()
+    for k in OUT_KEYS:
+        np.testing.assert_array_equal(gf[k], rg[k], err_msg="no argmax out: " + k)
+    assert int(gf["status"][0]) == 0
     # cap-accept over the strided rows commits the same, and reports the ceiling
     vs.status.zero_()
     vs.cap_accept(strided_dev)
