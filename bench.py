@@ -55,6 +55,7 @@ def parse():
     ap.add_argument("--no-cap", action="store_true")
     ap.add_argument("--separate-plan-pack", action="store_true",
                     help="issue dspark_plan and dspark_pack_verify instead of dspark_plan_pack")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay")
     ap.add_argument("--event-every", type=int, default=16,
                     help="bracket the accept call with events on every n-th timed step")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
@@ -390,6 +391,39 @@ def run_ours(args):
     torch.cuda.synchronize()
     acc_b2b_us = b2b[0].elapsed_time(b2b[1]) * 1e3 / n_acc
 
+    # ---- the same step replayed from a CUDA graph (secondary): 16 steps per
+    # graph, captured on a side stream with the calls bound to it
+    graph = None
+    if not args.no_graph:
+        try:
+            gs = torch.cuda.Stream()
+            bound = vs.bind_compact(compact, stream=gs)
+            calls = bound[1:] if args.separate_plan_pack else (bound[0], bound[3])
+            per_graph = 16
+            cg = torch.cuda.CUDAGraph()
+            gs.wait_stream(stream)
+            with torch.cuda.graph(cg, stream=gs):
+                for _ in range(per_graph):
+                    for fn in calls:
+                        fn()
+            torch.cuda.synchronize()
+            for _ in range(3):
+                cg.replay()
+            torch.cuda.synchronize()
+            reps = max(1, K // per_graph)
+            ge = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            ge[0].record(torch.cuda.current_stream())
+            for _ in range(reps):
+                cg.replay()
+            ge[1].record(torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            g_ms = ge[0].elapsed_time(ge[1])
+            graph = {"value": world * reps * per_graph / (g_ms / 1e3), "unit": UNIT,
+                     "steps": reps * per_graph, "steps_per_graph": per_graph,
+                     "us_per_step": g_ms * 1e3 / (reps * per_graph)}
+        except Exception as e:  # report, do not fail the run
+            graph = {"error": f"{type(e).__name__}: {e}"[:200]}
+
     # ---- cap-accept over the full strided block (secondary)
     cap = None
     if not args.no_cap:
@@ -487,6 +521,7 @@ def run_ours(args):
                          "accept_timed_mean": acc_us, "step_timed_mean": 1e3 * ms_per_step,
                          "accept_back_to_back": acc_b2b_us,
                          "accept_back_to_back_gbs": accept_bytes / (acc_b2b_us * 1e-6) / 1e9},
+        "cuda_graph": graph,
         "cap_accept": cap,
         "status": status,
     }
