@@ -424,6 +424,32 @@ def run_ours(args):
         except Exception as e:  # report, do not fail the run
             graph = {"error": f"{type(e).__name__}: {e}"[:200]}
 
+    # ---- ScatterCompactToStrided of the packed logits (secondary): read and
+    # write total x V x 2 bytes; calls back to back
+    scat = None
+    if not args.no_cap:
+        from confidence_scheduled_speculative_gb300 import api as _api
+        scat_dst = torch.empty_like(strided_dev)
+        st_s = torch.zeros(1, dtype=torch.int32, device=dev)
+        for _ in range(3):
+            _api.dspark_scatter_compact_to_strided(compact, vs.packed_src, vs.totals, scat_dst,
+                                                   status=st_s)
+        n_s = min(K, 200)
+        se = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        se[0].record(stream)
+        for _ in range(n_s):
+            _api.dspark_scatter_compact_to_strided(compact, vs.packed_src, vs.totals, scat_dst,
+                                                   status=st_s)
+        se[1].record(stream)
+        torch.cuda.synchronize()
+        s_us = se[0].elapsed_time(se[1]) * 1e3 / n_s
+        s_bytes = 2 * total * w.V * w.elem_bytes
+        scat = {"us": s_us, "rows": total, "bytes": s_bytes,
+                "gbs": s_bytes / (s_us * 1e-6) / 1e9,
+                "frac": s_bytes / (s_us * 1e-6) / 1e9 / load_peaks()[0],
+                "status": int(st_s.item())}
+        del scat_dst
+
     # ---- cap-accept over the full strided block (secondary)
     cap = None
     if not args.no_cap:
@@ -522,6 +548,7 @@ def run_ours(args):
                          "accept_back_to_back": acc_b2b_us,
                          "accept_back_to_back_gbs": accept_bytes / (acc_b2b_us * 1e-6) / 1e9},
         "cuda_graph": graph,
+        "scatter_compact_to_strided": scat,
         "cap_accept": cap,
         "status": status,
     }

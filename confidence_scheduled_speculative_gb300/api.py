@@ -76,6 +76,8 @@ _SIGS = {
                                         ctypes.POINTER(dspark_cost_table), _VP, _VP, _VP, _VP,
                                         _VP, _VP, _VP, ctypes.POINTER(ctypes.c_int32), _I32, _I32,
                                         _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
+    "dspark_scatter_compact_to_strided": (ctypes.c_int, [_VP, _I64, _I32, _I32, _VP, _VP, _I32,
+                                                         _VP, _I64, _I32, _VP, _VP]),
     "dspark_accept_workspace_bytes": (_SZ, [_I32, _I32]),
     "dspark_greedy_accept": (ctypes.c_int, [_VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP, _I32,
                                             _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP,
@@ -215,6 +217,24 @@ def dspark_plan_pack(conf_logits, sts_temps, anchor, draft, prefix_lens, *, B, g
         _p(totals, torch.int32, "totals"), _p(workspace), ws_bytes,
         _p(status, torch.int32, "status"), _stream(stream))
     _check("dspark_plan_pack", rc)
+
+
+def dspark_scatter_compact_to_strided(src, packed_src, totals, dst, *, status,
+                                      stream=None) -> None:
+    """Copy packed row i < totals[0] of ``src`` [max_rows, width] to row
+    packed_src[i] of ``dst`` [B*(gamma+1), >= width] (2-D, same dtype:
+    bfloat16, float16 or float32, unit inner stride)."""
+    for name, t in (("src", src), ("dst", dst)):
+        if not t.is_cuda or t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError(f"{name}: expected a 2-D CUDA tensor with unit inner stride")
+    if src.dtype != dst.dtype or src.element_size() not in (2, 4):
+        raise ValueError("src and dst: same dtype of 2 or 4 bytes")
+    rc = load().dspark_scatter_compact_to_strided(
+        src.data_ptr(), src.stride(0), src.size(1), src.element_size(),
+        _p(packed_src, torch.int32, "packed_src"), _p(totals, torch.int32, "totals"),
+        src.size(0), dst.data_ptr(), dst.stride(0), dst.size(0),
+        _p(status, torch.int32, "status"), _stream(stream))
+    _check("dspark_scatter_compact_to_strided", rc)
 
 
 def _dtype_code(t: torch.Tensor) -> int:

@@ -59,6 +59,8 @@ extern "C" {
 #define DSPARK_STATUS_BAD_LEN     16 /* a verify length / cu_seqlens range outside [1, gamma+1] */
 #define DSPARK_STATUS_BAD_COST    32 /* cost table not ascending, or a non-positive / non-finite cost used */
 #define DSPARK_STATUS_INFEASIBLE  64 /* no budget in range: budget set to 0 */
+#define DSPARK_STATUS_BAD_INDEX   128 /* a packed row's strided destination outside the buffer */
+#define DSPARK_STATUS_TIMEOUT     256 /* a kernel's bounded wait gave up (its outputs are incomplete) */
 
 /* Message for a DSPARK_ERR_* code (static string). */
 DSPARK_API const char *dspark_strerror(int code);
@@ -186,6 +188,30 @@ DSPARK_API int dspark_plan_pack(const float *conf_logits, const float *sts_temps
                      int32_t *packed_ids, int32_t *packed_pos, int32_t *packed_req,
                      int32_t *packed_src, int32_t *cu_seqlens, int32_t *totals,
                      void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
+
+/* ScatterCompactToStrided ([ROUND] §三): after the target forward over the
+ * compact verify rows, copy packed row i (i < totals[0]) to row
+ * packed_src[i] = r*(gamma+1) + j of the [B x (gamma+1)] strided buffer, so
+ * that the accept can address rows by fixed position (cap-accept); pad rows
+ * and the strided rows no request selected are left untouched.
+ *   src          device [max_rows, ld_src] rows of `width` elements of
+ *                elem_bytes (2: bf16 logits or hidden states, 4: fp32)
+ *   packed_src   device [max_rows] int32, the pack's output
+ *   totals       device [>= 1] int32, totals[0] = real packed rows (clamped
+ *                to [0, max_rows])
+ *   dst          device [dst_rows, ld_dst], strides in elements
+ * TMA bulk copies (16 KB segments staged in shared memory) when both
+ * buffers, both strides and the row size are 16-byte multiples, else 2-byte
+ * copies.  A destination outside [0, dst_rows) is skipped and flagged
+ * DSPARK_STATUS_BAD_INDEX; DSPARK_STATUS_TIMEOUT if a copy did not complete
+ * within 200 ms.
+ * Errors: INVALID_ARG (null pointer, elem_bytes not 2 or 4, width < 1, a
+ * stride below width, negative row counts); CUDA. */
+DSPARK_API int dspark_scatter_compact_to_strided(const void *src, int64_t ld_src, int32_t width,
+                                      int32_t elem_bytes, const int32_t *packed_src,
+                                      const int32_t *totals, int32_t max_rows, void *dst,
+                                      int64_t ld_dst, int32_t dst_rows, int32_t *status,
+                                      void *stream);
 
 /* ---------------------------------------------------------------- accept */
 

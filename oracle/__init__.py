@@ -32,6 +32,7 @@ ST_BAD_INPUT = 8
 ST_BAD_LEN = 16
 ST_BAD_COST = 32
 ST_INFEASIBLE = 64
+ST_BAD_INDEX = 128
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +78,9 @@ def lib():
             L.orc_pack.argtypes = [i32p, i32p, i32p, i32p, ci, ci, i32p, ci, ci, i32p, i32p, i32p,
                                    i32p, i32p, i32p, i32p]
             L.orc_pack.restype = None
+            u8p = ctypes.POINTER(ctypes.c_uint8)
+            L.orc_scatter_rows.argtypes = [u8p, cl, cl, i32p, ci, ci, u8p, cl, ci, i32p]
+            L.orc_scatter_rows.restype = None
             L.orc_argmax_rows_f32.argtypes = [f32p, cl, ci, ci, i32p, i32p]
             L.orc_argmax_rows_f32.restype = None
             L.orc_argmax_rows_bf16.argtypes = [u16p, cl, ci, ci, i32p, i32p]
@@ -197,6 +201,23 @@ def pack(anchor, draft, prefix, lens, tiers, capacity, sentinel=-7):
                    _ptr(st, ctypes.c_int32))
     return PlanResult(ids=outs[0], pos=outs[1], req=outs[2], src=outs[3], cu_seqlens=cu,
                       total=int(totals[0]), padded=int(totals[1]), status=int(st[0]))
+
+
+def scatter_rows(src, src_of, total, dst, max_rows=None):
+    """ScatterCompactToStrided: returns (a copy of dst with packed row i <
+    total written at row src_of[i], status).  src and dst are 2-D arrays of
+    the same dtype; their row widths may differ, the copied width is src's."""
+    src = np.ascontiguousarray(src)
+    out = np.array(dst, copy=True, order="C")
+    src_of = _c(src_of, np.int32)
+    max_rows = src.shape[0] if max_rows is None else max_rows
+    st = np.zeros(1, np.int32)
+    u8 = ctypes.POINTER(ctypes.c_uint8)
+    lib().orc_scatter_rows(src.ctypes.data_as(u8), src.strides[0], src.shape[1] * src.itemsize,
+                           _ptr(src_of, ctypes.c_int32), int(total), int(max_rows),
+                           out.ctypes.data_as(u8), out.strides[0], out.shape[0],
+                           _ptr(st, ctypes.c_int32))
+    return out, int(st[0])
 
 
 # ------------------------------------------------------------------- accept

@@ -1,6 +1,7 @@
 /*
  * dspark_oracle.c -- plain, slow, single-threaded CPU oracle for the DSpark
- * verify planner, ragged verify pack and greedy / cap-accept.
+ * verify planner, ragged verify pack, greedy / cap-accept and the scatter of
+ * compact rows back to the strided layout.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
  * benchmark's CPU-baseline leg load this file.  The product path (the CUDA
@@ -61,6 +62,7 @@
 #define ORC_ST_BAD_LEN     16
 #define ORC_ST_BAD_COST    32
 #define ORC_ST_INFEASIBLE  64
+#define ORC_ST_BAD_INDEX   128
 
 /* ------------------------------------------------------------------ STS */
 
@@ -431,4 +433,26 @@ void orc_cap_finalize(const int32_t *am, const int32_t *lens, const int32_t *dra
     }
     totals[0] = sum_commit;
     totals[1] = sum_ceiling;
+}
+
+
+/* ScatterCompactToStrided ([ROUND] §三): after the target forward, packed
+ * row i (i < min(total, max_rows)) goes back to row src_of[i] =
+ * r*(gamma+1) + j of the [B x (gamma+1)] strided layout; every other strided
+ * row is left as it was.  Rows are row_bytes bytes, strides in bytes.  A
+ * destination outside [0, dst_rows) is skipped and flagged. */
+void orc_scatter_rows(const unsigned char *src, long long ld_src, long long row_bytes,
+                      const int32_t *src_of, int total, int max_rows, unsigned char *dst,
+                      long long ld_dst, int dst_rows, int *status)
+{
+    int rows = total < 0 ? 0 : (total > max_rows ? max_rows : total);
+    for (int i = 0; i < rows; ++i) {
+        int d = src_of[i];
+        if (d < 0 || d >= dst_rows) {
+            *status |= ORC_ST_BAD_INDEX;
+            continue;
+        }
+        for (long long b = 0; b < row_bytes; ++b)
+            dst[(long long)d * ld_dst + b] = src[(long long)i * ld_src + b];
+    }
 }

@@ -178,3 +178,20 @@ def test_plan_pack_argument_checks(lib):
     assert call(cap=-1) == -1
     assert call(t=bad_tiers) == -1
     assert call(n_t=65) == -1
+
+
+def test_scatter_argument_checks(lib):
+    f = lib.dspark_scatter_compact_to_strided
+    f.restype = ctypes.c_int
+
+    def call(src=FAKE, ld_src=8, width=8, eb=2, rows=4, ld_dst=8, dst_rows=10, dst=FAKE):
+        return f(src, ctypes.c_int64(ld_src), width, eb, FAKE, FAKE, rows, dst,
+                 ctypes.c_int64(ld_dst), dst_rows, FAKE, None)
+
+    assert call(src=None) == -1
+    assert call(dst=None) == -1
+    assert call(eb=3) == -1
+    assert call(width=0) == -1
+    assert call(ld_src=7) == -1
+    assert call(ld_dst=4) == -1
+    assert call(rows=-1) == -1

@@ -289,6 +289,56 @@ def test_pack_capacity_and_bad_len(orc):
     assert r.status & orc.ST_CAPACITY and r.padded == 12
 
 
+# ---------------------------------------------------------------- scatter
+
+def test_scatter_example_of_the_page(orc):
+    """[ROUND] §三: lengths [2, 5, 3] at a stride of 5 -- 10 compact rows go
+    back to their places among 15 strided rows; the other 5 stay untouched."""
+    ex = golden("pack_examples.json")["scatter"]
+    lens = np.array(ex["verify_lens"], np.int32)
+    B, stride = len(lens), ex["stride"]
+    p = orc.pack(np.zeros(B), np.zeros((B, stride - 1)), np.zeros(B), lens, [], 32)
+    assert p.total == ex["compact_rows"]
+    compact = np.arange(p.total * 3, dtype=np.uint16).reshape(p.total, 3) + 1
+    strided = np.zeros((ex["strided_rows"], 3), np.uint16)
+    out, st = orc.scatter_rows(compact, p.src, p.total, strided)
+    assert st == 0
+    # request r's row j lands at r*stride + j
+    want = [r * stride + j for r in range(B) for j in range(int(lens[r]))]
+    assert list(p.src[:p.total]) == want == [0, 1, 5, 6, 7, 8, 9, 10, 11, 12]
+    for i, d in enumerate(want):
+        assert np.array_equal(out[d], compact[i])
+    untouched = sorted(set(range(ex["strided_rows"])) - set(want))
+    assert untouched == [2, 3, 4, 13, 14] and not out[untouched].any()
+
+
+def test_scatter_inverts_the_compact_gather(orc):
+    """Gathering the selected strided rows into compact order and scattering
+    them back restores exactly those rows; pad rows and rows past the total
+    are not written; a destination outside the buffer is flagged."""
+    rng = np.random.default_rng(11)
+    for _ in range(20):
+        B, g = int(rng.integers(1, 9)), int(rng.integers(1, 6))
+        lens = rng.integers(1, g + 2, size=B).astype(np.int32)
+        tiers = [int(lens.sum()) + int(rng.integers(0, 4))]
+        p = orc.pack(np.zeros(B), np.zeros((B, g)), np.zeros(B), lens, tiers, 64)
+        S = rng.integers(1, 60000, size=(B * (g + 1), 5)).astype(np.uint16)
+        compact = np.zeros((64, 5), np.uint16)
+        compact[:p.total] = S[p.src[:p.total]]
+        compact[p.total:] = 9  # pad rows: never copied
+        back, st = orc.scatter_rows(compact, p.src, p.total, np.zeros_like(S))
+        sel = p.src[:p.total]
+        assert st == 0 and np.array_equal(back[sel], S[sel])
+        rest = np.setdiff1d(np.arange(B * (g + 1)), sel)
+        assert not back[rest].any()
+    src_of = np.array([0, 7, -1, 2], np.int32)
+    out, st = orc.scatter_rows(np.ones((4, 2), np.float32), src_of, 4, np.zeros((3, 2), np.float32))
+    assert st & orc.ST_BAD_INDEX and out[0].all() and out[2].all() and not out[1].any()
+    out2, st2 = orc.scatter_rows(np.ones((4, 2), np.float32), [0, 1, 2, 0], 9,
+                                 np.zeros((3, 2), np.float32), max_rows=2)
+    assert st2 == 0 and out2[:2].all() and not out2[2].any()  # total clamped to max_rows
+
+
 # ---------------------------------------------------------------- accept
 
 _TOK = {"A": 11, "B": 12, "C": 13, "D": 14, "E": 15, "X": 5, "Y": 6, "Z": 7}
