@@ -57,6 +57,12 @@ class dspark_cost_table(ctypes.Structure):
                 ("alpha_ms", ctypes.c_double)]
 
 
+class dspark_plan_options(ctypes.Structure):
+    _fields_ = [("conf_generation", ctypes.c_void_p), ("req_generation", ctypes.c_void_p),
+                ("lagged_conf_logits", ctypes.c_void_p), ("align_to_tiers", ctypes.c_int32),
+                ("host_tiers", ctypes.POINTER(ctypes.c_int32)), ("n_tiers", ctypes.c_int32)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -72,6 +78,15 @@ _SIGS = {
     "dspark_pack_verify": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _I32,
                                           ctypes.POINTER(ctypes.c_int32), _I32, _I32, _VP, _VP,
                                           _VP, _VP, _VP, _VP, _VP, _VP]),
+    "dspark_plan_ex": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(dspark_plan_params),
+                                      ctypes.POINTER(dspark_cost_table),
+                                      ctypes.POINTER(dspark_plan_options), _VP, _VP, _VP, _VP, _VP,
+                                      _SZ, _VP, _VP]),
+    "dspark_plan_pack_ex": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(dspark_plan_params),
+                                           ctypes.POINTER(dspark_cost_table),
+                                           ctypes.POINTER(dspark_plan_options), _VP, _VP, _VP, _VP,
+                                           _VP, _VP, _VP, ctypes.POINTER(ctypes.c_int32), _I32,
+                                           _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
     "dspark_plan_pack": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(dspark_plan_params),
                                         ctypes.POINTER(dspark_cost_table), _VP, _VP, _VP, _VP,
                                         _VP, _VP, _VP, ctypes.POINTER(ctypes.c_int32), _I32, _I32,
@@ -190,14 +205,55 @@ def dspark_pack_verify(anchor, draft, prefix_lens, verify_lens, *, B, gamma, tie
     _check("dspark_pack_verify", rc)
 
 
+def plan_options(conf_generation=None, req_generation=None, lagged_conf_logits=None,
+                 align_tiers=None):
+    """A dspark_plan_options (kept alive by the returned tuple's second item)
+    from device tensors and a host tier list; None when no option is set."""
+    if conf_generation is None and req_generation is None and lagged_conf_logits is None \
+            and not align_tiers:
+        return None, None
+    tiers = [int(t) for t in (align_tiers or [])]
+    arr = (ctypes.c_int32 * max(1, len(tiers)))(*tiers)
+    opt = dspark_plan_options(_p(conf_generation, torch.int32, "conf_generation"),
+                              _p(req_generation, torch.int32, "req_generation"),
+                              _p(lagged_conf_logits, torch.float32, "lagged_conf_logits"),
+                              1 if tiers else 0, arr, len(tiers))
+    return opt, arr
+
+
+def dspark_plan_ex(conf_logits, sts_temps, *, B, gamma, survival_eps, min_verify_len,
+                   max_verify_len, forced_budget, cost_kind, cost_M, cost_val, bias_ms=0.0,
+                   alpha_ms=0.0, survivals, verify_lens, budget, tau_theta, status, workspace,
+                   conf_generation=None, req_generation=None, lagged_conf_logits=None,
+                   align_tiers=None, stream=None) -> None:
+    """dspark_plan with the planner options (generation mask, lagged-
+    confidence budget, graph-tier alignment to ``align_tiers``)."""
+    params = dspark_plan_params(B, gamma, survival_eps, min_verify_len, max_verify_len,
+                                forced_budget)
+    cost = dspark_cost_table(cost_kind, int(cost_M.numel()), _p(cost_M, torch.int32, "cost_M"),
+                             _p(cost_val, torch.float64, "cost_val"), bias_ms, alpha_ms)
+    opt, _keep = plan_options(conf_generation, req_generation, lagged_conf_logits, align_tiers)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().dspark_plan_ex(
+        _p(conf_logits, torch.float32, "conf_logits"), _p(sts_temps, torch.float32, "sts_temps"),
+        ctypes.byref(params), ctypes.byref(cost), None if opt is None else ctypes.byref(opt),
+        _p(survivals, torch.float32, "survivals"), _p(verify_lens, torch.int32, "verify_lens"),
+        _p(budget, torch.int32, "budget"), _p(tau_theta, torch.float64, "tau_theta"),
+        _p(workspace), ws_bytes, _p(status, torch.int32, "status"), _stream(stream))
+    _check("dspark_plan_ex", rc)
+
+
 def dspark_plan_pack(conf_logits, sts_temps, anchor, draft, prefix_lens, *, B, gamma,
                      survival_eps, min_verify_len, max_verify_len, forced_budget, cost_kind,
                      cost_M, cost_val, bias_ms=0.0, alpha_ms=0.0, tiers, capacity, survivals,
                      verify_lens, budget, tau_theta, packed_ids, packed_pos, packed_req,
-                     packed_src, cu_seqlens, totals, status, workspace, stream=None) -> None:
+                     packed_src, cu_seqlens, totals, status, workspace, conf_generation=None,
+                     req_generation=None, lagged_conf_logits=None, align_to_tiers=False,
+                     stream=None) -> None:
     """dspark_plan then dspark_pack_verify on its verify_lens, in fewer launches
     (the pack runs inside the planner's last kernel for tables of <= 16
-    entries)."""
+    entries).  The planner options as in dspark_plan_ex; alignment uses the
+    pack's ``tiers``."""
     params = dspark_plan_params(B, gamma, survival_eps, min_verify_len, max_verify_len,
                                 forced_budget)
     cost = dspark_cost_table(cost_kind, int(cost_M.numel()), _p(cost_M, torch.int32, "cost_M"),
@@ -205,9 +261,12 @@ def dspark_plan_pack(conf_logits, sts_temps, anchor, draft, prefix_lens, *, B, g
     tiers = [int(t) for t in tiers]
     arr = (ctypes.c_int32 * max(1, len(tiers)))(*tiers)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = load().dspark_plan_pack(
+    opt, _keep = plan_options(conf_generation, req_generation, lagged_conf_logits,
+                              tiers if align_to_tiers else None)
+    rc = load().dspark_plan_pack_ex(
         _p(conf_logits, torch.float32, "conf_logits"), _p(sts_temps, torch.float32, "sts_temps"),
-        ctypes.byref(params), ctypes.byref(cost), _p(survivals, torch.float32, "survivals"),
+        ctypes.byref(params), ctypes.byref(cost), None if opt is None else ctypes.byref(opt),
+        _p(survivals, torch.float32, "survivals"),
         _p(verify_lens, torch.int32, "verify_lens"), _p(budget, torch.int32, "budget"),
         _p(tau_theta, torch.float64, "tau_theta"), _p(anchor, torch.int32, "anchor"),
         _p(draft, torch.int32, "draft"), _p(prefix_lens, torch.int32, "prefix_lens"), arr,

@@ -98,12 +98,28 @@ __host__ __device__ inline size_t plan_prefix_offset(int N) {
 __host__ __device__ inline size_t plan_count_offset(int N) {
     return (plan_prefix_offset(N) + (size_t)(N + 1) * 8 + 15) & ~size_t(15);
 }
+// Between the passes of one call (dspark_plan_ex): the lagged pass's
+// budget, the tier-filled budget, and the lengths / tau-theta / survivals a
+// pass computes that the caller does not receive.
+struct PassScratch {
+    int32_t lagged_budget, exec_budget, pass_budget, pad;
+    double pass_tau_theta[2];
+};
+__host__ __device__ inline size_t plan_pass_offset(int B, int N) {
+    return (plan_count_offset(N) + (size_t)B * (kMaxSparse + 1) * 4 + 255) & ~size_t(255);
+}
+__host__ __device__ inline size_t plan_pass_lens_offset(int B, int N) {
+    return plan_pass_offset(B, N) + 256;
+}
+__host__ __device__ inline size_t plan_pass_surv_offset(int B, int N) {
+    return (plan_pass_lens_offset(B, N) + (size_t)B * 4 + 255) & ~size_t(255);
+}
 __host__ __device__ inline size_t plan_scratch_bytes(int B, int N) {
-    return plan_count_offset(N) + (size_t)B * (kMaxSparse + 1) * 4;
+    return plan_pass_surv_offset(B, N) + (size_t)N * 4;
 }
 
 template <typename T>
-__device__ __forceinline__ T *scratch_at(PlanScratch *sc, size_t off) {
+__host__ __device__ __forceinline__ T *scratch_at(PlanScratch *sc, size_t off) {
     return reinterpret_cast<T *>(reinterpret_cast<unsigned char *>(sc) + off);
 }
 
@@ -126,7 +142,8 @@ __device__ __forceinline__ long long fixed_of_key(uint32_t key) {
 
 __global__ void __launch_bounds__(kSurvThreads)
 survival_kernel(const float *__restrict__ z, const float *__restrict__ T, int B, int gamma,
-                float eps, int kmax, bool bin_keys, float *__restrict__ s_out,
+                float eps, int kmax, bool bin_keys, const int32_t *__restrict__ conf_gen,
+                const int32_t *__restrict__ req_gen, float *__restrict__ s_out,
                 int32_t *__restrict__ status, PlanScratch *__restrict__ scratch) {
     pdl_trigger();
     if (blockIdx.x == 0) {  // reset the rank kernel's ticket and accumulators
@@ -141,9 +158,12 @@ survival_kernel(const float *__restrict__ z, const float *__restrict__ T, int B,
         for (int j = lane; j <= kMaxSparse; j += 32) cnt[j] = 0;
     }
     const bool active = lane < gamma;
+    // a request whose pool slot was reused since its confidences were
+    // recorded falls back to survivals of 1 ([AVS] §三, req_generation)
+    const bool stale = conf_gen && __ldg(conf_gen + r) != __ldg(req_gen + r);
     float c = 1.0f;
     bool bad = false;
-    if (active) {
+    if (active && !stale) {
         const float zk = z[(size_t)r * gamma + lane];
         const float tk = T[lane];
         bad = (zk != zk) || !(tk > 0.0f);
@@ -198,7 +218,32 @@ struct PlanArgs {
     int32_t *status;
     PlanScratch *scratch;
     PackArgs pk;
+    const int32_t *forced_dev;  // device forced budget (a previous pass's), read after the wait
+    bool more_passes;           // another pass over the same survivals follows: the select
+                                // path keeps the bins, the rank path resets its ticket and
+                                // accumulators for it
+    TierArgs align;             // align.n > 0: write the tier-filled budget to *exec_budget
+    int32_t *exec_budget;
 };
+
+// The forced budget of this pass: from device memory when a previous pass
+// chose it, else the caller's.  Call after the dependency wait.
+__device__ __forceinline__ int resolve_forced(const PlanArgs &a) {
+    return a.forced_dev ? *a.forced_dev : a.forced;
+}
+
+// Graph-tier alignment ([AVS] §三, §五 "paid-padding reclamation"): with
+// `total` verify rows at budget b (b <= b_top), the rows up to the smallest
+// tier >= total are paid for anyway; the executed budget takes one more
+// candidate per spare row, within the candidates that are in range.  No tier
+// holds the total: b.
+__device__ __forceinline__ int aligned_budget(const TierArgs &t, int b, int total, long long b_top) {
+    if (t.n <= 0 || b_top < 0) return b;
+    bool no_tier;
+    const int tier = tier_round_up(t, total, &no_tier);
+    if (no_tier) return b;
+    return (int)min((long long)b + (tier - total), b_top);
+}
 
 // tau = (B * 2^37 + P) * 2^-37 as an fp64 built with integer operations:
 // the value is below 2^53 units, so it is exactly representable.
@@ -231,7 +276,7 @@ struct RankSmem {
     int cand_b[kMaxSparse + 1];                 // candidate budget of each table entry (-1: none)
     unsigned long long acc_s[kMaxSparse + 1];   // this CTA's part of each candidate's prefix
     double val_s[kMaxSparse];                   // sparse path: the cost table values
-    int budget, last, n_kept, sparse;
+    int budget, last, n_kept, sparse, forced;
     long long b_top;
 };
 
@@ -282,6 +327,7 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
     }
     const int Mlast = __ldg(c.M + c.n - 1);
     pdl_wait();  // survivals come from survival_kernel
+    const int forced = resolve_forced(a);
 
     // every CTA holds all keys: run r = K[r*S .. r*S + P2)
     int kept_local = 0;
@@ -317,13 +363,14 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
             sm.cand_b[tid] = entry_last_budget(c, tid, Mj, Mprev, Mnext, B, b_top);
             sm.val_s[tid] = vj;
         }
-        if (tid == c.n) sm.cand_b[tid] = (a.forced >= 0 && b_top >= 0) ? (int)min((long long)a.forced, b_top) : -1;
+        if (tid == c.n) sm.cand_b[tid] = (forced >= 0 && b_top >= 0) ? (int)min((long long)forced, b_top) : -1;
         if (tid <= c.n) sm.acc_s[tid] = 0ull;
     }
     if (tid == 0) {
         sm.n_kept = n_kept;
         sm.b_top = b_top;
         sm.sparse = sparse ? 1 : 0;
+        sm.forced = forced;
     }
     __syncthreads();
 
@@ -403,6 +450,15 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
     if (!sm.last) return;
     __threadfence();
     finish_plan(a, sm);
+    if (a.more_passes) {  // leave the ticket and accumulators at zero for the next pass
+        __syncthreads();
+        if (tid == 0) a.scratch->ticket = 0u;
+        for (int j = tid; j <= kMaxSparse; j += kRankThreads) a.scratch->acc[j] = 0ull;
+        if (c.n <= kMaxSparse) {
+            int32_t *cnt = scratch_at<int32_t>(a.scratch, plan_count_offset(N));
+            for (int i = tid; i < B * (kMaxSparse + 1); i += kRankThreads) cnt[i] = 0;
+        }
+    }
 }
 
 __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
@@ -412,6 +468,7 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
     const int n_kept = sm.n_kept;
     const long long b_top = sm.b_top;
     const bool sparse = sm.sparse != 0;
+    const int forced = sm.forced;
     const int32_t *rank_in = scratch_at<int32_t>(a.scratch, plan_rank_offset());
     const long long *sorted = scratch_at<long long>(a.scratch, plan_sorted_offset(a.N));
     long long *P = scratch_at<long long>(a.scratch, plan_prefix_offset(a.N));
@@ -498,7 +555,7 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
             int budget;
             long long Pbud = 0;
             double theta_out = 0.0;
-            if (a.forced < 0) {
+            if (forced < 0) {
                 if (any_bad_table || bb == 0x7FFFFFFF) {
                     budget = 0;
                     st |= DSPARK_STATUS_INFEASIBLE;
@@ -512,14 +569,14 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
                     budget = 0;
                     st |= DSPARK_STATUS_INFEASIBLE;
                 } else {
-                    budget = (int)min((long long)a.forced, bh);
+                    budget = (int)min((long long)forced, bh);
                 }
             }
             // P at the budget: the candidate's accumulator (sparse) or the scan
             if (budget > 0) {
                 if (!sparse) {
                     Pbud = __ldcg(P + budget);
-                } else if (a.forced >= 0) {
+                } else if (forced >= 0) {
                     Pbud = (long long)sm.acc_s[c.n];
                 } else {
                     for (int j = 0; j < c.n; ++j)
@@ -529,7 +586,7 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
                         }
                 }
             }
-            if (a.forced >= 0 && budget == (int)min((long long)a.forced, b_top) && b_top >= 0 &&
+            if (forced >= 0 && budget == (int)min((long long)forced, b_top) && b_top >= 0 &&
                 !any_bad_table) {
                 // theta at the forced budget: the entry covering M = B + budget
                 const long long Mv = (long long)B + budget;
@@ -555,7 +612,7 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
             // sparse path: the entry whose counts hold the selection
             int slot = -1;
             if (sparse && budget > 0) {
-                if (a.forced >= 0) slot = c.n;
+                if (forced >= 0) slot = c.n;
                 else
                     for (int j = 0; j < c.n; ++j)
                         if (sm.cand_b[j] == budget) {
@@ -576,6 +633,7 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
     const int slot = sm.last;
     const int kmax = min(G, a.max_len - 1);
     const int32_t *counts = scratch_at<int32_t>(a.scratch, plan_count_offset(a.N));
+    int lens_sum = 0;
     for (int r = tid; r < B; r += kRankThreads) {
         int cnt = 0;
         if (sparse) {
@@ -584,7 +642,13 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
 #pragma unroll 8
             for (int k = 0; k < kmax; ++k) cnt += __ldcg(rank_in + r * G + k) < budget ? 1 : 0;
         }
-        a.verify_lens[r] = min(max(1 + cnt, a.min_len), a.max_len);
+        const int L = min(max(1 + cnt, a.min_len), a.max_len);
+        a.verify_lens[r] = L;
+        lens_sum += L;
+    }
+    if (a.align.n > 0) {  // the tier-filled budget for the next pass
+        const int total = block_sum<int>(lens_sum, sm.scan32);
+        if (tid == 0) *a.exec_budget = aligned_budget(a.align, budget, total, b_top);
     }
 }
 
@@ -669,7 +733,7 @@ struct SelSmem {
     double div_s[kMaxSelect];              // theta divisor T of entry j (additive tables)
     int ok_s[kMaxSelect];                  // entry j's SPS or T is a positive finite number
     int32_t M_s[kMaxSelect];
-    int n_gather, bad_table;
+    int n_gather, bad_table, budget_s;
     unsigned long long cstar;  // C* of the chosen budget (kNoComposite: none)
 };
 
@@ -896,10 +960,11 @@ __device__ __forceinline__ void select_pack(const PlanArgs &a, SelSmem &sm, bool
 // Step (3) of select_kernel, run by warp 0: theta at every candidate budget,
 // the first maximiser (or the forced budget) and the plan's scalar outputs.
 // Kept out of line so that the compiler schedules it on its own.
-__device__ __noinline__ void select_theta(const PlanArgs &a, SelSmem &sm, long long b_top) {
+__device__ __noinline__ void select_theta(const PlanArgs &a, SelSmem &sm, long long b_top,
+                                         int forced) {
     // arguments into registers first (the output stores could alias them)
     const int lane = threadIdx.x & 31;
-    const int B = a.B, n = a.cost.n, kind = a.cost.kind, forced = a.forced;
+    const int B = a.B, n = a.cost.n, kind = a.cost.kind;
     const double bias = a.cost.bias, alpha = a.cost.alpha;
     int32_t *budget_out = a.budget, *status = a.status;
     double *tau_theta = a.tau_theta;
@@ -977,6 +1042,7 @@ __device__ __noinline__ void select_theta(const PlanArgs &a, SelSmem &sm, long l
         const bool chosen = budget > 0 && slot >= 0;
         if (st) flag(status, st);
         sm.cstar = chosen ? sm.cthr[slot] : kNoComposite;
+        sm.budget_s = budget;
         budget_out[0] = budget;
         tau_theta[0] = tau_of(B, chosen ? (long long)sm.P[slot] : 0);
         tau_theta[1] = theta_out;
@@ -1041,8 +1107,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
         for (int i = tid; i < N; i += kSelThreads) sm.stage[2 * B + i] = __ldg(a.pk.draft + i);
     }
     pdl_wait();  // survivals and bins come from survival_kernel
+    const int forced = resolve_forced(a);
 
-    // (1) this thread's two bins, cleared for the next call; its keys
+    // (1) this thread's two bins, cleared for the next call (unless a later
+    // pass of the same call reads them); its keys
     unsigned int h0, h1;
     unsigned long long s0, s1;
     {
@@ -1054,8 +1122,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
         h1 = cv.y;
         s0 = sv.x;
         s1 = sv.y;
-        *hc = make_uint2(0u, 0u);
-        *hs = make_ulonglong2(0ull, 0ull);
+        if (!a.more_passes) {
+            *hc = make_uint2(0u, 0u);
+            *hs = make_ulonglong2(0ull, 0ull);
+        }
     }
     uint32_t key[IPT];
     {
@@ -1122,7 +1192,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
     if (warp < nc) {
         int b;
         if (warp < c.n) b = entry_last_budget(c, warp, Mj, Mprev, Mnext, B, b_top);
-        else b = (a.forced >= 0 && b_top >= 0) ? (int)min((long long)a.forced, b_top) : -1;
+        else b = (forced >= 0 && b_top >= 0) ? (int)min((long long)forced, b_top) : -1;
         int rem = 0, d = 0, cnt = 0;
         unsigned long long ps = 0ull;
         if (b >= 1) {  // b <= n_kept = cum[2047]
@@ -1219,7 +1289,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
     __syncthreads();
 
     // (3) theta at every candidate (all in warp 0) and the budget
-    if (warp == 0) select_theta(a, sm, b_top);
+    if (warp == 0) select_theta(a, sm, b_top, forced);
     __syncthreads();
 
     // (4) ScheduleVerifyLensTopk: request r selects its candidates with
@@ -1256,6 +1326,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
                 prev_in = false;
             }
         }
+    }
+    if (a.align.n > 0) {  // the tier-filled budget for the next pass
+        __syncthreads();
+        int mine = 0;
+        for (int r = tid; r < B; r += kSelThreads) mine += sm.lens_s[r];
+        const int total = block_sum<int>(mine, sm.scan32);
+        if (tid == 0) *a.exec_budget = aligned_budget(a.align, sm.budget_s, total, b_top);
     }
     if (a.pk.on) {
         __syncthreads();
@@ -1311,23 +1388,59 @@ int check_plan(const float *conf_logits, const float *sts_temps, const dspark_pl
     return DSPARK_OK;
 }
 
-// The planner's launches; with pk->on the select path also packs the
-// verify window, and the rank path is followed by the pack kernel.
+// One planner pass over survivals already computed: select_kernel (tables
+// of <= 16 entries) or rank_kernel.
+int launch_pass(PlanArgs a, bool select, cudaStream_t s) {
+    if (select) {
+        const int ipt = (a.N + kSelThreads - 1) / kSelThreads;
+        cudaError_t e;
+        if (ipt <= 1) e = launch_select<1>(a, s);
+        else if (ipt <= 2) e = launch_select<2>(a, s);
+        else if (ipt <= 4) e = launch_select<4>(a, s);
+        else if (ipt <= 8) e = launch_select<8>(a, s);
+        else e = launch_select<16>(a, s);
+        if (e == cudaSuccess) return DSPARK_OK;
+        // the bins survival_kernel filled must not reach the next call
+        cudaMemsetAsync(&a.scratch->hcount[0], 0,
+                        sizeof(a.scratch->hcount) + sizeof(a.scratch->hsum), s);
+        return DSPARK_ERR_CUDA;
+    }
+    a.pk.on = false;
+    const size_t smem = rank_smem_bytes(a.B, a.P2);
+    if (ensure_smem(reinterpret_cast<const void *>(rank_kernel), (int)rank_smem_max(), 0) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    // about one warp per candidate, at most one CTA per SM
+    int grid = (a.N + kRankWarps - 1) / kRankWarps;
+    grid = grid < 1 ? 1 : (grid > sm_count() ? sm_count() : grid);
+    return launch_pdl(rank_kernel, dim3(grid), dim3(kRankThreads), smem, s, a) == cudaSuccess
+               ? DSPARK_OK
+               : DSPARK_ERR_CUDA;
+}
+
+// The planner's launches.  Without options: survival_kernel, then one
+// pass.  opt->lagged_conf_logits: a first survival + pass on the lagged
+// confidences chooses the budget, and the pass on the current ones
+// allocates it ([AVS] §三: lagged confidence sets the budget, the current
+// one the allocation).  opt->align_to_tiers: a pass chooses the budget and
+// the tier-filled budget, and a last pass allocates that.  pk.on: the last
+// pass also packs the verify window (the select path in the same kernel,
+// the rank path with the pack kernel after it).
 int run_plan(const float *conf_logits, const float *sts_temps, const dspark_plan_params *p,
-             const dspark_cost_table *cost, float *survivals, int32_t *verify_lens,
-             int32_t *budget, double *tau_theta, void *workspace, int32_t *status,
-             const PackArgs &pk, cudaStream_t s) {
+             const dspark_cost_table *cost, const dspark_plan_options *opt, float *survivals,
+             int32_t *verify_lens, int32_t *budget, double *tau_theta, void *workspace,
+             int32_t *status, const PackArgs &pk, const TierArgs &align, cudaStream_t s) {
     const int B = p->B, G = p->gamma, N = B * G;
     PlanScratch *scratch = static_cast<PlanScratch *>(workspace);
-    const int sblocks = (B * 32 + kSurvThreads - 1) / kSurvThreads;
+    PassScratch *ps = scratch_at<PassScratch>(scratch, plan_pass_offset(B, N));
+    int32_t *pass_lens = scratch_at<int32_t>(scratch, plan_pass_lens_offset(B, N));
+    float *lagged_surv = scratch_at<float>(scratch, plan_pass_surv_offset(B, N));
     const bool select = cost->n <= kMaxSelect;  // few candidate budgets: one-CTA select
-    survival_kernel<<<sblocks, kSurvThreads, 0, s>>>(conf_logits, sts_temps, B, G,
-                                                     p->survival_eps, p->max_verify_len - 1,
-                                                     select, survivals, status, scratch);
-    if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+    const int32_t *conf_gen = opt ? opt->conf_generation : nullptr;
+    const int32_t *req_gen = opt ? opt->req_generation : nullptr;
+    const bool lagged = opt && opt->lagged_conf_logits;
+    const int sblocks = (B * 32 + kSurvThreads - 1) / kSurvThreads;
 
     PlanArgs a;
-    a.surv = survivals;
     a.B = B;
     a.gamma = G;
     a.N = N;
@@ -1337,39 +1450,71 @@ int run_plan(const float *conf_logits, const float *sts_temps, const dspark_plan
     a.max_len = p->max_verify_len;
     a.forced = p->forced_budget;
     a.cost = CostArgs{cost->kind, cost->n, cost->M, cost->val, cost->bias_ms, cost->alpha_ms};
+    a.status = status;
+    a.scratch = scratch;
+    a.pk = PackArgs{};
+    a.pk.on = false;
+    a.forced_dev = nullptr;
+    a.more_passes = false;
+    a.align.n = 0;
+    a.exec_budget = nullptr;
+    // outputs of a pass whose results only the next pass reads
+    a.verify_lens = pass_lens;
+    a.budget = &ps->pass_budget;
+    a.tau_theta = ps->pass_tau_theta;
+
+    int rc;
+    if (lagged) {
+        survival_kernel<<<sblocks, kSurvThreads, 0, s>>>(
+            opt->lagged_conf_logits, sts_temps, B, G, p->survival_eps, p->max_verify_len - 1,
+            select, conf_gen, req_gen, lagged_surv, status, scratch);
+        if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+        a.surv = lagged_surv;
+        a.budget = &ps->lagged_budget;
+        if ((rc = launch_pass(a, select, s)) != DSPARK_OK) return rc;
+        a.budget = &ps->pass_budget;
+        a.forced_dev = &ps->lagged_budget;
+    }
+    survival_kernel<<<sblocks, kSurvThreads, 0, s>>>(conf_logits, sts_temps, B, G,
+                                                     p->survival_eps, p->max_verify_len - 1,
+                                                     select, conf_gen, req_gen, survivals, status,
+                                                     scratch);
+    if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+    a.surv = survivals;
+    if (align.n > 0) {
+        a.more_passes = true;
+        a.align = align;
+        a.exec_budget = &ps->exec_budget;
+        if ((rc = launch_pass(a, select, s)) != DSPARK_OK) return rc;
+        a.more_passes = false;
+        a.align.n = 0;
+        a.exec_budget = nullptr;
+        a.forced_dev = &ps->exec_budget;
+    }
     a.verify_lens = verify_lens;
     a.budget = budget;
     a.tau_theta = tau_theta;
-    a.status = status;
-    a.scratch = scratch;
     a.pk = pk;
-    if (select) {
-        const int ipt = (N + kSelThreads - 1) / kSelThreads;
-        cudaError_t e;
-        if (ipt <= 1) e = launch_select<1>(a, s);
-        else if (ipt <= 2) e = launch_select<2>(a, s);
-        else if (ipt <= 4) e = launch_select<4>(a, s);
-        else if (ipt <= 8) e = launch_select<8>(a, s);
-        else e = launch_select<16>(a, s);
-        if (e == cudaSuccess) return DSPARK_OK;
-        // the bins survival_kernel filled must not reach the next call
-        cudaMemsetAsync(&scratch->hcount[0], 0,
-                        sizeof(scratch->hcount) + sizeof(scratch->hsum), s);
+    if ((rc = launch_pass(a, select, s)) != DSPARK_OK) return rc;
+    if (!select && pk.on &&
+        launch_pack(pk.anchor, pk.draft, pk.prefix, verify_lens, B, G, pk.tiers, pk.capacity,
+                    pk.ids, pk.pos, pk.req, pk.src, pk.cu, pk.totals, status, s) != cudaSuccess)
         return DSPARK_ERR_CUDA;
+    return DSPARK_OK;
+}
+
+// Checks of the options; DSPARK_OK when they may be used.
+int check_options(const dspark_plan_options *opt, TierArgs *align, const int32_t *pack_tiers,
+                  int32_t pack_n_tiers) {
+    align->n = 0;
+    if (!opt) return DSPARK_OK;
+    if ((opt->conf_generation == nullptr) != (opt->req_generation == nullptr))
+        return DSPARK_ERR_INVALID_ARG;
+    if (opt->align_to_tiers) {
+        const int32_t *t = pack_tiers ? pack_tiers : opt->host_tiers;
+        const int32_t n = pack_tiers ? pack_n_tiers : opt->n_tiers;
+        if (n < 1 || !load_tiers(t, n, align)) return DSPARK_ERR_INVALID_ARG;
     }
-    a.pk.on = false;
-    const size_t smem = rank_smem_bytes(B, a.P2);
-    if (ensure_smem(reinterpret_cast<const void *>(rank_kernel), (int)rank_smem_max(), 0) != cudaSuccess)
-        return DSPARK_ERR_CUDA;
-    // about one warp per candidate, at most one CTA per SM
-    int grid = (N + kRankWarps - 1) / kRankWarps;
-    grid = grid < 1 ? 1 : (grid > sm_count() ? sm_count() : grid);
-    if (launch_pdl(rank_kernel, dim3(grid), dim3(kRankThreads), smem, s, a) != cudaSuccess)
-        return DSPARK_ERR_CUDA;
-    if (pk.on && launch_pack(pk.anchor, pk.draft, pk.prefix, verify_lens, B, G, pk.tiers,
-                             pk.capacity, pk.ids, pk.pos, pk.req, pk.src, pk.cu, pk.totals,
-                             status, s) != cudaSuccess)
-        return DSPARK_ERR_CUDA;
     return DSPARK_OK;
 }
 
@@ -1380,13 +1525,25 @@ extern "C" int dspark_plan(const float *conf_logits, const float *sts_temps,
                            float *survivals, int32_t *verify_lens, int32_t *budget,
                            double *tau_theta, void *workspace, size_t workspace_bytes,
                            int32_t *status, void *stream) {
-    const int rc = check_plan(conf_logits, sts_temps, p, cost, survivals, verify_lens, budget,
-                              tau_theta, workspace, workspace_bytes, status);
+    return dspark_plan_ex(conf_logits, sts_temps, p, cost, nullptr, survivals, verify_lens,
+                          budget, tau_theta, workspace, workspace_bytes, status, stream);
+}
+
+extern "C" int dspark_plan_ex(const float *conf_logits, const float *sts_temps,
+                              const dspark_plan_params *p, const dspark_cost_table *cost,
+                              const dspark_plan_options *opt, float *survivals,
+                              int32_t *verify_lens, int32_t *budget, double *tau_theta,
+                              void *workspace, size_t workspace_bytes, int32_t *status,
+                              void *stream) {
+    int rc = check_plan(conf_logits, sts_temps, p, cost, survivals, verify_lens, budget,
+                        tau_theta, workspace, workspace_bytes, status);
     if (rc != DSPARK_OK) return rc;
+    TierArgs align;
+    if ((rc = check_options(opt, &align, nullptr, 0)) != DSPARK_OK) return rc;
     PackArgs pk = {};
     pk.on = false;
-    return run_plan(conf_logits, sts_temps, p, cost, survivals, verify_lens, budget, tau_theta,
-                    workspace, status, pk, static_cast<cudaStream_t>(stream));
+    return run_plan(conf_logits, sts_temps, p, cost, opt, survivals, verify_lens, budget,
+                    tau_theta, workspace, status, pk, align, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int dspark_plan_pack(const float *conf_logits, const float *sts_temps,
@@ -1398,14 +1555,32 @@ extern "C" int dspark_plan_pack(const float *conf_logits, const float *sts_temps
                                 int32_t *packed_pos, int32_t *packed_req, int32_t *packed_src,
                                 int32_t *cu_seqlens, int32_t *totals, void *workspace,
                                 size_t workspace_bytes, int32_t *status, void *stream) {
-    const int rc = check_plan(conf_logits, sts_temps, p, cost, survivals, verify_lens, budget,
-                              tau_theta, workspace, workspace_bytes, status);
+    return dspark_plan_pack_ex(conf_logits, sts_temps, p, cost, nullptr, survivals, verify_lens,
+                               budget, tau_theta, anchor, draft, prefix_lens, host_tiers, n_tiers,
+                               capacity, packed_ids, packed_pos, packed_req, packed_src,
+                               cu_seqlens, totals, workspace, workspace_bytes, status, stream);
+}
+
+extern "C" int dspark_plan_pack_ex(const float *conf_logits, const float *sts_temps,
+                                   const dspark_plan_params *p, const dspark_cost_table *cost,
+                                   const dspark_plan_options *opt, float *survivals,
+                                   int32_t *verify_lens, int32_t *budget, double *tau_theta,
+                                   const int32_t *anchor, const int32_t *draft,
+                                   const int32_t *prefix_lens, const int32_t *host_tiers,
+                                   int32_t n_tiers, int32_t capacity, int32_t *packed_ids,
+                                   int32_t *packed_pos, int32_t *packed_req, int32_t *packed_src,
+                                   int32_t *cu_seqlens, int32_t *totals, void *workspace,
+                                   size_t workspace_bytes, int32_t *status, void *stream) {
+    int rc = check_plan(conf_logits, sts_temps, p, cost, survivals, verify_lens, budget,
+                        tau_theta, workspace, workspace_bytes, status);
     if (rc != DSPARK_OK) return rc;
     if (!anchor || !draft || !prefix_lens || !packed_ids || !packed_pos || !packed_req ||
         !packed_src || !cu_seqlens || !totals || capacity < 0)
         return DSPARK_ERR_INVALID_ARG;
     PackArgs pk = {};
     if (!load_tiers(host_tiers, n_tiers, &pk.tiers)) return DSPARK_ERR_INVALID_ARG;
+    TierArgs align;
+    if ((rc = check_options(opt, &align, host_tiers, n_tiers)) != DSPARK_OK) return rc;
     pk.on = true;
     pk.anchor = anchor;
     pk.draft = draft;
@@ -1417,6 +1592,6 @@ extern "C" int dspark_plan_pack(const float *conf_logits, const float *sts_temps
     pk.src = packed_src;
     pk.cu = cu_seqlens;
     pk.totals = totals;
-    return run_plan(conf_logits, sts_temps, p, cost, survivals, verify_lens, budget, tau_theta,
-                    workspace, status, pk, static_cast<cudaStream_t>(stream));
+    return run_plan(conf_logits, sts_temps, p, cost, opt, survivals, verify_lens, budget,
+                    tau_theta, workspace, status, pk, align, static_cast<cudaStream_t>(stream));
 }

@@ -105,9 +105,9 @@ typedef struct {
     double alpha_ms;       /* additive only */
 } dspark_cost_table;
 
-/* Device scratch of one planner call: about 12 * B * gamma + 26 KB
- * (candidate ranks, the sorted survivals, a completion counter and a
- * 2048-bin histogram of the survivals).  The workspace must be zero-filled
+/* Device scratch of one planner call: about 16 * B * gamma + 26 KB
+ * (candidate ranks, the sorted survivals, a completion counter, a 2048-bin
+ * histogram of the survivals, and what passes of one call hand over).  The workspace must be zero-filled
  * once before its first dspark_plan call (cudaMemset); every call that
  * returns DSPARK_OK leaves the histogram zero again, and a call that
  * returns DSPARK_ERR_CUDA after launching clears it on the stream, so the
@@ -139,6 +139,45 @@ DSPARK_API int dspark_plan(const float *conf_logits, const float *sts_temps,
                 const dspark_plan_params *p /* host */, const dspark_cost_table *cost /* host */,
                 float *survivals, int32_t *verify_lens, int32_t *budget, double *tau_theta,
                 void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
+
+/* Options of the planner ([AVS] §三, the conditions under which the
+ * executed budget departs from the plain plan).  Every field may be left
+ * zero / NULL.
+ *   conf_generation, req_generation  device [B] int32, both or neither: a
+ *       request whose confidences were recorded for another generation of
+ *       its pool slot plans with survivals of 1 at every depth (optimistic;
+ *       [AVS] §三 "req_generation")
+ *   lagged_conf_logits  device [B, gamma] fp32: the budget is chosen from
+ *       these (lagged) confidences, then allocated over the current ones by
+ *       the same ordering, as with a forced budget ([AVS] §三, overlap
+ *       scheduler: lagged confidence sets the budget, the current one the
+ *       allocation); tau/theta are reported for the allocation
+ *   align_to_tiers  1: graph-tier alignment ([AVS] §三, §五 "paid-padding
+ *       reclamation"): with T verify rows at the chosen budget and the
+ *       smallest tier >= T, the executed budget takes one more candidate per
+ *       spare row of that tier, as long as candidates remain in range; no
+ *       tier holds T: unchanged.  Also applies to a forced budget.
+ *   host_tiers, n_tiers  host: the tiers for alignment (dspark_plan_ex; the
+ *       pack's tiers are used by dspark_plan_pack_ex) */
+typedef struct {
+    const int32_t *conf_generation;
+    const int32_t *req_generation;
+    const float *lagged_conf_logits;
+    int32_t align_to_tiers;
+    const int32_t *host_tiers;
+    int32_t n_tiers;
+} dspark_plan_options;
+
+/* dspark_plan with options (opt may be NULL: dspark_plan).  Each option adds
+ * planner passes over the same workspace: lagged confidences a survival
+ * kernel and a pass, alignment a pass.  Errors: those of dspark_plan, and
+ * INVALID_ARG for one generation array without the other or alignment
+ * without a valid tier list. */
+DSPARK_API int dspark_plan_ex(const float *conf_logits, const float *sts_temps,
+                   const dspark_plan_params *p /* host */, const dspark_cost_table *cost /* host */,
+                   const dspark_plan_options *opt /* host, nullable */, float *survivals,
+                   int32_t *verify_lens, int32_t *budget, double *tau_theta, void *workspace,
+                   size_t workspace_bytes, int32_t *status, void *stream);
 
 /* ------------------------------------------------------------------ pack */
 
@@ -212,6 +251,19 @@ DSPARK_API int dspark_scatter_compact_to_strided(const void *src, int64_t ld_src
                                       const int32_t *totals, int32_t max_rows, void *dst,
                                       int64_t ld_dst, int32_t dst_rows, int32_t *status,
                                       void *stream);
+
+/* dspark_plan_pack with options (see dspark_plan_options; alignment uses
+ * the pack's tiers). */
+DSPARK_API int dspark_plan_pack_ex(const float *conf_logits, const float *sts_temps,
+                        const dspark_plan_params *p /* host */,
+                        const dspark_cost_table *cost /* host */,
+                        const dspark_plan_options *opt /* host, nullable */, float *survivals,
+                        int32_t *verify_lens, int32_t *budget, double *tau_theta,
+                        const int32_t *anchor, const int32_t *draft, const int32_t *prefix_lens,
+                        const int32_t *host_tiers /* host */, int32_t n_tiers, int32_t capacity,
+                        int32_t *packed_ids, int32_t *packed_pos, int32_t *packed_req,
+                        int32_t *packed_src, int32_t *cu_seqlens, int32_t *totals,
+                        void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
 
 /* ---------------------------------------------------------------- accept */
 

@@ -175,6 +175,53 @@ def plan(z, T, eps, min_len, max_len, forced, kind, M, val, bias=0.0, alpha=0.0)
                       theta=float(tt[1]), n_kept=int(n_kept), status=int(st[0]))
 
 
+def plan_ex(z, T, eps, min_len, max_len, forced, kind, M, val, bias=0.0, alpha=0.0,
+            conf_gen=None, req_gen=None, lagged_z=None, align_tiers=None):
+    """The planner with the options of [AVS] §三, composed from the plain
+    planner's definitions:
+      * generation mask: a request whose confidences belong to another
+        generation of its slot has survival 1 at every depth;
+      * lagged_z: the budget is the plain plan's budget on the lagged
+        confidences; the allocation (lens, tau, theta) is the plan on the
+        current confidences with that budget forced;
+      * align_tiers: with T rows at the chosen budget b and the smallest tier
+        t >= T, the executed budget is b + (t - T) (then clipped to the
+        in-range candidates like any forced budget); no tier >= T: b."""
+    z = _c(z, np.float32)
+    B, g = z.shape
+    live = np.ones(B, bool) if conf_gen is None else (np.asarray(conf_gen) == np.asarray(req_gen))
+
+    def surv(zz):
+        s_raw = np.ones((B, g), np.float32)
+        st = 0
+        if live.any():
+            r, _, st = survival(_c(zz, np.float32)[live], T, eps)
+            s_raw[live] = r
+        s_out = np.where(s_raw >= np.float32(eps), s_raw, np.float32(0)).astype(np.float32)
+        return s_raw, s_out, st
+
+    status = 0
+    if lagged_z is not None:
+        lag_raw, _, st = surv(lagged_z)
+        status |= st
+        first = plan_from_survivals(lag_raw, eps, min_len, max_len, forced, kind, M, val, bias, alpha)
+        status |= first.status
+        forced = first.budget
+    s_raw, s_out, st = surv(z)
+    status |= st
+    res = plan_from_survivals(s_raw, eps, min_len, max_len, forced, kind, M, val, bias, alpha)
+    if align_tiers is not None and len(align_tiers) > 0:
+        status |= res.status
+        total = int(res.verify_lens.sum())
+        tiers = [int(t) for t in align_tiers]
+        tier = next((t for t in tiers if t >= total), None)
+        b_exec = res.budget if tier is None else res.budget + (tier - total)
+        res = plan_from_survivals(s_raw, eps, min_len, max_len, b_exec, kind, M, val, bias, alpha)
+    res["status"] = res.status | status
+    res["survivals"] = s_out
+    return res
+
+
 def plan_step(step):
     """Run the planner on a ``workloads.StepInputs``."""
     w, c = step.workload, step.cost

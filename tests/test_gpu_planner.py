@@ -409,3 +409,115 @@ def test_plan_pack_fused_matches_separate_calls(dev, name, seed, forced):
         res.append(r)
     for k in res[0]:
         np.testing.assert_array_equal(np.asarray(res[1][k]), np.asarray(res[0][k]), err_msg=k)
+
+
+# ----------------------------------------- planner options ([AVS] §三)
+
+def _options(rng, P):
+    B, g = P["B"], P["gamma"]
+    opt = {}
+    if rng.random() < 0.5:
+        cg = rng.integers(0, 4, B).astype(np.int32)
+        rg = cg.copy()
+        flip = rng.random(B) < 0.3
+        rg[flip] += 1
+        opt["conf_gen"], opt["req_gen"] = cg, rg
+    if rng.random() < 0.5:
+        opt["lagged_z"] = rng.normal(rng.uniform(-1, 3), rng.uniform(0.2, 2), (B, g)).astype(np.float32)
+    if rng.random() < 0.6:
+        hi = B * (g + 1) + 3
+        opt["align_tiers"] = sorted(set(int(x) for x in rng.integers(1, hi + 1, size=int(rng.integers(1, 6)))))
+    return opt
+
+
+def _gpu_plan_ex(dev, P, opt):
+    from confidence_scheduled_speculative_gb300 import api
+    B, g = P["B"], P["gamma"]
+    i32 = dict(dtype=torch.int32, device=dev)
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    out = dict(survivals=torch.zeros((B, g), dtype=torch.float32, device=dev),
+               verify_lens=torch.zeros(B, **i32), budget=torch.zeros(1, **i32),
+               tau_theta=torch.zeros(2, dtype=torch.float64, device=dev),
+               status=torch.zeros(1, **i32))
+    ws = api.workspace(api.dspark_plan_workspace_bytes(B, g), dev)
+    api.dspark_plan_ex(t(P["z"]), t(P["T"]), B=B, gamma=g, survival_eps=P["eps"],
+                       min_verify_len=P["min_len"], max_verify_len=P["max_len"],
+                       forced_budget=P["forced"], cost_kind=P["kind"], cost_M=t(P["M"]),
+                       cost_val=t(P["val"]), bias_ms=P["bias"], alpha_ms=P["alpha"],
+                       workspace=ws, conf_generation=t(opt.get("conf_gen")),
+                       req_generation=t(opt.get("req_gen")),
+                       lagged_conf_logits=t(opt.get("lagged_z")),
+                       align_tiers=opt.get("align_tiers"), **out)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def _oracle_plan_ex(orc, P, opt):
+    return orc.plan_ex(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"], P["kind"],
+                       P["M"], P["val"], P["bias"], P["alpha"], conf_gen=opt.get("conf_gen"),
+                       req_gen=opt.get("req_gen"), lagged_z=opt.get("lagged_z"),
+                       align_tiers=opt.get("align_tiers"))
+
+
+@pytest.mark.parametrize("seed", range(80))
+def test_plan_options_random(dev, orc, seed):
+    """dspark_plan_ex with a random mix of the generation mask, a lagged
+    budget and tier alignment, on both planner paths, against the oracle's
+    composition of the plain planner."""
+    rng = np.random.default_rng(61000 + seed)
+    P = _random_problem(rng)
+    if seed % 4 == 3:  # a dense 1-D table: the rank path
+        B, g = P["B"], P["gamma"]
+        P["kind"] = 0
+        P["M"] = np.arange(B, B + max(B * g + 2, 40), dtype=np.int32)
+        P["val"] = 1.0 / (1e-3 + 2e-6 * P["M"])
+    opt = _options(rng, P)
+    g = _gpu_plan_ex(dev, P, opt)
+    ref = _oracle_plan_ex(orc, P, opt)
+    if compare_plan(f"options/{seed}/{sorted(opt)}", g, ref, P["B"], P["gamma"], P["min_len"]):
+        assert int(g["status"][0]) == ref.status
+
+
+@pytest.mark.parametrize("name", ["dsv4_like", "stress", "mixed"])
+def test_plan_pack_options_workloads(dev, orc, name):
+    """The fused call with every option on a workload: lagged confidences
+    from another seed, a third of the slots stale, alignment to the pack's
+    tiers (the workload's, or powers of two where it has none)."""
+    from confidence_scheduled_speculative_gb300 import api
+    from confidence_scheduled_speculative_gb300.engine import StepConfig, VerifyStep
+    step = wl.make_step(wl.WORKLOADS[name], seed=2)
+    lag = wl.make_step(wl.WORKLOADS[name], seed=3)
+    B, g = step.B, step.gamma
+    rng = np.random.default_rng(9)
+    cg = np.arange(B, dtype=np.int32)
+    rg = cg + (rng.random(B) < 0.33).astype(np.int32)
+    cfg = StepConfig.from_step(step)
+    tiers = list(cfg.tiers) or [1 << i for i in range(4, 16)]
+    cfg.tiers = tiers
+    cfg.capacity = max(cfg.capacity, tiers[-1])
+    vs = VerifyStep(cfg, dev)
+    vs.load_inputs(step)
+    vs.status.zero_()
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    api.dspark_plan_pack(vs.conf_logits, vs.sts_temps, vs.anchor, vs.draft, vs.prefix_lens,
+                         B=B, gamma=g, survival_eps=cfg.survival_eps,
+                         min_verify_len=cfg.min_verify_len, max_verify_len=cfg.max_verify_len,
+                         forced_budget=cfg.forced_budget, cost_kind=cfg.cost_kind,
+                         cost_M=vs.cost_M, cost_val=vs.cost_val, bias_ms=cfg.bias_ms,
+                         alpha_ms=cfg.alpha_ms, tiers=tiers, capacity=cfg.capacity,
+                         survivals=vs.survivals, verify_lens=vs.verify_lens, budget=vs.budget,
+                         tau_theta=vs.tau_theta, packed_ids=vs.packed_ids,
+                         packed_pos=vs.packed_pos, packed_req=vs.packed_req,
+                         packed_src=vs.packed_src, cu_seqlens=vs.cu_seqlens, totals=vs.totals,
+                         status=vs.status, workspace=vs.plan_ws, conf_generation=t(cg),
+                         req_generation=t(rg), lagged_conf_logits=t(lag.conf_logits),
+                         align_to_tiers=True)
+    got = vs.result()
+    w, c = step.workload, step.cost
+    ref = orc.plan_ex(step.conf_logits, step.sts_temps, w.survival_eps, w.min_verify_len, w.max_len,
+                      w.forced_budget, c.kind, c.M, c.val, c.bias_ms, c.alpha_ms, conf_gen=cg,
+                      req_gen=rg, lagged_z=lag.conf_logits, align_tiers=tiers)
+    assert compare_plan(f"options/{name}", got, ref, B, g, w.min_verify_len)
+    p = orc.pack(step.anchor, step.draft, step.prefix_lens, ref.verify_lens, tiers, cfg.capacity)
+    np.testing.assert_array_equal(got["cu_seqlens"], p.cu_seqlens)
+    assert list(got["totals"]) == [p.total, p.padded]

@@ -496,3 +496,91 @@ def test_budget_theta_tie_goes_to_smaller_budget(orc):
     np.testing.assert_array_equal(r.theta_curve, [10.0, 10.0, 8.25])
     assert r.budget == int(np.argmax(r.theta_curve)) == 0
     assert list(r.verify_lens) == [1, 1]
+
+
+# ------------------------------------------------- planner options ([AVS] §三)
+
+def test_plan_ex_without_options_is_the_plan(orc):
+    rng = np.random.default_rng(21)
+    for _ in range(10):
+        B, g = int(rng.integers(1, 7)), int(rng.integers(1, 8))
+        z = rng.normal(1, 1.5, (B, g)).astype(np.float32)
+        T = rng.uniform(0.5, 2, g).astype(np.float32)
+        M = np.sort(rng.choice(np.arange(1, B * (g + 1) + 4), 3, replace=False)).astype(np.int32)
+        val = rng.uniform(0.1, 2, 3)
+        a = orc.plan(z, T, 1e-4, 1, g + 1, -1, 1, M, val, 0.5, 0.2)
+        b = orc.plan_ex(z, T, 1e-4, 1, g + 1, -1, 1, M, val, 0.5, 0.2)
+        assert a.budget == b.budget and a.tau == b.tau and a.theta == b.theta
+        assert np.array_equal(a.verify_lens, b.verify_lens) and np.array_equal(a.survivals, b.survivals)
+        # the same confidences as "lagged" change nothing either
+        c = orc.plan_ex(z, T, 1e-4, 1, g + 1, -1, 1, M, val, 0.5, 0.2, lagged_z=z)
+        assert c.budget == a.budget and np.array_equal(c.verify_lens, a.verify_lens)
+
+
+def test_plan_ex_stale_generation_survives_with_one(orc):
+    """A request whose confidences belong to another generation of its slot
+    plans with survival 1 at every depth: its candidates come first (depth,
+    then request order) and tau grows by exactly 1 per candidate taken."""
+    z = np.full((3, 4), -3.0, np.float32)  # low confidence everywhere
+    T = np.ones(4, np.float32)
+    M = np.array([1, 100], np.int32)
+    val = np.array([1.0, 1.0])  # 1-D SPS constant: theta = tau, largest budget wins
+    res = orc.plan_ex(z, T, 0.5, 1, 5, 2, 0, M, val, conf_gen=[7, 8, 9], req_gen=[7, 1, 9])
+    assert np.all(res.survivals[1] == 1.0) and np.all(res.survivals[[0, 2]] < 0.5)
+    # eps 0.5 keeps only the stale request's candidates; a forced budget of 2
+    # takes its two shallowest depths: tau = B + 2 exactly
+    assert res.budget == 2 and list(res.verify_lens) == [1, 3, 1] and res.tau == 3 + 2
+    fresh = orc.plan_ex(z, T, 0.5, 1, 5, 2, 0, M, val, conf_gen=[7, 8, 9], req_gen=[7, 8, 9])
+    assert fresh.budget == 0 and list(fresh.verify_lens) == [1, 1, 1]
+
+
+def test_plan_ex_lagged_budget_current_allocation(orc):
+    """The budget comes from the lagged confidences, the allocation from the
+    current ones: lens are the top-b of the current order, however the lagged
+    survivals were ranked."""
+    rng = np.random.default_rng(22)
+    for _ in range(20):
+        B, g = int(rng.integers(2, 7)), int(rng.integers(2, 8))
+        z_now = rng.normal(1, 1.5, (B, g)).astype(np.float32)
+        z_lag = rng.normal(0, 2, (B, g)).astype(np.float32)
+        T = np.ones(g, np.float32)
+        M = np.arange(1, B * (g + 1) + 2, dtype=np.int32)
+        val = 1.0 / (1e-3 + rng.uniform(1e-5, 5e-4) * M)
+        lag = orc.plan(z_lag, T, 1e-4, 1, g + 1, -1, 0, M, val)
+        res = orc.plan_ex(z_now, T, 1e-4, 1, g + 1, -1, 0, M, val, lagged_z=z_lag)
+        now = orc.plan(z_now, T, 1e-4, 1, g + 1, lag.budget, 0, M, val)
+        assert res.budget == now.budget == min(lag.budget, now.n_kept)
+        assert np.array_equal(res.verify_lens, now.verify_lens) and res.tau == now.tau
+        # brute force: the top-b of the current order, survival desc, depth, request
+        s = now.survivals
+        cand = sorted(((-float(s[r, k]), k, r) for r in range(B) for k in range(g)
+                       if s[r, k] >= np.float32(1e-4)))[:res.budget]
+        cnt = np.zeros(B, int)
+        for _, _, r in cand:
+            cnt[r] += 1
+        assert list(res.verify_lens) == list(1 + cnt)
+
+
+def test_plan_ex_tier_alignment_paid_padding(orc):
+    """[AVS] §五: 37 real rows replayed at a 64-row tier -- alignment fills
+    the 27 padding rows with the next candidates by survival, never past the
+    tier, and only as far as candidates remain."""
+    B, g = 4, 31
+    z = np.full((B, g), 6.0, np.float32)
+    T = np.ones(g, np.float32)
+    M = np.array([4, 38], np.int32)
+    val = np.array([1000.0, 1.0])  # SPS drops past 37 rows: the plan takes 37
+    tiers = [16, 32, 64, 128]
+    plain = orc.plan_ex(z, T, 1e-4, 1, g + 1, -1, 0, M, val)
+    assert plain.budget == 33 and plain.verify_lens.sum() == 37
+    al = orc.plan_ex(z, T, 1e-4, 1, g + 1, -1, 0, M, val, align_tiers=tiers)
+    assert al.budget == 60 and al.verify_lens.sum() == 64
+    # the extra rows are the next candidates of the order: a superset of the plan
+    assert np.all(al.verify_lens >= plain.verify_lens)
+    # too few candidates left (eps keeps 40): filled as far as they go
+    z2 = np.tile(np.concatenate([np.full(10, 6.0), np.full(g - 10, -20.0)]).astype(np.float32), (B, 1))
+    few = orc.plan_ex(z2, T, 1e-4, 1, g + 1, -1, 0, M, val, align_tiers=tiers)
+    assert few.n_kept == 40 and few.budget == 40 and few.verify_lens.sum() == 44
+    # no tier holds the plan's rows: unchanged
+    none = orc.plan_ex(z, T, 1e-4, 1, g + 1, -1, 0, M, val, align_tiers=[8, 16])
+    assert none.budget == plain.budget and np.array_equal(none.verify_lens, plain.verify_lens)
