@@ -78,6 +78,9 @@ def lib():
             L.orc_pack.argtypes = [i32p, i32p, i32p, i32p, ci, ci, i32p, ci, ci, i32p, i32p, i32p,
                                    i32p, i32p, i32p, i32p]
             L.orc_pack.restype = None
+            L.orc_sampling_accept.argtypes = [f32p, cl, ci, ci, i32p, f32p, cl, i32p, i32p, ci, ci,
+                                              f32p, f32p, i32p, i32p, i32p, i32p, i32p, i32p]
+            L.orc_sampling_accept.restype = None
             u8p = ctypes.POINTER(ctypes.c_uint8)
             L.orc_scatter_rows.argtypes = [u8p, cl, cl, i32p, ci, ci, u8p, cl, ci, i32p]
             L.orc_scatter_rows.restype = None
@@ -342,3 +345,40 @@ def cap_accept(logits, V, lens, draft, prefix):
                       new_seq_lens=o[3], out_tokens=out, ceiling=o[4],
                       sum_commit=int(totals[0]), sum_ceiling=int(totals[1]),
                       status=st | int(st2[0]))
+
+
+def _as_f32_rows(x):
+    """fp32 rows from fp32 or bf16-bit (uint16) logits."""
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        return (x.astype(np.uint32) << 16).view(np.float32)
+    return x.astype(np.float32, copy=False)
+
+
+def sampling_accept(target, V, cu, draft_logits, draft, prefix, u_accept, u_bonus, max_rows=None):
+    """Speculative sampling accept over compact target rows (cu_seqlens) and
+    the draft's proposal rows [B*gamma, ld] (row r*gamma + j = q_j of request
+    r), with the given uniforms u_accept [B, gamma] and u_bonus [B]."""
+    tgt = _as_f32_rows(target)
+    dft = _as_f32_rows(draft_logits)
+    cu = _c(cu, np.int32)
+    draft = _c(draft, np.int32)
+    B, g = draft.shape
+    prefix = _c(prefix, np.int32)
+    ua = _c(u_accept, np.float32)
+    ub = _c(u_bonus, np.float32)
+    max_rows = tgt.shape[0] if max_rows is None else max_rows
+    want = int(cu[B])
+    status = ST_CAPACITY if want > max_rows else 0
+    rows = max(0, min(want, max_rows))
+    o = [np.empty(B, np.int32) for _ in range(4)]
+    out = np.empty((B, g + 1), np.int32)
+    st = np.zeros(1, np.int32)
+    lib().orc_sampling_accept(_ptr(tgt, ctypes.c_float), tgt.shape[1], int(V), rows,
+                              _ptr(cu, ctypes.c_int32), _ptr(dft, ctypes.c_float), dft.shape[1],
+                              _ptr(draft, ctypes.c_int32), _ptr(prefix, ctypes.c_int32), B, g,
+                              _ptr(ua, ctypes.c_float), _ptr(ub, ctypes.c_float),
+                              *[_ptr(x, ctypes.c_int32) for x in o], _ptr(out, ctypes.c_int32),
+                              _ptr(st, ctypes.c_int32))
+    return PlanResult(num_accepted=o[0], bonus=o[1], commit_lens=o[2], new_seq_lens=o[3],
+                      out_tokens=out, status=int(st[0]) | status)

@@ -456,3 +456,116 @@ void orc_scatter_rows(const unsigned char *src, long long ld_src, long long row_
             dst[(long long)d * ld_dst + b] = src[(long long)i * ld_src + b];
     }
 }
+
+/* ------------------------------------------------------------ sampling
+ *
+ * Speculative sampling accept (NEXT-2 of the scope table): [ROUND] §五 names
+ * the path (AcceptSampling: chain speculative sampling over the draft's
+ * proposal probabilities -- the corrected ones that actually produced the
+ * drafts -- and the target probabilities, giving correct_len and the bonus)
+ * and leaves the rule to the speculative algorithm; [AVS] §一 states its
+ * classic form: a draft x drawn from q is accepted with probability
+ * min(1, p(x)/q(x)), so the mean acceptance is sum_x min(p, q) = 1 - TV.
+ * Written out here as the textbook rule: accept draft j iff u_j * q_j(x) <
+ * p_j(x); at the first rejection the bonus is drawn from the residual
+ * max(0, p_j - q_j) (normalised); when every draft is accepted, from the
+ * last row's p.  The draws are inverse-CDF draws with one uniform per
+ * request: the smallest token whose cumulative weight exceeds u * W.
+ *
+ * Arithmetic: logits are fp32 (bf16 widened exactly); m = the row's largest
+ * non-NaN logit; e_y = expf(z_y - m) in fp32 (NaN logits weigh 0 and are
+ * flagged); S = sum of e_y in fp64 in index order; p_y = e_y / S in fp64.
+ */
+
+/* m and S of one row (S in fp64, index order). */
+static double orc_row_norm(const float *z, int V, float *m_out, int *status)
+{
+    float m = -INFINITY;
+    for (int y = 0; y < V; ++y) {
+        if (z[y] != z[y]) { *status |= ORC_ST_NAN_LOGIT; continue; }
+        if (z[y] > m) m = z[y];
+    }
+    double S = 0.0;
+    for (int y = 0; y < V; ++y)
+        if (z[y] == z[y]) S += (double)expf(z[y] - m);
+    *m_out = m;
+    return S;
+}
+
+static double orc_prob(const float *z, int y, float m, double S)
+{
+    if (z[y] != z[y] || !(S > 0.0)) return 0.0;
+    return (double)expf(z[y] - m) / S;
+}
+
+void orc_sampling_accept(const float *tgt, int64_t ld_t, int V, int rows_avail, const int32_t *cu,
+                         const float *dft, int64_t ld_d, const int32_t *draft,
+                         const int32_t *prefix, int B, int gamma, const float *u_acc,
+                         const float *u_bonus, int32_t *num_acc, int32_t *bonus,
+                         int32_t *commit, int32_t *new_seq, int32_t *out, int *status)
+{
+    orc_check_tokens(draft, B, gamma, V, status);
+    double *w = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    for (int r = 0; r < B; ++r) {
+        const int lo = cu[r], hi = cu[r + 1], L = hi - lo;
+        if (lo < 0 || hi > rows_avail || L < 1 || L > gamma + 1) {
+            *status |= ORC_ST_BAD_LEN;
+            num_acc[r] = 0;
+            bonus[r] = -1;
+            commit[r] = 0;
+            if (new_seq) new_seq[r] = prefix[r];
+            for (int j = 0; j < gamma; ++j) out[(size_t)r * (gamma + 1) + j] = draft[(size_t)r * gamma + j];
+            out[(size_t)r * (gamma + 1) + gamma] = -1;
+            continue;
+        }
+        /* acceptance, draft by draft; the chain stops at the first rejection */
+        int correct = L - 1;
+        for (int j = 0; j < L - 1; ++j) {
+            const int x = draft[(size_t)r * gamma + j];
+            const float *zt = tgt + (size_t)(lo + j) * (size_t)ld_t;
+            const float *zd = dft + ((size_t)r * gamma + j) * (size_t)ld_d;
+            float mt, md;
+            const double St = orc_row_norm(zt, V, &mt, status);
+            const double Sd = orc_row_norm(zd, V, &md, status);
+            double p = 0.0, q = 0.0;
+            if (x >= 0 && x < V) {
+                p = orc_prob(zt, x, mt, St);
+                q = orc_prob(zd, x, md, Sd);
+            }
+            if (!((double)u_acc[(size_t)r * gamma + j] * q < p)) { correct = j; break; }
+        }
+        /* the bonus: residual of row `correct` after a rejection, else p of the last row */
+        const float *zt = tgt + (size_t)(lo + correct) * (size_t)ld_t;
+        float mt, md = 0.0f;
+        const double St = orc_row_norm(zt, V, &mt, status);
+        const int rejected = correct < L - 1;
+        const float *zd = rejected ? dft + ((size_t)r * gamma + correct) * (size_t)ld_d : NULL;
+        const double Sd = rejected ? orc_row_norm(zd, V, &md, status) : 0.0;
+        double W = 0.0;
+        for (int y = 0; y < V; ++y) {
+            double p = orc_prob(zt, y, mt, St);
+            double v = p;
+            if (rejected) {
+                v = p - orc_prob(zd, y, md, Sd);
+                if (v < 0.0) v = 0.0;
+            }
+            w[y] = v;
+            W += v;
+        }
+        if (!(W > 0.0)) { /* p == q: the residual is empty, draw from p */
+            W = 0.0;
+            for (int y = 0; y < V; ++y) { w[y] = orc_prob(zt, y, mt, St); W += w[y]; }
+        }
+        const double target = (double)u_bonus[r] * W;
+        int tok = -1, last_pos = -1;
+        double C = 0.0;
+        for (int y = 0; y < V; ++y) {
+            if (w[y] > 0.0) last_pos = y;
+            C += w[y];
+            if (C > target) { tok = y; break; }
+        }
+        if (tok < 0) tok = last_pos;
+        orc_finish(r, correct, tok, draft, prefix, gamma, num_acc, bonus, commit, new_seq, out);
+    }
+    free(w);
+}

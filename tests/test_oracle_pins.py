@@ -584,3 +584,87 @@ def test_plan_ex_tier_alignment_paid_padding(orc):
     # no tier holds the plan's rows: unchanged
     none = orc.plan_ex(z, T, 1e-4, 1, g + 1, -1, 0, M, val, align_tiers=[8, 16])
     assert none.budget == plain.budget and np.array_equal(none.verify_lens, plain.verify_lens)
+
+
+# ------------------------------------------------ sampling accept (NEXT-2)
+
+def _logp(p):
+    with np.errstate(divide="ignore"):
+        return np.log(np.asarray(p, np.float64)).astype(np.float32)
+
+
+def test_sampling_accept_hand_case(orc):
+    """p = [.5, .3, .2, 0], q uniform, draft token 3 (p = 0): rejected at
+    any u; the residual max(0, p - q) = [.25, .05, 0, 0] (W = .3) gives token
+    1 for u = .9 (.27 lies in (.25, .30]) and token 0 for u = .5."""
+    tgt = np.stack([_logp([.5, .3, .2, 0]), _logp([.1, .2, .3, .4])])
+    dft = np.zeros((1, 4), np.float32)  # uniform q
+    for ub, tok in ((0.9, 1), (0.5, 0)):
+        r = orc.sampling_accept(tgt, 4, [0, 2], dft, [[3]], [10], [[0.5]], [ub])
+        assert r.num_accepted[0] == 0 and r.bonus[0] == tok and r.commit_lens[0] == 1
+        assert list(r.out_tokens[0]) == [tok, -1] and r.new_seq_lens[0] == 11
+    # accepted when u * q < p: draft 0 (p = .5, q = .25) always, then the
+    # bonus comes from the last row's p: C = .1, .3, .6, 1.0 and u = .65 -> 3
+    r = orc.sampling_accept(tgt, 4, [0, 2], dft, [[0]], [10], [[0.99]], [0.65])
+    assert r.num_accepted[0] == 1 and r.bonus[0] == 3 and list(r.out_tokens[0]) == [0, 3]
+
+
+def test_sampling_accept_equal_distributions_always_accept(orc):
+    rng = np.random.default_rng(31)
+    B, g, V = 50, 4, 16
+    rows = rng.normal(0, 2, (B * g, V)).astype(np.float32)
+    tgt = np.zeros((B * (g + 1), V), np.float32)
+    for r in range(B):
+        tgt[r * (g + 1):r * (g + 1) + g] = rows[r * g:(r + 1) * g]
+    cu = np.arange(0, B * (g + 1) + 1, g + 1, dtype=np.int32)
+    draft = rng.integers(0, V, (B, g)).astype(np.int32)
+    res = orc.sampling_accept(tgt, V, cu, rows, draft, np.zeros(B), rng.random((B, g)), rng.random(B))
+    assert np.all(res.num_accepted == g) and res.status == 0
+
+
+def test_sampling_accept_rate_is_one_minus_tv(orc):
+    """Drafts drawn from q are accepted with mean probability sum min(p, q)
+    = 1 - TV(p, q) ([AVS] §一): Monte Carlo over 40000 requests."""
+    rng = np.random.default_rng(32)
+    V, n = 6, 40000
+    p = rng.dirichlet(np.ones(V))
+    q = rng.dirichlet(np.ones(V))
+    tgt = np.tile(_logp(p), (2 * n, 1))
+    dft = np.tile(_logp(q), (n, 1))
+    draft = rng.choice(V, size=(n, 1), p=q).astype(np.int32)
+    cu = np.arange(0, 2 * n + 1, 2, dtype=np.int32)
+    res = orc.sampling_accept(tgt, V, cu, dft, draft, np.zeros(n), rng.random((n, 1)), rng.random(n))
+    rate = res.num_accepted.mean()
+    want = np.minimum(p, q).sum()
+    assert abs(rate - want) < 4 * np.sqrt(want * (1 - want) / n), (rate, want)
+
+
+def test_sampling_accept_output_is_distributed_as_p(orc):
+    """The point of the rule: with the draft drawn from q, the first token
+    the request commits (the accepted draft, or the bonus drawn from the
+    residual) is distributed exactly as p.  Chi-square over 60000 draws; a
+    residual of max(0, q - p) or an unnormalised draw fails it."""
+    rng = np.random.default_rng(33)
+    V, n = 5, 60000
+    p = np.array([0.35, 0.05, 0.3, 0.2, 0.1])
+    q = np.array([0.1, 0.4, 0.1, 0.25, 0.15])
+    tgt = np.tile(_logp(p), (2 * n, 1))
+    dft = np.tile(_logp(q), (n, 1))
+    draft = rng.choice(V, size=(n, 1), p=q).astype(np.int32)
+    cu = np.arange(0, 2 * n + 1, 2, dtype=np.int32)
+    res = orc.sampling_accept(tgt, V, cu, dft, draft, np.zeros(n), rng.random((n, 1)), rng.random(n))
+    first = res.out_tokens[:, 0]
+    counts = np.bincount(first, minlength=V)
+    chi2 = float(((counts - n * p) ** 2 / (n * p)).sum())
+    assert chi2 < 20.5, (chi2, counts / n)  # 4 degrees of freedom, p-value 4e-4
+
+
+def test_sampling_accept_flags(orc):
+    tgt = np.zeros((2, 4), np.float32)
+    tgt[0, 2] = np.nan
+    dft = np.zeros((1, 4), np.float32)
+    r = orc.sampling_accept(tgt, 4, [0, 2], dft, [[7]], [0], [[0.1]], [0.5])
+    assert r.status & orc.ST_NAN_LOGIT and r.status & orc.ST_TOKEN_RANGE
+    assert r.num_accepted[0] == 0  # an out-of-range draft has p = q = 0: rejected
+    bad = orc.sampling_accept(tgt, 4, [0, 3], dft, [[1]], [5], [[0.1]], [0.5])
+    assert bad.status & orc.ST_BAD_LEN and bad.bonus[0] == -1 and bad.new_seq_lens[0] == 5
