@@ -88,7 +88,7 @@ def ncu_traffic(workload: str):
     if not d:
         return None
     h = hashlib.sha256()
-    for rel in ("csrc/accept.cu", "csrc/dspark_common.cuh"):
+    for rel in ("csrc/accept.cu", "csrc/logits.cuh", "csrc/dspark_common.cuh"):
         with open(os.path.join(ROOT, "confidence_scheduled_speculative_gb300", rel), "rb") as f:
             h.update(f.read())
     return d["bytes_per_launch"] if h.hexdigest() == d.get("sources_sha256") else None
@@ -450,6 +450,52 @@ def run_ours(args):
                 "status": int(st_s.item())}
         del scat_dst
 
+    # ---- speculative sampling accept over the same packed rows (secondary):
+    # draft proposal rows = the strided target rows of the same depth, so
+    # drafts pass often; calls back to back
+    samp = None
+    if not args.no_cap:
+        from confidence_scheduled_speculative_gb300 import api as _api
+        g_ = w.gamma
+        sel = torch.arange(w.B * g_, device=dev)
+        sel = (sel // g_) * (g_ + 1) + sel % g_
+        dft_dev = strided_dev.index_select(0, sel)
+        gen = torch.Generator(device=dev).manual_seed(11)
+        ua = torch.rand((w.B, g_), generator=gen, device=dev)
+        ub = torch.rand((w.B,), generator=gen, device=dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        so = dict(num_accepted=torch.zeros(w.B, **i32), bonus=torch.zeros(w.B, **i32),
+                  commit_lens=torch.zeros(w.B, **i32), new_seq_lens=torch.zeros(w.B, **i32),
+                  out_tokens=torch.zeros((w.B, g_ + 1), **i32))
+        st_p = torch.zeros(1, **i32)
+        sws = _api.workspace(_api.dspark_sampling_workspace_bytes(compact.size(0), w.B, g_), dev)
+
+        def samp_call():
+            _api.dspark_sampling_accept(compact, dft_dev, V=w.V, cu_seqlens=vs.cu_seqlens,
+                                        draft=vs.draft, prefix_lens=vs.prefix_lens, B=w.B,
+                                        gamma=g_, u_accept=ua, u_bonus=ub, workspace=sws,
+                                        status=st_p, **so)
+
+        for _ in range(3):
+            samp_call()
+        n_p = min(K, 200)
+        pe = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        pe[0].record(stream)
+        for _ in range(n_p):
+            samp_call()
+        pe[1].record(stream)
+        torch.cuda.synchronize()
+        p_us = pe[0].elapsed_time(pe[1]) * 1e3 / n_p
+        tested = int((torch.diff(vs.cu_seqlens) - 1).clamp(min=0).sum().item())
+        p_bytes = (total + tested) * w.V * w.elem_bytes  # the normalizer's rows, read once
+        samp = {"us": p_us, "target_rows": total, "draft_rows": tested,
+                "normalizer_bytes": p_bytes,
+                "gbs_normalizer_bytes": p_bytes / (p_us * 1e-6) / 1e9,
+                "frac_of_peak": p_bytes / (p_us * 1e-6) / 1e9 / load_peaks()[0],
+                "mean_accepted": float(so["num_accepted"].float().mean().item()),
+                "status": int(st_p.item())}
+        del dft_dev, sws
+
     # ---- cap-accept over the full strided block (secondary)
     cap = None
     if not args.no_cap:
@@ -549,6 +595,7 @@ def run_ours(args):
                          "accept_back_to_back_gbs": accept_bytes / (acc_b2b_us * 1e-6) / 1e9},
         "cuda_graph": graph,
         "scatter_compact_to_strided": scat,
+        "sampling_accept": samp,
         "cap_accept": cap,
         "status": status,
     }

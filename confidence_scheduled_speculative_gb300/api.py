@@ -93,6 +93,10 @@ _SIGS = {
                                         _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
     "dspark_scatter_compact_to_strided": (ctypes.c_int, [_VP, _I64, _I32, _I32, _VP, _VP, _I32,
                                                          _VP, _I64, _I32, _VP, _VP]),
+    "dspark_sampling_workspace_bytes": (_SZ, [_I32, _I32, _I32]),
+    "dspark_sampling_accept": (ctypes.c_int, [_VP, _I32, _I64, _I32, _I32, _VP, _VP, _I64, _VP,
+                                              _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                              _VP, _SZ, _VP, _VP]),
     "dspark_accept_workspace_bytes": (_SZ, [_I32, _I32]),
     "dspark_greedy_accept": (ctypes.c_int, [_VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP, _I32,
                                             _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP,
@@ -327,6 +331,34 @@ def dspark_greedy_accept(logits, *, V, cu_seqlens, draft, prefix_lens, B, gamma,
         _p(workspace), workspace.numel() * workspace.element_size(),
         _p(status, torch.int32, "status"), _stream(stream))
     _check("dspark_greedy_accept", rc)
+
+
+def dspark_sampling_workspace_bytes(max_rows: int, B: int, gamma: int) -> int:
+    return int(load().dspark_sampling_workspace_bytes(max_rows, B, gamma))
+
+
+def dspark_sampling_accept(logits, draft_logits, *, V, cu_seqlens, draft, prefix_lens, B, gamma,
+                           u_accept, u_bonus, num_accepted, bonus, commit_lens, out_tokens,
+                           workspace, status, new_seq_lens=None, max_rows=None,
+                           stream=None) -> None:
+    """Speculative sampling accept: packed target rows ``logits`` and the
+    draft's proposal rows ``draft_logits`` [B*gamma, >= V] (same dtype);
+    ``u_accept`` [B, gamma] and ``u_bonus`` [B] are fp32 uniforms."""
+    ptr, ld = _logits_ptr(logits, V)
+    dptr, dld = _logits_ptr(draft_logits, V)
+    if draft_logits.dtype != logits.dtype:
+        raise ValueError("draft_logits: expected the dtype of logits")
+    max_rows = logits.size(0) if max_rows is None else max_rows
+    rc = load().dspark_sampling_accept(
+        ptr, _dtype_code(logits), ld, V, max_rows, _p(cu_seqlens, torch.int32, "cu_seqlens"),
+        dptr, dld, _p(draft, torch.int32, "draft"), _p(prefix_lens, torch.int32, "prefix_lens"),
+        B, gamma, _p(u_accept, torch.float32, "u_accept"), _p(u_bonus, torch.float32, "u_bonus"),
+        _p(num_accepted, torch.int32, "num_accepted"), _p(bonus, torch.int32, "bonus"),
+        _p(commit_lens, torch.int32, "commit_lens"), _p(new_seq_lens, torch.int32, "new_seq_lens"),
+        _p(out_tokens, torch.int32, "out_tokens"), _p(workspace),
+        workspace.numel() * workspace.element_size(), _p(status, torch.int32, "status"),
+        _stream(stream))
+    _check("dspark_sampling_accept", rc)
 
 
 def dspark_cap_accept(logits, *, V, verify_lens, draft, prefix_lens, B, gamma, num_accepted,

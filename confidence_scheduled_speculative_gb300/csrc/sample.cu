@@ -1,0 +1,592 @@
+// sample.cu -- speculative sampling accept (compact mode) on sm_103a.
+//
+// Pages (by title and section):
+//   [ROUND] "DeepSeek-V4 DSpark一轮 Draft、Verify、Accept 与 Commit", §五
+//           (AcceptSampling: chain speculative sampling over the draft's
+//           proposal probabilities -- the corrected ones that produced the
+//           drafts -- and the target probabilities, giving correct_len and
+//           the bonus; then FinalizeAcceptLens / BuildOutTokens as in the
+//           greedy path)
+//   [AVS]   "DSpark 自适应 Verify 怎样分配候选预算", §一 (a draft drawn from q
+//           is accepted with probability min(1, p/q); mean acceptance
+//           sum min(p, q) = 1 - TV)
+//
+// The rule, as the pages' classic form: draft j of request r (token x) is
+// accepted iff u_j * q_j(x) < p_j(x), p_j = softmax of packed target row
+// cu[r] + j, q_j = softmax of draft row r*gamma + j; at the first rejection
+// the bonus is the inverse-CDF draw (uniform u_bonus[r]) from the residual
+// max(0, p_j - q_j), normalised; when every draft is accepted, from the
+// last row's p.  An empty residual (p == q) draws from p.
+//
+// Two kernels:
+//   softmax_norm_kernel  HBM-bound: for every packed target row and every
+//     draft row some test reads (j < len - 1), the row max m and S = sum
+//     exp(z - m).  The target rows, then the draft rows in (request, depth)
+//     order, form one list of "virtual rows", flattened into 16-byte chunks
+//     and split into one equal contiguous range per CTA of a persistent grid
+//     (as the greedy argmax does); each (CTA, row) piece leaves a partial
+//     (m, S) at slot CTA + row.  Per thread an online max / sum of exps
+//     (hardware ex2), combined per piece in fp64.
+//   sampling_accept_kernel  one CTA per request: combines the partials of its
+//     rows, runs the acceptance tests (warp 0, one lane per draft), then
+//     draws the bonus: the residual (or p) of the bonus row is summed in
+//     rounds of 256 tokens, one warp per contiguous eighth of the
+//     vocabulary, and the round holding u * W is searched token by token.
+// Sums of exps are fp32 per thread and fp64 beyond, so p and q agree with
+// an fp64 index-order evaluation to about 1e-6 relative: decisions can
+// differ from such an evaluation only when u * q and p (or u * W and a
+// cumulative weight) are that close.
+
+#include "dspark_common.cuh"
+#include "logits.cuh"
+
+namespace dspark {
+
+constexpr int kNormThreads = 256;
+constexpr int kNormCtasPerSm = 4;
+constexpr int kNormUnroll = 4;
+constexpr int kSampThreads = 256;
+constexpr int kSampWarps = kSampThreads / 32;
+constexpr int kSampMaxB = 4096;   // cu_seqlens staged in shared memory by every CTA
+constexpr int kSampMaxCtas = 4096;
+constexpr int kRound = 256;       // tokens per round of the bonus draw (32 lanes x 8)
+constexpr int kMaxRounds = 512;   // rounds per warp: V / 8 / 256 for V <= 1M
+
+struct NormPartial {
+    float m;     // largest logit of the piece (-inf: none)
+    float pad;
+    double s;    // sum of exp(z - m) over the piece
+};
+
+struct SampArgs {
+    const void *tgt;
+    long long ld_t;  // elements
+    const void *dft;
+    long long ld_d;
+    int V, B, gamma, max_rows;
+    const int32_t *cu, *draft, *prefix;
+    const float *u_acc, *u_bonus;
+    int32_t *num_acc, *bonus, *commit, *new_seq, *out, *status;
+    NormPartial *part;  // [kSampMaxCtas + max_rows + B*gamma + 1]
+    int32_t *dcu;       // [B+1] first virtual draft row of each request (written by CTA 0)
+    int grid;           // normalizer grid size
+};
+
+__device__ __forceinline__ int samp_rows(const SampArgs &a) {
+    const int r = a.cu[a.B];
+    return r < 0 ? 0 : (r > a.max_rows ? a.max_rows : r);
+}
+
+// A request reads packed rows [lo, hi) with 1 <= hi - lo <= gamma + 1.
+__device__ __forceinline__ bool samp_valid(int lo, int hi, int rows, int gamma) {
+    return lo >= 0 && hi <= rows && hi - lo >= 1 && hi - lo <= gamma + 1;
+}
+
+// Online (max, sum of exps) of one value; NaN counts as -inf.
+__device__ __forceinline__ void norm_take(float z, float &m, float &s) {
+    if (z > m) {
+        s = s * __expf(m - z) + 1.0f;
+        m = z;
+    } else if (z > -INFINITY) {
+        s += __expf(z - m);
+    }
+}
+
+// One 16-byte chunk into the thread's running (m, s): the chunk max first,
+// one rescale, then one exp per value.
+template <typename T>
+__device__ __forceinline__ void norm_chunk(const uint4 &v, float &m, float &s, bool &nan) {
+    constexpr int E = Elem<T>::kPerChunk;
+    float z[E];
+    float cm = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        z[e] = Elem<T>::at(v, e);
+        nan |= z[e] != z[e];
+        cm = fmaxf(cm, z[e]);  // NaN ignored
+    }
+    if (cm > m) {
+        s *= __expf(m - cm);
+        m = cm;
+    }
+    if (m > -INFINITY) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) s += (z[e] == z[e]) ? __expf(z[e] - m) : 0.0f;
+    }
+}
+
+// Block-wide combine of the threads' (m, s); thread 0 writes the piece's
+// partial.  Contains __syncthreads(): every thread calls it.
+__device__ void norm_block(float m, float s, float *red_m, double *red_s, NormPartial *dst) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float M = m;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, d));
+    if (lane == 0) red_m[warp] = M;
+    __syncthreads();
+    M = red_m[0];
+#pragma unroll
+    for (int w = 1; w < kNormThreads / 32; ++w) M = fmaxf(M, red_m[w]);
+    double t = (m > -INFINITY) ? (double)(s * __expf(m - M)) : 0.0;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) t += __shfl_xor_sync(kFullMask, t, d);
+    if (lane == 0) red_s[warp] = t;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double S = 0.0;
+        for (int w = 0; w < kNormThreads / 32; ++w) S += red_s[w];
+        *dst = NormPartial{M, 0.0f, M > -INFINITY ? S : 0.0};
+    }
+    __syncthreads();
+}
+
+// Virtual row v: a packed target row (v < rows) or the draft row of the
+// (v - rows)-th draft a test reads, in (request, depth) order; dcu[r] is the
+// first such draft of request r.  Returns the element offset of the row in
+// its buffer and whether it is a draft row.
+__device__ __forceinline__ long long virtual_row(const SampArgs &a, const int32_t *dcu, int rows,
+                                                 int v, bool &is_draft) {
+    if (v < rows) {
+        is_draft = false;
+        return (long long)v * a.ld_t;
+    }
+    is_draft = true;
+    const int d = v - rows;
+    int lo = 0, hi = a.B - 1;  // the last request whose first draft row is <= d
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (dcu[mid] <= d) lo = mid;
+        else hi = mid - 1;
+    }
+    const int j = d - dcu[lo];  // < its number of tested drafts <= gamma
+    return ((long long)lo * a.gamma + j) * a.ld_d;
+}
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) softmax_norm_kernel(SampArgs a) {
+    extern __shared__ int32_t dcu[];  // [B+1]
+    __shared__ float red_m[kNormThreads / 32];
+    __shared__ double red_s[kNormThreads / 32];
+    __shared__ int scan32[40];
+    __shared__ long long row_off;
+    __shared__ int row_draft;
+    constexpr int EPC = VEC ? Elem<T>::kPerChunk : 1;
+    const int tid = threadIdx.x;
+    const int B = a.B, G = a.gamma;
+
+    pdl_trigger();
+    pdl_wait();  // cu_seqlens and the logits come from the kernels before
+    const int rows = samp_rows(a);
+    if (blockIdx.x == 0 && tid == 0 && a.cu[B] > a.max_rows) flag(a.status, DSPARK_STATUS_CAPACITY);
+    // the tested drafts of each valid request, scanned: dcu
+    {
+        const int per = (B + kNormThreads - 1) / kNormThreads;
+        const int q0 = min(tid * per, B), q1 = min(q0 + per, B);
+        int mine = 0;
+        for (int q = q0; q < q1; ++q) {
+            const int lo = a.cu[q], hi = a.cu[q + 1];
+            mine += samp_valid(lo, hi, rows, G) ? hi - lo - 1 : 0;
+        }
+        int total;
+        int off = block_exclusive_scan<int>(mine, scan32, &total);
+        for (int q = q0; q < q1; ++q) {
+            dcu[q] = off;
+            const int lo = a.cu[q], hi = a.cu[q + 1];
+            off += samp_valid(lo, hi, rows, G) ? hi - lo - 1 : 0;
+        }
+        if (tid == 0) dcu[B] = total;
+        __syncthreads();
+        if (blockIdx.x == 0)
+            for (int q = tid; q <= B; q += kNormThreads) a.dcu[q] = dcu[q];
+    }
+    const int VR = rows + dcu[B];
+    const int cpr = (a.V + EPC - 1) / EPC;  // chunks per row, the last maybe partial
+    const int full = a.V / EPC;
+    const long long W = (long long)VR * cpr;
+    const long long per = (W + a.grid - 1) / a.grid;
+    const long long q0 = (long long)blockIdx.x * per;
+    const long long q1 = min(q0 + per, W);
+    bool nan = false;
+    for (long long q = q0; q < q1;) {
+        const int v = (int)(q / cpr);
+        const int c0 = (int)(q - (long long)v * cpr);
+        const long long seg_end = min(q1, (long long)(v + 1) * cpr);
+        const int c1 = c0 + (int)(seg_end - q);
+        if (tid == 0) {
+            bool is_draft;
+            row_off = virtual_row(a, dcu, rows, v, is_draft);
+            row_draft = is_draft ? 1 : 0;
+        }
+        __syncthreads();
+        const T *row = reinterpret_cast<const T *>(row_draft ? a.dft : a.tgt) + row_off;
+        float m = -INFINITY, s = 0.0f;
+        if (VEC) {
+            const uint4 *row4 = reinterpret_cast<const uint4 *>(row);
+            const int cf = min(c1, full);
+            int c = c0 + tid;
+            for (; c + (kNormUnroll - 1) * kNormThreads < cf; c += kNormUnroll * kNormThreads) {
+                uint4 x[kNormUnroll];
+#pragma unroll
+                for (int u = 0; u < kNormUnroll; ++u) x[u] = ld_stream16(row4 + c + u * kNormThreads);
+#pragma unroll
+                for (int u = 0; u < kNormUnroll; ++u) norm_chunk<T>(x[u], m, s, nan);
+            }
+            for (; c < cf; c += kNormThreads) norm_chunk<T>(ld_stream16(row4 + c), m, s, nan);
+            // the row's partial last chunk, element by element
+            if (c1 > full && tid == 0)
+                for (int e = full * EPC; e < a.V; ++e) {
+                    const float z = Elem<T>::load(row + e);
+                    nan |= z != z;
+                    norm_take(z, m, s);
+                }
+        } else {
+            for (int e = c0 + tid; e < c1; e += kNormThreads) {
+                const float z = Elem<T>::load(row + e);
+                nan |= z != z;
+                norm_take(z, m, s);
+            }
+        }
+        norm_block(m, s, red_m, red_s, a.part + blockIdx.x + v);
+        q = seg_end;
+    }
+    if (__syncthreads_or(nan) && tid == 0) flag(a.status, DSPARK_STATUS_NAN_LOGIT);
+}
+
+// ---------------------------------------------------- acceptance and bonus
+
+// (M, S) of virtual row v from the partials of the CTAs that covered it.
+__device__ __forceinline__ void row_stats(const NormPartial *part, long long cpr, long long per,
+                                          int v, float &M, double &S) {
+    const long long q_first = (long long)v * cpr;
+    const int c_lo = (int)(q_first / per), c_hi = (int)((q_first + cpr - 1) / per);
+    M = -INFINITY;
+    for (int c = c_lo; c <= c_hi; ++c) M = fmaxf(M, part[c + v].m);
+    S = 0.0;
+    if (M > -INFINITY)
+        for (int c = c_lo; c <= c_hi; ++c) {
+            const NormPartial p = part[c + v];
+            if (p.m > -INFINITY) S += p.s * (double)__expf(p.m - M);
+        }
+}
+
+// p(y) of a row with statistics (M, S) from its logit z.
+__device__ __forceinline__ double row_prob(float z, float M, double S) {
+    return (z == z && S > 0.0) ? (double)__expf(z - M) / S : 0.0;
+}
+
+// Weights of the bonus draw are summed exactly as integers in units of 2^-40.
+__device__ __forceinline__ unsigned long long quantize(float w) {
+    return w > 0.0f ? (unsigned long long)__float2ull_rn(w * 1099511627776.0f) : 0ull;
+}
+
+struct BonusRow {
+    const void *t;  // target row
+    const void *d;  // draft row (residual) or null (p)
+    float mt, md;
+    float inv_st, inv_sd;
+};
+
+// Weight of token y in the bonus draw, fp32.
+template <typename T>
+__device__ __forceinline__ float bonus_weight(const BonusRow &b, int y) {
+    const float zt = Elem<T>::load(reinterpret_cast<const T *>(b.t) + y);
+    float w = (zt == zt) ? __expf(zt - b.mt) * b.inv_st : 0.0f;
+    if (b.d) {
+        const float zd = Elem<T>::load(reinterpret_cast<const T *>(b.d) + y);
+        const float q = (zd == zd) ? __expf(zd - b.md) * b.inv_sd : 0.0f;
+        w = fmaxf(w - q, 0.0f);
+    }
+    return w;
+}
+
+// The 8 tokens y0..y0+7 of one lane in one round: quantized weights summed,
+// and the last token with a positive weight (or -1).
+template <typename T>
+__device__ __forceinline__ unsigned long long lane_round(const BonusRow &b, int y0, int V,
+                                                         int &last_pos) {
+    unsigned long long acc = 0ull;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const int y = y0 + e;
+        if (y < V) {
+            const unsigned long long wq = quantize(bonus_weight<T>(b, y));
+            acc += wq;
+            if (wq) last_pos = y;
+        }
+    }
+    return acc;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs a, int epc) {
+    __shared__ unsigned long long rsum[kSampWarps * kMaxRounds];  // weight of each round
+    __shared__ int last_w[kSampWarps];
+    __shared__ BonusRow brow;
+    __shared__ int s_correct, s_round, s_retry;
+    __shared__ unsigned long long s_pre, s_target;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r = blockIdx.x;
+    const int G = a.gamma, V = a.V;
+    // drafts and uniforms are step inputs: fetch them before the wait
+    const int dj = (warp == 0 && lane < G) ? __ldg(a.draft + (size_t)r * G + lane) : -1;
+    const float uj = (warp == 0 && lane < G) ? __ldg(a.u_acc + (size_t)r * G + lane) : 1.0f;
+    pdl_trigger();
+    pdl_wait();  // partials and dcu come from softmax_norm_kernel
+
+    const int rows = samp_rows(a);
+    const int lo = a.cu[r], hi = a.cu[r + 1], L = hi - lo;
+    if (warp == 0 && __any_sync(kFullMask, lane < G && (dj < 0 || dj >= V)) && lane == 0)
+        flag(a.status, DSPARK_STATUS_TOKEN_RANGE);
+    if (!samp_valid(lo, hi, rows, G)) {
+        if (tid == 0) {
+            flag(a.status, DSPARK_STATUS_BAD_LEN);
+            a.num_acc[r] = 0;
+            a.bonus[r] = -1;
+            a.commit[r] = 0;
+            if (a.new_seq) a.new_seq[r] = __ldg(a.prefix + r);
+        }
+        if (warp == 0 && lane <= G) a.out[(size_t)r * (G + 1) + lane] = lane < G ? dj : -1;
+        return;
+    }
+    const int D = a.dcu[a.B];
+    const long long cpr = (V + epc - 1) / epc;
+    const long long W = (long long)(rows + D) * cpr;
+    const long long per = (W + a.grid - 1) / a.grid;
+    const int vd0 = rows + a.dcu[r];  // virtual row of this request's first tested draft
+
+    // (1) acceptance tests: lane j tests draft j < L - 1
+    if (warp == 0) {
+        bool accept = true;
+        if (lane < L - 1) {
+            accept = false;
+            if (dj >= 0 && dj < V) {
+                float mt, md;
+                double st, sd;
+                row_stats(a.part, cpr, per, lo + lane, mt, st);
+                row_stats(a.part, cpr, per, vd0 + lane, md, sd);
+                const T *zt = reinterpret_cast<const T *>(a.tgt) + (long long)(lo + lane) * a.ld_t;
+                const T *zd = reinterpret_cast<const T *>(a.dft) + ((long long)r * G + lane) * a.ld_d;
+                const double p = row_prob(Elem<T>::load(zt + dj), mt, st);
+                const double q = row_prob(Elem<T>::load(zd + dj), md, sd);
+                accept = (double)uj * q < p;
+            }
+        }
+        const unsigned rej = __ballot_sync(kFullMask, !accept);
+        const int correct = rej ? __ffs(rej) - 1 : L - 1;
+        if (lane == 0) {
+            s_correct = correct;
+            float mt, md = 0.0f;
+            double st, sd = 0.0;
+            row_stats(a.part, cpr, per, lo + correct, mt, st);
+            const bool rejected = correct < L - 1;
+            if (rejected) row_stats(a.part, cpr, per, vd0 + correct, md, sd);
+            brow.t = reinterpret_cast<const T *>(a.tgt) + (long long)(lo + correct) * a.ld_t;
+            brow.d = rejected ? reinterpret_cast<const T *>(a.dft) + ((long long)r * G + correct) * a.ld_d
+                              : nullptr;
+            brow.mt = mt;
+            brow.md = md;
+            brow.inv_st = st > 0.0 ? (float)(1.0 / st) : 0.0f;
+            brow.inv_sd = sd > 0.0 ? (float)(1.0 / sd) : 0.0f;
+        }
+    }
+    __syncthreads();
+    const int correct = s_correct;
+
+    // (2) the bonus draw: round sums of the quantized weights, one warp per
+    // contiguous share of the vocabulary; an empty residual draws from p
+    const int per_warp = (int)((((long long)V + kSampWarps - 1) / kSampWarps + kRound - 1) / kRound) * kRound;
+    const int nr = per_warp / kRound;  // rounds per warp (<= kMaxRounds: V is bounded on the host)
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        const BonusRow b = brow;
+        int last_pos = -1;
+        for (int k = 0; k < nr; ++k) {
+            const int y0 = warp * per_warp + k * kRound + lane * 8;
+            unsigned long long s = lane_round<T>(b, y0, V, last_pos);
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) s += __shfl_xor_sync(kFullMask, s, d);
+            if (lane == 0) rsum[warp * nr + k] = s;
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) last_pos = max(last_pos, __shfl_xor_sync(kFullMask, last_pos, d));
+        if (lane == 0) last_w[warp] = last_pos;
+        __syncthreads();
+        // warp 0: the total, the target u * W, and the round it falls in
+        if (warp == 0) {
+            const int nt = kSampWarps * nr;
+            const int nb = (nt + 31) / 32;
+            unsigned long long mine = 0ull;
+            for (int i = lane * nb; i < min(nt, (lane + 1) * nb); ++i) mine += rsum[i];
+            unsigned long long incl = mine;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const unsigned long long o = __shfl_up_sync(kFullMask, incl, d);
+                if (lane >= d) incl += o;
+            }
+            const unsigned long long Wq = __shfl_sync(kFullMask, incl, 31);
+            if (Wq == 0ull && brow.d != nullptr) {  // p == q: the residual is empty
+                if (lane == 0) {
+                    brow.d = nullptr;
+                    s_retry = 1;
+                }
+            } else {
+                const unsigned long long target =
+                    (unsigned long long)((double)__ldg(a.u_bonus + r) * (double)Wq);
+                const unsigned found = __ballot_sync(kFullMask, incl > target);
+                int round = -1;
+                unsigned long long pre = 0ull;
+                if (found) {
+                    const int fl = __ffs(found) - 1;
+                    if (lane == fl) {
+                        unsigned long long c = incl - mine;
+                        for (int i = lane * nb; i < min(nt, (lane + 1) * nb); ++i) {
+                            if (c + rsum[i] > target) {
+                                round = i;
+                                break;
+                            }
+                            c += rsum[i];
+                        }
+                        pre = c;
+                    }
+                    round = __shfl_sync(kFullMask, round, fl);
+                    pre = __shfl_sync(kFullMask, pre, fl);
+                }
+                if (lane == 0) {
+                    s_retry = 0;
+                    s_round = round;
+                    s_pre = pre;
+                    s_target = target;
+                }
+            }
+        }
+        __syncthreads();
+        if (!s_retry) break;
+    }
+
+    // (3) warp 0: the token within the round; then FinalizeAcceptLens and
+    // BuildOutTokens
+    if (warp == 0) {
+        const int round = s_round;
+        int tok = -1;
+        if (round >= 0) {
+            const BonusRow b = brow;
+            const int w = round / nr, k = round - w * nr;
+            const int y0 = w * per_warp + k * kRound + lane * 8;
+            int dummy = -1;
+            const unsigned long long mine = lane_round<T>(b, y0, V, dummy);
+            unsigned long long incl = mine;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const unsigned long long o = __shfl_up_sync(kFullMask, incl, d);
+                if (lane >= d) incl += o;
+            }
+            const unsigned long long target = s_target, pre = s_pre;
+            const unsigned found = __ballot_sync(kFullMask, pre + incl > target);
+            if (found) {
+                const int fl = __ffs(found) - 1;
+                if (lane == fl) {
+                    unsigned long long c = pre + incl - mine;
+                    for (int e = 0; e < 8 && y0 + e < V; ++e) {
+                        c += quantize(bonus_weight<T>(b, y0 + e));
+                        if (c > target) {
+                            tok = y0 + e;
+                            break;
+                        }
+                    }
+                }
+                tok = __shfl_sync(kFullMask, tok, fl);
+            }
+        }
+        if (tok < 0) {  // u * W at or past the total: the last token with weight
+            for (int w = 0; w < kSampWarps; ++w) tok = max(tok, last_w[w]);
+        }
+        if (lane == 0) {
+            a.num_acc[r] = correct;
+            a.bonus[r] = tok;
+            a.commit[r] = correct + 1;
+            if (a.new_seq) a.new_seq[r] = __ldg(a.prefix + r) + correct + 1;
+        }
+        if (lane < G) a.out[(size_t)r * (G + 1) + lane] = lane == correct ? tok : dj;
+        else if (lane == G) a.out[(size_t)r * (G + 1) + G] = G == correct ? tok : -1;
+    }
+}
+
+constexpr int kSampMaxV = kSampWarps * kMaxRounds * kRound;
+
+size_t samp_partial_bytes(int max_rows, int B, int gamma) {
+    const size_t slots = (size_t)kSampMaxCtas + (size_t)max_rows + (size_t)B * gamma + 1;
+    return (slots * sizeof(NormPartial) + 255) & ~size_t(255);
+}
+
+template <typename T>
+cudaError_t launch_sampling(const SampArgs &a, bool vec, cudaStream_t s) {
+    const size_t smem = (size_t)(a.B + 1) * sizeof(int32_t);
+    cudaError_t e = vec ? launch_pdl(softmax_norm_kernel<T, true>, dim3(a.grid), dim3(kNormThreads), smem, s, a)
+                        : launch_pdl(softmax_norm_kernel<T, false>, dim3(a.grid), dim3(kNormThreads), smem, s, a);
+    if (e != cudaSuccess) return e;
+    const int epc = vec ? Elem<T>::kPerChunk : 1;
+    return launch_pdl(sampling_accept_kernel<T>, dim3(a.B), dim3(kSampThreads), 0, s, a, epc);
+}
+
+}  // namespace dspark
+
+using namespace dspark;
+
+extern "C" size_t dspark_sampling_workspace_bytes(int32_t max_rows, int32_t B, int32_t gamma) {
+    if (max_rows < 0) max_rows = 0;
+    if (B < 0) B = 0;
+    if (gamma < 0) gamma = 0;
+    return samp_partial_bytes(max_rows, B, gamma) + ((((size_t)B + 1) * 4 + 255) & ~size_t(255));
+}
+
+extern "C" int dspark_sampling_accept(const void *target_logits, int32_t dtype, int64_t ld_t,
+                                      int32_t V, int32_t max_rows, const int32_t *cu_seqlens,
+                                      const void *draft_logits, int64_t ld_d,
+                                      const int32_t *draft, const int32_t *prefix_lens, int32_t B,
+                                      int32_t gamma, const float *u_accept, const float *u_bonus,
+                                      int32_t *num_accepted, int32_t *bonus, int32_t *commit_lens,
+                                      int32_t *new_seq_lens, int32_t *out_tokens, void *workspace,
+                                      size_t workspace_bytes, int32_t *status, void *stream) {
+    if (!target_logits || !cu_seqlens || !draft_logits || !draft || !u_accept || !u_bonus ||
+        !num_accepted || !bonus || !commit_lens || !out_tokens || !status)
+        return DSPARK_ERR_INVALID_ARG;
+    if (new_seq_lens && !prefix_lens) return DSPARK_ERR_INVALID_ARG;
+    if (dtype != DSPARK_DTYPE_BF16 && dtype != DSPARK_DTYPE_F32) return DSPARK_ERR_INVALID_ARG;
+    if (B < 1 || gamma < 1 || gamma > 31 || V < 1 || ld_t < V || ld_d < V || max_rows < 0)
+        return DSPARK_ERR_INVALID_ARG;
+    if (B > kSampMaxB || V > kSampMaxV) return DSPARK_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < dspark_sampling_workspace_bytes(max_rows, B, gamma) ||
+        !aligned(workspace, 256))
+        return DSPARK_ERR_WORKSPACE;
+    const long long esize = dtype == DSPARK_DTYPE_BF16 ? 2 : 4;
+    SampArgs a;
+    a.tgt = target_logits;
+    a.ld_t = ld_t;
+    a.dft = draft_logits;
+    a.ld_d = ld_d;
+    a.V = V;
+    a.B = B;
+    a.gamma = gamma;
+    a.max_rows = max_rows;
+    a.cu = cu_seqlens;
+    a.draft = draft;
+    a.prefix = prefix_lens;
+    a.u_acc = u_accept;
+    a.u_bonus = u_bonus;
+    a.num_acc = num_accepted;
+    a.bonus = bonus;
+    a.commit = commit_lens;
+    a.new_seq = new_seq_lens;
+    a.out = out_tokens;
+    a.status = status;
+    a.part = static_cast<NormPartial *>(workspace);
+    a.dcu = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) +
+                                        samp_partial_bytes(max_rows, B, gamma));
+    const int g = sm_count() * kNormCtasPerSm;
+    a.grid = g < 1 ? 1 : (g > kSampMaxCtas ? kSampMaxCtas : g);
+    const bool vec = aligned(target_logits, 16) && aligned(draft_logits, 16) &&
+                     (ld_t * esize) % 16 == 0 && (ld_d * esize) % 16 == 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = dtype == DSPARK_DTYPE_BF16 ? launch_sampling<__nv_bfloat16>(a, vec, s)
+                                                     : launch_sampling<float>(a, vec, s);
+    return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}

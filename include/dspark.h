@@ -228,6 +228,45 @@ DSPARK_API int dspark_plan_pack(const float *conf_logits, const float *sts_temps
                      int32_t *packed_src, int32_t *cu_seqlens, int32_t *totals,
                      void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
 
+/* Scratch of one sampling accept: per-(CTA, row) softmax partials for up
+ * to max_rows target rows and B*gamma draft rows, and B+1 offsets. */
+DSPARK_API size_t dspark_sampling_workspace_bytes(int32_t max_rows, int32_t B, int32_t gamma);
+
+/* Speculative sampling accept, compact mode ([ROUND] §五 AcceptSampling
+ * with chain speculative sampling; [AVS] §一: a draft drawn from q is
+ * accepted with probability min(1, p/q)).  The pages leave the rule to the
+ * speculative algorithm; this is the textbook one:
+ *   p_j = softmax(target row cu[r] + j), q_j = softmax(draft row r*gamma+j)
+ *   draft j (token x) is accepted iff u_accept[r][j] * q_j(x) < p_j(x); the
+ *   chain stops at the first rejection (correct_len = j)
+ *   bonus: inverse-CDF draw with u_bonus[r] -- the smallest token whose
+ *   cumulative weight exceeds u * W -- from max(0, p_j - q_j) after a
+ *   rejection (from p_j when that residual is empty), else from the last
+ *   row's p; then num_accepted / commit_lens / new_seq_lens / out_tokens as
+ *   dspark_greedy_accept.
+ *   target_logits  [max_rows, ld_t] bf16 or fp32, draft_logits [B*gamma,
+ *                  ld_d] of the same dtype: the proposal logits that produced
+ *                  each draft (after any correction)
+ *   u_accept [B, gamma], u_bonus [B]: fp32 uniforms in [0, 1) (the caller's
+ *                  random numbers)
+ * Softmax sums are fp32 per thread and fp64 beyond, the bonus weights are
+ * summed exactly in units of 2^-40: a decision can differ from an exact
+ * evaluation only within ~1e-6 relative of its threshold.  NaN logits weigh
+ * 0 (DSPARK_STATUS_NAN_LOGIT); a draft token outside [0, V) is rejected
+ * (TOKEN_RANGE); a bad cu range gives the greedy defaults (BAD_LEN).
+ * Errors: INVALID_ARG (null pointer, dtype, B < 1, gamma outside 1..31,
+ * V < 1, a stride below V, max_rows < 0); UNSUPPORTED (B > 4096 or
+ * V > 2^20); WORKSPACE; CUDA. */
+DSPARK_API int dspark_sampling_accept(const void *target_logits, int32_t dtype, int64_t ld_t,
+                           int32_t V, int32_t max_rows, const int32_t *cu_seqlens,
+                           const void *draft_logits, int64_t ld_d, const int32_t *draft,
+                           const int32_t *prefix_lens /* nullable with new_seq_lens */,
+                           int32_t B, int32_t gamma, const float *u_accept,
+                           const float *u_bonus, int32_t *num_accepted, int32_t *bonus,
+                           int32_t *commit_lens, int32_t *new_seq_lens /* nullable */,
+                           int32_t *out_tokens, void *workspace, size_t workspace_bytes,
+                           int32_t *status, void *stream);
+
 /* ScatterCompactToStrided ([ROUND] §三): after the target forward over the
  * compact verify rows, copy packed row i (i < totals[0]) to row
  * packed_src[i] = r*(gamma+1) + j of the [B x (gamma+1)] strided buffer, so

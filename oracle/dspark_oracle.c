@@ -505,6 +505,22 @@ void orc_sampling_accept(const float *tgt, int64_t ld_t, int V, int rows_avail, 
                          int32_t *commit, int32_t *new_seq, int32_t *out, int *status)
 {
     orc_check_tokens(draft, B, gamma, V, status);
+    /* NaN logits are flagged in every packed target row and in every draft
+     * row a test of a valid request reads, whether or not the chain gets
+     * there */
+    for (int i = 0; i < rows_avail; ++i)
+        for (int y = 0; y < V; ++y)
+            if (tgt[(size_t)i * (size_t)ld_t + y] != tgt[(size_t)i * (size_t)ld_t + y])
+                *status |= ORC_ST_NAN_LOGIT;
+    for (int r = 0; r < B; ++r) {
+        const int lo = cu[r], hi = cu[r + 1], L = hi - lo;
+        if (lo < 0 || hi > rows_avail || L < 1 || L > gamma + 1) continue;
+        for (int j = 0; j < L - 1; ++j)
+            for (int y = 0; y < V; ++y) {
+                const float z = dft[((size_t)r * gamma + j) * (size_t)ld_d + y];
+                if (z != z) *status |= ORC_ST_NAN_LOGIT;
+            }
+    }
     double *w = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
     for (int r = 0; r < B; ++r) {
         const int lo = cu[r], hi = cu[r + 1], L = hi - lo;

@@ -195,3 +195,25 @@ def test_scatter_argument_checks(lib):
     assert call(ld_src=7) == -1
     assert call(ld_dst=4) == -1
     assert call(rows=-1) == -1
+
+
+def test_sampling_argument_checks(lib):
+    f = lib.dspark_sampling_accept
+    f.restype = ctypes.c_int
+    lib.dspark_sampling_workspace_bytes.restype = ctypes.c_size_t
+    need = lib.dspark_sampling_workspace_bytes(100, 4, 4)
+    assert need % 256 == 0 and need >= 16 * 104
+
+    def call(dtype=0, ld=1024, V=1000, B=4, g=4, ws=FAKE, wsb=need, u=FAKE, prefix=FAKE, new_seq=None):
+        return f(FAKE, dtype, ctypes.c_int64(ld), V, 100, FAKE, FAKE, ctypes.c_int64(ld), FAKE,
+                 prefix, B, g, u, FAKE, FAKE, FAKE, FAKE, new_seq, FAKE, ws, ctypes.c_size_t(wsb),
+                 FAKE, None)
+
+    assert call(dtype=3) == -1
+    assert call(ld=999) == -1
+    assert call(u=None) == -1
+    assert call(g=32) == -1
+    assert call(new_seq=FAKE, prefix=None) == -1
+    assert call(B=5000) == -4
+    assert call(ws=None) == -2
+    assert call(wsb=need - 256) == -2
