@@ -16,7 +16,8 @@
 // cu[r] + j, q_j = softmax of draft row r*gamma + j; at the first rejection
 // the bonus is the inverse-CDF draw (uniform u_bonus[r]) from the residual
 // max(0, p_j - q_j), normalised; when every draft is accepted, from the
-// last row's p.  An empty residual (p == q) draws from p.
+// last row's p.  An empty residual (p == q; in practice a total mass below
+// 2^-20, the precision of the softmax sums) draws from p.
 //
 // Two kernels:
 //   softmax_norm_kernel  HBM-bound: for every packed target row and every
@@ -30,7 +31,7 @@
 //   sampling_accept_kernel  one CTA per request: combines the partials of its
 //     rows, runs the acceptance tests (warp 0, one lane per draft), then
 //     draws the bonus: the residual (or p) of the bonus row is summed in
-//     rounds of 256 tokens, one warp per contiguous eighth of the
+//     rounds of 256 tokens, one warp per contiguous sixteenth of the
 //     vocabulary, and the round holding u * W is searched token by token.
 // Sums of exps are fp32 per thread and fp64 beyond, so p and q agree with
 // an fp64 index-order evaluation to about 1e-6 relative: decisions can
@@ -45,12 +46,12 @@ namespace dspark {
 constexpr int kNormThreads = 256;
 constexpr int kNormCtasPerSm = 4;
 constexpr int kNormUnroll = 4;
-constexpr int kSampThreads = 256;
+constexpr int kSampThreads = 512;
 constexpr int kSampWarps = kSampThreads / 32;
 constexpr int kSampMaxB = 4096;   // cu_seqlens staged in shared memory by every CTA
 constexpr int kSampMaxCtas = 4096;
 constexpr int kRound = 256;       // tokens per round of the bonus draw (32 lanes x 8)
-constexpr int kMaxRounds = 512;   // rounds per warp: V / 8 / 256 for V <= 1M
+constexpr int kMaxRounds = 256;   // rounds per warp: V / 16 / 256 for V <= 1M
 
 struct NormPartial {
     float m;     // largest logit of the piece (-inf: none)
@@ -82,6 +83,20 @@ __device__ __forceinline__ bool samp_valid(int lo, int hi, int rows, int gamma) 
     return lo >= 0 && hi <= rows && hi - lo >= 1 && hi - lo <= gamma + 1;
 }
 
+constexpr float kLog2e = 1.4426950408889634f;
+
+// A residual max(0, p - q) of total mass below 2^-20 -- under the precision
+// of the softmax sums -- is empty: the bonus is drawn from p.  (2^20 units
+// of 2^-40.)
+constexpr unsigned long long kEmptyResidual = 1ull << 20;
+
+// 2^x by the hardware approximation (relative error about 2^-22).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Online (max, sum of exps) of one value; NaN counts as -inf.
 __device__ __forceinline__ void norm_take(float z, float &m, float &s) {
     if (z > m) {
@@ -92,26 +107,32 @@ __device__ __forceinline__ void norm_take(float z, float &m, float &s) {
     }
 }
 
-// One 16-byte chunk into the thread's running (m, s): the chunk max first,
-// one rescale, then one exp per value.
+// A chunk holding a NaN: value by value, NaN skipped (rare path).
+template <typename T>
+__device__ __noinline__ void norm_chunk_nan(uint4 v, float &m, float &s) {
+#pragma unroll
+    for (int e = 0; e < Elem<T>::kPerChunk; ++e) norm_take(Elem<T>::at(v, e), m, s);
+}
+
+// One 16-byte chunk into the thread's running (m, s): the chunk max (NaN-
+// propagating, packed for bf16), one rescale, then exp(z - m) =
+// 2^(z*log2e - m*log2e) with one FMA and one ex2 per value.
 template <typename T>
 __device__ __forceinline__ void norm_chunk(const uint4 &v, float &m, float &s, bool &nan) {
-    constexpr int E = Elem<T>::kPerChunk;
-    float z[E];
-    float cm = -INFINITY;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        z[e] = Elem<T>::at(v, e);
-        nan |= z[e] != z[e];
-        cm = fmaxf(cm, z[e]);  // NaN ignored
+    const float cm = Elem<T>::chunk_max(v);
+    if (cm != cm) {
+        nan = true;
+        norm_chunk_nan<T>(v, m, s);
+        return;
     }
     if (cm > m) {
-        s *= __expf(m - cm);
+        s *= ex2((m - cm) * kLog2e);
         m = cm;
     }
     if (m > -INFINITY) {
+        const float ml = m * kLog2e;
 #pragma unroll
-        for (int e = 0; e < E; ++e) s += (z[e] == z[e]) ? __expf(z[e] - m) : 0.0f;
+        for (int e = 0; e < Elem<T>::kPerChunk; ++e) s += ex2(fmaf(Elem<T>::at(v, e), kLog2e, -ml));
     }
 }
 
@@ -282,45 +303,78 @@ __device__ __forceinline__ unsigned long long quantize(float w) {
 struct BonusRow {
     const void *t;  // target row
     const void *d;  // draft row (residual) or null (p)
-    float mt, md;
+    float mt, md;   // row maxima, times log2(e)
     float inv_st, inv_sd;
 };
 
-// Weight of token y in the bonus draw, fp32.
-template <typename T>
-__device__ __forceinline__ float bonus_weight(const BonusRow &b, int y) {
-    const float zt = Elem<T>::load(reinterpret_cast<const T *>(b.t) + y);
-    float w = (zt == zt) ? __expf(zt - b.mt) * b.inv_st : 0.0f;
+// Weight of one token of the bonus draw from its target (and draft) logit;
+// a NaN logit weighs 0.
+__device__ __forceinline__ float weight_of(const BonusRow &b, float zt, float zd) {
+    float w = (zt == zt) ? ex2(fmaf(zt, kLog2e, -b.mt)) * b.inv_st : 0.0f;
     if (b.d) {
-        const float zd = Elem<T>::load(reinterpret_cast<const T *>(b.d) + y);
-        const float q = (zd == zd) ? __expf(zd - b.md) * b.inv_sd : 0.0f;
+        const float q = (zd == zd) ? ex2(fmaf(zd, kLog2e, -b.md)) * b.inv_sd : 0.0f;
         w = fmaxf(w - q, 0.0f);
     }
     return w;
 }
 
-// The 8 tokens y0..y0+7 of one lane in one round: quantized weights summed,
-// and the last token with a positive weight (or -1).
+// The weights of the 8 tokens y0..y0+7 one lane handles in a round (0 past
+// V).  Aligned rows with no NaN among the 8: 16-byte loads and no per-token
+// checks; otherwise token by token.
 template <typename T>
-__device__ __forceinline__ unsigned long long lane_round(const BonusRow &b, int y0, int V,
-                                                         int &last_pos) {
-    unsigned long long acc = 0ull;
+__device__ __forceinline__ void weights8(const BonusRow &b, int y0, int V, bool vec, float (&w)[8]) {
+    constexpr int E = Elem<T>::kPerChunk, NC = 8 / E;
+    const T *rt = reinterpret_cast<const T *>(b.t);
+    const T *rd = reinterpret_cast<const T *>(b.d);
+    if (vec && y0 + 8 <= V) {
+        uint4 t[NC], d[NC];
+        bool nan = false;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            t[c] = ld_stream16(reinterpret_cast<const uint4 *>(rt + y0) + c);
+            const float mt = Elem<T>::chunk_max(t[c]);
+            nan |= mt != mt;
+            if (rd) {
+                d[c] = ld_stream16(reinterpret_cast<const uint4 *>(rd + y0) + c);
+                const float md = Elem<T>::chunk_max(d[c]);
+                nan |= md != md;
+            }
+        }
+        if (!nan) {
+            if (rd) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float p = ex2(fmaf(Elem<T>::at(t[e / E], e % E), kLog2e, -b.mt)) * b.inv_st;
+                    const float q = ex2(fmaf(Elem<T>::at(d[e / E], e % E), kLog2e, -b.md)) * b.inv_sd;
+                    w[e] = fmaxf(p - q, 0.0f);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    w[e] = ex2(fmaf(Elem<T>::at(t[e / E], e % E), kLog2e, -b.mt)) * b.inv_st;
+            }
+            return;
+        }
+    }
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
         const int y = y0 + e;
-        if (y < V) {
-            const unsigned long long wq = quantize(bonus_weight<T>(b, y));
-            acc += wq;
-            if (wq) last_pos = y;
-        }
+        w[e] = y < V ? weight_of(b, Elem<T>::load(rt + y), rd ? Elem<T>::load(rd + y) : 0.0f) : 0.0f;
     }
-    return acc;
+}
+
+// A lane's round total: the fp32 sum of its 8 weights in token order,
+// quantized once.
+__device__ __forceinline__ unsigned long long lane_total(const float (&w)[8]) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc += w[e];
+    return quantize(acc);
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs a, int epc) {
+__global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs a, int epc, bool vec) {
     __shared__ unsigned long long rsum[kSampWarps * kMaxRounds];  // weight of each round
-    __shared__ int last_w[kSampWarps];
     __shared__ BonusRow brow;
     __shared__ int s_correct, s_round, s_retry;
     __shared__ unsigned long long s_pre, s_target;
@@ -383,8 +437,8 @@ __global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs 
             brow.t = reinterpret_cast<const T *>(a.tgt) + (long long)(lo + correct) * a.ld_t;
             brow.d = rejected ? reinterpret_cast<const T *>(a.dft) + ((long long)r * G + correct) * a.ld_d
                               : nullptr;
-            brow.mt = mt;
-            brow.md = md;
+            brow.mt = mt * kLog2e;
+            brow.md = md * kLog2e;
             brow.inv_st = st > 0.0 ? (float)(1.0 / st) : 0.0f;
             brow.inv_sd = sd > 0.0 ? (float)(1.0 / sd) : 0.0f;
         }
@@ -398,17 +452,25 @@ __global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs 
     const int nr = per_warp / kRound;  // rounds per warp (<= kMaxRounds: V is bounded on the host)
     for (int attempt = 0; attempt < 2; ++attempt) {
         const BonusRow b = brow;
-        int last_pos = -1;
-        for (int k = 0; k < nr; ++k) {
-            const int y0 = warp * per_warp + k * kRound + lane * 8;
-            unsigned long long s = lane_round<T>(b, y0, V, last_pos);
+        constexpr int U = 2;  // rounds whose loads are in flight together
+        for (int k0 = 0; k0 < nr; k0 += U) {
+            unsigned long long sm[U];
 #pragma unroll
-            for (int d = 16; d > 0; d >>= 1) s += __shfl_xor_sync(kFullMask, s, d);
-            if (lane == 0) rsum[warp * nr + k] = s;
+            for (int u = 0; u < U; ++u) {
+                float w[8];
+                weights8<T>(b, warp * per_warp + (k0 + u) * kRound + lane * 8, (k0 + u < nr) ? V : 0,
+                            vec, w);
+                sm[u] = lane_total(w);
+            }
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1)
+#pragma unroll
+                for (int u = 0; u < U; ++u) sm[u] += __shfl_xor_sync(kFullMask, sm[u], d);
+            if (lane == 0)
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (k0 + u < nr) rsum[warp * nr + k0 + u] = sm[u];
         }
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) last_pos = max(last_pos, __shfl_xor_sync(kFullMask, last_pos, d));
-        if (lane == 0) last_w[warp] = last_pos;
         __syncthreads();
         // warp 0: the total, the target u * W, and the round it falls in
         if (warp == 0) {
@@ -423,7 +485,7 @@ __global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs 
                 if (lane >= d) incl += o;
             }
             const unsigned long long Wq = __shfl_sync(kFullMask, incl, 31);
-            if (Wq == 0ull && brow.d != nullptr) {  // p == q: the residual is empty
+            if (Wq < kEmptyResidual && brow.d != nullptr) {  // p == q within the sums' precision
                 if (lane == 0) {
                     brow.d = nullptr;
                     s_retry = 1;
@@ -469,10 +531,11 @@ __global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs 
         int tok = -1;
         if (round >= 0) {
             const BonusRow b = brow;
-            const int w = round / nr, k = round - w * nr;
-            const int y0 = w * per_warp + k * kRound + lane * 8;
-            int dummy = -1;
-            const unsigned long long mine = lane_round<T>(b, y0, V, dummy);
+            const int rw = round / nr, k = round - rw * nr;
+            const int y0 = rw * per_warp + k * kRound + lane * 8;
+            float w[8];
+            weights8<T>(b, y0, V, vec, w);
+            const unsigned long long mine = lane_total(w);
             unsigned long long incl = mine;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
@@ -484,10 +547,12 @@ __global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs 
             if (found) {
                 const int fl = __ffs(found) - 1;
                 if (lane == fl) {
-                    unsigned long long c = pre + incl - mine;
-                    for (int e = 0; e < 8 && y0 + e < V; ++e) {
-                        c += quantize(bonus_weight<T>(b, y0 + e));
-                        if (c > target) {
+                    // the same fp32 running sum as lane_total, quantized per prefix
+                    const unsigned long long base = pre + incl - mine;
+                    float acc = 0.0f;
+                    for (int e = 0; e < 8; ++e) {
+                        acc += w[e];
+                        if (base + quantize(acc) > target) {
                             tok = y0 + e;
                             break;
                         }
@@ -495,9 +560,6 @@ __global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs 
                 }
                 tok = __shfl_sync(kFullMask, tok, fl);
             }
-        }
-        if (tok < 0) {  // u * W at or past the total: the last token with weight
-            for (int w = 0; w < kSampWarps; ++w) tok = max(tok, last_w[w]);
         }
         if (lane == 0) {
             a.num_acc[r] = correct;
@@ -524,7 +586,7 @@ cudaError_t launch_sampling(const SampArgs &a, bool vec, cudaStream_t s) {
                         : launch_pdl(softmax_norm_kernel<T, false>, dim3(a.grid), dim3(kNormThreads), smem, s, a);
     if (e != cudaSuccess) return e;
     const int epc = vec ? Elem<T>::kPerChunk : 1;
-    return launch_pdl(sampling_accept_kernel<T>, dim3(a.B), dim3(kSampThreads), 0, s, a, epc);
+    return launch_pdl(sampling_accept_kernel<T>, dim3(a.B), dim3(kSampThreads), 0, s, a, epc, vec);
 }
 
 }  // namespace dspark

@@ -241,7 +241,7 @@ DSPARK_API size_t dspark_sampling_workspace_bytes(int32_t max_rows, int32_t B, i
  *   chain stops at the first rejection (correct_len = j)
  *   bonus: inverse-CDF draw with u_bonus[r] -- the smallest token whose
  *   cumulative weight exceeds u * W -- from max(0, p_j - q_j) after a
- *   rejection (from p_j when that residual is empty), else from the last
+ *   rejection (from p_j when that residual's mass is below 2^-20), else from the last
  *   row's p; then num_accepted / commit_lens / new_seq_lens / out_tokens as
  *   dspark_greedy_accept.
  *   target_logits  [max_rows, ld_t] bf16 or fp32, draft_logits [B*gamma,

@@ -470,7 +470,10 @@ void orc_scatter_rows(const unsigned char *src, long long ld_src, long long row_
  * p_j(x); at the first rejection the bonus is drawn from the residual
  * max(0, p_j - q_j) (normalised); when every draft is accepted, from the
  * last row's p.  The draws are inverse-CDF draws with one uniform per
- * request: the smallest token whose cumulative weight exceeds u * W.
+ * request: the smallest token whose cumulative weight exceeds u * W.  A
+ * residual of total mass below 2^-20 (p == q up to the precision any
+ * implementation of the softmax sums resolves) is read as empty: draw from
+ * p.
  *
  * Arithmetic: logits are fp32 (bf16 widened exactly); m = the row's largest
  * non-NaN logit; e_y = expf(z_y - m) in fp32 (NaN logits weigh 0 and are
@@ -568,7 +571,7 @@ void orc_sampling_accept(const float *tgt, int64_t ld_t, int V, int rows_avail, 
             w[y] = v;
             W += v;
         }
-        if (!(W > 0.0)) { /* p == q: the residual is empty, draw from p */
+        if (!(W >= 0x1p-20)) { /* p == q (a mass below 2^-20 counts as empty): draw from p */
             W = 0.0;
             for (int y = 0; y < V; ++y) { w[y] = orc_prob(zt, y, mt, St); W += w[y]; }
         }
