@@ -23,6 +23,14 @@ produced without materialising the full strided [B, gamma+1, V] tensor:
 
 bf16 rows are rounded to nearest-even from the fp32 draw and returned as raw
 uint16 bit patterns.
+
+Recorded calibration samples (``calibration_samples``) stand in for a log of
+served steps: each sample has a true per-depth acceptance probability drawn
+in probability space, a confidence-head logit that is that probability's
+logit scaled by a known "true" temperature (a head miscalibrated by exactly
+that temperature), the greedy prefix outcome drawn depth by depth, and a
+verify window that is the full block for a fraction of the samples and a
+random compact window otherwise.
 """
 
 from __future__ import annotations
@@ -273,6 +281,54 @@ def confidence_logits_for(probs: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(_logit(probs), dtype=np.float32)
 
 
+@dataclasses.dataclass(frozen=True)
+class CalibrationSamples:
+    """Recorded (z, correct, tested) rows and the truth they were drawn from."""
+
+    conf_logits: np.ndarray  # [N, gamma] fp32
+    correct: np.ndarray      # [N] int32, accepted drafts inside the window
+    tested: np.ndarray       # [N] int32, drafts the target checked
+    true_temps: np.ndarray   # [gamma] fp32
+    true_probs: np.ndarray   # [N, gamma] fp64
+
+
+_CAL_TAG = 0x5EED_0003
+
+
+def calibration_samples(N: int, gamma: int, true_temps, seed: int = 0, full_frac: float = 0.25,
+                        concentration: float = 6.0) -> CalibrationSamples:
+    """N recorded steps of one request each.  Depth k's true acceptance
+    probability is Beta-distributed with mean 0.92 - 0.03 k (the DSV4-like
+    decay) and the given concentration; the head logit is
+    logit(probability) * true_temps[k]; the prefix survives depth k with that
+    probability; the window is the whole block for ``full_frac`` of the
+    samples (cap-accept style) and 0..gamma drafts uniformly otherwise; the
+    recorded count is the accepted prefix cut to the window."""
+    rng = np.random.default_rng(np.random.SeedSequence([_CAL_TAG, N, gamma, seed]))
+    Tt = np.broadcast_to(np.asarray(true_temps, np.float64), (gamma,)).copy()
+    k = np.arange(gamma, dtype=np.float64)
+    mean = np.clip(0.92 - 0.03 * k, 0.05, 0.95)
+    a = mean * concentration
+    b = (1.0 - mean) * concentration
+    prob = np.clip(rng.beta(a[None, :], b[None, :], size=(N, gamma)), 1e-4, 1.0 - 1e-4)
+    z = _logit(prob) * Tt[None, :]
+    u = rng.random((N, gamma))
+    fail = u >= prob
+    raw = np.where(fail.any(axis=1), fail.argmax(axis=1), gamma)
+    full = rng.random(N) < full_frac
+    win = rng.integers(0, gamma + 1, size=N)
+    tested = np.where(full, gamma, win)
+    correct = np.minimum(raw, tested)
+    return CalibrationSamples(conf_logits=np.ascontiguousarray(z, dtype=np.float32),
+                              correct=correct.astype(np.int32), tested=tested.astype(np.int32),
+                              true_temps=Tt.astype(np.float32), true_probs=prob)
+
+
+def temperature_grid(n: int = 64, lo: float = 0.25, hi: float = 4.0) -> np.ndarray:
+    """n log-spaced candidate temperatures from lo to hi (fp32)."""
+    return np.geomspace(lo, hi, n).astype(np.float32)
+
+
 def seeds(n: int, start: int = 0) -> Sequence[int]:
     return range(start, start + n)
 
@@ -290,4 +346,5 @@ __all__ = [
     "COST_SPS_1D", "COST_ADDITIVE", "make_step", "cost_table_for", "target_rows", "strided_logits",
     "to_bf16_bits", "bf16_bits_to_f32", "strided_row_index", "pages_example_confidences",
     "confidence_logits_for", "seeds", "approx_bytes", "describe", "PEAK",
+    "CalibrationSamples", "calibration_samples", "temperature_grid",
 ]

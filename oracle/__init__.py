@@ -94,6 +94,17 @@ def lib():
             L.orc_cap_finalize.argtypes = [i32p, i32p, i32p, i32p, ci, ci, ci, i32p, i32p, i32p,
                                            i32p, i32p, i32p, i32p, i32p]
             L.orc_cap_finalize.restype = None
+            u64p, i64p = _P(ctypes.c_uint64), _P(ctypes.c_int64)
+            L.orc_sts_record.argtypes = [f32p, i32p, i32p, u8p, ci, ci, f32p, i32p, i32p, cl,
+                                         u64p, u8p, i32p]
+            L.orc_sts_record.restype = None
+            L.orc_reliability.argtypes = [f32p, u8p, cl, ci, u64p, f64p]
+            L.orc_reliability.restype = ctypes.c_uint64
+            L.orc_calib_stats.argtypes = [f32p, i32p, i32p, cl, ci, f32p, ci, u64p, f64p, i32p]
+            L.orc_calib_stats.restype = None
+            L.orc_sts_fit.argtypes = [f32p, i32p, i32p, cl, ci, f32p, ci, ci, f32p, i32p, f64p,
+                                      i64p, i32p]
+            L.orc_sts_fit.restype = None
             _lib = L
     return _lib
 
@@ -382,3 +393,80 @@ def sampling_accept(target, V, cu, draft_logits, draft, prefix, u_accept, u_bonu
                               _ptr(st, ctypes.c_int32))
     return PlanResult(num_accepted=o[0], bonus=o[1], commit_lens=o[2], new_seq_lens=o[3],
                       out_tokens=out, status=int(st[0]) | status)
+
+
+# -------------------------------------------------------------- calibration
+
+def sts_record(z, correct, verify_lens, B_select, rec_z, rec_correct, rec_tested, cursor,
+               want_mask=True):
+    """Append the selected requests' (z, correct, tested) rows to the ring
+    buffers rec_* (modified in place) starting at ``cursor``.  B_select is a
+    uint8 [B] mask or None (every request); verify_lens None = full block.
+    Returns (new_cursor, prefix_mask or None, status)."""
+    z = _c(z, np.float32)
+    B, g = z.shape
+    correct = _c(correct, np.int32)
+    vl = None if verify_lens is None else _c(verify_lens, np.int32)
+    sel = None if B_select is None else _c(B_select, np.uint8)
+    cap = rec_correct.shape[0]
+    cur = np.array([cursor], np.uint64)
+    mask = np.empty((B, g), np.uint8) if want_mask else None
+    st = np.zeros(1, np.int32)
+    lib().orc_sts_record(_ptr(z, ctypes.c_float), _ptr(correct, ctypes.c_int32),
+                         _ptr(vl, ctypes.c_int32), _ptr(sel, ctypes.c_uint8), B, g,
+                         _ptr(rec_z, ctypes.c_float), _ptr(rec_correct, ctypes.c_int32),
+                         _ptr(rec_tested, ctypes.c_int32), cap, _ptr(cur, ctypes.c_uint64),
+                         _ptr(mask, ctypes.c_uint8), _ptr(st, ctypes.c_int32))
+    return int(cur[0]), mask, int(st[0])
+
+
+def reliability(p, y, n_bins):
+    """(hist [n_bins, 3] uint64, metrics [4] = n, ECE, Brier, log loss,
+    E = ECE*n*2^32 as an exact integer) of (prediction, label) pairs."""
+    p = _c(p, np.float32).reshape(-1)
+    y = _c(y, np.uint8).reshape(-1)
+    hist = np.zeros((n_bins, 3), np.uint64)
+    met = np.zeros(4, np.float64)
+    E = lib().orc_reliability(_ptr(p, ctypes.c_float), _ptr(y, ctypes.c_uint8), p.shape[0],
+                              int(n_bins), _ptr(hist, ctypes.c_uint64),
+                              _ptr(met, ctypes.c_double))
+    return hist, met, int(E)
+
+
+def calib_stats(z, correct, tested, T, n_bins):
+    """Per-depth calibration of recorded samples: hist [2, gamma, n_bins, 3]
+    and metrics [2, gamma, 4] (flavour 0 cumulative S_k, 1 per-position c_k)."""
+    z = _c(z, np.float32)
+    N, g = z.shape
+    correct = _c(correct, np.int32)
+    tested = _c(tested, np.int32)
+    T = _c(T, np.float32)
+    hist = np.zeros((2, g, n_bins, 3), np.uint64)
+    met = np.zeros((2, g, 4), np.float64)
+    st = np.zeros(1, np.int32)
+    lib().orc_calib_stats(_ptr(z, ctypes.c_float), _ptr(correct, ctypes.c_int32),
+                          _ptr(tested, ctypes.c_int32), N, g, _ptr(T, ctypes.c_float),
+                          int(n_bins), _ptr(hist, ctypes.c_uint64), _ptr(met, ctypes.c_double),
+                          _ptr(st, ctypes.c_int32))
+    return PlanResult(hist=hist, metrics=met, status=int(st[0]))
+
+
+def sts_fit(z, correct, tested, grid, n_bins):
+    """Sequential per-depth temperature fit over a grid of temperatures."""
+    z = _c(z, np.float32)
+    N, g = z.shape
+    correct = _c(correct, np.int32)
+    tested = _c(tested, np.int32)
+    grid = _c(grid, np.float32)
+    J = grid.shape[0]
+    T = np.zeros(g, np.float32)
+    choice = np.zeros(g, np.int32)
+    curve = np.zeros((g, J), np.float64)
+    n_obs = np.zeros(g, np.int64)
+    st = np.zeros(1, np.int32)
+    lib().orc_sts_fit(_ptr(z, ctypes.c_float), _ptr(correct, ctypes.c_int32),
+                      _ptr(tested, ctypes.c_int32), N, g, _ptr(grid, ctypes.c_float), J,
+                      int(n_bins), _ptr(T, ctypes.c_float), _ptr(choice, ctypes.c_int32),
+                      _ptr(curve, ctypes.c_double), _ptr(n_obs, ctypes.c_int64),
+                      _ptr(st, ctypes.c_int32))
+    return PlanResult(T=T, choice=choice, ece_curve=curve, n_obs=n_obs, status=int(st[0]))

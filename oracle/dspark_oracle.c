@@ -1,7 +1,9 @@
 /*
  * dspark_oracle.c -- plain, slow, single-threaded CPU oracle for the DSpark
- * verify planner, ragged verify pack, greedy / cap-accept and the scatter of
- * compact rows back to the strided layout.
+ * verify planner, ragged verify pack, greedy / cap-accept, the scatter of
+ * compact rows back to the strided layout, speculative sampling accept, and
+ * the calibration side (STS recorder, reliability statistics, sequential
+ * temperature fit).
  *
  * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
  * benchmark's CPU-baseline leg load this file.  The product path (the CUDA
@@ -587,4 +589,253 @@ void orc_sampling_accept(const float *tgt, int64_t ld_t, int V, int rows_avail, 
         orc_finish(r, correct, tok, draft, prefix, gamma, num_acc, bonus, commit, new_seq, out);
     }
     free(w);
+}
+
+/* --------------------------------------------------------- calibration
+ *
+ * STS recorder, calibration statistics and the sequential temperature
+ * fitter (NEXT-4 of the scope table).
+ *
+ *   [AVS] §二 "但 SGLang STS 校准的不是同一个 soft target": the recorder
+ *         labels a recorded step with the greedy prefix mask, position k is 1
+ *         iff k < num_correct_drafts (a later chance match after the first
+ *         mismatch stays 0).
+ *   [AVS] §二 "STS 更像运行时语义桥": c_i = sigmoid(z_i / T_i), S_k = prod
+ *         c_i; the fitter searches a temperature position by position,
+ *         keeping the cumulative survival of the positions already fitted,
+ *         and takes for the current position the temperature of lowest ECE.
+ *   [TUT] "为什么置信度必须校准": ECE = sum_b |I_b|/n |acc(I_b) - conf(I_b)|
+ *         over confidence bins; the label of position k only means something
+ *         when the positions before it survived.
+ *   [TUT] "截短会制造观测盲区": a compact verify that stops at position L
+ *         leaves the later positions unobserved (censored), unless the chain
+ *         already broke inside the window.
+ *   [AVS] §七 A and [TUT] "置信度质量": per-position and cumulative
+ *         calibration, ECE, Brier score or log loss, by depth, with a
+ *         reliability diagram.
+ *
+ * Readings (also in the design notes):
+ *   R24 a recorded sample is (z[gamma], correct, tested): tested = drafts
+ *       the target checked (verify_len - 1; gamma for a full block).  Depth
+ *       k is observed iff k < tested; label y_k = (k < correct).  A depth
+ *       past the window stays unobserved even when the chain broke inside it
+ *       (its label is then known to be 0): keeping those samples would keep
+ *       them only when their label is 0, the selection bias the truncation
+ *       passage warns of.  Out-of-range values are clamped (tested to [0,
+ *       gamma], correct to [0, tested]) and flagged BAD_LEN.
+ *   R25 cumulative flavour at depth k: prediction S_k, over observed
+ *       samples; per-position flavour: prediction c_k, over samples with k <
+ *       tested and correct >= k (tested and the prefix survived).  A NaN
+ *       prediction leaves the sample out.
+ *   R26 n_bins equal-width bins over [0, 1]: bin = min(floor(p*n_bins),
+ *       n_bins-1).  Confidences enter the bin sums floored to multiples of
+ *       2^-32, so every sum is an exact integer and ECE*n*2^32 =
+ *       sum_b |L_b*2^32 - C_b| is an exact integer (ECE within 2^-32 of the
+ *       real-number value).  Brier = mean (p - y)^2; log loss = mean
+ *       -[y ln p + (1-y) ln(1-p)] with p clamped to [2^-24, 1 - 2^-24]; both
+ *       summed in fp64.  A flavour with no sample reports n = 0 and zeros.
+ *   R27 the fitter chooses from a caller's grid of temperatures; the lowest
+ *       ECE*n*2^32 wins, ties to the lower grid index; a depth with no
+ *       observed sample takes T = 1 and choice -1.
+ *   R28 recorder: selected rows are appended in request order at slots
+ *       (cursor + i) mod capacity and the cursor advances by their count;
+ *       when one call selects more than capacity rows, only the last
+ *       capacity of them are written (CAPACITY).
+ */
+
+#define ORC_Q32 4294967296.0  /* 2^32 */
+
+/* tested and correct of one recorded sample, clamped (reading R24) */
+static void orc_sample_lens(int32_t correct, int32_t tested, int gamma, int *c_out, int *t_out,
+                            int *status)
+{
+    int t = tested, c = correct;
+    if (t < 0 || t > gamma) {
+        *status |= ORC_ST_BAD_LEN;
+        t = t < 0 ? 0 : gamma;
+    }
+    if (c < 0 || c > t) {
+        *status |= ORC_ST_BAD_LEN;
+        c = c < 0 ? 0 : t;
+    }
+    *c_out = c;
+    *t_out = t;
+}
+
+/* The recorder ([AVS] §二; reading R28).  tested = verify_len - 1 (every
+ * draft when verify_lens is NULL: a full verify or the cap-accept ceiling);
+ * verify_len is clamped to [1, gamma+1] and correct to [0, tested] (BAD_LEN).
+ * prefix_mask (nullable) [B, gamma] gets (k < correct) for every request. */
+void orc_sts_record(const float *z, const int32_t *correct, const int32_t *verify_lens,
+                    const uint8_t *select, int B, int gamma, float *rec_z, int32_t *rec_correct,
+                    int32_t *rec_tested, int64_t capacity, uint64_t *cursor, uint8_t *prefix_mask,
+                    int *status)
+{
+    int64_t count = 0;
+    for (int r = 0; r < B; ++r)
+        if (!select || select[r]) ++count;
+    if (count > capacity) *status |= ORC_ST_CAPACITY;
+    int64_t i = 0;
+    for (int r = 0; r < B; ++r) {
+        int tested = gamma;
+        if (verify_lens) {
+            int L = verify_lens[r];
+            if (L < 1 || L > gamma + 1) {
+                *status |= ORC_ST_BAD_LEN;
+                L = L < 1 ? 1 : gamma + 1;
+            }
+            tested = L - 1;
+        }
+        int c = correct[r];
+        if (c < 0 || c > tested) {
+            *status |= ORC_ST_BAD_LEN;
+            c = c < 0 ? 0 : tested;
+        }
+        if (prefix_mask)
+            for (int k = 0; k < gamma; ++k) prefix_mask[(size_t)r * gamma + k] = (uint8_t)(k < c);
+        if (select && !select[r]) continue;
+        /* appended one after the other: a later row overwrites an earlier
+         * one on the same slot */
+        uint64_t slot = (*cursor + (uint64_t)i) % (uint64_t)capacity;
+        for (int k = 0; k < gamma; ++k) rec_z[slot * (uint64_t)gamma + k] = z[(size_t)r * gamma + k];
+        rec_correct[slot] = c;
+        rec_tested[slot] = tested;
+        ++i;
+    }
+    *cursor += (uint64_t)count;
+}
+
+/* Reliability statistics of n (prediction, label) pairs ([TUT]
+ * "为什么置信度必须校准", "置信度质量"; reading R26).
+ *   hist    [n_bins][3]: count, label sum, confidence sum in 2^-32 units
+ *   metrics [4]: n, ECE, Brier, log loss
+ * Returns ECE*n*2^32 as an exact integer. */
+uint64_t orc_reliability(const float *p, const uint8_t *y, int64_t n, int n_bins, uint64_t *hist,
+                         double *metrics)
+{
+    memset(hist, 0, sizeof(uint64_t) * 3 * (size_t)n_bins);
+    double brier = 0.0, logloss = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double pd = (double)p[i];
+        int b = (int)floor(pd * n_bins);
+        if (b > n_bins - 1) b = n_bins - 1;
+        hist[3 * b + 0] += 1;
+        hist[3 * b + 1] += y[i] ? 1 : 0;
+        hist[3 * b + 2] += (uint64_t)floor(pd * ORC_Q32);
+        double d = pd - (y[i] ? 1.0 : 0.0);
+        brier += d * d;
+        double pc = pd < 0x1p-24 ? 0x1p-24 : (pd > 1.0 - 0x1p-24 ? 1.0 - 0x1p-24 : pd);
+        logloss += y[i] ? -log(pc) : -log(1.0 - pc);
+    }
+    /* ECE: sum over bins of |I_b|/n |acc - conf| = |L_b - C_b 2^-32| / n */
+    uint64_t E = 0;
+    for (int b = 0; b < n_bins; ++b) {
+        uint64_t L = hist[3 * b + 1] << 32, C = hist[3 * b + 2];
+        E += L > C ? L - C : C - L;
+    }
+    metrics[0] = (double)n;
+    metrics[1] = n ? (double)E / ((double)n * ORC_Q32) : 0.0;
+    metrics[2] = n ? brier / (double)n : 0.0;
+    metrics[3] = n ? logloss / (double)n : 0.0;
+    return E;
+}
+
+/* Calibration of recorded samples under temperatures T[gamma], by depth and
+ * flavour ([AVS] §七 A; [TUT] "置信度质量"; readings R24-R26).
+ *   hist    [2][gamma][n_bins][3], metrics [2][gamma][4]; flavour 0 = the
+ *   cumulative survival S_k against the prefix label, flavour 1 = the
+ *   per-position c_k given that the prefix survived. */
+void orc_calib_stats(const float *z, const int32_t *correct, const int32_t *tested, int64_t N,
+                     int gamma, const float *T, int n_bins, uint64_t *hist, double *metrics,
+                     int *status)
+{
+    for (int k = 0; k < gamma; ++k)
+        if (!(T[k] > 0.0f)) *status |= ORC_ST_BAD_INPUT;
+    float *S = (float *)malloc(sizeof(float) * (size_t)(N ? N : 1));
+    float *c = (float *)malloc(sizeof(float) * (size_t)(N ? N : 1));
+    int *cor = (int *)malloc(sizeof(int) * (size_t)(N ? N : 1));
+    int *tst = (int *)malloc(sizeof(int) * (size_t)(N ? N : 1));
+    float *p = (float *)malloc(sizeof(float) * (size_t)(N ? N : 1));
+    uint8_t *y = (uint8_t *)malloc((size_t)(N ? N : 1));
+    for (int64_t i = 0; i < N; ++i) orc_sample_lens(correct[i], tested[i], gamma, &cor[i], &tst[i], status);
+    for (int k = 0; k < gamma; ++k) {
+        for (int64_t i = 0; i < N; ++i) {
+            float zk = z[(size_t)i * gamma + k];
+            if (zk != zk) *status |= ORC_ST_BAD_INPUT;
+            c[i] = orc_sts(zk, T[k]);
+            S[i] = (k == 0) ? c[i] : S[i] * c[i];
+        }
+        for (int f = 0; f < 2; ++f) {
+            int64_t n = 0;
+            for (int64_t i = 0; i < N; ++i) {
+                int take;
+                float pi = f == 0 ? S[i] : c[i];
+                if (f == 0) take = k < tst[i];
+                else take = k < tst[i] && cor[i] >= k;
+                if (!take || pi != pi) continue;
+                p[n] = pi;
+                y[n] = (uint8_t)(k < cor[i]);
+                ++n;
+            }
+            orc_reliability(p, y, n, n_bins, hist + ((size_t)f * gamma + k) * 3 * (size_t)n_bins,
+                            metrics + ((size_t)f * gamma + k) * 4);
+        }
+    }
+    free(S); free(c); free(cor); free(tst); free(p); free(y);
+}
+
+/* Sequential temperature scaling fit ([AVS] §二 "STS 更像运行时语义桥";
+ * readings R24-R27).  For depth k = 0, 1, ...: for every grid temperature
+ * T_j, the cumulative survival S_k = S_{k-1} * sigmoid(z_k / T_j) (S_{k-1}
+ * from the temperatures already chosen) is scored by its ECE against the
+ * prefix label over the samples observed at depth k; the lowest wins.
+ *   T_fit [gamma], choice [gamma], ece_curve [gamma][J] (nullable), n_obs
+ *   [gamma] (nullable).  The grid must hold positive finite values. */
+void orc_sts_fit(const float *z, const int32_t *correct, const int32_t *tested, int64_t N,
+                 int gamma, const float *grid, int J, int n_bins, float *T_fit, int32_t *choice,
+                 double *ece_curve, int64_t *n_obs, int *status)
+{
+    float *S = (float *)malloc(sizeof(float) * (size_t)(N ? N : 1));
+    int *cor = (int *)malloc(sizeof(int) * (size_t)(N ? N : 1));
+    int *tst = (int *)malloc(sizeof(int) * (size_t)(N ? N : 1));
+    float *p = (float *)malloc(sizeof(float) * (size_t)(N ? N : 1));
+    uint8_t *y = (uint8_t *)malloc((size_t)(N ? N : 1));
+    uint64_t *hist = (uint64_t *)malloc(sizeof(uint64_t) * 3 * (size_t)n_bins);
+    double met[4];
+    for (int64_t i = 0; i < N; ++i) {
+        orc_sample_lens(correct[i], tested[i], gamma, &cor[i], &tst[i], status);
+        S[i] = 1.0f;
+    }
+    for (int k = 0; k < gamma; ++k) {
+        uint64_t best = 0;
+        int jbest = -1;
+        int64_t n = 0;
+        for (int j = 0; j < J; ++j) {
+            n = 0;
+            for (int64_t i = 0; i < N; ++i) {
+                float zk = z[(size_t)i * gamma + k];
+                if (j == 0 && zk != zk) *status |= ORC_ST_BAD_INPUT;
+                if (!(k < tst[i])) continue;     /* past the window: censored */
+                float c = orc_sts(zk, grid[j]);
+                float pi = (k == 0) ? c : S[i] * c;
+                if (pi != pi) continue;
+                p[n] = pi;
+                y[n] = (uint8_t)(k < cor[i]);
+                ++n;
+            }
+            uint64_t E = orc_reliability(p, y, n, n_bins, hist, met);
+            if (ece_curve) ece_curve[(size_t)k * J + j] = met[1];
+            if (n > 0 && (jbest < 0 || E < best)) { best = E; jbest = j; }
+        }
+        if (n_obs) n_obs[k] = n;
+        float Tk = jbest >= 0 ? grid[jbest] : 1.0f;
+        T_fit[k] = Tk;
+        choice[k] = jbest;
+        /* keep this depth's survival for the next one */
+        for (int64_t i = 0; i < N; ++i) {
+            float c = orc_sts(z[(size_t)i * gamma + k], Tk);
+            S[i] = (k == 0) ? c : S[i] * c;
+        }
+    }
+    free(S); free(cor); free(tst); free(p); free(y); free(hist);
 }
