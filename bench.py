@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--separate-plan-pack", action="store_true",
                     help="issue dspark_plan and dspark_pack_verify instead of dspark_plan_pack")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay")
+    ap.add_argument("--no-calib", action="store_true",
+                    help="skip the calibration (recorder, statistics, fit) measurements")
     ap.add_argument("--event-every", type=int, default=16,
                     help="bracket the accept call with events on every n-th timed step")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
@@ -260,6 +262,83 @@ def emit(line, args):
 
 
 # --------------------------------------------------------------------- ours
+
+CAL_N, CAL_GAMMA, CAL_TEMPS, CAL_BINS = 262144, 16, 64, 15
+
+
+def calibration_timing(dev, stream, vs, w, K):
+    """Recorder, statistics and fit timings (CUDA events on the stream)."""
+    import torch
+    from confidence_scheduled_speculative_gb300 import api as _api
+    from confidence_scheduled_speculative_gb300 import workloads as wl
+    out = {}
+    i32 = dict(dtype=torch.int32, device=dev)
+    cap_rows = 1 << 16
+    rz = torch.zeros((cap_rows, w.gamma), dtype=torch.float32, device=dev)
+    rc = torch.zeros(cap_rows, **i32)
+    rt = torch.zeros(cap_rows, **i32)
+    cur = torch.zeros(1, dtype=torch.int64, device=dev)
+    st = torch.zeros(1, **i32)
+    mask = torch.zeros((w.B, w.gamma), dtype=torch.uint8, device=dev)
+
+    def rec():
+        _api.dspark_sts_record(vs.conf_logits, num_correct=vs.num_accepted, B=w.B,
+                               gamma=w.gamma, rec_logits=rz, rec_correct=rc, rec_tested=rt,
+                               cursor=cur, status=st, verify_lens=vs.verify_lens,
+                               prefix_mask=mask)
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for _ in range(n):
+            fn()
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]) * 1e3 / n
+
+    out["record_us"] = timed(rec, min(K, 200))
+    out["record_rows_per_call"] = w.B
+    cs = wl.calibration_samples(CAL_N, CAL_GAMMA, 1.0 + 0.05 * np.arange(CAL_GAMMA), seed=2026)
+    z = torch.from_numpy(cs.conf_logits).to(dev)
+    cor = torch.from_numpy(cs.correct).to(dev)
+    tst = torch.from_numpy(cs.tested).to(dev)
+    T = torch.ones(CAL_GAMMA, dtype=torch.float32, device=dev)
+    met = torch.zeros((2, CAL_GAMMA, 4), dtype=torch.float64, device=dev)
+    ws_s = _api.workspace(_api.dspark_calibration_workspace_bytes(CAL_GAMMA, CAL_BINS), dev)
+
+    def stats():
+        _api.dspark_calibration_stats(z, rec_correct=cor, rec_tested=tst, N=CAL_N,
+                                      gamma=CAL_GAMMA, sts_temps=T, n_bins=CAL_BINS, metrics=met,
+                                      workspace=ws_s, status=st)
+
+    grid = wl.temperature_grid(CAL_TEMPS)
+    T_fit = torch.zeros(CAL_GAMMA, dtype=torch.float32, device=dev)
+    choice = torch.zeros(CAL_GAMMA, **i32)
+    ws_f = _api.workspace(_api.dspark_sts_fit_workspace_bytes(CAL_N, CAL_TEMPS, CAL_BINS), dev)
+
+    def fit():
+        _api.dspark_sts_fit(z, rec_correct=cor, rec_tested=tst, N=CAL_N, gamma=CAL_GAMMA,
+                            temp_grid=grid, n_bins=CAL_BINS, sts_temps_out=T_fit, choice=choice,
+                            workspace=ws_f, status=st)
+
+    s_us = timed(stats, 20)
+    f_us = timed(fit, 5)
+    # sigmoids the fit evaluates: every (sample, candidate) at each depth the
+    # sample's window reached, plus one per sample and depth for S
+    reached = int(np.minimum(cs.tested, CAL_GAMMA).sum())
+    evals = reached * (CAL_TEMPS + 1)
+    out.update({
+        "samples": CAL_N, "gamma": CAL_GAMMA, "temps": CAL_TEMPS, "bins": CAL_BINS,
+        "stats_us": s_us, "stats_samples_per_s": CAL_N / (s_us * 1e-6),
+        "fit_us": f_us, "fit_sigmoids": evals, "fit_sigmoids_per_s": evals / (f_us * 1e-6),
+        "fit_T": [float(x) for x in T_fit.cpu().tolist()],
+        "status": int(st.item()),
+    })
+    return out
+
 
 def run_ours(args):
     import torch
@@ -496,6 +575,13 @@ def run_ours(args):
                 "status": int(st_p.item())}
         del dft_dev, sws
 
+    # ---- calibration (secondary): the STS recorder on this step's accept
+    # outputs, then statistics and the sequential fit over a log of recorded
+    # samples
+    calib = None
+    if not args.no_cap and not args.no_calib:
+        calib = calibration_timing(dev, stream, vs, w, K)
+
     # ---- cap-accept over the full strided block (secondary)
     cap = None
     if not args.no_cap:
@@ -596,6 +682,7 @@ def run_ours(args):
         "cuda_graph": graph,
         "scatter_compact_to_strided": scat,
         "sampling_accept": samp,
+        "calibration": calib,
         "cap_accept": cap,
         "status": status,
     }

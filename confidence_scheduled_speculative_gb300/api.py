@@ -106,6 +106,14 @@ _SIGS = {
     "dspark_greedy_accept_static": (ctypes.c_int, [_VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP,
                                                    _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                                    _VP]),
+    "dspark_sts_record": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _I32, _VP, _VP, _VP, _I64,
+                                         _VP, _VP, _VP, _VP]),
+    "dspark_calibration_workspace_bytes": (_SZ, [_I32, _I32]),
+    "dspark_calibration_stats": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I32, _VP, _I32, _VP, _VP,
+                                                _VP, _SZ, _VP, _VP]),
+    "dspark_sts_fit_workspace_bytes": (_SZ, [_I64, _I32, _I32]),
+    "dspark_sts_fit": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I32, ctypes.POINTER(ctypes.c_float),
+                                      _I32, _I32, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
 }
 
 
@@ -406,3 +414,60 @@ def dspark_greedy_accept_static(logits, *, V, cu_seqlens, draft, prefix_lens, B,
         _p(new_seq_lens, torch.int32, "new_seq_lens"), _p(out_tokens, torch.int32, "out_tokens"),
         _p(status, torch.int32, "status"), _stream(stream))
     _check("dspark_greedy_accept_static", rc)
+
+
+# -------------------------------------------------------------- calibration
+
+def dspark_sts_record(conf_logits, *, num_correct, B, gamma, rec_logits, rec_correct, rec_tested,
+                      cursor, status, verify_lens=None, select=None, prefix_mask=None,
+                      stream=None) -> None:
+    """Append the selected requests of one step to the recorded-sample ring
+    (rec_logits [capacity, gamma] fp32, rec_correct / rec_tested [capacity]
+    int32) at the device cursor (an int64 [1] tensor, bit-identical to the
+    C ABI's uint64)."""
+    rc = load().dspark_sts_record(
+        _p(conf_logits, torch.float32, "conf_logits"), _p(num_correct, torch.int32, "num_correct"),
+        _p(verify_lens, torch.int32, "verify_lens"), _p(select, torch.uint8, "select"), B, gamma,
+        _p(rec_logits, torch.float32, "rec_logits"), _p(rec_correct, torch.int32, "rec_correct"),
+        _p(rec_tested, torch.int32, "rec_tested"), rec_correct.numel(),
+        _p(cursor, torch.int64, "cursor"), _p(prefix_mask, torch.uint8, "prefix_mask"),
+        _p(status, torch.int32, "status"), _stream(stream))
+    _check("dspark_sts_record", rc)
+
+
+def dspark_calibration_workspace_bytes(gamma: int, n_bins: int) -> int:
+    return int(load().dspark_calibration_workspace_bytes(gamma, n_bins))
+
+
+def dspark_calibration_stats(rec_logits, *, rec_correct, rec_tested, N, gamma, sts_temps, n_bins,
+                             metrics, workspace, status, hist=None, stream=None) -> None:
+    """Per-depth calibration (metrics [2, gamma, 4] fp64; hist [2, gamma,
+    n_bins, 3] int64 holding the C ABI's uint64 counts)."""
+    rc = load().dspark_calibration_stats(
+        _p(rec_logits, torch.float32, "rec_logits"), _p(rec_correct, torch.int32, "rec_correct"),
+        _p(rec_tested, torch.int32, "rec_tested"), N, gamma,
+        _p(sts_temps, torch.float32, "sts_temps"), n_bins, _p(hist, torch.int64, "hist"),
+        _p(metrics, torch.float64, "metrics"), _p(workspace),
+        workspace.numel() * workspace.element_size(), _p(status, torch.int32, "status"),
+        _stream(stream))
+    _check("dspark_calibration_stats", rc)
+
+
+def dspark_sts_fit_workspace_bytes(N: int, n_temps: int, n_bins: int) -> int:
+    return int(load().dspark_sts_fit_workspace_bytes(N, n_temps, n_bins))
+
+
+def dspark_sts_fit(rec_logits, *, rec_correct, rec_tested, N, gamma, temp_grid, n_bins,
+                   sts_temps_out, choice, workspace, status, ece_curve=None, n_obs=None,
+                   stream=None) -> None:
+    """Sequential per-depth temperature fit over ``temp_grid`` (a host
+    sequence of positive temperatures)."""
+    grid = (ctypes.c_float * len(temp_grid))(*[float(t) for t in temp_grid])
+    rc = load().dspark_sts_fit(
+        _p(rec_logits, torch.float32, "rec_logits"), _p(rec_correct, torch.int32, "rec_correct"),
+        _p(rec_tested, torch.int32, "rec_tested"), N, gamma, grid, len(temp_grid), n_bins,
+        _p(sts_temps_out, torch.float32, "sts_temps_out"), _p(choice, torch.int32, "choice"),
+        _p(ece_curve, torch.float64, "ece_curve"), _p(n_obs, torch.int64, "n_obs"),
+        _p(workspace), workspace.numel() * workspace.element_size(),
+        _p(status, torch.int32, "status"), _stream(stream))
+    _check("dspark_sts_fit", rc)

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libdspark.so")
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "plan.cu", "pack.cu", "accept.cu", "scatter.cu", "sample.cu"]
+SOURCES = ["api.cu", "plan.cu", "pack.cu", "accept.cu", "scatter.cu", "sample.cu", "calib.cu"]
 
 
 def nvcc() -> str:

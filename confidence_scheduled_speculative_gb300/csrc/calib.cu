@@ -1,0 +1,647 @@
+// calib.cu -- STS recorder, calibration statistics and the sequential
+// temperature fit on sm_103a.
+//
+// Pages (by title and section):
+//   [AVS] "DSpark 自适应 Verify 怎样分配候选预算" §二 (the STS recorder labels
+//         a step with the greedy prefix mask, position k set iff k <
+//         num_correct_drafts; the fitter searches a temperature position by
+//         position, keeping the cumulative survival of the positions already
+//         fitted, and takes the one of lower ECE), §七 A (per-position and
+//         cumulative calibration, ECE, Brier)
+//   [TUT] charlestar.github.io tutorial, "为什么置信度必须校准" (binned ECE;
+//         a position's label only means something once the earlier
+//         positions survived), "截短会制造观测盲区" (positions past a compact
+//         window are censored), "置信度质量" (reliability diagram, ECE,
+//         Brier score or log loss, by depth)
+//
+// A recorded sample is (z[gamma], correct, tested): tested = drafts the
+// target checked, correct = accepted drafts among them.  Depth k is observed
+// iff k < tested (a depth past the window stays out even when the chain broke
+// inside it: keeping it only when its label is known to be 0 would bias the
+// labels).  Label y_k = (k < correct).  Two flavours per depth: the
+// cumulative survival S_k over observed samples, and the conditional c_k over
+// observed samples whose prefix survived through k-1 (correct >= k).
+//
+// Bins and exact sums.  A confidence p (an fp32 in [0, 1]) enters as q =
+// floor(p * 2^32), an integer (p * 2^32 is exact in fp32); its bin is
+// min(q * n_bins >> 32, n_bins - 1), which equals floor(p * n_bins) (for p >=
+// 2^-8 q is p * 2^32 itself, below it both are 0).  Bin counts, label counts
+// and confidence sums are integers added with integer atomics, so they and
+// ECE * n * 2^32 = sum_b |L_b 2^32 - C_b| do not depend on the order in which
+// the GPU adds them.  Brier and log-loss sums are fp64: per-thread terms,
+// warp trees, warps in order, CTAs in order.
+//
+// Kernels
+//   sts_record_kernel  one CTA: block scans number the selected requests,
+//                      rows land at (cursor + i) mod capacity, coalesced
+//                      element copies; the cursor lives on the device, so
+//                      a captured graph can record every step.
+//   calib_stats_kernel one sample per thread, every depth in a loop (the
+//                      fp32 survival product runs left to right); per
+//                      (flavour, depth) the lanes of a warp that share a bin
+//                      are combined with ballots and redux sums and one lane
+//                      adds them to the CTA's shared histogram; CTAs add
+//                      their histograms to a global one with u64 atomics and
+//                      the last CTA (atomic ticket, no waiting) turns it into
+//                      the metrics.
+//   sts_fit_kernel     one launch per depth (programmatic serialization
+//                      chains them).  A CTA stages a tile of 256 samples --
+//                      z_k, the survival S_{k-1} under the temperatures
+//                      already chosen (updated in place in the workspace),
+//                      the label and whether the sample counts -- then every
+//                      thread owns one grid temperature (and one phase of the
+//                      tile when there are fewer than 256 candidates) and
+//                      adds each sample's p = S_{k-1} * c(z_k, T_j) to bins
+//                      private to the thread (shared memory, [bin][thread]
+//                      layout: no atomics, no bank conflicts).  The CTA
+//                      folds its phases into global per-candidate histograms
+//                      with atomics; the last CTA scores every candidate
+//                      (exact integer ECE), picks the lowest (ties to the
+//                      lower index) and clears the histograms for the next
+//                      depth.  The work is N * J fp64 sigmoids per depth: the
+//                      kernel is bound by the fp64 units, not by memory.
+//
+// No kernel waits on another CTA: the last-CTA tickets never spin.
+
+#include "dspark_common.cuh"
+
+namespace dspark {
+
+constexpr int kRecThreads = 1024;
+constexpr int kStatsThreads = 256;
+constexpr int kStatsWarps = kStatsThreads / 32;
+constexpr int kStatsMaxCtas = 1024;
+constexpr int kFitThreads = 256;
+constexpr int kFitTile = 256;  // samples staged per step
+constexpr int kMaxBins = 32;
+constexpr int kMaxTemps = 256;
+constexpr int kMaxGamma = 31;
+constexpr double kQ32 = 4294967296.0;
+
+// q = floor(p * 2^32) for p in [0, 1]
+__device__ __forceinline__ unsigned long long conf_q(float p) {
+    return __float2ull_rz(__fmul_rn(p, 4294967296.0f));
+}
+
+__device__ __forceinline__ int conf_bin(unsigned long long q, int M) {
+    const unsigned long long b = (q * (unsigned long long)M) >> 32;
+    return b < (unsigned long long)(M - 1) ? (int)b : M - 1;
+}
+
+// tested clamped to [0, gamma], correct to [0, tested]
+__device__ __forceinline__ bool sample_lens(int32_t correct, int32_t tested, int gamma, int &c,
+                                            int &t) {
+    bool bad = false;
+    t = tested;
+    c = correct;
+    if (t < 0 || t > gamma) {
+        bad = true;
+        t = t < 0 ? 0 : gamma;
+    }
+    if (c < 0 || c > t) {
+        bad = true;
+        c = c < 0 ? 0 : t;
+    }
+    return bad;
+}
+
+// |L 2^32 - C| summed over the bins of one histogram [M][3]
+__device__ __forceinline__ unsigned long long ece_numerator(const unsigned long long *h, int M,
+                                                            unsigned long long *n_out) {
+    unsigned long long E = 0, n = 0;
+    for (int b = 0; b < M; ++b) {
+        const unsigned long long cnt = __ldcg(h + 3 * b), L = __ldcg(h + 3 * b + 1) << 32,
+                                 C = __ldcg(h + 3 * b + 2);
+        n += cnt;
+        E += L > C ? L - C : C - L;
+    }
+    *n_out = n;
+    return E;
+}
+
+__device__ __forceinline__ double ece_of(unsigned long long E, unsigned long long n) {
+    return n ? __ddiv_rn((double)E, __dmul_rn((double)n, kQ32)) : 0.0;
+}
+
+// ------------------------------------------------------------------ recorder
+
+struct RecordArgs {
+    const float *z;
+    const int32_t *correct;
+    const int32_t *verify_lens;  // nullable: the full block was verified
+    const uint8_t *select;       // nullable: every request
+    int B, gamma;
+    float *rec_z;
+    int32_t *rec_correct, *rec_tested;
+    long long capacity;
+    unsigned long long *cursor;
+    uint8_t *mask;  // nullable
+    int32_t *status;
+};
+
+__global__ void __launch_bounds__(kRecThreads) sts_record_kernel(RecordArgs a) {
+    __shared__ int scan_tmp[33];
+    __shared__ long long slot_s[kRecThreads];
+    __shared__ int corr_s[kRecThreads];
+    pdl_trigger();
+    pdl_wait();  // num_correct / verify_lens come from the accept
+    const unsigned long long cur0 = *a.cursor;
+    int mine = 0;
+    for (int r = threadIdx.x; r < a.B; r += kRecThreads) mine += (!a.select || a.select[r]) ? 1 : 0;
+    const long long count = block_sum<int>(mine, scan_tmp);
+    // more rows than slots: only the last `capacity` selected rows are kept
+    const long long skip = count > a.capacity ? count - a.capacity : 0;
+    bool bad_len = false;
+    long long base = 0;
+    for (int r0 = 0; r0 < a.B; r0 += kRecThreads) {
+        const int r = r0 + (int)threadIdx.x;
+        int tested = a.gamma, c = 0;
+        bool sel = false;
+        if (r < a.B) {
+            if (a.verify_lens) {
+                int L = a.verify_lens[r];
+                if (L < 1 || L > a.gamma + 1) {
+                    bad_len = true;
+                    L = L < 1 ? 1 : a.gamma + 1;
+                }
+                tested = L - 1;
+            }
+            c = a.correct[r];
+            if (c < 0 || c > tested) {
+                bad_len = true;
+                c = c < 0 ? 0 : tested;
+            }
+            sel = !a.select || a.select[r];
+        }
+        int tot;
+        const int pre = block_exclusive_scan<int>(sel ? 1 : 0, scan_tmp, &tot);
+        const long long i = base + pre;
+        long long slot = -1;
+        if (sel && i >= skip)
+            slot = (long long)((cur0 + (unsigned long long)i) % (unsigned long long)a.capacity);
+        if (slot >= 0) {
+            a.rec_correct[slot] = c;
+            a.rec_tested[slot] = tested;
+        }
+        slot_s[threadIdx.x] = slot;
+        corr_s[threadIdx.x] = c;
+        __syncthreads();
+        const int rows = min(kRecThreads, a.B - r0);
+        for (int e = threadIdx.x; e < rows * a.gamma; e += kRecThreads) {
+            const int rr = e / a.gamma, k = e - rr * a.gamma;
+            const size_t src = (size_t)(r0 + rr) * a.gamma + k;
+            const long long s = slot_s[rr];
+            if (s >= 0) a.rec_z[(size_t)s * a.gamma + k] = a.z[src];
+            if (a.mask) a.mask[src] = (uint8_t)(k < corr_s[rr]);
+        }
+        __syncthreads();
+        base += tot;
+    }
+    if (__syncthreads_or(bad_len) && threadIdx.x == 0) flag(a.status, DSPARK_STATUS_BAD_LEN);
+    if (threadIdx.x == 0) {
+        *a.cursor = cur0 + (unsigned long long)count;
+        if (count > a.capacity) flag(a.status, DSPARK_STATUS_CAPACITY);
+    }
+}
+
+// --------------------------------------------------------------- statistics
+
+struct StatsArgs {
+    const float *z;
+    const int32_t *correct, *tested;
+    long long N;
+    int gamma, M;
+    const float *T;
+    unsigned long long *hist_ws;   // [2][gamma][M][3], all zero between calls
+    double *part_ws;               // [gridDim.x][2][gamma][2]
+    unsigned int *ticket;          // zero between calls
+    unsigned long long *hist_out;  // nullable
+    double *metrics;               // [2][gamma][4]
+    int32_t *status;
+};
+
+// Sum over the warp; every lane gets a value, lane 0's is the one used.
+__device__ __forceinline__ double warp_sum_f64(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);
+    return v;
+}
+
+// Add one (prediction, label) per lane, where `inc`, to flavour f, depth k:
+// lanes that share a bin are combined (ballot counts, redux sums of the two
+// 16-bit halves of q) and one of them adds to the CTA histogram; the Brier
+// and log-loss terms go to the warp's own slots.
+__device__ __forceinline__ void stats_add(unsigned long long *hs, double *wsum, int f, int k,
+                                          float p, bool y, bool inc, int lane, int G, int M) {
+    const unsigned any = __ballot_sync(kFullMask, inc);
+    if (!any) return;
+    unsigned long long q = 0;
+    int b = -1;
+    double br = 0.0, ll = 0.0;
+    if (inc) {
+        q = conf_q(p);
+        b = conf_bin(q, M);
+        const double pd = (double)p;
+        const double d = __dsub_rn(pd, y ? 1.0 : 0.0);
+        br = __dmul_rn(d, d);
+        const double pc = fmin(fmax(pd, 0x1p-24), 1.0 - 0x1p-24);
+        ll = y ? -log(pc) : -log(__dsub_rn(1.0, pc));
+    }
+    unsigned pending = any;
+    while (pending) {
+        const int leader = __ffs(pending) - 1;
+        const int b0 = __shfl_sync(kFullMask, b, leader);
+        const bool mine = inc && b == b0;
+        const unsigned m = __ballot_sync(kFullMask, mine);
+        const unsigned ym = __ballot_sync(kFullMask, mine && y);
+        const unsigned hi = __reduce_add_sync(kFullMask, mine ? (unsigned)(q >> 16) : 0u);
+        const unsigned lo = __reduce_add_sync(kFullMask, mine ? (unsigned)(q & 0xffffu) : 0u);
+        if (lane == leader) {
+            unsigned long long *h = hs + ((size_t)(f * G + k) * M + b0) * 3;
+            atomicAdd(h, (unsigned long long)__popc(m));
+            atomicAdd(h + 1, (unsigned long long)__popc(ym));
+            atomicAdd(h + 2, ((unsigned long long)hi << 16) + lo);
+        }
+        pending &= ~m;
+    }
+    br = warp_sum_f64(br);
+    ll = warp_sum_f64(ll);
+    if (lane == 0) {
+        wsum[(f * kMaxGamma + k) * 2] += br;
+        wsum[(f * kMaxGamma + k) * 2 + 1] += ll;
+    }
+}
+
+__global__ void __launch_bounds__(kStatsThreads) calib_stats_kernel(StatsArgs a) {
+    extern __shared__ __align__(16) unsigned long long hs[];  // [2][gamma][M][3]
+    __shared__ double wsum[kStatsWarps][2 * kMaxGamma * 2];
+    __shared__ float T_s[kMaxGamma];
+    __shared__ bool last_s;
+    pdl_trigger();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int G = a.gamma, M = a.M;
+    const int HN = 2 * G * M * 3;
+    for (int i = threadIdx.x; i < HN; i += kStatsThreads) hs[i] = 0;
+    for (int i = threadIdx.x; i < kStatsWarps * 2 * kMaxGamma * 2; i += kStatsThreads)
+        (&wsum[0][0])[i] = 0.0;
+    pdl_wait();
+    if (threadIdx.x < G) T_s[threadIdx.x] = a.T[threadIdx.x];
+    __syncthreads();
+    bool bad_in = blockIdx.x == 0 && threadIdx.x < G && !(T_s[threadIdx.x] > 0.0f);
+    bool bad_len = false;
+    const long long stride = (long long)gridDim.x * kStatsThreads;
+    for (long long base = (long long)blockIdx.x * kStatsThreads; base < a.N; base += stride) {
+        const long long n = base + threadIdx.x;
+        const bool act = n < a.N;
+        int cor = 0, tst = 0;
+        if (act) bad_len |= sample_lens(a.correct[n], a.tested[n], G, cor, tst);
+        float S = 1.0f;
+        for (int k = 0; k < G; ++k) {
+            const float zk = act ? a.z[n * G + k] : 0.0f;
+            if (zk != zk) bad_in = true;
+            const bool obs = act && k < tst;  // the window reached depth k
+            float c = 0.0f;
+            if (obs) {
+                c = sts_confidence(zk, T_s[k]);
+                S = (k == 0) ? c : __fmul_rn(S, c);
+            }
+            const bool y = k < cor;
+            stats_add(hs, wsum[warp], 0, k, S, y, obs && S == S, lane, G, M);
+            stats_add(hs, wsum[warp], 1, k, c, y, obs && cor >= k && c == c, lane, G, M);
+        }
+    }
+    if (__syncthreads_or(bad_in) && threadIdx.x == 0) flag(a.status, DSPARK_STATUS_BAD_INPUT);
+    if (__syncthreads_or(bad_len) && threadIdx.x == 0) flag(a.status, DSPARK_STATUS_BAD_LEN);
+    for (int i = threadIdx.x; i < HN; i += kStatsThreads) {
+        const unsigned long long v = hs[i];
+        if (v) atomicAdd(a.hist_ws + i, v);
+    }
+    // this CTA's Brier / log-loss sums, warps in order; slot (f*G + k)*2 + s
+    for (int i = threadIdx.x; i < 4 * G; i += kStatsThreads) {
+        const int f = i / (2 * G), k = (i >> 1) % G, s = i & 1;
+        double v = 0.0;
+        for (int w = 0; w < kStatsWarps; ++w) v += wsum[w][(f * kMaxGamma + k) * 2 + s];
+        a.part_ws[(size_t)blockIdx.x * (4 * G) + i] = v;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last_s = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!last_s) return;
+    __threadfence();
+    for (int fk = threadIdx.x; fk < 2 * G; fk += kStatsThreads) {
+        unsigned long long n;
+        const unsigned long long E = ece_numerator(a.hist_ws + (size_t)fk * M * 3, M, &n);
+        double br = 0.0, ll = 0.0;
+        for (unsigned c = 0; c < gridDim.x; ++c) {
+            br += __ldcg(a.part_ws + (size_t)c * (4 * G) + 2 * fk);
+            ll += __ldcg(a.part_ws + (size_t)c * (4 * G) + 2 * fk + 1);
+        }
+        double *m = a.metrics + (size_t)fk * 4;
+        m[0] = (double)n;
+        m[1] = ece_of(E, n);
+        m[2] = n ? __ddiv_rn(br, (double)n) : 0.0;
+        m[3] = n ? __ddiv_rn(ll, (double)n) : 0.0;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < HN; i += kStatsThreads) {
+        const unsigned long long v = __ldcg(a.hist_ws + i);
+        if (a.hist_out) a.hist_out[i] = v;
+        a.hist_ws[i] = 0;
+    }
+    if (threadIdx.x == 0) *a.ticket = 0;
+}
+
+// ---------------------------------------------------------------------- fit
+
+struct FitState {
+    unsigned int ticket;
+    int32_t pad;
+    int32_t choice[kMaxGamma + 1];  // the grid index chosen per depth (-1: none)
+};
+
+struct FitArgs {
+    const float *z;
+    const int32_t *correct, *tested;
+    long long N;
+    int gamma, k, J, M, P;     // P = sample phases per tile (kFitThreads / J)
+    float *S;                  // [N] survival of the depths already fitted
+    unsigned long long *hist;  // [J][M][3], all zero between depths
+    FitState *st;
+    float *T_out;
+    int32_t *choice_out;
+    double *ece_curve;  // nullable [gamma][J]
+    long long *n_obs;   // nullable [gamma]
+    int32_t *status;
+    float grid[kMaxTemps];
+};
+
+__global__ void __launch_bounds__(kFitThreads) sts_fit_kernel(const __grid_constant__ FitArgs a) {
+    extern __shared__ __align__(16) unsigned char fsm[];
+    __shared__ float z_s[kFitTile], sp_s[kFitTile];
+    __shared__ unsigned char fl_s[kFitTile];  // bit 0: counts at this depth, bit 1: label
+    __shared__ unsigned long long e_s[kMaxTemps];
+    __shared__ bool last_s;
+    const int M = a.M, J = a.J, P = a.P, k = a.k, G = a.gamma;
+    // private bins, [bin][thread]: confidence sums, counts, label counts
+    unsigned long long *bconf = reinterpret_cast<unsigned long long *>(fsm);
+    unsigned int *bcnt = reinterpret_cast<unsigned int *>(bconf + (size_t)M * kFitThreads);
+    unsigned int *blab = bcnt + (size_t)M * kFitThreads;
+    pdl_trigger();
+    const int tid = threadIdx.x;
+    for (int i = tid; i < M * kFitThreads; i += kFitThreads) {
+        bconf[i] = 0;
+        bcnt[i] = 0;
+        blab[i] = 0;
+    }
+    const int j = tid % J, ph = tid / J;
+    const bool worker = ph < P;
+    const float Tj = a.grid[worker ? j : 0];
+    pdl_wait();  // the previous depth chose its temperature and updated S
+    float Tprev = 1.0f;
+    if (k > 0) {
+        const int cp = __ldcg(&a.st->choice[k - 1]);
+        Tprev = cp >= 0 ? a.grid[cp] : 1.0f;
+    }
+    bool bad_in = false, bad_len = false;
+    const long long ntiles = (a.N + kFitTile - 1) / kFitTile;
+    for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const long long n = t * kFitTile + tid;
+        unsigned char fl = 0;
+        float zk = 0.0f, sp = 1.0f;
+        if (n < a.N) {
+            int cor, tst;
+            const bool bl = sample_lens(a.correct[n], a.tested[n], G, cor, tst);
+            if (k == 0) bad_len |= bl;
+            zk = a.z[n * G + k];
+            if (zk != zk) bad_in = true;
+            if (k < tst) {
+                // S_{k-1} under the chosen temperatures; only samples whose
+                // window reaches k need it, now or at any later depth
+                if (k > 0) {
+                    const float cprev = sts_confidence(a.z[n * G + k - 1], Tprev);
+                    sp = (k == 1) ? cprev : __fmul_rn(a.S[n], cprev);
+                    a.S[n] = sp;
+                }
+                if (zk == zk && sp == sp) fl = 1;
+            }
+            if (k < cor) fl |= 2;
+        }
+        z_s[tid] = zk;
+        sp_s[tid] = sp;
+        fl_s[tid] = fl;
+        __syncthreads();
+        if (worker) {
+            for (int s = ph; s < kFitTile; s += P) {
+                const unsigned f = fl_s[s];
+                if (!(f & 1u)) continue;
+                const float c = sts_confidence(z_s[s], Tj);
+                const float p = (k == 0) ? c : __fmul_rn(sp_s[s], c);
+                const unsigned long long q = conf_q(p);
+                const int idx = conf_bin(q, M) * kFitThreads + tid;
+                bcnt[idx] += 1u;
+                blab[idx] += f >> 1;
+                bconf[idx] += q;
+            }
+        }
+        __syncthreads();
+    }
+    if (__syncthreads_or(bad_in) && tid == 0) flag(a.status, DSPARK_STATUS_BAD_INPUT);
+    if (__syncthreads_or(bad_len) && tid == 0) flag(a.status, DSPARK_STATUS_BAD_LEN);
+    // fold the phases of each candidate and publish
+    for (int pair = tid; pair < J * M; pair += kFitThreads) {
+        const int jj = pair % J, b = pair / J;
+        unsigned long long cnt = 0, lab = 0, conf = 0;
+        for (int q = 0; q < P; ++q) {
+            const int idx = b * kFitThreads + q * J + jj;
+            cnt += bcnt[idx];
+            lab += blab[idx];
+            conf += bconf[idx];
+        }
+        if (cnt) {
+            unsigned long long *h = a.hist + ((size_t)jj * M + b) * 3;
+            atomicAdd(h, cnt);
+            atomicAdd(h + 1, lab);
+            atomicAdd(h + 2, conf);
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) last_s = atomicAdd(&a.st->ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!last_s) return;
+    __threadfence();
+    unsigned long long n = 0;
+    if (tid < J) {
+        const unsigned long long E = ece_numerator(a.hist + (size_t)tid * M * 3, M, &n);
+        e_s[tid] = E;
+        if (a.ece_curve) a.ece_curve[(size_t)k * J + tid] = ece_of(E, n);
+    }
+    __syncthreads();
+    if (tid == 0) {  // n: samples counted at this depth (the same for every candidate)
+        int best = -1;
+        unsigned long long bestE = 0;
+        if (n > 0)
+            for (int jj = 0; jj < J; ++jj)
+                if (best < 0 || e_s[jj] < bestE) {
+                    best = jj;
+                    bestE = e_s[jj];
+                }
+        a.st->choice[k] = best;
+        a.choice_out[k] = best;
+        a.T_out[k] = best >= 0 ? a.grid[best] : 1.0f;
+        if (a.n_obs) a.n_obs[k] = (long long)n;
+        a.st->ticket = 0;
+    }
+    for (int i = tid; i < J * M * 3; i += kFitThreads) a.hist[i] = 0;
+}
+
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+size_t stats_hist_bytes(int gamma, int M) { return align256((size_t)2 * gamma * M * 3 * 8); }
+
+size_t fit_hist_bytes(int J, int M) { return align256((size_t)J * M * 3 * 8); }
+
+}  // namespace dspark
+
+using namespace dspark;
+
+extern "C" int dspark_sts_record(const float *conf_logits, const int32_t *num_correct,
+                                 const int32_t *verify_lens, const uint8_t *select, int32_t B,
+                                 int32_t gamma, float *rec_logits, int32_t *rec_correct,
+                                 int32_t *rec_tested, int64_t capacity, uint64_t *cursor,
+                                 uint8_t *prefix_mask, int32_t *status, void *stream) {
+    if (!conf_logits || !num_correct || !rec_logits || !rec_correct || !rec_tested || !cursor ||
+        !status)
+        return DSPARK_ERR_INVALID_ARG;
+    if (B < 1 || gamma < 1 || gamma > kMaxGamma || capacity < 1) return DSPARK_ERR_INVALID_ARG;
+    RecordArgs a;
+    a.z = conf_logits;
+    a.correct = num_correct;
+    a.verify_lens = verify_lens;
+    a.select = select;
+    a.B = B;
+    a.gamma = gamma;
+    a.rec_z = rec_logits;
+    a.rec_correct = rec_correct;
+    a.rec_tested = rec_tested;
+    a.capacity = capacity;
+    a.cursor = reinterpret_cast<unsigned long long *>(cursor);
+    a.mask = prefix_mask;
+    a.status = status;
+    const cudaError_t e = launch_pdl(sts_record_kernel, dim3(1), dim3(kRecThreads), 0,
+                                     static_cast<cudaStream_t>(stream), a);
+    return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+extern "C" size_t dspark_calibration_workspace_bytes(int32_t gamma, int32_t n_bins) {
+    if (gamma < 1 || gamma > kMaxGamma || n_bins < 1 || n_bins > kMaxBins) return 0;
+    return stats_hist_bytes(gamma, n_bins) + 256 +
+           align256((size_t)kStatsMaxCtas * 4 * gamma * sizeof(double));
+}
+
+extern "C" int dspark_calibration_stats(const float *rec_logits, const int32_t *rec_correct,
+                                        const int32_t *rec_tested, int64_t N, int32_t gamma,
+                                        const float *sts_temps, int32_t n_bins, uint64_t *hist,
+                                        double *metrics, void *workspace,
+                                        size_t workspace_bytes, int32_t *status, void *stream) {
+    if (!sts_temps || !metrics || !status) return DSPARK_ERR_INVALID_ARG;
+    if (N > 0 && (!rec_logits || !rec_correct || !rec_tested)) return DSPARK_ERR_INVALID_ARG;
+    if (N < 0 || gamma < 1 || gamma > kMaxGamma || n_bins < 1 || n_bins > kMaxBins)
+        return DSPARK_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < dspark_calibration_workspace_bytes(gamma, n_bins) ||
+        !aligned(workspace, 256))
+        return DSPARK_ERR_WORKSPACE;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    StatsArgs a;
+    a.z = rec_logits;
+    a.correct = rec_correct;
+    a.tested = rec_tested;
+    a.N = N;
+    a.gamma = gamma;
+    a.M = n_bins;
+    a.T = sts_temps;
+    a.hist_ws = reinterpret_cast<unsigned long long *>(ws);
+    a.ticket = reinterpret_cast<unsigned int *>(ws + stats_hist_bytes(gamma, n_bins));
+    a.part_ws = reinterpret_cast<double *>(ws + stats_hist_bytes(gamma, n_bins) + 256);
+    a.hist_out = reinterpret_cast<unsigned long long *>(hist);
+    a.metrics = metrics;
+    a.status = status;
+    const int smem = 2 * gamma * n_bins * 3 * 8;
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(calib_stats_kernel), smem, 7);
+    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, calib_stats_kernel, kStatsThreads,
+                                                      (size_t)smem);
+    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+    const long long tiles = (N + kStatsThreads - 1) / kStatsThreads;
+    long long g = (long long)sm_count() * (occ > 0 ? occ : 1);
+    g = g < tiles ? g : tiles;
+    g = g < kStatsMaxCtas ? g : kStatsMaxCtas;
+    g = g < 1 ? 1 : g;
+    e = launch_pdl(calib_stats_kernel, dim3((unsigned)g), dim3(kStatsThreads), (size_t)smem,
+                   static_cast<cudaStream_t>(stream), a);
+    return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+extern "C" size_t dspark_sts_fit_workspace_bytes(int64_t N, int32_t n_temps, int32_t n_bins) {
+    if (N < 0 || n_temps < 1 || n_temps > kMaxTemps || n_bins < 1 || n_bins > kMaxBins) return 0;
+    return align256(sizeof(FitState)) + fit_hist_bytes(n_temps, n_bins) +
+           align256((size_t)N * sizeof(float));
+}
+
+extern "C" int dspark_sts_fit(const float *rec_logits, const int32_t *rec_correct,
+                              const int32_t *rec_tested, int64_t N, int32_t gamma,
+                              const float *temp_grid, int32_t n_temps, int32_t n_bins,
+                              float *sts_temps_out, int32_t *choice, double *ece_curve,
+                              int64_t *n_obs, void *workspace, size_t workspace_bytes,
+                              int32_t *status, void *stream) {
+    if (!temp_grid || !sts_temps_out || !choice || !status) return DSPARK_ERR_INVALID_ARG;
+    if (N > 0 && (!rec_logits || !rec_correct || !rec_tested)) return DSPARK_ERR_INVALID_ARG;
+    if (N < 0 || gamma < 1 || gamma > kMaxGamma || n_temps < 1 || n_temps > kMaxTemps ||
+        n_bins < 1 || n_bins > kMaxBins)
+        return DSPARK_ERR_INVALID_ARG;
+    for (int i = 0; i < n_temps; ++i)  // the grid is host memory
+        if (!(temp_grid[i] > 0.0f) || !(temp_grid[i] < INFINITY)) return DSPARK_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < dspark_sts_fit_workspace_bytes(N, n_temps, n_bins) ||
+        !aligned(workspace, 256))
+        return DSPARK_ERR_WORKSPACE;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    FitArgs a;
+    a.z = rec_logits;
+    a.correct = rec_correct;
+    a.tested = rec_tested;
+    a.N = N;
+    a.gamma = gamma;
+    a.J = n_temps;
+    a.M = n_bins;
+    a.P = kFitThreads / n_temps;
+    a.st = reinterpret_cast<FitState *>(ws);
+    a.hist = reinterpret_cast<unsigned long long *>(ws + align256(sizeof(FitState)));
+    a.S = reinterpret_cast<float *>(ws + align256(sizeof(FitState)) +
+                                    fit_hist_bytes(n_temps, n_bins));
+    a.T_out = sts_temps_out;
+    a.choice_out = choice;
+    a.ece_curve = ece_curve;
+    a.n_obs = reinterpret_cast<long long *>(n_obs);
+    a.status = status;
+    for (int i = 0; i < kMaxTemps; ++i) a.grid[i] = i < n_temps ? temp_grid[i] : 1.0f;
+    const int smem = n_bins * kFitThreads * 16;
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(sts_fit_kernel), smem, 8);
+    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sts_fit_kernel, kFitThreads,
+                                                      (size_t)smem);
+    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+    const long long tiles = (N + kFitTile - 1) / kFitTile;
+    long long g = (long long)sm_count() * (occ > 0 ? occ : 1);
+    g = g < tiles ? g : tiles;
+    g = g < 1 ? 1 : g;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (int k = 0; k < gamma; ++k) {
+        a.k = k;
+        e = launch_pdl(sts_fit_kernel, dim3((unsigned)g), dim3(kFitThreads), (size_t)smem, s, a);
+        if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+    }
+    return DSPARK_OK;
+}

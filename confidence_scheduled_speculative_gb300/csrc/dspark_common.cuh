@@ -1,5 +1,5 @@
 // dspark_common.cuh -- device helpers and host plumbing shared by the
-// library's translation units (plan.cu, pack.cu, accept.cu, api.cu).
+// library's translation units.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -29,6 +29,17 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// STS-calibrated conditional confidence c = sigmoid(z / T) ([AVS] §二, the
+// runtime formula c_i = sigmoid(z_i / T_i)): IEEE fp32 division, the sigmoid
+// in fp64 with CUDA's exp, rounded once to fp32.  The planner's survivals and
+// the calibration statistics and fit all go through this one function, so a
+// fitted temperature scores exactly the survivals the planner will compute.
+__device__ __forceinline__ float sts_confidence(float z, float T) {
+    const float t = __fdiv_rn(z, T);                        // IEEE fp32 division
+    const double e = exp(-(double)t);                       // CUDA's fp64 exp
+    return __double2float_rn(__ddiv_rn(1.0, __dadd_rn(1.0, e)));
 }
 
 // Block-wide exclusive scan over blockDim.x threads (a multiple of 32, at

@@ -167,9 +167,7 @@ survival_kernel(const float *__restrict__ z, const float *__restrict__ T, int B,
         const float zk = z[(size_t)r * gamma + lane];
         const float tk = T[lane];
         bad = (zk != zk) || !(tk > 0.0f);
-        const float t = __fdiv_rn(zk, tk);                      // IEEE fp32 division
-        const double e = exp(-(double)t);                       // CUDA's fp64 exp
-        c = __double2float_rn(__ddiv_rn(1.0, __dadd_rn(1.0, e)));
+        c = sts_confidence(zk, tk);
     }
     // S_k = (((c_0 c_1) c_2) ... c_k): every lane gathers c_0..c_k and multiplies
     // them strictly left to right.

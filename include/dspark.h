@@ -1,6 +1,7 @@
 /*
  * dspark.h -- C ABI of the GB300 (sm_103a) DSpark verify planner, ragged
- * verify pack and greedy / cap-accept library (libdspark.so).
+ * verify pack, greedy / cap / sampling accept, compact-to-strided scatter and
+ * calibration library (libdspark.so).
  *
  * Pages cited below (by title and section):
  *   [AVS]   "DSpark 自适应 Verify 怎样分配候选预算" -- DSpark adaptive
@@ -393,6 +394,116 @@ DSPARK_API int dspark_greedy_accept_static(const void *logits, int32_t dtype, in
                          int32_t *num_accepted, int32_t *bonus, int32_t *commit_lens,
                          int32_t *new_seq_lens, int32_t *out_tokens, int32_t *status,
                          void *stream);
+
+/* ------------------------------------------------------------ calibration
+ *
+ * STS recorder, calibration statistics and the sequential temperature fit.
+ *   [AVS] §二 "但 SGLang STS 校准的不是同一个 soft target" (the recorder's
+ *   label: prefix_mask = positions < num_correct_drafts) and "STS
+ *   更像运行时语义桥" (c_i = sigmoid(z_i / T_i); the fitter picks a
+ *   temperature position by position, keeping the cumulative survival of the
+ *   positions already fitted, by lowest ECE); §七 A (per-position and
+ *   cumulative calibration, ECE, Brier).  [TUT] "为什么置信度必须校准"
+ *   (ECE = sum_b |I_b|/n |acc(I_b) - conf(I_b)|), "截短会制造观测盲区"
+ *   (positions past a compact window are censored), "置信度质量" (by depth;
+ *   reliability diagram; ECE, Brier score or log loss).
+ *
+ * A recorded sample is one request of one step: its confidence logits
+ * z[gamma] (fp32), `correct` = drafts accepted and `tested` = drafts the
+ * target checked.  Definitions used by the statistics and the fit:
+ *   - tested is clamped to [0, gamma] and correct to [0, tested] (BAD_LEN);
+ *   - depth k is observed iff k < tested; its label is y_k = (k < correct);
+ *   - flavour 0 (cumulative): prediction S_k = c_0 * ... * c_k (fp32, left
+ *     to right, c as in dspark_plan), over observed samples; flavour 1
+ *     (per-position): prediction c_k over observed samples with correct >= k
+ *     (the prefix survived through k-1); a NaN prediction is left out;
+ *   - n_bins equal-width bins over [0, 1]: bin = min(floor(p*n_bins),
+ *     n_bins-1); each confidence enters the bin sums as floor(p * 2^32), so
+ *     the bin sums are exact integers and ECE = sum_b |L_b 2^32 - C_b| /
+ *     (n 2^32) is exact up to its final rounding (within 2^-32 of the
+ *     real-number ECE);
+ *   - Brier = mean (p - y)^2 and log loss = mean -[y ln p + (1-y) ln(1-p)]
+ *     with p clamped to [2^-24, 1 - 2^-24], summed in fp64 (deterministic
+ *     for a given GPU; the order differs from a sequential sum);
+ *   - a flavour/depth with no sample reports n = 0 and zeros. */
+
+/* Append the selected requests of one step to ring buffers of recorded
+ * samples, and optionally write the step's greedy prefix mask.
+ *   conf_logits  [B, gamma] fp32 confidence logits of the step
+ *   num_correct  [B] accepted drafts (num_accepted of the compact accept, or
+ *                the cap-accept ceiling with verify_lens NULL)
+ *   verify_lens  [B] (nullable): tested = verify_len - 1, verify_len clamped
+ *                to [1, gamma+1] (BAD_LEN); NULL = the full block was tested
+ *   select       [B] uint8 (nullable): record request r iff select[r] != 0;
+ *                NULL records every request
+ *   rec_logits   [capacity, gamma] fp32, rec_correct / rec_tested
+ *                [capacity] int32: the ring; the i-th selected request of the
+ *                call (request order) goes to slot (*cursor + i) % capacity;
+ *                num_correct is stored clamped to [0, tested] (BAD_LEN)
+ *   cursor       device uint64[1], advanced by the number selected (so a
+ *                captured graph can record every step); when one call
+ *                selects more than capacity requests only the last capacity
+ *                are written (CAPACITY)
+ *   prefix_mask  [B, gamma] uint8 (nullable): (k < clamped num_correct)
+ * One CTA; any B.  Errors: INVALID_ARG (null required pointer, B < 1, gamma
+ * outside 1..31, capacity < 1); CUDA. */
+DSPARK_API int dspark_sts_record(const float *conf_logits, const int32_t *num_correct,
+                                 const int32_t *verify_lens, const uint8_t *select, int32_t B,
+                                 int32_t gamma, float *rec_logits, int32_t *rec_correct,
+                                 int32_t *rec_tested, int64_t capacity, uint64_t *cursor,
+                                 uint8_t *prefix_mask, int32_t *status, void *stream);
+
+/* Workspace of dspark_calibration_stats (independent of N); 0 for gamma
+ * outside 1..31 or n_bins outside 1..32.  Zero-fill it once before its first
+ * use: every call leaves it zeroed again. */
+DSPARK_API size_t dspark_calibration_workspace_bytes(int32_t gamma, int32_t n_bins);
+
+/* Calibration of N recorded samples under temperatures sts_temps, by depth.
+ *   rec_logits [N, gamma] fp32, rec_correct / rec_tested [N] int32 (may be
+ *              NULL when N == 0)
+ *   sts_temps  [gamma] fp32 (a value that is not > 0 flags BAD_INPUT and is
+ *              used as given)
+ *   hist       out [2][gamma][n_bins][3] uint64 (nullable): per flavour,
+ *              depth and bin -- count, label sum, confidence sum in 2^-32
+ *              units (a reliability diagram)
+ *   metrics    out [2][gamma][4] fp64: n, ECE, Brier, log loss
+ * Device flags: BAD_INPUT (NaN logit anywhere, temperature not > 0),
+ * BAD_LEN.  Errors: INVALID_ARG (null required pointer, N < 0, gamma outside
+ * 1..31, n_bins outside 1..32); WORKSPACE; CUDA. */
+DSPARK_API int dspark_calibration_stats(const float *rec_logits, const int32_t *rec_correct,
+                                        const int32_t *rec_tested, int64_t N, int32_t gamma,
+                                        const float *sts_temps, int32_t n_bins, uint64_t *hist,
+                                        double *metrics, void *workspace,
+                                        size_t workspace_bytes, int32_t *status, void *stream);
+
+/* Workspace of dspark_sts_fit; 0 outside the envelope.  Zero-fill it once
+ * before its first use: every call leaves the part that must be zero zeroed
+ * again. */
+DSPARK_API size_t dspark_sts_fit_workspace_bytes(int64_t N, int32_t n_temps, int32_t n_bins);
+
+/* Sequential temperature scaling fit.  For depth k = 0, 1, ..., gamma-1 and
+ * every grid temperature T_j: the cumulative survival S_k = S_{k-1} *
+ * sigmoid(z_k / T_j), with S_{k-1} under the temperatures already chosen,
+ * is scored by its ECE (flavour 0 above) over the samples observed at depth
+ * k; the lowest ECE * n * 2^32 (an exact integer) wins, ties to the lower
+ * grid index.  A depth with no observed sample gets T = 1 and choice -1.
+ *   rec_*         as in dspark_calibration_stats (NULL allowed when N == 0)
+ *   temp_grid     HOST [n_temps] fp32, each positive and finite
+ *   sts_temps_out out [gamma] fp32: the fitted temperatures (grid values)
+ *   choice        out [gamma] int32: grid index per depth, -1 = none
+ *   ece_curve     out [gamma][n_temps] fp64 (nullable): ECE of every candidate
+ *   n_obs         out [gamma] int64 (nullable): samples observed per depth
+ * gamma launches (one per depth), N * n_temps fp32-rounded fp64 sigmoids
+ * each.  Device flags: BAD_INPUT (NaN logit), BAD_LEN.  Errors: INVALID_ARG
+ * (null required pointer, N < 0, gamma outside 1..31, n_temps outside
+ * 1..256, a grid value not positive and finite, n_bins outside 1..32);
+ * WORKSPACE; CUDA. */
+DSPARK_API int dspark_sts_fit(const float *rec_logits, const int32_t *rec_correct,
+                              const int32_t *rec_tested, int64_t N, int32_t gamma,
+                              const float *temp_grid /* host */, int32_t n_temps, int32_t n_bins,
+                              float *sts_temps_out, int32_t *choice, double *ece_curve,
+                              int64_t *n_obs, void *workspace, size_t workspace_bytes,
+                              int32_t *status, void *stream);
 
 #ifdef __cplusplus
 }

@@ -217,3 +217,64 @@ def test_sampling_argument_checks(lib):
     assert call(B=5000) == -4
     assert call(ws=None) == -2
     assert call(wsb=need - 256) == -2
+
+
+def test_calibration_argument_checks(lib):
+    rec = lib.dspark_sts_record
+    rec.restype = ctypes.c_int
+
+    def record(z=FAKE, corr=FAKE, B=4, g=4, cap=10, cursor=FAKE):
+        return rec(z, corr, None, None, B, g, FAKE, FAKE, FAKE, ctypes.c_int64(cap), cursor, None,
+                   FAKE, None)
+
+    assert record(z=None) == -1
+    assert record(corr=None) == -1
+    assert record(cursor=None) == -1
+    assert record(B=0) == -1
+    assert record(g=32) == -1
+    assert record(cap=0) == -1
+
+    lib.dspark_calibration_workspace_bytes.restype = ctypes.c_size_t
+    need = lib.dspark_calibration_workspace_bytes(8, 10)
+    assert need % 256 == 0 and need >= 2 * 8 * 10 * 3 * 8
+    assert lib.dspark_calibration_workspace_bytes(8, 33) == 0
+    assert lib.dspark_calibration_workspace_bytes(0, 10) == 0
+    stats = lib.dspark_calibration_stats
+    stats.restype = ctypes.c_int
+
+    def call_stats(N=100, g=8, M=10, T=FAKE, ws=FAKE, wsb=need, met=FAKE):
+        return stats(FAKE, FAKE, FAKE, ctypes.c_int64(N), g, T, M, None, met, ws,
+                     ctypes.c_size_t(wsb), FAKE, None)
+
+    assert call_stats(N=-1) == -1
+    assert call_stats(T=None) == -1
+    assert call_stats(met=None) == -1
+    assert call_stats(M=0) == -1
+    assert call_stats(M=33) == -1
+    assert call_stats(ws=None) == -2
+    assert call_stats(wsb=need - 1) == -2
+    assert call_stats(ws=ctypes.c_void_p(0x10010)) == -2
+
+    lib.dspark_sts_fit_workspace_bytes.restype = ctypes.c_size_t
+    need = lib.dspark_sts_fit_workspace_bytes(ctypes.c_int64(1000), 2, 10)
+    assert need % 256 == 0 and need >= 1000 * 4 + 2 * 10 * 24
+    assert lib.dspark_sts_fit_workspace_bytes(ctypes.c_int64(10), 257, 10) == 0
+    fit = lib.dspark_sts_fit
+    fit.restype = ctypes.c_int
+
+    def call_fit(grid=(1.0, 2.0), N=1000, g=8, M=10, ws=FAKE, wsb=need, out=FAKE):
+        arr = (ctypes.c_float * max(1, len(grid)))(*grid)
+        return fit(FAKE, FAKE, FAKE, ctypes.c_int64(N), g, arr, len(grid), M, out, FAKE, None,
+                   None, ws, ctypes.c_size_t(wsb), FAKE, None)
+
+    assert call_fit(grid=()) == -1
+    assert call_fit(grid=[1.0] * 257) == -1
+    assert call_fit(grid=(1.0, 0.0)) == -1
+    assert call_fit(grid=(1.0, -2.0)) == -1
+    assert call_fit(grid=(1.0, float("inf"))) == -1
+    assert call_fit(grid=(float("nan"),)) == -1
+    assert call_fit(out=None) == -1
+    assert call_fit(g=0) == -1
+    assert call_fit(M=40) == -1
+    assert call_fit(ws=None) == -2
+    assert call_fit(wsb=need - 256) == -2
