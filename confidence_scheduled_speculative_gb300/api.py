@@ -106,6 +106,7 @@ _SIGS = {
     "dspark_greedy_accept_static": (ctypes.c_int, [_VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP,
                                                    _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                                    _VP]),
+    "dspark_sts_confidence": (ctypes.c_int, [_VP, _VP, _I64, _I32, _VP, _VP, _VP]),
     "dspark_sts_record": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _I32, _VP, _VP, _VP, _I64,
                                          _VP, _VP, _VP, _VP]),
     "dspark_calibration_workspace_bytes": (_SZ, [_I32, _I32]),
@@ -417,6 +418,16 @@ def dspark_greedy_accept_static(logits, *, V, cu_seqlens, draft, prefix_lens, B,
 
 
 # -------------------------------------------------------------- calibration
+
+def dspark_sts_confidence(conf_logits, *, sts_temps, conf_out, status, stream=None) -> None:
+    """c = sigmoid(z / T) elementwise over conf_logits [n_rows, gamma]."""
+    n_rows, gamma = conf_logits.shape
+    rc = load().dspark_sts_confidence(
+        _p(conf_logits, torch.float32, "conf_logits"), _p(sts_temps, torch.float32, "sts_temps"),
+        n_rows, gamma, _p(conf_out, torch.float32, "conf_out"), _p(status, torch.int32, "status"),
+        _stream(stream))
+    _check("dspark_sts_confidence", rc)
+
 
 def dspark_sts_record(conf_logits, *, num_correct, B, gamma, rec_logits, rec_correct, rec_tested,
                       cursor, status, verify_lens=None, select=None, prefix_mask=None,

@@ -204,6 +204,24 @@ __global__ void __launch_bounds__(kRecThreads) sts_record_kernel(RecordArgs a) {
     }
 }
 
+// -------------------------------------------------------------------- STS
+
+// c[r][k] = sigmoid(z[r][k] / T[k]), elementwise over a grid-stride loop.
+__global__ void __launch_bounds__(256) sts_confidence_kernel(const float *z, const float *T,
+                                                             long long n, int gamma, float *c,
+                                                             int32_t *status) {
+    pdl_trigger();
+    pdl_wait();
+    bool bad = false;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const float zi = z[i], Ti = __ldg(T + i % gamma);
+        bad |= (zi != zi) || !(Ti > 0.0f);
+        c[i] = sts_confidence(zi, Ti);
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0) flag(status, DSPARK_STATUS_BAD_INPUT);
+}
+
 // --------------------------------------------------------------- statistics
 
 struct StatsArgs {
@@ -531,6 +549,23 @@ extern "C" int dspark_sts_record(const float *conf_logits, const int32_t *num_co
     a.status = status;
     const cudaError_t e = launch_pdl(sts_record_kernel, dim3(1), dim3(kRecThreads), 0,
                                      static_cast<cudaStream_t>(stream), a);
+    return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+extern "C" int dspark_sts_confidence(const float *conf_logits, const float *sts_temps,
+                                    int64_t n_rows, int32_t gamma, float *conf_out,
+                                    int32_t *status, void *stream) {
+    if (!sts_temps || !status) return DSPARK_ERR_INVALID_ARG;
+    if (n_rows < 0 || gamma < 1) return DSPARK_ERR_INVALID_ARG;
+    if (n_rows > 0 && (!conf_logits || !conf_out)) return DSPARK_ERR_INVALID_ARG;
+    const long long n = (long long)n_rows * gamma;
+    if (n == 0) return DSPARK_OK;
+    long long g = (n + 255) / 256;
+    const long long cap = (long long)sm_count() * 8;
+    g = g < cap ? g : cap;
+    const cudaError_t e = launch_pdl(sts_confidence_kernel, dim3((unsigned)g), dim3(256), 0,
+                                     static_cast<cudaStream_t>(stream), conf_logits, sts_temps, n,
+                                     (int)gamma, conf_out, status);
     return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 

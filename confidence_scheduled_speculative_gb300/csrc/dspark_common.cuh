@@ -7,6 +7,7 @@
 #include <cstdint>
 
 #include "../../include/dspark.h"
+#include "sigmoid.cuh"
 
 namespace dspark {
 
@@ -32,14 +33,17 @@ __device__ __forceinline__ void pdl_trigger() {
 }
 
 // STS-calibrated conditional confidence c = sigmoid(z / T) ([AVS] §二, the
-// runtime formula c_i = sigmoid(z_i / T_i)): IEEE fp32 division, the sigmoid
-// in fp64 with CUDA's exp, rounded once to fp32.  The planner's survivals and
-// the calibration statistics and fit all go through this one function, so a
-// fitted temperature scores exactly the survivals the planner will compute.
+// runtime formula c_i = sigmoid(z_i / T_i)): IEEE fp32 division, then the
+// fp64 sigmoid 1 / (1 + exp(-t)) with CUDA's exp, rounded once to fp32 --
+// computed in fp32 arithmetic where that certifies the same rounding
+// (sigmoid.cuh).  The planner's survivals and the calibration statistics and
+// fit all go through this one function, so a fitted temperature scores
+// exactly the survivals the planner will compute.
 __device__ __forceinline__ float sts_confidence(float z, float T) {
-    const float t = __fdiv_rn(z, T);                        // IEEE fp32 division
-    const double e = exp(-(double)t);                       // CUDA's fp64 exp
-    return __double2float_rn(__ddiv_rn(1.0, __dadd_rn(1.0, e)));
+    const float t = __fdiv_rn(z, T);  // IEEE fp32 division
+    float c;
+    if (sigmoid_f32(t, c)) return c;
+    return sigmoid_f64(t);
 }
 
 // Block-wide exclusive scan over blockDim.x threads (a multiple of 32, at

@@ -427,6 +427,18 @@ DSPARK_API int dspark_greedy_accept_static(const void *logits, int32_t dtype, in
  *     for a given GPU; the order differs from a sequential sum);
  *   - a flavour/depth with no sample reports n = 0 and zeros. */
 
+/* STS-calibrated confidences c[r][k] = sigmoid(conf_logits[r][k] /
+ * sts_temps[k]) ([AVS] §二, c_i = sigmoid(z_i / T_i)), elementwise over
+ * [n_rows, gamma] fp32 -- the same values the planner multiplies into its
+ * survivals: IEEE fp32 division, then the fp64 formula 1 / (1 + exp(-t))
+ * rounded once to fp32 (evaluated in fp32 arithmetic wherever that
+ * certifies the same rounding).  Flags BAD_INPUT for a NaN logit or a
+ * temperature that is not > 0.  Errors: INVALID_ARG (null pointer, n_rows <
+ * 0, gamma < 1); CUDA. */
+DSPARK_API int dspark_sts_confidence(const float *conf_logits, const float *sts_temps,
+                                     int64_t n_rows, int32_t gamma, float *conf_out,
+                                     int32_t *status, void *stream);
+
 /* Append the selected requests of one step to ring buffers of recorded
  * samples, and optionally write the step's greedy prefix mask.
  *   conf_logits  [B, gamma] fp32 confidence logits of the step

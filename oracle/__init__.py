@@ -67,6 +67,8 @@ def lib():
             ci, cf, cd, cl = ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_int64
             L.orc_sts.argtypes = [cf, cf]
             L.orc_sts.restype = cf
+            L.orc_sts_rows.argtypes = [f32p, f32p, ctypes.c_int64, ci, f32p, i32p]
+            L.orc_sts_rows.restype = None
             L.orc_survival.argtypes = [f32p, f32p, ci, ci, cf, f32p, f32p, i32p]
             L.orc_survival.restype = None
             L.orc_plan_from_survivals.argtypes = [f32p, ci, ci, cf, ci, ci, ci, ci, ci, i32p, f64p,
@@ -124,6 +126,18 @@ def _c(a, dtype):
 
 def sts(z: float, T: float) -> float:
     return float(lib().orc_sts(ctypes.c_float(z), ctypes.c_float(T)))
+
+
+def sts_rows(z, T):
+    """(c [n, gamma] fp32, status): c = sigmoid(z / T_k) elementwise."""
+    z = _c(z, np.float32)
+    T = _c(T, np.float32)
+    n, g = z.shape
+    c = np.empty((n, g), np.float32)
+    st = np.zeros(1, np.int32)
+    lib().orc_sts_rows(_ptr(z, ctypes.c_float), _ptr(T, ctypes.c_float), n, g,
+                       _ptr(c, ctypes.c_float), _ptr(st, ctypes.c_int32))
+    return c, int(st[0])
 
 
 def survival(z, T, eps):

@@ -77,6 +77,20 @@ float orc_sts(float z, float T)
     return (float)c;
 }
 
+/* c[r][k] = orc_sts(z[r][k], T[k]) over [n, gamma]; NaN logits and
+ * temperatures that are not > 0 flag BAD_INPUT. */
+void orc_sts_rows(const float *z, const float *T, int64_t n, int gamma, float *c, int *status)
+{
+    for (int k = 0; k < gamma; ++k)
+        if (!(T[k] > 0.0f)) *status |= ORC_ST_BAD_INPUT;
+    for (int64_t i = 0; i < n; ++i)
+        for (int k = 0; k < gamma; ++k) {
+            float zk = z[(size_t)i * gamma + k];
+            if (zk != zk) *status |= ORC_ST_BAD_INPUT;
+            c[(size_t)i * gamma + k] = orc_sts(zk, T[k]);
+        }
+}
+
 /* Prefix survivals S_k = prod_{i<=k} c_i per request, in sequential order.
  * [AVS] §一 (same-request survival is a cumulative product) and §二 (S_k);
  * [TUT] "接受是一件前缀事件" (prefix survival table).

@@ -220,6 +220,14 @@ def test_sampling_argument_checks(lib):
 
 
 def test_calibration_argument_checks(lib):
+    conf = lib.dspark_sts_confidence
+    conf.restype = ctypes.c_int
+    assert conf(FAKE, None, ctypes.c_int64(4), 4, FAKE, FAKE, None) == -1
+    assert conf(FAKE, FAKE, ctypes.c_int64(-1), 4, FAKE, FAKE, None) == -1
+    assert conf(FAKE, FAKE, ctypes.c_int64(4), 0, FAKE, FAKE, None) == -1
+    assert conf(None, FAKE, ctypes.c_int64(4), 4, FAKE, FAKE, None) == -1
+    assert conf(None, FAKE, ctypes.c_int64(0), 4, None, FAKE, None) == 0  # nothing to do
+
     rec = lib.dspark_sts_record
     rec.restype = ctypes.c_int
 

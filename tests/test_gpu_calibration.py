@@ -294,3 +294,63 @@ def test_fit_full_size_sampled(orc, dev):
     grid = wl.temperature_grid(J)
     ref = orc.sts_fit(cs.conf_logits, cs.correct, cs.tested, grid, M)
     compare_fit("fit full", run_fit(dev, cs.conf_logits, cs.correct, cs.tested, grid, M), ref)
+
+
+# ------------------------------------------------------------- STS sigmoid
+
+def _sts_gpu(dev, z, T):
+    out = torch.empty(z.shape, dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    api.dspark_sts_confidence(_t(z, dev), sts_temps=_t(T, dev), conf_out=out, status=st)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), int(st.item())
+
+
+def _check_near_ties(t, got, ref):
+    """Elements where the GPU and the host differ must sit on an fp32
+    rounding midpoint to within a few fp64 ulps (CUDA's and the host's fp64
+    exp may differ in the last bit there); none is expected."""
+    bad = np.flatnonzero(got.view(np.uint32) != ref.view(np.uint32))
+    for i in bad[:16]:
+        v = 1.0 / (1.0 + np.exp(-np.float64(t[i])))
+        a, b = sorted((np.float64(got[i]), np.float64(ref[i])))
+        assert np.nextafter(np.float32(a), np.float32(2)) == np.float32(b), (t[i], got[i], ref[i])
+        mid = (a + b) / 2
+        assert abs(v - mid) <= 8 * np.spacing(v), (t[i], v, mid)
+        log_near_tie({"tag": "sts sweep", "t": float(t[i])})
+    return bad.size
+
+
+def test_sts_confidence_sweep(orc, dev):
+    """Every 64th fp32 value with |t| <= 70, both signs, T = 1: the fp32
+    evaluation (|t| <= 60) and the fp64 formula beyond it against the host."""
+    top = int(np.float32(70.0).view(np.uint32))
+    pos = np.arange(0, top + 1, 64, dtype=np.uint32).view(np.float32)
+    t = np.concatenate([pos, -pos]).reshape(-1, 1)
+    got, st = _sts_gpu(dev, t, np.ones(1, np.float32))
+    ref, st_ref = orc.sts_rows(t, np.ones(1, np.float32))
+    assert st == st_ref == 0
+    assert _check_near_ties(t.ravel(), got.ravel(), ref.ravel()) <= 2
+
+
+def test_sts_confidence_random_and_edges(orc, dev):
+    rng = np.random.default_rng(8)
+    z = np.concatenate([rng.normal(0, 3, 200000), rng.normal(0, 40, 50000),
+                        rng.uniform(-1e-30, 1e-30, 1000)]).astype(np.float32)
+    z[:8] = [np.inf, -np.inf, 0.0, -0.0, 3e38, -3e38, 1e-45, -1e-45]
+    gamma = 5
+    z = z[: (z.size // gamma) * gamma].reshape(-1, gamma)
+    T = np.array([1.0, 0.37, 2.5, 1e-3, 7.0], np.float32)
+    got, st = _sts_gpu(dev, z, T)
+    ref, st_ref = orc.sts_rows(z, T)
+    assert st == st_ref == 0
+    assert _check_near_ties((z / T).ravel(), got.ravel(), ref.ravel()) <= 1
+    # NaN logits and a zero temperature flag BAD_INPUT and propagate like the host
+    z[3, 1] = np.nan
+    T[4] = 0.0
+    got, st = _sts_gpu(dev, z, T)
+    ref, st_ref = orc.sts_rows(z, T)
+    assert st == st_ref == orc.ST_BAD_INPUT
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[ok], ref[ok])
