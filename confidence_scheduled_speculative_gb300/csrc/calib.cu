@@ -28,8 +28,10 @@
 // 2^-8 q is p * 2^32 itself, below it both are 0).  Bin counts, label counts
 // and confidence sums are integers added with integer atomics, so they and
 // ECE * n * 2^32 = sum_b |L_b 2^32 - C_b| do not depend on the order in which
-// the GPU adds them.  Brier and log-loss sums are fp64: per-thread terms,
-// warp trees, warps in order, CTAs in order.
+// the GPU adds them.  Brier and log-loss terms are float pairs (the square
+// exact to ~2^-47, -ln p to ~2^-43 absolute), summed as float pairs over a
+// warp tree and within a warp's slot, then in fp64 over warps and CTAs in
+// order: deterministic, within ~1e-13 of a sequential fp64 sum.
 //
 // Kernels
 //   sts_record_kernel  one CTA: block scans number the selected requests,
@@ -67,7 +69,7 @@
 
 namespace dspark {
 
-constexpr int kRecThreads = 1024;
+constexpr int kRecThreads = 512;
 constexpr int kStatsThreads = 256;
 constexpr int kStatsWarps = kStatsThreads / 32;
 constexpr int kStatsMaxCtas = 1024;
@@ -78,9 +80,62 @@ constexpr int kMaxTemps = 256;
 constexpr int kMaxGamma = 31;
 constexpr double kQ32 = 4294967296.0;
 
-// q = floor(p * 2^32) for p in [0, 1]
+// q = floor(p * 2^32) for p in [0, 1], from the bits of p: p = 1.f * 2^e
+// gives (1.f * 2^23) shifted by e + 9 (integer work only; float-to-integer
+// conversions run on the fp64 unit)
 __device__ __forceinline__ unsigned long long conf_q(float p) {
-    return __float2ull_rz(__fmul_rn(p, 4294967296.0f));
+    const unsigned bits = __float_as_uint(p);
+    const int sh = (int)(bits >> 23) - 127 + 9;  // e + 9; p in [0, 1] is never negative
+    const unsigned long long m = (unsigned long long)((bits & 0x007fffffu) | 0x00800000u);
+    if (sh >= 0) return m << sh;                  // e >= -9 (p = 1: 2^23 << 9)
+    return sh > -24 ? m >> (-sh) : 0ull;          // below 2^-32 (and +0, subnormals): 0
+}
+
+// --- float-pair terms of the Brier score and the log loss (no fp64 in the
+// per-sample work: GB300's fp64 unit is 1/64 of its fp32 rate)
+
+// (p - y)^2 as hi + lo (relative error ~2^-47)
+__device__ __forceinline__ void brier_pair(float p, bool y, float &hi, float &lo) {
+    float dh, dl;
+    two_sum(p, y ? -1.0f : 0.0f, dh, dl);
+    hi = __fmul_rn(dh, dh);
+    lo = fmaf(dh, dh, -hi);
+    lo = fmaf(__fmul_rn(2.0f, dh), dl, lo);
+}
+
+// -ln q for q = qh + ql in [2^-24, 1] (absolute error ~2^-43): a float
+// estimate y0 of ln q, then ln q = y0 + ln(1 + w) with w = q e^{-y0} - 1
+// (|w| < 2^-20, so w - w^2/2 leaves an error below 2^-60).
+__device__ __forceinline__ void neglog_pair(float qh, float ql, float &hi, float &lo) {
+    const float y0 = __logf(qh);
+    float eh, el;
+    exp_pair(-y0, eh, el);
+    const float ph = __fmul_rn(qh, eh);
+    float pl = fmaf(qh, eh, -ph);
+    pl = fmaf(qh, el, fmaf(ql, eh, pl));
+    const float w = __fadd_rn(__fsub_rn(ph, 1.0f), pl);  // ph - 1 is exact
+    const float l1 = __fsub_rn(w, __fmul_rn(__fmul_rn(0.5f, w), w));
+    two_sum(-y0, -l1, hi, lo);
+}
+
+// hi + lo summed over the warp (every lane gets the sum)
+__device__ __forceinline__ void warp_sum_pair(float &hi, float &lo) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float oh = __shfl_xor_sync(kFullMask, hi, o), ol = __shfl_xor_sync(kFullMask, lo, o);
+        float s, e;
+        two_sum(hi, oh, s, e);
+        e = __fadd_rn(e, __fadd_rn(lo, ol));
+        fast_two_sum(s, e, hi, lo);
+    }
+}
+
+// acc (a float pair in shared memory) += hi + lo
+__device__ __forceinline__ void add_pair(float *acc, float hi, float lo) {
+    float s, e;
+    two_sum(acc[0], hi, s, e);
+    e = __fadd_rn(e, __fadd_rn(acc[1], lo));
+    fast_two_sum(s, e, acc[0], acc[1]);
 }
 
 __device__ __forceinline__ int conf_bin(unsigned long long q, int M) {
@@ -143,63 +198,92 @@ __global__ void __launch_bounds__(kRecThreads) sts_record_kernel(RecordArgs a) {
     __shared__ int scan_tmp[33];
     __shared__ long long slot_s[kRecThreads];
     __shared__ int corr_s[kRecThreads];
+    __shared__ unsigned long long off_s, first_s;
+    __shared__ long long count_s;
     pdl_trigger();
     pdl_wait();  // num_correct / verify_lens come from the accept
-    const unsigned long long cur0 = *a.cursor;
-    int mine = 0;
-    for (int r = threadIdx.x; r < a.B; r += kRecThreads) mine += (!a.select || a.select[r]) ? 1 : 0;
-    const long long count = block_sum<int>(mine, scan_tmp);
-    // more rows than slots: only the last `capacity` selected rows are kept
-    const long long skip = count > a.capacity ? count - a.capacity : 0;
+    const int tid = threadIdx.x, G = a.gamma;
+    const unsigned long long cap = (unsigned long long)a.capacity;
+    // selected rows in all; a second pass over `select` only when the
+    // requests span more than one chunk
+    long long count = a.B;
+    if (a.select && a.B > kRecThreads) {
+        int mine = 0;
+        for (int r = tid; r < a.B; r += kRecThreads) mine += a.select[r] ? 1 : 0;
+        count = block_sum<int>(mine, scan_tmp);
+    }
     bool bad_len = false;
     long long base = 0;
     for (int r0 = 0; r0 < a.B; r0 += kRecThreads) {
-        const int r = r0 + (int)threadIdx.x;
-        int tested = a.gamma, c = 0;
+        const int rows = min(kRecThreads, a.B - r0);
+        const int nel = rows * G;
+        // every load of the chunk is issued before the scan
+        float zr[kMaxGamma];
+#pragma unroll
+        for (int i = 0; i < kMaxGamma; ++i) {
+            const int e = tid + i * kRecThreads;
+            if (i < G && e < nel) zr[i] = a.z[(size_t)r0 * G + e];
+        }
+        const int r = r0 + tid;
+        int tested = G, c = 0;
         bool sel = false;
         if (r < a.B) {
+            c = a.correct[r];
+            sel = !a.select || a.select[r];
             if (a.verify_lens) {
                 int L = a.verify_lens[r];
-                if (L < 1 || L > a.gamma + 1) {
+                if (L < 1 || L > G + 1) {
                     bad_len = true;
-                    L = L < 1 ? 1 : a.gamma + 1;
+                    L = L < 1 ? 1 : G + 1;
                 }
                 tested = L - 1;
             }
-            c = a.correct[r];
             if (c < 0 || c > tested) {
                 bad_len = true;
                 c = c < 0 ? 0 : tested;
             }
-            sel = !a.select || a.select[r];
         }
         int tot;
         const int pre = block_exclusive_scan<int>(sel ? 1 : 0, scan_tmp, &tot);
-        const long long i = base + pre;
+        if (r0 == 0 && tid == 0) {
+            const long long n = (a.select && a.B <= kRecThreads) ? tot : count;
+            // more rows than slots: only the last `capacity` are written
+            const unsigned long long skip =
+                n > a.capacity ? (unsigned long long)(n - a.capacity) : 0ull;
+            count_s = n;
+            first_s = skip;
+            off_s = (*a.cursor % cap + skip % cap) % cap;  // slot of row `skip`
+        }
+        __syncthreads();
+        count = count_s;
+        const unsigned long long first = first_s;
+        const unsigned long long i = (unsigned long long)(base + pre);
         long long slot = -1;
-        if (sel && i >= skip)
-            slot = (long long)((cur0 + (unsigned long long)i) % (unsigned long long)a.capacity);
-        if (slot >= 0) {
+        if (sel && i >= first) {
+            unsigned long long s = off_s + (i - first);  // i - first < capacity
+            slot = (long long)(s >= cap ? s - cap : s);
             a.rec_correct[slot] = c;
             a.rec_tested[slot] = tested;
         }
-        slot_s[threadIdx.x] = slot;
-        corr_s[threadIdx.x] = c;
+        slot_s[tid] = slot;
+        corr_s[tid] = c;
         __syncthreads();
-        const int rows = min(kRecThreads, a.B - r0);
-        for (int e = threadIdx.x; e < rows * a.gamma; e += kRecThreads) {
-            const int rr = e / a.gamma, k = e - rr * a.gamma;
-            const size_t src = (size_t)(r0 + rr) * a.gamma + k;
-            const long long s = slot_s[rr];
-            if (s >= 0) a.rec_z[(size_t)s * a.gamma + k] = a.z[src];
-            if (a.mask) a.mask[src] = (uint8_t)(k < corr_s[rr]);
+#pragma unroll
+        for (int i2 = 0; i2 < kMaxGamma; ++i2) {
+            const int e = tid + i2 * kRecThreads;
+            if (i2 < G && e < nel) {
+                const int rr = e / G, k = e - rr * G;
+                const long long sl = slot_s[rr];
+                if (sl >= 0) a.rec_z[(size_t)sl * G + k] = zr[i2];
+                if (a.mask) a.mask[(size_t)r0 * G + e] = (uint8_t)(k < corr_s[rr]);
+            }
         }
         __syncthreads();
         base += tot;
     }
-    if (__syncthreads_or(bad_len) && threadIdx.x == 0) flag(a.status, DSPARK_STATUS_BAD_LEN);
-    if (threadIdx.x == 0) {
-        *a.cursor = cur0 + (unsigned long long)count;
+    if (__syncthreads_or(bad_len) && tid == 0) flag(a.status, DSPARK_STATUS_BAD_LEN);
+    if (tid == 0) {
+        *a.cursor += (unsigned long long)count;
         if (count > a.capacity) flag(a.status, DSPARK_STATUS_CAPACITY);
     }
 }
@@ -238,32 +322,25 @@ struct StatsArgs {
     int32_t *status;
 };
 
-// Sum over the warp; every lane gets a value, lane 0's is the one used.
-__device__ __forceinline__ double warp_sum_f64(double v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);
-    return v;
-}
-
 // Add one (prediction, label) per lane, where `inc`, to flavour f, depth k:
 // lanes that share a bin are combined (ballot counts, redux sums of the two
 // 16-bit halves of q) and one of them adds to the CTA histogram; the Brier
 // and log-loss terms go to the warp's own slots.
-__device__ __forceinline__ void stats_add(unsigned long long *hs, double *wsum, int f, int k,
+__device__ __forceinline__ void stats_add(unsigned long long *hs, float *wsum, int f, int k,
                                           float p, bool y, bool inc, int lane, int G, int M) {
     const unsigned any = __ballot_sync(kFullMask, inc);
     if (!any) return;
     unsigned long long q = 0;
     int b = -1;
-    double br = 0.0, ll = 0.0;
+    float bh = 0.0f, bl = 0.0f, lh = 0.0f, ll = 0.0f;
     if (inc) {
         q = conf_q(p);
         b = conf_bin(q, M);
-        const double pd = (double)p;
-        const double d = __dsub_rn(pd, y ? 1.0 : 0.0);
-        br = __dmul_rn(d, d);
-        const double pc = fmin(fmax(pd, 0x1p-24), 1.0 - 0x1p-24);
-        ll = y ? -log(pc) : -log(__dsub_rn(1.0, pc));
+        brier_pair(p, y, bh, bl);
+        const float pc = fminf(fmaxf(p, 0x1p-24f), 1.0f - 0x1p-24f);
+        float qh = pc, ql = 0.0f;
+        if (!y) two_sum(1.0f, -pc, qh, ql);  // 1 - pc exactly
+        neglog_pair(qh, ql, lh, ll);
     }
     unsigned pending = any;
     while (pending) {
@@ -282,17 +359,17 @@ __device__ __forceinline__ void stats_add(unsigned long long *hs, double *wsum, 
         }
         pending &= ~m;
     }
-    br = warp_sum_f64(br);
-    ll = warp_sum_f64(ll);
+    warp_sum_pair(bh, bl);
+    warp_sum_pair(lh, ll);
     if (lane == 0) {
-        wsum[(f * kMaxGamma + k) * 2] += br;
-        wsum[(f * kMaxGamma + k) * 2 + 1] += ll;
+        add_pair(wsum + (f * kMaxGamma + k) * 4, bh, bl);
+        add_pair(wsum + (f * kMaxGamma + k) * 4 + 2, lh, ll);
     }
 }
 
 __global__ void __launch_bounds__(kStatsThreads) calib_stats_kernel(StatsArgs a) {
     extern __shared__ __align__(16) unsigned long long hs[];  // [2][gamma][M][3]
-    __shared__ double wsum[kStatsWarps][2 * kMaxGamma * 2];
+    __shared__ float wsum[kStatsWarps][2 * kMaxGamma * 4];  // float pairs
     __shared__ float T_s[kMaxGamma];
     __shared__ bool last_s;
     pdl_trigger();
@@ -300,8 +377,8 @@ __global__ void __launch_bounds__(kStatsThreads) calib_stats_kernel(StatsArgs a)
     const int G = a.gamma, M = a.M;
     const int HN = 2 * G * M * 3;
     for (int i = threadIdx.x; i < HN; i += kStatsThreads) hs[i] = 0;
-    for (int i = threadIdx.x; i < kStatsWarps * 2 * kMaxGamma * 2; i += kStatsThreads)
-        (&wsum[0][0])[i] = 0.0;
+    for (int i = threadIdx.x; i < kStatsWarps * 2 * kMaxGamma * 4; i += kStatsThreads)
+        (&wsum[0][0])[i] = 0.0f;
     pdl_wait();
     if (threadIdx.x < G) T_s[threadIdx.x] = a.T[threadIdx.x];
     __syncthreads();
@@ -338,7 +415,10 @@ __global__ void __launch_bounds__(kStatsThreads) calib_stats_kernel(StatsArgs a)
     for (int i = threadIdx.x; i < 4 * G; i += kStatsThreads) {
         const int f = i / (2 * G), k = (i >> 1) % G, s = i & 1;
         double v = 0.0;
-        for (int w = 0; w < kStatsWarps; ++w) v += wsum[w][(f * kMaxGamma + k) * 2 + s];
+        for (int w = 0; w < kStatsWarps; ++w) {
+            const float *pr = &wsum[w][(f * kMaxGamma + k) * 4 + 2 * s];
+            v += (double)pr[0] + (double)pr[1];
+        }
         a.part_ws[(size_t)blockIdx.x * (4 * G) + i] = v;
     }
     __threadfence();
@@ -397,20 +477,20 @@ struct FitArgs {
 __global__ void __launch_bounds__(kFitThreads) sts_fit_kernel(const __grid_constant__ FitArgs a) {
     extern __shared__ __align__(16) unsigned char fsm[];
     __shared__ float z_s[kFitTile], sp_s[kFitTile];
-    __shared__ unsigned char fl_s[kFitTile];  // bit 0: counts at this depth, bit 1: label
+    __shared__ unsigned char y_s[kFitTile];  // labels of the compacted samples
+    __shared__ int scan_tmp[33];
     __shared__ unsigned long long e_s[kMaxTemps];
     __shared__ bool last_s;
     const int M = a.M, J = a.J, P = a.P, k = a.k, G = a.gamma;
-    // private bins, [bin][thread]: confidence sums, counts, label counts
+    // private bins, [bin][thread]: confidence sums, and count + (label
+    // count << 32) in one word
     unsigned long long *bconf = reinterpret_cast<unsigned long long *>(fsm);
-    unsigned int *bcnt = reinterpret_cast<unsigned int *>(bconf + (size_t)M * kFitThreads);
-    unsigned int *blab = bcnt + (size_t)M * kFitThreads;
+    unsigned long long *bcl = bconf + (size_t)M * kFitThreads;
     pdl_trigger();
     const int tid = threadIdx.x;
     for (int i = tid; i < M * kFitThreads; i += kFitThreads) {
         bconf[i] = 0;
-        bcnt[i] = 0;
-        blab[i] = 0;
+        bcl[i] = 0;
     }
     const int j = tid % J, ph = tid / J;
     const bool worker = ph < P;
@@ -445,22 +525,40 @@ __global__ void __launch_bounds__(kFitThreads) sts_fit_kernel(const __grid_const
             }
             if (k < cor) fl |= 2;
         }
-        z_s[tid] = zk;
-        sp_s[tid] = sp;
-        fl_s[tid] = fl;
+        // the samples that count, packed to the front of the tile
+        int n_in;
+        const int pos = block_exclusive_scan<int>(fl & 1, scan_tmp, &n_in);
+        if (fl & 1) {
+            z_s[pos] = zk;
+            sp_s[pos] = sp;
+            y_s[pos] = fl >> 1;
+        }
         __syncthreads();
         if (worker) {
-            for (int s = ph; s < kFitTile; s += P) {
-                const unsigned f = fl_s[s];
-                if (!(f & 1u)) continue;
-                const float c = sts_confidence(z_s[s], Tj);
+            // bins private to this thread; four samples at a time so that
+            // their dependent float-pair chains interleave
+            auto add = [&](int s, float c) {
                 const float p = (k == 0) ? c : __fmul_rn(sp_s[s], c);
                 const unsigned long long q = conf_q(p);
                 const int idx = conf_bin(q, M) * kFitThreads + tid;
-                bcnt[idx] += 1u;
-                blab[idx] += f >> 1;
+                bcl[idx] += 1ull + ((unsigned long long)y_s[s] << 32);
                 bconf[idx] += q;
+            };
+            int s = ph;
+            for (; s + 3 * P < n_in; s += 4 * P) {
+                float t[4], c[4];
+                bool ok[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) t[u] = __fdiv_rn(z_s[s + u * P], Tj);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) ok[u] = sigmoid_f32(t[u], c[u]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (!ok[u]) c[u] = sigmoid_f64(t[u]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) add(s + u * P, c[u]);
             }
+            for (; s < n_in; s += P) add(s, sts_confidence(z_s[s], Tj));
         }
         __syncthreads();
     }
@@ -472,8 +570,8 @@ __global__ void __launch_bounds__(kFitThreads) sts_fit_kernel(const __grid_const
         unsigned long long cnt = 0, lab = 0, conf = 0;
         for (int q = 0; q < P; ++q) {
             const int idx = b * kFitThreads + q * J + jj;
-            cnt += bcnt[idx];
-            lab += blab[idx];
+            cnt += bcl[idx] & 0xffffffffull;
+            lab += bcl[idx] >> 32;
             conf += bconf[idx];
         }
         if (cnt) {

@@ -423,8 +423,10 @@ DSPARK_API int dspark_greedy_accept_static(const void *logits, int32_t dtype, in
  *     (n 2^32) is exact up to its final rounding (within 2^-32 of the
  *     real-number ECE);
  *   - Brier = mean (p - y)^2 and log loss = mean -[y ln p + (1-y) ln(1-p)]
- *     with p clamped to [2^-24, 1 - 2^-24], summed in fp64 (deterministic
- *     for a given GPU; the order differs from a sequential sum);
+ *     with p clamped to [2^-24, 1 - 2^-24]; each term is evaluated as a pair
+ *     of floats (Brier to ~2^-47 relative, the log term to ~2^-43 absolute)
+ *     and the sums end in fp64 (deterministic for a given GPU; within ~1e-13
+ *     of a sequential fp64 sum);
  *   - a flavour/depth with no sample reports n = 0 and zeros. */
 
 /* STS-calibrated confidences c[r][k] = sigmoid(conf_logits[r][k] /
