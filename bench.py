@@ -90,7 +90,8 @@ def ncu_traffic(workload: str):
     if not d:
         return None
     h = hashlib.sha256()
-    for rel in ("csrc/accept.cu", "csrc/logits.cuh", "csrc/dspark_common.cuh"):
+    for rel in ("csrc/accept.cu", "csrc/logits.cuh", "csrc/dspark_common.cuh",
+                "csrc/sigmoid.cuh"):
         with open(os.path.join(ROOT, "confidence_scheduled_speculative_gb300", rel), "rb") as f:
             h.update(f.read())
     return d["bytes_per_launch"] if h.hexdigest() == d.get("sources_sha256") else None

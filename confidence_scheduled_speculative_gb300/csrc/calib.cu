@@ -78,6 +78,7 @@ constexpr int kFitTile = 256;  // samples staged per step
 constexpr int kMaxBins = 32;
 constexpr int kMaxTemps = 256;
 constexpr int kMaxGamma = 31;
+constexpr long long kMaxSamples = 0x7fffffffLL;  // bin counters of a CTA or thread are 32-bit
 constexpr double kQ32 = 4294967296.0;
 
 // q = floor(p * 2^32) for p in [0, 1], from the bits of p: p = 1.f * 2^e
@@ -128,6 +129,14 @@ __device__ __forceinline__ void warp_sum_pair(float &hi, float &lo) {
         e = __fadd_rn(e, __fadd_rn(lo, ol));
         fast_two_sum(s, e, hi, lo);
     }
+}
+
+// (ah, al) += hi + lo, all float pairs
+__device__ __forceinline__ void acc_pair(float &ah, float &al, float hi, float lo) {
+    float s, e;
+    two_sum(ah, hi, s, e);
+    e = __fadd_rn(e, __fadd_rn(al, lo));
+    fast_two_sum(s, e, ah, al);
 }
 
 // acc (a float pair in shared memory) += hi + lo
@@ -322,61 +331,38 @@ struct StatsArgs {
     int32_t *status;
 };
 
-// Add one (prediction, label) per lane, where `inc`, to flavour f, depth k:
-// lanes that share a bin are combined (ballot counts, redux sums of the two
-// 16-bit halves of q) and one of them adds to the CTA histogram; the Brier
-// and log-loss terms go to the warp's own slots.
-__device__ __forceinline__ void stats_add(unsigned long long *hs, float *wsum, int f, int k,
-                                          float p, bool y, bool inc, int lane, int G, int M) {
-    const unsigned any = __ballot_sync(kFullMask, inc);
-    if (!any) return;
-    unsigned long long q = 0;
-    int b = -1;
-    float bh = 0.0f, bl = 0.0f, lh = 0.0f, ll = 0.0f;
-    if (inc) {
-        q = conf_q(p);
-        b = conf_bin(q, M);
-        brier_pair(p, y, bh, bl);
-        const float pc = fminf(fmaxf(p, 0x1p-24f), 1.0f - 0x1p-24f);
-        float qh = pc, ql = 0.0f;
-        if (!y) two_sum(1.0f, -pc, qh, ql);  // 1 - pc exactly
-        neglog_pair(qh, ql, lh, ll);
-    }
-    unsigned pending = any;
-    while (pending) {
-        const int leader = __ffs(pending) - 1;
-        const int b0 = __shfl_sync(kFullMask, b, leader);
-        const bool mine = inc && b == b0;
-        const unsigned m = __ballot_sync(kFullMask, mine);
-        const unsigned ym = __ballot_sync(kFullMask, mine && y);
-        const unsigned hi = __reduce_add_sync(kFullMask, mine ? (unsigned)(q >> 16) : 0u);
-        const unsigned lo = __reduce_add_sync(kFullMask, mine ? (unsigned)(q & 0xffffu) : 0u);
-        if (lane == leader) {
-            unsigned long long *h = hs + ((size_t)(f * G + k) * M + b0) * 3;
-            atomicAdd(h, (unsigned long long)__popc(m));
-            atomicAdd(h + 1, (unsigned long long)__popc(ym));
-            atomicAdd(h + 2, ((unsigned long long)hi << 16) + lo);
-        }
-        pending &= ~m;
-    }
-    warp_sum_pair(bh, bl);
-    warp_sum_pair(lh, ll);
-    if (lane == 0) {
-        add_pair(wsum + (f * kMaxGamma + k) * 4, bh, bl);
-        add_pair(wsum + (f * kMaxGamma + k) * 4 + 2, lh, ll);
-    }
+// One (prediction, label) of flavour f at depth k: the bin of the CTA's
+// histogram gets count + (label << 32) and floor(p 2^32) by shared atomics;
+// the Brier and log-loss terms add to the thread's float pairs acc[0..3].
+__device__ __forceinline__ void stats_add(unsigned long long *hs, float *acc, int f, int k,
+                                          float p, bool y, int G, int M) {
+    const unsigned long long q = conf_q(p);
+    unsigned long long *h = hs + ((size_t)(f * G + k) * M + conf_bin(q, M)) * 2;
+    atomicAdd(h, 1ull + ((unsigned long long)y << 32));
+    atomicAdd(h + 1, q);
+    float th, tl;
+    brier_pair(p, y, th, tl);
+    acc_pair(acc[0], acc[1], th, tl);
+    const float pc = fminf(fmaxf(p, 0x1p-24f), 1.0f - 0x1p-24f);
+    float qh = pc, ql = 0.0f;
+    if (!y) two_sum(1.0f, -pc, qh, ql);  // 1 - pc exactly
+    neglog_pair(qh, ql, th, tl);
+    acc_pair(acc[2], acc[3], th, tl);
 }
 
+constexpr int kStatsR = 2;  // samples per thread held across the depth loop
+
 __global__ void __launch_bounds__(kStatsThreads) calib_stats_kernel(StatsArgs a) {
-    extern __shared__ __align__(16) unsigned long long hs[];  // [2][gamma][M][3]
+    // [2][gamma][M][2]: count + (label count << 32), confidence sum
+    extern __shared__ __align__(16) unsigned long long hs[];
     __shared__ float wsum[kStatsWarps][2 * kMaxGamma * 4];  // float pairs
     __shared__ float T_s[kMaxGamma];
     __shared__ bool last_s;
     pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int G = a.gamma, M = a.M;
-    const int HN = 2 * G * M * 3;
-    for (int i = threadIdx.x; i < HN; i += kStatsThreads) hs[i] = 0;
+    const int HS = 2 * G * M * 2;
+    for (int i = threadIdx.x; i < HS; i += kStatsThreads) hs[i] = 0;
     for (int i = threadIdx.x; i < kStatsWarps * 2 * kMaxGamma * 4; i += kStatsThreads)
         (&wsum[0][0])[i] = 0.0f;
     pdl_wait();
@@ -384,32 +370,60 @@ __global__ void __launch_bounds__(kStatsThreads) calib_stats_kernel(StatsArgs a)
     __syncthreads();
     bool bad_in = blockIdx.x == 0 && threadIdx.x < G && !(T_s[threadIdx.x] > 0.0f);
     bool bad_len = false;
-    const long long stride = (long long)gridDim.x * kStatsThreads;
-    for (long long base = (long long)blockIdx.x * kStatsThreads; base < a.N; base += stride) {
-        const long long n = base + threadIdx.x;
-        const bool act = n < a.N;
-        int cor = 0, tst = 0;
-        if (act) bad_len |= sample_lens(a.correct[n], a.tested[n], G, cor, tst);
-        float S = 1.0f;
+    const long long per_pass = (long long)kStatsThreads * kStatsR;
+    for (long long base = (long long)blockIdx.x * per_pass; base < a.N;
+         base += (long long)gridDim.x * per_pass) {
+        // this thread's samples, kept in registers over the depths
+        int cor[kStatsR], tst[kStatsR];
+        float S[kStatsR];
+#pragma unroll
+        for (int r = 0; r < kStatsR; ++r) {
+            const long long n = base + r * kStatsThreads + threadIdx.x;
+            cor[r] = tst[r] = 0;  // tested 0: never observed
+            S[r] = 1.0f;
+            if (n < a.N) bad_len |= sample_lens(a.correct[n], a.tested[n], G, cor[r], tst[r]);
+        }
         for (int k = 0; k < G; ++k) {
-            const float zk = act ? a.z[n * G + k] : 0.0f;
-            if (zk != zk) bad_in = true;
-            const bool obs = act && k < tst;  // the window reached depth k
-            float c = 0.0f;
-            if (obs) {
-                c = sts_confidence(zk, T_s[k]);
-                S = (k == 0) ? c : __fmul_rn(S, c);
+            float acc[8];  // per flavour: Brier pair, log-loss pair
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+            bool any = false;
+#pragma unroll
+            for (int r = 0; r < kStatsR; ++r) {
+                const long long n = base + r * kStatsThreads + threadIdx.x;
+                const float zk = n < a.N ? a.z[n * G + k] : 0.0f;
+                if (zk != zk) bad_in = true;
+                if (k >= tst[r]) continue;  // the window did not reach depth k
+                const float c = sts_confidence(zk, T_s[k]);
+                S[r] = (k == 0) ? c : __fmul_rn(S[r], c);
+                const bool y = k < cor[r];
+                if (S[r] == S[r]) stats_add(hs, acc, 0, k, S[r], y, G, M);
+                if (cor[r] >= k && c == c) stats_add(hs, acc + 4, 1, k, c, y, G, M);
+                any = true;
             }
-            const bool y = k < cor;
-            stats_add(hs, wsum[warp], 0, k, S, y, obs && S == S, lane, G, M);
-            stats_add(hs, wsum[warp], 1, k, c, y, obs && cor >= k && c == c, lane, G, M);
+            if (__any_sync(kFullMask, any)) {
+#pragma unroll
+                for (int i = 0; i < 8; i += 2) warp_sum_pair(acc[i], acc[i + 1]);
+                if (lane == 0) {
+                    float *w = wsum[warp];
+                    add_pair(w + k * 4, acc[0], acc[1]);
+                    add_pair(w + k * 4 + 2, acc[2], acc[3]);
+                    add_pair(w + (kMaxGamma + k) * 4, acc[4], acc[5]);
+                    add_pair(w + (kMaxGamma + k) * 4 + 2, acc[6], acc[7]);
+                }
+            }
         }
     }
     if (__syncthreads_or(bad_in) && threadIdx.x == 0) flag(a.status, DSPARK_STATUS_BAD_INPUT);
     if (__syncthreads_or(bad_len) && threadIdx.x == 0) flag(a.status, DSPARK_STATUS_BAD_LEN);
-    for (int i = threadIdx.x; i < HN; i += kStatsThreads) {
-        const unsigned long long v = hs[i];
-        if (v) atomicAdd(a.hist_ws + i, v);
+    // to the global [2][gamma][M][3] histogram: count, label count, confidence sum
+    for (int i = threadIdx.x; i < 2 * G * M; i += kStatsThreads) {
+        const unsigned long long cl = hs[2 * i], conf = hs[2 * i + 1];
+        if (cl) {
+            atomicAdd(a.hist_ws + 3 * i, cl & 0xffffffffull);
+            atomicAdd(a.hist_ws + 3 * i + 1, cl >> 32);
+            atomicAdd(a.hist_ws + 3 * i + 2, conf);
+        }
     }
     // this CTA's Brier / log-loss sums, warps in order; slot (f*G + k)*2 + s
     for (int i = threadIdx.x; i < 4 * G; i += kStatsThreads) {
@@ -442,6 +456,7 @@ __global__ void __launch_bounds__(kStatsThreads) calib_stats_kernel(StatsArgs a)
         m[3] = n ? __ddiv_rn(ll, (double)n) : 0.0;
     }
     __syncthreads();
+    const int HN = 2 * G * M * 3;
     for (int i = threadIdx.x; i < HN; i += kStatsThreads) {
         const unsigned long long v = __ldcg(a.hist_ws + i);
         if (a.hist_out) a.hist_out[i] = v;
@@ -680,7 +695,8 @@ extern "C" int dspark_calibration_stats(const float *rec_logits, const int32_t *
                                         size_t workspace_bytes, int32_t *status, void *stream) {
     if (!sts_temps || !metrics || !status) return DSPARK_ERR_INVALID_ARG;
     if (N > 0 && (!rec_logits || !rec_correct || !rec_tested)) return DSPARK_ERR_INVALID_ARG;
-    if (N < 0 || gamma < 1 || gamma > kMaxGamma || n_bins < 1 || n_bins > kMaxBins)
+    if (N < 0 || N > kMaxSamples || gamma < 1 || gamma > kMaxGamma || n_bins < 1 ||
+        n_bins > kMaxBins)
         return DSPARK_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < dspark_calibration_workspace_bytes(gamma, n_bins) ||
         !aligned(workspace, 256))
@@ -700,14 +716,14 @@ extern "C" int dspark_calibration_stats(const float *rec_logits, const int32_t *
     a.hist_out = reinterpret_cast<unsigned long long *>(hist);
     a.metrics = metrics;
     a.status = status;
-    const int smem = 2 * gamma * n_bins * 3 * 8;
+    const int smem = 2 * gamma * n_bins * 2 * 8;
     cudaError_t e = ensure_smem(reinterpret_cast<const void *>(calib_stats_kernel), smem, 7);
     if (e != cudaSuccess) return DSPARK_ERR_CUDA;
     int occ = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, calib_stats_kernel, kStatsThreads,
                                                       (size_t)smem);
     if (e != cudaSuccess) return DSPARK_ERR_CUDA;
-    const long long tiles = (N + kStatsThreads - 1) / kStatsThreads;
+    const long long tiles = (N + kStatsThreads * kStatsR - 1) / (kStatsThreads * kStatsR);
     long long g = (long long)sm_count() * (occ > 0 ? occ : 1);
     g = g < tiles ? g : tiles;
     g = g < kStatsMaxCtas ? g : kStatsMaxCtas;
@@ -718,7 +734,7 @@ extern "C" int dspark_calibration_stats(const float *rec_logits, const int32_t *
 }
 
 extern "C" size_t dspark_sts_fit_workspace_bytes(int64_t N, int32_t n_temps, int32_t n_bins) {
-    if (N < 0 || n_temps < 1 || n_temps > kMaxTemps || n_bins < 1 || n_bins > kMaxBins) return 0;
+    if (N < 0 || N > kMaxSamples || n_temps < 1 || n_temps > kMaxTemps || n_bins < 1 || n_bins > kMaxBins) return 0;
     return align256(sizeof(FitState)) + fit_hist_bytes(n_temps, n_bins) +
            align256((size_t)N * sizeof(float));
 }
@@ -731,8 +747,8 @@ extern "C" int dspark_sts_fit(const float *rec_logits, const int32_t *rec_correc
                               int32_t *status, void *stream) {
     if (!temp_grid || !sts_temps_out || !choice || !status) return DSPARK_ERR_INVALID_ARG;
     if (N > 0 && (!rec_logits || !rec_correct || !rec_tested)) return DSPARK_ERR_INVALID_ARG;
-    if (N < 0 || gamma < 1 || gamma > kMaxGamma || n_temps < 1 || n_temps > kMaxTemps ||
-        n_bins < 1 || n_bins > kMaxBins)
+    if (N < 0 || N > kMaxSamples || gamma < 1 || gamma > kMaxGamma || n_temps < 1 ||
+        n_temps > kMaxTemps || n_bins < 1 || n_bins > kMaxBins)
         return DSPARK_ERR_INVALID_ARG;
     for (int i = 0; i < n_temps; ++i)  // the grid is host memory
         if (!(temp_grid[i] > 0.0f) || !(temp_grid[i] < INFINITY)) return DSPARK_ERR_INVALID_ARG;

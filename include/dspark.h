@@ -482,8 +482,8 @@ DSPARK_API size_t dspark_calibration_workspace_bytes(int32_t gamma, int32_t n_bi
  *              units (a reliability diagram)
  *   metrics    out [2][gamma][4] fp64: n, ECE, Brier, log loss
  * Device flags: BAD_INPUT (NaN logit anywhere, temperature not > 0),
- * BAD_LEN.  Errors: INVALID_ARG (null required pointer, N < 0, gamma outside
- * 1..31, n_bins outside 1..32); WORKSPACE; CUDA. */
+ * BAD_LEN.  Errors: INVALID_ARG (null required pointer, N outside
+ * 0..2^31-1, gamma outside 1..31, n_bins outside 1..32); WORKSPACE; CUDA. */
 DSPARK_API int dspark_calibration_stats(const float *rec_logits, const int32_t *rec_correct,
                                         const int32_t *rec_tested, int64_t N, int32_t gamma,
                                         const float *sts_temps, int32_t n_bins, uint64_t *hist,
@@ -509,7 +509,7 @@ DSPARK_API size_t dspark_sts_fit_workspace_bytes(int64_t N, int32_t n_temps, int
  *   n_obs         out [gamma] int64 (nullable): samples observed per depth
  * gamma launches (one per depth), N * n_temps fp32-rounded fp64 sigmoids
  * each.  Device flags: BAD_INPUT (NaN logit), BAD_LEN.  Errors: INVALID_ARG
- * (null required pointer, N < 0, gamma outside 1..31, n_temps outside
+ * (null required pointer, N outside 0..2^31-1, gamma outside 1..31, n_temps outside
  * 1..256, a grid value not positive and finite, n_bins outside 1..32);
  * WORKSPACE; CUDA. */
 DSPARK_API int dspark_sts_fit(const float *rec_logits, const int32_t *rec_correct,
