@@ -34,6 +34,7 @@ STATUS_INFEASIBLE = 64
 
 COST_SPS_1D = 0
 COST_ADDITIVE = 1
+COST_ADDITIVE_INTERP = 2
 DTYPE_BF16 = 0
 DTYPE_F32 = 1
 MAX_TIERS = 64

@@ -43,6 +43,7 @@ import numpy as np
 # cost-table kinds, matching the C-ABI's dspark_cost_table.kind
 COST_SPS_1D = 0
 COST_ADDITIVE = 1
+COST_ADDITIVE_INTERP = 2
 
 _ROW_TAG = 0x5EED_0001
 _STEP_TAG = 0x5EED_0002
@@ -343,7 +344,7 @@ def describe(w: Workload) -> str:
 
 __all__ = [
     "Workload", "CostTable", "StepInputs", "WORKLOADS", "TINY", "QWEN", "DSV4", "MIXED", "STRESS",
-    "COST_SPS_1D", "COST_ADDITIVE", "make_step", "cost_table_for", "target_rows", "strided_logits",
+    "COST_SPS_1D", "COST_ADDITIVE", "COST_ADDITIVE_INTERP", "make_step", "cost_table_for", "target_rows", "strided_logits",
     "to_bf16_bits", "bf16_bits_to_f32", "strided_row_index", "pages_example_confidences",
     "confidence_logits_for", "seeds", "approx_bytes", "describe", "PEAK",
     "CalibrationSamples", "calibration_samples", "temperature_grid",

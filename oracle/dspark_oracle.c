@@ -45,6 +45,9 @@
  *      value, -0 equal to +0; a row with no value above -inf returns 0.
  *   R8 out_tokens[r][gamma] is -1 before the bonus scatter; pad rows carry
  *      id 0, position 0, request -1, source -1.
+ *   R29 the interpolated additive table (kind 2): theta(M) linear between
+ *      samples in the fp64 order val_j + (M - M_j) * slope_j; val_0 below
+ *      the first sample; budgets above the last sample are infeasible.
  *
  * Parity pins: every function below is pinned in the oracle's CPU tests
  * against the pages' worked examples, closed forms or brute force.
@@ -136,6 +139,12 @@ static int orc_cand_cmp(const void *a, const void *b)
  * additive table theta = tau(b) / T(B, B+b).  [AVS] §四 "1D SpsCostTable"
  * (floor lookup, no interpolation) and "Additive SPS" (T = bias + alpha(B) +
  * theta(M)); [TUT] "调度器要比较期望收益与边际成本" (M = bs + K).
+ * kind 1 looks theta(M) up at the smallest graph tier >= M; kind 2 is the
+ * exported additive table's runtime linear interpolation of theta(M)
+ * ([AVS] §四 "三个关键假设", the third): with M_j <= M < M_{j+1},
+ * theta(M) = val_j + (M - M_j) * slope_j, slope_j = (val_{j+1} - val_j) /
+ * (M_{j+1} - M_j), in that fp64 order; val_j itself at M = M_j; val_0 below
+ * M_0 and infeasible above the last sample (reading R29).
  * Returns 1 if b is feasible and writes theta; sets *bad when the entry used
  * holds an invalid value (reading R4). */
 static int orc_theta(double tau, int B, int b, int kind, int n, const int32_t *M,
@@ -151,12 +160,32 @@ static int orc_theta(double tau, int B, int b, int kind, int n, const int32_t *M
         if (!(sps > 0.0) || !isfinite(sps)) { *bad = 1; return 0; }
         *theta = tau * sps;
         return 1;
-    } else {
+    } else if (kind == 1) {
         int j = -1;
         for (int i = 0; i < n; ++i)
             if (M[i] >= Mv) { j = i; break; }
         if (j < 0) return 0;                       /* above the largest tier */
         double T = (bias + alpha) + val[j];
+        if (!(T > 0.0) || !isfinite(T)) { *bad = 1; return 0; }
+        *theta = tau / T;
+        return 1;
+    } else {
+        if (Mv > M[n - 1]) return 0;               /* above the last sample */
+        double th;
+        if (Mv <= M[0]) {
+            th = val[0];
+        } else {
+            int j = 0;                             /* last sample with M_j <= Mv */
+            for (int i = 0; i < n; ++i)
+                if (M[i] <= Mv) j = i;
+            if (M[j] == Mv) {
+                th = val[j];
+            } else {
+                double slope = (val[j + 1] - val[j]) / (double)(M[j + 1] - M[j]);
+                th = val[j] + (double)(Mv - M[j]) * slope;
+            }
+        }
+        double T = (bias + alpha) + th;
         if (!(T > 0.0) || !isfinite(T)) { *bad = 1; return 0; }
         *theta = tau / T;
         return 1;
@@ -223,7 +252,7 @@ int orc_plan_from_survivals(const float *s_raw, int B, int gamma, float eps, int
         if (budget < 0) { budget = 0; *status |= ORC_ST_INFEASIBLE; }
     } else {
         long b_hi = N;
-        if (kind == 1 && n >= 1) {
+        if (kind != 0 && n >= 1) {
             long top = (long)M[n - 1] - B;
             if (top < b_hi) b_hi = top;
         }

@@ -207,6 +207,47 @@ def test_cost_lookup_additive_ceil_tier(orc):
     assert f.budget == 3 and list(f.verify_lens) == [3, 2]
 
 
+def test_cost_lookup_additive_interpolated(orc):
+    """The additive table's runtime linear interpolation of theta(M): one
+    request, survivals 0.875 0.5 0.25 0.0625 (tau 1, 1.875, 2.375, 2.625,
+    2.6875), samples theta(1) = 0, theta(5) = 0.5 ms, bias + alpha = 1 ms:
+    T(b) = 1 + b/8, so theta = 1, 1.667, 1.9, 1.909, 1.792 -> budget 3.
+    The ceil-to-tier lookup of the same table gives T = 1, 1.5, 1.5, 1.5,
+    1.5 -> budget 4: the two modes differ only between samples."""
+    s = _f32([[0.875, 0.5, 0.25, 0.0625]])
+    r = orc.plan_from_survivals(s, EPS_MIN, 1, 5, -1, wl.COST_ADDITIVE_INTERP, [1, 5], [0.0, 0.5],
+                                bias=0.25, alpha=0.75)
+    tau = [1.0, 1.875, 2.375, 2.625, 2.6875]
+    np.testing.assert_array_equal(r.tau_curve, tau)
+    np.testing.assert_allclose(r.theta_curve, [t / (1 + b / 8) for b, t in enumerate(tau)],
+                               rtol=1e-15)
+    assert r.budget == 3 and list(r.verify_lens) == [4]
+    c = orc.plan_from_survivals(s, EPS_MIN, 1, 5, -1, wl.COST_ADDITIVE, [1, 5], [0.0, 0.5],
+                                bias=0.25, alpha=0.75)
+    assert c.budget == 4
+    # at the samples themselves both lookups give the same T
+    assert r.theta_curve[0] == c.theta_curve[0] and r.theta_curve[4] == c.theta_curve[4]
+
+
+def test_cost_lookup_interpolated_edges(orc):
+    s = _f32([[0.5, 0.25], [0.5, 0.25]])  # tau 2 2.5 3 3.25 3.5, M = 2 + b
+    # samples at M = 3 and 4 only: M = 2 is below the first (val_0), M > 4 infeasible
+    r = orc.plan_from_survivals(s, EPS_MIN, 1, 3, -1, wl.COST_ADDITIVE_INTERP, [3, 4], [1.0, 3.0],
+                                bias=0.5, alpha=0.5)
+    assert list(r.feasible) == [True, True, True, False, False]
+    np.testing.assert_allclose(r.theta_curve[:3], [1.0, 1.25, 0.75], rtol=1e-15)
+    # three samples, a midpoint: M = 4 between (3, 1 ms) and (5, 5 ms) -> 3 ms
+    q = orc.plan_from_survivals(s, EPS_MIN, 1, 3, -1, wl.COST_ADDITIVE_INTERP, [3, 5, 9],
+                                [1.0, 5.0, 6.0], bias=0.5, alpha=0.5)
+    np.testing.assert_allclose(q.theta_curve, [2 / 2, 2.5 / 2, 3 / 4, 3.25 / 6, 3.5 / 6.25],
+                               rtol=1e-15)
+    assert q.budget == 1
+    # a non-positive interpolated T is infeasible and flagged
+    z = orc.plan_from_survivals(s, EPS_MIN, 1, 3, -1, wl.COST_ADDITIVE_INTERP, [2, 6],
+                                [-1.0, 3.0], bias=0.0, alpha=0.0)
+    assert z.status & orc.ST_BAD_COST and not z.feasible[0] and z.feasible[2]
+
+
 def test_invalid_cost_and_infeasible(orc):
     s = _f32([[0.5, 0.25]])
     r = orc.plan_from_survivals(s, EPS_MIN, 1, 3, -1, wl.COST_SPS_1D, [1, 2], [0.0, 5.0])
