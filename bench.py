@@ -267,6 +267,51 @@ def emit(line, args):
 CAL_N, CAL_GAMMA, CAL_TEMPS, CAL_BINS = 262144, 16, 64, 15
 
 
+def plan_kind_timing(dev, stream, vs, kind, reps=32, table=None):
+    """GPU time of one dspark_plan call (survival + planner pass) with the
+    step's cost table (or `table` = (M, val) tensors) read as `kind`: 32
+    calls captured in a CUDA graph."""
+    import torch
+    from confidence_scheduled_speculative_gb300 import api as _api
+    c = vs.cfg
+    cM, cval = (vs.cost_M, vs.cost_val) if table is None else table
+    out = {}
+
+    def call():
+        _api.dspark_plan(vs.conf_logits, vs.sts_temps, B=c.B, gamma=c.gamma,
+                         survival_eps=c.survival_eps, min_verify_len=c.min_verify_len,
+                         max_verify_len=c.max_verify_len, forced_budget=c.forced_budget,
+                         cost_kind=kind, cost_M=cM, cost_val=cval,
+                         bias_ms=c.bias_ms, alpha_ms=c.alpha_ms, survivals=vs.survivals,
+                         verify_lens=vs.verify_lens, budget=vs.budget, tau_theta=vs.tau_theta,
+                         status=vs.status, workspace=vs.plan_ws)
+
+    try:
+        for _ in range(3):
+            call()
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=gs):
+            for _ in range(reps):
+                call()
+        torch.cuda.synchronize()
+        cg.replay()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record(stream)
+        for _ in range(5):
+            cg.replay()
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        out["us"] = ev[0].elapsed_time(ev[1]) * 1e3 / (5 * reps)
+        out["budget"] = int(vs.budget.item())
+        out["status"] = int(vs.status.item())
+    except Exception as e:  # report, do not fail the run
+        out["error"] = f"{type(e).__name__}: {e}"[:200]
+    return out
+
+
 def calibration_timing(dev, stream, vs, w, K):
     """Recorder, statistics and fit timings (CUDA events on the stream)."""
     import torch
@@ -597,6 +642,23 @@ def run_ours(args):
     if not args.no_cap and not args.no_calib:
         calib = calibration_timing(dev, stream, vs, w, K)
 
+    # ---- the planner alone from a CUDA graph, with the step's additive table
+    # and with the same samples interpolated (secondary)
+    plan_kinds = None
+    if not args.no_cap and w.name == "dsv4_like":
+        from confidence_scheduled_speculative_gb300 import api as _api
+        vs.status.zero_()
+        # the same tier costs at every 128 rows: 31 entries, past the select
+        # path's 16, so the planner takes the rank path
+        dM = torch.arange(256, 4097, 128, dtype=torch.int32, device=dev)
+        dense = (dM, 0.002 * dM.to(torch.float64))
+        plan_kinds = {"additive_tier": plan_kind_timing(dev, stream, vs, _api.COST_ADDITIVE),
+                      "additive_tier_31_entries_rank_path":
+                          plan_kind_timing(dev, stream, vs, _api.COST_ADDITIVE, table=dense),
+                      "additive_interpolated":
+                          plan_kind_timing(dev, stream, vs, _api.COST_ADDITIVE_INTERP)}
+        vs.status.zero_()
+
     # ---- cap-accept over the full strided block (secondary)
     cap = None
     if not args.no_cap:
@@ -698,6 +760,7 @@ def run_ours(args):
         "scatter_compact_to_strided": scat,
         "sampling_accept": samp,
         "calibration": calib,
+        "plan_by_cost_kind": plan_kinds,
         "cap_accept": cap,
         "status": status,
     }

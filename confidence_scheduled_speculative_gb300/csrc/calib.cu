@@ -38,13 +38,15 @@
 //                      rows land at (cursor + i) mod capacity, coalesced
 //                      element copies; the cursor lives on the device, so
 //                      a captured graph can record every step.
-//   calib_stats_kernel one sample per thread, every depth in a loop (the
-//                      fp32 survival product runs left to right); per
-//                      (flavour, depth) the lanes of a warp that share a bin
-//                      are combined with ballots and redux sums and one lane
-//                      adds them to the CTA's shared histogram; CTAs add
-//                      their histograms to a global one with u64 atomics and
-//                      the last CTA (atomic ticket, no waiting) turns it into
+//   calib_stats_kernel each thread holds two samples in registers over the
+//                      depth loop (the fp32 survival product runs left to
+//                      right); per (flavour, depth) a sample's bin gets
+//                      count + (label << 32) and its confidence by shared
+//                      atomics, its Brier and log-loss terms add to float
+//                      pairs that one warp reduction per depth and pass
+//                      folds into the warp's slot; CTAs add their
+//                      histograms to a global one with u64 atomics and the
+//                      last CTA (atomic ticket, no waiting) turns it into
 //                      the metrics.
 //   sts_fit_kernel     one launch per depth (programmatic serialization
 //                      chains them).  A CTA stages a tile of 256 samples --
@@ -60,8 +62,10 @@
 //                      with atomics; the last CTA scores every candidate
 //                      (exact integer ECE), picks the lowest (ties to the
 //                      lower index) and clears the histograms for the next
-//                      depth.  The work is N * J fp64 sigmoids per depth: the
-//                      kernel is bound by the fp64 units, not by memory.
+//                      depth.  The work is N * J sigmoids per depth, four
+//                      interleaved per thread over tiles compacted to the
+//                      samples that count: the kernel is bound by
+//                      instruction issue, not by memory.
 //
 // No kernel waits on another CTA: the last-CTA tickets never spin.
 

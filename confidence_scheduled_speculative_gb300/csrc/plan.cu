@@ -275,6 +275,7 @@ struct RankSmem {
     unsigned long long acc_s[kMaxSparse + 1];   // this CTA's part of each candidate's prefix
     double val_s[kMaxSparse];                   // sparse path: the cost table values
     int budget, last, n_kept, sparse, forced;
+    unsigned int theta_floor;  // interpolated table: a lower bound of the largest theta (float bits)
     long long b_top;
 };
 
@@ -315,7 +316,7 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
     pdl_trigger();
     // the cost table is written before the step: fetch it while waiting
     int Mj = 0, Mprev = 0, Mnext = 0;
-    const bool sparse = c.n <= kMaxSparse;
+    const bool sparse = c.n <= kMaxSparse && c.kind != DSPARK_COST_ADDITIVE_INTERP;
     double vj = 0.0;
     if (sparse && tid < c.n) {
         Mj = __ldg(c.M + tid);
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
     }
     const int n_kept = block_sum<int>(kept_local, sm.scan32);  // syncs
     long long b_top = n_kept;  // largest in-range budget
-    if (c.kind == DSPARK_COST_ADDITIVE) b_top = min(b_top, (long long)Mlast - (long long)B);
+    if (c.kind != DSPARK_COST_SPS_1D) b_top = min(b_top, (long long)Mlast - (long long)B);
     if (sparse) {
         if (tid < c.n) {
             sm.cand_b[tid] = entry_last_budget(c, tid, Mj, Mprev, Mnext, B, b_top);
@@ -459,6 +460,112 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
     }
 }
 
+// T(B, M) of the interpolated additive table at M = Mv <= M_{n-1}
+// ([AVS] §四, the exported table's runtime linear interpolation of theta(M)):
+// val_j + (Mv - M_j) * slope_j with slope_j = (val_{j+1} - val_j) /
+// (M_{j+1} - M_j) in that fp64 order, val_j at Mv = M_j, val_0 below M_0.
+// False when T is not a positive finite number.
+__device__ __forceinline__ bool interp_cost(const CostArgs &c, long long Mv, double fixed_cost,
+                                            double &T) {
+    double th;
+    if (Mv <= (long long)__ldg(c.M)) {
+        th = __ldg(c.val);
+    } else {
+        int lo = 0, hi = c.n - 1;  // the last sample with M_j <= Mv
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((long long)__ldg(c.M + mid) <= Mv) lo = mid;
+            else hi = mid - 1;
+        }
+        const long long Mj = __ldg(c.M + lo);
+        const double vj = __ldg(c.val + lo);
+        if (Mj == Mv || lo + 1 >= c.n) {  // the second: only a table out of order gets here
+            th = vj;
+        } else {
+            const long long Mn = __ldg(c.M + lo + 1);
+            const double slope = __ddiv_rn(__dsub_rn(__ldg(c.val + lo + 1), vj), (double)(Mn - Mj));
+            th = __dadd_rn(vj, __dmul_rn((double)(Mv - Mj), slope));
+        }
+    }
+    T = __dadd_rn(fixed_cost, th);
+    return T > 0.0 && isfinite(T);
+}
+
+// tau = B + P 2^-37 as a float, truncated (relative error below 2^-23), by
+// integer operations only
+__device__ __forceinline__ float tau_float(int B, long long P) {
+    const unsigned long long x = ((unsigned long long)B << 37) + (unsigned long long)P;
+    const int msb = 63 - __clzll((long long)x);  // >= 37
+    const unsigned mant = (unsigned)((x >> (msb - 23)) & 0x7fffffull);
+    return __uint_as_float(((unsigned)(msb - 37 + 127) << 23) | mant);
+}
+
+// fp32 view of the interpolated table for a walk over increasing budgets:
+// the segment [M_j, M_{j+1}) holding M = B + b (j = -1 below M_0), loaded
+// once per segment crossed.
+struct InterpWalk {
+    int seg = -2;
+    long long Mj = 0, Mn = 0;
+    float vj = 0.0f, slope = 0.0f, mag_v = 0.0f;
+
+    __device__ void load(const CostArgs &c, int j) {
+        seg = j;
+        const int jj = j < 0 ? 0 : j;
+        Mj = __ldg(c.M + jj);
+        vj = (float)__ldg(c.val + jj);
+        if (j >= 0 && j + 1 < c.n) {
+            Mn = __ldg(c.M + j + 1);
+            const float vn = (float)__ldg(c.val + j + 1);
+            slope = __fdiv_rn(vn - vj, (float)(Mn - Mj));
+            mag_v = fabsf(vj) + fabsf(vn);
+        } else {
+            Mn = j < 0 ? Mj + 1 : LLONG_MAX;  // below M_0: up to M_0 inclusive
+            slope = 0.0f;
+            mag_v = fabsf(vj);
+        }
+    }
+
+    // Bounds lo <= tau/T <= hi of theta(b) from fp32 arithmetic: the real
+    // quotient of the fp64 definition's tau and T lies inside, with room for
+    // its final rounding.  The fp32 T differs from the fp64 T by less than
+    // 2^-20 times the sum of the magnitudes it is built from (conversions,
+    // the slope's subtraction and division, the FMA and the add each
+    // contribute at most 2^-23 of one of them).  False when that bound
+    // cannot show T > 0 or a value is not finite in fp32: the caller then
+    // evaluates the budget in fp64.  Budgets must come in increasing order.
+    __device__ bool bounds(const CostArgs &c, int B, long long b, long long Pb, float fixed32,
+                           float &lo, float &hi) {
+        const long long Mv = (long long)B + b;
+        if (seg == -2) {
+            if (Mv <= (long long)__ldg(c.M)) {
+                load(c, -1);
+            } else {
+                int l = 0, h = c.n - 1;  // the last sample with M_j <= Mv
+                while (l < h) {
+                    const int mid = (l + h + 1) >> 1;
+                    if ((long long)__ldg(c.M + mid) <= Mv) l = mid;
+                    else h = mid - 1;
+                }
+                load(c, l);
+            }
+        }
+        while (Mv >= Mn && seg + 1 < c.n) load(c, seg + 1);
+        const float d = seg < 0 ? 0.0f : (float)(int)(Mv - Mj);
+        const float th = fmaf(d, slope, vj);
+        const float T = fixed32 + th;
+        const float err = 0x1p-20f * (fabsf(fixed32) + mag_v + fabsf(d * slope));
+        if (!(isfinite(T) && isfinite(err)) || !(T - err > 0.0f)) return false;
+        float rT, rTe;
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rT) : "f"(T));
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rTe) : "f"(T - err));
+        const float q = tau_float(B, Pb) * rT;
+        const float rel = 0x1p-19f + 2.0f * err * rTe;
+        lo = q * (1.0f - rel);
+        hi = q * (1.0f + rel);
+        return isfinite(hi);
+    }
+};
+
 __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = a.B, G = a.gamma;
@@ -495,7 +602,56 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
     long long my_key = -1;
     int my_b = 0x7FFFFFFF;
     bool my_bad_cost = false, my_bad_table = false;
-    for (int j = tid; j < c.n; j += kRankThreads) {
+    const bool interp = c.kind == DSPARK_COST_ADDITIVE_INTERP;
+    if (interp) {
+        // The cost changes with every budget.  fp32 bounds of theta at every
+        // in-range budget first; the fp64 definition is then evaluated only
+        // where the bounds cannot exclude the maximum (or cannot show T > 0):
+        // a budget whose upper bound is below the largest lower bound cannot
+        // be the first maximiser.
+        for (int j = tid + 1; j < c.n; j += kRankThreads)
+            if (!(__ldg(c.M + j) > __ldg(c.M + j - 1))) my_bad_table = true;
+        const float fixed32 = (float)fixed_cost;
+        if (tid == 0) sm.theta_floor = 0u;
+        __syncthreads();
+        auto exact = [&](long long b) {
+            double Tm;
+            if (!interp_cost(c, (long long)B + b, fixed_cost, Tm)) {
+                my_bad_cost = true;
+                return;
+            }
+            const double theta = __ddiv_rn(tau_of(B, __ldcg(P + b)), Tm);
+            const long long kk = __double_as_longlong(theta);
+            if (cand_better(kk, (int)b, my_key, my_b)) {
+                my_key = kk;
+                my_b = (int)b;
+            }
+        };
+        // each thread walks a contiguous range of budgets
+        const long long per = (b_top + kRankThreads) / kRankThreads;
+        const long long b0 = (long long)tid * per, b1 = min(b0 + per, b_top + 1);
+        float my_floor = 0.0f;
+        InterpWalk wk;
+        for (long long b = b0; b < b1; ++b) {
+            float lo, hi;
+            if (wk.bounds(c, B, b, __ldcg(P + b), fixed32, lo, hi)) {
+                my_floor = fmaxf(my_floor, lo);
+            } else {
+                exact(b);  // uncertain sign of T, or not finite in fp32
+                if (my_b == (int)b)
+                    my_floor = fmaxf(my_floor, (float)__longlong_as_double(my_key) * (1.0f - 0x1p-20f));
+            }
+        }
+        atomicMax(&sm.theta_floor, __float_as_uint(my_floor));  // non-negative floats
+        __syncthreads();
+        const float floor_all = __uint_as_float(sm.theta_floor);
+        InterpWalk wk2;
+        for (long long b = b0; b < b1; ++b) {
+            float lo, hi;
+            if (wk2.bounds(c, B, b, __ldcg(P + b), fixed32, lo, hi) && hi >= floor_all) exact(b);
+        }
+    }
+    for (int j = tid; j < (interp ? 0 : c.n); j += kRankThreads) {
         const int Mj = __ldg(c.M + j);
         const double vj = sparse ? sm.val_s[j] : __ldg(c.val + j);
         const int Mprev = j > 0 ? __ldg(c.M + j - 1) : 0;
@@ -588,7 +744,10 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
                 !any_bad_table) {
                 // theta at the forced budget: the entry covering M = B + budget
                 const long long Mv = (long long)B + budget;
-                int lo = 0, hi = c.n;  // first index with M > Mv (1-D) / M >= Mv (additive)
+                double Ti;
+                if (interp && interp_cost(c, Mv, fixed_cost, Ti))
+                    theta_out = __ddiv_rn(tau_of(B, Pbud), Ti);
+                int lo = 0, hi = interp ? 0 : c.n;  // first index with M > Mv (1-D) / M >= Mv (additive)
                 while (lo < hi) {
                     const int mid = (lo + hi) >> 1;
                     const long long Mm = __ldg(c.M + mid);
@@ -600,7 +759,7 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
                     const int j = lo > 0 ? lo - 1 : 0;
                     const double sps = __ldg(c.val + j);
                     if (sps > 0.0 && isfinite(sps)) theta_out = __dmul_rn(tau_of(B, Pbud), sps);
-                } else if (lo < c.n) {
+                } else if (!interp && lo < c.n) {
                     const double Tm = __dadd_rn(fixed_cost, __ldg(c.val + lo));
                     if (Tm > 0.0 && isfinite(Tm)) theta_out = __ddiv_rn(tau_of(B, Pbud), Tm);
                 }
@@ -1377,7 +1536,8 @@ int check_plan(const float *conf_logits, const float *sts_temps, const dspark_pl
     if (p->min_verify_len < 1 || p->min_verify_len > p->max_verify_len ||
         p->max_verify_len > p->gamma + 1)
         return DSPARK_ERR_INVALID_ARG;
-    if (cost->kind != DSPARK_COST_SPS_1D && cost->kind != DSPARK_COST_ADDITIVE)
+    if (cost->kind != DSPARK_COST_SPS_1D && cost->kind != DSPARK_COST_ADDITIVE &&
+        cost->kind != DSPARK_COST_ADDITIVE_INTERP)
         return DSPARK_ERR_INVALID_ARG;
     if (cost->n < 1 || !cost->M || !cost->val) return DSPARK_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < dspark_plan_workspace_bytes(p->B, p->gamma) ||
@@ -1432,7 +1592,9 @@ int run_plan(const float *conf_logits, const float *sts_temps, const dspark_plan
     PassScratch *ps = scratch_at<PassScratch>(scratch, plan_pass_offset(B, N));
     int32_t *pass_lens = scratch_at<int32_t>(scratch, plan_pass_lens_offset(B, N));
     float *lagged_surv = scratch_at<float>(scratch, plan_pass_surv_offset(B, N));
-    const bool select = cost->n <= kMaxSelect;  // few candidate budgets: one-CTA select
+    // few candidate budgets: one-CTA select; an interpolated table makes every
+    // budget a candidate and takes the rank path
+    const bool select = cost->n <= kMaxSelect && cost->kind != DSPARK_COST_ADDITIVE_INTERP;
     const int32_t *conf_gen = opt ? opt->conf_generation : nullptr;
     const int32_t *req_gen = opt ? opt->req_generation : nullptr;
     const bool lagged = opt && opt->lagged_conf_logits;

@@ -73,6 +73,7 @@ DSPARK_API int dspark_version(void);
 
 #define DSPARK_COST_SPS_1D   0
 #define DSPARK_COST_ADDITIVE 1
+#define DSPARK_COST_ADDITIVE_INTERP 2
 
 /* Planner parameters (host struct).  [AVS] §一: ScheduleVerifyLensTopk is
  * bounded by min_verify_len, max_verify_len and survival_eps. */
@@ -94,11 +95,19 @@ typedef struct {
  *     theta(b) = tau(b) / T, T = (bias_ms + alpha_ms) + val[j] with j the
  *     smallest graph tier M_j >= B + b; budgets above the largest tier are
  *     infeasible.  alpha_ms is alpha(B) already evaluated for this B.
+ *   DSPARK_COST_ADDITIVE_INTERP ([AVS] §四 "三个关键假设", the third: the
+ *     exported additive table interpolates theta(M) linearly at runtime):
+ *     T = (bias_ms + alpha_ms) + theta(B + b), with M_j <= M < M_{j+1}
+ *     theta(M) = val[j] + (M - M_j) * slope_j, slope_j = (val[j+1] - val[j])
+ *     / (M_{j+1} - M_j), in that fp64 order; val[j] at M = M_j; val[0] below
+ *     M_0; budgets with B + b above the last sample are infeasible.  Every
+ *     budget has its own cost, so theta is evaluated at every in-range
+ *     budget (one fp64 division each, on one CTA).
  *   M must be strictly ascending (else DSPARK_STATUS_BAD_COST, all budgets
  *   infeasible).  A used entry whose SPS or T is not a positive finite
  *   number is infeasible and flagged DSPARK_STATUS_BAD_COST. */
 typedef struct {
-    int32_t kind;          /* DSPARK_COST_SPS_1D or DSPARK_COST_ADDITIVE */
+    int32_t kind;          /* DSPARK_COST_SPS_1D, _ADDITIVE or _ADDITIVE_INTERP */
     int32_t n;             /* entries, >= 1 */
     const int32_t *M;      /* device [n]: total verify rows (1-D) or graph tiers (additive) */
     const double *val;     /* device [n]: SPS (steps/s) or token-side cost theta(M) in ms */

@@ -86,7 +86,9 @@ def test_plan_argument_checks(lib):
     assert _plan(lib, Params(**{**good, "max_len": 6}), cost) == -1
     assert _plan(lib, Params(**{**good, "B": 2048, "gamma": 16}), cost) == -4  # 2048*17 > 2^16
     assert _plan(lib, Params(**{**good, "B": 1025, "gamma": 16}), cost) == -4  # > 16384 candidates
-    assert _plan(lib, Params(**good), Cost(2, 3, FAKE.value, FAKE.value, 0, 0)) == -1
+    assert _plan(lib, Params(**good), Cost(3, 3, FAKE.value, FAKE.value, 0, 0)) == -1
+    # kind 2 (interpolated additive) passes the kind check and stops at the workspace
+    assert _plan(lib, Params(**good), Cost(2, 3, FAKE.value, FAKE.value, 0, 0)) == -2
     assert _plan(lib, Params(**good), Cost(0, 0, FAKE.value, FAKE.value, 0, 0)) == -1
     assert _plan(lib, Params(**good), Cost(1, 3, None, FAKE.value, 0, 0)) == -1
     lib.dspark_plan_workspace_bytes.restype = ctypes.c_size_t

@@ -115,6 +115,47 @@ def test_plan_random(dev, orc, seed):
         assert int(g["status"][0]) == ref.status
 
 
+@pytest.mark.parametrize("seed", range(80))
+def test_plan_random_interpolated_table(dev, orc, seed):
+    """The interpolated additive table (every budget its own cost; rank path),
+    with sparse and dense tables, forced budgets and invalid entries."""
+    rng = np.random.default_rng(91000 + seed)
+    P = _random_problem(rng)
+    P["kind"] = 2
+    B, g = P["B"], P["gamma"]
+    n = int(rng.integers(1, 12)) if rng.random() < 0.5 else int(rng.integers(17, 200))
+    hi = B + B * g + 6
+    M = np.sort(rng.choice(np.arange(1, hi + 1), size=min(n, hi), replace=False)).astype(np.int32)
+    val = np.sort(rng.uniform(0.0, 3.0, M.size))
+    if rng.random() < 0.3:
+        val = rng.uniform(-0.5, 3.0, M.size)  # not monotone; may go non-positive
+    if rng.random() < 0.1:
+        val[int(rng.integers(0, M.size))] = np.inf
+    P["M"], P["val"] = M, val
+    gres = _gpu_plan(dev, P)
+    ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"], 2,
+                   P["M"], P["val"], P["bias"], P["alpha"])
+    if compare_plan(f"interp/{seed}", gres, ref, B, g, P["min_len"]):
+        assert int(gres["status"][0]) == ref.status
+
+
+@pytest.mark.parametrize("name", ["dsv4_like", "stress", "qwen_like"])
+def test_plan_interpolated_table_workloads(dev, orc, name):
+    """Full-size workloads with their additive tier table read as samples of
+    an interpolated cost curve."""
+    step = wl.make_step(wl.WORKLOADS[name], seed=3)
+    w, c = step.workload, step.cost
+    P = dict(B=w.B, gamma=w.gamma, z=step.conf_logits, T=step.sts_temps, eps=w.survival_eps,
+             min_len=w.min_verify_len, max_len=w.max_len, forced=-1, kind=2,
+             M=np.asarray(c.M, np.int32), val=np.asarray(c.val, np.float64), bias=c.bias_ms,
+             alpha=c.alpha_ms)
+    gres = _gpu_plan(dev, P)
+    ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], -1, 2, P["M"],
+                   P["val"], P["bias"], P["alpha"])
+    if compare_plan(f"interp/{name}", gres, ref, w.B, w.gamma, w.min_verify_len):
+        assert int(gres["status"][0]) == ref.status
+
+
 def _select_case(name):
     """Problems for the few-entry-table planner whose threshold bins hold few
     candidates (ranked by counting) or thousands of equal survivals (radix
