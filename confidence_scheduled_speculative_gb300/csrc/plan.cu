@@ -55,6 +55,8 @@ constexpr int kSurvThreads = 64;  // 2 requests per CTA: spreads the fp64 sigmoi
 constexpr int kRankThreads = 1024;
 constexpr int kRankWarps = kRankThreads / 32;
 constexpr int kMaxCandidates = 16384;       // B*gamma limit of the planner
+constexpr int kInterpPer = (kMaxCandidates + kRankThreads) / kRankThreads;  // budgets per thread
+constexpr int kScanReg = 4;  // kept candidates per thread held in registers by the prefix scan
 constexpr uint32_t kOneBits = 0x3F800000u;  // bits of 1.0f
 constexpr uint32_t kDroppedKey = 0x07FFFFFFu;
 constexpr int kMinExpBiased = 113;          // 2^-14: the smallest allowed eps
@@ -271,11 +273,19 @@ struct RankSmem {
     int scan32[40];
     long long best_key[kRankWarps];
     int best_b[kRankWarps];
+    long long best_P[kRankWarps];                // P at each warp's best budget
     int cand_b[kMaxSparse + 1];                 // candidate budget of each table entry (-1: none)
     unsigned long long acc_s[kMaxSparse + 1];   // this CTA's part of each candidate's prefix
-    double val_s[kMaxSparse];                   // sparse path: the cost table values
+    double val_s[kMaxSparse];                   // sparse path and small interpolated tables: values
+    int M_s[kMaxSparse];                        // small interpolated tables: samples
+    float v32_s[kMaxSparse];                    // small interpolated tables: values as floats
+    float fixed32;                              // bias + alpha as a float
+    double fixed_cost;                          // bias + alpha
+    int itab_bad;                               // interpolated table: samples out of order
     int budget, last, n_kept, sparse, forced;
     unsigned int theta_floor;  // interpolated table: a lower bound of the largest theta (float bits)
+    int n_icand;               // interpolated table: budgets left for the fp64 definition
+    int icand_b[kRankThreads], icand_seg[kRankThreads];
     long long b_top;
 };
 
@@ -316,15 +326,22 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
     pdl_trigger();
     // the cost table is written before the step: fetch it while waiting
     int Mj = 0, Mprev = 0, Mnext = 0;
-    const bool sparse = c.n <= kMaxSparse && c.kind != DSPARK_COST_ADDITIVE_INTERP;
+    const bool interp = c.kind == DSPARK_COST_ADDITIVE_INTERP;
+    const bool sparse = c.n <= kMaxSparse && !interp;
+    const bool itab = interp && c.n <= kMaxSparse;  // staged in shared memory
     double vj = 0.0;
-    if (sparse && tid < c.n) {
+    if ((sparse || itab) && tid < c.n) {
         Mj = __ldg(c.M + tid);
         Mprev = tid > 0 ? __ldg(c.M + tid - 1) : 0;
         Mnext = tid < c.n - 1 ? __ldg(c.M + tid + 1) : 0;
         vj = __ldg(c.val + tid);
     }
     const int Mlast = __ldg(c.M + c.n - 1);
+    // interpolated table: its order, checked while the survivals are on the way
+    bool order_bad = false;
+    if (interp)
+        for (int j = tid + 1; j < c.n; j += kRankThreads)
+            if (!(__ldg(c.M + j) > __ldg(c.M + j - 1))) order_bad = true;
     pdl_wait();  // survivals come from survival_kernel
     const int forced = resolve_forced(a);
 
@@ -355,8 +372,20 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
         K[r * S + G + (j - r * pad)] = kDroppedKey;
     }
     const int n_kept = block_sum<int>(kept_local, sm.scan32);  // syncs
+    const int any_order_bad = __syncthreads_or(order_bad);
     long long b_top = n_kept;  // largest in-range budget
     if (c.kind != DSPARK_COST_SPS_1D) b_top = min(b_top, (long long)Mlast - (long long)B);
+    // (conversions from fp64 run on the fp64 unit: done once per entry here)
+    if (itab && tid < c.n) {
+        sm.M_s[tid] = Mj;
+        sm.val_s[tid] = vj;
+        sm.v32_s[tid] = (float)vj;
+    }
+    // fp64 operations and conversions share GB300's small fp64 unit: once per CTA
+    if (tid == 0) {
+        sm.fixed_cost = __dadd_rn(c.bias, c.alpha);
+        sm.fixed32 = (float)sm.fixed_cost;
+    }
     if (sparse) {
         if (tid < c.n) {
             sm.cand_b[tid] = entry_last_budget(c, tid, Mj, Mprev, Mnext, B, b_top);
@@ -366,6 +395,7 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
         if (tid <= c.n) sm.acc_s[tid] = 0ull;
     }
     if (tid == 0) {
+        sm.itab_bad = any_order_bad;
         sm.n_kept = n_kept;
         sm.b_top = b_top;
         sm.sparse = sparse ? 1 : 0;
@@ -464,31 +494,55 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
 // ([AVS] §四, the exported table's runtime linear interpolation of theta(M)):
 // val_j + (Mv - M_j) * slope_j with slope_j = (val_{j+1} - val_j) /
 // (M_{j+1} - M_j) in that fp64 order, val_j at Mv = M_j, val_0 below M_0.
-// False when T is not a positive finite number.
+// False when T is not a positive finite number.  j = the last sample with
+// M_j <= Mv, or -1 when Mv <= M_0 (interp_cost below finds it).
+// tM / tV: the table's samples and values, in shared or global memory.
+__device__ __forceinline__ bool interp_cost_at(const int32_t *tM, const double *tV, int n,
+                                               long long Mv, int j, double fixed_cost, double &T) {
+    double th;
+    if (j < 0) {
+        th = tV[0];
+    } else {
+        const int lo = j;
+        const long long Mj = tM[lo];
+        const double vj = tV[lo];
+        if (Mj == Mv || lo + 1 >= n) {  // the second: only a table out of order gets here
+            th = vj;
+        } else {
+            const long long Mn = tM[lo + 1];
+            const double slope = __ddiv_rn(__dsub_rn(tV[lo + 1], vj), (double)(Mn - Mj));
+            th = __dadd_rn(vj, __dmul_rn((double)(Mv - Mj), slope));
+        }
+    }
+    T = __dadd_rn(fixed_cost, th);
+    return T > 0.0 && isfinite(T);
+}
+
 __device__ __forceinline__ bool interp_cost(const CostArgs &c, long long Mv, double fixed_cost,
                                             double &T) {
-    double th;
-    if (Mv <= (long long)__ldg(c.M)) {
-        th = __ldg(c.val);
-    } else {
+    int j = -1;
+    if (Mv > (long long)__ldg(c.M)) {
         int lo = 0, hi = c.n - 1;  // the last sample with M_j <= Mv
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if ((long long)__ldg(c.M + mid) <= Mv) lo = mid;
             else hi = mid - 1;
         }
-        const long long Mj = __ldg(c.M + lo);
-        const double vj = __ldg(c.val + lo);
-        if (Mj == Mv || lo + 1 >= c.n) {  // the second: only a table out of order gets here
-            th = vj;
-        } else {
-            const long long Mn = __ldg(c.M + lo + 1);
-            const double slope = __ddiv_rn(__dsub_rn(__ldg(c.val + lo + 1), vj), (double)(Mn - Mj));
-            th = __dadd_rn(vj, __dmul_rn((double)(Mv - Mj), slope));
-        }
+        j = lo;
     }
-    T = __dadd_rn(fixed_cost, th);
-    return T > 0.0 && isfinite(T);
+    return interp_cost_at(c.M, c.val, c.n, Mv, j, fixed_cost, T);
+}
+
+// The key region of the rank kernel's shared memory (after RankSmem), reused
+// by the last CTA for the float tau of every budget of an interpolated table.
+__device__ __forceinline__ float *interp_tau_smem(RankSmem &sm) {
+    return reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(&sm) +
+                                     ((sizeof(RankSmem) + 15) & ~size_t(15)));
+}
+
+// x as a float for 0 <= x < 2^23, from its bits (no conversion instruction)
+__device__ __forceinline__ float small_int_float(int x) {
+    return __fsub_rn(__int_as_float(0x4B000000 | x), 8388608.0f);
 }
 
 // tau = B + P 2^-37 as a float, truncated (relative error below 2^-23), by
@@ -504,19 +558,29 @@ __device__ __forceinline__ float tau_float(int B, long long P) {
 // the segment [M_j, M_{j+1}) holding M = B + b (j = -1 below M_0), loaded
 // once per segment crossed.
 struct InterpWalk {
+    const int32_t *tM;  // the table, in shared or global memory
+    const double *tV;
+    const float *tV32;  // its values as floats, or null (converted here)
+    int n;
     int seg = -2;
     long long Mj = 0, Mn = 0;
     float vj = 0.0f, slope = 0.0f, mag_v = 0.0f;
 
-    __device__ void load(const CostArgs &c, int j) {
+    __device__ InterpWalk(const int32_t *M, const double *V, const float *V32, int count)
+        : tM(M), tV(V), tV32(V32), n(count) {}
+
+    __device__ float value(int j) const { return tV32 ? tV32[j] : (float)tV[j]; }
+
+    __device__ void load(int j) {
         seg = j;
         const int jj = j < 0 ? 0 : j;
-        Mj = __ldg(c.M + jj);
-        vj = (float)__ldg(c.val + jj);
-        if (j >= 0 && j + 1 < c.n) {
-            Mn = __ldg(c.M + j + 1);
-            const float vn = (float)__ldg(c.val + j + 1);
-            slope = __fdiv_rn(vn - vj, (float)(Mn - Mj));
+        Mj = tM[jj];
+        vj = value(jj);
+        if (j >= 0 && j + 1 < n) {
+            Mn = tM[j + 1];
+            const float vn = value(j + 1);
+            const long long dM = Mn - Mj;
+            slope = __fdiv_rn(vn - vj, dM < (1 << 23) ? small_int_float((int)dM) : (float)dM);
             mag_v = fabsf(vj) + fabsf(vn);
         } else {
             Mn = j < 0 ? Mj + 1 : LLONG_MAX;  // below M_0: up to M_0 inclusive
@@ -533,24 +597,26 @@ struct InterpWalk {
     // contribute at most 2^-23 of one of them).  False when that bound
     // cannot show T > 0 or a value is not finite in fp32: the caller then
     // evaluates the budget in fp64.  Budgets must come in increasing order.
-    __device__ bool bounds(const CostArgs &c, int B, long long b, long long Pb, float fixed32,
-                           float &lo, float &hi) {
-        const long long Mv = (long long)B + b;
-        if (seg == -2) {
-            if (Mv <= (long long)__ldg(c.M)) {
-                load(c, -1);
-            } else {
-                int l = 0, h = c.n - 1;  // the last sample with M_j <= Mv
-                while (l < h) {
-                    const int mid = (l + h + 1) >> 1;
-                    if ((long long)__ldg(c.M + mid) <= Mv) l = mid;
-                    else h = mid - 1;
-                }
-                load(c, l);
-            }
+    // the segment of M = Mv, by binary search
+    __device__ void init(long long Mv) {
+        if (Mv <= (long long)tM[0]) {
+            load(-1);
+            return;
         }
-        while (Mv >= Mn && seg + 1 < c.n) load(c, seg + 1);
-        const float d = seg < 0 ? 0.0f : (float)(int)(Mv - Mj);
+        int l = 0, h = n - 1;  // the last sample with M_j <= Mv
+        while (l < h) {
+            const int mid = (l + h + 1) >> 1;
+            if ((long long)tM[mid] <= Mv) l = mid;
+            else h = mid - 1;
+        }
+        load(l);
+    }
+
+    __device__ bool bounds(int B, long long b, float tau32, float fixed32, float &lo, float &hi) {
+        const long long Mv = (long long)B + b;
+        while (Mv >= Mn && seg + 1 < n) load(seg + 1);
+        const long long dv = Mv - Mj;  // in [0, M_{j+1} - M_j)
+        const float d = seg < 0 ? 0.0f : (dv < (1 << 23) ? small_int_float((int)dv) : (float)dv);
         const float th = fmaf(d, slope, vj);
         const float T = fixed32 + th;
         const float err = 0x1p-20f * (fabsf(fixed32) + mag_v + fabsf(d * slope));
@@ -558,7 +624,7 @@ struct InterpWalk {
         float rT, rTe;
         asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rT) : "f"(T));
         asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rTe) : "f"(T - err));
-        const float q = tau_float(B, Pb) * rT;
+        const float q = tau32 * rT;
         const float rel = 0x1p-19f + 2.0f * err * rTe;
         lo = q * (1.0f - rel);
         hi = q * (1.0f + rel);
@@ -581,25 +647,48 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
     // (a) dense tables: P[i] = sum of the i largest survivals in units of
     // 2^-37 (P[0] = 0), a blocked scan written to the workspace
     if (!sparse) {
-        const int per = (n_kept + kRankThreads - 1) / kRankThreads;
+        const int per = (n_kept + kRankThreads - 1) / kRankThreads;  // <= kScanPer
         const int lo = tid * per, hi = min(lo + per, n_kept);
+        // the thread's chunk (up to kScanReg in registers, all in flight at once)
+        long long v[kScanReg];
         long long local = 0;
-        for (int i = lo; i < hi; ++i) local += __ldcg(sorted + i);
+#pragma unroll
+        for (int u = 0; u < kScanReg; ++u) v[u] = lo + u < hi ? __ldcg(sorted + lo + u) : 0;
+        for (int i = lo + kScanReg; i < hi; ++i) local += __ldcg(sorted + i);
+#pragma unroll
+        for (int u = 0; u < kScanReg; ++u) local += v[u];
         long long tot;
         long long run = block_exclusive_scan<long long>(local, sm.scan64, &tot);
-        for (int i = lo; i < hi; ++i) {
+        // interpolated table: tau of every budget as a float as well, in the
+        // key region of shared memory (free once the ranks are out; it holds
+        // B * (gamma + 1) >= n_kept + 1 words)
+        float *tauf = interp_tau_smem(sm);
+        const bool want_f = c.kind == DSPARK_COST_ADDITIVE_INTERP;
+#pragma unroll
+        for (int u = 0; u < kScanReg; ++u) {
+            if (lo + u < hi) {
+                run += v[u];
+                P[lo + u + 1] = run;
+                if (want_f) tauf[lo + u + 1] = tau_float(B, run);
+            }
+        }
+        for (int i = lo + kScanReg; i < hi; ++i) {
             run += __ldcg(sorted + i);
             P[i + 1] = run;
+            if (want_f) tauf[i + 1] = tau_float(B, run);
         }
-        if (tid == 0) P[0] = 0;
+        if (tid == 0) {
+            P[0] = 0;
+            if (want_f) tauf[0] = tau_float(B, 0);
+        }
         __syncthreads();
     }
 
     // (b) theta at the last budget of every table entry's range of M = B + b
     if (sparse && tid <= c.n) sm.acc_s[tid] = __ldcg(&a.scratch->acc[tid]);
     if (sparse) __syncthreads();
-    const double fixed_cost = __dadd_rn(c.bias, c.alpha);
-    long long my_key = -1;
+    const double fixed_cost = sm.fixed_cost;
+    long long my_key = -1, my_P = 0;
     int my_b = 0x7FFFFFFF;
     bool my_bad_cost = false, my_bad_table = false;
     const bool interp = c.kind == DSPARK_COST_ADDITIVE_INTERP;
@@ -609,47 +698,78 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
         // where the bounds cannot exclude the maximum (or cannot show T > 0):
         // a budget whose upper bound is below the largest lower bound cannot
         // be the first maximiser.
-        for (int j = tid + 1; j < c.n; j += kRankThreads)
-            if (!(__ldg(c.M + j) > __ldg(c.M + j - 1))) my_bad_table = true;
-        const float fixed32 = (float)fixed_cost;
-        if (tid == 0) sm.theta_floor = 0u;
+        if (sm.itab_bad) my_bad_table = true;  // checked in the prologue
+        const bool itab = c.n <= kMaxSparse;      // staged in shared memory
+        const int32_t *tM = itab ? sm.M_s : c.M;
+        const double *tV = itab ? sm.val_s : c.val;
+        const float *tV32 = itab ? sm.v32_s : nullptr;
+        const float fixed32 = sm.fixed32;
+        if (tid == 0) {
+            sm.theta_floor = 0u;
+            sm.n_icand = 0;
+        }
         __syncthreads();
-        auto exact = [&](long long b) {
+        auto exact = [&](long long b, int seg) {
             double Tm;
-            if (!interp_cost(c, (long long)B + b, fixed_cost, Tm)) {
+            if (!interp_cost_at(tM, tV, c.n, (long long)B + b, seg, fixed_cost, Tm)) {
                 my_bad_cost = true;
                 return;
             }
-            const double theta = __ddiv_rn(tau_of(B, __ldcg(P + b)), Tm);
+            const long long Pb = __ldcg(P + b);
+            const double theta = __ddiv_rn(tau_of(B, Pb), Tm);
             const long long kk = __double_as_longlong(theta);
             if (cand_better(kk, (int)b, my_key, my_b)) {
                 my_key = kk;
                 my_b = (int)b;
+                my_P = Pb;
             }
         };
-        // each thread walks a contiguous range of budgets
-        const long long per = (b_top + kRankThreads) / kRankThreads;
-        const long long b0 = (long long)tid * per, b1 = min(b0 + per, b_top + 1);
+        // each thread walks a contiguous range of at most kInterpPer budgets;
+        // its tau values are loaded together, once
+        const int per = (int)((b_top + kRankThreads) / kRankThreads);
+        const long long b0 = (long long)tid * per;
+        const int cnt = (int)max(0LL, min(b0 + per, b_top + 1) - b0);
+        const float *tauf = interp_tau_smem(sm);  // tau of every budget, from the scan
+        InterpWalk wk0(tM, tV, tV32, c.n);
+        if (cnt > 0) wk0.init((long long)B + b0);
         float my_floor = 0.0f;
-        InterpWalk wk;
-        for (long long b = b0; b < b1; ++b) {
+        InterpWalk wk = wk0;
+#pragma unroll
+        for (int i = 0; i < kInterpPer; ++i) {
+            if (i >= cnt) break;
             float lo, hi;
-            if (wk.bounds(c, B, b, __ldcg(P + b), fixed32, lo, hi)) {
+            if (wk.bounds(B, b0 + i, tauf[b0 + i], fixed32, lo, hi)) {
                 my_floor = fmaxf(my_floor, lo);
             } else {
-                exact(b);  // uncertain sign of T, or not finite in fp32
-                if (my_b == (int)b)
+                exact(b0 + i, wk.seg);  // uncertain sign of T, or not finite in fp32
+                if (my_b == (int)(b0 + i))
                     my_floor = fmaxf(my_floor, (float)__longlong_as_double(my_key) * (1.0f - 0x1p-20f));
             }
         }
-        atomicMax(&sm.theta_floor, __float_as_uint(my_floor));  // non-negative floats
+        // non-negative floats order like their bits: one atomic per warp
+        const unsigned wfloor = __reduce_max_sync(kFullMask, __float_as_uint(my_floor));
+        if (lane == 0) atomicMax(&sm.theta_floor, wfloor);
         __syncthreads();
         const float floor_all = __uint_as_float(sm.theta_floor);
-        InterpWalk wk2;
-        for (long long b = b0; b < b1; ++b) {
+        // the budgets the bounds cannot exclude sit next to each other: list
+        // them and give each its own thread for the fp64 definition
+        wk = wk0;
+#pragma unroll
+        for (int i = 0; i < kInterpPer; ++i) {
+            if (i >= cnt) break;
             float lo, hi;
-            if (wk2.bounds(c, B, b, __ldcg(P + b), fixed32, lo, hi) && hi >= floor_all) exact(b);
+            if (wk.bounds(B, b0 + i, tauf[b0 + i], fixed32, lo, hi) && hi >= floor_all) {
+                const int slot = atomicAdd(&sm.n_icand, 1);
+                if (slot < kRankThreads) {
+                    sm.icand_b[slot] = (int)(b0 + i);
+                    sm.icand_seg[slot] = wk.seg;
+                } else {
+                    exact(b0 + i, wk.seg);  // more than a thread each
+                }
+            }
         }
+        __syncthreads();
+        if (tid < min(sm.n_icand, kRankThreads)) exact(sm.icand_b[tid], sm.icand_seg[tid]);
     }
     for (int j = tid; j < (interp ? 0 : c.n); j += kRankThreads) {
         const int Mj = __ldg(c.M + j);
@@ -675,33 +795,40 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
         if (cand_better(kk, b, my_key, my_b)) {
             my_key = kk;
             my_b = b;
+            my_P = Pb;
         }
     }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) {
         const long long ok = __shfl_down_sync(kFullMask, my_key, d);
         const int ob = __shfl_down_sync(kFullMask, my_b, d);
+        const long long oP = __shfl_down_sync(kFullMask, my_P, d);
         if (cand_better(ok, ob, my_key, my_b)) {
             my_key = ok;
             my_b = ob;
+            my_P = oP;
         }
     }
     if (lane == 0) {
         sm.best_key[warp] = my_key;
         sm.best_b[warp] = my_b;
+        sm.best_P[warp] = my_P;
     }
     const int any_bad_cost = __syncthreads_or(my_bad_cost);
     const int any_bad_table = __syncthreads_or(my_bad_table);
     if (warp == 0) {
         long long bk = lane < kRankWarps ? sm.best_key[lane] : -1;
         int bb = lane < kRankWarps ? sm.best_b[lane] : 0x7FFFFFFF;
+        long long bP = lane < kRankWarps ? sm.best_P[lane] : 0;
 #pragma unroll
         for (int d = 16; d > 0; d >>= 1) {
             const long long ok = __shfl_down_sync(kFullMask, bk, d);
             const int ob = __shfl_down_sync(kFullMask, bb, d);
+            const long long oP = __shfl_down_sync(kFullMask, bP, d);
             if (cand_better(ok, ob, bk, bb)) {
                 bk = ok;
                 bb = ob;
+                bP = oP;
             }
         }
         if (lane == 0) {
@@ -728,7 +855,9 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
             }
             // P at the budget: the candidate's accumulator (sparse) or the scan
             if (budget > 0) {
-                if (!sparse) {
+                if (!sparse && forced < 0) {
+                    Pbud = bP;  // carried with the best candidate
+                } else if (!sparse) {
                     Pbud = __ldcg(P + budget);
                 } else if (forced >= 0) {
                     Pbud = (long long)sm.acc_s[c.n];
