@@ -138,7 +138,10 @@ __device__ __forceinline__ void norm_chunk(const uint4 &v, float &m, float &s, b
 
 // Block-wide combine of the threads' (m, s); thread 0 writes the piece's
 // partial.  Contains __syncthreads(): every thread calls it.
-__device__ void norm_block(float m, float s, float *red_m, double *red_s, NormPartial *dst) {
+// The sums travel as float pairs (hi + lo, error-free additions), so the
+// combine runs no fp64 instruction per thread (GB300's fp64 unit is small);
+// thread 0 converts the total once.
+__device__ void norm_block(float m, float s, float *red_m, float2 *red_s, NormPartial *dst) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float M = m;
 #pragma unroll
@@ -148,15 +151,26 @@ __device__ void norm_block(float m, float s, float *red_m, double *red_s, NormPa
     M = red_m[0];
 #pragma unroll
     for (int w = 1; w < kNormThreads / 32; ++w) M = fmaxf(M, red_m[w]);
-    double t = (m > -INFINITY) ? (double)(s * __expf(m - M)) : 0.0;
+    float th = (m > -INFINITY) ? s * __expf(m - M) : 0.0f, tl = 0.0f;
 #pragma unroll
-    for (int d = 16; d > 0; d >>= 1) t += __shfl_xor_sync(kFullMask, t, d);
-    if (lane == 0) red_s[warp] = t;
+    for (int d = 16; d > 0; d >>= 1) {
+        const float oh = __shfl_xor_sync(kFullMask, th, d), ol = __shfl_xor_sync(kFullMask, tl, d);
+        float h, e;
+        two_sum(th, oh, h, e);
+        e = __fadd_rn(e, __fadd_rn(tl, ol));
+        fast_two_sum(h, e, th, tl);
+    }
+    if (lane == 0) red_s[warp] = make_float2(th, tl);
     __syncthreads();
     if (threadIdx.x == 0) {
-        double S = 0.0;
-        for (int w = 0; w < kNormThreads / 32; ++w) S += red_s[w];
-        *dst = NormPartial{M, 0.0f, M > -INFINITY ? S : 0.0};
+        float Sh = 0.0f, Sl = 0.0f;
+        for (int w = 0; w < kNormThreads / 32; ++w) {
+            float h, e;
+            two_sum(Sh, red_s[w].x, h, e);
+            e = __fadd_rn(e, __fadd_rn(Sl, red_s[w].y));
+            fast_two_sum(h, e, Sh, Sl);
+        }
+        *dst = NormPartial{M, 0.0f, M > -INFINITY ? (double)Sh + (double)Sl : 0.0};
     }
     __syncthreads();
 }
@@ -187,7 +201,7 @@ template <typename T, bool VEC>
 __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) softmax_norm_kernel(SampArgs a) {
     extern __shared__ int32_t dcu[];  // [B+1]
     __shared__ float red_m[kNormThreads / 32];
-    __shared__ double red_s[kNormThreads / 32];
+    __shared__ float2 red_s[kNormThreads / 32];
     __shared__ int scan32[40];
     __shared__ long long row_off;
     __shared__ int row_draft;
@@ -295,9 +309,21 @@ __device__ __forceinline__ double row_prob(float z, float M, double S) {
     return (z == z && S > 0.0) ? (double)__expf(z - M) / S : 0.0;
 }
 
-// Weights of the bonus draw are summed exactly as integers in units of 2^-40.
+// Weights of the bonus draw are summed exactly as integers in units of 2^-40:
+// q = w * 2^40 rounded to the nearest integer, ties to even, from the bits of
+// the (exact) float product -- the value a round-to-nearest conversion
+// gives, without the conversion instruction (it runs on the fp64 unit).
 __device__ __forceinline__ unsigned long long quantize(float w) {
-    return w > 0.0f ? (unsigned long long)__float2ull_rn(w * 1099511627776.0f) : 0ull;
+    if (!(w > 0.0f)) return 0ull;
+    const unsigned bits = __float_as_uint(w * 1099511627776.0f);
+    const int e = (int)(bits >> 23) - 127;
+    const unsigned long long m = (unsigned long long)((bits & 0x7fffffu) | 0x800000u);
+    if (e >= 64) return ~0ull;         // saturates, as the conversion does
+    if (e >= 23) return m << (e - 23);
+    if (e < -1) return 0ull;           // below 1/2
+    const int sh = 23 - e;             // 1..24
+    const unsigned long long q = m >> sh, rem = m & ((1ull << sh) - 1), half = 1ull << (sh - 1);
+    return q + ((rem > half || (rem == half && (q & 1ull))) ? 1ull : 0ull);
 }
 
 struct BonusRow {
