@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs 
     const int nr = per_warp / kRound;  // rounds per warp (<= kMaxRounds: V is bounded on the host)
     for (int attempt = 0; attempt < 2; ++attempt) {
         const BonusRow b = brow;
-        constexpr int U = 2;  // rounds whose loads are in flight together
+        constexpr int U = 8;  // rounds whose loads are in flight together
         for (int k0 = 0; k0 < nr; k0 += U) {
             unsigned long long sm[U];
 #pragma unroll
