@@ -254,6 +254,28 @@ def run_reference(args):
     emit(line, args)
 
 
+def max_over_ranks(x: float, dev, world: int) -> float:
+    """The largest x over the ranks: the job's time is its slowest rank's."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], device=dev, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput: every rank processes its own units (weak
+    scaling, no data exchanged), all within the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank draws its own requests (an independent data-parallel shard)."""
+    return seed + rank
+
+
 def emit(line, args):
     s = json.dumps(line)
     print(s, flush=True)
@@ -421,7 +443,7 @@ def run_ours(args):
     _b.build()
     api.load()
 
-    step, strided = make_inputs(args.workload, args.seed + rank)
+    step, strided = make_inputs(args.workload, rank_seed(args.seed, rank))
     w = step.workload
     vs = VerifyStep(StepConfig.from_step(step), dev)
     vs.load_inputs(step)
@@ -494,10 +516,7 @@ def run_ours(args):
                         [ev_s[K - 1].elapsed_time(t_end)]) * 1e3
     clean = [i for i in range(K) if i % every != 0] or list(range(K))
     step_us = step_all[clean]
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev, world)
     status = int(vs.status.item())
 
     # ---- breakdown (outside the timed region): per call on the same stream,
@@ -696,10 +715,7 @@ def run_ours(args):
         logit_bytes = run_host(vs, io, host_logits, e2e_dev)
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, dev, world)
     e2e_ok = (np.array_equal(io.out_tokens.numpy(), vs.out_tokens.cpu().numpy())
               and int(io.status.item()) == 0)
 
@@ -723,7 +739,7 @@ def run_ours(args):
     acc_us = float(np.mean(accept_ms)) * 1e3
     achieved = accept_bytes / (acc_us * 1e-6) / 1e9
     ms_per_step = elapsed_ms / K
-    value = world * K / (elapsed_ms / 1e3)
+    value = job_rate(K, world, elapsed_ms / 1e3)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": warm, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -739,7 +755,7 @@ def run_ours(args):
                      "kernel": "dspark_greedy_accept (argmax + finalize)",
                      "bytes_per_launch": accept_bytes,
                      "traffic": ncu_traffic(w.name)},
-        "e2e": {"value": world * n_e / e2e_s, "unit": UNIT,
+        "e2e": {"value": job_rate(n_e, world, e2e_s), "unit": UNIT,
                 "h2d_bytes_per_step": io.h2d_input_bytes() + logit_bytes,
                 "d2h_bytes_per_step": io.d2h_output_bytes(), "steps": n_e,
                 "matches_device_path": bool(e2e_ok)},
