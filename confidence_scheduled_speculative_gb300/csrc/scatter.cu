@@ -24,6 +24,7 @@
 // time by all threads.
 
 #include "dspark_common.cuh"
+#include "bulk.cuh"
 
 namespace dspark {
 
@@ -31,7 +32,6 @@ constexpr int kScatterThreads = 256;    // 2-byte path
 constexpr int kBulkCtasPerSm = 3;       // 64 KB of stages each
 constexpr int kBulkStages = 4;
 constexpr int kBulkSeg = 16384;         // bytes per bulk copy
-constexpr unsigned long long kWaitLimitNs = 200000000ull;
 
 struct ScatterArgs {
     const unsigned char *src;
@@ -48,34 +48,6 @@ struct ScatterArgs {
 __device__ __forceinline__ int scatter_rows_of(const ScatterArgs &a) {
     const int rows = *a.totals;
     return rows < 0 ? 0 : (rows > a.max_rows ? a.max_rows : rows);
-}
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait for the given phase parity of an mbarrier: a non-blocking test in a
-// loop, given up after kWaitLimitNs of wall time.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    const unsigned long long start = global_ns();
-    for (;;) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            " selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(done)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if (global_ns() - start > kWaitLimitNs) return false;
-        __nanosleep(32);
-    }
 }
 
 // Segment t of the CTA's range: source row, byte offset and size (a
@@ -100,8 +72,7 @@ __global__ void __launch_bounds__(32) scatter_bulk_kernel(ScatterArgs a) {
     const long long per = (T + gridDim.x - 1) / gridDim.x;
     const long long t0 = (long long)blockIdx.x * per;
     const long long n = max(0LL, min(t0 + per, T) - t0);
-    for (int s = 0; s < kBulkStages; ++s)
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar[s])) : "memory");
+    for (int s = 0; s < kBulkStages; ++s) mbar_init(smem_addr(&bar[s]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 
     auto load = [&](long long i) {

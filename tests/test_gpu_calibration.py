@@ -159,7 +159,7 @@ def compare_stats(tag, gpu, ref):
 
 @pytest.mark.parametrize("N,gamma,M", [
     (0, 4, 10), (1, 1, 1), (255, 3, 2), (257, 8, 10), (5000, 16, 15), (70001, 8, 32),
-    (3000, 31, 10), (40000, 16, 10),
+    (3000, 31, 10), (40000, 16, 10), (2000, 31, 32),
 ])
 def test_stats_parity(orc, dev, N, gamma, M):
     z, correct, tested = _samples(N, gamma, seed=N + gamma)
@@ -242,7 +242,7 @@ def compare_fit(tag, gpu, ref):
 
 @pytest.mark.parametrize("N,gamma,J,M", [
     (0, 3, 4, 10), (1, 1, 1, 1), (300, 4, 7, 10), (4097, 8, 32, 15), (20000, 8, 64, 10),
-    (4097, 5, 256, 10), (2000, 31, 16, 32), (513, 6, 100, 3),
+    (4097, 5, 256, 10), (2000, 31, 16, 32), (513, 6, 100, 3), (1500, 31, 256, 32),
 ])
 def test_fit_parity(orc, dev, N, gamma, J, M):
     z, correct, tested = _samples(N, gamma, seed=3 * N + J)
