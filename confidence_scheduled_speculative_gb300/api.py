@@ -319,8 +319,11 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 
 def _logits_ptr(logits: torch.Tensor, V: int) -> tuple[int, int]:
-    if not logits.is_cuda or logits.dim() != 2 or logits.stride(1) != 1:
-        raise ValueError("logits: expected a 2-D CUDA tensor with unit column stride")
+    """Device or pinned host logits: pinned host memory is device-accessible
+    at the same address (unified addressing), and the kernels then read it
+    over the host link."""
+    if not (logits.is_cuda or logits.is_pinned()) or logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits: expected a 2-D CUDA or pinned tensor with unit column stride")
     if logits.size(1) < V:
         raise ValueError("logits: fewer columns than V")
     return logits.data_ptr(), logits.stride(0)

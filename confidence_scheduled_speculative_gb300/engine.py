@@ -275,15 +275,36 @@ class HostStepIO:
 
 
 def run_host(vs: VerifyStep, io: HostStepIO, host_logits: torch.Tensor,
-             dev_logits: torch.Tensor, stream=None) -> int:
+             dev_logits: torch.Tensor | None, stream=None) -> int:
     """One end-to-end compact step from pinned host buffers.
 
     ``host_logits`` (pinned, [rows, V]) holds the target logits of the packed
-    rows in packed order, standing in for the verify forward's output;
-    ``dev_logits`` is the device buffer they are copied into.  Returns the
-    number of logits bytes copied host -> device.
+    rows in packed order, standing in for the verify forward's output.  With
+    ``dev_logits`` (a device buffer) the host reads the packed total after the
+    plan and copies that many rows in; with ``dev_logits=None`` the accept
+    reads the packed rows straight from the pinned buffer over the host link
+    (no host synchronisation inside the step).  Returns the number of logits
+    bytes moved host -> device.
     """
     s = torch.cuda.current_stream() if stream is None else stream
+    if dev_logits is None:
+        with torch.cuda.stream(s):
+            vs.conf_logits.copy_(io.conf_logits, non_blocking=True)
+            vs.sts_temps.copy_(io.sts_temps, non_blocking=True)
+            vs.anchor.copy_(io.anchor, non_blocking=True)
+            vs.draft.copy_(io.draft, non_blocking=True)
+            vs.prefix_lens.copy_(io.prefix_lens, non_blocking=True)
+            vs.status.zero_()
+            vs.plan_pack(s)
+            vs.greedy_accept(host_logits, write_argmax=False, stream=s)
+            io.totals.copy_(vs.totals, non_blocking=True)
+            io.out_tokens.copy_(vs.out_tokens, non_blocking=True)
+            io.commit_lens.copy_(vs.commit_lens, non_blocking=True)
+            io.new_seq_lens.copy_(vs.new_seq_lens, non_blocking=True)
+            io.verify_lens.copy_(vs.verify_lens, non_blocking=True)
+            io.status.copy_(vs.status, non_blocking=True)
+            s.synchronize()
+        return int(io.totals[0]) * host_logits.stride(0) * host_logits.element_size()
     with torch.cuda.stream(s):
         vs.conf_logits.copy_(io.conf_logits, non_blocking=True)
         vs.sts_temps.copy_(io.sts_temps, non_blocking=True)

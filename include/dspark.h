@@ -328,7 +328,10 @@ DSPARK_API size_t dspark_accept_workspace_bytes(int32_t max_rows, int32_t V);
  * mismatch), FinalizeAcceptLens and BuildOutTokens.
  *   logits       [max_rows, ld] bf16 or fp32 (dtype), row stride ld >= V
  *                elements; 16-byte aligned base and ld*elem % 16 == 0 take
- *                the vector path, anything else a scalar path
+ *                the vector path, anything else a scalar path.  Device
+ *                memory, or pinned host memory (device-accessible at the
+ *                same address under unified addressing): the kernels then
+ *                read the packed rows over the host link, with no copy step
  *   cu_seqlens   [B+1]: request r owns packed rows [cu[r], cu[r+1]); rows
  *                = min(cu[B], max_rows) rows are read (CAPACITY if cu[B] >
  *                max_rows)

@@ -330,3 +330,35 @@ def test_stress_full_size_sampled(dev, orc):
             np.testing.assert_array_equal(gg[k][r], sub[k][0], err_msg=f"r={r} {k}")
     assert int(gg["status"][0]) == 0
     assert int(gg["commit_lens"].min()) >= 1
+
+
+def test_greedy_accept_reads_pinned_host_logits(dev, orc):
+    """The accept over packed logits in pinned host memory (read by the
+    kernels through unified addressing) equals the device-memory call."""
+    from confidence_scheduled_speculative_gb300 import api
+    rng = np.random.default_rng(21)
+    B, g, V = 24, 6, 5000
+    lens = rng.integers(1, g + 2, size=B)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    rows = int(cu[-1])
+    logits = rng.normal(size=(rows, V)).astype(np.float32)
+    draft = rng.integers(0, V, size=(B, g)).astype(np.int32)
+    for r in range(B):  # plant matches so some chains run long
+        for j in range(lens[r] - 1):
+            if rng.random() < 0.7:
+                logits[cu[r] + j, draft[r, j]] = 9.0
+    bf = torch.from_numpy(logits).to(torch.bfloat16)
+    outs = []
+    for src in (bf.to(dev), bf.pin_memory()):
+        i32 = dict(dtype=torch.int32, device=dev)
+        o = dict(num_accepted=torch.zeros(B, **i32), bonus=torch.zeros(B, **i32),
+                 commit_lens=torch.zeros(B, **i32), out_tokens=torch.zeros((B, g + 1), **i32))
+        st = torch.zeros(1, **i32)
+        ws = api.workspace(api.dspark_accept_workspace_bytes(rows, V), dev)
+        api.dspark_greedy_accept(src, V=V, cu_seqlens=torch.from_numpy(cu).to(dev),
+                                 draft=torch.from_numpy(draft).to(dev), prefix_lens=None, B=B,
+                                 gamma=g, workspace=ws, status=st, **o)
+        torch.cuda.synchronize()
+        outs.append({k: v.cpu().numpy() for k, v in o.items()} | {"status": int(st.item())})
+    for k in outs[0]:
+        np.testing.assert_array_equal(outs[0][k], outs[1][k], err_msg=k)
