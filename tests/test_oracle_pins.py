@@ -248,6 +248,23 @@ def test_cost_lookup_interpolated_edges(orc):
     assert z.status & orc.ST_BAD_COST and not z.feasible[0] and z.feasible[2]
 
 
+def test_cost_lookup_interpolated_at_samples_is_exact(orc):
+    """At a sample M = M_j the interpolated cost is val_j itself, even when
+    the segment's slope is not exact in binary (0.6 / 3 here): the
+    interpolation does not pass through the previous segment."""
+    s = _f32([[0.5, 0.25, 0.125, 0.0625, 0.03125, 0.015625, 0.0078125, 0.00390625, 0.001953125]])
+    M, val, bias, alpha = [1, 4, 7, 10], [0.1, 0.7, 0.3, 0.9], 0.2, 0.05
+    r = orc.plan_from_survivals(s, EPS_MIN, 1, 10, -1, wl.COST_ADDITIVE_INTERP, M, val,
+                                bias=bias, alpha=alpha)
+    for j, Mj in enumerate(M):
+        b = Mj - 1  # B = 1
+        assert r.theta_curve[b] == r.tau_curve[b] / ((bias + alpha) + val[j]), j
+    # between samples: val_j + (M - M_j) * slope_j in that order
+    b = 5  # M = 6, segment [4, 7)
+    slope = (val[2] - val[1]) / (M[2] - M[1])
+    assert r.theta_curve[b] == r.tau_curve[b] / ((bias + alpha) + (val[1] + (6 - 4) * slope))
+
+
 def test_invalid_cost_and_infeasible(orc):
     s = _f32([[0.5, 0.25]])
     r = orc.plan_from_survivals(s, EPS_MIN, 1, 3, -1, wl.COST_SPS_1D, [1, 2], [0.0, 5.0])
