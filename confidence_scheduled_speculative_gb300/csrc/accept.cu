@@ -96,11 +96,11 @@ __device__ __forceinline__ void scan_chunks(const uint4 *row4, int c0, int c1, f
     for (; c + (kUnroll - 1) * kArgmaxThreads < c1; c += kUnroll * kArgmaxThreads) {
         uint4 v[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream16(row4 + c + u * kArgmaxThreads);
+        for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream16_pf(row4 + c + u * kArgmaxThreads);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) chunk_step<T>(v[u], c + u * kArgmaxThreads, best, bchunk, nan);
     }
-    for (; c < c1; c += kArgmaxThreads) chunk_step<T>(ld_stream16(row4 + c), c, best, bchunk, nan);
+    for (; c < c1; c += kArgmaxThreads) chunk_step<T>(ld_stream16_pf(row4 + c), c, best, bchunk, nan);
 }
 
 // Scalar scan of elements [e0, e1) (unaligned rows).
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kArgmaxThreads, kCtasPerSm) argmax_kernel(Argm
                 bidx = c0 * EPC;
                 if (best > -INFINITY) {
                     // first element of that chunk equal to the max (-0 == +0)
-                    const uint4 v = ld_stream16(reinterpret_cast<const uint4 *>(row) + bchunk);
+                    const uint4 v = ld_stream16_pf(reinterpret_cast<const uint4 *>(row) + bchunk);
                     bidx = bchunk * EPC + EPC - 1;
 #pragma unroll
                     for (int e = EPC - 1; e >= 0; --e)

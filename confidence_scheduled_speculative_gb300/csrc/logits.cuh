@@ -17,6 +17,16 @@ __device__ __forceinline__ uint4 ld_stream16(const uint4 *p) {
     return r;
 }
 
+// The same with a 256-byte L2 prefetch per access (the argmax's pure row
+// stream: 6.58 against 6.50 TB/s back to back on dsv4_like).
+__device__ __forceinline__ uint4 ld_stream16_pf(const uint4 *p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
 __device__ __forceinline__ void take(float f, int idx, float &best, int &bidx, bool &nan) {
     if (f != f) nan = true;
     else if (f > best) {
