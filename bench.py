@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--separate-plan-pack", action="store_true",
                     help="issue dspark_plan and dspark_pack_verify instead of dspark_plan_pack")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the stress row sweep and the qwen_like cold-L2 step")
     ap.add_argument("--no-calib", action="store_true",
                     help="skip the calibration (recorder, statistics, fit) measurements")
     ap.add_argument("--event-every", type=int, default=16,
@@ -331,6 +333,98 @@ def plan_kind_timing(dev, stream, vs, kind, reps=32, table=None):
         out["us"] = ev[0].elapsed_time(ev[1]) * 1e3 / (5 * reps)
         out["budget"] = int(vs.budget.item())
         out["status"] = int(vs.status.item())
+    except Exception as e:  # report, do not fail the run
+        out["error"] = f"{type(e).__name__}: {e}"[:200]
+    return out
+
+
+def accept_rows_sweep(dev, stream, seed, reps=20):
+    """Accept bandwidth against the packed row count on the stress workload
+    (B=1024, gamma=16, V=129280): forced budgets 0..16384 step 1024 give
+    1024..17408 packed rows (0.26..4.5 GB of bf16, every point larger than
+    L2).  Per point: the real planner + pack with that forced budget, then
+    the accept calls back to back over filler logits (N(0,1) bf16; the
+    argmax results are not checked here, the parity tests do that)."""
+    import torch
+    from confidence_scheduled_speculative_gb300 import workloads as wl
+    from confidence_scheduled_speculative_gb300.engine import StepConfig, VerifyStep
+    w = wl.STRESS
+    peak = load_peaks()[0]
+    out = {"workload": f"stress B={w.B} gamma={w.gamma} V={w.V} compact, forced budgets",
+           "points": []}
+    try:
+        buf = torch.empty((w.B * (w.gamma + 1), w.V), dtype=torch.bfloat16, device=dev)
+        buf.normal_(generator=torch.Generator(device=dev).manual_seed(seed))
+        for f in range(0, w.B * w.gamma + 1, 1024):
+            step = wl.make_step(w, seed=seed, forced_budget=f)
+            vs = VerifyStep(StepConfig.from_step(step), dev)
+            vs.load_inputs(step)
+            vs.plan_pack()
+            torch.cuda.synchronize()
+            total = int(vs.totals[0].item())
+            _, _, _, acc_fn = vs.bind_compact(buf[:total])
+            for _ in range(3):
+                acc_fn()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            ev[0].record(stream)
+            for _ in range(reps):
+                acc_fn()
+            ev[1].record(stream)
+            torch.cuda.synchronize()
+            us = ev[0].elapsed_time(ev[1]) * 1e3 / reps
+            nbytes = total * w.V * w.elem_bytes
+            gbs = nbytes / (us * 1e-6) / 1e9
+            out["points"].append({"forced_budget": f, "rows": total, "accept_us": us,
+                                  "gbs": gbs, "frac": gbs / peak,
+                                  "status": int(vs.status.item())})
+            del vs
+        del buf
+    except Exception as e:  # report, do not fail the run
+        out["error"] = f"{type(e).__name__}: {e}"[:200]
+    return out
+
+
+def small_step_timing(dev, stream, name, seed, reps=50):
+    """plan + pack + accept step time of a workload whose logits fit in L2
+    (qwen_like: 256 packed rows x 151936 bf16 = 77.8 MB): a 256 MB buffer is
+    rewritten before every timed step so that each step reads its logits
+    from HBM; only the step is bracketed by events."""
+    import torch
+    from confidence_scheduled_speculative_gb300.engine import StepConfig, VerifyStep
+    out = {}
+    try:
+        step, strided = make_inputs(name, seed)
+        w = step.workload
+        vs = VerifyStep(StepConfig.from_step(step), dev)
+        vs.load_inputs(step)
+        vs.plan_pack()
+        torch.cuda.synchronize()
+        total = int(vs.totals[0].item())
+        strided_dev = torch.from_numpy(strided.view(np.int16)).to(dev).view(torch.bfloat16)
+        compact = strided_dev.index_select(0, vs.packed_src[:total].long()).contiguous()
+        plan_pack_fn, _, _, acc_fn = vs.bind_compact(compact)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            plan_pack_fn()
+            acc_fn()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+        for e in evs:
+            flush.fill_(1)
+            e[0].record(stream)
+            plan_pack_fn()
+            e[1].record(stream)
+            acc_fn()
+            e[2].record(stream)
+        torch.cuda.synchronize()
+        step_us = np.array([e[0].elapsed_time(e[2]) for e in evs]) * 1e3
+        acc_us = np.array([e[1].elapsed_time(e[2]) for e in evs]) * 1e3
+        nbytes = total * w.V * w.elem_bytes
+        out = {"workload": f"{w.name} B={w.B} gamma={w.gamma} V={w.V} compact",
+               "rows": total, "l2": "256 MB buffer rewritten before every step",
+               "step_us_p50": float(np.median(step_us)),
+               "accept_us_p50": float(np.median(acc_us)),
+               "accept_gbs": nbytes / (float(np.median(acc_us)) * 1e-6) / 1e9,
+               "status": int(vs.status.item())}
     except Exception as e:  # report, do not fail the run
         out["error"] = f"{type(e).__name__}: {e}"[:200]
     return out
@@ -680,6 +774,13 @@ def run_ours(args):
                           plan_kind_timing(dev, stream, vs, _api.COST_ADDITIVE_INTERP)}
         vs.status.zero_()
 
+    # ---- accept bandwidth against packed rows (stress workload) and the
+    # small workload whose logits fit in L2 (secondary)
+    sweep = small = None
+    if not args.no_cap and not args.no_sweep and w.name == "dsv4_like":
+        sweep = accept_rows_sweep(dev, stream, args.seed)
+        small = small_step_timing(dev, stream, "qwen_like", args.seed)
+
     # ---- cap-accept over the full strided block (secondary)
     cap = None
     if not args.no_cap:
@@ -793,6 +894,8 @@ def run_ours(args):
         "calibration": calib,
         "plan_by_cost_kind": plan_kinds,
         "cap_accept": cap,
+        "accept_by_rows": sweep,
+        "qwen_like_cold_l2": small,
         "status": status,
     }
     emit(line, args)
