@@ -28,11 +28,18 @@
 //     (as the greedy argmax does); each (CTA, row) piece leaves a partial
 //     (m, S) at slot CTA + row.  Per thread an online max / sum of exps
 //     (hardware ex2), combined per piece in fp64.
-//   sampling_accept_kernel  one CTA per request: combines the partials of its
-//     rows, runs the acceptance tests (warp 0, one lane per draft), then
-//     draws the bonus: the residual (or p) of the bonus row is summed in
-//     rounds of 256 tokens, one warp per contiguous sixteenth of the
-//     vocabulary, and the round holding u * W is searched token by token.
+//   sampling_accept_kernel  one thread-block cluster of S CTAs per request
+//     (S up to 8, as many as fill the GPU in one wave).  Every CTA combines
+//     the partials of the request's rows and runs the acceptance tests (warp
+//     0, one lane per draft), so each knows the bonus row; the residual (or
+//     p) of that row is then summed in rounds of 512 tokens (16 per lane),
+//     each warp of the cluster owning one contiguous range of rounds.  The
+//     CTAs swap their slice totals through distributed shared memory; the
+//     CTA whose slice holds u * W finds the round and the token in it and
+//     writes the request's results.
+//   Every weight is quantized per lane and round to a multiple of 2^-40 and
+//   summed as an integer, so the draw does not depend on how the rounds are
+//   split among warps and CTAs.
 // Sums of exps are fp32 per thread and fp64 beyond, so p and q agree with
 // an fp64 index-order evaluation to about 1e-6 relative: decisions can
 // differ from such an evaluation only when u * q and p (or u * W and a
@@ -46,12 +53,17 @@ namespace dspark {
 constexpr int kNormThreads = 256;
 constexpr int kNormCtasPerSm = 4;
 constexpr int kNormUnroll = 4;
-constexpr int kSampThreads = 512;
+constexpr int kSampThreads = 256;
 constexpr int kSampWarps = kSampThreads / 32;
 constexpr int kSampMaxB = 4096;   // cu_seqlens staged in shared memory by every CTA
 constexpr int kSampMaxCtas = 4096;
-constexpr int kRound = 256;       // tokens per round of the bonus draw (32 lanes x 8)
-constexpr int kMaxRounds = 256;   // rounds per warp: V / 16 / 256 for V <= 1M
+constexpr int kSampMaxV = 1 << 20;
+constexpr int kTokLane = 16;                  // tokens of one lane in a round of the bonus draw
+constexpr int kRound = 32 * kTokLane;         // tokens of one warp-round
+constexpr int kMaxRounds = kSampMaxV / kRound / kSampWarps;  // rounds per warp (one CTA per request)
+constexpr int kSampMaxCluster = 8;            // CTAs sharing one request's bonus draw
+constexpr int kSampCtasPerSm = 4;             // resident accept CTAs per SM (launch bound)
+constexpr int kBonusChunks = 4;               // 16-byte target chunks in flight per lane
 
 struct NormPartial {
     float m;     // largest logit of the piece (-inf: none)
@@ -71,6 +83,7 @@ struct SampArgs {
     NormPartial *part;  // [kSampMaxCtas + max_rows + B*gamma + 1]
     int32_t *dcu;       // [B+1] first virtual draft row of each request (written by CTA 0)
     int grid;           // normalizer grid size
+    int split;          // CTAs (one thread-block cluster) per request in the accept kernel
 };
 
 __device__ __forceinline__ int samp_rows(const SampArgs &a) {
@@ -336,76 +349,215 @@ struct BonusRow {
 // Weight of one token of the bonus draw from its target (and draft) logit;
 // a NaN logit weighs 0.
 __device__ __forceinline__ float weight_of(const BonusRow &b, float zt, float zd) {
-    float w = (zt == zt) ? ex2(fmaf(zt, kLog2e, -b.mt)) * b.inv_st : 0.0f;
+    float w = (zt == zt) ? __fmul_rn(ex2(fmaf(zt, kLog2e, -b.mt)), b.inv_st) : 0.0f;
     if (b.d) {
-        const float q = (zd == zd) ? ex2(fmaf(zd, kLog2e, -b.md)) * b.inv_sd : 0.0f;
-        w = fmaxf(w - q, 0.0f);
+        const float q = (zd == zd) ? __fmul_rn(ex2(fmaf(zd, kLog2e, -b.md)), b.inv_sd) : 0.0f;
+        w = fmaxf(__fsub_rn(w, q), 0.0f);
     }
     return w;
 }
 
-// The weights of the 8 tokens y0..y0+7 one lane handles in a round (0 past
-// V).  Aligned rows with no NaN among the 8: 16-byte loads and no per-token
-// checks; otherwise token by token.
+// The 16-byte chunks of the kTokLane tokens one lane handles in a round.
 template <typename T>
-__device__ __forceinline__ void weights8(const BonusRow &b, int y0, int V, bool vec, float (&w)[8]) {
-    constexpr int E = Elem<T>::kPerChunk, NC = 8 / E;
-    const T *rt = reinterpret_cast<const T *>(b.t);
-    const T *rd = reinterpret_cast<const T *>(b.d);
-    if (vec && y0 + 8 <= V) {
-        uint4 t[NC], d[NC];
+struct LaneChunks {
+    static constexpr int NC = kTokLane / Elem<T>::kPerChunk;
+    uint4 t[NC], d[NC];
+};
+
+// Issue the loads of tokens y0 .. y0 + kTokLane - 1 when the rows are
+// aligned and every token is in range; false selects the token-by-token
+// path.
+// HAS_D: the draft row is read too (b.d is not null).
+template <typename T, bool HAS_D>
+__device__ __forceinline__ bool lane_load(const BonusRow &b, int y0, int V, bool vec,
+                                          LaneChunks<T> &c) {
+    constexpr int NC = LaneChunks<T>::NC;
+    if (!vec || y0 + kTokLane > V) return false;
+    const uint4 *pt = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(b.t) + y0);
+#pragma unroll
+    for (int i = 0; i < NC; ++i) c.t[i] = ld_stream16(pt + i);
+    if (HAS_D) {
+        const uint4 *pd = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(b.d) + y0);
+#pragma unroll
+        for (int i = 0; i < NC; ++i) c.d[i] = ld_stream16(pd + i);
+    }
+    return true;
+}
+
+// The weights of the lane's tokens y0 .. y0 + kTokLane - 1 (0 past V): from
+// the loaded chunks when they hold no NaN, otherwise token by token.
+template <typename T>
+__device__ __forceinline__ void lane_weights(const BonusRow &b, int y0, int V, bool loaded,
+                                             const LaneChunks<T> &c, float (&w)[kTokLane]) {
+    constexpr int E = Elem<T>::kPerChunk, NC = LaneChunks<T>::NC;
+    if (loaded) {
         bool nan = false;
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            t[c] = ld_stream16(reinterpret_cast<const uint4 *>(rt + y0) + c);
-            const float mt = Elem<T>::chunk_max(t[c]);
+        for (int i = 0; i < NC; ++i) {
+            const float mt = Elem<T>::chunk_max(c.t[i]);
             nan |= mt != mt;
-            if (rd) {
-                d[c] = ld_stream16(reinterpret_cast<const uint4 *>(rd + y0) + c);
-                const float md = Elem<T>::chunk_max(d[c]);
+            if (b.d) {
+                const float md = Elem<T>::chunk_max(c.d[i]);
                 nan |= md != md;
             }
         }
         if (!nan) {
-            if (rd) {
+            if (b.d) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float p = ex2(fmaf(Elem<T>::at(t[e / E], e % E), kLog2e, -b.mt)) * b.inv_st;
-                    const float q = ex2(fmaf(Elem<T>::at(d[e / E], e % E), kLog2e, -b.md)) * b.inv_sd;
-                    w[e] = fmaxf(p - q, 0.0f);
+                for (int e = 0; e < kTokLane; ++e) {
+                    const float p = __fmul_rn(ex2(fmaf(Elem<T>::at(c.t[e / E], e % E), kLog2e, -b.mt)), b.inv_st);
+                    const float q = __fmul_rn(ex2(fmaf(Elem<T>::at(c.d[e / E], e % E), kLog2e, -b.md)), b.inv_sd);
+                    w[e] = fmaxf(__fsub_rn(p, q), 0.0f);
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    w[e] = ex2(fmaf(Elem<T>::at(t[e / E], e % E), kLog2e, -b.mt)) * b.inv_st;
+                for (int e = 0; e < kTokLane; ++e)
+                    w[e] = __fmul_rn(ex2(fmaf(Elem<T>::at(c.t[e / E], e % E), kLog2e, -b.mt)), b.inv_st);
             }
             return;
         }
     }
+    const T *rt = reinterpret_cast<const T *>(b.t);
+    const T *rd = reinterpret_cast<const T *>(b.d);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
+    for (int e = 0; e < kTokLane; ++e) {
         const int y = y0 + e;
         w[e] = y < V ? weight_of(b, Elem<T>::load(rt + y), rd ? Elem<T>::load(rd + y) : 0.0f) : 0.0f;
     }
 }
 
-// A lane's round total: the fp32 sum of its 8 weights in token order,
-// quantized once.
-__device__ __forceinline__ unsigned long long lane_total(const float (&w)[8]) {
+// A lane's round total: the fp32 sum of its weights in token order (at most
+// kTokLane = 16), quantized once (below 2^45 units).
+__device__ __forceinline__ unsigned long long lane_total(const float (&w)[kTokLane]) {
     float acc = 0.0f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc += w[e];
+    for (int e = 0; e < kTokLane; ++e) acc = __fadd_rn(acc, w[e]);
     return quantize(acc);
 }
 
+// The same total straight from the loaded chunks (the weights are added as
+// they are made, in the same order, so the sum is lane_total's).
+template <typename T, bool HAS_D>
+__device__ __forceinline__ unsigned long long lane_total_of(const BonusRow &b, int y0, int V,
+                                                           bool loaded, const LaneChunks<T> &c) {
+    constexpr int E = Elem<T>::kPerChunk, NC = LaneChunks<T>::NC;
+    if (loaded) {
+        bool nan = false;
+#pragma unroll
+        for (int i = 0; i < NC; ++i) {
+            const float mt = Elem<T>::chunk_max(c.t[i]);
+            nan |= mt != mt;
+            if (HAS_D) {
+                const float md = Elem<T>::chunk_max(c.d[i]);
+                nan |= md != md;
+            }
+        }
+        if (!nan) {
+            float acc = 0.0f;
+            if (HAS_D) {
+#pragma unroll
+                for (int e = 0; e < kTokLane; ++e) {
+                    const float p = __fmul_rn(ex2(fmaf(Elem<T>::at(c.t[e / E], e % E), kLog2e, -b.mt)), b.inv_st);
+                    const float q = __fmul_rn(ex2(fmaf(Elem<T>::at(c.d[e / E], e % E), kLog2e, -b.md)), b.inv_sd);
+                    acc = __fadd_rn(acc, fmaxf(__fsub_rn(p, q), 0.0f));
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < kTokLane; ++e)
+                    acc = __fadd_rn(acc, __fmul_rn(ex2(fmaf(Elem<T>::at(c.t[e / E], e % E), kLog2e, -b.mt)), b.inv_st));
+            }
+            return quantize(acc);
+        }
+    }
+    float w[kTokLane];
+    lane_weights<T>(b, y0, V, false, c, w);
+    return lane_total(w);
+}
+
+// The warp's sum of the lanes' round totals: each total is split at bit 22
+// into two parts below 2^23, so that 32 of each sum exactly in a 32-bit warp
+// reduction.
+__device__ __forceinline__ unsigned long long warp_round_total(unsigned long long q) {
+    const unsigned lo = __reduce_add_sync(kFullMask, (unsigned)q & 0x3FFFFFu);
+    const unsigned hi = __reduce_add_sync(kFullMask, (unsigned)(q >> 22));
+    return ((unsigned long long)hi << 22) + lo;
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(kFullMask, v, d);
+    return v;
+}
+
+// ---- the thread-block cluster of one request (PTX: %cluster_ctarank,
+// barrier.cluster, mapa + ld.shared::cluster)
+
+__device__ __forceinline__ unsigned cluster_rank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster: writes before it (shared memory
+// included) are visible to the whole cluster after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// A 64-bit value at the same shared-memory offset in the CTA of the given
+// cluster rank.
+__device__ __forceinline__ unsigned long long ld_cluster_u64(const void *local, unsigned rank) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(local);
+    unsigned ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    unsigned long long v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(ra) : "memory");
+    return v;
+}
+
+// This CTA's share of the bonus draw's round sums: the request's rounds
+// (kRound tokens each, in token order) are cut into one contiguous range of
+// rpw rounds per warp of the cluster, CTA rank q holding warps q*kSampWarps..;
+// rsum[w * rpw + k] = round k of warp w (0 past the row).
+template <typename T, bool HAS_D>
+__device__ __forceinline__ void bonus_rounds(const BonusRow &b, int V, bool vec, int q, int rpw,
+                                             unsigned long long *rsum) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // rounds in flight per lane: kBonusChunks 16-byte chunks of the rows read
+    constexpr int U = kBonusChunks / (LaneChunks<T>::NC * (HAS_D ? 2 : 1)) > 0
+                          ? kBonusChunks / (LaneChunks<T>::NC * (HAS_D ? 2 : 1)) : 1;
+    const int first = (q * kSampWarps + warp) * rpw;     // first round of this warp
+    for (int k0 = 0; k0 < rpw; k0 += U) {
+        LaneChunks<T> c[U];
+        bool ld[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            ld[u] = k0 + u < rpw &&
+                    lane_load<T, HAS_D>(b, (first + k0 + u) * kRound + lane * kTokLane, V, vec, c[u]);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (k0 + u < rpw) {  // warp-uniform
+                const unsigned long long t = warp_round_total(
+                    lane_total_of<T, HAS_D>(b, (first + k0 + u) * kRound + lane * kTokLane, V, ld[u], c[u]));
+                if (lane == 0) rsum[warp * rpw + k0 + u] = t;
+            }
+        }
+    }
+}
+
 template <typename T>
-__global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs a, int epc, bool vec) {
-    __shared__ unsigned long long rsum[kSampWarps * kMaxRounds];  // weight of each round
+__global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sampling_accept_kernel(SampArgs a, int epc, bool vec) {
+    __shared__ unsigned long long rsum[kSampWarps * kMaxRounds];  // this CTA's round sums
     __shared__ BonusRow brow;
-    __shared__ int s_correct, s_round, s_retry;
-    __shared__ unsigned long long s_pre, s_target;
+    __shared__ int s_correct;
+    __shared__ unsigned long long s_slice;      // this CTA's total (read by the cluster)
+    __shared__ unsigned long long s_W, s_before;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int r = blockIdx.x;
+    const int S = a.split;
+    const int r = blockIdx.x / S;
+    const int q = (int)cluster_rank();  // == blockIdx.x % S
     const int G = a.gamma, V = a.V;
     // drafts and uniforms are step inputs: fetch them before the wait
     const int dj = (warp == 0 && lane < G) ? __ldg(a.draft + (size_t)r * G + lane) : -1;
@@ -415,9 +567,10 @@ __global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs 
 
     const int rows = samp_rows(a);
     const int lo = a.cu[r], hi = a.cu[r + 1], L = hi - lo;
-    if (warp == 0 && __any_sync(kFullMask, lane < G && (dj < 0 || dj >= V)) && lane == 0)
+    if (q == 0 && warp == 0 && __any_sync(kFullMask, lane < G && (dj < 0 || dj >= V)) && lane == 0)
         flag(a.status, DSPARK_STATUS_TOKEN_RANGE);
-    if (!samp_valid(lo, hi, rows, G)) {
+    if (!samp_valid(lo, hi, rows, G)) {  // the whole cluster leaves here
+        if (q != 0) return;
         if (tid == 0) {
             flag(a.status, DSPARK_STATUS_BAD_LEN);
             a.num_acc[r] = 0;
@@ -434,7 +587,8 @@ __global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs 
     const long long per = (W + a.grid - 1) / a.grid;
     const int vd0 = rows + a.dcu[r];  // virtual row of this request's first tested draft
 
-    // (1) acceptance tests: lane j tests draft j < L - 1
+    // (1) acceptance tests, in every CTA of the cluster (each needs the
+    // bonus row): lane j tests draft j < L - 1
     if (warp == 0) {
         bool accept = true;
         if (lane < L - 1) {
@@ -447,8 +601,8 @@ __global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs 
                 const T *zt = reinterpret_cast<const T *>(a.tgt) + (long long)(lo + lane) * a.ld_t;
                 const T *zd = reinterpret_cast<const T *>(a.dft) + ((long long)r * G + lane) * a.ld_d;
                 const double p = row_prob(Elem<T>::load(zt + dj), mt, st);
-                const double q = row_prob(Elem<T>::load(zd + dj), md, sd);
-                accept = (double)uj * q < p;
+                const double qd = row_prob(Elem<T>::load(zd + dj), md, sd);
+                accept = (double)uj * qd < p;
             }
         }
         const unsigned rej = __ballot_sync(kFullMask, !accept);
@@ -471,36 +625,60 @@ __global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs 
     }
     __syncthreads();
     const int correct = s_correct;
+    BonusRow b = brow;
 
-    // (2) the bonus draw: round sums of the quantized weights, one warp per
-    // contiguous share of the vocabulary; an empty residual draws from p
-    const int per_warp = (int)((((long long)V + kSampWarps - 1) / kSampWarps + kRound - 1) / kRound) * kRound;
-    const int nr = per_warp / kRound;  // rounds per warp (<= kMaxRounds: V is bounded on the host)
+    // (2) the bonus draw.  Round sums of the quantized weights over this
+    // CTA's slice of the vocabulary; the slice totals are exchanged through
+    // the cluster's shared memory, so every CTA knows the total W and the
+    // weight before its slice.  An empty residual draws from p (the whole
+    // cluster takes the same decision from the same W).
+    const int R = (V + kRound - 1) / kRound;
+    const int rpw = (R + S * kSampWarps - 1) / (S * kSampWarps);  // <= kMaxRounds
+    const int nt = kSampWarps * rpw;
     for (int attempt = 0; attempt < 2; ++attempt) {
-        const BonusRow b = brow;
-        constexpr int U = 8;  // rounds whose loads are in flight together
-        for (int k0 = 0; k0 < nr; k0 += U) {
-            unsigned long long sm[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                float w[8];
-                weights8<T>(b, warp * per_warp + (k0 + u) * kRound + lane * 8, (k0 + u < nr) ? V : 0,
-                            vec, w);
-                sm[u] = lane_total(w);
-            }
-#pragma unroll
-            for (int d = 16; d > 0; d >>= 1)
-#pragma unroll
-                for (int u = 0; u < U; ++u) sm[u] += __shfl_xor_sync(kFullMask, sm[u], d);
-            if (lane == 0)
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-                    if (k0 + u < nr) rsum[warp * nr + k0 + u] = sm[u];
-        }
+        if (b.d) bonus_rounds<T, true>(b, V, vec, q, rpw, rsum);
+        else bonus_rounds<T, false>(b, V, vec, q, rpw, rsum);
         __syncthreads();
-        // warp 0: the total, the target u * W, and the round it falls in
         if (warp == 0) {
-            const int nt = kSampWarps * nr;
+            unsigned long long m = 0ull;
+            for (int i = lane; i < nt; i += 32) m += rsum[i];
+            m = warp_sum_u64(m);
+            if (lane == 0) s_slice = m;
+        }
+        cluster_sync();  // every slice total is written
+        if (warp == 0) {
+            const unsigned long long v = lane < S ? ld_cluster_u64(&s_slice, (unsigned)lane) : 0ull;
+            unsigned long long incl = v;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const unsigned long long o = __shfl_up_sync(kFullMask, incl, d);
+                if (lane >= d) incl += o;
+            }
+            const unsigned long long before = __shfl_sync(kFullMask, incl - v, q);
+            const unsigned long long tot = __shfl_sync(kFullMask, incl, 31);
+            if (lane == 0) {
+                s_W = tot;
+                s_before = before;
+            }
+        }
+        cluster_sync();  // every remote read is done: s_slice may be rewritten or freed
+        if (!(s_W < kEmptyResidual && b.d != nullptr)) break;
+        b.d = nullptr;  // p == q within the sums' precision: draw from p
+    }
+    const unsigned long long Wq = s_W, before = s_before;
+    const unsigned long long target = (unsigned long long)((double)__ldg(a.u_bonus + r) * (double)Wq);
+    const bool owner = target >= before && target - before < s_slice;
+    // the CTA whose slice holds u * W writes the request's results; when no
+    // slice holds it (W = 0), rank 0 does, with no bonus token
+    if (!owner && !(q == 0 && !(target < Wq))) return;
+
+    // (3) warp 0 of the writing CTA: the round, then the token within it;
+    // then FinalizeAcceptLens and BuildOutTokens
+    if (warp == 0) {
+        int round = -1;
+        unsigned long long pre = 0ull;
+        if (owner) {
+            const unsigned long long lt = target - before;  // within this slice
             const int nb = (nt + 31) / 32;
             unsigned long long mine = 0ull;
             for (int i = lane * nb; i < min(nt, (lane + 1) * nb); ++i) mine += rsum[i];
@@ -510,57 +688,33 @@ __global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs 
                 const unsigned long long o = __shfl_up_sync(kFullMask, incl, d);
                 if (lane >= d) incl += o;
             }
-            const unsigned long long Wq = __shfl_sync(kFullMask, incl, 31);
-            if (Wq < kEmptyResidual && brow.d != nullptr) {  // p == q within the sums' precision
-                if (lane == 0) {
-                    brow.d = nullptr;
-                    s_retry = 1;
-                }
-            } else {
-                const unsigned long long target =
-                    (unsigned long long)((double)__ldg(a.u_bonus + r) * (double)Wq);
-                const unsigned found = __ballot_sync(kFullMask, incl > target);
-                int round = -1;
-                unsigned long long pre = 0ull;
-                if (found) {
-                    const int fl = __ffs(found) - 1;
-                    if (lane == fl) {
-                        unsigned long long c = incl - mine;
-                        for (int i = lane * nb; i < min(nt, (lane + 1) * nb); ++i) {
-                            if (c + rsum[i] > target) {
-                                round = i;
-                                break;
-                            }
-                            c += rsum[i];
+            const unsigned found = __ballot_sync(kFullMask, incl > lt);
+            if (found) {
+                const int fl = __ffs(found) - 1;
+                if (lane == fl) {
+                    unsigned long long c = incl - mine;
+                    for (int i = lane * nb; i < min(nt, (lane + 1) * nb); ++i) {
+                        if (c + rsum[i] > lt) {
+                            round = i;
+                            break;
                         }
-                        pre = c;
+                        c += rsum[i];
                     }
-                    round = __shfl_sync(kFullMask, round, fl);
-                    pre = __shfl_sync(kFullMask, pre, fl);
+                    pre = c;
                 }
-                if (lane == 0) {
-                    s_retry = 0;
-                    s_round = round;
-                    s_pre = pre;
-                    s_target = target;
-                }
+                round = __shfl_sync(kFullMask, round, fl);
+                pre = __shfl_sync(kFullMask, pre, fl);
             }
         }
-        __syncthreads();
-        if (!s_retry) break;
-    }
-
-    // (3) warp 0: the token within the round; then FinalizeAcceptLens and
-    // BuildOutTokens
-    if (warp == 0) {
-        const int round = s_round;
         int tok = -1;
         if (round >= 0) {
-            const BonusRow b = brow;
-            const int rw = round / nr, k = round - rw * nr;
-            const int y0 = rw * per_warp + k * kRound + lane * 8;
-            float w[8];
-            weights8<T>(b, y0, V, vec, w);
+            const unsigned long long lt = target - before;
+            const int rw = round / rpw, k = round - rw * rpw;
+            const int y0 = ((q * kSampWarps + rw) * rpw + k) * kRound + lane * kTokLane;
+            LaneChunks<T> c;
+            const bool ld = b.d ? lane_load<T, true>(b, y0, V, vec, c) : lane_load<T, false>(b, y0, V, vec, c);
+            float w[kTokLane];
+            lane_weights<T>(b, y0, V, ld, c, w);
             const unsigned long long mine = lane_total(w);
             unsigned long long incl = mine;
 #pragma unroll
@@ -568,17 +722,16 @@ __global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs 
                 const unsigned long long o = __shfl_up_sync(kFullMask, incl, d);
                 if (lane >= d) incl += o;
             }
-            const unsigned long long target = s_target, pre = s_pre;
-            const unsigned found = __ballot_sync(kFullMask, pre + incl > target);
+            const unsigned found = __ballot_sync(kFullMask, pre + incl > lt);
             if (found) {
                 const int fl = __ffs(found) - 1;
                 if (lane == fl) {
                     // the same fp32 running sum as lane_total, quantized per prefix
                     const unsigned long long base = pre + incl - mine;
                     float acc = 0.0f;
-                    for (int e = 0; e < 8; ++e) {
-                        acc += w[e];
-                        if (base + quantize(acc) > target) {
+                    for (int e = 0; e < kTokLane; ++e) {
+                        acc = __fadd_rn(acc, w[e]);
+                        if (base + quantize(acc) > lt) {
                             tok = y0 + e;
                             break;
                         }
@@ -598,8 +751,6 @@ __global__ void __launch_bounds__(kSampThreads) sampling_accept_kernel(SampArgs 
     }
 }
 
-constexpr int kSampMaxV = kSampWarps * kMaxRounds * kRound;
-
 size_t samp_partial_bytes(int max_rows, int B, int gamma) {
     const size_t slots = (size_t)kSampMaxCtas + (size_t)max_rows + (size_t)B * gamma + 1;
     return (slots * sizeof(NormPartial) + 255) & ~size_t(255);
@@ -612,7 +763,8 @@ cudaError_t launch_sampling(const SampArgs &a, bool vec, cudaStream_t s) {
                         : launch_pdl(softmax_norm_kernel<T, false>, dim3(a.grid), dim3(kNormThreads), smem, s, a);
     if (e != cudaSuccess) return e;
     const int epc = vec ? Elem<T>::kPerChunk : 1;
-    return launch_pdl(sampling_accept_kernel<T>, dim3(a.B), dim3(kSampThreads), 0, s, a, epc, vec);
+    return launch_pdl_cluster(sampling_accept_kernel<T>, dim3(a.B * a.split), dim3(kSampThreads), 0, s,
+                              a.split, a, epc, vec);
 }
 
 }  // namespace dspark
@@ -671,6 +823,10 @@ extern "C" int dspark_sampling_accept(const void *target_logits, int32_t dtype, 
                                         samp_partial_bytes(max_rows, B, gamma));
     const int g = sm_count() * kNormCtasPerSm;
     a.grid = g < 1 ? 1 : (g > kSampMaxCtas ? kSampMaxCtas : g);
+    // the accept kernel: as many CTAs per request as stay resident together
+    // (one wave), at most one cluster's worth
+    const int split = sm_count() * kSampCtasPerSm / B;
+    a.split = split < 1 ? 1 : (split > kSampMaxCluster ? kSampMaxCluster : split);
     const bool vec = aligned(target_logits, 16) && aligned(draft_logits, 16) &&
                      (ld_t * esize) % 16 == 0 && (ld_d * esize) % 16 == 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
