@@ -25,9 +25,12 @@
 //     exp(z - m).  The target rows, then the draft rows in (request, depth)
 //     order, form one list of "virtual rows", flattened into 16-byte chunks
 //     and split into one equal contiguous range per CTA of a persistent grid
-//     (as the greedy argmax does); each (CTA, row) piece leaves a partial
-//     (m, S) at slot CTA + row.  Per thread an online max / sum of exps
-//     (hardware ex2), combined per piece in fp64.
+//     (as the greedy argmax does); each warp leaves a partial (m, S) of
+//     each (CTA, row) piece, so no block barrier separates one row from the
+//     next; at its end the CTA folds each piece's warp partials into one at
+//     slot CTA + row.  Per thread an online max / sum of exps (hardware
+//     ex2), float-pair sums per warp and piece; the accept kernel combines
+//     a row's partials in fp64.
 //   sampling_accept_kernel  one thread-block cluster of S CTAs per request
 //     (S up to 8, as many as fill the GPU in one wave).  Every CTA combines
 //     the partials of the request's rows and runs the acceptance tests (warp
@@ -65,10 +68,13 @@ constexpr int kSampMaxCluster = 8;            // CTAs sharing one request's bonu
 constexpr int kSampCtasPerSm = 4;             // resident accept CTAs per SM (launch bound)
 constexpr int kBonusChunks = 4;               // 16-byte target chunks in flight per lane
 
-struct NormPartial {
-    float m;     // largest logit of the piece (-inf: none)
+constexpr int kNormWarps = kNormThreads / 32;
+
+// One warp's share of one (CTA, row) piece.
+struct __align__(16) NormPartial {
+    float m;       // largest logit the warp read (-inf: none)
+    float sh, sl;  // sum of exp(z - m) over them, as a float pair sh + sl
     float pad;
-    double s;    // sum of exp(z - m) over the piece
 };
 
 struct SampArgs {
@@ -80,7 +86,8 @@ struct SampArgs {
     const int32_t *cu, *draft, *prefix;
     const float *u_acc, *u_bonus;
     int32_t *num_acc, *bonus, *commit, *new_seq, *out, *status;
-    NormPartial *part;  // [kSampMaxCtas + max_rows + B*gamma + 1]
+    NormPartial *part;    // [kSampMaxCtas + max_rows + B*gamma + 1]: one per (CTA, row) piece
+    NormPartial *part_w;  // [(kSampMaxCtas + max_rows + B*gamma + 1) * kNormWarps]: per warp
     int32_t *dcu;       // [B+1] first virtual draft row of each request (written by CTA 0)
     int grid;           // normalizer grid size
     int split;          // CTAs (one thread-block cluster) per request in the accept kernel
@@ -149,22 +156,15 @@ __device__ __forceinline__ void norm_chunk(const uint4 &v, float &m, float &s, b
     }
 }
 
-// Block-wide combine of the threads' (m, s); thread 0 writes the piece's
-// partial.  Contains __syncthreads(): every thread calls it.
-// The sums travel as float pairs (hi + lo, error-free additions), so the
-// combine runs no fp64 instruction per thread (GB300's fp64 unit is small);
-// thread 0 converts the total once.
-__device__ void norm_block(float m, float s, float *red_m, float2 *red_s, NormPartial *dst) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Warp-wide combine of the lanes' (m, s); lane 0 writes the warp's partial
+// of the piece.  The sums travel as float pairs (hi + lo, error-free
+// additions): no fp64 instruction in the streaming kernel (GB300's fp64
+// unit is small), no block barrier between pieces.
+__device__ __forceinline__ void norm_warp(float m, float s, NormPartial *dst) {
     float M = m;
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, d));
-    if (lane == 0) red_m[warp] = M;
-    __syncthreads();
-    M = red_m[0];
-#pragma unroll
-    for (int w = 1; w < kNormThreads / 32; ++w) M = fmaxf(M, red_m[w]);
-    float th = (m > -INFINITY) ? s * __expf(m - M) : 0.0f, tl = 0.0f;
+    float th = (m > -INFINITY) ? s * ex2((m - M) * kLog2e) : 0.0f, tl = 0.0f;
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) {
         const float oh = __shfl_xor_sync(kFullMask, th, d), ol = __shfl_xor_sync(kFullMask, tl, d);
@@ -173,19 +173,31 @@ __device__ void norm_block(float m, float s, float *red_m, float2 *red_s, NormPa
         e = __fadd_rn(e, __fadd_rn(tl, ol));
         fast_two_sum(h, e, th, tl);
     }
-    if (lane == 0) red_s[warp] = make_float2(th, tl);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float Sh = 0.0f, Sl = 0.0f;
-        for (int w = 0; w < kNormThreads / 32; ++w) {
-            float h, e;
-            two_sum(Sh, red_s[w].x, h, e);
-            e = __fadd_rn(e, __fadd_rn(Sl, red_s[w].y));
-            fast_two_sum(h, e, Sh, Sl);
-        }
-        *dst = NormPartial{M, 0.0f, M > -INFINITY ? (double)Sh + (double)Sl : 0.0};
+    if ((threadIdx.x & 31) == 0) *dst = NormPartial{M, th, tl, 0.0f};
+}
+
+// Warp-wide fold of one partial per lane (lanes past the piece's warps hold
+// m = -inf, s = 0); lane 0 writes the result.
+__device__ __forceinline__ void norm_fold(const NormPartial &p, NormPartial *dst) {
+    float M = p.m;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, d));
+    float th = 0.0f, tl = 0.0f;
+    if (p.m > -INFINITY) {
+        const float e = ex2((p.m - M) * kLog2e);  // 1 for the largest
+        th = __fmul_rn(p.sh, e);
+        tl = fmaf(p.sh, e, -th);  // the product's rounding error
+        tl = fmaf(p.sl, e, tl);
     }
-    __syncthreads();
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+        const float oh = __shfl_xor_sync(kFullMask, th, d), ol = __shfl_xor_sync(kFullMask, tl, d);
+        float h, e;
+        two_sum(th, oh, h, e);
+        e = __fadd_rn(e, __fadd_rn(tl, ol));
+        fast_two_sum(h, e, th, tl);
+    }
+    if ((threadIdx.x & 31) == 0) *dst = NormPartial{M, th, tl, 0.0f};
 }
 
 // Virtual row v: a packed target row (v < rows) or the draft row of the
@@ -213,11 +225,7 @@ __device__ __forceinline__ long long virtual_row(const SampArgs &a, const int32_
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) softmax_norm_kernel(SampArgs a) {
     extern __shared__ int32_t dcu[];  // [B+1]
-    __shared__ float red_m[kNormThreads / 32];
-    __shared__ float2 red_s[kNormThreads / 32];
     __shared__ int scan32[40];
-    __shared__ long long row_off;
-    __shared__ int row_draft;
     constexpr int EPC = VEC ? Elem<T>::kPerChunk : 1;
     const int tid = threadIdx.x;
     const int B = a.B, G = a.gamma;
@@ -260,13 +268,9 @@ __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) softmax_norm_ker
         const int c0 = (int)(q - (long long)v * cpr);
         const long long seg_end = min(q1, (long long)(v + 1) * cpr);
         const int c1 = c0 + (int)(seg_end - q);
-        if (tid == 0) {
-            bool is_draft;
-            row_off = virtual_row(a, dcu, rows, v, is_draft);
-            row_draft = is_draft ? 1 : 0;
-        }
-        __syncthreads();
-        const T *row = reinterpret_cast<const T *>(row_draft ? a.dft : a.tgt) + row_off;
+        bool is_draft;
+        const long long row_off = virtual_row(a, dcu, rows, v, is_draft);  // every thread
+        const T *row = reinterpret_cast<const T *>(is_draft ? a.dft : a.tgt) + row_off;
         float m = -INFINITY, s = 0.0f;
         if (VEC) {
             const uint4 *row4 = reinterpret_cast<const uint4 *>(row);
@@ -294,10 +298,21 @@ __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) softmax_norm_ker
                 norm_take(z, m, s);
             }
         }
-        norm_block(m, s, red_m, red_s, a.part + blockIdx.x + v);
+        norm_warp(m, s, a.part_w + (size_t)(blockIdx.x + v) * kNormWarps + (tid >> 5));
         q = seg_end;
     }
     if (__syncthreads_or(nan) && tid == 0) flag(a.status, DSPARK_STATUS_NAN_LOGIT);
+    // the warps' partials of each piece of this CTA, folded into one (warp
+    // j % kNormWarps folds piece j; lane w reads warp w's partial)
+    if (q0 < q1) {
+        const int v0 = (int)(q0 / cpr), v1 = (int)((q1 - 1) / cpr);
+        const int lane = tid & 31;
+        for (int v = v0 + (tid >> 5); v <= v1; v += kNormWarps) {
+            NormPartial p = NormPartial{-INFINITY, 0.0f, 0.0f, 0.0f};
+            if (lane < kNormWarps) p = a.part_w[(size_t)(blockIdx.x + v) * kNormWarps + lane];
+            norm_fold(p, a.part + blockIdx.x + v);
+        }
+    }
 }
 
 // ---------------------------------------------------- acceptance and bonus
@@ -313,7 +328,7 @@ __device__ __forceinline__ void row_stats(const NormPartial *part, long long cpr
     if (M > -INFINITY)
         for (int c = c_lo; c <= c_hi; ++c) {
             const NormPartial p = part[c + v];
-            if (p.m > -INFINITY) S += p.s * (double)__expf(p.m - M);
+            if (p.m > -INFINITY) S += ((double)p.sh + (double)p.sl) * (double)__expf(p.m - M);
         }
 }
 
@@ -753,7 +768,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sampling_accept_
 
 size_t samp_partial_bytes(int max_rows, int B, int gamma) {
     const size_t slots = (size_t)kSampMaxCtas + (size_t)max_rows + (size_t)B * gamma + 1;
-    return (slots * sizeof(NormPartial) + 255) & ~size_t(255);
+    return (slots * (1 + kNormWarps) * sizeof(NormPartial) + 255) & ~size_t(255);
 }
 
 template <typename T>
@@ -819,6 +834,10 @@ extern "C" int dspark_sampling_accept(const void *target_logits, int32_t dtype, 
     a.out = out_tokens;
     a.status = status;
     a.part = static_cast<NormPartial *>(workspace);
+    {
+        const size_t slots = (size_t)kSampMaxCtas + (size_t)max_rows + (size_t)B * gamma + 1;
+        a.part_w = a.part + slots;
+    }
     a.dcu = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) +
                                         samp_partial_bytes(max_rows, B, gamma));
     const int g = sm_count() * kNormCtasPerSm;
