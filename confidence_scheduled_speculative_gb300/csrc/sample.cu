@@ -521,15 +521,23 @@ __device__ __forceinline__ void cluster_sync() {
         "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// A 64-bit value at the same shared-memory offset in the CTA of the given
-// cluster rank.
-__device__ __forceinline__ unsigned long long ld_cluster_u64(const void *local, unsigned rank) {
+// The two halves of a cluster barrier: every CTA arrives early, so that by
+// the wait every CTA of the cluster is known to run (the condition for
+// touching another CTA's shared memory).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Store a 64-bit value at the same shared-memory offset in the CTA of the
+// given cluster rank.
+__device__ __forceinline__ void st_cluster_u64(void *local, unsigned rank, unsigned long long v) {
     const unsigned a = (unsigned)__cvta_generic_to_shared(local);
     unsigned ra;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-    unsigned long long v;
-    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(ra) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(ra), "l"(v) : "memory");
 }
 
 // This CTA's share of the bonus draw's round sums: the request's rounds
@@ -567,8 +575,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sampling_accept_
     __shared__ unsigned long long rsum[kSampWarps * kMaxRounds];  // this CTA's round sums
     __shared__ BonusRow brow;
     __shared__ int s_correct;
-    __shared__ unsigned long long s_slice;      // this CTA's total (read by the cluster)
-    __shared__ unsigned long long s_W, s_before;
+    __shared__ unsigned long long s_tot[kSampMaxCluster];  // slice totals, written by the cluster
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int S = a.split;
     const int r = blockIdx.x / S;
@@ -596,6 +603,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sampling_accept_
         if (warp == 0 && lane <= G) a.out[(size_t)r * (G + 1) + lane] = lane < G ? dj : -1;
         return;
     }
+    cluster_arrive_relaxed();  // waited for before the first remote store
     const int D = a.dcu[a.B];
     const long long cpr = (V + epc - 1) / epc;
     const long long W = (long long)(rows + D) * cpr;
@@ -603,39 +611,47 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sampling_accept_
     const int vd0 = rows + a.dcu[r];  // virtual row of this request's first tested draft
 
     // (1) acceptance tests, in every CTA of the cluster (each needs the
-    // bonus row): lane j tests draft j < L - 1
+    // bonus row).  Lane j: the statistics of target row lo + j (j < L: the
+    // tests and any bonus row) and of draft row j (j < L - 1), all in
+    // parallel; lane j < L - 1 tests draft j.
     if (warp == 0) {
+        const bool has_t = lane < L, has_d = lane < L - 1;
+        const bool tok_ok = dj >= 0 && dj < V;
+        float zt = 0.0f, zd = 0.0f;  // the two logits the test reads, fetched first
+        if (has_d && tok_ok) {
+            zt = Elem<T>::load(reinterpret_cast<const T *>(a.tgt) + (long long)(lo + lane) * a.ld_t + dj);
+            zd = Elem<T>::load(reinterpret_cast<const T *>(a.dft) + ((long long)r * G + lane) * a.ld_d + dj);
+        }
+        float mt = -INFINITY, md = -INFINITY;
+        double st = 0.0, sd = 0.0;
+        if (has_t) row_stats(a.part, cpr, per, lo + lane, mt, st);
+        if (has_d) row_stats(a.part, cpr, per, vd0 + lane, md, sd);
+        const float inv_t = st > 0.0 ? (float)(1.0 / st) : 0.0f;
+        const float inv_d = sd > 0.0 ? (float)(1.0 / sd) : 0.0f;
         bool accept = true;
-        if (lane < L - 1) {
+        if (has_d) {
             accept = false;
-            if (dj >= 0 && dj < V) {
-                float mt, md;
-                double st, sd;
-                row_stats(a.part, cpr, per, lo + lane, mt, st);
-                row_stats(a.part, cpr, per, vd0 + lane, md, sd);
-                const T *zt = reinterpret_cast<const T *>(a.tgt) + (long long)(lo + lane) * a.ld_t;
-                const T *zd = reinterpret_cast<const T *>(a.dft) + ((long long)r * G + lane) * a.ld_d;
-                const double p = row_prob(Elem<T>::load(zt + dj), mt, st);
-                const double qd = row_prob(Elem<T>::load(zd + dj), md, sd);
-                accept = (double)uj * qd < p;
+            if (tok_ok) {
+                // p = et / st, q = ed / sd; u q < p  <=>  u ed st < et sd
+                const double et = (zt == zt && st > 0.0) ? (double)__expf(zt - mt) : 0.0;
+                const double ed = (zd == zd && sd > 0.0) ? (double)__expf(zd - md) : 0.0;
+                accept = et > 0.0 && (ed == 0.0 || (double)uj * ed * st < et * sd);
             }
         }
         const unsigned rej = __ballot_sync(kFullMask, !accept);
         const int correct = rej ? __ffs(rej) - 1 : L - 1;
+        const float bmt = __shfl_sync(kFullMask, mt, correct), bit = __shfl_sync(kFullMask, inv_t, correct);
+        const float bmd = __shfl_sync(kFullMask, md, correct), bid = __shfl_sync(kFullMask, inv_d, correct);
         if (lane == 0) {
             s_correct = correct;
-            float mt, md = 0.0f;
-            double st, sd = 0.0;
-            row_stats(a.part, cpr, per, lo + correct, mt, st);
             const bool rejected = correct < L - 1;
-            if (rejected) row_stats(a.part, cpr, per, vd0 + correct, md, sd);
             brow.t = reinterpret_cast<const T *>(a.tgt) + (long long)(lo + correct) * a.ld_t;
             brow.d = rejected ? reinterpret_cast<const T *>(a.dft) + ((long long)r * G + correct) * a.ld_d
                               : nullptr;
-            brow.mt = mt * kLog2e;
-            brow.md = md * kLog2e;
-            brow.inv_st = st > 0.0 ? (float)(1.0 / st) : 0.0f;
-            brow.inv_sd = sd > 0.0 ? (float)(1.0 / sd) : 0.0f;
+            brow.mt = bmt * kLog2e;
+            brow.md = rejected ? bmd * kLog2e : 0.0f;
+            brow.inv_st = bit;
+            brow.inv_sd = rejected ? bid : 0.0f;
         }
     }
     __syncthreads();
@@ -650,39 +666,33 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sampling_accept_
     const int R = (V + kRound - 1) / kRound;
     const int rpw = (R + S * kSampWarps - 1) / (S * kSampWarps);  // <= kMaxRounds
     const int nt = kSampWarps * rpw;
+    unsigned long long Wq = 0ull, before = 0ull, slice = 0ull;
     for (int attempt = 0; attempt < 2; ++attempt) {
+        if (attempt > 0) cluster_sync();  // every CTA has read the previous totals
         if (b.d) bonus_rounds<T, true>(b, V, vec, q, rpw, rsum);
         else bonus_rounds<T, false>(b, V, vec, q, rpw, rsum);
+        if (attempt == 0) cluster_wait();  // every CTA of the cluster runs
         __syncthreads();
-        if (warp == 0) {
+        if (warp == 0) {  // this slice's total into slot q of every CTA of the cluster
             unsigned long long m = 0ull;
             for (int i = lane; i < nt; i += 32) m += rsum[i];
             m = warp_sum_u64(m);
-            if (lane == 0) s_slice = m;
+            if (lane < S) st_cluster_u64(&s_tot[q], (unsigned)lane, m);
         }
-        cluster_sync();  // every slice total is written
-        if (warp == 0) {
-            const unsigned long long v = lane < S ? ld_cluster_u64(&s_slice, (unsigned)lane) : 0ull;
-            unsigned long long incl = v;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const unsigned long long o = __shfl_up_sync(kFullMask, incl, d);
-                if (lane >= d) incl += o;
-            }
-            const unsigned long long before = __shfl_sync(kFullMask, incl - v, q);
-            const unsigned long long tot = __shfl_sync(kFullMask, incl, 31);
-            if (lane == 0) {
-                s_W = tot;
-                s_before = before;
-            }
+        cluster_sync();  // s_tot holds every slice total, in rank order
+        Wq = 0ull;
+        before = 0ull;
+        for (int i = 0; i < S; ++i) {
+            const unsigned long long t = s_tot[i];
+            before += i < q ? t : 0ull;
+            Wq += t;
         }
-        cluster_sync();  // every remote read is done: s_slice may be rewritten or freed
-        if (!(s_W < kEmptyResidual && b.d != nullptr)) break;
+        slice = s_tot[q];
+        if (!(Wq < kEmptyResidual && b.d != nullptr)) break;
         b.d = nullptr;  // p == q within the sums' precision: draw from p
     }
-    const unsigned long long Wq = s_W, before = s_before;
     const unsigned long long target = (unsigned long long)((double)__ldg(a.u_bonus + r) * (double)Wq);
-    const bool owner = target >= before && target - before < s_slice;
+    const bool owner = target >= before && target - before < slice;
     // the CTA whose slice holds u * W writes the request's results; when no
     // slice holds it (W = 0), rank 0 does, with no bonus token
     if (!owner && !(q == 0 && !(target < Wq))) return;
