@@ -781,6 +781,28 @@ size_t samp_partial_bytes(int max_rows, int B, int gamma) {
     return (slots * (1 + kNormWarps) * sizeof(NormPartial) + 255) & ~size_t(255);
 }
 
+// launch_pdl in thread-block clusters of `cluster` CTAs along x (gridDim.x
+// a multiple of it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t stream, int cluster, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 template <typename T>
 cudaError_t launch_sampling(const SampArgs &a, bool vec, cudaStream_t s) {
     const size_t smem = (size_t)(a.B + 1) * sizeof(int32_t);
