@@ -157,8 +157,10 @@ __global__ void __launch_bounds__(kArgmaxThreads, kCtasPerSm) argmax_kernel(Argm
     __shared__ int red_i[kArgmaxThreads / 32];
     constexpr int EPC = VEC ? Elem<T>::kPerChunk : 1;
 
-    pdl_trigger();
     pdl_wait();  // cu_seqlens / logits come from the kernels before
+    // the finalize launches once every CTA is past its wait, so it may read
+    // what the kernels before wrote (cu_seqlens, verify_lens) in its prologue
+    pdl_trigger();
     const int rows = device_rows(a.rows_dev, a.rows_host, a.max_rows);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (a.rows_dev && *a.rows_dev > a.max_rows) flag(a.status, DSPARK_STATUS_CAPACITY);
@@ -265,10 +267,13 @@ __device__ __forceinline__ void finish(const FinalArgs &a, int r, int lane, int 
 __global__ void __launch_bounds__(kFinalWarps * 32) greedy_finalize_kernel(FinalArgs a) {
     const int rq = blockIdx.x * kFinalWarps + (threadIdx.x >> 5);
     const int ln = threadIdx.x & 31;
-    // drafts are step inputs: fetch them while the argmax finishes
+    // drafts are step inputs, and cu_seqlens was written before any argmax
+    // CTA passed its wait (which precedes this grid's launch): fetch them
+    // while the argmax finishes, from L2
     const int dj = (rq < a.B && ln < a.gamma) ? __ldg(a.draft + (size_t)rq * a.gamma + ln) : -1;
+    const int rows = a.rows_dev ? min(max(__ldcg(a.rows_dev), 0), a.max_rows) : a.rows_host;
+    const int lo = rq < a.B ? __ldcg(a.cu + rq) : 0, hi = rq < a.B ? __ldcg(a.cu + rq + 1) : 0;
     pdl_wait();
-    const int rows = device_rows(a.rows_dev, a.rows_host, a.max_rows);
     const long long cpr = (a.V + a.epc - 1) / a.epc;
     const long long W = (long long)rows * cpr;
     const long long per = (W + a.grid - 1) / a.grid;
@@ -280,7 +285,7 @@ __global__ void __launch_bounds__(kFinalWarps * 32) greedy_finalize_kernel(Final
     const int g = a.gamma;
     if (__any_sync(kFullMask, lane < g && (dj < 0 || dj >= a.V)) && lane == 0)
         flag(a.status, DSPARK_STATUS_TOKEN_RANGE);
-    const int lo = a.cu[r], hi = a.cu[r + 1], L = hi - lo;
+    const int L = hi - lo;
     if (lo < 0 || hi > rows || L < 1 || L > g + 1) {
         if (lane == 0) {
             a.num_acc[r] = 0;
@@ -305,6 +310,7 @@ __global__ void __launch_bounds__(kFinalWarps * 32) cap_finalize_kernel(FinalArg
     const int rq = blockIdx.x * kFinalWarps + (threadIdx.x >> 5);
     const int ln = threadIdx.x & 31;
     const int dj0 = (rq < a.B && ln < a.gamma) ? __ldg(a.draft + (size_t)rq * a.gamma + ln) : -1;
+    const int len0 = rq < a.B ? __ldcg(a.lens + rq) : 0;  // written before the argmax's wait
     pdl_wait();
     const int rows = a.rows_host;
     const long long cpr = (a.V + a.epc - 1) / a.epc;
@@ -325,7 +331,7 @@ __global__ void __launch_bounds__(kFinalWarps * 32) cap_finalize_kernel(FinalArg
         const int am = lane <= g ? row_argmax(a.partial, base + lane, cpr, per) : 0;
         const unsigned mism = __ballot_sync(kFullMask, lane < g && am != dj);
         const int raw = mism ? __ffs(mism) - 1 : g;
-        int len = a.lens[r];
+        int len = len0;
         if (len < 1 || len > g + 1) {
             if (lane == 0) flag(a.status, DSPARK_STATUS_BAD_LEN);
             len = len < 1 ? 1 : g + 1;
