@@ -230,8 +230,10 @@ __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) softmax_norm_ker
     const int tid = threadIdx.x;
     const int B = a.B, G = a.gamma;
 
-    pdl_trigger();
     pdl_wait();  // cu_seqlens and the logits come from the kernels before
+    // the accept kernel launches once every CTA is past its wait, so it may
+    // read cu_seqlens and the logits in its prologue
+    pdl_trigger();
     const int rows = samp_rows(a);
     if (blockIdx.x == 0 && tid == 0 && a.cu[B] > a.max_rows) flag(a.status, DSPARK_STATUS_CAPACITY);
     // the tested drafts of each valid request, scanned: dcu
@@ -584,11 +586,19 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sampling_accept_
     // drafts and uniforms are step inputs: fetch them before the wait
     const int dj = (warp == 0 && lane < G) ? __ldg(a.draft + (size_t)r * G + lane) : -1;
     const float uj = (warp == 0 && lane < G) ? __ldg(a.u_acc + (size_t)r * G + lane) : 1.0f;
+    // cu_seqlens and the logits were written before the normalizer passed
+    // its wait, which precedes this grid's launch: the tested logits are
+    // fetched (from HBM) while the normalizer finishes
+    const int rows = min(max(__ldcg(a.cu + a.B), 0), a.max_rows);
+    const int lo = __ldcg(a.cu + r), hi = __ldcg(a.cu + r + 1), L = hi - lo;
+    float zt = 0.0f, zd = 0.0f;  // the two logits lane j's test reads
+    if (warp == 0 && samp_valid(lo, hi, rows, G) && lane < L - 1 && dj >= 0 && dj < V) {
+        zt = Elem<T>::load(reinterpret_cast<const T *>(a.tgt) + (long long)(lo + lane) * a.ld_t + dj);
+        zd = Elem<T>::load(reinterpret_cast<const T *>(a.dft) + ((long long)r * G + lane) * a.ld_d + dj);
+    }
     pdl_trigger();
     pdl_wait();  // partials and dcu come from softmax_norm_kernel
 
-    const int rows = samp_rows(a);
-    const int lo = a.cu[r], hi = a.cu[r + 1], L = hi - lo;
     if (q == 0 && warp == 0 && __any_sync(kFullMask, lane < G && (dj < 0 || dj >= V)) && lane == 0)
         flag(a.status, DSPARK_STATUS_TOKEN_RANGE);
     if (!samp_valid(lo, hi, rows, G)) {  // the whole cluster leaves here
@@ -617,11 +627,6 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sampling_accept_
     if (warp == 0) {
         const bool has_t = lane < L, has_d = lane < L - 1;
         const bool tok_ok = dj >= 0 && dj < V;
-        float zt = 0.0f, zd = 0.0f;  // the two logits the test reads, fetched first
-        if (has_d && tok_ok) {
-            zt = Elem<T>::load(reinterpret_cast<const T *>(a.tgt) + (long long)(lo + lane) * a.ld_t + dj);
-            zd = Elem<T>::load(reinterpret_cast<const T *>(a.dft) + ((long long)r * G + lane) * a.ld_d + dj);
-        }
         float mt = -INFINITY, md = -INFINITY;
         double st = 0.0, sd = 0.0;
         if (has_t) row_stats(a.part, cpr, per, lo + lane, mt, st);
