@@ -767,7 +767,12 @@ def run_ours(args):
         # path's 16, so the planner takes the rank path
         dM = torch.arange(256, 4097, 128, dtype=torch.int32, device=dev)
         dense = (dM, 0.002 * dM.to(torch.float64))
+        # the pages' 1-D table: SPS sampled at every integer M in [B, B + B*gamma]
+        sM = torch.arange(w.B, w.B + w.B * w.gamma + 1, dtype=torch.int32, device=dev)
+        sps = (sM, 1.0 / (3e-3 + 3e-6 * sM.to(torch.float64)))
         plan_kinds = {"additive_tier": plan_kind_timing(dev, stream, vs, _api.COST_ADDITIVE),
+                      "sps_1d_every_M_rank_path":
+                          plan_kind_timing(dev, stream, vs, _api.COST_SPS_1D, table=sps),
                       "additive_tier_31_entries_rank_path":
                           plan_kind_timing(dev, stream, vs, _api.COST_ADDITIVE, table=dense),
                       "additive_interpolated":

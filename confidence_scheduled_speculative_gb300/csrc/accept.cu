@@ -172,12 +172,12 @@ __global__ void __launch_bounds__(kArgmaxThreads, kCtasPerSm) argmax_kernel(Argm
     const int cpr = (a.V + EPC - 1) / EPC;  // chunks per row, the last one maybe partial
     const int full = a.V / EPC;             // full chunks per row
     const long long W = (long long)rows * cpr;
-    const long long per = (W + gridDim.x - 1) / gridDim.x;
+    const long long per = div_nonneg(W + gridDim.x - 1, gridDim.x);
     const long long q0 = (long long)blockIdx.x * per;
     const long long q1 = min(q0 + per, W);
     bool nan = false;
     for (long long q = q0; q < q1;) {
-        const int r = (int)(q / cpr);
+        const int r = (int)div_nonneg(q, cpr);
         const int c0 = (int)(q - (long long)r * cpr);
         const long long seg_end = min(q1, (long long)(r + 1) * cpr);
         const int c1 = c0 + (int)(seg_end - q);
@@ -229,10 +229,18 @@ struct FinalArgs {
 __device__ __forceinline__ int row_argmax(const Partial *partial, int row, long long cpr,
                                           long long per) {
     const long long q_first = (long long)row * cpr;
-    const int c_lo = (int)(q_first / per), c_hi = (int)((q_first + cpr - 1) / per);
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-    for (int c = c_lo; c <= c_hi; ++c) {
+    const int c_lo = (int)div_nonneg(q_first, per), c_hi = (int)div_nonneg(q_first + cpr - 1, per);
+    // the first two partials (a row usually spans one or two CTAs) are
+    // loaded together
+    const Partial p0 = partial[c_lo + row];
+    const Partial p1 = c_hi > c_lo ? partial[c_lo + 1 + row] : Partial{-INFINITY, 0x7FFFFFFF};
+    float bv = p0.v;
+    int bi = p0.i;
+    if (better(p1.v, p1.i, bv, bi)) {
+        bv = p1.v;
+        bi = p1.i;
+    }
+    for (int c = c_lo + 2; c <= c_hi; ++c) {
         const Partial p = partial[c + row];
         if (better(p.v, p.i, bv, bi)) {
             bv = p.v;
@@ -276,17 +284,21 @@ __global__ void __launch_bounds__(kFinalWarps * 32) greedy_finalize_kernel(Final
     pdl_wait();
     const long long cpr = (a.V + a.epc - 1) / a.epc;
     const long long W = (long long)rows * cpr;
-    const long long per = (W + a.grid - 1) / a.grid;
-    write_argmax(a, rows, cpr, per);
-
+    const long long per = div_nonneg(W + a.grid - 1, a.grid);
     const int lane = ln;
     const int r = rq;
-    if (r >= a.B) return;  // warp-uniform
     const int g = a.gamma;
+    const int L = hi - lo;
+    const bool valid = r < a.B && lo >= 0 && hi <= rows && L >= 1 && L <= g + 1;
+    // the request's row argmaxes first, so that their partial loads and the
+    // argmax output pass's are in flight together
+    const int am = valid && lane < L ? row_argmax(a.partial, lo + lane, cpr, per) : 0;
+    write_argmax(a, rows, cpr, per);
+
+    if (r >= a.B) return;  // warp-uniform
     if (__any_sync(kFullMask, lane < g && (dj < 0 || dj >= a.V)) && lane == 0)
         flag(a.status, DSPARK_STATUS_TOKEN_RANGE);
-    const int L = hi - lo;
-    if (lo < 0 || hi > rows || L < 1 || L > g + 1) {
+    if (!valid) {
         if (lane == 0) {
             a.num_acc[r] = 0;
             a.bonus[r] = -1;
@@ -298,7 +310,6 @@ __global__ void __launch_bounds__(kFinalWarps * 32) greedy_finalize_kernel(Final
         else if (lane == g) a.out[(size_t)r * (g + 1) + g] = -1;
         return;
     }
-    const int am = lane < L ? row_argmax(a.partial, lo + lane, cpr, per) : 0;
     const unsigned mism = __ballot_sync(kFullMask, lane < L - 1 && am != dj);
     const int correct = mism ? __ffs(mism) - 1 : L - 1;
     const int bon = __shfl_sync(kFullMask, am, correct);
@@ -315,20 +326,22 @@ __global__ void __launch_bounds__(kFinalWarps * 32) cap_finalize_kernel(FinalArg
     const int rows = a.rows_host;
     const long long cpr = (a.V + a.epc - 1) / a.epc;
     const long long W = (long long)rows * cpr;
-    const long long per = (W + a.grid - 1) / a.grid;
+    const long long per = div_nonneg(W + a.grid - 1, a.grid);
+    const int lane = ln;
+    const int r = rq;
+    const int g = a.gamma;
+    // the request's row argmaxes first (their loads in flight with the
+    // argmax output pass's)
+    const int am0 = r < a.B && lane <= g ? row_argmax(a.partial, r * (g + 1) + lane, cpr, per) : 0;
     write_argmax(a, rows, cpr, per);
     if (threadIdx.x == 0) sums[0] = sums[1] = 0;
     __syncthreads();
 
-    const int lane = ln;
-    const int r = rq;
-    const int g = a.gamma;
     if (r < a.B) {
         const int dj = dj0;
         if (__any_sync(kFullMask, lane < g && (dj < 0 || dj >= a.V)) && lane == 0)
             flag(a.status, DSPARK_STATUS_TOKEN_RANGE);
-        const int base = r * (g + 1);
-        const int am = lane <= g ? row_argmax(a.partial, base + lane, cpr, per) : 0;
+        const int am = am0;
         const unsigned mism = __ballot_sync(kFullMask, lane < g && am != dj);
         const int raw = mism ? __ffs(mism) - 1 : g;
         int len = len0;

@@ -130,6 +130,14 @@ cudaError_t ensure_smem(const void *kernel, int bytes, int slot);
 
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// x / d for non-negative x and positive d, in 32-bit arithmetic when both
+// fit (a 64-bit division is a long software sequence on the GPU).
+__device__ __forceinline__ long long div_nonneg(long long x, long long d) {
+    if (((unsigned long long)x | (unsigned long long)d) <= 0xFFFFFFFFull)
+        return (long long)((unsigned)x / (unsigned)d);
+    return x / d;
+}
+
 // Launch with the programmatic stream-serialization attribute so that the
 // kernel's prologue overlaps its predecessor on the stream (the kernel calls
 // pdl_wait() before reading what the predecessor wrote).

@@ -261,12 +261,12 @@ __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) softmax_norm_ker
     const int cpr = (a.V + EPC - 1) / EPC;  // chunks per row, the last maybe partial
     const int full = a.V / EPC;
     const long long W = (long long)VR * cpr;
-    const long long per = (W + a.grid - 1) / a.grid;
+    const long long per = div_nonneg(W + a.grid - 1, a.grid);
     const long long q0 = (long long)blockIdx.x * per;
     const long long q1 = min(q0 + per, W);
     bool nan = false;
     for (long long q = q0; q < q1;) {
-        const int v = (int)(q / cpr);
+        const int v = (int)div_nonneg(q, cpr);
         const int c0 = (int)(q - (long long)v * cpr);
         const long long seg_end = min(q1, (long long)(v + 1) * cpr);
         const int c1 = c0 + (int)(seg_end - q);
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) softmax_norm_ker
     // the warps' partials of each piece of this CTA, folded into one (warp
     // j % kNormWarps folds piece j; lane w reads warp w's partial)
     if (q0 < q1) {
-        const int v0 = (int)(q0 / cpr), v1 = (int)((q1 - 1) / cpr);
+        const int v0 = (int)div_nonneg(q0, cpr), v1 = (int)div_nonneg(q1 - 1, cpr);
         const int lane = tid & 31;
         for (int v = v0 + (tid >> 5); v <= v1; v += kNormWarps) {
             NormPartial p = NormPartial{-INFINITY, 0.0f, 0.0f, 0.0f};
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) softmax_norm_ker
 __device__ __forceinline__ void row_stats(const NormPartial *part, long long cpr, long long per,
                                           int v, float &M, double &S) {
     const long long q_first = (long long)v * cpr;
-    const int c_lo = (int)(q_first / per), c_hi = (int)((q_first + cpr - 1) / per);
+    const int c_lo = (int)div_nonneg(q_first, per), c_hi = (int)div_nonneg(q_first + cpr - 1, per);
     M = -INFINITY;
     for (int c = c_lo; c <= c_hi; ++c) M = fmaxf(M, part[c + v].m);
     S = 0.0;
@@ -617,7 +617,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sampling_accept_
     const int D = a.dcu[a.B];
     const long long cpr = (V + epc - 1) / epc;
     const long long W = (long long)(rows + D) * cpr;
-    const long long per = (W + a.grid - 1) / a.grid;
+    const long long per = div_nonneg(W + a.grid - 1, a.grid);
     const int vd0 = rows + a.dcu[r];  // virtual row of this request's first tested draft
 
     // (1) acceptance tests, in every CTA of the cluster (each needs the

@@ -148,6 +148,19 @@ def test_sampling_random(dev, orc, seed):
     _compare(f"random/{seed}", got, ref, tgt, dft, V, cu, draft, ua, ub)
 
 
+@pytest.mark.parametrize("B", [80, 100, 120, 160, 220])
+def test_sampling_cluster_splits(dev, orc, B):
+    """Batch sizes whose bonus draws are split over 7, 6, 5, 3 and 2 CTAs
+    per request on a 152-SM GPU (the split is floor(4 * SMs / B), 1..8):
+    the integer round sums make the draw independent of the split."""
+    rng = np.random.default_rng(9300 + B)
+    V, g = 4099, 4
+    tgt, dft, cu, draft, prefix, ua, ub = _problem(rng, B, g, V, "bf16", 0.5)
+    got = _gpu_sampling(dev, tgt, dft, V, cu, draft, prefix, ua, ub)
+    ref = orc.sampling_accept(tgt, V, cu, dft, draft, prefix, ua, ub)
+    _compare(f"split/{B}", got, ref, tgt, dft, V, cu, draft, ua, ub)
+
+
 def test_sampling_edge_cases(dev, orc):
     rng = np.random.default_rng(77)
     V, g, B = 1000, 4, 6
