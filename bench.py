@@ -59,7 +59,7 @@ def parse():
                     help="issue dspark_plan and dspark_pack_verify instead of dspark_plan_pack")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay")
     ap.add_argument("--no-sweep", action="store_true",
-                    help="skip the stress row sweep and the qwen_like cold-L2 step")
+                    help="skip the stress row sweep, the qwen_like cold-L2 step and the mixed report")
     ap.add_argument("--no-calib", action="store_true",
                     help="skip the calibration (recorder, statistics, fit) measurements")
     ap.add_argument("--event-every", type=int, default=16,
@@ -379,6 +379,57 @@ def accept_rows_sweep(dev, stream, seed, reps=20):
                                   "status": int(vs.status.item())})
             del vs
         del buf
+    except Exception as e:  # report, do not fail the run
+        out["error"] = f"{type(e).__name__}: {e}"[:200]
+    return out
+
+
+def mixed_cap_report(dev, n_steps=16):
+    """The mixed-traffic report of cap-accept (B=128, gamma=12, three
+    acceptance classes, 1-D SPS table): over independent steps (seeds
+    0..n_steps-1, no state carried) the planner's tau at its budget (the
+    expected commit under calibrated confidences), the delivered commit
+    sum(min(raw, len - 1) + 1) and the ceiling sum(raw + 1) of verifying
+    every depth.  The target rows follow the workload recipe -- N(0,1) with a
+    +8 peak at the draft token with the row's match probability, else at
+    another uniform token -- drawn on the device (a statistical report: the
+    rows are not the shared generator's bits)."""
+    import torch
+    from confidence_scheduled_speculative_gb300 import workloads as wl
+    from confidence_scheduled_speculative_gb300.engine import StepConfig, VerifyStep
+    w = wl.MIXED
+    out = {"workload": f"mixed B={w.B} gamma={w.gamma} V={w.V} cap-accept, 1-D SPS table",
+           "steps": n_steps}
+    try:
+        rows = w.B * (w.gamma + 1)
+        logits = torch.empty((rows, w.V), dtype=torch.bfloat16, device=dev)
+        gen = torch.Generator(device=dev)
+        tau = deliv = ceil = 0.0
+        for seed in range(n_steps):
+            step = wl.make_step(w, seed=seed)
+            rng = np.random.default_rng(np.random.SeedSequence([7919, seed]))
+            peak = rng.integers(0, w.V - 1, size=(w.B, w.gamma + 1))
+            d = step.draft.astype(np.int64)
+            other = peak[:, :w.gamma] + (peak[:, :w.gamma] >= d)
+            hit = rng.random((w.B, w.gamma)) < step.match_prob
+            peak[:, :w.gamma] = np.where(hit, d, other)
+            gen.manual_seed(seed)
+            logits.normal_(generator=gen)
+            flat = torch.from_numpy(peak.reshape(-1)).to(dev)
+            logits[torch.arange(rows, device=dev), flat] += wl.PEAK
+            vs = VerifyStep(StepConfig.from_step(step), dev)
+            vs.load_inputs(step)
+            vs.plan()
+            vs.cap_accept(logits, write_argmax=False)
+            tot = vs.cap_totals.cpu().tolist()
+            tau += float(vs.tau_theta[0].item())
+            deliv += tot[0]
+            ceil += tot[1]
+            out["status"] = out.get("status", 0) | int(vs.status.item())
+        out.update({"mean_tau": tau / n_steps, "mean_delivered": deliv / n_steps,
+                    "mean_ceiling": ceil / n_steps, "delivered_over_ceiling": deliv / ceil,
+                    "delivered_over_tau": deliv / tau})
+        del logits
     except Exception as e:  # report, do not fail the run
         out["error"] = f"{type(e).__name__}: {e}"[:200]
     return out
@@ -781,10 +832,11 @@ def run_ours(args):
 
     # ---- accept bandwidth against packed rows (stress workload) and the
     # small workload whose logits fit in L2 (secondary)
-    sweep = small = None
+    sweep = small = mixed = None
     if not args.no_cap and not args.no_sweep and w.name == "dsv4_like":
         sweep = accept_rows_sweep(dev, stream, args.seed)
         small = small_step_timing(dev, stream, "qwen_like", args.seed)
+        mixed = mixed_cap_report(dev)
 
     # ---- cap-accept over the full strided block (secondary)
     cap = None
@@ -901,6 +953,7 @@ def run_ours(args):
         "cap_accept": cap,
         "accept_by_rows": sweep,
         "qwen_like_cold_l2": small,
+        "mixed_cap_report": mixed,
         "status": status,
     }
     emit(line, args)
