@@ -25,7 +25,9 @@
  *     call has no effect on the device.
  *   - `status` (device int32[1], zeroed by the caller) collects
  *     DSPARK_STATUS_* bits that the kernels OR in for conditions only the
- *     device can see.  Kernels never trap, assert or spin.
+ *     device can see.  Kernels never trap or assert; their only waits on
+ *     memory (the scatter's copy barriers) give up after 200 ms and set
+ *     DSPARK_STATUS_TIMEOUT.
  *   - Calls are stateless and thread-safe; concurrent calls must not share
  *     workspaces.
  */
