@@ -944,7 +944,9 @@ def run_ours(args):
                          "pack_alone": float(np.median(br[:, 3])),
                          "accept_timed_mean": acc_us, "step_timed_mean": 1e3 * ms_per_step,
                          "accept_back_to_back": acc_b2b_us,
-                         "accept_back_to_back_gbs": accept_bytes / (acc_b2b_us * 1e-6) / 1e9},
+                         "accept_back_to_back_gbs": accept_bytes / (acc_b2b_us * 1e-6) / 1e9,
+                         "accept_rows_per_s": total / (acc_b2b_us * 1e-6),
+                         "planner_calls_per_s": 1e6 / float(np.median(br[:, 2]))},
         "cuda_graph": graph,
         "scatter_compact_to_strided": scat,
         "sampling_accept": samp,
