@@ -55,6 +55,46 @@ class StepConfig:
                    tiers=tuple(int(t) for t in step.tiers), capacity=int(step.capacity))
 
 
+_IN_PIECES = (("conf_logits", torch.float32, "Bg"), ("sts_temps", torch.float32, "g"),
+              ("anchor", torch.int32, "B"), ("draft", torch.int32, "Bg"),
+              ("prefix_lens", torch.int32, "B"))
+_OUT_PIECES = (("status", torch.int32, "1"), ("totals", torch.int32, "2"),
+               ("out_tokens", torch.int32, "Bg1"), ("commit_lens", torch.int32, "B"),
+               ("new_seq_lens", torch.int32, "B"), ("verify_lens", torch.int32, "B"))
+
+
+def _shape(kind: str, B: int, g: int) -> tuple[int, ...]:
+    return {"Bg": (B, g), "g": (g,), "B": (B,), "1": (1,), "2": (2,), "Bg1": (B, g + 1)}[kind]
+
+
+def _arena(B: int, g: int, device, pin: bool = False):
+    """One zeroed int32 arena laid out as [inputs | status | outputs], each
+    piece starting on a 16-byte boundary; returns (arena, named views, words
+    of the inputs and the status, first word of the status)."""
+    offsets, at = {}, 0
+    for name, _, kind in _IN_PIECES + _OUT_PIECES:
+        at = (at + 3) & ~3
+        offsets[name] = at
+        n = 1
+        for d in _shape(kind, B, g):
+            n *= d
+        at += n
+    if pin:
+        arena = torch.zeros(at, dtype=torch.int32).pin_memory()
+    else:
+        arena = torch.zeros(at, dtype=torch.int32, device=device)
+    views = {}
+    for name, dt, kind in _IN_PIECES + _OUT_PIECES:
+        shp = _shape(kind, B, g)
+        n = 1
+        for d in shp:
+            n *= d
+        v = arena[offsets[name]:offsets[name] + n]
+        views[name] = (v.view(dt) if dt != torch.int32 else v).view(shp)
+    n_in = offsets["status"] + 1  # the inputs and the status word
+    return arena, views, n_in, offsets["status"]
+
+
 class VerifyStep:
     """All device state of one verify-side step for a fixed configuration."""
 
@@ -64,34 +104,41 @@ class VerifyStep:
         B, g, cap = cfg.B, cfg.gamma, cfg.capacity
         i32 = dict(dtype=torch.int32, device=self.device)
         f32 = dict(dtype=torch.float32, device=self.device)
-        self.conf_logits = torch.zeros((B, g), **f32)
-        self.sts_temps = torch.ones(g, **f32)
-        self.anchor = torch.zeros(B, **i32)
-        self.draft = torch.zeros((B, g), **i32)
-        self.prefix_lens = torch.zeros(B, **i32)
+        # the step's inputs, the status word and the outputs a host reads
+        # back share one arena of 4-byte words ([inputs | status | outputs],
+        # each piece 16-byte aligned): the end-to-end path moves the inputs
+        # (with a zero status) in one copy and the status and outputs out in
+        # another
+        self.arena, views, self.n_in, self.out_lo = _arena(B, g, self.device)
+        self.conf_logits = views["conf_logits"]
+        self.sts_temps = views["sts_temps"]
+        self.sts_temps.fill_(1.0)
+        self.anchor = views["anchor"]
+        self.draft = views["draft"]
+        self.prefix_lens = views["prefix_lens"]
         self.cost_M = torch.as_tensor(cfg.cost_M, dtype=torch.int32, device=self.device)
         self.cost_val = torch.as_tensor(cfg.cost_val, dtype=torch.float64, device=self.device)
         # planner outputs
         self.survivals = torch.zeros((B, g), **f32)
-        self.verify_lens = torch.zeros(B, **i32)
+        self.verify_lens = views["verify_lens"]
         self.budget = torch.zeros(1, **i32)
         self.tau_theta = torch.zeros(2, dtype=torch.float64, device=self.device)
-        self.status = torch.zeros(1, **i32)
+        self.status = views["status"]
         # pack outputs
         self.packed_ids = torch.zeros(cap, **i32)
         self.packed_pos = torch.zeros(cap, **i32)
         self.packed_req = torch.zeros(cap, **i32)
         self.packed_src = torch.zeros(cap, **i32)
         self.cu_seqlens = torch.zeros(B + 1, **i32)
-        self.totals = torch.zeros(2, **i32)
+        self.totals = views["totals"]
         # accept outputs
         rows_max = max(cap, B * (g + 1))
         self.argmax = torch.zeros(rows_max, **i32)
         self.num_accepted = torch.zeros(B, **i32)
         self.bonus = torch.zeros(B, **i32)
-        self.commit_lens = torch.zeros(B, **i32)
-        self.new_seq_lens = torch.zeros(B, **i32)
-        self.out_tokens = torch.zeros((B, g + 1), **i32)
+        self.commit_lens = views["commit_lens"]
+        self.new_seq_lens = views["new_seq_lens"]
+        self.out_tokens = views["out_tokens"]
         self.ceiling = torch.zeros(B, **i32)
         self.cap_totals = torch.zeros(2, **i32)
         self.accept_ws = api.workspace(api.dspark_accept_workspace_bytes(rows_max, cfg.V),
@@ -244,18 +291,30 @@ class HostStepIO:
 
     def __init__(self, vs: VerifyStep):
         c = vs.cfg
-        pin = dict(pin_memory=True)
-        self.conf_logits = torch.zeros((c.B, c.gamma), dtype=torch.float32, **pin)
-        self.sts_temps = torch.zeros(c.gamma, dtype=torch.float32, **pin)
-        self.anchor = torch.zeros(c.B, dtype=torch.int32, **pin)
-        self.draft = torch.zeros((c.B, c.gamma), dtype=torch.int32, **pin)
-        self.prefix_lens = torch.zeros(c.B, dtype=torch.int32, **pin)
-        self.totals = torch.zeros(2, dtype=torch.int32, **pin)
-        self.out_tokens = torch.zeros((c.B, c.gamma + 1), dtype=torch.int32, **pin)
-        self.commit_lens = torch.zeros(c.B, dtype=torch.int32, **pin)
-        self.new_seq_lens = torch.zeros(c.B, dtype=torch.int32, **pin)
-        self.verify_lens = torch.zeros(c.B, dtype=torch.int32, **pin)
-        self.status = torch.zeros(1, dtype=torch.int32, **pin)
+        # the device arena's layout in pinned memory: the inputs (and a
+        # status word that stays zero) go in with one copy, the status and
+        # the outputs come back with one copy
+        self.arena, views, self.n_in, self.out_lo = _arena(c.B, c.gamma, None, pin=True)
+        self.in_arena = self.arena[:self.n_in]
+        self.out_host = torch.zeros(self.arena.numel() - self.out_lo, dtype=torch.int32).pin_memory()
+        self.conf_logits = views["conf_logits"]
+        self.sts_temps = views["sts_temps"]
+        self.anchor = views["anchor"]
+        self.draft = views["draft"]
+        self.prefix_lens = views["prefix_lens"]
+        # outputs: views of out_host at the device arena's offsets
+        _, oviews, _, _ = _arena(c.B, c.gamma, None, pin=False)
+        base = self.out_lo
+        def out_view(name):
+            v = oviews[name]
+            off = v.storage_offset() - base
+            return self.out_host[off:off + v.numel()].view(v.shape)
+        self.status = out_view("status")
+        self.totals = out_view("totals")
+        self.out_tokens = out_view("out_tokens")
+        self.commit_lens = out_view("commit_lens")
+        self.new_seq_lens = out_view("new_seq_lens")
+        self.verify_lens = out_view("verify_lens")
 
     def fill(self, step) -> None:
         self.conf_logits.copy_(torch.from_numpy(step.conf_logits))
@@ -265,13 +324,10 @@ class HostStepIO:
         self.prefix_lens.copy_(torch.from_numpy(step.prefix_lens))
 
     def h2d_input_bytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in
-                   (self.conf_logits, self.sts_temps, self.anchor, self.draft, self.prefix_lens))
+        return self.in_arena.numel() * 4
 
     def d2h_output_bytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in
-                   (self.totals, self.out_tokens, self.commit_lens, self.new_seq_lens,
-                    self.verify_lens, self.status))
+        return self.out_host.numel() * 4
 
 
 def run_host(vs: VerifyStep, io: HostStepIO, host_logits: torch.Tensor,
@@ -287,41 +343,22 @@ def run_host(vs: VerifyStep, io: HostStepIO, host_logits: torch.Tensor,
     bytes moved host -> device.
     """
     s = torch.cuda.current_stream() if stream is None else stream
-    if dev_logits is None:
-        with torch.cuda.stream(s):
-            vs.conf_logits.copy_(io.conf_logits, non_blocking=True)
-            vs.sts_temps.copy_(io.sts_temps, non_blocking=True)
-            vs.anchor.copy_(io.anchor, non_blocking=True)
-            vs.draft.copy_(io.draft, non_blocking=True)
-            vs.prefix_lens.copy_(io.prefix_lens, non_blocking=True)
-            vs.status.zero_()
-            vs.plan_pack(s)
-            vs.greedy_accept(host_logits, write_argmax=False, stream=s)
-            io.totals.copy_(vs.totals, non_blocking=True)
-            io.out_tokens.copy_(vs.out_tokens, non_blocking=True)
-            io.commit_lens.copy_(vs.commit_lens, non_blocking=True)
-            io.new_seq_lens.copy_(vs.new_seq_lens, non_blocking=True)
-            io.verify_lens.copy_(vs.verify_lens, non_blocking=True)
-            io.status.copy_(vs.status, non_blocking=True)
-            s.synchronize()
-        return int(io.totals[0]) * host_logits.stride(0) * host_logits.element_size()
     with torch.cuda.stream(s):
-        vs.conf_logits.copy_(io.conf_logits, non_blocking=True)
-        vs.sts_temps.copy_(io.sts_temps, non_blocking=True)
-        vs.anchor.copy_(io.anchor, non_blocking=True)
-        vs.draft.copy_(io.draft, non_blocking=True)
-        vs.prefix_lens.copy_(io.prefix_lens, non_blocking=True)
-        vs.status.zero_()
+        # the inputs and a zero status word: one copy
+        vs.arena[:vs.n_in].copy_(io.in_arena, non_blocking=True)
         vs.plan_pack(s)
-        io.totals.copy_(vs.totals, non_blocking=True)
-        s.synchronize()  # the host needs the packed total to run the verify window
-        rows = int(io.totals[0])
-        dev_logits[:rows].copy_(host_logits[:rows], non_blocking=True)
-        vs.greedy_accept(dev_logits, write_argmax=False, stream=s)
-        io.out_tokens.copy_(vs.out_tokens, non_blocking=True)
-        io.commit_lens.copy_(vs.commit_lens, non_blocking=True)
-        io.new_seq_lens.copy_(vs.new_seq_lens, non_blocking=True)
-        io.verify_lens.copy_(vs.verify_lens, non_blocking=True)
-        io.status.copy_(vs.status, non_blocking=True)
+        if dev_logits is None:
+            vs.greedy_accept(host_logits, write_argmax=False, stream=s)
+            rows = -1
+        else:
+            io.totals.copy_(vs.totals, non_blocking=True)
+            s.synchronize()  # the host needs the packed total to run the verify window
+            rows = int(io.totals[0])
+            dev_logits[:rows].copy_(host_logits[:rows], non_blocking=True)
+            vs.greedy_accept(dev_logits, write_argmax=False, stream=s)
+        # the status and every output: one copy
+        io.out_host.copy_(vs.arena[vs.out_lo:], non_blocking=True)
         s.synchronize()
+    if rows < 0:
+        rows = int(io.totals[0])
     return rows * host_logits.stride(0) * host_logits.element_size()

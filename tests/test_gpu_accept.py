@@ -362,3 +362,40 @@ def test_greedy_accept_reads_pinned_host_logits(dev, orc):
         outs.append({k: v.cpu().numpy() for k, v in o.items()} | {"status": int(st.item())})
     for k in outs[0]:
         np.testing.assert_array_equal(outs[0][k], outs[1][k], err_msg=k)
+
+
+@pytest.mark.parametrize("name", ["qwen_like", "tiny"])
+def test_run_host_end_to_end(dev, orc, name):
+    """engine.run_host from pinned host buffers (inputs in one copy, the
+    status and outputs back in one copy), with the accept reading the packed
+    logits over the host link and with them copied in first: every output
+    equals the oracle's plan + pack + greedy accept."""
+    from confidence_scheduled_speculative_gb300.engine import (HostStepIO, StepConfig, VerifyStep,
+                                                               run_host)
+    step = wl.make_step(wl.WORKLOADS[name], seed=3)
+    w = step.workload
+    ref = oracle_plan(orc, step)
+    p = orc.pack(step.anchor, step.draft, step.prefix_lens, ref.verify_lens, step.tiers,
+                 step.capacity)
+    cu = np.asarray(p.cu_seqlens)
+    rows_rj = [(r, j) for r in range(w.B) for j in range(int(cu[r + 1] - cu[r]))]
+    host_rows = wl.target_rows(step, rows_rj)
+    acc = orc.greedy_accept(host_rows, w.V, cu, step.draft, step.prefix_lens)
+    if w.logits_dtype == "fp32":
+        host = torch.from_numpy(host_rows)
+    else:
+        host = torch.from_numpy(host_rows.view(np.int16)).view(torch.bfloat16)
+    host = host.pin_memory()
+    vs = VerifyStep(StepConfig.from_step(step), dev)
+    io = HostStepIO(vs)
+    io.fill(step)
+    for dev_logits in (None, torch.empty(host.shape, dtype=host.dtype, device=dev)):
+        io.out_host.fill_(-7)
+        nbytes = run_host(vs, io, host, dev_logits)
+        assert nbytes == p.total * host.stride(0) * host.element_size()
+        assert int(io.status.item()) == 0
+        assert list(io.totals.numpy()) == [p.total, p.padded]
+        np.testing.assert_array_equal(io.verify_lens.numpy(), ref.verify_lens)
+        np.testing.assert_array_equal(io.out_tokens.numpy(), acc.out_tokens)
+        np.testing.assert_array_equal(io.commit_lens.numpy(), acc.commit_lens)
+        np.testing.assert_array_equal(io.new_seq_lens.numpy(), acc.new_seq_lens)
