@@ -799,6 +799,31 @@ def run_ours(args):
                 "frac_of_peak": p_bytes / (p_us * 1e-6) / 1e9 / load_peaks()[0],
                 "mean_accepted": float(so["num_accepted"].float().mean().item()),
                 "status": int(st_p.item())}
+        # the same call with the draft rows' log-sum-exp supplied (as the
+        # drafting step's sampler has it): only the target rows are normalised
+        lse = torch.logsumexp(dft_dev.float(), dim=1).contiguous()
+
+        def samp_call_lse():
+            _api.dspark_sampling_accept(compact, dft_dev, V=w.V, cu_seqlens=vs.cu_seqlens,
+                                        draft=vs.draft, prefix_lens=vs.prefix_lens, B=w.B,
+                                        gamma=g_, u_accept=ua, u_bonus=ub, workspace=sws,
+                                        status=st_p, draft_lse=lse, **so)
+
+        ref_out = so["out_tokens"].clone()
+        for _ in range(3):
+            samp_call_lse()
+        pe2 = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        pe2[0].record(stream)
+        for _ in range(n_p):
+            samp_call_lse()
+        pe2[1].record(stream)
+        torch.cuda.synchronize()
+        l_us = pe2[0].elapsed_time(pe2[1]) * 1e3 / n_p
+        l_bytes = total * w.V * w.elem_bytes
+        samp["with_draft_lse"] = {"us": l_us, "normalizer_bytes": l_bytes,
+                                  "gbs_normalizer_bytes": l_bytes / (l_us * 1e-6) / 1e9,
+                                  "same_out_tokens": bool(torch.equal(ref_out, so["out_tokens"])),
+                                  "status": int(st_p.item())}
         del dft_dev, sws
 
     # ---- calibration (secondary): the STS recorder on this step's accept

@@ -98,6 +98,9 @@ _SIGS = {
     "dspark_sampling_accept": (ctypes.c_int, [_VP, _I32, _I64, _I32, _I32, _VP, _VP, _I64, _VP,
                                               _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                               _VP, _SZ, _VP, _VP]),
+    "dspark_sampling_accept_ex": (ctypes.c_int, [_VP, _I32, _I64, _I32, _I32, _VP, _VP, _I64,
+                                                 _VP, _VP, _VP, _I32, _I32, _VP, _VP, _VP, _VP,
+                                                 _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
     "dspark_accept_workspace_bytes": (_SZ, [_I32, _I32]),
     "dspark_greedy_accept": (ctypes.c_int, [_VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP, _I32,
                                             _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP,
@@ -353,15 +356,30 @@ def dspark_sampling_workspace_bytes(max_rows: int, B: int, gamma: int) -> int:
 def dspark_sampling_accept(logits, draft_logits, *, V, cu_seqlens, draft, prefix_lens, B, gamma,
                            u_accept, u_bonus, num_accepted, bonus, commit_lens, out_tokens,
                            workspace, status, new_seq_lens=None, max_rows=None,
-                           stream=None) -> None:
+                           draft_lse=None, stream=None) -> None:
     """Speculative sampling accept: packed target rows ``logits`` and the
     draft's proposal rows ``draft_logits`` [B*gamma, >= V] (same dtype);
-    ``u_accept`` [B, gamma] and ``u_bonus`` [B] are fp32 uniforms."""
+    ``u_accept`` [B, gamma] and ``u_bonus`` [B] are fp32 uniforms.  With
+    ``draft_lse`` ([B*gamma] fp32, each draft row's log-sum-exp) the call is
+    dspark_sampling_accept_ex and the draft rows are not normalised here."""
     ptr, ld = _logits_ptr(logits, V)
     dptr, dld = _logits_ptr(draft_logits, V)
     if draft_logits.dtype != logits.dtype:
         raise ValueError("draft_logits: expected the dtype of logits")
     max_rows = logits.size(0) if max_rows is None else max_rows
+    if draft_lse is not None:
+        rc = load().dspark_sampling_accept_ex(
+            ptr, _dtype_code(logits), ld, V, max_rows, _p(cu_seqlens, torch.int32, "cu_seqlens"),
+            dptr, dld, _p(draft_lse, torch.float32, "draft_lse"), _p(draft, torch.int32, "draft"),
+            _p(prefix_lens, torch.int32, "prefix_lens"), B, gamma,
+            _p(u_accept, torch.float32, "u_accept"), _p(u_bonus, torch.float32, "u_bonus"),
+            _p(num_accepted, torch.int32, "num_accepted"), _p(bonus, torch.int32, "bonus"),
+            _p(commit_lens, torch.int32, "commit_lens"),
+            _p(new_seq_lens, torch.int32, "new_seq_lens"), _p(out_tokens, torch.int32, "out_tokens"),
+            _p(workspace), workspace.numel() * workspace.element_size(),
+            _p(status, torch.int32, "status"), _stream(stream))
+        _check("dspark_sampling_accept_ex", rc)
+        return
     rc = load().dspark_sampling_accept(
         ptr, _dtype_code(logits), ld, V, max_rows, _p(cu_seqlens, torch.int32, "cu_seqlens"),
         dptr, dld, _p(draft, torch.int32, "draft"), _p(prefix_lens, torch.int32, "prefix_lens"),

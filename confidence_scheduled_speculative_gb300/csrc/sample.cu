@@ -82,6 +82,7 @@ struct SampArgs {
     long long ld_t;  // elements
     const void *dft;
     long long ld_d;
+    const float *draft_lse;  // [B*gamma] the draft rows' log-sum-exp, or null (normalised here)
     int V, B, gamma, max_rows;
     const int32_t *cu, *draft, *prefix;
     const float *u_acc, *u_bonus;
@@ -257,7 +258,8 @@ __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) softmax_norm_ker
         if (blockIdx.x == 0)
             for (int q = tid; q <= B; q += kNormThreads) a.dcu[q] = dcu[q];
     }
-    const int VR = rows + dcu[B];
+    // the tested draft rows too, unless the caller gave their normalizers
+    const int VR = rows + (a.draft_lse ? 0 : dcu[B]);
     const int cpr = (a.V + EPC - 1) / EPC;  // chunks per row, the last maybe partial
     const int full = a.V / EPC;
     const long long W = (long long)VR * cpr;
@@ -592,9 +594,13 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sampling_accept_
     const int rows = min(max(__ldcg(a.cu + a.B), 0), a.max_rows);
     const int lo = __ldcg(a.cu + r), hi = __ldcg(a.cu + r + 1), L = hi - lo;
     float zt = 0.0f, zd = 0.0f;  // the two logits lane j's test reads
-    if (warp == 0 && samp_valid(lo, hi, rows, G) && lane < L - 1 && dj >= 0 && dj < V) {
-        zt = Elem<T>::load(reinterpret_cast<const T *>(a.tgt) + (long long)(lo + lane) * a.ld_t + dj);
-        zd = Elem<T>::load(reinterpret_cast<const T *>(a.dft) + ((long long)r * G + lane) * a.ld_d + dj);
+    float lse = 0.0f;            // the caller's normalizer of draft row j
+    if (warp == 0 && samp_valid(lo, hi, rows, G) && lane < L - 1) {
+        if (dj >= 0 && dj < V) {
+            zt = Elem<T>::load(reinterpret_cast<const T *>(a.tgt) + (long long)(lo + lane) * a.ld_t + dj);
+            zd = Elem<T>::load(reinterpret_cast<const T *>(a.dft) + ((long long)r * G + lane) * a.ld_d + dj);
+        }
+        if (a.draft_lse) lse = __ldg(a.draft_lse + (size_t)r * G + lane);
     }
     pdl_trigger();
     pdl_wait();  // partials and dcu come from softmax_norm_kernel
@@ -614,7 +620,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sampling_accept_
         return;
     }
     cluster_arrive_relaxed();  // waited for before the first remote store
-    const int D = a.dcu[a.B];
+    const int D = a.draft_lse ? 0 : a.dcu[a.B];  // the normaliser's virtual draft rows
     const long long cpr = (V + epc - 1) / epc;
     const long long W = (long long)(rows + D) * cpr;
     const long long per = div_nonneg(W + a.grid - 1, a.grid);
@@ -630,7 +636,14 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sampling_accept_
         float mt = -INFINITY, md = -INFINITY;
         double st = 0.0, sd = 0.0;
         if (has_t) row_stats(a.part, cpr, per, lo + lane, mt, st);
-        if (has_d) row_stats(a.part, cpr, per, vd0 + lane, md, sd);
+        if (has_d) {
+            if (!a.draft_lse) {
+                row_stats(a.part, cpr, per, vd0 + lane, md, sd);
+            } else if (isfinite(lse)) {  // q = exp(z - lse): "max" lse, sum 1
+                md = lse;
+                sd = 1.0;
+            }
+        }
         const float inv_t = st > 0.0 ? (float)(1.0 / st) : 0.0f;
         const float inv_d = sd > 0.0 ? (float)(1.0 / sd) : 0.0f;
         bool accept = true;
@@ -830,10 +843,11 @@ extern "C" size_t dspark_sampling_workspace_bytes(int32_t max_rows, int32_t B, i
     return samp_partial_bytes(max_rows, B, gamma) + ((((size_t)B + 1) * 4 + 255) & ~size_t(255));
 }
 
-extern "C" int dspark_sampling_accept(const void *target_logits, int32_t dtype, int64_t ld_t,
-                                      int32_t V, int32_t max_rows, const int32_t *cu_seqlens,
-                                      const void *draft_logits, int64_t ld_d,
-                                      const int32_t *draft, const int32_t *prefix_lens, int32_t B,
+extern "C" int dspark_sampling_accept_ex(const void *target_logits, int32_t dtype, int64_t ld_t,
+                                         int32_t V, int32_t max_rows, const int32_t *cu_seqlens,
+                                         const void *draft_logits, int64_t ld_d,
+                                         const float *draft_lse, const int32_t *draft,
+                                         const int32_t *prefix_lens, int32_t B,
                                       int32_t gamma, const float *u_accept, const float *u_bonus,
                                       int32_t *num_accepted, int32_t *bonus, int32_t *commit_lens,
                                       int32_t *new_seq_lens, int32_t *out_tokens, void *workspace,
@@ -855,6 +869,7 @@ extern "C" int dspark_sampling_accept(const void *target_logits, int32_t dtype, 
     a.ld_t = ld_t;
     a.dft = draft_logits;
     a.ld_d = ld_d;
+    a.draft_lse = draft_lse;
     a.V = V;
     a.B = B;
     a.gamma = gamma;
@@ -889,4 +904,19 @@ extern "C" int dspark_sampling_accept(const void *target_logits, int32_t dtype, 
     const cudaError_t e = dtype == DSPARK_DTYPE_BF16 ? launch_sampling<__nv_bfloat16>(a, vec, s)
                                                      : launch_sampling<float>(a, vec, s);
     return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+extern "C" int dspark_sampling_accept(const void *target_logits, int32_t dtype, int64_t ld_t,
+                                      int32_t V, int32_t max_rows, const int32_t *cu_seqlens,
+                                      const void *draft_logits, int64_t ld_d,
+                                      const int32_t *draft, const int32_t *prefix_lens, int32_t B,
+                                      int32_t gamma, const float *u_accept, const float *u_bonus,
+                                      int32_t *num_accepted, int32_t *bonus, int32_t *commit_lens,
+                                      int32_t *new_seq_lens, int32_t *out_tokens, void *workspace,
+                                      size_t workspace_bytes, int32_t *status, void *stream) {
+    return dspark_sampling_accept_ex(target_logits, dtype, ld_t, V, max_rows, cu_seqlens,
+                                     draft_logits, ld_d, nullptr, draft, prefix_lens, B, gamma,
+                                     u_accept, u_bonus, num_accepted, bonus, commit_lens,
+                                     new_seq_lens, out_tokens, workspace, workspace_bytes, status,
+                                     stream);
 }

@@ -279,6 +279,25 @@ DSPARK_API int dspark_sampling_accept(const void *target_logits, int32_t dtype, 
                            int32_t *out_tokens, void *workspace, size_t workspace_bytes,
                            int32_t *status, void *stream);
 
+/* dspark_sampling_accept with the draft rows' softmax normalizers supplied
+ * by the caller -- the drafting step's sampler has them -- so that the
+ * draft rows are not streamed to normalise them (only the target rows are;
+ * a rejected request's draft row is still read for the residual bonus):
+ *   draft_lse  [B*gamma] fp32 (nullable: dspark_sampling_accept):
+ *              log(sum_y exp(z_y)) of draft row r*gamma + j (natural log);
+ *              q_j(x) = exp(z_x - draft_lse[r*gamma + j]).  Read for the
+ *              tested drafts only.  A non-finite value makes that row's q
+ *              zero everywhere.
+ * Everything else, including the workspace size, as dspark_sampling_accept. */
+DSPARK_API int dspark_sampling_accept_ex(const void *target_logits, int32_t dtype, int64_t ld_t,
+                           int32_t V, int32_t max_rows, const int32_t *cu_seqlens,
+                           const void *draft_logits, int64_t ld_d, const float *draft_lse,
+                           const int32_t *draft, const int32_t *prefix_lens, int32_t B,
+                           int32_t gamma, const float *u_accept, const float *u_bonus,
+                           int32_t *num_accepted, int32_t *bonus, int32_t *commit_lens,
+                           int32_t *new_seq_lens, int32_t *out_tokens, void *workspace,
+                           size_t workspace_bytes, int32_t *status, void *stream);
+
 /* ScatterCompactToStrided ([ROUND] §三): after the target forward over the
  * compact verify rows, copy packed row i (i < totals[0]) to row
  * packed_src[i] = r*(gamma+1) + j of the [B x (gamma+1)] strided buffer, so

@@ -219,6 +219,17 @@ def test_sampling_argument_checks(lib):
     assert call(B=5000) == -4
     assert call(ws=None) == -2
     assert call(wsb=need - 256) == -2
+    fx = lib.dspark_sampling_accept_ex
+    fx.restype = ctypes.c_int
+
+    def call_ex(dtype=0, lse=FAKE):
+        return fx(FAKE, dtype, ctypes.c_int64(1024), 1000, 100, FAKE, FAKE, ctypes.c_int64(1024),
+                  lse, FAKE, FAKE, 4, 4, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None,
+                  ctypes.c_size_t(need), FAKE, None)
+
+    assert call_ex(dtype=3) == -1
+    assert call_ex(lse=None, dtype=3) == -1
+    assert call_ex() == -2  # null workspace
 
 
 def test_calibration_argument_checks(lib):

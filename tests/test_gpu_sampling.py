@@ -27,7 +27,7 @@ def dev():
     return require_gpu()
 
 
-def _gpu_sampling(dev, tgt, dft, V, cu, draft, prefix, ua, ub, max_rows=None):
+def _gpu_sampling(dev, tgt, dft, V, cu, draft, prefix, ua, ub, max_rows=None, draft_lse=None):
     from confidence_scheduled_speculative_gb300 import api
     B, g = draft.shape
     t = lambda a, d=np.int32: torch.from_numpy(np.ascontiguousarray(a, dtype=d)).to(dev)
@@ -41,7 +41,8 @@ def _gpu_sampling(dev, tgt, dft, V, cu, draft, prefix, ua, ub, max_rows=None):
     api.dspark_sampling_accept(to_dev_logits(tgt, dev), to_dev_logits(dft, dev), V=V,
                                cu_seqlens=t(cu), draft=t(draft), prefix_lens=t(prefix), B=B,
                                gamma=g, u_accept=t(ua, np.float32), u_bonus=t(ub, np.float32),
-                               workspace=ws, status=st, max_rows=rows_cap, **o)
+                               workspace=ws, status=st, max_rows=rows_cap,
+                               draft_lse=None if draft_lse is None else t(draft_lse, np.float32), **o)
     torch.cuda.synchronize()
     res = {k: v.cpu().numpy() for k, v in o.items()}
     res["status"] = int(st.item())
@@ -159,6 +160,34 @@ def test_sampling_cluster_splits(dev, orc, B):
     got = _gpu_sampling(dev, tgt, dft, V, cu, draft, prefix, ua, ub)
     ref = orc.sampling_accept(tgt, V, cu, dft, draft, prefix, ua, ub)
     _compare(f"split/{B}", got, ref, tgt, dft, V, cu, draft, ua, ub)
+
+
+def _lse_rows(dft, V):
+    """log(sum exp(z)) of every draft row in fp64 (NaN weighs 0), as fp32:
+    what the drafting step's sampler hands over."""
+    z = _f32(dft[:, :V]).astype(np.float64)
+    z = np.where(np.isnan(z), -np.inf, z)
+    m = z.max(axis=1)
+    ok = np.isfinite(m)
+    s = np.exp(z - np.where(ok, m, 0.0)[:, None]).sum(axis=1)
+    return np.where(ok, m + np.log(np.where(ok, s, 1.0)), -np.inf).astype(np.float32)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_sampling_with_draft_normalizers(dev, orc, seed):
+    """dspark_sampling_accept_ex: with each draft row's log-sum-exp supplied
+    the draft rows are not normalised by the library; the decisions equal
+    the oracle's (which normalises them itself) up to its near-tie
+    tolerance."""
+    rng = np.random.default_rng(8700 + seed)
+    dtype = "bf16" if seed % 2 == 0 else "fp32"
+    V = int(rng.choice([33, 1000, 4099, 20000]))
+    g = int(rng.integers(1, 9))
+    B = int(rng.choice([3, 17, 90]))
+    tgt, dft, cu, draft, prefix, ua, ub = _problem(rng, B, g, V, dtype, float(rng.choice([0.05, 0.5])))
+    got = _gpu_sampling(dev, tgt, dft, V, cu, draft, prefix, ua, ub, draft_lse=_lse_rows(dft, V))
+    ref = orc.sampling_accept(tgt, V, cu, dft, draft, prefix, ua, ub)
+    _compare(f"lse/{seed}", got, ref, tgt, dft, V, cu, draft, ua, ub)
 
 
 def test_sampling_edge_cases(dev, orc):
