@@ -435,6 +435,67 @@ def mixed_cap_report(dev, n_steps=16):
     return out
 
 
+def configs_report(dev, stream, seed, reps=20, e2e_reps=10):
+    """Every workload's step through the same calls: packed rows, the device
+    step (plan + pack + greedy accept, back to back), the planner alone, and
+    end-to-end steps/s through engine.run_host (inputs from pinned host
+    buffers, the accept reading the packed logits over the host link).  The
+    target logits are N(0,1) filler of the packed rows' shape (timing only;
+    the parity tests check values); stress runs at its largest forced
+    budget."""
+    import torch
+    from confidence_scheduled_speculative_gb300 import workloads as wl
+    from confidence_scheduled_speculative_gb300.engine import (HostStepIO, StepConfig,
+                                                               VerifyStep, run_host)
+    out = {}
+    for name in ("tiny", "qwen_like", "dsv4_like", "mixed", "stress"):
+        try:
+            w = wl.WORKLOADS[name]
+            step = wl.make_step(w, seed=seed, forced_budget=w.B * w.gamma if name == "stress" else None)
+            vs = VerifyStep(StepConfig.from_step(step), dev)
+            vs.load_inputs(step)
+            vs.plan_pack()
+            torch.cuda.synchronize()
+            total = int(vs.totals[0].item())
+            dt = torch.float32 if w.logits_dtype == "fp32" else torch.bfloat16
+            logits = torch.empty((max(total, 1), w.V), dtype=dt, device=dev)
+            logits.normal_(generator=torch.Generator(device=dev).manual_seed(seed))
+            plan_pack_fn, plan_fn, _, acc_fn = vs.bind_compact(logits)
+
+            def timed(fn, n):
+                for _ in range(3):
+                    fn()
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                ev[0].record(stream)
+                for _ in range(n):
+                    fn()
+                ev[1].record(stream)
+                torch.cuda.synchronize()
+                return ev[0].elapsed_time(ev[1]) * 1e3 / n
+
+            step_us = timed(lambda: (plan_pack_fn(), acc_fn()), reps)
+            plan_us = timed(plan_fn, reps)
+            io = HostStepIO(vs)
+            io.fill(step)
+            host = torch.empty(logits.shape, dtype=dt).pin_memory()
+            host.copy_(logits)
+            for _ in range(2):
+                run_host(vs, io, host, None)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(e2e_reps):
+                run_host(vs, io, host, None)
+            e2e = e2e_reps / (time.perf_counter() - t0)
+            out[name] = {"B": w.B, "gamma": w.gamma, "V": w.V, "rows": total,
+                         "step_us": step_us, "plan_us": plan_us, "e2e_steps_per_s": e2e,
+                         "accept_gbs_in_step": total * w.V * w.elem_bytes / (step_us * 1e-6) / 1e9,
+                         "status": int(vs.status.item()) | int(io.status.item())}
+            del logits, host, vs, io
+        except Exception as e:  # report, do not fail the run
+            out[name] = {"error": f"{type(e).__name__}: {e}"[:200]}
+    return out
+
+
 def small_step_timing(dev, stream, name, seed, reps=50):
     """plan + pack + accept step time of a workload whose logits fit in L2
     (qwen_like: 256 packed rows x 151936 bf16 = 77.8 MB): a 256 MB buffer is
@@ -857,11 +918,12 @@ def run_ours(args):
 
     # ---- accept bandwidth against packed rows (stress workload) and the
     # small workload whose logits fit in L2 (secondary)
-    sweep = small = mixed = None
+    sweep = small = mixed = by_config = None
     if not args.no_cap and not args.no_sweep and w.name == "dsv4_like":
         sweep = accept_rows_sweep(dev, stream, args.seed)
         small = small_step_timing(dev, stream, "qwen_like", args.seed)
         mixed = mixed_cap_report(dev)
+        by_config = configs_report(dev, stream, args.seed)
 
     # ---- cap-accept over the full strided block (secondary)
     cap = None
@@ -981,6 +1043,7 @@ def run_ours(args):
         "accept_by_rows": sweep,
         "qwen_like_cold_l2": small,
         "mixed_cap_report": mixed,
+        "by_config": by_config,
         "status": status,
     }
     emit(line, args)
