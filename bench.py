@@ -900,18 +900,22 @@ def run_ours(args):
     if not args.no_cap and w.name == "dsv4_like":
         from confidence_scheduled_speculative_gb300 import api as _api
         vs.status.zero_()
-        # the same tier costs at every 128 rows: 31 entries, past the select
-        # path's 16, so the planner takes the rank path
+        # the same tier costs at every 128 rows: 31 entries, the select
+        # path's largest table; at every 64 rows: 61 entries, the rank path
         dM = torch.arange(256, 4097, 128, dtype=torch.int32, device=dev)
         dense = (dM, 0.002 * dM.to(torch.float64))
+        dM2 = torch.arange(256, 4097, 64, dtype=torch.int32, device=dev)
+        dense2 = (dM2, 0.002 * dM2.to(torch.float64))
         # the pages' 1-D table: SPS sampled at every integer M in [B, B + B*gamma]
         sM = torch.arange(w.B, w.B + w.B * w.gamma + 1, dtype=torch.int32, device=dev)
         sps = (sM, 1.0 / (3e-3 + 3e-6 * sM.to(torch.float64)))
         plan_kinds = {"additive_tier": plan_kind_timing(dev, stream, vs, _api.COST_ADDITIVE),
                       "sps_1d_every_M_rank_path":
                           plan_kind_timing(dev, stream, vs, _api.COST_SPS_1D, table=sps),
-                      "additive_tier_31_entries_rank_path":
+                      "additive_tier_31_entries":
                           plan_kind_timing(dev, stream, vs, _api.COST_ADDITIVE, table=dense),
+                      "additive_tier_61_entries_rank_path":
+                          plan_kind_timing(dev, stream, vs, _api.COST_ADDITIVE, table=dense2),
                       "additive_interpolated":
                           plan_kind_timing(dev, stream, vs, _api.COST_ADDITIVE_INTERP)}
         vs.status.zero_()

@@ -32,6 +32,9 @@ STATUS_BAD_LEN = 16
 STATUS_BAD_COST = 32
 STATUS_INFEASIBLE = 64
 
+# cost tables of at most this many entries take the planner's single-CTA
+# select path (the pack fused into it); larger ones the multi-CTA rank path
+SELECT_MAX_ENTRIES = 31
 COST_SPS_1D = 0
 COST_ADDITIVE = 1
 COST_ADDITIVE_INTERP = 2
@@ -268,7 +271,7 @@ def dspark_plan_pack(conf_logits, sts_temps, anchor, draft, prefix_lens, *, B, g
                      req_generation=None, lagged_conf_logits=None, align_to_tiers=False,
                      stream=None) -> None:
     """dspark_plan then dspark_pack_verify on its verify_lens, in fewer launches
-    (the pack runs inside the planner's last kernel for tables of <= 16
+    (the pack runs inside the planner's last kernel for tables of <= 31
     entries).  The planner options as in dspark_plan_ex; alignment uses the
     pack's ``tiers``."""
     params = dspark_plan_params(B, gamma, survival_eps, min_verify_len, max_verify_len,

@@ -980,7 +980,7 @@ size_t rank_smem_max() {
 //       C*: the thread holding that position writes the verify length.
 // Each thread holds IPT consecutive candidates of the request-major order.
 
-constexpr int kMaxSelect = 16;
+constexpr int kMaxSelect = 31;  // + the forced budget: one warp each of the 32
 constexpr int kSelSlots = kMaxSelect + 1;  // table entries + the forced budget
 constexpr int kSelThreads = 1024;
 constexpr int kRadixBins = 256;
@@ -1676,7 +1676,7 @@ int check_plan(const float *conf_logits, const float *sts_temps, const dspark_pl
 }
 
 // One planner pass over survivals already computed: select_kernel (tables
-// of <= 16 entries) or rank_kernel.
+// of <= kMaxSelect entries) or rank_kernel.
 int launch_pass(PlanArgs a, bool select, cudaStream_t s) {
     if (select) {
         const int ipt = (a.N + kSelThreads - 1) / kSelThreads;

@@ -197,9 +197,9 @@ class VerifyStep:
 
     def kernels_per_step(self, separate_plan_pack: bool = False) -> int:
         """Kernels one compact step launches: survival + select (the pack
-        inside) for tables of <= 16 entries, else survival + rank + pack
+        inside) for tables of <= api.SELECT_MAX_ENTRIES entries, else survival + rank + pack
         (separate calls add the pack kernel); then argmax + finalize."""
-        select = len(self.cfg.cost_M) <= 16
+        select = len(self.cfg.cost_M) <= api.SELECT_MAX_ENTRIES
         return (3 if (separate_plan_pack or not select) else 2) + 2
 
     def greedy_accept(self, logits: torch.Tensor, write_argmax: bool = True, stream=None) -> None:

@@ -73,7 +73,8 @@ def _random_problem(rng):
     max_len = int(rng.integers(1, gamma + 2))
     min_len = int(rng.integers(1, max_len + 1)) if rng.random() < 0.3 else 1
     kind = int(rng.integers(0, 2))
-    n = int(rng.integers(1, 12))
+    # tables up to 31 entries take the select path, longer ones the rank path
+    n = int(rng.integers(1, 12)) if rng.random() < 0.6 else int(rng.integers(12, 40))
     hi = B + B * gamma + 6
     M = np.sort(rng.choice(np.arange(1, hi + 1), size=min(n, hi), replace=False)).astype(np.int32)
     val = (rng.uniform(100, 1000, M.size) if kind == 0 else rng.uniform(0.01, 3.0, M.size))
@@ -187,16 +188,25 @@ def _select_case(name):
         return dict(base, B=600, gamma=20, z=z, T=np.full(20, 1.3, np.float32), max_len=21,
                     M=np.array([600, 1024, 2048, 4096, 8192, 12600], np.int32),
                     val=np.array([0.5, 0.9, 1.8, 3.5, 7.0, 11.0]))
-    if name == "sixteen_entries":   # the largest table the select path takes
+    if name == "sixteen_entries":
         z = rng.normal(1.0, 1.2, (512, 16)).astype(np.float32)
         M = np.linspace(512, 512 * 17, 16).astype(np.int32)
         return dict(base, B=512, gamma=16, z=z, kind=0, M=M, val=1.0 / (1e-3 + 2e-6 * M))
+    if name == "thirty_one_entries":  # the largest table the select path takes
+        z = rng.normal(1.0, 1.2, (512, 16)).astype(np.float32)
+        M = np.linspace(512, 512 * 17, 31).astype(np.int32)
+        return dict(base, B=512, gamma=16, z=z, kind=0, M=M, val=1.0 / (1e-3 + 2e-6 * M))
+    if name == "thirty_one_entries_ties":  # 32 slots through the radix passes
+        z = np.tile(rng.normal(2.0, 1.0, 16).astype(np.float32), (1000, 1))
+        M = np.linspace(1000, 16000, 31).astype(np.int32)
+        return dict(base, B=1000, gamma=16, z=z, M=M, val=2e-4 * M, forced=4321)
     raise KeyError(name)
 
 
 @pytest.mark.parametrize("name", ["all_ones", "all_ones_forced", "half_saturated",
                                   "identical_requests", "identical_forced", "large_spread",
-                                  "sixteen_entries"])
+                                  "sixteen_entries", "thirty_one_entries",
+                                  "thirty_one_entries_ties"])
 def test_plan_select_bins(dev, orc, name):
     P = _select_case(name)
     g = _gpu_plan(dev, P)
@@ -399,7 +409,7 @@ def _pack_inputs(rng, B, g, total_hint):
 def test_plan_pack_fused_random(dev, orc, seed):
     """dspark_plan_pack equals the oracle's planner followed by its pack,
     including untouched rows past the window, capacity overflow and tier
-    lists with no tier above the total; tables of more than 16 entries take
+    lists with no tier above the total; tables of more than 31 entries take
     the separate kernels."""
     rng = np.random.default_rng(90000 + seed)
     P = _random_problem(rng)
