@@ -31,3 +31,17 @@ def test_step_arena_layout(B, g):
         assert views[name].data_ptr() - base > status, name
     assert views["conf_logits"].dtype == torch.float32 and views["draft"].dtype == torch.int32
     assert tuple(views["out_tokens"].shape) == (B, g + 1)
+
+
+def test_select_path_limit_matches_kernel():
+    """The step's launch count follows the planner's dispatch: the binding's
+    select-path table limit is the kernel source's."""
+    import os
+    import re
+
+    from confidence_scheduled_speculative_gb300 import api
+    src = os.path.join(os.path.dirname(api.__file__), "csrc", "plan.cu")
+    with open(src) as f:
+        m = re.search(r"constexpr int kMaxSelect = (\d+);", f.read())
+    assert m is not None
+    assert api.SELECT_MAX_ENTRIES == int(m.group(1))
