@@ -204,7 +204,7 @@ def plan(z, T, eps, min_len, max_len, forced, kind, M, val, bias=0.0, alpha=0.0)
 
 
 def plan_ex(z, T, eps, min_len, max_len, forced, kind, M, val, bias=0.0, alpha=0.0,
-            conf_gen=None, req_gen=None, lagged_z=None, align_tiers=None):
+            conf_gen=None, req_gen=None, lagged_z=None, align_tiers=None, survivals=None):
     """The planner with the options of [AVS] §三, composed from the plain
     planner's definitions:
       * generation mask: a request whose confidences belong to another
@@ -214,7 +214,10 @@ def plan_ex(z, T, eps, min_len, max_len, forced, kind, M, val, bias=0.0, alpha=0
         current confidences with that budget forced;
       * align_tiers: with T rows at the chosen budget b and the smallest tier
         t >= T, the executed budget is b + (t - T) (then clipped to the
-        in-range candidates like any forced budget); no tier >= T: b."""
+        in-range candidates like any forced budget); no tier >= T: b.
+    ``survivals`` (optional, [B, gamma] fp32) replaces the current
+    confidences' survivals computed from z: the later steps then run on
+    those values (staged parity: another implementation's survivals)."""
     z = _c(z, np.float32)
     B, g = z.shape
     live = np.ones(B, bool) if conf_gen is None else (np.asarray(conf_gen) == np.asarray(req_gen))
@@ -237,6 +240,9 @@ def plan_ex(z, T, eps, min_len, max_len, forced, kind, M, val, bias=0.0, alpha=0
         forced = first.budget
     s_raw, s_out, st = surv(z)
     status |= st
+    if survivals is not None:
+        s_raw = _c(survivals, np.float32)
+        s_out = np.where(s_raw >= np.float32(eps), s_raw, np.float32(0)).astype(np.float32)
     res = plan_from_survivals(s_raw, eps, min_len, max_len, forced, kind, M, val, bias, alpha)
     if align_tiers is not None and len(align_tiers) > 0:
         status |= res.status
