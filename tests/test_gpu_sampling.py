@@ -315,3 +315,23 @@ def test_sampling_dsv4_like_full_size(dev, orc):
     sub_got = {k: got[k][sample] for k in KEYS}
     sub_got["status"] = ref.status
     _compare("dsv4", sub_got, ref, sub_t, sub_d, V, sub_cu, draft[sample], ua[sample], ub[sample])
+
+
+def test_sampling_residual_mass_threshold(dev, orc):
+    """The empty-residual cut-off on the GPU, on the oracle pin's hand case
+    (V = 2, residual masses 2^-19 and 2^-21 on the two sides of 2^-20): the
+    larger residual is drawn from (bonus 0), the smaller one is read as
+    empty and the bonus is drawn from p (u_bonus 0.75 -> token 1)."""
+    b = np.array([-(2.0 ** -17), -(2.0 ** -19)], np.float32)
+    tgt = np.zeros((4, 2), np.float32)
+    dft = np.stack([[b[0], 0.0], [b[1], 0.0]]).astype(np.float32)
+    cu = np.array([0, 2, 4], np.int32)
+    draft = np.array([[1], [1]], np.int32)
+    ua = np.full((2, 1), np.float32(1.0 - 2.0 ** -24), np.float32)
+    for ub, want in ((0.75, [0, 1]), (0.25, [0, 0])):
+        ubv = np.full(2, ub, np.float32)
+        got = _gpu_sampling(dev, tgt, dft, 2, cu, draft, np.zeros(2), ua, ubv)
+        ref = orc.sampling_accept(tgt, 2, cu, dft, draft, np.zeros(2), ua, ubv)
+        assert got["num_accepted"].tolist() == [0, 0] and ref.num_accepted.tolist() == [0, 0]
+        assert got["bonus"].tolist() == want == ref.bonus.tolist()
+        assert got["status"] == 0

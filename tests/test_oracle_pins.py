@@ -726,3 +726,46 @@ def test_sampling_accept_flags(orc):
     assert r.num_accepted[0] == 0  # an out-of-range draft has p = q = 0: rejected
     bad = orc.sampling_accept(tgt, 4, [0, 3], dft, [[1]], [5], [[0.1]], [0.5])
     assert bad.status & orc.ST_BAD_LEN and bad.bonus[0] == -1 and bad.new_seq_lens[0] == 5
+
+
+def _residual_threshold_case():
+    """Two requests, V = 2, one draft each (token 1), target row p = (1/2,
+    1/2) (logits 0, 0) and proposal q from logits (b, 0): with e = exp(b)
+    (fp32, exact here: 1 - 2^-17 and 1 - 2^-19), q_0 = e / (1 + e) < 1/2 and
+    the residual max(0, p - q) = (W, 0) with W = (1 - e) / (2 (1 + e)):
+    W = 2^-19 / (1 - 2^-18) for request 0 (above 2^-20) and W = 2^-21 /
+    (1 - 2^-20) for request 1 (below).  u_accept = 1 - 2^-24 rejects both
+    drafts (accept iff u q_1 < p_1, and q_1 = 1/2 + W exceeds 1/2 by more
+    than 2^-24 q_1)."""
+    b = np.array([-(2.0 ** -17), -(2.0 ** -19)], np.float32)
+    tgt = np.zeros((4, 2), np.float32)  # rows 0-1 request 0, rows 2-3 request 1
+    dft = np.stack([[b[0], 0.0], [b[1], 0.0]]).astype(np.float32)
+    cu = np.array([0, 2, 4], np.int32)
+    draft = np.array([[1], [1]], np.int32)
+    ua = np.full((2, 1), np.float32(1.0 - 2.0 ** -24), np.float32)
+    return tgt, dft, cu, draft, ua
+
+
+def test_sampling_residual_mass_threshold(orc):
+    """Reading R23's cut-off, pinned on both sides by hand-derived masses
+    ([AVS] §一: accept with probability min(1, p/q), else draw from the
+    normalised residual max(0, p - q)).  A residual of mass W >= 2^-20 is
+    drawn from: it holds token 0 only, so the bonus is 0 whatever u_bonus.
+    A residual of mass W < 2^-20 is read as empty and the bonus is drawn
+    from p = (1/2, 1/2) by inverse CDF: u_bonus = 0.75 gives token 1,
+    u_bonus = 0.25 token 0.  Drawing from p there moves the committed
+    token's distribution by at most W in total variation (the output is
+    min(p, q) + W p instead of min(p, q) + (p - q)+, and both vectors have
+    mass W)."""
+    tgt, dft, cu, draft, ua = _residual_threshold_case()
+    hi = orc.sampling_accept(tgt, 2, cu, dft, draft, np.zeros(2), ua, np.array([0.75, 0.75]))
+    assert hi.num_accepted.tolist() == [0, 0]
+    assert hi.bonus.tolist() == [0, 1]  # residual (token 0) / p (u = 0.75 -> token 1)
+    assert hi.out_tokens.tolist() == [[0, -1], [1, -1]] and hi.status == 0
+    lo = orc.sampling_accept(tgt, 2, cu, dft, draft, np.zeros(2), ua, np.array([0.25, 0.25]))
+    assert lo.num_accepted.tolist() == [0, 0] and lo.bonus.tolist() == [0, 0]
+    # the same masses one step further from the cut-off keep their sides
+    ua_lo = np.full((2, 1), np.float32(0.5), np.float32)
+    acc = orc.sampling_accept(tgt, 2, cu, dft, draft, np.zeros(2), ua_lo, np.array([0.75, 0.75]))
+    assert acc.num_accepted.tolist() == [1, 1]  # u q_1 < p_1: accepted, bonus from row 1's p
+    assert acc.bonus.tolist() == [1, 1]
