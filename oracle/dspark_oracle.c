@@ -504,7 +504,7 @@ void orc_scatter_rows(const unsigned char *src, long long ld_src, long long row_
 
 /* ------------------------------------------------------------ sampling
  *
- * Speculative sampling accept (NEXT-2 of the scope table): [ROUND] §五 names
+ * Speculative sampling accept: [ROUND] §五 names
  * the path (AcceptSampling: chain speculative sampling over the draft's
  * proposal probabilities -- the corrected ones that actually produced the
  * drafts -- and the target probabilities, giving correct_len and the bonus)
@@ -637,7 +637,7 @@ void orc_sampling_accept(const float *tgt, int64_t ld_t, int V, int rows_avail, 
 /* --------------------------------------------------------- calibration
  *
  * STS recorder, calibration statistics and the sequential temperature
- * fitter (NEXT-4 of the scope table).
+ * fitter.
  *
  *   [AVS] §二 "但 SGLang STS 校准的不是同一个 soft target": the recorder
  *         labels a recorded step with the greedy prefix mask, position k is 1
@@ -657,7 +657,7 @@ void orc_sampling_accept(const float *tgt, int64_t ld_t, int V, int rows_avail, 
  *         calibration, ECE, Brier score or log loss, by depth, with a
  *         reliability diagram.
  *
- * Readings (also in the design notes):
+ * Readings of what the pages leave open:
  *   R24 a recorded sample is (z[gamma], correct, tested): tested = drafts
  *       the target checked (verify_len - 1; gamma for a full block).  Depth
  *       k is observed iff k < tested; label y_k = (k < correct).  A depth

@@ -644,7 +644,7 @@ def test_plan_ex_tier_alignment_paid_padding(orc):
     assert none.budget == plain.budget and np.array_equal(none.verify_lens, plain.verify_lens)
 
 
-# ------------------------------------------------ sampling accept (NEXT-2)
+# ------------------------------------------------ sampling accept ([ROUND] §五 AcceptSampling)
 
 def _logp(p):
     with np.errstate(divide="ignore"):
