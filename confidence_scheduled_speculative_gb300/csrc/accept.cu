@@ -496,18 +496,20 @@ extern "C" int dspark_cap_accept(const void *logits, int32_t dtype, int64_t ld, 
 // ------------------------------------------------- allocation-free variant
 //
 // dspark_greedy_accept_static: the same compact-mode greedy accept, for
-// callers that cannot allocate device memory -- for example code running
-// inside a captured or replayed graph whose allocator is frozen, an embedding
-// that only hands over tensors it owns, or a runtime that forbids cudaMalloc
-// after start-up.  Its scratch (the per-CTA partials of the argmax) lives in
-// the file-scope array below instead of a caller workspace.  Every GPU that
-// loads this library holds the array (about 300 KB) until the process exits.
+// callers that cannot allocate device memory -- an embedding that hands over
+// only tensors it owns, or a runtime whose device memory is fixed at start-up
+// and which forbids cudaMalloc afterwards.  Its scratch (the per-CTA partials
+// of the argmax) lives in the file-scope array below instead of a caller
+// workspace.  Every GPU that loads this library holds the array (about
+// 300 KB) until the process exits.
 
 namespace dspark {
 
 constexpr int kStaticMaxRows = 32768;  // largest max_rows the static scratch serves
+// partial slots, rounded up to whole 256-byte blocks like a workspace
+constexpr int kStaticSlots = ((kMaxCtas + kStaticMaxRows + 1) + 31) / 32 * 32;
 
-static __device__ __align__(256) Partial g_static_partials[kMaxCtas + kStaticMaxRows + 1];
+static __device__ __align__(256) Partial g_static_partials[kStaticSlots];
 
 namespace {
 constexpr int kMaxStaticDevices = 64;
@@ -517,7 +519,8 @@ std::atomic<Partial *> g_static_ptr[kMaxStaticDevices];
 // Device address of g_static_partials on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is taken
 // once per device with cudaGetSymbolAddress (which also loads this module
-// on that device).
+// on that device) and kept for the life of the process; a cudaDeviceReset
+// unloads the module, so the kept address is then stale.
 static cudaError_t static_partials(Partial **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -543,6 +546,7 @@ extern "C" int dspark_greedy_accept_static(const void *logits, int32_t dtype, in
                                            int32_t *bonus, int32_t *commit_lens,
                                            int32_t *new_seq_lens, int32_t *out_tokens,
                                            int32_t *status, void *stream) {
+    static_assert(sizeof(g_static_partials) % 256 == 0, "whole 256-byte blocks");
     int rc = check_common(logits, dtype, ld, V, draft, prefix_lens, B, gamma, num_accepted, bonus,
                           commit_lens, new_seq_lens, out_tokens, status);
     if (rc != DSPARK_OK) return rc;
@@ -550,31 +554,7 @@ extern "C" int dspark_greedy_accept_static(const void *logits, int32_t dtype, in
     if (max_rows > kStaticMaxRows) return DSPARK_ERR_UNSUPPORTED;
     Partial *partial = nullptr;
     if (static_partials(&partial) != cudaSuccess) return DSPARK_ERR_CUDA;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t esize = dtype == DSPARK_DTYPE_BF16 ? 2 : 4;
-    const bool vec = aligned(logits, 16) && ((ld * (long long)esize) % 16 == 0);
-    const int grid = argmax_grid();
-    ArgmaxArgs a;
-    a.logits = logits;
-    a.ld = ld;
-    a.V = V;
-    a.rows_host = 0;
-    a.rows_dev = cu_seqlens + B;
-    a.max_rows = max_rows;
-    a.partial = partial;  // every slot the finalize reads is written first: no clearing needed
-    a.status = status;
-    a.zero_totals = nullptr;
-    cudaError_t e = dtype == DSPARK_DTYPE_BF16 ? launch_argmax<__nv_bfloat16>(a, vec, grid, s)
-                                               : launch_argmax<float>(a, vec, grid, s);
-    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
     FinalArgs f = {};
-    f.rows_host = 0;
-    f.rows_dev = cu_seqlens + B;
-    f.max_rows = max_rows;
-    f.V = V;
-    f.epc = vec ? (int)(16 / esize) : 1;
-    f.grid = grid;
-    f.partial = partial;
     f.cu = cu_seqlens;
     f.draft = draft;
     f.prefix = prefix_lens;
@@ -587,7 +567,8 @@ extern "C" int dspark_greedy_accept_static(const void *logits, int32_t dtype, in
     f.new_seq = new_seq_lens;
     f.out = out_tokens;
     f.status = status;
-    const int fgrid = (B + kFinalWarps - 1) / kFinalWarps;
-    e = launch_pdl(greedy_finalize_kernel, dim3(fgrid), dim3(kFinalWarps * 32), 0, s, f);
-    return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+    // the array stands in for the workspace: every slot the finalize reads
+    // is written earlier in the same call, so nothing needs clearing
+    return run_accept(logits, dtype, ld, V, max_rows, 0, cu_seqlens + B, f, false, partial,
+                      sizeof(g_static_partials), static_cast<cudaStream_t>(stream));
 }

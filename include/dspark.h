@@ -313,13 +313,31 @@ DSPARK_API int dspark_sampling_accept_ex(const void *target_logits, int32_t dtyp
  * buffers, both strides and the row size are 16-byte multiples, else 2-byte
  * copies.  A destination outside [0, dst_rows) is skipped and flagged
  * DSPARK_STATUS_BAD_INDEX; DSPARK_STATUS_TIMEOUT if a copy did not complete
- * within 200 ms.
+ * within 200 ms (that CTA then copies nothing more: the rows it had left are
+ * not written).
  * Errors: INVALID_ARG (null pointer, elem_bytes not 2 or 4, width < 1, a
  * stride below width, negative row counts); CUDA. */
 DSPARK_API int dspark_scatter_compact_to_strided(const void *src, int64_t ld_src, int32_t width,
                                       int32_t elem_bytes, const int32_t *packed_src,
                                       const int32_t *totals, int32_t max_rows, void *dst,
                                       int64_t ld_dst, int32_t dst_rows, int32_t *status,
+                                      void *stream);
+
+/* dspark_scatter_compact_to_strided with the limit of one pipeline wait of
+ * the TMA path in the caller's hands (no counterpart on the pages: failure
+ * detection).
+ *   wait_limit_ns  < 0: 200 ms (the default); 0: each wait tests its copy
+ *                  once, so a copy not yet landed at the first test gives
+ *                  up -- how the tests exercise the give-up path.
+ * A CTA that gives up flags DSPARK_STATUS_TIMEOUT, issues nothing more,
+ * waits (up to 200 ms each, whatever wait_limit_ns) for the loads it still
+ * has in flight and for its stores, and exits; the call returns normally and
+ * the rows that CTA had left are not written.  The 2-byte path has no waits. */
+DSPARK_API int dspark_scatter_compact_to_strided_ex(const void *src, int64_t ld_src,
+                                      int32_t width, int32_t elem_bytes,
+                                      const int32_t *packed_src, const int32_t *totals,
+                                      int32_t max_rows, void *dst, int64_t ld_dst,
+                                      int32_t dst_rows, int64_t wait_limit_ns, int32_t *status,
                                       void *stream);
 
 /* dspark_plan_pack with options (see dspark_plan_options; alignment uses
@@ -404,18 +422,23 @@ DSPARK_API int dspark_cap_accept(const void *logits, int32_t dtype, int64_t ld, 
 #define DSPARK_STATIC_MAX_ROWS 32768
 
 /* dspark_greedy_accept without a workspace.  The pages have no counterpart:
- * this exists for callers that cannot allocate device memory (code running
- * while a graph's memory is frozen, embeddings that only pass in buffers they
- * own, runtimes that forbid cudaMalloc after start-up).
+ * this exists for callers that cannot allocate device memory (embeddings
+ * that only pass in buffers they own, runtimes whose device memory is fixed
+ * at start-up and that forbid cudaMalloc afterwards).
  *   Arguments, outputs and device flags are those of dspark_greedy_accept,
  *   minus workspace / workspace_bytes.
  *   Scratch: a file-scope device array of (4096 + 32768 + 1) * 8 bytes
- *   (~300 KB) that every GPU loading this library holds until the process
- *   exits.  max_rows may be at most DSPARK_STATIC_MAX_ROWS (else
- *   DSPARK_ERR_UNSUPPORTED, nothing enqueued).
+ *   rounded up to 256 (~300 KB) that every GPU loading this library holds
+ *   until the process exits.  max_rows may be at most DSPARK_STATIC_MAX_ROWS
+ *   (else DSPARK_ERR_UNSUPPORTED, nothing enqueued); a device row count
+ *   cu_seqlens[B] above max_rows is clamped to max_rows and flags
+ *   DSPARK_STATUS_CAPACITY, as in dspark_greedy_accept.
  *   The first call on a device looks up the array's device address with
- *   cudaGetSymbolAddress (and so loads the module on that device); make that
- *   first call on each device before any stream capture.
+ *   cudaGetSymbolAddress (and so loads the module on that device) and keeps
+ *   it for the life of the process; make that first call on each device
+ *   before any stream capture.  cudaDeviceReset unloads the module and makes
+ *   the kept address stale: a process that resets a device must not call
+ *   this function on that device afterwards.
  *   Every call shares the one array: calls whose kernels may overlap on the
  *   GPU (different streams without ordering) race on it.  The array keeps the
  *   last call's contents; nothing in it needs clearing, because every slot a

@@ -1,13 +1,13 @@
 """The allocation-free greedy accept (dspark_greedy_accept_static) against the
 workspace version (dspark_greedy_accept), through the C ABI.
 
-Some callers cannot allocate device memory -- code running while a graph's
-memory pool is frozen, embeddings that only pass in buffers they own,
-runtimes that forbid cudaMalloc after start-up -- so the library offers this
-variant whose scratch is a library-owned device array.  Two calls in a row,
-on inputs of different sizes, must each match the workspace version exactly
-(the outputs are token ids and counts), also when the second call runs over
-the scratch the first one left behind.  This file is collected last."""
+Some callers cannot allocate device memory -- embeddings that only pass in
+buffers they own, runtimes whose device memory is fixed at start-up and that
+forbid cudaMalloc afterwards -- so the library offers this variant whose
+scratch is a library-owned device array.  Two calls in a row, on inputs of
+different sizes, must each match the workspace version exactly (the outputs
+are token ids and counts), also when the second call runs over the scratch
+the first one left behind.  This file is collected last."""
 
 import numpy as np
 import pytest
@@ -38,7 +38,7 @@ def _problem(seed, B, gamma, V, dtype):
     return x, cu, draft, prefix
 
 
-def _run(dev, fn, x, cu, draft, prefix, V, with_ws):
+def _run(dev, fn, x, cu, draft, prefix, V, with_ws, max_rows=None):
     from confidence_scheduled_speculative_gb300 import api
     B, g = draft.shape
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
@@ -51,6 +51,8 @@ def _run(dev, fn, x, cu, draft, prefix, V, with_ws):
     status = torch.zeros(1, **i32)
     kw = dict(V=V, cu_seqlens=t(cu), draft=t(draft), prefix_lens=t(prefix), B=B, gamma=g,
               status=status, **out)
+    if max_rows is not None:
+        kw["max_rows"] = max_rows
     if with_ws:
         kw["workspace"] = api.workspace(api.dspark_accept_workspace_bytes(rows, V), dev)
     fn(logits, **kw)
@@ -86,3 +88,22 @@ def test_static_scratch_rejects_rows_beyond_its_maximum():
             num_accepted=z(2), bonus=z(2), commit_lens=z(2), out_tokens=z(2, 4), status=z(1),
             max_rows=api.STATIC_MAX_ROWS + 1)
     assert e.value.code == api.DSPARK_ERR_UNSUPPORTED
+
+
+def test_static_scratch_clamps_device_rows_above_max_rows():
+    """cu_seqlens[B] above max_rows: both versions clamp the rows to max_rows,
+    flag DSPARK_STATUS_CAPACITY, leave the argmax of later rows untouched and
+    give the requests past the clamp no acceptance (BAD_LEN), identically."""
+    dev = require_gpu()
+    from confidence_scheduled_speculative_gb300 import api
+    x, cu, draft, prefix = _problem(21, 40, 8, 20000, "bf16")
+    max_rows = int(cu[-1]) - 13
+    ref = _run(dev, api.dspark_greedy_accept, x, cu, draft, prefix, 20000, True, max_rows)
+    got = _run(dev, api.dspark_greedy_accept_static, x, cu, draft, prefix, 20000, False,
+               max_rows)
+    for k in KEYS:
+        np.testing.assert_array_equal(got[k], ref[k], err_msg=k)
+    assert got["status"] & api.STATUS_CAPACITY and got["status"] & api.STATUS_BAD_LEN
+    assert np.all(got["argmax"][max_rows:] == -5) and np.all(got["argmax"][:max_rows] >= 0)
+    cut = int(np.searchsorted(cu, max_rows, side="right")) - 1  # first request past the clamp
+    assert np.all(got["num_accepted"][cut:] == 0) and np.all(got["bonus"][cut:] == -1)
