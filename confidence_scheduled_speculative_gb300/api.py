@@ -31,6 +31,8 @@ STATUS_BAD_INPUT = 8
 STATUS_BAD_LEN = 16
 STATUS_BAD_COST = 32
 STATUS_INFEASIBLE = 64
+STATUS_BAD_INDEX = 128
+STATUS_TIMEOUT = 256
 
 # cost tables of at most this many entries take the planner's single-CTA
 # select path (the pack fused into it); larger ones the multi-CTA rank path
@@ -97,6 +99,9 @@ _SIGS = {
                                         _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
     "dspark_scatter_compact_to_strided": (ctypes.c_int, [_VP, _I64, _I32, _I32, _VP, _VP, _I32,
                                                          _VP, _I64, _I32, _VP, _VP]),
+    "dspark_scatter_compact_to_strided_ex": (ctypes.c_int, [_VP, _I64, _I32, _I32, _VP, _VP,
+                                                            _I32, _VP, _I64, _I32, _I64, _VP,
+                                                            _VP]),
     "dspark_sampling_workspace_bytes": (_SZ, [_I32, _I32, _I32]),
     "dspark_sampling_accept": (ctypes.c_int, [_VP, _I32, _I64, _I32, _I32, _VP, _VP, _I64, _VP,
                                               _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
@@ -299,21 +304,30 @@ def dspark_plan_pack(conf_logits, sts_temps, anchor, draft, prefix_lens, *, B, g
 
 
 def dspark_scatter_compact_to_strided(src, packed_src, totals, dst, *, status,
-                                      stream=None) -> None:
+                                      wait_limit_ns=None, stream=None) -> None:
     """Copy packed row i < totals[0] of ``src`` [max_rows, width] to row
     packed_src[i] of ``dst`` [B*(gamma+1), >= width] (2-D, same dtype:
-    bfloat16, float16 or float32, unit inner stride)."""
+    bfloat16, float16 or float32, unit inner stride).  ``wait_limit_ns``
+    (dspark_scatter_compact_to_strided_ex) bounds one pipeline wait of the
+    TMA path; None keeps the 200 ms default."""
     for name, t in (("src", src), ("dst", dst)):
         if not t.is_cuda or t.dim() != 2 or t.stride(1) != 1:
             raise ValueError(f"{name}: expected a 2-D CUDA tensor with unit inner stride")
     if src.dtype != dst.dtype or src.element_size() not in (2, 4):
         raise ValueError("src and dst: same dtype of 2 or 4 bytes")
-    rc = load().dspark_scatter_compact_to_strided(
-        src.data_ptr(), src.stride(0), src.size(1), src.element_size(),
-        _p(packed_src, torch.int32, "packed_src"), _p(totals, torch.int32, "totals"),
-        src.size(0), dst.data_ptr(), dst.stride(0), dst.size(0),
-        _p(status, torch.int32, "status"), _stream(stream))
-    _check("dspark_scatter_compact_to_strided", rc)
+    args = (src.data_ptr(), src.stride(0), src.size(1), src.element_size(),
+            _p(packed_src, torch.int32, "packed_src"), _p(totals, torch.int32, "totals"),
+            src.size(0), dst.data_ptr(), dst.stride(0), dst.size(0))
+    if wait_limit_ns is None:
+        name = "dspark_scatter_compact_to_strided"
+        rc = load().dspark_scatter_compact_to_strided(*args, _p(status, torch.int32, "status"),
+                                                      _stream(stream))
+    else:
+        name = "dspark_scatter_compact_to_strided_ex"
+        rc = load().dspark_scatter_compact_to_strided_ex(*args, int(wait_limit_ns),
+                                                         _p(status, torch.int32, "status"),
+                                                         _stream(stream))
+    _check(name, rc)
 
 
 def _dtype_code(t: torch.Tensor) -> int:

@@ -1,13 +1,12 @@
 // bulk.cuh -- helpers for TMA bulk copies (cp.async.bulk) completing on
-// shared-memory mbarriers, shared by the scatter and the sampling
-// normalizer.
+// shared-memory mbarriers (used by the scatter).
 #pragma once
 
 #include <cstdint>
 
 namespace dspark {
 
-constexpr unsigned long long kWaitLimitNs = 200000000ull;  // 200 ms
+constexpr unsigned long long kWaitLimitNs = 200000000ull;  // 200 ms: the default limit
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -24,8 +23,10 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
 }
 
 // Wait for the given phase parity of an mbarrier: a non-blocking test in a
-// loop, given up after kWaitLimitNs of wall time (false).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// loop, given up (false) once limit_ns of wall time have passed since the
+// first test; limit_ns = 0 tests once.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     const unsigned long long start = global_ns();
     for (;;) {
         uint32_t done;
@@ -36,7 +37,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
             : "r"(bar), "r"(parity)
             : "memory");
         if (done) return true;
-        if (global_ns() - start > kWaitLimitNs) return false;
+        if (global_ns() - start >= limit_ns) return false;
         __nanosleep(32);
     }
 }

@@ -18,9 +18,11 @@
 // per CTA does not depend on the ragged row count, which only the device
 // knows), and one thread runs a 4-stage pipeline -- cp.async.bulk global ->
 // shared completing on an mbarrier, then cp.async.bulk shared -> global --
-// so 64 KB per CTA are in flight with no per-element instructions.  Every
-// wait on an mbarrier gives up after 200 ms (DSPARK_STATUS_TIMEOUT), after
-// letting the copies in flight land.  Other rows are copied 2 bytes at a
+// so 64 KB per CTA are in flight with no per-element instructions.  A
+// pipeline wait on an mbarrier gives up after wait_ns (200 ms unless the
+// caller sets it) and flags DSPARK_STATUS_TIMEOUT; the CTA then copies
+// nothing more, waits (up to 200 ms each) for the loads it still has in
+// flight and for its stores, and exits.  Other rows are copied 2 bytes at a
 // time by all threads.
 
 #include "dspark_common.cuh"
@@ -42,6 +44,7 @@ struct ScatterArgs {
     const int32_t *packed_src;
     const int32_t *totals;
     int max_rows, dst_rows;
+    unsigned long long wait_ns;  // limit of one pipeline wait
     int32_t *status;
 };
 
@@ -75,11 +78,13 @@ __global__ void __launch_bounds__(32) scatter_bulk_kernel(ScatterArgs a) {
     for (int s = 0; s < kBulkStages; ++s) mbar_init(smem_addr(&bar[s]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 
+    uint32_t inflight = 0;  // bit s: a load into stage s is issued and not yet waited for
     auto load = [&](long long i) {
         int r, bytes;
         long long off;
         bulk_segment(a, spr, t0 + i, r, off, bytes);
         const int s = (int)(i % kBulkStages);
+        inflight |= 1u << s;
         const uint32_t b = smem_addr(&bar[s]);
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes)
                      : "memory");
@@ -94,10 +99,11 @@ __global__ void __launch_bounds__(32) scatter_bulk_kernel(ScatterArgs a) {
     for (long long i = 0; i < min(n, (long long)kBulkStages); ++i) load(i);
     for (long long i = 0; i < n; ++i) {
         const int s = (int)(i % kBulkStages);
-        if (!mbar_wait(smem_addr(&bar[s]), (phase >> s) & 1u)) {
+        if (!mbar_wait(smem_addr(&bar[s]), (phase >> s) & 1u, a.wait_ns)) {
             timeout = true;
             break;
         }
+        inflight &= ~(1u << s);
         phase ^= 1u << s;
         int r, bytes;
         long long off;
@@ -119,8 +125,9 @@ __global__ void __launch_bounds__(32) scatter_bulk_kernel(ScatterArgs a) {
             load(i + kBulkStages);
         }
     }
-    if (timeout) {  // let the loads in flight land before the CTA exits
-        for (int s = 0; s < kBulkStages; ++s) mbar_wait(smem_addr(&bar[s]), (phase >> s) & 1u);
+    if (timeout) {  // let the loads still in flight land before the CTA exits
+        for (int s = 0; s < kBulkStages; ++s)
+            if ((inflight >> s) & 1u) mbar_wait(smem_addr(&bar[s]), (phase >> s) & 1u);
         flag(a.status, DSPARK_STATUS_TIMEOUT);
     }
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -162,11 +169,13 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_rows_kernel(ScatterAr
 
 using namespace dspark;
 
-extern "C" int dspark_scatter_compact_to_strided(const void *src, int64_t ld_src, int32_t width,
-                                                 int32_t elem_bytes, const int32_t *packed_src,
-                                                 const int32_t *totals, int32_t max_rows,
-                                                 void *dst, int64_t ld_dst, int32_t dst_rows,
-                                                 int32_t *status, void *stream) {
+extern "C" int dspark_scatter_compact_to_strided_ex(const void *src, int64_t ld_src,
+                                                    int32_t width, int32_t elem_bytes,
+                                                    const int32_t *packed_src,
+                                                    const int32_t *totals, int32_t max_rows,
+                                                    void *dst, int64_t ld_dst, int32_t dst_rows,
+                                                    int64_t wait_limit_ns, int32_t *status,
+                                                    void *stream) {
     if (!src || !dst || !packed_src || !totals || !status) return DSPARK_ERR_INVALID_ARG;
     if (elem_bytes != 2 && elem_bytes != 4) return DSPARK_ERR_INVALID_ARG;
     if (width < 1 || ld_src < width || ld_dst < width || max_rows < 0 || dst_rows < 0)
@@ -181,6 +190,7 @@ extern "C" int dspark_scatter_compact_to_strided(const void *src, int64_t ld_src
     a.totals = totals;
     a.max_rows = max_rows;
     a.dst_rows = dst_rows;
+    a.wait_ns = wait_limit_ns < 0 ? kWaitLimitNs : (unsigned long long)wait_limit_ns;
     a.status = status;
     // TMA bulk copies need 16-byte aligned addresses and sizes
     const bool bulk = aligned(src, 16) && aligned(dst, 16) && a.ld_src % 16 == 0 &&
@@ -197,4 +207,14 @@ extern "C" int dspark_scatter_compact_to_strided(const void *src, int64_t ld_src
         e = launch_pdl(scatter_rows_kernel, dim3(sm_count() * 4), dim3(kScatterThreads), 0, s, a);
     }
     return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+extern "C" int dspark_scatter_compact_to_strided(const void *src, int64_t ld_src, int32_t width,
+                                                 int32_t elem_bytes, const int32_t *packed_src,
+                                                 const int32_t *totals, int32_t max_rows,
+                                                 void *dst, int64_t ld_dst, int32_t dst_rows,
+                                                 int32_t *status, void *stream) {
+    return dspark_scatter_compact_to_strided_ex(src, ld_src, width, elem_bytes, packed_src, totals,
+                                                max_rows, dst, ld_dst, dst_rows, -1, status,
+                                                stream);
 }

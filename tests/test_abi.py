@@ -197,6 +197,12 @@ def test_scatter_argument_checks(lib):
     assert call(ld_src=7) == -1
     assert call(ld_dst=4) == -1
     assert call(rows=-1) == -1
+    g = lib.dspark_scatter_compact_to_strided_ex
+    g.restype = ctypes.c_int
+    assert g(None, ctypes.c_int64(8), 8, 2, FAKE, FAKE, 4, FAKE, ctypes.c_int64(8), 10,
+             ctypes.c_int64(0), FAKE, None) == -1
+    assert g(FAKE, ctypes.c_int64(8), 8, 3, FAKE, FAKE, 4, FAKE, ctypes.c_int64(8), 10,
+             ctypes.c_int64(-1), FAKE, None) == -1
 
 
 def test_sampling_argument_checks(lib):

@@ -88,3 +88,31 @@ def test_scatter_workload_full_size(dev, orc):
     mask = torch.ones(strided.size(0), dtype=torch.bool, device=dev)
     mask[src] = False
     assert bool((strided[mask] == -7.0).all()) and int(st.item()) == 0
+
+
+def test_scatter_gives_up_and_returns(dev, orc):
+    """Failure detection without a fault: with the pipeline wait limited to 0
+    (one test per wait) the TMA path's first wait finds its copy still in
+    flight, gives up, flags DSPARK_STATUS_TIMEOUT, lets its in-flight copies
+    land and returns.  The context stays usable: the same call with the
+    default limit, and with a long explicit one, then matches the oracle."""
+    from confidence_scheduled_speculative_gb300 import api
+    rng = np.random.default_rng(17)
+    B, g, width = 24, 7, 24576  # 48 KB bf16 rows: three 16 KB segments each
+    lens = rng.integers(1, g + 2, size=B).astype(np.int32)
+    p = orc.pack(np.zeros(B), np.zeros((B, g)), np.zeros(B), lens, [], B * (g + 1))
+    src_np = rng.integers(0, 2 ** 15, size=(p.total, width)).astype(np.uint16)
+    dst_np = rng.integers(0, 2 ** 15, size=(B * (g + 1), width)).astype(np.uint16)
+    t32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    src = torch.from_numpy(src_np.view(np.int16)).to(dev).view(torch.bfloat16)
+    src_of, totals = t32(p.src[:p.total]), t32([p.total])
+    ref, _ = orc.scatter_rows(src_np, p.src[:p.total], p.total, dst_np)
+    for limit, want in ((0, api.STATUS_TIMEOUT), (None, 0), (10 ** 10, 0)):
+        dst = torch.from_numpy(dst_np.view(np.int16)).to(dev).view(torch.bfloat16)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        api.dspark_scatter_compact_to_strided(src, src_of, totals, dst, status=st,
+                                              wait_limit_ns=limit)
+        torch.cuda.synchronize()
+        assert int(st.item()) == want, (limit, int(st.item()))
+        if want == 0:
+            np.testing.assert_array_equal(dst.cpu().view(torch.int16).numpy(), ref.view(np.int16))
