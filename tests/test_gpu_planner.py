@@ -203,6 +203,14 @@ def _select_case(name):
         z = rng.normal(1.0, 1.2, (512, 16)).astype(np.float32)
         M = np.linspace(512, 512 * 17, 31).astype(np.int32)
         return dict(base, B=512, gamma=16, z=z, kind=0, M=M, val=1.0 / (1e-3 + 2e-6 * M))
+    if name == "thirty_one_entries_forced":  # 32 slots, few gathered candidates
+        # every table entry's range holds budgets <= the 8048 kept candidates
+        # and the forced budget takes the 32nd slot; the marked bins gather
+        # 187 candidates, ranked by counting (not the radix passes)
+        z = rng.normal(1.0, 1.2, (512, 16)).astype(np.float32)
+        M = np.linspace(512, 8400, 31).astype(np.int32)
+        return dict(base, B=512, gamma=16, z=z, kind=0, M=M, val=1.0 / (1e-3 + 2e-6 * M),
+                    forced=2222)
     if name == "thirty_one_entries_ties":  # 32 slots through the radix passes
         z = np.tile(rng.normal(2.0, 1.0, 16).astype(np.float32), (1000, 1))
         M = np.linspace(1000, 16000, 31).astype(np.int32)
@@ -213,7 +221,7 @@ def _select_case(name):
 @pytest.mark.parametrize("name", ["all_ones", "all_ones_forced", "half_saturated",
                                   "identical_requests", "identical_forced", "large_spread",
                                   "sixteen_entries", "thirty_one_entries",
-                                  "thirty_one_entries_ties"])
+                                  "thirty_one_entries_forced", "thirty_one_entries_ties"])
 def test_plan_select_bins(dev, orc, name):
     P = _select_case(name)
     g = _gpu_plan(dev, P)
@@ -434,6 +442,33 @@ def test_plan_pack_fused_random(dev, orc, seed):
     ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"], P["kind"],
                    P["M"], P["val"], P["bias"], P["alpha"])
     exp = compare_plan(f"fused/{seed}", got, ref, B, g, P["min_len"], _restage(orc, P))
+    pr = orc.pack(anchor, draft, prefix, exp.verify_lens, tiers, cap, sentinel=-9)
+    np.testing.assert_array_equal(got["cu_seqlens"], pr.cu_seqlens)
+    assert list(got["totals"]) == [pr.total, pr.padded]
+    for k in ("ids", "pos", "req", "src"):
+        np.testing.assert_array_equal(got[k], pr[k][:cap], err_msg=k)
+    assert int(got["status"][0]) == (exp.status | pr.status)
+
+
+@pytest.mark.parametrize("name", ["thirty_one_entries", "thirty_one_entries_forced",
+                                  "thirty_one_entries_ties"])
+def test_plan_pack_fused_select_31_entries(dev, orc, name):
+    """The select path's largest table through the fused call: budget,
+    verify_lens and the packed window bit for bit against the oracle's
+    planner and pack, with both ways of finding the thresholds (counting the
+    gathered candidates, radix passes) holding all 32 slots."""
+    P = _select_case(name)
+    B, g = P["B"], P["gamma"]
+    rng = np.random.default_rng(5)
+    anchor = rng.integers(0, 1 << 20, B).astype(np.int32)
+    draft = rng.integers(0, 1 << 20, (B, g)).astype(np.int32)
+    prefix = rng.integers(1, 8192, B).astype(np.int32)
+    tiers = [1 << i for i in range(9, 16)]
+    cap = 1 << 15
+    got = _fused(dev, P, anchor, prefix, draft, tiers, cap)
+    ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"], P["kind"],
+                   P["M"], P["val"], P["bias"], P["alpha"])
+    exp = compare_plan(f"fused31/{name}", got, ref, B, g, P["min_len"], _restage(orc, P))
     pr = orc.pack(anchor, draft, prefix, exp.verify_lens, tiers, cap, sentinel=-9)
     np.testing.assert_array_equal(got["cu_seqlens"], pr.cu_seqlens)
     assert list(got["totals"]) == [pr.total, pr.padded]
