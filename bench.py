@@ -175,17 +175,22 @@ def oracle_step_timing(step, compact, budget_s, max_steps=None, row_fraction=1.0
         p = oracle.pack(step.anchor, step.draft, step.prefix_lens, r.verify_lens, step.tiers,
                         step.capacity)
         t1 = time.perf_counter()
+        # n_rows consecutive packed rows from the cursor, wrapping around at
+        # the end: every step samples the same number of rows
         lo = cursor % rows
-        hi = min(rows, lo + n_rows)
-        am, _ = oracle.argmax_rows(compact[lo:hi], V=w.V)
+        hi = lo + n_rows
         full_am = np.zeros(rows, np.int32)
-        full_am[lo:hi] = am
+        am, _ = oracle.argmax_rows(compact[lo:min(hi, rows)], V=w.V)
+        full_am[lo:min(hi, rows)] = am
+        if hi > rows:
+            am2, _ = oracle.argmax_rows(compact[:hi - rows], V=w.V)
+            full_am[:hi - rows] = am2
         oracle.greedy_finalize(full_am, rows, p.cu_seqlens, step.draft, step.prefix_lens, w.V)
         t2 = time.perf_counter()
-        cursor = hi
+        cursor = hi % rows
         t_pp += t1 - t0
         t_acc += t2 - t1
-        rows_done += hi - lo
+        rows_done += n_rows
         steps += 1
         if time.perf_counter() - start >= budget_s or (max_steps and steps >= max_steps):
             break
@@ -202,16 +207,43 @@ def make_inputs(name: str, seed: int):
     return step, strided
 
 
+# Arm Ltd. (implementer 0x41) part numbers of the server cores this may run on
+ARM_PARTS = {0xd0c: "Neoverse-N1", 0xd40: "Neoverse-V1", 0xd49: "Neoverse-N2",
+             0xd4f: "Neoverse-V2", 0xd84: "Neoverse-V3", 0xd8e: "Neoverse-N3"}
+
+
 def cpu_info():
-    model = None
+    """Host CPU: the x86 model name, else lscpu's model name, else the Arm
+    part number named from ARM_PARTS."""
+    model, part, impl = None, None, None
     try:
         with open("/proc/cpuinfo") as f:
             for ln in f:
-                if ln.lower().startswith(("model name", "cpu part", "processor name")):
-                    model = ln.split(":", 1)[1].strip()
-                    break
+                key, _, val = ln.partition(":")
+                key, val = key.strip().lower(), val.strip()
+                if key in ("model name", "processor name") and model is None:
+                    model = val
+                elif key == "cpu part" and part is None:
+                    part = val
+                elif key == "cpu implementer" and impl is None:
+                    impl = val
     except OSError:
         pass
+    if model is None:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for ln in out.splitlines():
+                if ln.lower().startswith("model name:"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    if (model is None or model.startswith("-")) and part is not None:
+        try:
+            name = ARM_PARTS.get(int(part, 16)) if impl in (None, "0x41") else None
+        except ValueError:
+            name = None
+        model = name or f"cpu part {part}"
     return {"nproc": os.cpu_count(), "model": model}
 
 
@@ -384,27 +416,33 @@ def accept_rows_sweep(dev, stream, seed, reps=20):
     return out
 
 
-def mixed_cap_report(dev, n_steps=16):
+def mixed_cap_report(dev, n_steps=200):
     """The mixed-traffic report of cap-accept (B=128, gamma=12, three
     acceptance classes, 1-D SPS table): over independent steps (seeds
     0..n_steps-1, no state carried) the planner's tau at its budget (the
     expected commit under calibrated confidences), the delivered commit
     sum(min(raw, len - 1) + 1) and the ceiling sum(raw + 1) of verifying
-    every depth.  The target rows follow the workload recipe -- N(0,1) with a
-    +8 peak at the draft token with the row's match probability, else at
-    another uniform token -- drawn on the device (a statistical report: the
-    rows are not the shared generator's bits)."""
+    every depth, overall and per class (request r has class r mod 3, match
+    probability 0.9 / 0.6 / 0.3 per depth): a class's tau is the number of
+    its requests plus its selected survivals.  The target rows follow the
+    workload recipe -- N(0,1) with a +8 peak at the draft token with the
+    row's match probability, else at another uniform token -- drawn on the
+    device (a statistical report: the rows are not the shared generator's
+    bits)."""
     import torch
     from confidence_scheduled_speculative_gb300 import workloads as wl
     from confidence_scheduled_speculative_gb300.engine import StepConfig, VerifyStep
     w = wl.MIXED
     out = {"workload": f"mixed B={w.B} gamma={w.gamma} V={w.V} cap-accept, 1-D SPS table",
-           "steps": n_steps}
+           "steps": n_steps, "seeds": f"0..{n_steps - 1}"}
     try:
         rows = w.B * (w.gamma + 1)
         logits = torch.empty((rows, w.V), dtype=torch.bfloat16, device=dev)
         gen = torch.Generator(device=dev)
-        tau = deliv = ceil = 0.0
+        cls = np.arange(w.B) % 3
+        names = ("p0.9", "p0.6", "p0.3")
+        acc = {k: np.zeros(3) for k in ("tau", "delivered", "ceiling", "rows")}
+        budget = 0
         for seed in range(n_steps):
             step = wl.make_step(w, seed=seed)
             rng = np.random.default_rng(np.random.SeedSequence([7919, seed]))
@@ -421,14 +459,36 @@ def mixed_cap_report(dev, n_steps=16):
             vs.load_inputs(step)
             vs.plan()
             vs.cap_accept(logits, write_argmax=False)
-            tot = vs.cap_totals.cpu().tolist()
-            tau += float(vs.tau_theta[0].item())
-            deliv += tot[0]
-            ceil += tot[1]
+            lens = vs.verify_lens.cpu().numpy().astype(np.int64)
+            s = vs.survivals.cpu().numpy().astype(np.float64)
+            commit = vs.commit_lens.cpu().numpy().astype(np.int64)
+            raw = vs.ceiling.cpu().numpy().astype(np.int64)
+            sel = np.arange(w.gamma)[None, :] < (lens - 1)[:, None]  # selected candidates
+            tau_r = 1.0 + (s * sel).sum(axis=1)
+            for c in range(3):
+                m = cls == c
+                acc["tau"][c] += tau_r[m].sum()
+                acc["delivered"][c] += commit[m].sum()
+                acc["ceiling"][c] += (raw[m] + 1).sum()
+                acc["rows"][c] += lens[m].sum()
+            budget += int(vs.budget.item())
             out["status"] = out.get("status", 0) | int(vs.status.item())
-        out.update({"mean_tau": tau / n_steps, "mean_delivered": deliv / n_steps,
-                    "mean_ceiling": ceil / n_steps, "delivered_over_ceiling": deliv / ceil,
-                    "delivered_over_tau": deliv / tau})
+        n_cls = np.bincount(cls, minlength=3)
+        per = {}
+        for c in range(3):
+            per[names[c]] = {
+                "requests": int(n_cls[c]),
+                "mean_verify_len": acc["rows"][c] / (n_steps * n_cls[c]),
+                "mean_tau": acc["tau"][c] / n_steps,
+                "mean_delivered": acc["delivered"][c] / n_steps,
+                "mean_ceiling": acc["ceiling"][c] / n_steps,
+                "delivered_over_ceiling": acc["delivered"][c] / acc["ceiling"][c],
+                "delivered_over_tau": acc["delivered"][c] / acc["tau"][c]}
+        tau, deliv, ceil = (acc[k].sum() for k in ("tau", "delivered", "ceiling"))
+        out.update({"mean_budget": budget / n_steps, "mean_tau": tau / n_steps,
+                    "mean_delivered": deliv / n_steps, "mean_ceiling": ceil / n_steps,
+                    "delivered_over_ceiling": deliv / ceil, "delivered_over_tau": deliv / tau,
+                    "per_class": per})
         del logits
     except Exception as e:  # report, do not fail the run
         out["error"] = f"{type(e).__name__}: {e}"[:200]
@@ -727,6 +787,21 @@ def run_ours(args):
     elapsed_ms = max_over_ranks(elapsed_ms, dev, world)
     status = int(vs.status.item())
 
+    # ---- the accept call's duration for the roofline: n_roof steps after the
+    # timed region, each one's accept bracketed by events after its plan +
+    # pack (the bracket keeps the accept from launching early, so a sample
+    # includes that launch gap); the mean over the samples gives
+    # roofline.achieved, reported with its spread
+    n_roof = max(256, min(K, 1024))
+    ra = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_roof)]
+    for e in ra:
+        plan_pack_fn()
+        e[0].record(stream)
+        acc_fn()
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    roof_us = np.array([a.elapsed_time(b) for a, b in ra]) * 1e3
+
     # ---- breakdown (outside the timed region): per call on the same stream,
     # the fused plan+pack and, for reference, the two separate calls
     n_b = min(K, 200)
@@ -996,8 +1071,10 @@ def run_ours(args):
             dist.destroy_process_group()
         return
     peak, peak_kind = load_peaks()
-    acc_us = float(np.mean(accept_ms)) * 1e3
-    achieved = accept_bytes / (acc_us * 1e-6) / 1e9
+    acc_us = float(np.mean(accept_ms)) * 1e3  # the timed region's sampled accepts
+    roof_mean = float(np.mean(roof_us))
+    achieved = accept_bytes / (roof_mean * 1e-6) / 1e9
+    in_step = accept_bytes / (acc_us * 1e-6) / 1e9
     ms_per_step = elapsed_ms / K
     value = job_rate(K, world, elapsed_ms / 1e3)
     line = {
@@ -1014,7 +1091,18 @@ def run_ours(args):
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": "dspark_greedy_accept (argmax + finalize)",
                      "bytes_per_launch": accept_bytes,
-                     "traffic": ncu_traffic(w.name)},
+                     "traffic": ncu_traffic(w.name),
+                     "samples": int(roof_us.size),
+                     "accept_us": {"mean": roof_mean,
+                                   "p10": float(np.percentile(roof_us, 10)),
+                                   "p50": float(np.percentile(roof_us, 50)),
+                                   "p90": float(np.percentile(roof_us, 90))},
+                     "method": (f"{roof_us.size} steps after the timed region, each accept "
+                                "call bracketed by CUDA events after its plan + pack; "
+                                "achieved = bytes_per_launch / mean"),
+                     "in_step": {"achieved": in_step, "frac": in_step / peak,
+                                 "samples": len(accept_ms),
+                                 "method": f"every {every}-th timed step's accept bracketed"}},
         "e2e": {"value": job_rate(n_e, world, e2e_s), "unit": UNIT,
                 "h2d_bytes_per_step": io.h2d_input_bytes() + logit_bytes,
                 "d2h_bytes_per_step": io.d2h_output_bytes(), "steps": n_e,
