@@ -5,8 +5,10 @@ mode, and the accept kernel's HBM bandwidth against the measured peak.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own batch
-of B requests (weak scaling, no data-path collective); the elapsed time is
-the maximum over ranks.
+of B requests (weak scaling); the one exchange per step is the MAX
+all-reduce of the ranks' verify tiers, after which each rank pads its window
+to the shared tier (dspark_pad_to_tier).  The elapsed time is the maximum
+over ranks.
 
 A step = dspark_plan + dspark_pack_verify + dspark_greedy_accept over one
 batch, with every input resident in HBM when the timed region starts.  The
@@ -731,6 +733,16 @@ def run_ours(args):
             plan_fn()
             pack_fn()
 
+    if world > 1:
+        # data-parallel ranks replay one verify tier: after each rank's plan
+        # + pack, the MAX all-reduce of the local tiers (one int32, NCCL, on
+        # the stream) and the pad to the shared tier
+        local_plan_pack = plan_pack_fn
+
+        def plan_pack_fn():
+            local_plan_pack()
+            vs.share_tier()
+
     def one_step():
         plan_pack_fn()
         acc_fn()
@@ -835,7 +847,7 @@ def run_ours(args):
     # ---- the same step replayed from a CUDA graph (secondary): 16 steps per
     # graph, captured on a side stream with the calls bound to it
     graph = None
-    if not args.no_graph:
+    if not args.no_graph and world == 1:
         try:
             gs = torch.cuda.Stream()
             bound = vs.bind_compact(compact, stream=gs)
@@ -1086,7 +1098,8 @@ def run_ours(args):
                    "packed_rows": total, "padded_rows": padded, "seed": args.seed,
                    "plan_pack": "separate calls" if args.separate_plan_pack else "dspark_plan_pack",
                    "l2": f"inputs larger than L2: {accept_bytes / 1e6:.1f} MB of logits per step",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": (f"dp{world}: own requests per rank, MAX all-reduce of the "
+                                   "verify tier each step" if world > 1 else "replicas x1")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": "dspark_greedy_accept (argmax + finalize)",
@@ -1112,7 +1125,7 @@ def run_ours(args):
                                      "h2d_bytes_per_step": io.h2d_input_bytes() + copy_bytes,
                                      "matches_device_path": bool(copy_ok)}},
         "cpu_baseline": cpu,
-        "gpu_launches": vs.kernels_per_step(args.separate_plan_pack) * K,
+        "gpu_launches": (vs.kernels_per_step(args.separate_plan_pack) + (world > 1)) * K,
         "clocks": clocks,
         "step_us": {"p10": float(np.percentile(step_us, 10)),
                     "p50": float(np.percentile(step_us, 50)),

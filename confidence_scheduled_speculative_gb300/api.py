@@ -33,6 +33,7 @@ STATUS_BAD_COST = 32
 STATUS_INFEASIBLE = 64
 STATUS_BAD_INDEX = 128
 STATUS_TIMEOUT = 256
+STATUS_BAD_TIER = 512
 
 # cost tables of at most this many entries take the planner's single-CTA
 # select path (the pack fused into it); larger ones the multi-CTA rank path
@@ -99,6 +100,7 @@ _SIGS = {
                                         _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
     "dspark_scatter_compact_to_strided": (ctypes.c_int, [_VP, _I64, _I32, _I32, _VP, _VP, _I32,
                                                          _VP, _I64, _I32, _VP, _VP]),
+    "dspark_pad_to_tier": (ctypes.c_int, [_VP, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "dspark_scatter_compact_to_strided_ex": (ctypes.c_int, [_VP, _I64, _I32, _I32, _VP, _VP,
                                                             _I32, _VP, _I64, _I32, _I64, _VP,
                                                             _VP]),
@@ -328,6 +330,19 @@ def dspark_scatter_compact_to_strided(src, packed_src, totals, dst, *, status,
                                                          _p(status, torch.int32, "status"),
                                                          _stream(stream))
     _check(name, rc)
+
+
+def dspark_pad_to_tier(pad_to, *, packed_ids, packed_pos, packed_req, packed_src, totals,
+                       status, capacity=None, stream=None) -> None:
+    """Pad one rank's packed window to the verify tier the data-parallel
+    ranks share (``pad_to``: device int32 [1], may be ``totals[1:2]``)."""
+    capacity = packed_ids.numel() if capacity is None else capacity
+    rc = load().dspark_pad_to_tier(
+        _p(pad_to, torch.int32, "pad_to"), int(capacity), _p(packed_ids, torch.int32, "packed_ids"),
+        _p(packed_pos, torch.int32, "packed_pos"), _p(packed_req, torch.int32, "packed_req"),
+        _p(packed_src, torch.int32, "packed_src"), _p(totals, torch.int32, "totals"),
+        _p(status, torch.int32, "status"), _stream(stream))
+    _check("dspark_pad_to_tier", rc)
 
 
 def _dtype_code(t: torch.Tensor) -> int:

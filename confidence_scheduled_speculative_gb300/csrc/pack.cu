@@ -120,6 +120,39 @@ pack_kernel(const int32_t *__restrict__ anchor, const int32_t *__restrict__ draf
     if (__syncthreads_or(over) && tid == 0) flag(status, DSPARK_STATUS_CAPACITY);
 }
 
+// The data-parallel shared tier ([AVS] §六: local verify tier -> DP gather
+// -> DP-global max token tier; [SGL] "Ragged verify": DP ranks share the
+// largest tier any rank needs).  After the rank-local pack and the max over
+// ranks, rows [totals[0], pad_to) become pad rows and totals[1] = pad_to.
+// Starting from the real total (not the local padded end) rewrites the
+// local pad rows with the same values, and lets pad_to alias totals + 1 (an
+// in-place all-reduce).  A grid-stride loop over at most `capacity` rows.
+__global__ void __launch_bounds__(kPackThreads)
+pad_tier_kernel(const int32_t *pad_to, int capacity, int32_t *__restrict__ ids,
+                int32_t *__restrict__ pos, int32_t *__restrict__ req, int32_t *__restrict__ src,
+                int32_t *totals, int32_t *status) {
+    pdl_trigger();
+    pdl_wait();  // totals from the pack, pad_to from the collective
+    const int total = __ldcg(totals);
+    const int P = __ldcg(pad_to);  // when pad_to is totals + 1, the store below rewrites P
+    if (P < total) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) flag(status, DSPARK_STATUS_BAD_TIER);
+        return;
+    }
+    const int end = min(P, capacity);
+    for (int i = total + blockIdx.x * kPackThreads + threadIdx.x; i < end;
+         i += gridDim.x * kPackThreads) {
+        ids[i] = 0;
+        pos[i] = 0;
+        req[i] = -1;
+        src[i] = -1;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        totals[1] = P;
+        if (P > capacity) flag(status, DSPARK_STATUS_CAPACITY);
+    }
+}
+
 bool load_tiers(const int32_t *host_tiers, int32_t n_tiers, TierArgs *out) {
     if (n_tiers < 0 || n_tiers > DSPARK_MAX_TIERS || (n_tiers > 0 && !host_tiers)) return false;
     out->n = n_tiers;
@@ -161,6 +194,24 @@ extern "C" int dspark_pack_verify(const int32_t *anchor, const int32_t *draft,
     if (launch_pack(anchor, draft, prefix_lens, verify_lens, B, gamma, t, capacity, packed_ids,
                     packed_pos, packed_req, packed_src, cu_seqlens, totals, status,
                     static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    return DSPARK_OK;
+}
+
+extern "C" int dspark_pad_to_tier(const int32_t *pad_to, int32_t capacity, int32_t *packed_ids,
+                                  int32_t *packed_pos, int32_t *packed_req,
+                                  int32_t *packed_src, int32_t *totals, int32_t *status,
+                                  void *stream) {
+    if (!pad_to || !packed_ids || !packed_pos || !packed_req || !packed_src || !totals ||
+        !status)
+        return DSPARK_ERR_INVALID_ARG;
+    if (capacity < 0) return DSPARK_ERR_INVALID_ARG;
+    // enough CTAs for 4 rows a thread, at most two per SM
+    const int want = (capacity + 4 * kPackThreads - 1) / (4 * kPackThreads);
+    const int grid = max(1, min(want, 2 * sm_count()));
+    if (launch_pdl(pad_tier_kernel, dim3(grid), dim3(kPackThreads), 0,
+                   static_cast<cudaStream_t>(stream), pad_to, (int)capacity, packed_ids,
+                   packed_pos, packed_req, packed_src, totals, status) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     return DSPARK_OK;
 }

@@ -195,6 +195,22 @@ class VerifyStep:
                              totals=self.totals, status=self.status, workspace=self.plan_ws,
                              stream=stream)
 
+    def pad_to_tier(self, pad_to: torch.Tensor | None = None, stream=None) -> None:
+        """Pad the packed window to a verify tier shared with other ranks
+        (dspark_pad_to_tier); ``pad_to`` defaults to totals[1] itself, as
+        left by ``share_tier``'s in-place all-reduce."""
+        api.dspark_pad_to_tier(self.totals[1:2] if pad_to is None else pad_to,
+                               packed_ids=self.packed_ids, packed_pos=self.packed_pos,
+                               packed_req=self.packed_req, packed_src=self.packed_src,
+                               totals=self.totals, status=self.status,
+                               capacity=self.cfg.capacity, stream=stream)
+
+    def share_tier(self, group=None, stream=None) -> None:
+        """The data-parallel step's one exchange: the max of the ranks' local
+        verify tiers (in place on totals[1]), then the pad to it."""
+        share_tier(self.totals, group)
+        self.pad_to_tier(None, stream)
+
     def kernels_per_step(self, separate_plan_pack: bool = False) -> int:
         """Kernels one compact step launches: survival + select (the pack
         inside) for tables of <= api.SELECT_MAX_ENTRIES entries, else survival + rank + pack
@@ -284,6 +300,24 @@ class VerifyStep:
                  "num_accepted", "bonus", "commit_lens", "new_seq_lens", "out_tokens", "ceiling",
                  "cap_totals"]
         return {n: getattr(self, n).cpu().numpy() for n in names}
+
+
+def share_tier(totals: torch.Tensor, group=None) -> torch.Tensor:
+    """The exchange data-parallel ranks make each step ([AVS] §六: local
+    verify tier -> DP gather -> DP-global max token tier; [SGL] "Ragged
+    verify": the ranks share the largest tier any rank needs).  ``totals`` is
+    a rank's pack output (real rows, padded rows = its local tier); totals[1]
+    becomes the largest local tier over the ranks of ``group`` by one int32
+    MAX all-reduce in place (NCCL on the current stream, no host
+    synchronisation, or gloo on CPU tensors).  Nothing else crosses ranks:
+    each rank plans, packs and accepts its own requests.  With one rank (or
+    no process group) nothing happens.  Returns the view totals[1:2], the
+    shared tier, for dspark_pad_to_tier."""
+    import torch.distributed as dist
+    tier = totals[1:2]
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size(group) > 1:
+        dist.all_reduce(tier, op=dist.ReduceOp.MAX, group=group)
+    return tier
 
 
 class HostStepIO:

@@ -64,6 +64,7 @@ extern "C" {
 #define DSPARK_STATUS_INFEASIBLE  64 /* no budget in range: budget set to 0 */
 #define DSPARK_STATUS_BAD_INDEX   128 /* a packed row's strided destination outside the buffer */
 #define DSPARK_STATUS_TIMEOUT     256 /* a kernel's bounded wait gave up (its outputs are incomplete) */
+#define DSPARK_STATUS_BAD_TIER    512 /* a shared verify tier below this rank's packed rows */
 
 /* Message for a DSPARK_ERR_* code (static string). */
 DSPARK_API const char *dspark_strerror(int code);
@@ -339,6 +340,30 @@ DSPARK_API int dspark_scatter_compact_to_strided_ex(const void *src, int64_t ld_
                                       int32_t max_rows, void *dst, int64_t ld_dst,
                                       int32_t dst_rows, int64_t wait_limit_ns, int32_t *status,
                                       void *stream);
+
+/* The verify tier shared by data-parallel ranks.  [AVS] §六 "DP / DeepEP
+ * 是第二层复杂度" (each rank's local verify tier is gathered and the
+ * DP-global max token tier is what every rank replays); [SGL] "Ragged
+ * verify" (under DP attention the ranks share one tier, the largest any rank
+ * needs).  Each rank packs its own requests (dspark_pack_verify or
+ * dspark_plan_pack: totals[1] = its local tier), the ranks take the max of
+ * totals[1] (one int32 MAX all-reduce, e.g. NCCL, on the step's stream), and
+ * this call pads the rank's window to the result:
+ *   pad_to       device [1] int32: the shared tier.  May point at totals + 1
+ *                (the all-reduce done in place).
+ *   capacity     rows of the packed_* buffers
+ *   packed_*     device [capacity], the pack's outputs; rows
+ *                [totals[0], min(*pad_to, capacity)) become pad rows (id 0,
+ *                position 0, request -1, source -1), other rows untouched
+ *   totals       device [2] in/out: totals[0] (real rows) is read,
+ *                totals[1] = *pad_to is written
+ * A shared tier below totals[0] changes nothing and flags
+ * DSPARK_STATUS_BAD_TIER; one above capacity writes up to capacity and flags
+ * DSPARK_STATUS_CAPACITY.  No host synchronisation.
+ * Errors: INVALID_ARG (null pointer, capacity < 0); CUDA. */
+DSPARK_API int dspark_pad_to_tier(const int32_t *pad_to, int32_t capacity, int32_t *packed_ids,
+                                  int32_t *packed_pos, int32_t *packed_req, int32_t *packed_src,
+                                  int32_t *totals, int32_t *status, void *stream);
 
 /* dspark_plan_pack with options (see dspark_plan_options; alignment uses
  * the pack's tiers). */

@@ -33,6 +33,7 @@ ST_BAD_LEN = 16
 ST_BAD_COST = 32
 ST_INFEASIBLE = 64
 ST_BAD_INDEX = 128
+ST_BAD_TIER = 512
 
 _lock = threading.Lock()
 _lib = None
@@ -80,6 +81,8 @@ def lib():
             L.orc_pack.argtypes = [i32p, i32p, i32p, i32p, ci, ci, i32p, ci, ci, i32p, i32p, i32p,
                                    i32p, i32p, i32p, i32p]
             L.orc_pack.restype = None
+            L.orc_pad_to_tier.argtypes = [ci, ci, i32p, i32p, i32p, i32p, i32p, i32p]
+            L.orc_pad_to_tier.restype = None
             L.orc_sampling_accept.argtypes = [f32p, cl, ci, ci, i32p, f32p, cl, i32p, i32p, ci, ci,
                                               f32p, f32p, i32p, i32p, i32p, i32p, i32p, i32p]
             L.orc_sampling_accept.restype = None
@@ -282,6 +285,20 @@ def pack(anchor, draft, prefix, lens, tiers, capacity, sentinel=-7):
                    _ptr(st, ctypes.c_int32))
     return PlanResult(ids=outs[0], pos=outs[1], req=outs[2], src=outs[3], cu_seqlens=cu,
                       total=int(totals[0]), padded=int(totals[1]), status=int(st[0]))
+
+
+def pad_to_tier(packed, pad_to, capacity):
+    """The data-parallel shared tier applied to one rank's pack result (a
+    ``pack`` PlanResult): a copy with rows [total, pad_to) turned into pad
+    rows and padded = pad_to (reading R30)."""
+    outs = [np.array(packed[k], np.int32, copy=True) for k in ("ids", "pos", "req", "src")]
+    totals = np.array([packed.total, packed.padded], np.int32)
+    st = np.zeros(1, np.int32)
+    lib().orc_pad_to_tier(int(pad_to), int(capacity), *[_ptr(o, ctypes.c_int32) for o in outs],
+                          _ptr(totals, ctypes.c_int32), _ptr(st, ctypes.c_int32))
+    return PlanResult(ids=outs[0], pos=outs[1], req=outs[2], src=outs[3],
+                      cu_seqlens=packed.cu_seqlens, total=int(totals[0]), padded=int(totals[1]),
+                      status=int(st[0]))
 
 
 def scatter_rows(src, src_of, total, dst, max_rows=None):

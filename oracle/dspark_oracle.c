@@ -68,6 +68,7 @@
 #define ORC_ST_BAD_COST    32
 #define ORC_ST_INFEASIBLE  64
 #define ORC_ST_BAD_INDEX   128
+#define ORC_ST_BAD_TIER    512
 
 /* ------------------------------------------------------------------ STS */
 
@@ -346,6 +347,28 @@ void orc_pack(const int32_t *anchor, const int32_t *draft, const int32_t *prefix
     totals[1] = padded;
 }
 
+/* Data-parallel ranks replay one shared verify tier: each rank's local tier
+ * (the pack's padded total) is gathered and the largest taken, and every
+ * rank pads its window to that tier.  [AVS] §六 "DP / DeepEP 是第二层复杂度"
+ * (local verify tier -> DP gather -> DP-global max token tier); [SGL]
+ * "Ragged verify" (under DP attention all ranks share one tier, the largest
+ * any rank needs).  Reading R30: after the rank-local pack, rows
+ * [totals[0], pad_to) become pad rows (id 0, position 0, request -1, source
+ * -1; reading R13) and totals[1] = pad_to; rows at or past capacity are not
+ * written and flag CAPACITY; a shared tier below the rank's real total
+ * changes nothing and flags BAD_TIER. */
+void orc_pad_to_tier(int pad_to, int capacity, int32_t *ids, int32_t *pos, int32_t *req,
+                     int32_t *src, int32_t *totals, int *status)
+{
+    const int total = totals[0];
+    if (pad_to < total) { *status |= ORC_ST_BAD_TIER; return; }
+    for (int i = total; i < pad_to; ++i) {
+        if (i >= capacity) { *status |= ORC_ST_CAPACITY; break; }
+        ids[i] = 0; pos[i] = 0; req[i] = -1; src[i] = -1;
+    }
+    totals[1] = pad_to;
+}
+
 /* -------------------------------------------------------------- accept */
 
 static float orc_bf16_to_f32(uint16_t h)
@@ -357,7 +380,7 @@ static float orc_bf16_to_f32(uint16_t h)
 }
 
 /* target_predict = argmax(target_logits) per row ([ROUND] §五 "Greedy"),
- * with the tie and NaN conventions of reading R7. */
+ * with the tie and NaN conventions of reading R12. */
 void orc_argmax_rows_f32(const float *x, int64_t ld, int V, int rows, int32_t *am, int *status)
 {
     for (int i = 0; i < rows; ++i) {

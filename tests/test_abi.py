@@ -205,6 +205,15 @@ def test_scatter_argument_checks(lib):
              ctypes.c_int64(-1), FAKE, None) == -1
 
 
+def test_pad_to_tier_argument_checks(lib):
+    f = lib.dspark_pad_to_tier
+    f.restype = ctypes.c_int
+    assert f(None, 8, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == -1
+    assert f(FAKE, -1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == -1
+    assert f(FAKE, 8, FAKE, FAKE, FAKE, None, FAKE, FAKE, None) == -1
+    assert f(FAKE, 8, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == -1
+
+
 def test_sampling_argument_checks(lib):
     f = lib.dspark_sampling_accept
     f.restype = ctypes.c_int

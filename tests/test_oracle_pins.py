@@ -347,6 +347,53 @@ def test_pack_capacity_and_bad_len(orc):
     assert r.status & orc.ST_CAPACITY and r.padded == 12
 
 
+def test_dp_shared_tier_pads_every_rank_to_the_largest(orc):
+    """[AVS] §六 (local verify tier -> DP gather -> DP-global max tier) and
+    [SGL] "Ragged verify" (DP ranks share the largest tier any rank needs),
+    with the tutorial's tiers {40, 64, 80}: a rank with 37 rows (local tier
+    40) and one with 58 (local tier 64) both replay 64; the first rank's rows
+    37..63 become pad rows (27, as in [AVS] §五's 37 real + 27 padding), its
+    real rows stay as they were."""
+    tiers = [40, 64, 80]
+    ranks = []
+    for total in (37, 58):
+        lens = np.ones(total, np.int32)
+        p = orc.pack(np.arange(1, total + 1), np.zeros((total, 1)), np.arange(total) + 100,
+                     lens, tiers, 96)
+        ranks.append(p)
+    assert [p.padded for p in ranks] == [40, 64]
+    shared = max(p.padded for p in ranks)
+    a, b = (orc.pad_to_tier(p, shared, 96) for p in ranks)
+    assert (a.total, a.padded, b.total, b.padded) == (37, 64, 58, 64)
+    assert a.status == 0 and b.status == 0
+    assert list(a.ids[:37]) == list(range(1, 38)) and list(a.pos[:37]) == list(range(100, 137))
+    assert list(a.req[:37]) == list(range(37)) and list(a.src[:37]) == [2 * r for r in range(37)]
+    for k, v in (("ids", 0), ("pos", 0), ("req", -1), ("src", -1)):
+        assert np.all(a[k][37:64] == v), k
+        assert np.all(a[k][64:] == -7), k  # past the shared tier: untouched
+    for k in ("ids", "pos", "req", "src"):  # the rank that set the tier is unchanged
+        np.testing.assert_array_equal(b[k], ranks[1][k])
+
+
+def test_dp_shared_tier_edges(orc):
+    """A shared tier below the rank's real rows changes nothing (BAD_TIER); a
+    shared tier past the capacity writes pad rows up to the capacity and
+    flags CAPACITY; a shared tier equal to the local one is a no-op."""
+    lens = np.ones(37, np.int32)
+    p = orc.pack(np.arange(37), np.zeros((37, 1)), np.zeros(37), lens, [40, 64], 50)
+    low = orc.pad_to_tier(p, 30, 50)
+    assert low.status == orc.ST_BAD_TIER and low.padded == 40
+    for k in ("ids", "pos", "req", "src"):
+        np.testing.assert_array_equal(low[k], p[k])
+    over = orc.pad_to_tier(p, 64, 50)
+    assert over.status == orc.ST_CAPACITY and over.padded == 64
+    assert np.all(over.req[37:50] == -1)
+    same = orc.pad_to_tier(p, 40, 50)
+    assert same.status == 0 and same.padded == 40
+    for k in ("ids", "pos", "req", "src"):
+        np.testing.assert_array_equal(same[k], p[k])
+
+
 # ---------------------------------------------------------------- scatter
 
 def test_scatter_example_of_the_page(orc):
