@@ -47,6 +47,8 @@
 
 #include "dspark_common.cuh"
 
+#include <cfloat>
+#include <climits>
 #include <cmath>
 
 namespace dspark {
@@ -54,6 +56,7 @@ namespace dspark {
 constexpr int kSurvThreads = 64;  // 2 requests per CTA: spreads the fp64 sigmoids over many SMs
 constexpr int kRankThreads = 1024;
 constexpr int kRankWarps = kRankThreads / 32;
+constexpr int kRankMinPerCta = 4;  // candidates per CTA below which the rank grid shrinks
 constexpr int kMaxCandidates = 16384;       // B*gamma limit of the planner
 constexpr int kInterpPer = (kMaxCandidates + kRankThreads) / kRankThreads;  // budgets per thread
 constexpr int kScanReg = 4;  // kept candidates per thread held in registers by the prefix scan
@@ -66,6 +69,13 @@ constexpr int kNoRank = 0x7FFFFFFF;
 // CTA adds the survivals ranked below each candidate budget into one
 // accumulator per candidate, so no prefix scan is needed.
 constexpr int kMaxSparse = 64;
+
+// Dense cost tables (more than kMaxSparse entries, not interpolated) of at
+// most this many entries are staged in the rank kernel's shared memory
+// before its dependency wait (the 1-D SPS table sampled at every M of a
+// B=256, gamma=16 batch has 4097 entries), and the last CTA keeps the prefix
+// sums there too.
+constexpr int kTabStage = 4608;
 
 // The select path ranks candidates inside the top-11-bit bins of their keys:
 // survival_kernel counts the kept keys (and adds their fixed-point
@@ -259,12 +269,29 @@ __device__ __forceinline__ bool cand_better(long long ka, int ba, long long kb, 
     return ka > kb || (ka == kb && ba < bb);
 }
 
-// Number of keys < key in a run of P2 keys (a power of two), padded past
-// gamma with the largest key: log2(P2) + 1 branch-free probes.
-__device__ __forceinline__ int run_lower_bound(const uint32_t *run, int P2, uint32_t key) {
-    int pos = 0;
-    for (int step = P2 >> 1; step > 0; step >>= 1) pos += (run[pos + step - 1] < key) ? step : 0;
-    return pos + ((run[pos] < key) ? 1 : 0);
+// Number of keys < key in each of four runs of P2 keys (a power of two,
+// at most 32; runs padded past gamma with the largest key): log2(P2) + 1
+// branch-free probes per run, the four probe chains interleaved.  The
+// caller ignores the result for a run index at or past B (probed as run 0).
+__device__ __forceinline__ void run_lower_bound4(const uint32_t *K, int S, int P2, int B,
+                                                 uint32_t key, int q0, int lb[4]) {
+    const uint32_t *run[4];
+    int pos[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int q = q0 + 32 * u;
+        run[u] = K + (q < B ? q : 0) * S;
+        pos[u] = 0;
+    }
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1) {
+        if (step < P2) {  // uniform: the steps P2/2, ..., 1
+#pragma unroll
+            for (int u = 0; u < 4; ++u) pos[u] += (run[u][pos[u] + step - 1] < key) ? step : 0;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) lb[u] = pos[u] + ((run[u][pos[u]] < key) ? 1 : 0);
 }
 
 // Shared state of the rank kernel.
@@ -289,7 +316,53 @@ struct RankSmem {
     long long b_top;
 };
 
+// Keys live in shared memory request-major, each run padded to P2 keys with
+// the largest key and laid out with an odd stride, so the 32 lanes of a warp
+// probing 32 different runs hit 32 different banks.
+__host__ __device__ inline int run_stride(int P2) { return P2 + 1; }
+
 __device__ void finish_plan(const PlanArgs &a, RankSmem &sm);
+
+// Dynamic shared memory of rank_kernel: RankSmem | region R | table stage.
+// R holds the keys while the CTAs rank; the last CTA then reuses it for the
+// prefix sums P[0..N] of a dense table (int64) or, for an interpolated
+// table, for the float tau of every budget.  The stage holds a dense
+// table's samples, values and values as floats (kTabStage entries at most).
+__host__ __device__ inline size_t rank_head_bytes() { return (sizeof(RankSmem) + 15) & ~size_t(15); }
+__host__ __device__ inline bool dense_table(int kind, int n) {
+    return kind != DSPARK_COST_ADDITIVE_INTERP && n > kMaxSparse;
+}
+__host__ __device__ inline bool staged_table(int kind, int n) {
+    return dense_table(kind, n) && n <= kTabStage;
+}
+__host__ __device__ inline size_t rank_region_bytes(int B, int S, int N, int kind, int n) {
+    size_t r = (size_t)4 * B * S;
+    if (dense_table(kind, n) && (size_t)8 * (N + 1) > r) r = (size_t)8 * (N + 1);
+    return (r + 15) & ~size_t(15);
+}
+// stage: each entry's range of budgets [lo, hi] (int2; before the clip to
+// the largest in-range budget) | its value as a float
+__host__ __device__ inline size_t stage_f32_offset(int n) { return (size_t)8 * n; }
+__host__ __device__ inline size_t rank_stage_bytes(int kind, int n) {
+    return staged_table(kind, n) ? ((stage_f32_offset(n) + (size_t)4 * n + 15) & ~size_t(15)) : 0;
+}
+
+struct TableStage {
+    int2 *range;
+    float *f32;
+};
+
+// The staged dense table (see rank_kernel's prologue) of a CTA.
+__device__ __forceinline__ TableStage table_stage(unsigned char *smem, const PlanArgs &a) {
+    unsigned char *st = smem + rank_head_bytes() +
+                        rank_region_bytes(a.B, run_stride(a.P2), a.N, a.cost.kind, a.cost.n);
+    return TableStage{reinterpret_cast<int2 *>(st),
+                      reinterpret_cast<float *>(st + stage_f32_offset(a.cost.n))};
+}
+
+__device__ __forceinline__ int sat_int(long long x) {
+    return x > INT_MAX ? INT_MAX : (x < INT_MIN ? INT_MIN : (int)x);
+}
 
 // The range of budgets whose M = B + b uses table entry j, clipped to
 // [0, b_top]; returns its last budget, or -1 if the range is empty.
@@ -308,18 +381,40 @@ __device__ __forceinline__ int entry_last_budget(const CostArgs &c, int j, int M
     return blo > bhi ? -1 : (int)bhi;
 }
 
-// Keys live in shared memory request-major, each run padded to P2 keys with
-// the largest key and laid out with an odd stride, so the 32 lanes of a warp
-// probing 32 different runs hit 32 different banks.
-__host__ __device__ inline int run_stride(int P2) { return P2 + 1; }
 
 __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     RankSmem &sm = *reinterpret_cast<RankSmem *>(smem_raw);
-    uint32_t *K = reinterpret_cast<uint32_t *>(smem_raw + ((sizeof(RankSmem) + 15) & ~size_t(15)));
+    uint32_t *K = reinterpret_cast<uint32_t *>(smem_raw + rank_head_bytes());
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = a.B, G = a.gamma, N = a.N, P2 = a.P2, S = run_stride(P2);
     const CostArgs &c = a.cost;
+    bool order_bad = false;
+    if (staged_table(c.kind, c.n)) {
+        // a dense table into shared memory while the survivals are on the
+        // way (only the last CTA reads it): each entry's range of budgets b
+        // whose M = B + b looks the entry up (as entry_last_budget, before
+        // the clip to the in-range budgets) and its value as a float; the
+        // 64-bit range arithmetic and the fp64 -> fp32 conversions run here,
+        // off the critical path
+        const TableStage ts = table_stage(smem_raw, a);
+        const long long Bl = B;
+        for (int j = tid; j < c.n; j += kRankThreads) {
+            const long long Mj = __ldg(c.M + j);
+            const long long Mp = j > 0 ? __ldg(c.M + j - 1) : 0;
+            if (j > 0 && !(Mj > Mp)) order_bad = true;
+            long long lo, hi;
+            if (c.kind == DSPARK_COST_SPS_1D) {
+                lo = j == 0 ? 0 : max(Mj - Bl, 0LL);
+                hi = j == c.n - 1 ? (long long)INT_MAX : (long long)__ldg(c.M + j + 1) - 1 - Bl;
+            } else {
+                lo = j == 0 ? 0 : max(Mp + 1 - Bl, 0LL);
+                hi = Mj - Bl;
+            }
+            ts.range[j] = make_int2(sat_int(lo), sat_int(hi));
+            ts.f32[j] = (float)__ldg(c.val + j);
+        }
+    }
     int32_t *rank_out = scratch_at<int32_t>(a.scratch, plan_rank_offset());
     long long *sorted = scratch_at<long long>(a.scratch, plan_sorted_offset(N));
 
@@ -338,7 +433,6 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
     }
     const int Mlast = __ldg(c.M + c.n - 1);
     // interpolated table: its order, checked while the survivals are on the way
-    bool order_bad = false;
     if (interp)
         for (int j = tid + 1; j < c.n; j += kRankThreads)
             if (!(__ldg(c.M + j) > __ldg(c.M + j - 1))) order_bad = true;
@@ -405,8 +499,10 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
 
     // ranks: one warp per candidate, lanes over the other requests' runs
     unsigned long long my_acc[3] = {0ull, 0ull, 0ull};  // candidates lane, lane+32, lane+64
+    // candidate x goes to CTA x mod grid (warps 0, 1, ... in turn), so every
+    // SM of the grid gets its share even when there are few candidates
     const int nwarps = gridDim.x * kRankWarps;
-    for (int x = blockIdx.x * kRankWarps + warp; x < N; x += nwarps) {
+    for (int x = blockIdx.x + gridDim.x * warp; x < N; x += nwarps) {
         const int r = x / G;
         const int k = x - r * G;
         const uint32_t key = K[r * S + k];
@@ -418,11 +514,7 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
         // four runs per lane at a time, so their probe chains overlap
         for (int q0 = lane; q0 < B; q0 += 4 * 32) {
             int lb[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int q = q0 + 32 * u;
-                lb[u] = q < B ? run_lower_bound(K + q * S, P2, key) : 0;
-            }
+            run_lower_bound4(K, S, P2, B, key, q0, lb);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int q = q0 + 32 * u;
@@ -632,6 +724,37 @@ struct InterpWalk {
     }
 };
 
+// fp32 bounds lo <= theta <= hi of a dense-table entry's theta (the value
+// of the fp64 definition: tau * SPS, or tau / (bias + alpha + theta(M))),
+// from tau as a float (truncated: relative error below 2^-23) and the
+// entry's value as a float.  1-D: the fp32 product is within 2^-21 of the
+// fp64 one, inside the 2^-20 margins.  Additive: the bounds of InterpWalk.
+// False when fp32 cannot bound theta (a value or the product not a normal
+// finite float, or T not shown positive): the caller then evaluates the fp64
+// definition, which also flags invalid values.
+__device__ __forceinline__ bool dense_theta_bounds(int kind, float tau32, float v32,
+                                                   float fixed32, float &lo, float &hi) {
+    if (kind == DSPARK_COST_SPS_1D) {
+        if (!(v32 >= FLT_MIN) || !(v32 <= FLT_MAX)) return false;
+        const float est = tau32 * v32;
+        if (!(est >= FLT_MIN) || !(est <= FLT_MAX)) return false;
+        lo = est * (1.0f - 0x1p-20f);
+        hi = est * (1.0f + 0x1p-20f);
+        return hi <= FLT_MAX;
+    }
+    const float T = fixed32 + v32;
+    const float err = 0x1p-20f * (fabsf(fixed32) + fabsf(v32));
+    if (!(isfinite(T) && isfinite(err)) || !(T - err > 0.0f)) return false;
+    float rT, rTe;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rT) : "f"(T));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rTe) : "f"(T - err));
+    const float q = tau32 * rT;
+    const float rel = 0x1p-19f + 2.0f * err * rTe;
+    lo = q * (1.0f - rel);
+    hi = q * (1.0f + rel);
+    return isfinite(hi) && lo >= 0.0f;
+}
+
 __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = a.B, G = a.gamma;
@@ -642,7 +765,13 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
     const int forced = sm.forced;
     const int32_t *rank_in = scratch_at<int32_t>(a.scratch, plan_rank_offset());
     const long long *sorted = scratch_at<long long>(a.scratch, plan_sorted_offset(a.N));
-    long long *P = scratch_at<long long>(a.scratch, plan_prefix_offset(a.N));
+    // the prefix sums: in shared memory (the key region) for a dense table,
+    // in the workspace for an interpolated one
+    unsigned char *smem = reinterpret_cast<unsigned char *>(&sm);
+    const bool dense = dense_table(c.kind, c.n);
+    long long *P = dense ? reinterpret_cast<long long *>(smem + rank_head_bytes())
+                         : scratch_at<long long>(a.scratch, plan_prefix_offset(a.N));
+    auto load_P = [&](long long b) -> long long { return dense ? P[b] : __ldcg(P + b); };
 
     // (a) dense tables: P[i] = sum of the i largest survivals in units of
     // 2^-37 (P[0] = 0), a blocked scan written to the workspace
@@ -771,7 +900,86 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
         __syncthreads();
         if (tid < min(sm.n_icand, kRankThreads)) exact(sm.icand_b[tid], sm.icand_seg[tid]);
     }
-    for (int j = tid; j < (interp ? 0 : c.n); j += kRankThreads) {
+    if (dense) {
+        // every entry's theta bounded in fp32 first; the fp64 definition
+        // runs only where the bounds cannot exclude the first maximiser (a
+        // budget whose upper bound is below the largest lower bound cannot
+        // be it), or cannot bound theta at all
+        const bool staged = staged_table(c.kind, c.n);
+        const TableStage ts = staged ? table_stage(smem, a) : TableStage{nullptr, nullptr};
+        const int b_top32 = (int)max(min(b_top, (long long)INT_MAX), -1LL);
+        if (staged && sm.itab_bad) my_bad_table = true;  // order checked in the prologue
+        // entry j's last budget b (false when its range holds none) and value
+        auto entry = [&](int j, int &b, float &v32) -> bool {
+            if (staged) {
+                const int2 r = ts.range[j];
+                b = min(r.y, b_top32);
+                v32 = ts.f32[j];
+                return b >= r.x;
+            }
+            const int Mj = __ldg(c.M + j);
+            const int Mprev = j > 0 ? __ldg(c.M + j - 1) : 0;
+            const int Mnext = j < c.n - 1 ? __ldg(c.M + j + 1) : 0;
+            if (j > 0 && !(Mj > Mprev)) my_bad_table = true;
+            b = entry_last_budget(c, j, Mj, Mprev, Mnext, B, b_top);
+            v32 = (float)__ldg(c.val + j);
+            return b >= 0;
+        };
+        auto exact = [&](int j, int b) {
+            const double vj = __ldg(c.val + j);
+            const long long Pb = P[b];
+            const double tau = tau_of(B, Pb);
+            double theta;
+            if (c.kind == DSPARK_COST_SPS_1D) {
+                if (!(vj > 0.0) || !isfinite(vj)) { my_bad_cost = true; return; }
+                theta = __dmul_rn(tau, vj);
+            } else {
+                const double Tm = __dadd_rn(fixed_cost, vj);
+                if (!(Tm > 0.0) || !isfinite(Tm)) { my_bad_cost = true; return; }
+                theta = __ddiv_rn(tau, Tm);
+            }
+            const long long kk = __double_as_longlong(theta);
+            if (cand_better(kk, b, my_key, my_b)) {
+                my_key = kk;
+                my_b = b;
+                my_P = Pb;
+            }
+        };
+        if (tid == 0) sm.theta_floor = 0u;
+        __syncthreads();
+        const float fixed32 = sm.fixed32;
+        float my_floor = 0.0f, my_top = -1.0f;
+        for (int j = tid; j < c.n; j += kRankThreads) {
+            int b;
+            float v32, lo, hi;
+            if (!entry(j, b, v32)) continue;
+            if (dense_theta_bounds(c.kind, tau_float(B, P[b]), v32, fixed32, lo, hi)) {
+                my_floor = fmaxf(my_floor, lo);
+                my_top = fmaxf(my_top, hi);
+            } else {
+                exact(j, b);
+                if (my_b == b)  // its exact theta is itself a lower bound of the maximum
+                    my_floor = fmaxf(my_floor,
+                                     (float)__longlong_as_double(my_key) * (1.0f - 0x1p-20f));
+            }
+        }
+        // non-negative floats order like their bits: one atomic per warp
+        const unsigned wfloor = __reduce_max_sync(kFullMask, __float_as_uint(my_floor));
+        if (lane == 0) atomicMax(&sm.theta_floor, wfloor);
+        __syncthreads();
+        const float floor_all = __uint_as_float(sm.theta_floor);
+        if (my_top >= floor_all) {  // only threads holding a possible maximiser
+            for (int j = tid; j < c.n; j += kRankThreads) {
+                int b;
+                float v32, lo, hi;
+                if (entry(j, b, v32) &&
+                    dense_theta_bounds(c.kind, tau_float(B, P[b]), v32, fixed32, lo, hi) &&
+                    hi >= floor_all)
+                    exact(j, b);
+            }
+        }
+    }
+    for (int j = tid; j < (interp || dense ? 0 : c.n); j += kRankThreads) {
         const int Mj = __ldg(c.M + j);
         const double vj = sparse ? sm.val_s[j] : __ldg(c.val + j);
         const int Mprev = j > 0 ? __ldg(c.M + j - 1) : 0;
@@ -779,7 +987,7 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
         if (j > 0 && !(Mj > Mprev)) my_bad_table = true;
         const int b = sparse ? sm.cand_b[j] : entry_last_budget(c, j, Mj, Mprev, Mnext, B, b_top);
         if (b < 0) continue;
-        const long long Pb = sparse ? (long long)sm.acc_s[j] : __ldcg(P + b);
+        const long long Pb = sparse ? (long long)sm.acc_s[j] : load_P(b);
         const double tau = tau_of(B, Pb);
         double theta;
         if (c.kind == DSPARK_COST_SPS_1D) {
@@ -858,7 +1066,7 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
                 if (!sparse && forced < 0) {
                     Pbud = bP;  // carried with the best candidate
                 } else if (!sparse) {
-                    Pbud = __ldcg(P + budget);
+                    Pbud = load_P(budget);
                 } else if (forced >= 0) {
                     Pbud = (long long)sm.acc_s[c.n];
                 } else {
@@ -938,8 +1146,9 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
     }
 }
 
-size_t rank_smem_bytes(int B, int P2) {
-    return ((sizeof(RankSmem) + 15) & ~size_t(15)) + (size_t)4 * B * run_stride(P2);
+size_t rank_smem_bytes(int B, int P2, int N, int kind, int n) {
+    return rank_head_bytes() + rank_region_bytes(B, run_stride(P2), N, kind, n) +
+           rank_stage_bytes(kind, n);
 }
 
 int pow2_at_least(int g) {
@@ -952,7 +1161,8 @@ int pow2_at_least(int g) {
 size_t rank_smem_max() {
     size_t m = 0;
     for (int g = 1; g <= 31; ++g) {
-        const size_t v = rank_smem_bytes(kMaxCandidates / g, pow2_at_least(g));
+        const int B = kMaxCandidates / g;
+        const size_t v = rank_smem_bytes(B, pow2_at_least(g), B * g, DSPARK_COST_SPS_1D, kTabStage);
         m = v > m ? v : m;
     }
     return m;
@@ -1693,11 +1903,12 @@ int launch_pass(PlanArgs a, bool select, cudaStream_t s) {
         return DSPARK_ERR_CUDA;
     }
     a.pk.on = false;
-    const size_t smem = rank_smem_bytes(a.B, a.P2);
+    const size_t smem = rank_smem_bytes(a.B, a.P2, a.N, a.cost.kind, a.cost.n);
     if (ensure_smem(reinterpret_cast<const void *>(rank_kernel), (int)rank_smem_max(), 0) != cudaSuccess)
         return DSPARK_ERR_CUDA;
-    // about one warp per candidate, at most one CTA per SM
-    int grid = (a.N + kRankWarps - 1) / kRankWarps;
+    // ranking is issue-bound: at least a few candidates per CTA, else every
+    // SM (one CTA each)
+    int grid = (a.N + kRankMinPerCta - 1) / kRankMinPerCta;
     grid = grid < 1 ? 1 : (grid > sm_count() ? sm_count() : grid);
     return launch_pdl(rank_kernel, dim3(grid), dim3(kRankThreads), smem, s, a) == cudaSuccess
                ? DSPARK_OK

@@ -146,6 +146,64 @@ def test_plan_random_interpolated_table(dev, orc, seed):
     assert int(gres["status"][0]) == exp.status
 
 
+def _dense_problem(rng, seed):
+    """A cost table of more than 64 entries read as given (1-D floor lookup or
+    additive ceil-to-tier): the rank path's dense tables, staged in shared
+    memory up to 4608 entries and read from global memory beyond."""
+    if seed % 4 == 3:  # large: more than 4608 entries
+        while True:
+            B, g = int(rng.integers(200, 700)), int(rng.integers(8, 32))
+            if B * g <= 16380 and B * (g + 1) <= 65536 and B * g > 4700:
+                break
+    else:
+        while True:
+            B, g = int(rng.integers(4, 300)), int(rng.integers(2, 32))
+            if B * g <= 16380 and B * g >= 70:
+                break
+    z = rng.normal(rng.uniform(0, 3), rng.uniform(0.3, 2), (B, g)).astype(np.float32)
+    if rng.random() < 0.3:
+        z[rng.integers(0, B, size=B // 3)] = z[int(rng.integers(0, B))]
+    T = np.ones(g, np.float32) if rng.random() < 0.5 else rng.uniform(0.7, 1.5, g).astype(np.float32)
+    kind = int(rng.integers(0, 2))
+    hi = B + B * g + 4
+    if rng.random() < 0.5:  # every M in a range
+        lo = int(rng.integers(1, B + 2))
+        M = np.arange(lo, hi + 1, dtype=np.int32)
+    else:
+        n = int(rng.integers(65, hi + 1))
+        M = np.sort(rng.choice(np.arange(1, hi + 1), size=min(n, hi), replace=False)).astype(np.int32)
+    if kind == 0:
+        a_, b_ = rng.uniform(1e-3, 4e-3), rng.uniform(1e-6, 1e-5)
+        val = 1.0 / (a_ + b_ * M) if rng.random() < 0.7 else rng.uniform(100, 1000, M.size)
+    else:
+        val = rng.uniform(0.002, 0.004) * M if rng.random() < 0.7 else rng.uniform(0.01, 3, M.size)
+    val = np.asarray(val, np.float64)
+    if rng.random() < 0.15:  # an invalid value somewhere
+        val[int(rng.integers(0, M.size))] = rng.choice([0.0, -5.0, np.inf, np.nan])
+    forced = -1 if rng.random() < 0.7 else int(rng.integers(0, B * g + 3))
+    eps = float(np.float32(rng.choice([2.0 ** -14, 1e-4, 0.01])))
+    max_len = int(rng.integers(2, g + 2))
+    return dict(B=B, gamma=g, z=z, T=T, eps=eps, min_len=1, max_len=max_len, kind=kind, M=M,
+                val=val, forced=forced, bias=float(rng.uniform(0, 2)),
+                alpha=float(rng.uniform(0, 1)))
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_plan_random_dense_table(dev, orc, seed):
+    """Dense tables on the rank path: theta bounded in fp32 at every entry
+    and evaluated in fp64 where the bounds cannot exclude the maximum; the
+    budget, lens, tau and theta must equal the oracle's, which evaluates
+    every budget in fp64."""
+    rng = np.random.default_rng(47000 + seed)
+    P = _dense_problem(rng, seed)
+    g = _gpu_plan(dev, P)
+    ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"], P["kind"],
+                   P["M"], P["val"], P["bias"], P["alpha"])
+    exp = compare_plan(f"dense/{seed}", g, ref, P["B"], P["gamma"], P["min_len"],
+                       _restage(orc, P))
+    assert int(g["status"][0]) == exp.status
+
+
 @pytest.mark.parametrize("name", ["dsv4_like", "stress", "qwen_like"])
 def test_plan_interpolated_table_workloads(dev, orc, name):
     """Full-size workloads with their additive tier table read as samples of
