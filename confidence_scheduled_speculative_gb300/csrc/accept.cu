@@ -273,6 +273,9 @@ __device__ __forceinline__ void finish(const FinalArgs &a, int r, int lane, int 
 }
 
 __global__ void __launch_bounds__(kFinalWarps * 32) greedy_finalize_kernel(FinalArgs a) {
+    // the next kernel may launch now: this library's kernels read nothing
+    // this one writes before their own dependency wait
+    pdl_trigger();
     const int rq = blockIdx.x * kFinalWarps + (threadIdx.x >> 5);
     const int ln = threadIdx.x & 31;
     // drafts are step inputs, and cu_seqlens was written before any argmax
@@ -318,6 +321,7 @@ __global__ void __launch_bounds__(kFinalWarps * 32) greedy_finalize_kernel(Final
 
 __global__ void __launch_bounds__(kFinalWarps * 32) cap_finalize_kernel(FinalArgs a) {
     __shared__ int sums[2];
+    pdl_trigger();  // as in greedy_finalize_kernel
     const int rq = blockIdx.x * kFinalWarps + (threadIdx.x >> 5);
     const int ln = threadIdx.x & 31;
     const int dj0 = (rq < a.B && ln < a.gamma) ? __ldg(a.draft + (size_t)rq * a.gamma + ln) : -1;

@@ -119,8 +119,10 @@ int sm_count();
 bool load_tiers(const int32_t *host_tiers, int32_t n_tiers, TierArgs *out);
 
 // The pack kernel on `stream` (pack.cu), launched after the planner with
-// programmatic serialization.
-cudaError_t launch_pack(const int32_t *anchor, const int32_t *draft, const int32_t *prefix,
+// programmatic serialization.  in_chain: launched behind this library's
+// planner pass, whose chain began after every earlier kernel completed, so
+// the kernel may fetch the step inputs before its dependency wait.
+cudaError_t launch_pack(bool in_chain, const int32_t *anchor, const int32_t *draft, const int32_t *prefix,
                         const int32_t *lens, int B, int gamma, const TierArgs &tiers,
                         int capacity, int32_t *ids, int32_t *pos, int32_t *req, int32_t *src,
                         int32_t *cu, int32_t *totals, int32_t *status, cudaStream_t stream);

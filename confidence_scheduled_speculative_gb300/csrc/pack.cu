@@ -38,7 +38,7 @@ pack_kernel(const int32_t *__restrict__ anchor, const int32_t *__restrict__ draf
             const int32_t *__restrict__ prefix, const int32_t *__restrict__ lens, int B, int gamma,
             TierArgs tiers, int capacity, int32_t *__restrict__ ids, int32_t *__restrict__ pos,
             int32_t *__restrict__ req, int32_t *__restrict__ src, int32_t *__restrict__ cu,
-            int32_t *__restrict__ totals, int32_t *__restrict__ status) {
+            int32_t *__restrict__ totals, int32_t *__restrict__ status, bool in_chain) {
     __shared__ long long scan64[40];
     __shared__ int offs[kPackReqPerCta];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -47,14 +47,20 @@ pack_kernel(const int32_t *__restrict__ anchor, const int32_t *__restrict__ draf
 
     pdl_trigger();
     // token ids and prefix lengths are step inputs (not written by the
-    // planner): fetch them while the planner finishes
+    // planner): behind the planner, fetch them while it finishes; called on
+    // its own, after the wait (they may be outputs of the kernel before, e.g.
+    // the bonus tokens and new sequence lengths of an accept)
     int tok = 0, pre = 0;
-    if (r < B) {
-        pre = __ldg(prefix + r);
-        if (lane == 0) tok = __ldg(anchor + r);
-        else if (lane <= gamma) tok = __ldg(draft + (size_t)r * gamma + lane - 1);
-    }
+    auto fetch = [&]() {
+        if (r < B) {
+            pre = __ldg(prefix + r);
+            if (lane == 0) tok = __ldg(anchor + r);
+            else if (lane <= gamma) tok = __ldg(draft + (size_t)r * gamma + lane - 1);
+        }
+    };
+    if (in_chain) fetch();
     pdl_wait();  // verify_lens come from the planner
+    if (!in_chain) fetch();
 
     // total packed rows and the rows before this CTA's first request, in one
     // block scan of (total << 32 | before)
@@ -164,14 +170,15 @@ bool load_tiers(const int32_t *host_tiers, int32_t n_tiers, TierArgs *out) {
     return true;
 }
 
-cudaError_t launch_pack(const int32_t *anchor, const int32_t *draft, const int32_t *prefix,
+cudaError_t launch_pack(bool in_chain, const int32_t *anchor, const int32_t *draft,
+                        const int32_t *prefix,
                         const int32_t *lens, int B, int gamma, const TierArgs &tiers,
                         int capacity, int32_t *ids, int32_t *pos, int32_t *req, int32_t *src,
                         int32_t *cu, int32_t *totals, int32_t *status, cudaStream_t stream) {
     const int grid = (B + kPackReqPerCta - 1) / kPackReqPerCta;
     return launch_pdl(pack_kernel, dim3(grid), dim3(kPackThreads), 0, stream, anchor, draft,
                       prefix, lens, B, gamma, tiers, capacity, ids, pos, req, src, cu, totals,
-                      status);
+                      status, in_chain);
 }
 
 }  // namespace dspark
@@ -191,7 +198,7 @@ extern "C" int dspark_pack_verify(const int32_t *anchor, const int32_t *draft,
     if ((long long)B * (gamma + 1) > 0x7FFFFFFF) return DSPARK_ERR_INVALID_ARG;
     TierArgs t;
     if (!load_tiers(host_tiers, n_tiers, &t)) return DSPARK_ERR_INVALID_ARG;
-    if (launch_pack(anchor, draft, prefix_lens, verify_lens, B, gamma, t, capacity, packed_ids,
+    if (launch_pack(false, anchor, draft, prefix_lens, verify_lens, B, gamma, t, capacity, packed_ids,
                     packed_pos, packed_req, packed_src, cu_seqlens, totals, status,
                     static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return DSPARK_ERR_CUDA;

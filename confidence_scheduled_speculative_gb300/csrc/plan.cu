@@ -157,6 +157,11 @@ survival_kernel(const float *__restrict__ z, const float *__restrict__ T, int B,
                 float eps, int kmax, bool bin_keys, const int32_t *__restrict__ conf_gen,
                 const int32_t *__restrict__ req_gen, float *__restrict__ s_out,
                 int32_t *__restrict__ status, PlanScratch *__restrict__ scratch) {
+    // launched early behind the previous kernel (programmatic dependent
+    // launch): wait for it before touching any input or output, then let the
+    // planner pass launch (its pre-wait loads of step inputs and the cost
+    // table then run after every earlier kernel has completed)
+    pdl_wait();
     pdl_trigger();
     if (blockIdx.x == 0) {  // reset the rank kernel's ticket and accumulators
         for (int j = threadIdx.x; j <= kMaxSparse; j += blockDim.x) scratch->acc[j] = 0ull;
@@ -1965,21 +1970,21 @@ int run_plan(const float *conf_logits, const float *sts_temps, const dspark_plan
 
     int rc;
     if (lagged) {
-        survival_kernel<<<sblocks, kSurvThreads, 0, s>>>(
-            opt->lagged_conf_logits, sts_temps, B, G, p->survival_eps, p->max_verify_len - 1,
-            select, conf_gen, req_gen, lagged_surv, status, scratch);
-        if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+        if (launch_pdl(survival_kernel, dim3(sblocks), dim3(kSurvThreads), 0, s,
+                       opt->lagged_conf_logits, sts_temps, B, G, p->survival_eps,
+                       p->max_verify_len - 1, select, conf_gen, req_gen, lagged_surv, status,
+                       scratch) != cudaSuccess)
+            return DSPARK_ERR_CUDA;
         a.surv = lagged_surv;
         a.budget = &ps->lagged_budget;
         if ((rc = launch_pass(a, select, s)) != DSPARK_OK) return rc;
         a.budget = &ps->pass_budget;
         a.forced_dev = &ps->lagged_budget;
     }
-    survival_kernel<<<sblocks, kSurvThreads, 0, s>>>(conf_logits, sts_temps, B, G,
-                                                     p->survival_eps, p->max_verify_len - 1,
-                                                     select, conf_gen, req_gen, survivals, status,
-                                                     scratch);
-    if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+    if (launch_pdl(survival_kernel, dim3(sblocks), dim3(kSurvThreads), 0, s, conf_logits,
+                   sts_temps, B, G, p->survival_eps, p->max_verify_len - 1, select, conf_gen,
+                   req_gen, survivals, status, scratch) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
     a.surv = survivals;
     if (align.n > 0) {
         a.more_passes = true;
@@ -1997,7 +2002,7 @@ int run_plan(const float *conf_logits, const float *sts_temps, const dspark_plan
     a.pk = pk;
     if ((rc = launch_pass(a, select, s)) != DSPARK_OK) return rc;
     if (!select && pk.on &&
-        launch_pack(pk.anchor, pk.draft, pk.prefix, verify_lens, B, G, pk.tiers, pk.capacity,
+        launch_pack(true, pk.anchor, pk.draft, pk.prefix, verify_lens, B, G, pk.tiers, pk.capacity,
                     pk.ids, pk.pos, pk.req, pk.src, pk.cu, pk.totals, status, s) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     return DSPARK_OK;
