@@ -1036,14 +1036,21 @@ def run_ours(args):
         sM = torch.arange(w.B, w.B + w.B * w.gamma + 1, dtype=torch.int32, device=dev)
         sps = (sM, 1.0 / (3e-3 + 3e-6 * sM.to(torch.float64)))
         plan_kinds = {"additive_tier": plan_kind_timing(dev, stream, vs, _api.COST_ADDITIVE),
-                      "sps_1d_every_M_rank_path":
+                      "sps_1d_every_M":
                           plan_kind_timing(dev, stream, vs, _api.COST_SPS_1D, table=sps),
                       "additive_tier_31_entries":
                           plan_kind_timing(dev, stream, vs, _api.COST_ADDITIVE, table=dense),
-                      "additive_tier_61_entries_rank_path":
+                      "additive_tier_61_entries":
                           plan_kind_timing(dev, stream, vs, _api.COST_ADDITIVE, table=dense2),
                       "additive_interpolated":
                           plan_kind_timing(dev, stream, vs, _api.COST_ADDITIVE_INTERP)}
+        for k, (kind, n) in {"additive_tier": (_api.COST_ADDITIVE, int(vs.cost_M.numel())),
+                             "sps_1d_every_M": (_api.COST_SPS_1D, int(sM.numel())),
+                             "additive_tier_31_entries": (_api.COST_ADDITIVE, int(dM.numel())),
+                             "additive_tier_61_entries": (_api.COST_ADDITIVE, int(dM2.numel())),
+                             "additive_interpolated": (_api.COST_ADDITIVE_INTERP,
+                                                       int(vs.cost_M.numel()))}.items():
+            plan_kinds[k]["path"] = _api.planner_path(w.B * w.gamma, kind, n)
         vs.status.zero_()
 
     # ---- accept bandwidth against packed rows (stress workload) and the

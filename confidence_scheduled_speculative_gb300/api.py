@@ -36,7 +36,8 @@ STATUS_TIMEOUT = 256
 STATUS_BAD_TIER = 512
 
 # cost tables of at most this many entries take the planner's single-CTA
-# select path (the pack fused into it); larger ones the multi-CTA rank path
+# select path (the pack fused into it); larger ones, and interpolated tables,
+# the multi-CTA rank path
 SELECT_MAX_ENTRIES = 31
 COST_SPS_1D = 0
 COST_ADDITIVE = 1
@@ -44,6 +45,13 @@ COST_ADDITIVE_INTERP = 2
 DTYPE_BF16 = 0
 DTYPE_F32 = 1
 MAX_TIERS = 64
+
+
+def planner_path(n_candidates: int, cost_kind: int, n_entries: int) -> str:
+    """Which planner kernel a call takes: "select" or "rank"."""
+    if n_entries <= SELECT_MAX_ENTRIES and cost_kind != COST_ADDITIVE_INTERP:
+        return "select"
+    return "rank"
 
 
 class DsparkError(RuntimeError):

@@ -213,9 +213,10 @@ class VerifyStep:
 
     def kernels_per_step(self, separate_plan_pack: bool = False) -> int:
         """Kernels one compact step launches: survival + select (the pack
-        inside) for tables of <= api.SELECT_MAX_ENTRIES entries, else survival + rank + pack
+        inside) on the select path, else survival + rank + pack
         (separate calls add the pack kernel); then argmax + finalize."""
-        select = len(self.cfg.cost_M) <= api.SELECT_MAX_ENTRIES
+        c = self.cfg
+        select = api.planner_path(c.B * c.gamma, c.cost_kind, len(c.cost_M)) == "select"
         return (3 if (separate_plan_pack or not select) else 2) + 2
 
     def greedy_accept(self, logits: torch.Tensor, write_argmax: bool = True, stream=None) -> None:

@@ -45,3 +45,13 @@ def test_select_path_limit_matches_kernel():
         m = re.search(r"constexpr int kMaxSelect = (\d+);", f.read())
     assert m is not None
     assert api.SELECT_MAX_ENTRIES == int(m.group(1))
+
+
+def test_binding_planner_paths():
+    """api.planner_path restates plan.cu's routing (the select path's table
+    limit is checked against the kernel source above)."""
+    from confidence_scheduled_speculative_gb300 import api
+    assert api.planner_path(4096, api.COST_ADDITIVE, 5) == "select"
+    assert api.planner_path(4096, api.COST_SPS_1D, 31) == "select"
+    assert api.planner_path(4096, api.COST_SPS_1D, 32) == "rank"
+    assert api.planner_path(64, api.COST_ADDITIVE_INTERP, 5) == "rank"
