@@ -34,6 +34,7 @@ STATUS_INFEASIBLE = 64
 STATUS_BAD_INDEX = 128
 STATUS_TIMEOUT = 256
 STATUS_BAD_TIER = 512
+STATUS_OUT_OF_BOUNDS = 1024  # only the bounds-checked library sets it
 
 # cost tables of at most this many entries take the planner's single-CTA
 # select path (the pack fused into it); larger ones, and interpolated tables,
@@ -86,6 +87,7 @@ _VP, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c
 _SIGS = {
     "dspark_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "dspark_version": (ctypes.c_int, []),
+    "dspark_checked_build": (ctypes.c_int, []),
     "dspark_plan_workspace_bytes": (_SZ, [_I32, _I32]),
     "dspark_plan": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(dspark_plan_params),
                                    ctypes.POINTER(dspark_cost_table), _VP, _VP, _VP, _VP, _VP,
@@ -141,6 +143,9 @@ _SIGS = {
 
 
 def library_path() -> str:
+    """The normal library, or the bounds-checked one when DSPARK_CHECKED=1."""
+    if os.environ.get("DSPARK_CHECKED", "0") == "1":
+        return _build.CHECKED_LIB_PATH
     return _build.LIB_PATH
 
 
@@ -152,7 +157,7 @@ def load() -> ctypes.CDLL:
             path = library_path()
             if not os.path.exists(path):
                 raise RuntimeError(
-                    f"libdspark.so not found at {path}: build it first "
+                    f"{os.path.basename(path)} not found at {path}: build it first "
                     "(python -c 'import __graft_entry__ as g; g.build()')")
             lib = ctypes.CDLL(path)
             for name, (res, args) in _SIGS.items():
@@ -194,6 +199,10 @@ def dspark_strerror(code: int) -> str:
 
 def dspark_version() -> int:
     return int(load().dspark_version())
+
+
+def dspark_checked_build() -> bool:
+    return bool(load().dspark_checked_build())
 
 
 def dspark_plan_workspace_bytes(B: int, gamma: int) -> int:

@@ -56,6 +56,12 @@ struct Partial {
     int i;
 };
 
+// Partial slots of a workspace for max_rows rows: slot c + r of CTA c < kMaxCtas
+// and row r < max_rows.
+__host__ __device__ __forceinline__ long long partial_slots(int max_rows) {
+    return (long long)kMaxCtas + (max_rows > 0 ? max_rows : 0) + 1;
+}
+
 struct ArgmaxArgs {
     const void *logits;
     long long ld;
@@ -208,7 +214,8 @@ __global__ void __launch_bounds__(kArgmaxThreads, kCtasPerSm) argmax_kernel(Argm
             scan_scalar<T>(row, c0, c1, best, bidx, nan);
             block_best(best, bidx, red_v, red_i);
         }
-        if (threadIdx.x == 0) a.partial[blockIdx.x + r] = Partial{best, bidx};
+        if (threadIdx.x == 0 && in_bounds(blockIdx.x + r, partial_slots(a.max_rows), a.status))
+            a.partial[blockIdx.x + r] = Partial{best, bidx};
         q = seg_end;
     }
     if (__syncthreads_or(nan) && threadIdx.x == 0) flag(a.status, DSPARK_STATUS_NAN_LOGIT);
@@ -227,9 +234,10 @@ struct FinalArgs {
 };
 
 __device__ __forceinline__ int row_argmax(const Partial *partial, int row, long long cpr,
-                                          long long per) {
+                                          long long per, int max_rows, int32_t *status) {
     const long long q_first = (long long)row * cpr;
     const int c_lo = (int)div_nonneg(q_first, per), c_hi = (int)div_nonneg(q_first + cpr - 1, per);
+    if (!in_bounds(c_hi + row, partial_slots(max_rows), status)) return 0;
     // the first two partials (a row usually spans one or two CTAs) are
     // loaded together
     const Partial p0 = partial[c_lo + row];
@@ -255,7 +263,7 @@ __device__ __forceinline__ void write_argmax(const FinalArgs &a, int rows, long 
     if (!a.argmax || per <= 0) return;
     const int nthreads = gridDim.x * blockDim.x;
     for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < rows; row += nthreads)
-        a.argmax[row] = row_argmax(a.partial, row, cpr, per);
+        a.argmax[row] = row_argmax(a.partial, row, cpr, per, a.max_rows, a.status);
 }
 
 // BuildOutTokens and FinalizeAcceptLens for request r (lane 0 writes the scalars)
@@ -295,7 +303,7 @@ __global__ void __launch_bounds__(kFinalWarps * 32) greedy_finalize_kernel(Final
     const bool valid = r < a.B && lo >= 0 && hi <= rows && L >= 1 && L <= g + 1;
     // the request's row argmaxes first, so that their partial loads and the
     // argmax output pass's are in flight together
-    const int am = valid && lane < L ? row_argmax(a.partial, lo + lane, cpr, per) : 0;
+    const int am = valid && lane < L ? row_argmax(a.partial, lo + lane, cpr, per, a.max_rows, a.status) : 0;
     write_argmax(a, rows, cpr, per);
 
     if (r >= a.B) return;  // warp-uniform
@@ -336,7 +344,9 @@ __global__ void __launch_bounds__(kFinalWarps * 32) cap_finalize_kernel(FinalArg
     const int g = a.gamma;
     // the request's row argmaxes first (their loads in flight with the
     // argmax output pass's)
-    const int am0 = r < a.B && lane <= g ? row_argmax(a.partial, r * (g + 1) + lane, cpr, per) : 0;
+    const int am0 = r < a.B && lane <= g
+                        ? row_argmax(a.partial, r * (g + 1) + lane, cpr, per, a.max_rows, a.status)
+                        : 0;
     write_argmax(a, rows, cpr, per);
     if (threadIdx.x == 0) sums[0] = sums[1] = 0;
     __syncthreads();
@@ -433,7 +443,7 @@ using namespace dspark;
 extern "C" size_t dspark_accept_workspace_bytes(int32_t max_rows, int32_t V) {
     (void)V;
     if (max_rows < 0) max_rows = 0;
-    const size_t n = (size_t)kMaxCtas + (size_t)max_rows + 1;
+    const size_t n = (size_t)partial_slots(max_rows);
     return (n * sizeof(Partial) + 255) & ~size_t(255);
 }
 

@@ -51,3 +51,5 @@ extern "C" const char *dspark_strerror(int code) {
 }
 
 extern "C" int dspark_version(void) { return 100; }
+
+extern "C" int dspark_checked_build(void) { return dspark::kCheckedBuild ? 1 : 0; }

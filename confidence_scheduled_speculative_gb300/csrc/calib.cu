@@ -275,8 +275,12 @@ __global__ void __launch_bounds__(kRecThreads) sts_record_kernel(RecordArgs a) {
         if (sel && i >= first) {
             unsigned long long s = off_s + (i - first);  // i - first < capacity
             slot = (long long)(s >= cap ? s - cap : s);
-            a.rec_correct[slot] = c;
-            a.rec_tested[slot] = tested;
+            if (in_bounds(slot, a.capacity, a.status)) {
+                a.rec_correct[slot] = c;
+                a.rec_tested[slot] = tested;
+            } else {
+                slot = -1;
+            }
         }
         slot_s[tid] = slot;
         corr_s[tid] = c;
@@ -339,11 +343,14 @@ struct StatsArgs {
 // histogram gets count + (label << 32) and floor(p 2^32) by shared atomics;
 // the Brier and log-loss terms add to the thread's float pairs acc[0..3].
 __device__ __forceinline__ void stats_add(unsigned long long *hs, float *acc, int f, int k,
-                                          float p, bool y, int G, int M) {
+                                          float p, bool y, int G, int M, int32_t *status) {
     const unsigned long long q = conf_q(p);
-    unsigned long long *h = hs + ((size_t)(f * G + k) * M + conf_bin(q, M)) * 2;
-    atomicAdd(h, 1ull + ((unsigned long long)y << 32));
-    atomicAdd(h + 1, q);
+    const int bin = conf_bin(q, M);
+    if (in_bounds(bin, M, status)) {
+        unsigned long long *h = hs + ((size_t)(f * G + k) * M + bin) * 2;
+        atomicAdd(h, 1ull + ((unsigned long long)y << 32));
+        atomicAdd(h + 1, q);
+    }
     float th, tl;
     brier_pair(p, y, th, tl);
     acc_pair(acc[0], acc[1], th, tl);
@@ -401,8 +408,8 @@ __global__ void __launch_bounds__(kStatsThreads) calib_stats_kernel(StatsArgs a)
                 const float c = sts_confidence(zk, T_s[k]);
                 S[r] = (k == 0) ? c : __fmul_rn(S[r], c);
                 const bool y = k < cor[r];
-                if (S[r] == S[r]) stats_add(hs, acc, 0, k, S[r], y, G, M);
-                if (cor[r] >= k && c == c) stats_add(hs, acc + 4, 1, k, c, y, G, M);
+                if (S[r] == S[r]) stats_add(hs, acc, 0, k, S[r], y, G, M, a.status);
+                if (cor[r] >= k && c == c) stats_add(hs, acc + 4, 1, k, c, y, G, M, a.status);
                 any = true;
             }
             if (__any_sync(kFullMask, any)) {
@@ -547,7 +554,7 @@ __global__ void __launch_bounds__(kFitThreads) sts_fit_kernel(const __grid_const
         // the samples that count, packed to the front of the tile
         int n_in;
         const int pos = block_exclusive_scan<int>(fl & 1, scan_tmp, &n_in);
-        if (fl & 1) {
+        if ((fl & 1) && in_bounds(pos, kFitTile, a.status)) {
             z_s[pos] = zk;
             sp_s[pos] = sp;
             y_s[pos] = fl >> 1;
@@ -559,7 +566,9 @@ __global__ void __launch_bounds__(kFitThreads) sts_fit_kernel(const __grid_const
             auto add = [&](int s, float c) {
                 const float p = (k == 0) ? c : __fmul_rn(sp_s[s], c);
                 const unsigned long long q = conf_q(p);
-                const int idx = conf_bin(q, M) * kFitThreads + tid;
+                const int bin = conf_bin(q, M);
+                if (!in_bounds(bin, M, a.status)) return;
+                const int idx = bin * kFitThreads + tid;
                 bcl[idx] += 1ull + ((unsigned long long)y_s[s] << 32);
                 bconf[idx] += q;
             };

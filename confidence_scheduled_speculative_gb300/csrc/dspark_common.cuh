@@ -17,6 +17,25 @@ constexpr unsigned kFullMask = 0xffffffffu;
 // kernel can detect is reported here and the host decides.
 __device__ __forceinline__ void flag(int32_t *status, int bit) { atomicOr(status, bit); }
 
+// Bounds-checked build (-DDSPARK_CHECKED, built as libdspark_checked.so):
+// the kernels pass each index they compute from data through in_bounds()
+// before the global or shared-memory access it addresses.  An index outside
+// [0, n) flags DSPARK_STATUS_OUT_OF_BOUNDS and the access is skipped.  Every
+// such index is in range by construction once the inputs have passed their
+// own checks, so a flag marks a defect of the library.  In the normal build
+// in_bounds() is the constant true and the compiler removes it.
+#ifdef DSPARK_CHECKED
+constexpr bool kCheckedBuild = true;
+#else
+constexpr bool kCheckedBuild = false;
+#endif
+
+__device__ __forceinline__ bool in_bounds(long long i, long long n, int32_t *status) {
+    if (!kCheckedBuild || (i >= 0 && i < n)) return true;
+    flag(status, DSPARK_STATUS_OUT_OF_BOUNDS);
+    return false;
+}
+
 __device__ __forceinline__ unsigned lanemask_lt() {
     unsigned m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));

@@ -93,10 +93,10 @@ pack_kernel(const int32_t *__restrict__ anchor, const int32_t *__restrict__ draf
     bool over = false;
     if (r < B) {
         const int off = offs[warp];
-        if (lane == 0) cu[r + 1] = off + L;
+        if (lane == 0 && in_bounds(r + 1, (long long)B + 1, status)) cu[r + 1] = off + L;
         if (lane < L) {
             const int dst = off + lane;
-            if (dst < capacity) {
+            if (dst < capacity && in_bounds(dst, capacity, status)) {
                 ids[dst] = tok;
                 pos[dst] = pre + lane;
                 req[dst] = r;

@@ -197,8 +197,11 @@ survival_kernel(const float *__restrict__ z, const float *__restrict__ T, int B,
     if (__any_sync(kFullMask, bad) && lane == 0) flag(status, DSPARK_STATUS_BAD_INPUT);
     if (bin_keys && active && lane < kmax && s >= eps) {  // select path: bin the kept key
         const uint32_t key = key_of(s, true);
-        atomicAdd(&scratch->hcount[key >> kHistShift], 1u);
-        atomicAdd(&scratch->hsum[key >> kHistShift], (unsigned long long)fixed_of_key(key));
+        const uint32_t bin = key >> kHistShift;
+        if (in_bounds(bin, kHistBins, status)) {
+            atomicAdd(&scratch->hcount[bin], 1u);
+            atomicAdd(&scratch->hsum[bin], (unsigned long long)fixed_of_key(key));
+        }
     }
 }
 
@@ -416,6 +419,7 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
                 lo = j == 0 ? 0 : max(Mp + 1 - Bl, 0LL);
                 hi = Mj - Bl;
             }
+            if (!in_bounds(j, kTabStage, a.status)) continue;
             ts.range[j] = make_int2(sat_int(lo), sat_int(hi));
             ts.f32[j] = (float)__ldg(c.val + j);
         }
@@ -460,7 +464,8 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
                 const int r = i / G;
                 const int k = i - r * G;
                 const bool kept = (k < a.max_len - 1) && (sv[u] >= a.eps);
-                K[r * S + k] = key_of(sv[u], kept);
+                if (in_bounds((long long)r * S + k, (long long)B * S, a.status))
+                    K[r * S + k] = key_of(sv[u], kept);
                 kept_local += kept ? 1 : 0;
             }
         }
@@ -468,7 +473,8 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
     const int pad = P2 - G;
     for (int j = tid; j < B * pad; j += kRankThreads) {
         const int r = j / pad;
-        K[r * S + G + (j - r * pad)] = kDroppedKey;
+        if (in_bounds((long long)r * S + G + (j - r * pad), (long long)B * S, a.status))
+            K[r * S + G + (j - r * pad)] = kDroppedKey;
     }
     const int n_kept = block_sum<int>(kept_local, sm.scan32);  // syncs
     const int any_order_bad = __syncthreads_or(order_bad);
@@ -540,14 +546,14 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
         const long long m = fixed_of_key(key);
         if (lane == 0) {
             rank_out[x] = rk;
-            sorted[rk] = m;
+            if (in_bounds(rk, N, a.status)) sorted[rk] = m;
         }
         if (sparse) {
             int32_t *cnt_r = scratch_at<int32_t>(a.scratch, plan_count_offset(N)) + (size_t)r * (kMaxSparse + 1);
 #pragma unroll
             for (int t = 0; t < 3; ++t) {
                 const int j = lane + 32 * t;
-                if (j <= c.n && rk < sm.cand_b[j]) {
+                if (j <= c.n && rk < sm.cand_b[j] && in_bounds(j, kMaxSparse + 1, a.status)) {
                     my_acc[t] += (unsigned long long)m;
                     atomicAdd(cnt_r + j, 1);
                 }
@@ -776,7 +782,16 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
     const bool dense = dense_table(c.kind, c.n);
     long long *P = dense ? reinterpret_cast<long long *>(smem + rank_head_bytes())
                          : scratch_at<long long>(a.scratch, plan_prefix_offset(a.N));
-    auto load_P = [&](long long b) -> long long { return dense ? P[b] : __ldcg(P + b); };
+    // P holds N + 1 sums; the float taus of an interpolated table fill the
+    // key region's B * (P2 + 1) words
+    const long long nP = (long long)a.N + 1, nT = (long long)B * run_stride(a.P2);
+    auto load_P = [&](long long b) -> long long {
+        if (!in_bounds(b, nP, a.status)) return 0;
+        return dense ? P[b] : __ldcg(P + b);
+    };
+    auto dense_P = [&](long long b) -> long long {  // a dense table's P (shared memory)
+        return in_bounds(b, nP, a.status) ? P[b] : 0;
+    };
 
     // (a) dense tables: P[i] = sum of the i largest survivals in units of
     // 2^-37 (P[0] = 0), a blocked scan written to the workspace
@@ -802,14 +817,14 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
         for (int u = 0; u < kScanReg; ++u) {
             if (lo + u < hi) {
                 run += v[u];
-                P[lo + u + 1] = run;
-                if (want_f) tauf[lo + u + 1] = tau_float(B, run);
+                if (in_bounds(lo + u + 1, nP, a.status)) P[lo + u + 1] = run;
+                if (want_f && in_bounds(lo + u + 1, nT, a.status)) tauf[lo + u + 1] = tau_float(B, run);
             }
         }
         for (int i = lo + kScanReg; i < hi; ++i) {
             run += __ldcg(sorted + i);
-            P[i + 1] = run;
-            if (want_f) tauf[i + 1] = tau_float(B, run);
+            if (in_bounds(i + 1, nP, a.status)) P[i + 1] = run;
+            if (want_f && in_bounds(i + 1, nT, a.status)) tauf[i + 1] = tau_float(B, run);
         }
         if (tid == 0) {
             P[0] = 0;
@@ -849,7 +864,7 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
                 my_bad_cost = true;
                 return;
             }
-            const long long Pb = __ldcg(P + b);
+            const long long Pb = in_bounds(b, nP, a.status) ? __ldcg(P + b) : 0;
             const double theta = __ddiv_rn(tau_of(B, Pb), Tm);
             const long long kk = __double_as_longlong(theta);
             if (cand_better(kk, (int)b, my_key, my_b)) {
@@ -864,6 +879,9 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
         const long long b0 = (long long)tid * per;
         const int cnt = (int)max(0LL, min(b0 + per, b_top + 1) - b0);
         const float *tauf = interp_tau_smem(sm);  // tau of every budget, from the scan
+        auto tau_at = [&](long long b) -> float {
+            return in_bounds(b, nT, a.status) ? tauf[b] : 0.0f;
+        };
         InterpWalk wk0(tM, tV, tV32, c.n);
         if (cnt > 0) wk0.init((long long)B + b0);
         float my_floor = 0.0f;
@@ -872,7 +890,7 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
         for (int i = 0; i < kInterpPer; ++i) {
             if (i >= cnt) break;
             float lo, hi;
-            if (wk.bounds(B, b0 + i, tauf[b0 + i], fixed32, lo, hi)) {
+            if (wk.bounds(B, b0 + i, tau_at(b0 + i), fixed32, lo, hi)) {
                 my_floor = fmaxf(my_floor, lo);
             } else {
                 exact(b0 + i, wk.seg);  // uncertain sign of T, or not finite in fp32
@@ -892,7 +910,7 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
         for (int i = 0; i < kInterpPer; ++i) {
             if (i >= cnt) break;
             float lo, hi;
-            if (wk.bounds(B, b0 + i, tauf[b0 + i], fixed32, lo, hi) && hi >= floor_all) {
+            if (wk.bounds(B, b0 + i, tau_at(b0 + i), fixed32, lo, hi) && hi >= floor_all) {
                 const int slot = atomicAdd(&sm.n_icand, 1);
                 if (slot < kRankThreads) {
                     sm.icand_b[slot] = (int)(b0 + i);
@@ -932,7 +950,7 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
         };
         auto exact = [&](int j, int b) {
             const double vj = __ldg(c.val + j);
-            const long long Pb = P[b];
+            const long long Pb = dense_P(b);
             const double tau = tau_of(B, Pb);
             double theta;
             if (c.kind == DSPARK_COST_SPS_1D) {
@@ -958,7 +976,7 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
             int b;
             float v32, lo, hi;
             if (!entry(j, b, v32)) continue;
-            if (dense_theta_bounds(c.kind, tau_float(B, P[b]), v32, fixed32, lo, hi)) {
+            if (dense_theta_bounds(c.kind, tau_float(B, dense_P(b)), v32, fixed32, lo, hi)) {
                 my_floor = fmaxf(my_floor, lo);
                 my_top = fmaxf(my_top, hi);
             } else {
@@ -978,7 +996,7 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
                 int b;
                 float v32, lo, hi;
                 if (entry(j, b, v32) &&
-                    dense_theta_bounds(c.kind, tau_float(B, P[b]), v32, fixed32, lo, hi) &&
+                    dense_theta_bounds(c.kind, tau_float(B, dense_P(b)), v32, fixed32, lo, hi) &&
                     hi >= floor_all)
                     exact(j, b);
             }
@@ -1136,7 +1154,8 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
     for (int r = tid; r < B; r += kRankThreads) {
         int cnt = 0;
         if (sparse) {
-            cnt = slot >= 0 ? __ldcg(counts + (size_t)r * (kMaxSparse + 1) + slot) : 0;
+            cnt = slot >= 0 && in_bounds(slot, kMaxSparse + 1, a.status)
+                      ? __ldcg(counts + (size_t)r * (kMaxSparse + 1) + slot) : 0;
         } else {
 #pragma unroll 8
             for (int k = 0; k < kmax; ++k) cnt += __ldcg(rank_in + r * G + k) < budget ? 1 : 0;
@@ -1298,7 +1317,9 @@ __device__ void radix_thresholds(const PlanArgs &a, SelSmem &sm, const uint32_t 
                         if (row == run_row && dg == run_d) {
                             ++run_c;
                         } else {
-                            if (run_row >= 0) atomicAdd(&sm.H[cur][run_row][run_d], run_c);
+                            if (run_row >= 0 && in_bounds(run_row * kRadixBins + (int)run_d,
+                                                          kSelSlots * kRadixBins, a.status))
+                                atomicAdd(&sm.H[cur][run_row][run_d], run_c);
                             run_row = row;
                             run_d = dg;
                             run_c = 1u;
@@ -1310,7 +1331,9 @@ __device__ void radix_thresholds(const PlanArgs &a, SelSmem &sm, const uint32_t 
                     ++r;
                 }
             }
-            if (run_row >= 0) atomicAdd(&sm.H[cur][run_row][run_d], run_c);
+            if (run_row >= 0 && in_bounds(run_row * kRadixBins + (int)run_d,
+                                          kSelSlots * kRadixBins, a.status))
+                atomicAdd(&sm.H[cur][run_row][run_d], run_c);
         }
         __syncthreads();
         // warp j: the digit where the running count reaches rem_j.  Meanwhile
@@ -1430,6 +1453,7 @@ __device__ __forceinline__ void select_pack(const PlanArgs &a, SelSmem &sm, bool
             else hi = mid - 1;
         }
         const int j = dst - sm.lens_s[lo];
+        if (!in_bounds(j, G + 1, a.status) || !in_bounds(dst, capacity, a.status)) continue;
         int tok, pre;
         if (staged) {
             tok = j == 0 ? sm.stage[lo] : sm.stage[2 * B + lo * G + j - 1];
@@ -1605,7 +1629,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
             sm.stage[i] = __ldg(a.pk.anchor + i);
             sm.stage[B + i] = __ldg(a.pk.prefix + i);
         }
-        for (int i = tid; i < N; i += kSelThreads) sm.stage[2 * B + i] = __ldg(a.pk.draft + i);
+        for (int i = tid; i < N; i += kSelThreads)
+            if (in_bounds(2 * B + i, kStage, a.status)) sm.stage[2 * B + i] = __ldg(a.pk.draft + i);
     }
     pdl_wait();  // survivals and bins come from survival_kernel
     const int forced = resolve_forced(a);
@@ -1709,7 +1734,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
             rem = b - before;
             cnt = (int)sm.cum[d] - before;
             ps = sm.csum[d];
-            if (lane == 0) atomicOr(&sm.binmask[d >> 5], 1u << (d & 31));
+            if (lane == 0 && in_bounds(d, kHistBins, a.status))
+                atomicOr(&sm.binmask[d >> 5], 1u << (d & 31));
         }
         if (lane == 0) {
             sm.cand_b[warp] = b;
@@ -1756,6 +1782,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
             const unsigned long long ci = sm.LC[i];
             int pos = 0;
             for (int y = 0; y < m; ++y) pos += sm.LC[y] < ci ? 1 : 0;
+            if (!in_bounds(pos, m, a.status)) continue;
             sm.SC[pos] = ci;
             sm.SF[pos] = sm.LF[i];
         }
@@ -1774,11 +1801,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
                     below = first ? sm.hcnt[lane] : 0;
                 }
                 const int start = __reduce_add_sync(kFullMask, below);
+                // the bin's candidates are all gathered: start + rem <= m
+                const bool in = in_bounds(start + rem - 1, m, a.status);
                 unsigned long long part = 0ull;
-                for (int q = lane; q < rem; q += 32) part += sm.SF[start + q];
+                for (int q = lane; in && q < rem; q += 32) part += sm.SF[start + q];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFullMask, part, o);
-                if (lane == 0) {
+                if (lane == 0 && in) {
                     sm.cthr[warp] = sm.SC[start + rem - 1];
                     sm.P[warp] = sm.psum[warp] + part;
                 }
@@ -1814,7 +1843,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
                 int len = -1;
                 if (!in && (k == 0 || prev_in)) len = k;  // first depth not selected
                 if (in && k == G - 1) len = G;            // every depth selected
-                if (len >= 0) {
+                if (len >= 0 && in_bounds(r, B, a.status)) {
                     const int L = min(max(1 + len, a.min_len), a.max_len);
                     a.verify_lens[r] = L;
                     sm.lens_s[r] = L;

@@ -94,6 +94,12 @@ struct SampArgs {
     int split;          // CTAs (one thread-block cluster) per request in the accept kernel
 };
 
+// Partial slots: one per (CTA, virtual row) piece, CTA c < kSampMaxCtas and
+// virtual row v < max_rows + B*gamma.
+__device__ __forceinline__ long long samp_slots(const SampArgs &a) {
+    return (long long)kSampMaxCtas + a.max_rows + (long long)a.B * a.gamma + 1;
+}
+
 __device__ __forceinline__ int samp_rows(const SampArgs &a) {
     const int r = a.cu[a.B];
     return r < 0 ? 0 : (r > a.max_rows ? a.max_rows : r);
@@ -161,7 +167,7 @@ __device__ __forceinline__ void norm_chunk(const uint4 &v, float &m, float &s, b
 // of the piece.  The sums travel as float pairs (hi + lo, error-free
 // additions): no fp64 instruction in the streaming kernel (GB300's fp64
 // unit is small), no block barrier between pieces.
-__device__ __forceinline__ void norm_warp(float m, float s, NormPartial *dst) {
+__device__ __forceinline__ void norm_warp(float m, float s, NormPartial *dst, bool store) {
     float M = m;
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, d));
@@ -174,12 +180,12 @@ __device__ __forceinline__ void norm_warp(float m, float s, NormPartial *dst) {
         e = __fadd_rn(e, __fadd_rn(tl, ol));
         fast_two_sum(h, e, th, tl);
     }
-    if ((threadIdx.x & 31) == 0) *dst = NormPartial{M, th, tl, 0.0f};
+    if ((threadIdx.x & 31) == 0 && store) *dst = NormPartial{M, th, tl, 0.0f};
 }
 
 // Warp-wide fold of one partial per lane (lanes past the piece's warps hold
 // m = -inf, s = 0); lane 0 writes the result.
-__device__ __forceinline__ void norm_fold(const NormPartial &p, NormPartial *dst) {
+__device__ __forceinline__ void norm_fold(const NormPartial &p, NormPartial *dst, bool store) {
     float M = p.m;
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, d));
@@ -198,7 +204,7 @@ __device__ __forceinline__ void norm_fold(const NormPartial &p, NormPartial *dst
         e = __fadd_rn(e, __fadd_rn(tl, ol));
         fast_two_sum(h, e, th, tl);
     }
-    if ((threadIdx.x & 31) == 0) *dst = NormPartial{M, th, tl, 0.0f};
+    if ((threadIdx.x & 31) == 0 && store) *dst = NormPartial{M, th, tl, 0.0f};
 }
 
 // Virtual row v: a packed target row (v < rows) or the draft row of the
@@ -302,7 +308,8 @@ __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) softmax_norm_ker
                 norm_take(z, m, s);
             }
         }
-        norm_warp(m, s, a.part_w + (size_t)(blockIdx.x + v) * kNormWarps + (tid >> 5));
+        const bool in = in_bounds(blockIdx.x + v, samp_slots(a), a.status);
+        norm_warp(m, s, a.part_w + (size_t)(blockIdx.x + v) * kNormWarps + (tid >> 5), in);
         q = seg_end;
     }
     if (__syncthreads_or(nan) && tid == 0) flag(a.status, DSPARK_STATUS_NAN_LOGIT);
@@ -313,8 +320,9 @@ __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) softmax_norm_ker
         const int lane = tid & 31;
         for (int v = v0 + (tid >> 5); v <= v1; v += kNormWarps) {
             NormPartial p = NormPartial{-INFINITY, 0.0f, 0.0f, 0.0f};
-            if (lane < kNormWarps) p = a.part_w[(size_t)(blockIdx.x + v) * kNormWarps + lane];
-            norm_fold(p, a.part + blockIdx.x + v);
+            const bool in = in_bounds(blockIdx.x + v, samp_slots(a), a.status);
+            if (lane < kNormWarps && in) p = a.part_w[(size_t)(blockIdx.x + v) * kNormWarps + lane];
+            norm_fold(p, a.part + blockIdx.x + v, in);
         }
     }
 }
@@ -322,13 +330,15 @@ __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) softmax_norm_ker
 // ---------------------------------------------------- acceptance and bonus
 
 // (M, S) of virtual row v from the partials of the CTAs that covered it.
-__device__ __forceinline__ void row_stats(const NormPartial *part, long long cpr, long long per,
+__device__ __forceinline__ void row_stats(const SampArgs &a, long long cpr, long long per,
                                           int v, float &M, double &S) {
+    const NormPartial *part = a.part;
     const long long q_first = (long long)v * cpr;
     const int c_lo = (int)div_nonneg(q_first, per), c_hi = (int)div_nonneg(q_first + cpr - 1, per);
     M = -INFINITY;
-    for (int c = c_lo; c <= c_hi; ++c) M = fmaxf(M, part[c + v].m);
     S = 0.0;
+    if (!in_bounds(c_hi + v, samp_slots(a), a.status)) return;
+    for (int c = c_lo; c <= c_hi; ++c) M = fmaxf(M, part[c + v].m);
     if (M > -INFINITY)
         for (int c = c_lo; c <= c_hi; ++c) {
             const NormPartial p = part[c + v];
@@ -550,7 +560,7 @@ __device__ __forceinline__ void st_cluster_u64(void *local, unsigned rank, unsig
 // rsum[w * rpw + k] = round k of warp w (0 past the row).
 template <typename T, bool HAS_D>
 __device__ __forceinline__ void bonus_rounds(const BonusRow &b, int V, bool vec, int q, int rpw,
-                                             unsigned long long *rsum) {
+                                             unsigned long long *rsum, int32_t *status) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     // rounds in flight per lane: kBonusChunks 16-byte chunks of the rows read
     constexpr int U = kBonusChunks / (LaneChunks<T>::NC * (HAS_D ? 2 : 1)) > 0
@@ -568,7 +578,8 @@ __device__ __forceinline__ void bonus_rounds(const BonusRow &b, int V, bool vec,
             if (k0 + u < rpw) {  // warp-uniform
                 const unsigned long long t = warp_round_total(
                     lane_total_of<T, HAS_D>(b, (first + k0 + u) * kRound + lane * kTokLane, V, ld[u], c[u]));
-                if (lane == 0) rsum[warp * rpw + k0 + u] = t;
+                if (lane == 0 && in_bounds(warp * rpw + k0 + u, kSampWarps * kMaxRounds, status))
+                    rsum[warp * rpw + k0 + u] = t;
             }
         }
     }
@@ -635,10 +646,10 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sampling_accept_
         const bool tok_ok = dj >= 0 && dj < V;
         float mt = -INFINITY, md = -INFINITY;
         double st = 0.0, sd = 0.0;
-        if (has_t) row_stats(a.part, cpr, per, lo + lane, mt, st);
+        if (has_t) row_stats(a, cpr, per, lo + lane, mt, st);
         if (has_d) {
             if (!a.draft_lse) {
-                row_stats(a.part, cpr, per, vd0 + lane, md, sd);
+                row_stats(a, cpr, per, vd0 + lane, md, sd);
             } else if (isfinite(lse)) {  // q = exp(z - lse): "max" lse, sum 1
                 md = lse;
                 sd = 1.0;
@@ -687,8 +698,8 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sampling_accept_
     unsigned long long Wq = 0ull, before = 0ull, slice = 0ull;
     for (int attempt = 0; attempt < 2; ++attempt) {
         if (attempt > 0) cluster_sync();  // every CTA has read the previous totals
-        if (b.d) bonus_rounds<T, true>(b, V, vec, q, rpw, rsum);
-        else bonus_rounds<T, false>(b, V, vec, q, rpw, rsum);
+        if (b.d) bonus_rounds<T, true>(b, V, vec, q, rpw, rsum, a.status);
+        else bonus_rounds<T, false>(b, V, vec, q, rpw, rsum, a.status);
         if (attempt == 0) cluster_wait();  // every CTA of the cluster runs
         __syncthreads();
         if (warp == 0) {  // this slice's total into slot q of every CTA of the cluster

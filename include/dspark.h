@@ -65,12 +65,22 @@ extern "C" {
 #define DSPARK_STATUS_BAD_INDEX   128 /* a packed row's strided destination outside the buffer */
 #define DSPARK_STATUS_TIMEOUT     256 /* a kernel's bounded wait gave up (its outputs are incomplete) */
 #define DSPARK_STATUS_BAD_TIER    512 /* a shared verify tier below this rank's packed rows */
+/* Set only by the bounds-checked build (libdspark_checked.so, compiled with
+ * -DDSPARK_CHECKED): an index a kernel computed from data fell outside the
+ * buffer (global or shared memory) it addresses; the access was skipped.  It
+ * always marks a defect of the library, never of the inputs.  The normal
+ * build carries no such checks and never sets it. */
+#define DSPARK_STATUS_OUT_OF_BOUNDS 1024
 
 /* Message for a DSPARK_ERR_* code (static string). */
 DSPARK_API const char *dspark_strerror(int code);
 
 /* Library version: major*10000 + minor*100 + patch. */
 DSPARK_API int dspark_version(void);
+
+/* 1 in the bounds-checked build (see DSPARK_STATUS_OUT_OF_BOUNDS), 0 in the
+ * normal one.  The two builds export the same calls with the same results. */
+DSPARK_API int dspark_checked_build(void);
 
 /* ---------------------------------------------------------------- planner */
 

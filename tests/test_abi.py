@@ -314,3 +314,18 @@ def test_calibration_argument_checks(lib):
     assert call_fit(M=40) == -1
     assert call_fit(ws=None) == -2
     assert call_fit(wsb=need - 256) == -2
+
+
+def test_checked_variant_builds_and_reports_itself():
+    """The bounds-checked library exports the same calls and says which it
+    is; the normal one says it is not checked."""
+    from confidence_scheduled_speculative_gb300 import build
+    try:
+        normal, checked = build.build(), build.build(checked=True)
+    except RuntimeError as e:  # pragma: no cover - toolkit missing
+        pytest.skip(str(e))
+    assert checked != normal
+    libs = ctypes.CDLL(normal), ctypes.CDLL(checked)
+    for n in declared_symbols():
+        assert all(hasattr(lib, n) for lib in libs), n
+    assert [lib.dspark_checked_build() for lib in libs] == [0, 1]
