@@ -36,10 +36,12 @@ STATUS_TIMEOUT = 256
 STATUS_BAD_TIER = 512
 STATUS_OUT_OF_BOUNDS = 1024  # only the bounds-checked library sets it
 
-# cost tables of at most this many entries take the planner's single-CTA
-# select path (the pack fused into it); larger ones, and interpolated tables,
-# the multi-CTA rank path
+# cost tables of at most SELECT_MAX_ENTRIES entries take the planner's
+# single-CTA select path, larger ones up to DENSE_MAX_ENTRIES its single-CTA
+# dense path (both with the pack fused in); larger tables, and interpolated
+# ones, the multi-CTA rank path
 SELECT_MAX_ENTRIES = 31
+DENSE_MAX_ENTRIES = 6143
 COST_SPS_1D = 0
 COST_ADDITIVE = 1
 COST_ADDITIVE_INTERP = 2
@@ -49,10 +51,12 @@ MAX_TIERS = 64
 
 
 def planner_path(n_candidates: int, cost_kind: int, n_entries: int) -> str:
-    """Which planner kernel a call takes: "select" or "rank"."""
-    if n_entries <= SELECT_MAX_ENTRIES and cost_kind != COST_ADDITIVE_INTERP:
+    """Which planner kernel a call takes: "select", "dense" or "rank"."""
+    if cost_kind == COST_ADDITIVE_INTERP:
+        return "rank"
+    if n_entries <= SELECT_MAX_ENTRIES:
         return "select"
-    return "rank"
+    return "dense" if n_entries <= DENSE_MAX_ENTRIES else "rank"
 
 
 class DsparkError(RuntimeError):

@@ -6,7 +6,10 @@
 //   [TUT] charlestar.github.io tutorial "DSpark confidence-scheduled
 //         speculative decoding"
 //
-// Two kernels:
+// The survival kernel, then one of three planner kernels by cost table:
+// select_kernel (at most 31 entries) and dense_select_kernel (up to 6143
+// entries, not interpolated) run on one CTA and are described at their
+// definitions; rank_kernel takes the rest:
 //   survival_kernel  one warp per request, lane k = depth: STS
 //                    c_k = sigmoid(z_k / T_k) ([AVS] §二) and the prefix
 //                    survival S_k = prod_{i<=k} c_i ([AVS] §一), each lane
@@ -389,6 +392,32 @@ __device__ __forceinline__ int entry_last_budget(const CostArgs &c, int j, int M
     return blo > bhi ? -1 : (int)bhi;
 }
 
+// Entry j's range of budgets [x, y] whose M = B + b looks it up, before the
+// clip to the largest in-range budget (saturated to int); order_bad is set
+// when M_j does not exceed M_{j-1}.
+__device__ __forceinline__ int2 entry_range_from(int kind, int n, int j, long long Mp,
+                                                 long long Mj, long long Mn, long long Bl,
+                                                 bool &order_bad) {
+    if (j > 0 && !(Mj > Mp)) order_bad = true;
+    long long lo, hi;
+    if (kind == DSPARK_COST_SPS_1D) {
+        lo = j == 0 ? 0 : max(Mj - Bl, 0LL);
+        hi = j == n - 1 ? (long long)INT_MAX : Mn - 1 - Bl;
+    } else {
+        lo = j == 0 ? 0 : max(Mp + 1 - Bl, 0LL);
+        hi = Mj - Bl;
+    }
+    return make_int2(sat_int(lo), sat_int(hi));
+}
+
+// The same with M_{j-1}, M_j, M_{j+1} loaded here.
+__device__ __forceinline__ int2 entry_range(const CostArgs &c, int j, long long Bl, bool &order_bad) {
+    const long long Mj = __ldg(c.M + j);
+    const long long Mp = j > 0 ? __ldg(c.M + j - 1) : 0;
+    const long long Mn = j < c.n - 1 ? __ldg(c.M + j + 1) : 0;
+    return entry_range_from(c.kind, c.n, j, Mp, Mj, Mn, Bl, order_bad);
+}
+
 
 __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -406,21 +435,9 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
         // 64-bit range arithmetic and the fp64 -> fp32 conversions run here,
         // off the critical path
         const TableStage ts = table_stage(smem_raw, a);
-        const long long Bl = B;
         for (int j = tid; j < c.n; j += kRankThreads) {
-            const long long Mj = __ldg(c.M + j);
-            const long long Mp = j > 0 ? __ldg(c.M + j - 1) : 0;
-            if (j > 0 && !(Mj > Mp)) order_bad = true;
-            long long lo, hi;
-            if (c.kind == DSPARK_COST_SPS_1D) {
-                lo = j == 0 ? 0 : max(Mj - Bl, 0LL);
-                hi = j == c.n - 1 ? (long long)INT_MAX : (long long)__ldg(c.M + j + 1) - 1 - Bl;
-            } else {
-                lo = j == 0 ? 0 : max(Mp + 1 - Bl, 0LL);
-                hi = Mj - Bl;
-            }
-            if (!in_bounds(j, kTabStage, a.status)) continue;
-            ts.range[j] = make_int2(sat_int(lo), sat_int(hi));
+            if (!in_bounds(j, kTabStage, a.status)) break;
+            ts.range[j] = entry_range(c, j, B, order_bad);
             ts.f32[j] = (float)__ldg(c.val + j);
         }
     }
@@ -1255,6 +1272,17 @@ struct SelSmem {
     int32_t M_s[kMaxSelect];
     int n_gather, bad_table, budget_s;
     unsigned long long cstar;  // C* of the chosen budget (kNoComposite: none)
+    // dense_select_kernel
+    unsigned long long scan64[40];
+    unsigned int d_floor;      // the largest lower bound of theta (float bits)
+    int d_ncand, d_marked;     // entries left after the bounds; keys in their bins
+    double d_fixed;            // bias + alpha
+    float d_fixed_lo, d_fixed_hi;  // rounded down and up to float
+    unsigned long long d_fP, d_fC;  // P and C* at the forced budget
+    int d_item[32];                 // entry of each threshold slot (-1: the forced budget)
+    long long d_bkey[32];           // per-warp first maximiser
+    int d_bb[32];
+    unsigned long long d_bP[32], d_bC[32];
 };
 
 __device__ __forceinline__ unsigned long long composite(uint32_t key, int e) {
@@ -1574,69 +1602,18 @@ __device__ __noinline__ void select_theta(const PlanArgs &a, SelSmem &sm, long l
     }
 }
 
+// (1) of select_kernel and dense_select_kernel, after the dependency wait:
+// the thread's two bins (cleared for the next call, unless a later pass of
+// the same call reads them), its keys, and the block scan of the bins into
+// inclusive counts (cum) and exclusive fixed-point sums (csum).  Returns the
+// number of kept candidates.
 template <int IPT>
-__global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    SelSmem &sm = *reinterpret_cast<SelSmem *>(smem_raw);
+__device__ __forceinline__ int select_bins(const PlanArgs &a, SelSmem &sm, uint32_t (&key)[IPT]) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int B = a.B, G = a.gamma, N = a.N;
+    const int G = a.gamma, N = a.N;
     const int kmax = a.max_len - 1;
-    const CostArgs &c = a.cost;
-    const int nc = c.n + 1;
     const int i0 = tid * IPT;
-    const int r0 = i0 / G, k0 = i0 - r0 * G;  // request and depth of this thread's first candidate
-
-    pdl_trigger();
-    // while the survivals are computed: warp j fetches cost entry j (for its
-    // budget range); warp 0 fetches entry `lane` and prepares its theta
-    // divisor, so that only the product or quotient is left for later
-    int Mj = 0, Mprev = 0, Mnext = 0;
-    if (warp < c.n) {
-        Mj = __ldg(c.M + warp);
-        Mprev = warp > 0 ? __ldg(c.M + warp - 1) : 0;
-        Mnext = warp < c.n - 1 ? __ldg(c.M + warp + 1) : 0;
-    }
-    const int Mlast = __ldg(c.M + c.n - 1);
-    if (warp == 0) {
-        bool bad_entry = false;
-        if (lane < c.n) {
-            const int m = __ldg(c.M + lane);
-            const double v = __ldg(c.val + lane);
-            bad_entry = lane > 0 && !(m > __ldg(c.M + lane - 1));
-            double Tm = 0.0;
-            bool ok;
-            if (c.kind == DSPARK_COST_SPS_1D) {
-                ok = v > 0.0 && isfinite(v);
-            } else {
-                Tm = __dadd_rn(__dadd_rn(c.bias, c.alpha), v);
-                ok = Tm > 0.0 && isfinite(Tm);
-            }
-            sm.val_s[lane] = v;
-            sm.div_s[lane] = Tm;
-            sm.ok_s[lane] = ok ? 1 : 0;
-            sm.M_s[lane] = m;
-        }
-        const bool bt = __any_sync(kFullMask, bad_entry);
-        if (lane == 0) sm.bad_table = bt ? 1 : 0;
-    }
-    if (tid < kHistBins / 32) sm.binmask[tid] = 0u;
-    if (tid == 0) sm.n_gather = 0;
-    // the fused pack's step inputs are not written by the planner: stage
-    // them now, while the survivals are computed
-    const bool staged = a.pk.on && (long long)B * (G + 2) <= kStage;
-    if (staged) {
-        for (int i = tid; i < B; i += kSelThreads) {
-            sm.stage[i] = __ldg(a.pk.anchor + i);
-            sm.stage[B + i] = __ldg(a.pk.prefix + i);
-        }
-        for (int i = tid; i < N; i += kSelThreads)
-            if (in_bounds(2 * B + i, kStage, a.status)) sm.stage[2 * B + i] = __ldg(a.pk.draft + i);
-    }
-    pdl_wait();  // survivals and bins come from survival_kernel
-    const int forced = resolve_forced(a);
-
-    // (1) this thread's two bins, cleared for the next call (unless a later
-    // pass of the same call reads them); its keys
+    const int k0 = i0 - (i0 / G) * G;
     unsigned int h0, h1;
     unsigned long long s0, s1;
     {
@@ -1653,7 +1630,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
             *hs = make_ulonglong2(0ull, 0ull);
         }
     }
-    uint32_t key[IPT];
     {
         float sv[IPT];
 #pragma unroll
@@ -1710,82 +1686,102 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
         sm.csum[2 * tid + 1] = sex + s0;
     }
     __syncthreads();
-    long long b_top = n_kept;  // largest in-range budget
-    if (c.kind == DSPARK_COST_ADDITIVE) b_top = min(b_top, (long long)Mlast - (long long)B);
+    return n_kept;
+}
 
-    // warp j: candidate budget b_j, the top bin holding its threshold and
-    // its rank inside the bin
-    if (warp < nc) {
-        int b;
-        if (warp < c.n) b = entry_last_budget(c, warp, Mj, Mprev, Mnext, B, b_top);
-        else b = (forced >= 0 && b_top >= 0) ? (int)min((long long)forced, b_top) : -1;
-        int rem = 0, d = 0, cnt = 0;
-        unsigned long long ps = 0ull;
-        if (b >= 1) {  // b <= n_kept = cum[2047]
-            const unsigned ub = (unsigned)b;
-            // lane 31 always votes (cum[2047] = n_kept >= b); the clamps only keep
-            // the indices inside the table
-            const int l1 = max(__ffs(__ballot_sync(kFullMask, sm.cum[64 * lane + 63] >= ub)) - 1, 0);
-            const int base = 64 * l1;
-            const int l2 = max(__ffs(__ballot_sync(kFullMask, sm.cum[base + 2 * lane + 1] >= ub)) - 1, 0);
-            d = base + 2 * l2;
-            if (sm.cum[d] < ub) ++d;
-            const int before = d > 0 ? (int)sm.cum[d - 1] : 0;
-            rem = b - before;
-            cnt = (int)sm.cum[d] - before;
-            ps = sm.csum[d];
-            if (lane == 0 && in_bounds(d, kHistBins, a.status))
-                atomicOr(&sm.binmask[d >> 5], 1u << (d & 31));
-        }
-        if (lane == 0) {
-            sm.cand_b[warp] = b;
-            sm.rem[warp] = rem;
-            sm.dbin[warp] = d;
-            sm.hcnt[warp] = cnt;
-            sm.psum[warp] = ps;
-            sm.P[warp] = 0ull;
-            sm.cthr[warp] = kNoComposite;
-        }
+// Threshold slot `slot` (one warp, every lane calls) takes candidate budget
+// b: the top bin holding its threshold, its rank inside the bin (rem, from
+// 1), the bin's count and the fixed-point sum of the bins before; the bin is
+// marked for the gather.  b < 1: no threshold.
+__device__ __forceinline__ void slot_setup(SelSmem &sm, int slot, int lane, int b,
+                                           int32_t *status) {
+    int rem = 0, d = 0, cnt = 0;
+    unsigned long long ps = 0ull;
+    if (b >= 1) {  // b <= n_kept = cum[2047]
+        const unsigned ub = (unsigned)b;
+        // lane 31 always votes (cum[2047] = n_kept >= b); the clamps only keep
+        // the indices inside the table
+        const int l1 = max(__ffs(__ballot_sync(kFullMask, sm.cum[64 * lane + 63] >= ub)) - 1, 0);
+        const int base = 64 * l1;
+        const int l2 = max(__ffs(__ballot_sync(kFullMask, sm.cum[base + 2 * lane + 1] >= ub)) - 1, 0);
+        d = base + 2 * l2;
+        if (sm.cum[d] < ub) ++d;
+        const int before = d > 0 ? (int)sm.cum[d - 1] : 0;
+        rem = b - before;
+        cnt = (int)sm.cum[d] - before;
+        ps = sm.csum[d];
+        if (lane == 0 && in_bounds(d, kHistBins, status))
+            atomicOr(&sm.binmask[d >> 5], 1u << (d & 31));
     }
-    __syncthreads();
+    if (lane == 0) {
+        sm.cand_b[slot] = b;
+        sm.rem[slot] = rem;
+        sm.dbin[slot] = d;
+        sm.hcnt[slot] = cnt;
+        sm.psum[slot] = ps;
+        sm.P[slot] = 0ull;
+        sm.cthr[slot] = kNoComposite;
+    }
+}
 
-    // (2) gather the candidates of the marked bins (order irrelevant)
-    {
-        int r = r0, k = k0;
+// Gather the candidates of the marked bins into LC (composites) and LF
+// (fixed-point survivals), in no particular order; sm.n_gather counts them
+// all, the first kGather are stored.
+template <int IPT>
+__device__ __forceinline__ void gather_marked(const PlanArgs &a, SelSmem &sm,
+                                              const uint32_t (&key)[IPT], int r0, int k0) {
+    const int lane = threadIdx.x & 31;
+    const int B = a.B, G = a.gamma;
+    int r = r0, k = k0;
 #pragma unroll
-        for (int u = 0; u < IPT; ++u) {
-            const uint32_t kk = key[u];
-            const uint32_t bin = kk >> kHistShift;
-            const bool take = kk != kDroppedKey && ((sm.binmask[bin >> 5] >> (bin & 31)) & 1u);
-            const unsigned vote = __ballot_sync(kFullMask, take);
-            if (vote) {
-                int base = 0;
-                if (lane == 0) base = atomicAdd(&sm.n_gather, __popc(vote));
-                base = __shfl_sync(kFullMask, base, 0);
-                const int pos = base + __popc(vote & lanemask_lt());
-                if (take && pos < kGather) {
-                    sm.LC[pos] = composite(kk, k * B + r);
-                    sm.LF[pos] = (unsigned long long)fixed_of_key(kk);
-                }
-            }
-            if (++k == G) {
-                k = 0;
-                ++r;
+    for (int u = 0; u < IPT; ++u) {
+        const uint32_t kk = key[u];
+        const uint32_t bin = kk >> kHistShift;
+        const bool take = kk != kDroppedKey && ((sm.binmask[bin >> 5] >> (bin & 31)) & 1u);
+        const unsigned vote = __ballot_sync(kFullMask, take);
+        if (vote) {
+            int base = 0;
+            if (lane == 0) base = atomicAdd(&sm.n_gather, __popc(vote));
+            base = __shfl_sync(kFullMask, base, 0);
+            const int pos = base + __popc(vote & lanemask_lt());
+            if (take && pos < kGather) {
+                sm.LC[pos] = composite(kk, k * B + r);
+                sm.LF[pos] = (unsigned long long)fixed_of_key(kk);
             }
         }
+        if (++k == G) {
+            k = 0;
+            ++r;
+        }
     }
+}
+
+// The m <= kGather gathered candidates in composite order: SC / SF (rank of
+// each by counting; composites are unique).
+__device__ __forceinline__ void rank_gathered(SelSmem &sm, int m, int32_t *status) {
+    for (int i = threadIdx.x; i < m; i += kSelThreads) {
+        const unsigned long long ci = sm.LC[i];
+        int pos = 0;
+        for (int y = 0; y < m; ++y) pos += sm.LC[y] < ci ? 1 : 0;
+        if (!in_bounds(pos, m, status)) continue;
+        sm.SC[pos] = ci;
+        sm.SF[pos] = sm.LF[i];
+    }
+}
+
+// (2) of select_kernel for the nc slots set up by slot_setup: gather the
+// candidates of the marked bins; C*_j and P_j of every active slot go to
+// sm.cthr and sm.P.  Ends with a barrier.
+template <int IPT>
+__device__ __forceinline__ void slot_thresholds(const PlanArgs &a, SelSmem &sm,
+                                                const uint32_t (&key)[IPT], int r0, int k0,
+                                                int nc) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    gather_marked<IPT>(a, sm, key, r0, k0);
     __syncthreads();
     const int m = sm.n_gather;
     if (m <= kGather) {
-        // rank of each gathered candidate among all gathered ones
-        for (int i = tid; i < m; i += kSelThreads) {
-            const unsigned long long ci = sm.LC[i];
-            int pos = 0;
-            for (int y = 0; y < m; ++y) pos += sm.LC[y] < ci ? 1 : 0;
-            if (!in_bounds(pos, m, a.status)) continue;
-            sm.SC[pos] = ci;
-            sm.SF[pos] = sm.LF[i];
-        }
+        rank_gathered(sm, m, a.status);
         __syncthreads();
         // warp j: its bin starts after the gathered candidates of the marked
         // bins below it; C*_j is the rem_j-th of its bin
@@ -1817,14 +1813,21 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
         radix_thresholds<IPT>(a, sm, key, r0, k0, nc);
     }
     __syncthreads();
+}
 
-    // (3) theta at every candidate (all in warp 0) and the budget
-    if (warp == 0) select_theta(a, sm, b_top, forced);
-    __syncthreads();
-
-    // (4) ScheduleVerifyLensTopk: request r selects its candidates with
-    // C <= C*, a prefix of its depths; the thread holding the first depth
-    // past that prefix (or the last depth) writes 1 + its length, clamped
+// (4)-(5) of select_kernel and dense_select_kernel, once sm.cstar and
+// sm.budget_s are set.  ScheduleVerifyLensTopk: request r selects its
+// candidates with C <= C*, a prefix of its depths; the thread holding the
+// first depth past that prefix (or the last depth) writes 1 + its length,
+// clamped.  Then the tier-filled budget for a next pass and the fused pack.
+template <int IPT>
+__device__ __forceinline__ void select_finish(const PlanArgs &a, SelSmem &sm,
+                                              const uint32_t (&key)[IPT], long long b_top,
+                                              bool staged) {
+    const int tid = threadIdx.x;
+    const int B = a.B, G = a.gamma, N = a.N;
+    const int i0 = tid * IPT;
+    const int r0 = i0 / G, k0 = i0 - r0 * G;
     const unsigned long long cstar = sm.cstar;
     {
         int r = r0, k = k0;
@@ -1870,15 +1873,611 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
     }
 }
 
-size_t select_smem_bytes() { return sizeof(SelSmem); }
+template <int IPT>
+__global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    SelSmem &sm = *reinterpret_cast<SelSmem *>(smem_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = a.B, G = a.gamma, N = a.N;
+    const CostArgs &c = a.cost;
+    const int nc = c.n + 1;
+    const int i0 = tid * IPT;
+    const int r0 = i0 / G, k0 = i0 - r0 * G;  // request and depth of this thread's first candidate
+
+    pdl_trigger();
+    // while the survivals are computed: warp j fetches cost entry j (for its
+    // budget range); warp 0 fetches entry `lane` and prepares its theta
+    // divisor, so that only the product or quotient is left for later
+    int Mj = 0, Mprev = 0, Mnext = 0;
+    if (warp < c.n) {
+        Mj = __ldg(c.M + warp);
+        Mprev = warp > 0 ? __ldg(c.M + warp - 1) : 0;
+        Mnext = warp < c.n - 1 ? __ldg(c.M + warp + 1) : 0;
+    }
+    const int Mlast = __ldg(c.M + c.n - 1);
+    if (warp == 0) {
+        bool bad_entry = false;
+        if (lane < c.n) {
+            const int m = __ldg(c.M + lane);
+            const double v = __ldg(c.val + lane);
+            bad_entry = lane > 0 && !(m > __ldg(c.M + lane - 1));
+            double Tm = 0.0;
+            bool ok;
+            if (c.kind == DSPARK_COST_SPS_1D) {
+                ok = v > 0.0 && isfinite(v);
+            } else {
+                Tm = __dadd_rn(__dadd_rn(c.bias, c.alpha), v);
+                ok = Tm > 0.0 && isfinite(Tm);
+            }
+            sm.val_s[lane] = v;
+            sm.div_s[lane] = Tm;
+            sm.ok_s[lane] = ok ? 1 : 0;
+            sm.M_s[lane] = m;
+        }
+        const bool bt = __any_sync(kFullMask, bad_entry);
+        if (lane == 0) sm.bad_table = bt ? 1 : 0;
+    }
+    if (tid < kHistBins / 32) sm.binmask[tid] = 0u;
+    if (tid == 0) sm.n_gather = 0;
+    // the fused pack's step inputs are not written by the planner: stage
+    // them now, while the survivals are computed
+    const bool staged = a.pk.on && (long long)B * (G + 2) <= kStage;
+    if (staged) {
+        for (int i = tid; i < B; i += kSelThreads) {
+            sm.stage[i] = __ldg(a.pk.anchor + i);
+            sm.stage[B + i] = __ldg(a.pk.prefix + i);
+        }
+        for (int i = tid; i < N; i += kSelThreads)
+            if (in_bounds(2 * B + i, kStage, a.status)) sm.stage[2 * B + i] = __ldg(a.pk.draft + i);
+    }
+    pdl_wait();  // survivals and bins come from survival_kernel
+    const int forced = resolve_forced(a);
+
+    // (1) bins, keys, scan
+    uint32_t key[IPT];
+    const int n_kept = select_bins<IPT>(a, sm, key);
+    long long b_top = n_kept;  // largest in-range budget
+    if (c.kind == DSPARK_COST_ADDITIVE) b_top = min(b_top, (long long)Mlast - (long long)B);
+
+    // warp j: candidate budget b_j, the top bin holding its threshold and
+    // its rank inside the bin
+    if (warp < nc) {
+        int b;
+        if (warp < c.n) b = entry_last_budget(c, warp, Mj, Mprev, Mnext, B, b_top);
+        else b = (forced >= 0 && b_top >= 0) ? (int)min((long long)forced, b_top) : -1;
+        slot_setup(sm, warp, lane, b, a.status);
+    }
+    __syncthreads();
+
+    // (2) thresholds of the candidate budgets
+    slot_thresholds<IPT>(a, sm, key, r0, k0, nc);
+
+    // (3) theta at every candidate (all in warp 0) and the budget
+    if (warp == 0) select_theta(a, sm, b_top, forced);
+    __syncthreads();
+
+    // (4)-(5) lengths, tier-filled budget, pack
+    select_finish<IPT>(a, sm, key, b_top, staged);
+}
+
+// ------------------------------------------------------------ dense select
+//
+// Dense cost tables (more than kMaxSelect entries, at most kDenseMaxEntries,
+// not interpolated; the 1-D SPS table with an entry per M) on one CTA,
+// without ranking every candidate.  The bins of select_kernel give P exactly
+// at every bin edge, and bound it inside a bin:
+//   (1) as in select_kernel: bins, keys, their scan;
+//   (2) entry j's last budget b_j falls in the bin d holding the b_j-th
+//       kept key; each of the r = b_j - cum[d-1] keys of that bin up to it
+//       survives between the bin's smallest and largest survival (and the
+//       bin's other keys between the same), so tau(b_j) lies in an interval
+//       and theta_j between fp32 bounds computed with directed rounding
+//       (which bound the fp64 definition as well).  The largest lower bound
+//       is a floor of the maximum;
+//       an entry whose upper bound is below the floor cannot be the first
+//       maximiser;
+//   (3) the entries left (in the workloads, a handful) and the forced
+//       budget mark their bins.  When those bins hold at most kGather keys,
+//       they are gathered, ordered by composite and prefix-summed: the exact
+//       P and C* of every entry left follow, and theta in fp64 as in the
+//       other paths; the first maximiser wins;
+//   (4) otherwise (bins crowded by near-equal survivals) the entries left
+//       take select_kernel's threshold slots, 32 at a time (radix passes
+//       inside crowded bins);
+//   (5) lengths, tier-filled budget and pack as in select_kernel.
+// The table is staged in shared memory before the dependency wait (each
+// entry's range of budgets and its value as a float), in the region the
+// select path stages the pack's inputs in; the fused pack reads its inputs
+// from global memory instead.
+
+// entries of the stage: range int2 + value float + candidate list int
+constexpr int kDenseMaxEntries = (kStage * 4 - 16) / 16;
+constexpr int kDensePer = (kDenseMaxEntries + kSelThreads - 1) / kSelThreads;  // entries a thread
+
+struct DenseStage {
+    int2 *range;  // entry j's budgets [x, y] whose M = B + b looks it up (before the clip to
+                  // b_top); after step (2): its last budget and that budget's bin
+    float *f32;   // its value rounded down to a float; after step (2): theta's upper bound
+    int *list;    // entries left after the bounds (step 3)
+};
+
+__device__ __forceinline__ DenseStage dense_stage(SelSmem &sm, int n) {
+    unsigned char *p = reinterpret_cast<unsigned char *>(sm.stage);
+    return DenseStage{reinterpret_cast<int2 *>(p), reinterpret_cast<float *>(p + (size_t)8 * n),
+                      reinterpret_cast<int *>(p + (size_t)12 * n)};
+}
+
+// the largest kept key: survivals are at least 2^-14
+constexpr uint32_t kMaxKeptKey = kOneBits - ((uint32_t)kMinExpBiased << 23);
+
+// B + P 2^-37 rounded down and up to floats, by integer operations
+// (tau_float truncates; one ulp more when bits were dropped)
+__device__ __forceinline__ void tau_float_rd_ru(int B, long long P, float &lo, float &hi) {
+    const unsigned long long x = ((unsigned long long)B << 37) + (unsigned long long)P;
+    const int msb = 63 - __clzll((long long)x);  // >= 37
+    const unsigned bits = ((unsigned)(msb - 37 + 127) << 23) | (unsigned)((x >> (msb - 23)) & 0x7fffffull);
+    lo = __uint_as_float(bits);
+    hi = __uint_as_float(bits + ((x & ((1ull << (msb - 23)) - 1ull)) ? 1u : 0u));
+}
+
+// The first maximiser over a warp: the largest key (-1: none), ties to the
+// smaller budget; every lane receives it with the winner's P and C.  32-bit
+// warp reductions (a loop of 64-bit shuffles and compares took ~8000 cycles
+// here).
+__device__ __forceinline__ void warp_first_max(long long &key, int &b, unsigned long long &P,
+                                               unsigned long long &C) {
+    const unsigned long long uk = key >= 0 ? (unsigned long long)key + 1ull : 0ull;
+    const unsigned hi = (unsigned)(uk >> 32), lo = (unsigned)uk;
+    const unsigned mhi = __reduce_max_sync(kFullMask, hi);
+    const unsigned mlo = __reduce_max_sync(kFullMask, hi == mhi ? lo : 0u);
+    const bool top = hi == mhi && lo == mlo;
+    const unsigned bmin = __reduce_min_sync(kFullMask, top ? (unsigned)b : 0x7FFFFFFFu);
+    const unsigned win = __ballot_sync(kFullMask, top && (unsigned)b == bmin);
+    const int src = __ffs(win) - 1;
+    P = __shfl_sync(kFullMask, P, src);
+    C = __shfl_sync(kFullMask, C, src);
+    key = (long long)((((unsigned long long)mhi << 32) | mlo) - 1ull);
+    b = (int)bmin;
+}
 
 template <int IPT>
-cudaError_t launch_select(const PlanArgs &a, cudaStream_t s) {
-    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(select_kernel<IPT>),
-                                (int)select_smem_bytes(),
-                                IPT == 1 ? 1 : IPT == 2 ? 2 : IPT == 4 ? 3 : IPT == 8 ? 4 : 5);
+__global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    SelSmem &sm = *reinterpret_cast<SelSmem *>(smem_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = a.B, G = a.gamma;
+    const CostArgs &c = a.cost;
+    const int n = c.n;
+    const int i0 = tid * IPT;
+    const int r0 = i0 / G, k0 = i0 - r0 * G;
+    const DenseStage ds = dense_stage(sm, n);
+
+    // each thread a contiguous run of entries (their budgets and bins do
+    // not decrease along it)
+    const int per = (n + kSelThreads - 1) / kSelThreads;  // <= kDensePer
+    const int j0 = min(tid * per, n), j1 = min(j0 + per, n);
+
+    pdl_trigger();
+    // while the survivals are computed: every entry's range of budgets (the
+    // 64-bit arithmetic of entry_last_budget, before the clip) and its value
+    // as a float; the run's loads are all issued first
+    bool order_bad = false;
+    {
+        long long Mv[kDensePer + 2];  // M_{j0-1} .. M_{j0+kDensePer}
+        double vv[kDensePer];
+#pragma unroll
+        for (int u = 0; u < kDensePer + 2; ++u) {
+            const int j = j0 - 1 + u;
+            Mv[u] = (u <= j1 - j0 + 1 && j >= 0 && j < n) ? __ldg(c.M + j) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kDensePer; ++u) vv[u] = j0 + u < j1 ? __ldg(c.val + j0 + u) : 0.0;
+#pragma unroll
+        for (int u = 0; u < kDensePer; ++u) {
+            const int j = j0 + u;
+            if (j < j1 && in_bounds(j, kDenseMaxEntries, a.status)) {
+                ds.range[j] = entry_range_from(c.kind, n, j, Mv[u], Mv[u + 1], Mv[u + 2], B,
+                                               order_bad);
+                ds.f32[j] = __double2float_rd(vv[u]);
+            }
+        }
+    }
+    const int Mlast = __ldg(c.M + n - 1);
+    if (tid < kHistBins / 32) sm.binmask[tid] = 0u;
+    if (tid == 0) {
+        sm.n_gather = 0;
+        sm.d_floor = 0u;
+        sm.d_ncand = 0;
+        sm.d_marked = 0;
+        sm.d_fixed = __dadd_rn(c.bias, c.alpha);
+        sm.d_fixed_lo = __double2float_rd(sm.d_fixed);
+        sm.d_fixed_hi = __double2float_ru(sm.d_fixed);
+        sm.d_fP = 0ull;
+        sm.d_fC = kNoComposite;
+    }
+    pdl_wait();  // survivals and bins come from survival_kernel
+    const int forced = resolve_forced(a);
+
+    // (1) bins, keys, scan (its barriers publish the prologue's stores)
+    uint32_t key[IPT];
+    const int n_kept = select_bins<IPT>(a, sm, key);
+    const bool bad_table = __syncthreads_or(order_bad) != 0;
+    long long b_top = n_kept;  // largest in-range budget
+    if (c.kind == DSPARK_COST_ADDITIVE) b_top = min(b_top, (long long)Mlast - (long long)B);
+    const int b_top32 = (int)max(min(b_top, (long long)INT_MAX), -1LL);
+    const double fixed_cost = sm.d_fixed;
+    const float fixed_lo = sm.d_fixed_lo, fixed_hi = sm.d_fixed_hi;
+    const bool has_forced = forced >= 0 && b_top >= 0 && !bad_table;
+    const int b_forced = has_forced ? (int)min((long long)forced, b_top) : -1;
+
+    // entry j's last budget b (false: its range holds none)
+    auto entry_b = [&](int j, int &b) -> bool {
+        const int2 r = ds.range[j];
+        b = min(r.y, b_top32);
+        return b >= r.x;
+    };
+    // the bin of budget b >= 1: the first whose inclusive count reaches b
+    // (cum[kHistBins-1] = n_kept >= b)
+    auto bin_search = [&](int b) -> int {
+        int lo = 0, hi = kHistBins - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (sm.cum[mid] >= (unsigned)b) hi = mid;
+            else lo = mid + 1;
+        }
+        return lo;
+    };
+    // the same from a bin d known to be at or below it
+    auto bin_from = [&](int b, int d) -> int {
+        while (d < kHistBins - 1 && sm.cum[d] < (unsigned)b) ++d;
+        return d;
+    };
+    // the fp64 definition of entry j's cost is a positive finite number
+    auto cost_ok = [&](int j) -> bool {
+        const double vj = __ldg(c.val + j);
+        if (c.kind == DSPARK_COST_SPS_1D) return vj > 0.0 && isfinite(vj);
+        const double Tm = __dadd_rn(fixed_cost, vj);
+        return Tm > 0.0 && isfinite(Tm);
+    };
+    auto mark_bin = [&](int d) {
+        if (!in_bounds(d, kHistBins, a.status)) return;
+        const unsigned bit = 1u << (d & 31);
+        if (!(atomicOr(&sm.binmask[d >> 5], bit) & bit))
+            atomicAdd(&sm.d_marked, (int)(sm.cum[d] - (d > 0 ? sm.cum[d - 1] : 0u)));
+    };
+
+    // theta's bounds in fp32 with directed rounding hold for the fp64
+    // definition too (rd32(x) <= rn64(x) <= ru32(x) for every real x).
+    // tau(b) = B + P 2^-37 lies in [B + c0 + r s_lo, B + c0 + r s_hi] and in
+    // [B + c1 - (cnt - r) s_hi, B + c1 - (cnt - r) s_lo], with c0 and c1 the
+    // fixed-point sums before and after b's bin d, cnt the bin's keys, s_lo
+    // and s_hi its smallest and largest survival (exact floats) and
+    // r = b - cum[d-1].
+    int cd = -1, c_before = 0, c_cnt = 0;  // the bin whose constants are held
+    float s_lo = 0.0f, s_hi = 0.0f, b0_lo = 0.0f, b0_hi = 0.0f, b1_lo = 0.0f, b1_hi = 0.0f;
+    auto tau_bounds = [&](int b, int d, float &t_lo, float &t_hi) {
+        t_lo = t_hi = (float)B;  // b = 0: tau = B exactly
+        if (b < 1 || !in_bounds(d + 1, kHistBins, a.status)) return;
+        if (d != cd) {
+            cd = d;
+            c_before = d > 0 ? (int)sm.cum[d - 1] : 0;
+            c_cnt = (int)sm.cum[d] - c_before;
+            const uint32_t last = (((uint32_t)d + 1) << kHistShift) - 1;
+            s_hi = __uint_as_float(kOneBits - ((uint32_t)d << kHistShift));
+            s_lo = __uint_as_float(kOneBits - (last < kMaxKeptKey ? last : kMaxKeptKey));
+            tau_float_rd_ru(B, (long long)sm.csum[d], b0_lo, b0_hi);
+            tau_float_rd_ru(B, (long long)sm.csum[d + 1], b1_lo, b1_hi);
+        }
+        const float r = (float)(b - c_before), rest = (float)(c_cnt - (b - c_before));
+        t_lo = fmaxf(__fmaf_rd(r, s_lo, b0_lo), __fmaf_rd(-rest, s_hi, b1_lo));
+        t_hi = fminf(__fmaf_ru(r, s_hi, b0_hi), __fmaf_ru(-rest, s_lo, b1_hi));
+    };
+    // the staged value v rounded down and an upper bound one float ulp up;
+    // the cost's bounds (SPS: v; additive: bias + alpha + v); false when
+    // fp32 cannot bound theta (the fp64 cost is then checked)
+    auto cost_bounds = [&](int j, float &k_lo, float &k_hi) -> bool {
+        const float v_lo = ds.f32[j];
+        const float v_hi = v_lo == 0.0f ? __int_as_float(1) : __fmaf_ru(fabsf(v_lo), 0x1p-23f, v_lo);
+        if (c.kind == DSPARK_COST_SPS_1D) {
+            k_lo = v_lo;
+            k_hi = v_hi;
+            return v_lo > 0.0f && v_hi < INFINITY;  // SPS must be positive: 0 is flagged
+        }
+        k_lo = __fadd_rd(fixed_lo, v_lo);
+        k_hi = __fadd_ru(fixed_hi, v_hi);
+        return k_lo > 0.0f && k_hi < INFINITY;
+    };
+    // theta's bounds from tau's and the cost's
+    auto theta_lo = [&](float t_lo, float k_lo, float k_hi) -> float {
+        return c.kind == DSPARK_COST_SPS_1D ? __fmul_rd(t_lo, k_lo) : __fdiv_rd(t_lo, k_hi);
+    };
+    auto theta_hi = [&](float t_hi, float k_lo, float k_hi) -> float {
+        return c.kind == DSPARK_COST_SPS_1D ? __fmul_ru(t_hi, k_hi) : __fdiv_ru(t_hi, k_lo);
+    };
+
+    // (2) per run: the last entry with a budget (the run's largest tau) is
+    // bounded and its lower bound feeds the floor; the whole run is bounded
+    // above by that tau with the run's largest SPS (smallest cost)
+    int jl = -1;            // the run's last entry with a budget
+    float run_hi = 0.0f;    // upper bound of theta over the run (NaN: none)
+    if (!bad_table) {
+        int bl = 0;
+        bool all_bounded = true;
+        float kmax_hi = 0.0f, kmin_lo = INFINITY;
+        for (int j = j0; j < j1; ++j) {
+            int b;
+            if (!entry_b(j, b)) continue;
+            jl = j;
+            bl = b;
+            float k_lo, k_hi;
+            all_bounded = cost_bounds(j, k_lo, k_hi) && all_bounded;
+            kmax_hi = fmaxf(kmax_hi, k_hi);
+            kmin_lo = fminf(kmin_lo, k_lo);
+        }
+        float my_floor = 0.0f;
+        if (jl >= 0) {
+            float t_lo, t_hi, k_lo, k_hi;
+            tau_bounds(bl, bl >= 1 ? bin_search(bl) : 0, t_lo, t_hi);
+            if (cost_bounds(jl, k_lo, k_hi)) my_floor = theta_lo(t_lo, k_lo, k_hi);
+            run_hi = all_bounded ? theta_hi(t_hi, kmin_lo, kmax_hi) : __int_as_float(0x7fffffff);
+        }
+        // non-negative floats order like their bits: one atomic per warp
+        const unsigned wfloor = __reduce_max_sync(kFullMask, __float_as_uint(my_floor));
+        if (lane == 0) atomicMax(&sm.d_floor, wfloor);
+    }
+    __syncthreads();
+    const float floor_all = __uint_as_float(sm.d_floor);
+
+    // (3) in the runs that can hold the maximum: every entry bounded; those
+    // whose upper bound reaches the floor (or that fp32 cannot bound) are
+    // left, with their budget and bin written over their stage range
+    bool my_bad_cost = false;
+    if (jl >= 0 && !(run_hi < floor_all)) {
+        unsigned left = 0u;  // bit u: entry j0 + u is left
+        int d = -1, d_last = -1;
+        for (int j = j0; j < j1; ++j) {
+            int b;
+            if (!entry_b(j, b)) continue;
+            if (b >= 1) d = d < 0 ? bin_search(b) : bin_from(b, d);
+            float t_lo, t_hi, k_lo, k_hi;
+            const bool bounded = cost_bounds(j, k_lo, k_hi);
+            if (bounded) {
+                tau_bounds(b, d, t_lo, t_hi);
+                if (theta_hi(t_hi, k_lo, k_hi) < floor_all) continue;
+            } else if (!cost_ok(j)) {  // flagged; never a maximiser
+                my_bad_cost = true;
+                continue;
+            }
+            ds.range[j] = make_int2(b, b >= 1 ? d : 0);
+            left |= 1u << (j - j0);
+            if (b >= 1 && d != d_last) {  // budgets do not decrease: each bin once
+                mark_bin(d);
+                d_last = d;
+            }
+        }
+        if (left) {  // list slots for the run, in one reservation
+            int slot = atomicAdd(&sm.d_ncand, __popc(left));
+            for (unsigned m = left; m; m &= m - 1, ++slot)
+                if (in_bounds(slot, n, a.status)) ds.list[slot] = j0 + __ffs(m) - 1;
+        }
+    }
+    if (tid == 0 && b_forced >= 1) mark_bin(bin_search(b_forced));
+    __syncthreads();
+    const int K = min(sm.d_ncand, n);
+
+    long long my_key = -1;
+    int my_b = 0x7FFFFFFF;
+    unsigned long long my_P = 0ull, my_C = kNoComposite;
+    // exact theta of entry j (value vj) at budget b with P, C*: the first
+    // maximiser
+    auto evaluate = [&](int j, double vj, int b, unsigned long long P, unsigned long long C) {
+        const double tau = tau_of(B, (long long)P);
+        double theta;
+        if (c.kind == DSPARK_COST_SPS_1D) {
+            if (!(vj > 0.0) || !isfinite(vj)) {
+                my_bad_cost = true;
+                return;
+            }
+            theta = __dmul_rn(tau, vj);
+        } else {
+            const double Tm = __dadd_rn(fixed_cost, vj);
+            if (!(Tm > 0.0) || !isfinite(Tm)) {
+                my_bad_cost = true;
+                return;
+            }
+            theta = __ddiv_rn(tau, Tm);
+        }
+        const long long kk = __double_as_longlong(theta);  // positive: orders like the values
+        if (cand_better(kk, b, my_key, my_b)) {
+            my_key = kk;
+            my_b = b;
+            my_P = P;
+            my_C = C;
+        }
+    };
+
+    if (sm.d_marked <= kGather) {
+        // (3) the marked bins' candidates in composite order, prefix-summed
+        gather_marked<IPT>(a, sm, key, r0, k0);
+        __syncthreads();
+        const int m = min(sm.n_gather, kGather);
+        rank_gathered(sm, m, a.status);
+        __syncthreads();
+        {
+            const unsigned long long v = tid < m ? sm.SF[tid] : 0ull;
+            unsigned long long tot;
+            const unsigned long long ex = block_exclusive_scan<unsigned long long>(v, sm.scan64, &tot);
+            if (tid < m) sm.LF[tid] = ex + v;  // inclusive sums, in composite order
+        }
+        __syncthreads();
+        // P and C* at budget b >= 1: the bin's keys start where the
+        // composites reach the bin (its number is the composite's top bits)
+        auto exact_at = [&](int b, int d, unsigned long long &P, unsigned long long &C) -> bool {
+            const int r = b - (d > 0 ? (int)sm.cum[d - 1] : 0);
+            const unsigned long long first = (unsigned long long)d << (kHistShift + 14);
+            int lo = 0, hi = m;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (sm.SC[mid] < first) lo = mid + 1;
+                else hi = mid;
+            }
+            const int idx = lo + r - 1;
+            if (!in_bounds(idx, m, a.status) || !in_bounds(lo, m, a.status)) return false;
+            P = sm.csum[d] + sm.LF[idx] - (lo > 0 ? sm.LF[lo - 1] : 0ull);
+            C = sm.SC[idx];
+            return true;
+        };
+        for (int i = tid; i < K; i += kSelThreads) {
+            const int j = ds.list[i];
+            const double vj = __ldg(c.val + j);  // in flight with the search below
+            const int2 bd = ds.range[j];
+            unsigned long long P = 0ull, C = kNoComposite;
+            if (bd.x >= 1 && !exact_at(bd.x, bd.y, P, C)) continue;
+            evaluate(j, vj, bd.x, P, C);
+        }
+        if (tid == 0 && b_forced >= 1) {
+            unsigned long long P, C;
+            if (exact_at(b_forced, bin_search(b_forced), P, C)) {
+                sm.d_fP = P;
+                sm.d_fC = C;
+            }
+        }
+    } else {
+        // (4) crowded bins: the entries left (then the forced budget) take
+        // the threshold slots 32 at a time
+        const int T = K + (b_forced >= 1 ? 1 : 0);
+        for (int base = 0; base < T; base += 32) {  // uniform
+            const int nc = min(32, T - base);
+            if (tid < kHistBins / 32) sm.binmask[tid] = 0u;
+            if (tid == 0) sm.n_gather = 0;
+            __syncthreads();
+            if (warp < nc) {
+                const int item = base + warp;
+                int b = b_forced, j = -1;
+                if (item < K) {
+                    j = ds.list[item];
+                    b = ds.range[j].x;
+                }
+                slot_setup(sm, warp, lane, b, a.status);
+                if (lane == 0) sm.d_item[warp] = j;
+            }
+            __syncthreads();
+            slot_thresholds<IPT>(a, sm, key, r0, k0, nc);
+            if (warp == 0 && lane < nc) {
+                const int b = sm.cand_b[lane], j = sm.d_item[lane];
+                const unsigned long long P = b >= 1 ? sm.P[lane] : 0ull;
+                const unsigned long long C = b >= 1 ? sm.cthr[lane] : kNoComposite;
+                if (j >= 0) {
+                    evaluate(j, __ldg(c.val + j), b, P, C);
+                } else {
+                    sm.d_fP = P;
+                    sm.d_fC = C;
+                }
+            }
+            __syncthreads();
+        }
+    }
+
+    // the first maximiser over the block
+    warp_first_max(my_key, my_b, my_P, my_C);
+    if (lane == 0) {
+        sm.d_bkey[warp] = my_key;
+        sm.d_bb[warp] = my_b;
+        sm.d_bP[warp] = my_P;
+        sm.d_bC[warp] = my_C;
+    }
+    const bool any_bad_cost = __syncthreads_or(my_bad_cost) != 0;
+    if (warp == 0) {
+        long long bk = sm.d_bkey[lane];
+        int bb = sm.d_bb[lane];
+        unsigned long long bP = sm.d_bP[lane], bC = sm.d_bC[lane];
+        warp_first_max(bk, bb, bP, bC);
+        if (lane == 0) {
+            int st = (any_bad_cost || bad_table) ? DSPARK_STATUS_BAD_COST : 0;
+            int budget = 0;
+            unsigned long long Pbud = 0ull, cstar = kNoComposite;
+            double theta_out = 0.0;
+            if (forced < 0) {
+                if (bad_table || bb == 0x7FFFFFFF) {
+                    st |= DSPARK_STATUS_INFEASIBLE;
+                } else {
+                    budget = bb;
+                    theta_out = __longlong_as_double(bk);
+                    if (budget > 0) {
+                        Pbud = bP;
+                        cstar = bC;
+                    }
+                }
+            } else if (!has_forced) {
+                st |= DSPARK_STATUS_INFEASIBLE;
+            } else {
+                budget = b_forced;
+                if (budget > 0) {
+                    Pbud = sm.d_fP;
+                    cstar = sm.d_fC;
+                }
+                // theta at the forced budget: the entry covering M = B + budget
+                const long long Mv = (long long)B + budget;
+                int lo = 0, hi = n;  // first index with M > Mv (1-D) / M >= Mv (additive)
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    const long long Mm = __ldg(c.M + mid);
+                    const bool right = (c.kind == DSPARK_COST_SPS_1D) ? (Mm > Mv) : (Mm >= Mv);
+                    if (right) hi = mid;
+                    else lo = mid + 1;
+                }
+                const double tau = tau_of(B, (long long)Pbud);
+                if (c.kind == DSPARK_COST_SPS_1D) {
+                    const double sps = __ldg(c.val + (lo > 0 ? lo - 1 : 0));
+                    if (sps > 0.0 && isfinite(sps)) theta_out = __dmul_rn(tau, sps);
+                } else if (lo < n) {
+                    const double Tm = __dadd_rn(fixed_cost, __ldg(c.val + lo));
+                    if (Tm > 0.0 && isfinite(Tm)) theta_out = __ddiv_rn(tau, Tm);
+                }
+            }
+            if (st) flag(a.status, st);
+            sm.cstar = cstar;
+            sm.budget_s = budget;
+            a.budget[0] = budget;
+            a.tau_theta[0] = tau_of(B, (long long)Pbud);
+            a.tau_theta[1] = theta_out;
+        }
+    }
+    __syncthreads();
+
+    // (5) lengths, tier-filled budget, pack (its inputs from global memory)
+    select_finish<IPT>(a, sm, key, b_top, false);
+}
+
+// The select kernels launch with the largest dynamic shared memory a CTA
+// may have, more than SelSmem needs, so that their one CTA has an SM to
+// itself: with 56 registers a thread, 1024 threads leave room for one CTA of
+// the argmax kernel, and a step whose planner shared its SM with the
+// previous step's argmax took 102 us instead of 90 in the chained bench
+// loop (dsv4_like).
+constexpr size_t kSelLaunchSmem = 227 * 1024;
+static_assert(sizeof(SelSmem) <= kSelLaunchSmem, "SelSmem fits the launch");
+size_t select_smem_bytes() { return kSelLaunchSmem; }
+
+
+template <int IPT>
+cudaError_t launch_select(const PlanArgs &a, bool dense, cudaStream_t s) {
+    const int slot = (IPT == 1 ? 1 : IPT == 2 ? 2 : IPT == 4 ? 3 : IPT == 8 ? 4 : 5) + (dense ? 9 : 0);
+    void (*kernel)(PlanArgs) = dense ? dense_select_kernel<IPT> : select_kernel<IPT>;
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(kernel), (int)select_smem_bytes(), slot);
     if (e != cudaSuccess) return e;
-    return launch_pdl(select_kernel<IPT>, dim3(1), dim3(kSelThreads), select_smem_bytes(), s, a);
+    return launch_pdl(kernel, dim3(1), dim3(kSelThreads), select_smem_bytes(), s, a);
+}
+
+// Which planner kernel takes a cost table: select_kernel for at most
+// kMaxSelect entries, dense_select_kernel for more (at most
+// kDenseMaxEntries), rank_kernel for larger and interpolated tables.
+enum class PlanPath { kSelect, kDense, kRank };
+
+PlanPath plan_path(const dspark_cost_table *cost) {
+    if (cost->kind == DSPARK_COST_ADDITIVE_INTERP) return PlanPath::kRank;
+    if (cost->n <= kMaxSelect) return PlanPath::kSelect;
+    return cost->n <= kDenseMaxEntries ? PlanPath::kDense : PlanPath::kRank;
 }
 
 }  // namespace dspark
@@ -1919,17 +2518,18 @@ int check_plan(const float *conf_logits, const float *sts_temps, const dspark_pl
     return DSPARK_OK;
 }
 
-// One planner pass over survivals already computed: select_kernel (tables
-// of <= kMaxSelect entries) or rank_kernel.
-int launch_pass(PlanArgs a, bool select, cudaStream_t s) {
-    if (select) {
+// One planner pass over survivals already computed, on the kernel plan_path
+// chose.
+int launch_pass(PlanArgs a, PlanPath path, cudaStream_t s) {
+    if (path != PlanPath::kRank) {
+        const bool dense = path == PlanPath::kDense;
         const int ipt = (a.N + kSelThreads - 1) / kSelThreads;
         cudaError_t e;
-        if (ipt <= 1) e = launch_select<1>(a, s);
-        else if (ipt <= 2) e = launch_select<2>(a, s);
-        else if (ipt <= 4) e = launch_select<4>(a, s);
-        else if (ipt <= 8) e = launch_select<8>(a, s);
-        else e = launch_select<16>(a, s);
+        if (ipt <= 1) e = launch_select<1>(a, dense, s);
+        else if (ipt <= 2) e = launch_select<2>(a, dense, s);
+        else if (ipt <= 4) e = launch_select<4>(a, dense, s);
+        else if (ipt <= 8) e = launch_select<8>(a, dense, s);
+        else e = launch_select<16>(a, dense, s);
         if (e == cudaSuccess) return DSPARK_OK;
         // the bins survival_kernel filled must not reach the next call
         cudaMemsetAsync(&a.scratch->hcount[0], 0,
@@ -1966,9 +2566,11 @@ int run_plan(const float *conf_logits, const float *sts_temps, const dspark_plan
     PassScratch *ps = scratch_at<PassScratch>(scratch, plan_pass_offset(B, N));
     int32_t *pass_lens = scratch_at<int32_t>(scratch, plan_pass_lens_offset(B, N));
     float *lagged_surv = scratch_at<float>(scratch, plan_pass_surv_offset(B, N));
-    // few candidate budgets: one-CTA select; an interpolated table makes every
-    // budget a candidate and takes the rank path
-    const bool select = cost->n <= kMaxSelect && cost->kind != DSPARK_COST_ADDITIVE_INTERP;
+    // one-CTA select (few candidate budgets, or a dense table bounded per
+    // entry); an interpolated table makes every budget a candidate and takes
+    // the rank path
+    const PlanPath path = plan_path(cost);
+    const bool select = path != PlanPath::kRank;  // the survival kernel bins the keys
     const int32_t *conf_gen = opt ? opt->conf_generation : nullptr;
     const int32_t *req_gen = opt ? opt->req_generation : nullptr;
     const bool lagged = opt && opt->lagged_conf_logits;
@@ -2006,7 +2608,7 @@ int run_plan(const float *conf_logits, const float *sts_temps, const dspark_plan
             return DSPARK_ERR_CUDA;
         a.surv = lagged_surv;
         a.budget = &ps->lagged_budget;
-        if ((rc = launch_pass(a, select, s)) != DSPARK_OK) return rc;
+        if ((rc = launch_pass(a, path, s)) != DSPARK_OK) return rc;
         a.budget = &ps->pass_budget;
         a.forced_dev = &ps->lagged_budget;
     }
@@ -2019,7 +2621,7 @@ int run_plan(const float *conf_logits, const float *sts_temps, const dspark_plan
         a.more_passes = true;
         a.align = align;
         a.exec_budget = &ps->exec_budget;
-        if ((rc = launch_pass(a, select, s)) != DSPARK_OK) return rc;
+        if ((rc = launch_pass(a, path, s)) != DSPARK_OK) return rc;
         a.more_passes = false;
         a.align.n = 0;
         a.exec_budget = nullptr;
@@ -2029,7 +2631,7 @@ int run_plan(const float *conf_logits, const float *sts_temps, const dspark_plan
     a.budget = budget;
     a.tau_theta = tau_theta;
     a.pk = pk;
-    if ((rc = launch_pass(a, select, s)) != DSPARK_OK) return rc;
+    if ((rc = launch_pass(a, path, s)) != DSPARK_OK) return rc;
     if (!select && pk.on &&
         launch_pack(true, pk.anchor, pk.draft, pk.prefix, verify_lens, B, G, pk.tiers, pk.capacity,
                     pk.ids, pk.pos, pk.req, pk.src, pk.cu, pk.totals, status, s) != cudaSuccess)

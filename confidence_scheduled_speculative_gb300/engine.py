@@ -216,7 +216,7 @@ class VerifyStep:
         inside) on the select path, else survival + rank + pack
         (separate calls add the pack kernel); then argmax + finalize."""
         c = self.cfg
-        select = api.planner_path(c.B * c.gamma, c.cost_kind, len(c.cost_M)) == "select"
+        select = api.planner_path(c.B * c.gamma, c.cost_kind, len(c.cost_M)) != "rank"
         return (3 if (separate_plan_pack or not select) else 2) + 2
 
     def greedy_accept(self, logits: torch.Tensor, write_argmax: bool = True, stream=None) -> None:

@@ -45,6 +45,11 @@ def test_select_path_limit_matches_kernel():
         m = re.search(r"constexpr int kMaxSelect = (\d+);", f.read())
     assert m is not None
     assert api.SELECT_MAX_ENTRIES == int(m.group(1))
+    with open(src) as f:
+        text = f.read()
+    stage = re.search(r"constexpr int kStage = (\d+);", text)
+    assert "constexpr int kDenseMaxEntries = (kStage * 4 - 16) / 16;" in text
+    assert api.DENSE_MAX_ENTRIES == (int(stage.group(1)) * 4 - 16) // 16
 
 
 def test_binding_planner_paths():
@@ -53,5 +58,8 @@ def test_binding_planner_paths():
     from confidence_scheduled_speculative_gb300 import api
     assert api.planner_path(4096, api.COST_ADDITIVE, 5) == "select"
     assert api.planner_path(4096, api.COST_SPS_1D, 31) == "select"
-    assert api.planner_path(4096, api.COST_SPS_1D, 32) == "rank"
+    assert api.planner_path(4096, api.COST_SPS_1D, 32) == "dense"
+    assert api.planner_path(4096, api.COST_SPS_1D, 4097) == "dense"
+    assert api.planner_path(4096, api.COST_ADDITIVE, api.DENSE_MAX_ENTRIES) == "dense"
+    assert api.planner_path(16384, api.COST_SPS_1D, api.DENSE_MAX_ENTRIES + 1) == "rank"
     assert api.planner_path(64, api.COST_ADDITIVE_INTERP, 5) == "rank"

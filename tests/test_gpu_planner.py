@@ -190,10 +190,10 @@ def _dense_problem(rng, seed):
 
 @pytest.mark.parametrize("seed", range(60))
 def test_plan_random_dense_table(dev, orc, seed):
-    """Dense tables on the rank path: theta bounded in fp32 at every entry
-    and evaluated in fp64 where the bounds cannot exclude the maximum; the
-    budget, lens, tau and theta must equal the oracle's, which evaluates
-    every budget in fp64."""
+    """Dense tables (the single-CTA dense path up to 6143 entries, the rank
+    path beyond): theta bounded in fp32 at every entry and evaluated in fp64
+    where the bounds cannot exclude the maximum; the budget, lens, tau and
+    theta must equal the oracle's, which evaluates every budget in fp64."""
     rng = np.random.default_rng(47000 + seed)
     P = _dense_problem(rng, seed)
     g = _gpu_plan(dev, P)
@@ -202,6 +202,88 @@ def test_plan_random_dense_table(dev, orc, seed):
     exp = compare_plan(f"dense/{seed}", g, ref, P["B"], P["gamma"], P["min_len"],
                        _restage(orc, P))
     assert int(g["status"][0]) == exp.status
+
+
+def _crowded_problem(B, g, p, kind, flat, forced=-1, eps=1e-4):
+    """Every request with the same confidences: each depth's survival is
+    shared by the whole batch, so one histogram bin holds B equal keys.  With
+    B > 512 the bins of the entries left after the bounds hold more keys than
+    the dense path gathers at once, and it takes the threshold slots 32
+    entries at a time.  A flat table (theta proportional to tau) with
+    survivals near eps leaves many entries within the fp32 margin of the
+    maximum."""
+    z = np.full((B, g), np.log(p / (1 - p)), np.float32)
+    M = np.arange(B, B + B * g + 1, dtype=np.int32)
+    if kind == 0:
+        val = np.full(M.size, 500.0) if flat else 1.0 / (2e-3 + 3e-6 * M)
+    else:
+        val = 1e-9 * M if flat else 0.002 * M
+    return dict(B=B, gamma=g, z=z, T=np.ones(g, np.float32), eps=eps, min_len=1,
+                max_len=g + 1, kind=kind, M=M, val=val, forced=forced, bias=1.0, alpha=0.5)
+
+
+@pytest.mark.parametrize("case", [
+    dict(B=600, g=8, p=0.3, kind=0, flat=False),
+    dict(B=600, g=8, p=0.3, kind=0, flat=True),
+    dict(B=700, g=6, p=0.2, kind=1, flat=True),
+    dict(B=520, g=11, p=0.6, kind=1, flat=False),
+    dict(B=600, g=8, p=0.3, kind=0, flat=True, forced=1234),
+    dict(B=600, g=8, p=0.999, kind=0, flat=True, eps=2.0 ** -14),
+    dict(B=64, g=8, p=0.3, kind=0, flat=True),
+])
+def test_plan_dense_path_crowded_bins(dev, orc, case):
+    """Dense tables (more than 31 entries: the single-CTA dense path) over
+    crowded bins and flat tables, against the oracle's fp64 evaluation of
+    every budget."""
+    P = _crowded_problem(**case)
+    from confidence_scheduled_speculative_gb300 import api
+    assert api.planner_path(P["B"] * P["gamma"], P["kind"], P["M"].size) == "dense"
+    g = _gpu_plan(dev, P)
+    ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"], P["kind"],
+                   P["M"], P["val"], P["bias"], P["alpha"])
+    exp = compare_plan(f"crowded/{case}", g, ref, P["B"], P["gamma"], P["min_len"],
+                       _restage(orc, P))
+    assert int(g["status"][0]) == exp.status
+
+
+@pytest.mark.parametrize("kind,bad", [(0, 0.0), (0, -3.0), (0, float("nan")), (1, -1.8),
+                                      (1, float("inf"))])
+def test_plan_dense_path_flags_bad_values_far_from_the_maximum(dev, orc, kind, bad):
+    """An invalid cost at a small budget, where theta is far below the
+    maximum: the dense path must still flag it (DSPARK_STATUS_BAD_COST), as
+    the oracle does, and plan as the oracle does."""
+    rng = np.random.default_rng(5151)
+    B, g = 256, 16
+    z = rng.normal(1.5, 1.2, (B, g)).astype(np.float32)
+    M = np.arange(B, B + B * g + 1, dtype=np.int32)
+    val = 1.0 / (3e-3 + 3e-6 * M) if kind == 0 else 0.002 * M
+    val = val.astype(np.float64)
+    val[3] = bad
+    P = dict(B=B, gamma=g, z=z, T=np.ones(g, np.float32), eps=1e-4, min_len=1, max_len=g + 1,
+             kind=kind, M=M, val=val, forced=-1, bias=1.0, alpha=0.5)
+    gres = _gpu_plan(dev, P)
+    ref = orc.plan(z, P["T"], 1e-4, 1, g + 1, -1, kind, M, val, 1.0, 0.5)
+    exp = compare_plan(f"bad/{kind}/{bad}", gres, ref, B, g, 1, _restage(orc, P))
+    assert int(gres["status"][0]) == exp.status
+    assert exp.status & 32  # BAD_COST
+
+
+def test_plan_dense_and_rank_paths_meet(dev, orc):
+    """The largest table the dense path takes and one entry more (the rank
+    path) on the same batch, both against the oracle."""
+    from confidence_scheduled_speculative_gb300 import api
+    rng = np.random.default_rng(4242)
+    B, g = 400, 16
+    z = rng.normal(1.0, 1.5, (B, g)).astype(np.float32)
+    for n in (api.DENSE_MAX_ENTRIES, api.DENSE_MAX_ENTRIES + 1):
+        M = np.arange(1, n + 1, dtype=np.int32)
+        P = dict(B=B, gamma=g, z=z, T=np.ones(g, np.float32), eps=1e-4, min_len=1,
+                 max_len=g + 1, kind=1, M=M, val=0.0025 * M, forced=-1, bias=1.0, alpha=0.3)
+        assert api.planner_path(B * g, 1, n) == ("dense" if n == api.DENSE_MAX_ENTRIES else "rank")
+        gres = _gpu_plan(dev, P)
+        ref = orc.plan(P["z"], P["T"], P["eps"], 1, g + 1, -1, 1, M, P["val"], 1.0, 0.3)
+        exp = compare_plan(f"meet/{n}", gres, ref, B, g, 1, _restage(orc, P))
+        assert int(gres["status"][0]) == exp.status
 
 
 @pytest.mark.parametrize("name", ["dsv4_like", "stress", "qwen_like"])
