@@ -280,6 +280,26 @@ __device__ __forceinline__ bool cand_better(long long ka, int ba, long long kb, 
     return ka > kb || (ka == kb && ba < bb);
 }
 
+// The first maximiser over a warp: the largest key (-1: none), ties to the
+// smaller budget; every lane receives it with the winner's P and C.  32-bit
+// warp reductions (a loop of 64-bit shuffles and compares took ~8000 cycles
+// here).
+__device__ __forceinline__ void warp_first_max(long long &key, int &b, unsigned long long &P,
+                                               unsigned long long &C) {
+    const unsigned long long uk = key >= 0 ? (unsigned long long)key + 1ull : 0ull;
+    const unsigned hi = (unsigned)(uk >> 32), lo = (unsigned)uk;
+    const unsigned mhi = __reduce_max_sync(kFullMask, hi);
+    const unsigned mlo = __reduce_max_sync(kFullMask, hi == mhi ? lo : 0u);
+    const bool top = hi == mhi && lo == mlo;
+    const unsigned bmin = __reduce_min_sync(kFullMask, top ? (unsigned)b : 0x7FFFFFFFu);
+    const unsigned win = __ballot_sync(kFullMask, top && (unsigned)b == bmin);
+    const int src = __ffs(win) - 1;
+    P = __shfl_sync(kFullMask, P, src);
+    C = __shfl_sync(kFullMask, C, src);
+    key = (long long)((((unsigned long long)mhi << 32) | mlo) - 1ull);
+    b = (int)bmin;
+}
+
 // Number of keys < key in each of four runs of P2 keys (a power of two,
 // at most 32; runs padded past gamma with the largest key): log2(P2) + 1
 // branch-free probes per run, the four probe chains interleaved.  The
@@ -1046,16 +1066,10 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
             my_P = Pb;
         }
     }
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-        const long long ok = __shfl_down_sync(kFullMask, my_key, d);
-        const int ob = __shfl_down_sync(kFullMask, my_b, d);
-        const long long oP = __shfl_down_sync(kFullMask, my_P, d);
-        if (cand_better(ok, ob, my_key, my_b)) {
-            my_key = ok;
-            my_b = ob;
-            my_P = oP;
-        }
+    {
+        unsigned long long P = (unsigned long long)my_P, unused = 0ull;
+        warp_first_max(my_key, my_b, P, unused);
+        my_P = (long long)P;
     }
     if (lane == 0) {
         sm.best_key[warp] = my_key;
@@ -1068,16 +1082,10 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
         long long bk = lane < kRankWarps ? sm.best_key[lane] : -1;
         int bb = lane < kRankWarps ? sm.best_b[lane] : 0x7FFFFFFF;
         long long bP = lane < kRankWarps ? sm.best_P[lane] : 0;
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) {
-            const long long ok = __shfl_down_sync(kFullMask, bk, d);
-            const int ob = __shfl_down_sync(kFullMask, bb, d);
-            const long long oP = __shfl_down_sync(kFullMask, bP, d);
-            if (cand_better(ok, ob, bk, bb)) {
-                bk = ok;
-                bb = ob;
-                bP = oP;
-            }
+        {
+            unsigned long long P = (unsigned long long)bP, unused = 0ull;
+            warp_first_max(bk, bb, P, unused);
+            bP = (long long)P;
         }
         if (lane == 0) {
             int st = (any_bad_cost || any_bad_table) ? DSPARK_STATUS_BAD_COST : 0;
@@ -1273,7 +1281,6 @@ struct SelSmem {
     int n_gather, bad_table, budget_s;
     unsigned long long cstar;  // C* of the chosen budget (kNoComposite: none)
     // dense_select_kernel
-    unsigned long long scan64[40];
     unsigned int d_floor;      // the largest lower bound of theta (float bits)
     int d_ncand, d_marked;     // entries left after the bounds; keys in their bins
     double d_fixed;            // bias + alpha
@@ -2010,6 +2017,12 @@ __device__ __forceinline__ DenseStage dense_stage(SelSmem &sm, int n) {
 // the largest kept key: survivals are at least 2^-14
 constexpr uint32_t kMaxKeptKey = kOneBits - ((uint32_t)kMinExpBiased << 23);
 
+// An upper bound of a value whose float rounded down is v_lo: one float ulp
+// up (the smallest positive float above 0).
+__device__ __forceinline__ float value_hi(float v_lo) {
+    return v_lo == 0.0f ? __int_as_float(1) : __fmaf_ru(fabsf(v_lo), 0x1p-23f, v_lo);
+}
+
 // B + P 2^-37 rounded down and up to floats, by integer operations
 // (tau_float truncates; one ulp more when bits were dropped)
 __device__ __forceinline__ void tau_float_rd_ru(int B, long long P, float &lo, float &hi) {
@@ -2020,25 +2033,6 @@ __device__ __forceinline__ void tau_float_rd_ru(int B, long long P, float &lo, f
     hi = __uint_as_float(bits + ((x & ((1ull << (msb - 23)) - 1ull)) ? 1u : 0u));
 }
 
-// The first maximiser over a warp: the largest key (-1: none), ties to the
-// smaller budget; every lane receives it with the winner's P and C.  32-bit
-// warp reductions (a loop of 64-bit shuffles and compares took ~8000 cycles
-// here).
-__device__ __forceinline__ void warp_first_max(long long &key, int &b, unsigned long long &P,
-                                               unsigned long long &C) {
-    const unsigned long long uk = key >= 0 ? (unsigned long long)key + 1ull : 0ull;
-    const unsigned hi = (unsigned)(uk >> 32), lo = (unsigned)uk;
-    const unsigned mhi = __reduce_max_sync(kFullMask, hi);
-    const unsigned mlo = __reduce_max_sync(kFullMask, hi == mhi ? lo : 0u);
-    const bool top = hi == mhi && lo == mlo;
-    const unsigned bmin = __reduce_min_sync(kFullMask, top ? (unsigned)b : 0x7FFFFFFFu);
-    const unsigned win = __ballot_sync(kFullMask, top && (unsigned)b == bmin);
-    const int src = __ffs(win) - 1;
-    P = __shfl_sync(kFullMask, P, src);
-    C = __shfl_sync(kFullMask, C, src);
-    key = (long long)((((unsigned long long)mhi << 32) | mlo) - 1ull);
-    b = (int)bmin;
-}
 
 template <int IPT>
 __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a) {
@@ -2062,6 +2056,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
     // 64-bit arithmetic of entry_last_budget, before the clip) and its value
     // as a float; the run's loads are all issued first
     bool order_bad = false;
+    // the run's smallest staged value and largest upper bound of a value
+    // (NaN when a value is NaN), for the run's bound after the wait
+    float run_vmin = INFINITY, run_vmax = 0.0f;
     {
         long long Mv[kDensePer + 2];  // M_{j0-1} .. M_{j0+kDensePer}
         double vv[kDensePer];
@@ -2078,7 +2075,11 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
             if (j < j1 && in_bounds(j, kDenseMaxEntries, a.status)) {
                 ds.range[j] = entry_range_from(c.kind, n, j, Mv[u], Mv[u + 1], Mv[u + 2], B,
                                                order_bad);
-                ds.f32[j] = __double2float_rd(vv[u]);
+                const float v_lo = __double2float_rd(vv[u]);
+                ds.f32[j] = v_lo;
+                run_vmin = fminf(run_vmin, v_lo);
+                run_vmax = (v_lo != v_lo || run_vmax != run_vmax) ? v_lo + run_vmax
+                                                                  : fmaxf(run_vmax, value_hi(v_lo));
             }
         }
     }
@@ -2177,7 +2178,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
     // fp32 cannot bound theta (the fp64 cost is then checked)
     auto cost_bounds = [&](int j, float &k_lo, float &k_hi) -> bool {
         const float v_lo = ds.f32[j];
-        const float v_hi = v_lo == 0.0f ? __int_as_float(1) : __fmaf_ru(fabsf(v_lo), 0x1p-23f, v_lo);
+        const float v_hi = value_hi(v_lo);
         if (c.kind == DSPARK_COST_SPS_1D) {
             k_lo = v_lo;
             k_hi = v_hi;
@@ -2202,24 +2203,27 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
     float run_hi = 0.0f;    // upper bound of theta over the run (NaN: none)
     if (!bad_table) {
         int bl = 0;
-        bool all_bounded = true;
-        float kmax_hi = 0.0f, kmin_lo = INFINITY;
-        for (int j = j0; j < j1; ++j) {
-            int b;
-            if (!entry_b(j, b)) continue;
-            jl = j;
-            bl = b;
-            float k_lo, k_hi;
-            all_bounded = cost_bounds(j, k_lo, k_hi) && all_bounded;
-            kmax_hi = fmaxf(kmax_hi, k_hi);
-            kmin_lo = fminf(kmin_lo, k_lo);
-        }
+        for (int j = j1 - 1; j >= j0 && jl < 0; --j)
+            if (entry_b(j, bl)) jl = j;
         float my_floor = 0.0f;
         if (jl >= 0) {
-            float t_lo, t_hi, k_lo, k_hi;
+            // every budget of the run is at most bl: tau(bl) bounds them all;
+            // the cost's bounds over the run from the prologue's value range
+            // (over every entry of the run, a superset of those with a budget)
+            float t_lo, t_hi, k_lo, k_hi, kr_lo, kr_hi;
             tau_bounds(bl, bl >= 1 ? bin_search(bl) : 0, t_lo, t_hi);
             if (cost_bounds(jl, k_lo, k_hi)) my_floor = theta_lo(t_lo, k_lo, k_hi);
-            run_hi = all_bounded ? theta_hi(t_hi, kmin_lo, kmax_hi) : __int_as_float(0x7fffffff);
+            bool run_bounded;
+            if (c.kind == DSPARK_COST_SPS_1D) {
+                kr_lo = run_vmin;
+                kr_hi = run_vmax;
+                run_bounded = run_vmin > 0.0f && run_vmax < INFINITY;
+            } else {
+                kr_lo = __fadd_rd(fixed_lo, run_vmin);
+                kr_hi = __fadd_ru(fixed_hi, run_vmax);
+                run_bounded = kr_lo > 0.0f && kr_hi < INFINITY;
+            }
+            run_hi = run_bounded ? theta_hi(t_hi, kr_lo, kr_hi) : __int_as_float(0x7fffffff);
         }
         // non-negative floats order like their bits: one atomic per warp
         const unsigned wfloor = __reduce_max_sync(kFullMask, __float_as_uint(my_floor));
@@ -2264,6 +2268,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
     if (tid == 0 && b_forced >= 1) mark_bin(bin_search(b_forced));
     __syncthreads();
     const int K = min(sm.d_ncand, n);
+    // the first candidate value of each thread's exact evaluation, in flight
+    // while the bins are gathered
+    const double v_first = tid < K ? __ldg(c.val + ds.list[tid]) : 0.0;
 
     long long my_key = -1;
     int my_b = 0x7FFFFFFF;
@@ -2301,13 +2308,20 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
         gather_marked<IPT>(a, sm, key, r0, k0);
         __syncthreads();
         const int m = min(sm.n_gather, kGather);
-        rank_gathered(sm, m, a.status);
-        __syncthreads();
-        {
-            const unsigned long long v = tid < m ? sm.SF[tid] : 0ull;
-            unsigned long long tot;
-            const unsigned long long ex = block_exclusive_scan<unsigned long long>(v, sm.scan64, &tot);
-            if (tid < m) sm.LF[tid] = ex + v;  // inclusive sums, in composite order
+        // each gathered candidate's rank and the inclusive fixed-point sum of
+        // the survivals up to it, both by counting: SC / SF in composite order
+        for (int i = tid; i < m; i += kSelThreads) {
+            const unsigned long long ci = sm.LC[i];
+            int pos = 0;
+            unsigned long long sum = 0ull;
+            for (int y = 0; y < m; ++y) {
+                const bool le = sm.LC[y] <= ci;
+                pos += le ? 1 : 0;
+                sum += le ? sm.LF[y] : 0ull;
+            }
+            if (!in_bounds(pos - 1, m, a.status)) continue;
+            sm.SC[pos - 1] = ci;
+            sm.SF[pos - 1] = sum;
         }
         __syncthreads();
         // P and C* at budget b >= 1: the bin's keys start where the
@@ -2323,13 +2337,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
             }
             const int idx = lo + r - 1;
             if (!in_bounds(idx, m, a.status) || !in_bounds(lo, m, a.status)) return false;
-            P = sm.csum[d] + sm.LF[idx] - (lo > 0 ? sm.LF[lo - 1] : 0ull);
+            P = sm.csum[d] + sm.SF[idx] - (lo > 0 ? sm.SF[lo - 1] : 0ull);
             C = sm.SC[idx];
             return true;
         };
         for (int i = tid; i < K; i += kSelThreads) {
             const int j = ds.list[i];
-            const double vj = __ldg(c.val + j);  // in flight with the search below
+            const double vj = i == tid ? v_first : __ldg(c.val + j);
             const int2 bd = ds.range[j];
             unsigned long long P = 0ull, C = kNoComposite;
             if (bd.x >= 1 && !exact_at(bd.x, bd.y, P, C)) continue;
