@@ -1979,23 +1979,26 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
 //       survives between the bin's smallest and largest survival (and the
 //       bin's other keys between the same), so tau(b_j) lies in an interval
 //       and theta_j between fp32 bounds computed with directed rounding
-//       (which bound the fp64 definition as well).  The largest lower bound
-//       is a floor of the maximum;
+//       (which bound the fp64 definition as well).  Each thread holds a
+//       contiguous run of entries: the run's last entry (its largest tau)
+//       gives a lower bound, and the largest over the CTA is a floor of the
+//       maximum; the run as a whole is bounded above by that tau with the
+//       run's largest SPS (smallest cost);
+//   (3) in the runs whose bound reaches the floor, every entry is bounded;
 //       an entry whose upper bound is below the floor cannot be the first
-//       maximiser;
-//   (3) the entries left (in the workloads, a handful) and the forced
-//       budget mark their bins.  When those bins hold at most kGather keys,
-//       they are gathered, ordered by composite and prefix-summed: the exact
-//       P and C* of every entry left follow, and theta in fp64 as in the
-//       other paths; the first maximiser wins;
+//       maximiser.  The entries left (in the workloads, a handful) and the
+//       forced budget mark their bins.  When those bins hold at most kGather
+//       keys, the keys are gathered, ordered by composite and prefix-summed
+//       (both by counting): the exact P and C* of every entry left follow,
+//       and theta in fp64 as in the other paths; the first maximiser wins;
 //   (4) otherwise (bins crowded by near-equal survivals) the entries left
 //       take select_kernel's threshold slots, 32 at a time (radix passes
 //       inside crowded bins);
 //   (5) lengths, tier-filled budget and pack as in select_kernel.
 // The table is staged in shared memory before the dependency wait (each
-// entry's range of budgets and its value as a float), in the region the
-// select path stages the pack's inputs in; the fused pack reads its inputs
-// from global memory instead.
+// entry's range of budgets and its value rounded down to a float, and each
+// run's value range), in the region the select path stages the pack's
+// inputs in; the fused pack reads its inputs from global memory instead.
 
 // entries of the stage: range int2 + value float + candidate list int
 constexpr int kDenseMaxEntries = (kStage * 4 - 16) / 16;
@@ -2003,9 +2006,9 @@ constexpr int kDensePer = (kDenseMaxEntries + kSelThreads - 1) / kSelThreads;  /
 
 struct DenseStage {
     int2 *range;  // entry j's budgets [x, y] whose M = B + b looks it up (before the clip to
-                  // b_top); after step (2): its last budget and that budget's bin
-    float *f32;   // its value rounded down to a float; after step (2): theta's upper bound
-    int *list;    // entries left after the bounds (step 3)
+                  // b_top); for an entry left by step (3): its last budget and that bin
+    float *f32;   // its value rounded down to a float
+    int *list;    // entries left by step (3)
 };
 
 __device__ __forceinline__ DenseStage dense_stage(SelSmem &sm, int n) {
