@@ -119,7 +119,8 @@ def _planner_cases(dev, out) -> None:
     every M (staged in shared memory), a table past the stage (global
     memory), additive tables of 5, 31, 32 and 61 entries, interpolated tables
     of 8 and 100 samples; budgets 0 and everything; every candidate below
-    eps; B=1 and gamma=1; the planner options."""
+    eps; B=1 and gamma=1; the dense path over crowded bins; the planner
+    options."""
     rng = np.random.default_rng(1234)
     B, g = 256, 16
     z = rng.normal(1.5, 1.2, (B, g)).astype(np.float32)
@@ -158,6 +159,16 @@ def _planner_cases(dev, out) -> None:
     _plan(dev, out, "B1_g1", z11, np.ones(1, np.float32), kind=api.COST_ADDITIVE,
           M=np.array([1, 2], np.int32), val=np.array([1.0, 1.5]), eps=1e-4, min_len=1,
           max_len=2, forced=-1)
+    # the dense path's crowded bins (every request with the same
+    # confidences: 600 equal keys a bin) and a flat table: the entries left
+    # go through the threshold slots 32 at a time
+    Bc, gc = 600, 8
+    zc = np.full((Bc, gc), np.log(0.3 / 0.7), np.float32)
+    Mc = np.arange(Bc, Bc + Bc * gc + 1, dtype=np.int32)
+    for forced in (-1, 1234):
+        _plan(dev, out, f"dense_crowded_{forced}", zc, np.ones(gc, np.float32),
+              kind=api.COST_SPS_1D, M=Mc, val=np.full(Mc.size, 500.0), eps=1e-4, min_len=1,
+              max_len=gc + 1, forced=forced)
     gen = _i32(dev, np.arange(B))
     stale = _i32(dev, np.where(np.arange(B) % 5 == 0, -1, np.arange(B)))
     lag = torch.from_numpy((z + rng.normal(0, 0.3, z.shape)).astype(np.float32)).to(dev)
