@@ -1283,6 +1283,8 @@ struct SelSmem {
     // dense_select_kernel
     unsigned int d_floor;      // the largest lower bound of theta (float bits)
     int d_ncand, d_marked;     // entries left after the bounds; keys in their bins
+    int d_nruns;               // runs whose bound reaches the floor
+    int d_runs[kSelThreads];   // their threads
     double d_fixed;            // bias + alpha
     float d_fixed_lo, d_fixed_hi;  // rounded down and up to float
     unsigned long long d_fP, d_fC;  // P and C* at the forced budget
@@ -1984,9 +1986,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
 //       gives a lower bound, and the largest over the CTA is a floor of the
 //       maximum; the run as a whole is bounded above by that tau with the
 //       run's largest SPS (smallest cost);
-//   (3) in the runs whose bound reaches the floor, every entry is bounded;
-//       an entry whose upper bound is below the floor cannot be the first
-//       maximiser.  The entries left (in the workloads, a handful) and the
+//   (3) the runs whose bound reaches the floor are listed and every entry
+//       of theirs is bounded by a thread of its own; an entry whose upper
+//       bound is below the floor cannot be the first maximiser.  The entries left (in the workloads, a handful) and the
 //       forced budget mark their bins.  When those bins hold at most kGather
 //       keys, the keys are gathered, ordered by composite and prefix-summed
 //       (both by counting): the exact P and C* of every entry left follow,
@@ -2093,6 +2095,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
         sm.d_floor = 0u;
         sm.d_ncand = 0;
         sm.d_marked = 0;
+        sm.d_nruns = 0;
         sm.d_fixed = __dadd_rn(c.bias, c.alpha);
         sm.d_fixed_lo = __double2float_rd(sm.d_fixed);
         sm.d_fixed_hi = __double2float_ru(sm.d_fixed);
@@ -2235,38 +2238,37 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
     __syncthreads();
     const float floor_all = __uint_as_float(sm.d_floor);
 
-    // (3) in the runs that can hold the maximum: every entry bounded; those
-    // whose upper bound reaches the floor (or that fp32 cannot bound) are
-    // left, with their budget and bin written over their stage range
-    bool my_bad_cost = false;
+    // (3) the runs that can hold the maximum are listed; then every entry
+    // of theirs gets a thread and its own bounds: those whose upper bound
+    // reaches the floor (or that fp32 cannot bound) are left, with their
+    // budget and bin written over their stage range
     if (jl >= 0 && !(run_hi < floor_all)) {
-        unsigned left = 0u;  // bit u: entry j0 + u is left
-        int d = -1, d_last = -1;
-        for (int j = j0; j < j1; ++j) {
-            int b;
-            if (!entry_b(j, b)) continue;
-            if (b >= 1) d = d < 0 ? bin_search(b) : bin_from(b, d);
-            float t_lo, t_hi, k_lo, k_hi;
-            const bool bounded = cost_bounds(j, k_lo, k_hi);
-            if (bounded) {
-                tau_bounds(b, d, t_lo, t_hi);
-                if (theta_hi(t_hi, k_lo, k_hi) < floor_all) continue;
-            } else if (!cost_ok(j)) {  // flagged; never a maximiser
-                my_bad_cost = true;
-                continue;
-            }
-            ds.range[j] = make_int2(b, b >= 1 ? d : 0);
-            left |= 1u << (j - j0);
-            if (b >= 1 && d != d_last) {  // budgets do not decrease: each bin once
-                mark_bin(d);
-                d_last = d;
-            }
+        const int k = atomicAdd(&sm.d_nruns, 1);
+        if (in_bounds(k, kSelThreads, a.status)) sm.d_runs[k] = tid;
+    }
+    __syncthreads();
+    const int n_runs = min(sm.d_nruns, kSelThreads);
+    bool my_bad_cost = false;
+    for (int e = tid; e < n_runs * per; e += kSelThreads) {
+        const int r = e / per;
+        const int j = sm.d_runs[r] * per + (e - r * per);  // the run's thread t holds [t * per, ...)
+        if (j >= n) continue;  // the table's last run is short
+        int b;
+        if (!entry_b(j, b)) continue;
+        const int d = b >= 1 ? bin_search(b) : 0;
+        float k_lo, k_hi;
+        if (cost_bounds(j, k_lo, k_hi)) {
+            float t_lo, t_hi;
+            tau_bounds(b, d, t_lo, t_hi);
+            if (theta_hi(t_hi, k_lo, k_hi) < floor_all) continue;
+        } else if (!cost_ok(j)) {  // flagged; never a maximiser
+            my_bad_cost = true;
+            continue;
         }
-        if (left) {  // list slots for the run, in one reservation
-            int slot = atomicAdd(&sm.d_ncand, __popc(left));
-            for (unsigned m = left; m; m &= m - 1, ++slot)
-                if (in_bounds(slot, n, a.status)) ds.list[slot] = j0 + __ffs(m) - 1;
-        }
+        ds.range[j] = make_int2(b, d);
+        const int slot = atomicAdd(&sm.d_ncand, 1);
+        if (in_bounds(slot, n, a.status)) ds.list[slot] = j;
+        if (b >= 1) mark_bin(d);
     }
     if (tid == 0 && b_forced >= 1) mark_bin(bin_search(b_forced));
     __syncthreads();
