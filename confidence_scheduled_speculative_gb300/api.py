@@ -38,10 +38,12 @@ STATUS_OUT_OF_BOUNDS = 1024  # only the bounds-checked library sets it
 
 # cost tables of at most SELECT_MAX_ENTRIES entries take the planner's
 # single-CTA select path, larger ones up to DENSE_MAX_ENTRIES its single-CTA
-# dense path (both with the pack fused in); larger tables, and interpolated
-# ones, the multi-CTA rank path
+# dense path, interpolated tables of at most INTERP_MAX_SAMPLES samples its
+# single-CTA interp path (all three with the pack fused in); the rest the
+# multi-CTA rank path
 SELECT_MAX_ENTRIES = 31
 DENSE_MAX_ENTRIES = 6143
+INTERP_MAX_SAMPLES = 2048
 COST_SPS_1D = 0
 COST_ADDITIVE = 1
 COST_ADDITIVE_INTERP = 2
@@ -51,9 +53,9 @@ MAX_TIERS = 64
 
 
 def planner_path(n_candidates: int, cost_kind: int, n_entries: int) -> str:
-    """Which planner kernel a call takes: "select", "dense" or "rank"."""
+    """Which planner kernel a call takes: "select", "dense", "interp" or "rank"."""
     if cost_kind == COST_ADDITIVE_INTERP:
-        return "rank"
+        return "interp" if n_entries <= INTERP_MAX_SAMPLES else "rank"
     if n_entries <= SELECT_MAX_ENTRIES:
         return "select"
     return "dense" if n_entries <= DENSE_MAX_ENTRIES else "rank"

@@ -9,7 +9,7 @@ namespace dspark {
 
 namespace {
 constexpr int kMaxDevices = 64;
-constexpr int kMaxSmemSlots = 16;
+constexpr int kMaxSmemSlots = 24;
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_smem_done[kMaxDevices][kMaxSmemSlots];
 }  // namespace

@@ -6,10 +6,11 @@
 //   [TUT] charlestar.github.io tutorial "DSpark confidence-scheduled
 //         speculative decoding"
 //
-// The survival kernel, then one of three planner kernels by cost table:
-// select_kernel (at most 31 entries) and dense_select_kernel (up to 6143
-// entries, not interpolated) run on one CTA and are described at their
-// definitions; rank_kernel takes the rest:
+// The survival kernel, then one of four planner kernels by cost table:
+// select_kernel (at most 31 entries), dense_select_kernel (up to 6143
+// entries, not interpolated) and interp_select_kernel (interpolated, up to
+// 2048 samples) run on one CTA and are described at their definitions;
+// rank_kernel takes the rest:
 //   survival_kernel  one warp per request, lane k = depth: STS
 //                    c_k = sigmoid(z_k / T_k) ([AVS] §二) and the prefix
 //                    survival S_k = prod_{i<=k} c_i ([AVS] §一), each lane
@@ -1287,6 +1288,7 @@ struct SelSmem {
     int d_runs[kSelThreads];   // their threads
     double d_fixed;            // bias + alpha
     float d_fixed_lo, d_fixed_hi;  // rounded down and up to float
+    float d_fixed32;               // rounded to the nearest float (interp_select_kernel)
     unsigned long long d_fP, d_fC;  // P and C* at the forced budget
     int d_item[32];                 // entry of each threshold slot (-1: the forced budget)
     long long d_bkey[32];           // per-warp first maximiser
@@ -2039,6 +2041,116 @@ __device__ __forceinline__ void tau_float_rd_ru(int B, long long P, float &lo, f
 }
 
 
+// The bin of budget b >= 1: the first whose inclusive count reaches b
+// (cum[kHistBins-1] = n_kept >= b).
+__device__ __forceinline__ int bin_of_budget(const SelSmem &sm, int b) {
+    int lo = 0, hi = kHistBins - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (sm.cum[mid] >= (unsigned)b) hi = mid;
+        else lo = mid + 1;
+    }
+    return lo;
+}
+
+// Bin d marked for the gather; its first marker adds the bin's keys to
+// d_marked.
+__device__ __forceinline__ void mark_bin(SelSmem &sm, int d, int32_t *status) {
+    if (!in_bounds(d, kHistBins, status)) return;
+    const unsigned bit = 1u << (d & 31);
+    if (!(atomicOr(&sm.binmask[d >> 5], bit) & bit))
+        atomicAdd(&sm.d_marked, (int)(sm.cum[d] - (d > 0 ? sm.cum[d - 1] : 0u)));
+}
+
+// tau(b) = B + P 2^-37 in fp32 with directed rounding (bounds of the fp64
+// definition too: rd32(x) <= rn64(x) <= ru32(x) for every real x).  tau(b)
+// lies in [B + c0 + r s_lo, B + c0 + r s_hi] and in [B + c1 - (cnt - r) s_hi,
+// B + c1 - (cnt - r) s_lo], with c0 and c1 the fixed-point sums before and
+// after b's bin d, cnt the bin's keys, s_lo and s_hi its smallest and largest
+// survival (exact floats) and r = b - cum[d-1].  b = 0: tau = B exactly.
+__device__ __forceinline__ void tau_interval(const SelSmem &sm, int B, int b, int d, float &t_lo,
+                                             float &t_hi, int32_t *status) {
+    t_lo = t_hi = (float)B;
+    if (b < 1 || !in_bounds(d + 1, kHistBins, status)) return;
+    const int before = d > 0 ? (int)sm.cum[d - 1] : 0;
+    const int cnt = (int)sm.cum[d] - before;
+    const uint32_t last = (((uint32_t)d + 1) << kHistShift) - 1;
+    const float s_hi = __uint_as_float(kOneBits - ((uint32_t)d << kHistShift));
+    const float s_lo = __uint_as_float(kOneBits - (last < kMaxKeptKey ? last : kMaxKeptKey));
+    float b0_lo, b0_hi, b1_lo, b1_hi;
+    tau_float_rd_ru(B, (long long)sm.csum[d], b0_lo, b0_hi);
+    tau_float_rd_ru(B, (long long)sm.csum[d + 1], b1_lo, b1_hi);
+    const float r = (float)(b - before), rest = (float)(cnt - (b - before));
+    t_lo = fmaxf(__fmaf_rd(r, s_lo, b0_lo), __fmaf_rd(-rest, s_hi, b1_lo));
+    t_hi = fminf(__fmaf_ru(r, s_hi, b0_hi), __fmaf_ru(-rest, s_lo, b1_hi));
+}
+
+// Each of the m <= kGather gathered candidates' rank and the inclusive
+// fixed-point sum of the survivals up to it, both by counting: SC / SF in
+// composite order.
+__device__ __forceinline__ void rank_gathered_prefix(SelSmem &sm, int m, int32_t *status) {
+    for (int i = threadIdx.x; i < m; i += kSelThreads) {
+        const unsigned long long ci = sm.LC[i];
+        int pos = 0;
+        unsigned long long sum = 0ull;
+        for (int y = 0; y < m; ++y) {
+            const bool le = sm.LC[y] <= ci;
+            pos += le ? 1 : 0;
+            sum += le ? sm.LF[y] : 0ull;
+        }
+        if (!in_bounds(pos - 1, m, status)) continue;
+        sm.SC[pos - 1] = ci;
+        sm.SF[pos - 1] = sum;
+    }
+}
+
+// P and C* at budget b >= 1 in bin d, from SC / SF when every key of the bin
+// is among the m gathered: the bin's keys start where the composites reach
+// the bin (its number is the composite's top bits).
+__device__ __forceinline__ bool exact_at_budget(const SelSmem &sm, int m, int b, int d,
+                                                unsigned long long &P, unsigned long long &C,
+                                                int32_t *status) {
+    const int r = b - (d > 0 ? (int)sm.cum[d - 1] : 0);
+    const unsigned long long first = (unsigned long long)d << (kHistShift + 14);
+    int lo = 0, hi = m;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (sm.SC[mid] < first) lo = mid + 1;
+        else hi = mid;
+    }
+    const int idx = lo + r - 1;
+    if (!in_bounds(idx, m, status) || !in_bounds(lo, m, status)) return false;
+    P = sm.csum[d] + sm.SF[idx] - (lo > 0 ? sm.SF[lo - 1] : 0ull);
+    C = sm.SC[idx];
+    return true;
+}
+
+// The first maximiser over the block, left in every lane of warp 0 (the
+// other warps keep their own); true when any thread's `bad` is set.
+// Contains a barrier: every thread of the block calls it.
+__device__ __forceinline__ bool block_first_max(SelSmem &sm, long long &key, int &b,
+                                                unsigned long long &P, unsigned long long &C,
+                                                bool bad) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    warp_first_max(key, b, P, C);
+    if (lane == 0) {
+        sm.d_bkey[warp] = key;
+        sm.d_bb[warp] = b;
+        sm.d_bP[warp] = P;
+        sm.d_bC[warp] = C;
+    }
+    const bool any_bad = __syncthreads_or(bad) != 0;
+    if (warp == 0) {
+        key = sm.d_bkey[lane];
+        b = sm.d_bb[lane];
+        P = sm.d_bP[lane];
+        C = sm.d_bC[lane];
+        warp_first_max(key, b, P, C);
+    }
+    return any_bad;
+}
+
+
 template <int IPT>
 __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -2123,61 +2235,12 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
         b = min(r.y, b_top32);
         return b >= r.x;
     };
-    // the bin of budget b >= 1: the first whose inclusive count reaches b
-    // (cum[kHistBins-1] = n_kept >= b)
-    auto bin_search = [&](int b) -> int {
-        int lo = 0, hi = kHistBins - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (sm.cum[mid] >= (unsigned)b) hi = mid;
-            else lo = mid + 1;
-        }
-        return lo;
-    };
-    // the same from a bin d known to be at or below it
-    auto bin_from = [&](int b, int d) -> int {
-        while (d < kHistBins - 1 && sm.cum[d] < (unsigned)b) ++d;
-        return d;
-    };
     // the fp64 definition of entry j's cost is a positive finite number
     auto cost_ok = [&](int j) -> bool {
         const double vj = __ldg(c.val + j);
         if (c.kind == DSPARK_COST_SPS_1D) return vj > 0.0 && isfinite(vj);
         const double Tm = __dadd_rn(fixed_cost, vj);
         return Tm > 0.0 && isfinite(Tm);
-    };
-    auto mark_bin = [&](int d) {
-        if (!in_bounds(d, kHistBins, a.status)) return;
-        const unsigned bit = 1u << (d & 31);
-        if (!(atomicOr(&sm.binmask[d >> 5], bit) & bit))
-            atomicAdd(&sm.d_marked, (int)(sm.cum[d] - (d > 0 ? sm.cum[d - 1] : 0u)));
-    };
-
-    // theta's bounds in fp32 with directed rounding hold for the fp64
-    // definition too (rd32(x) <= rn64(x) <= ru32(x) for every real x).
-    // tau(b) = B + P 2^-37 lies in [B + c0 + r s_lo, B + c0 + r s_hi] and in
-    // [B + c1 - (cnt - r) s_hi, B + c1 - (cnt - r) s_lo], with c0 and c1 the
-    // fixed-point sums before and after b's bin d, cnt the bin's keys, s_lo
-    // and s_hi its smallest and largest survival (exact floats) and
-    // r = b - cum[d-1].
-    int cd = -1, c_before = 0, c_cnt = 0;  // the bin whose constants are held
-    float s_lo = 0.0f, s_hi = 0.0f, b0_lo = 0.0f, b0_hi = 0.0f, b1_lo = 0.0f, b1_hi = 0.0f;
-    auto tau_bounds = [&](int b, int d, float &t_lo, float &t_hi) {
-        t_lo = t_hi = (float)B;  // b = 0: tau = B exactly
-        if (b < 1 || !in_bounds(d + 1, kHistBins, a.status)) return;
-        if (d != cd) {
-            cd = d;
-            c_before = d > 0 ? (int)sm.cum[d - 1] : 0;
-            c_cnt = (int)sm.cum[d] - c_before;
-            const uint32_t last = (((uint32_t)d + 1) << kHistShift) - 1;
-            s_hi = __uint_as_float(kOneBits - ((uint32_t)d << kHistShift));
-            s_lo = __uint_as_float(kOneBits - (last < kMaxKeptKey ? last : kMaxKeptKey));
-            tau_float_rd_ru(B, (long long)sm.csum[d], b0_lo, b0_hi);
-            tau_float_rd_ru(B, (long long)sm.csum[d + 1], b1_lo, b1_hi);
-        }
-        const float r = (float)(b - c_before), rest = (float)(c_cnt - (b - c_before));
-        t_lo = fmaxf(__fmaf_rd(r, s_lo, b0_lo), __fmaf_rd(-rest, s_hi, b1_lo));
-        t_hi = fminf(__fmaf_ru(r, s_hi, b0_hi), __fmaf_ru(-rest, s_lo, b1_hi));
     };
     // the staged value v rounded down and an upper bound one float ulp up;
     // the cost's bounds (SPS: v; additive: bias + alpha + v); false when
@@ -2217,7 +2280,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
             // the cost's bounds over the run from the prologue's value range
             // (over every entry of the run, a superset of those with a budget)
             float t_lo, t_hi, k_lo, k_hi, kr_lo, kr_hi;
-            tau_bounds(bl, bl >= 1 ? bin_search(bl) : 0, t_lo, t_hi);
+            tau_interval(sm, B, bl, bl >= 1 ? bin_of_budget(sm, bl) : 0, t_lo, t_hi, a.status);
             if (cost_bounds(jl, k_lo, k_hi)) my_floor = theta_lo(t_lo, k_lo, k_hi);
             bool run_bounded;
             if (c.kind == DSPARK_COST_SPS_1D) {
@@ -2255,11 +2318,11 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
         if (j >= n) continue;  // the table's last run is short
         int b;
         if (!entry_b(j, b)) continue;
-        const int d = b >= 1 ? bin_search(b) : 0;
+        const int d = b >= 1 ? bin_of_budget(sm, b) : 0;
         float k_lo, k_hi;
         if (cost_bounds(j, k_lo, k_hi)) {
             float t_lo, t_hi;
-            tau_bounds(b, d, t_lo, t_hi);
+            tau_interval(sm, B, b, d, t_lo, t_hi, a.status);
             if (theta_hi(t_hi, k_lo, k_hi) < floor_all) continue;
         } else if (!cost_ok(j)) {  // flagged; never a maximiser
             my_bad_cost = true;
@@ -2268,9 +2331,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
         ds.range[j] = make_int2(b, d);
         const int slot = atomicAdd(&sm.d_ncand, 1);
         if (in_bounds(slot, n, a.status)) ds.list[slot] = j;
-        if (b >= 1) mark_bin(d);
+        if (b >= 1) mark_bin(sm, d, a.status);
     }
-    if (tid == 0 && b_forced >= 1) mark_bin(bin_search(b_forced));
+    if (tid == 0 && b_forced >= 1) mark_bin(sm, bin_of_budget(sm, b_forced), a.status);
     __syncthreads();
     const int K = min(sm.d_ncand, n);
     // the first candidate value of each thread's exact evaluation, in flight
@@ -2313,38 +2376,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
         gather_marked<IPT>(a, sm, key, r0, k0);
         __syncthreads();
         const int m = min(sm.n_gather, kGather);
-        // each gathered candidate's rank and the inclusive fixed-point sum of
-        // the survivals up to it, both by counting: SC / SF in composite order
-        for (int i = tid; i < m; i += kSelThreads) {
-            const unsigned long long ci = sm.LC[i];
-            int pos = 0;
-            unsigned long long sum = 0ull;
-            for (int y = 0; y < m; ++y) {
-                const bool le = sm.LC[y] <= ci;
-                pos += le ? 1 : 0;
-                sum += le ? sm.LF[y] : 0ull;
-            }
-            if (!in_bounds(pos - 1, m, a.status)) continue;
-            sm.SC[pos - 1] = ci;
-            sm.SF[pos - 1] = sum;
-        }
+        rank_gathered_prefix(sm, m, a.status);
         __syncthreads();
-        // P and C* at budget b >= 1: the bin's keys start where the
-        // composites reach the bin (its number is the composite's top bits)
         auto exact_at = [&](int b, int d, unsigned long long &P, unsigned long long &C) -> bool {
-            const int r = b - (d > 0 ? (int)sm.cum[d - 1] : 0);
-            const unsigned long long first = (unsigned long long)d << (kHistShift + 14);
-            int lo = 0, hi = m;
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (sm.SC[mid] < first) lo = mid + 1;
-                else hi = mid;
-            }
-            const int idx = lo + r - 1;
-            if (!in_bounds(idx, m, a.status) || !in_bounds(lo, m, a.status)) return false;
-            P = sm.csum[d] + sm.SF[idx] - (lo > 0 ? sm.SF[lo - 1] : 0ull);
-            C = sm.SC[idx];
-            return true;
+            return exact_at_budget(sm, m, b, d, P, C, a.status);
         };
         for (int i = tid; i < K; i += kSelThreads) {
             const int j = ds.list[i];
@@ -2356,7 +2391,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
         }
         if (tid == 0 && b_forced >= 1) {
             unsigned long long P, C;
-            if (exact_at(b_forced, bin_search(b_forced), P, C)) {
+            if (exact_at(b_forced, bin_of_budget(sm, b_forced), P, C)) {
                 sm.d_fP = P;
                 sm.d_fC = C;
             }
@@ -2397,20 +2432,12 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
         }
     }
 
-    // the first maximiser over the block
-    warp_first_max(my_key, my_b, my_P, my_C);
-    if (lane == 0) {
-        sm.d_bkey[warp] = my_key;
-        sm.d_bb[warp] = my_b;
-        sm.d_bP[warp] = my_P;
-        sm.d_bC[warp] = my_C;
-    }
-    const bool any_bad_cost = __syncthreads_or(my_bad_cost) != 0;
+    // the first maximiser over the block, in warp 0
+    const bool any_bad_cost = block_first_max(sm, my_key, my_b, my_P, my_C, my_bad_cost);
     if (warp == 0) {
-        long long bk = sm.d_bkey[lane];
-        int bb = sm.d_bb[lane];
-        unsigned long long bP = sm.d_bP[lane], bC = sm.d_bC[lane];
-        warp_first_max(bk, bb, bP, bC);
+        const long long bk = my_key;
+        const int bb = my_b;
+        const unsigned long long bP = my_P, bC = my_C;
         if (lane == 0) {
             int st = (any_bad_cost || bad_table) ? DSPARK_STATUS_BAD_COST : 0;
             int budget = 0;
@@ -2468,6 +2495,279 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
     select_finish<IPT>(a, sm, key, b_top, false);
 }
 
+// ------------------------------------------------------ interpolated select
+//
+// Interpolated additive tables ([AVS] §四: theta(M) read between the exported
+// samples by linear interpolation, so every budget has its own cost and is a
+// candidate) of at most kInterpMaxSamples samples, on one CTA, as
+// dense_select_kernel plans dense tables, with budgets in the place of the
+// table's entries:
+//   (1) bins, keys, their scan;
+//   (2) each thread holds a contiguous run of the budgets 0..b_top; tau's
+//       interval at the run's last budget (the run's largest tau) and the
+//       cost walked along the run in fp32 (InterpWalk: T with its error
+//       bound, a reciprocal with margins) bound theta over the run; the last
+//       budget's lower bound feeds the floor;
+//   (3) the runs reaching the floor are listed and each of their budgets is
+//       bounded by a thread of its own; the budgets left (or that fp32
+//       cannot bound, whose cost is checked in fp64) mark their bins;
+//   (4) exact P and C* from the gathered bins (or the threshold slots when
+//       they are crowded), T in fp64 from the samples and theta = tau / T;
+//       the first maximiser wins;
+//   (5) lengths, tier-filled budget and pack as in select_kernel.
+// The samples (M as int32, the value as a float) are staged in shared memory
+// before the dependency wait, then the list of budgets left.
+
+constexpr int kInterpMaxSamples = 2048;
+static_assert(8 * kInterpMaxSamples + 4 * (kMaxCandidates + 1) <= 4 * kStage,
+              "samples and the budget list fit the stage");
+
+// T(B, M) of the interpolated table at M = Mv from the staged samples (the
+// segment by binary search; the fp64 values from global memory), as
+// interp_cost: false when T is not a positive finite number.
+__device__ __forceinline__ bool interp_cost_staged(const int32_t *sM, const double *val, int n,
+                                                   long long Mv, double fixed_cost, double &T) {
+    int j = -1;
+    if (Mv > (long long)sM[0]) {
+        int lo = 0, hi = n - 1;  // the last sample with M_j <= Mv
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((long long)sM[mid] <= Mv) lo = mid;
+            else hi = mid - 1;
+        }
+        j = lo;
+    }
+    return interp_cost_at(sM, val, n, Mv, j, fixed_cost, T);
+}
+
+template <int IPT>
+__global__ void __launch_bounds__(kSelThreads, 1) interp_select_kernel(PlanArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    SelSmem &sm = *reinterpret_cast<SelSmem *>(smem_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = a.B, G = a.gamma;
+    const CostArgs &c = a.cost;
+    const int n = c.n;
+    const int i0 = tid * IPT;
+    const int r0 = i0 / G, k0 = i0 - r0 * G;
+    int32_t *sM = sm.stage;
+    float *sV = reinterpret_cast<float *>(sm.stage + n);
+    int *list = sm.stage + 2 * n;  // budgets left by step (3)
+
+    pdl_trigger();
+    // while the survivals are computed: the samples, their order
+    bool order_bad = false;
+    for (int j = tid; j < n; j += kSelThreads) {
+        if (!in_bounds(j, kInterpMaxSamples, a.status)) break;
+        const int m = __ldg(c.M + j);
+        sM[j] = m;
+        sV[j] = (float)__ldg(c.val + j);
+        if (j > 0 && !(m > __ldg(c.M + j - 1))) order_bad = true;
+    }
+    const int Mlast = __ldg(c.M + n - 1);
+    if (tid < kHistBins / 32) sm.binmask[tid] = 0u;
+    if (tid == 0) {
+        sm.n_gather = 0;
+        sm.d_floor = 0u;
+        sm.d_ncand = 0;
+        sm.d_marked = 0;
+        sm.d_nruns = 0;
+        sm.d_fixed = __dadd_rn(c.bias, c.alpha);
+        sm.d_fixed32 = (float)sm.d_fixed;  // bias + alpha as a float (InterpWalk's bounds)
+        sm.d_fP = 0ull;
+        sm.d_fC = kNoComposite;
+    }
+    pdl_wait();  // survivals and bins come from survival_kernel
+    const int forced = resolve_forced(a);
+
+    // (1) bins, keys, scan (its barriers publish the prologue's stores)
+    uint32_t key[IPT];
+    const int n_kept = select_bins<IPT>(a, sm, key);
+    const bool bad_table = __syncthreads_or(order_bad) != 0;
+    const long long b_top = min((long long)n_kept, (long long)Mlast - (long long)B);
+    const double fixed_cost = sm.d_fixed;
+    const float fixed32 = sm.d_fixed32;
+    const bool has_forced = forced >= 0 && b_top >= 0 && !bad_table;
+    const int b_forced = has_forced ? (int)min((long long)forced, b_top) : -1;
+    const int nb = (bad_table || b_top < 0) ? 0 : (int)b_top + 1;  // the budgets 0..b_top
+    const int per = (nb + kSelThreads - 1) / kSelThreads;
+    const int b0 = min(tid * per, nb), b1 = min(b0 + per, nb);
+
+    // (2) the run's bound and the floor
+    float run_hi = 0.0f;  // upper bound of theta over the run (NaN: none)
+    {
+        float my_floor = 0.0f;
+        if (b0 < b1) {
+            const int bl = b1 - 1;
+            float t_lo, t_hi;
+            tau_interval(sm, B, bl, bl >= 1 ? bin_of_budget(sm, bl) : 0, t_lo, t_hi, a.status);
+            InterpWalk wk(sM, c.val, sV, n);
+            wk.init((long long)B + b0);
+            bool bounded = true;
+            float lo, hi;
+            for (int b = b0; b < b1; ++b) {
+                if (wk.bounds(B, b, t_hi, fixed32, lo, hi)) run_hi = fmaxf(run_hi, hi);
+                else bounded = false;
+            }
+            if (!bounded) run_hi = __int_as_float(0x7fffffff);
+            if (wk.bounds(B, bl, t_lo, fixed32, lo, hi)) my_floor = lo;
+        }
+        // non-negative floats order like their bits: one atomic per warp
+        const unsigned wfloor = __reduce_max_sync(kFullMask, __float_as_uint(my_floor));
+        if (lane == 0) atomicMax(&sm.d_floor, wfloor);
+    }
+    __syncthreads();
+    const float floor_all = __uint_as_float(sm.d_floor);
+
+    // (3) the runs that can hold the maximum, then each of their budgets
+    if (b0 < b1 && !(run_hi < floor_all)) {
+        const int k = atomicAdd(&sm.d_nruns, 1);
+        if (in_bounds(k, kSelThreads, a.status)) sm.d_runs[k] = tid;
+    }
+    __syncthreads();
+    const int n_runs = min(sm.d_nruns, kSelThreads);
+    bool my_bad_cost = false;
+    for (int e = tid; e < n_runs * per; e += kSelThreads) {
+        const int r = e / per;
+        const int b = sm.d_runs[r] * per + (e - r * per);  // the run's thread t holds [t * per, ...)
+        if (b >= nb) continue;  // the last run is short
+        const int d = b >= 1 ? bin_of_budget(sm, b) : 0;
+        float t_lo, t_hi, lo, hi;
+        tau_interval(sm, B, b, d, t_lo, t_hi, a.status);
+        InterpWalk wk(sM, c.val, sV, n);
+        wk.init((long long)B + b);
+        if (wk.bounds(B, b, t_hi, fixed32, lo, hi)) {
+            if (hi < floor_all) continue;
+        } else {
+            double T;
+            if (!interp_cost_staged(sM, c.val, n, (long long)B + b, fixed_cost, T)) {
+                my_bad_cost = true;  // flagged; never a maximiser
+                continue;
+            }
+        }
+        const int slot = atomicAdd(&sm.d_ncand, 1);
+        if (in_bounds(slot, kMaxCandidates + 1, a.status)) list[slot] = b;
+        if (b >= 1) mark_bin(sm, d, a.status);
+    }
+    if (tid == 0 && b_forced >= 1) mark_bin(sm, bin_of_budget(sm, b_forced), a.status);
+    __syncthreads();
+    const int K = min(sm.d_ncand, kMaxCandidates + 1);
+
+    long long my_key = -1;
+    int my_b = 0x7FFFFFFF;
+    unsigned long long my_P = 0ull, my_C = kNoComposite;
+    // exact theta at budget b with P, C*: the first maximiser
+    auto evaluate = [&](int b, unsigned long long P, unsigned long long C) {
+        double T;
+        if (!interp_cost_staged(sM, c.val, n, (long long)B + b, fixed_cost, T)) {
+            my_bad_cost = true;
+            return;
+        }
+        const double theta = __ddiv_rn(tau_of(B, (long long)P), T);
+        const long long kk = __double_as_longlong(theta);  // positive: orders like the values
+        if (cand_better(kk, b, my_key, my_b)) {
+            my_key = kk;
+            my_b = b;
+            my_P = P;
+            my_C = C;
+        }
+    };
+
+    if (sm.d_marked <= kGather) {
+        // (4) the marked bins' candidates in composite order, prefix-summed
+        gather_marked<IPT>(a, sm, key, r0, k0);
+        __syncthreads();
+        const int m = min(sm.n_gather, kGather);
+        rank_gathered_prefix(sm, m, a.status);
+        __syncthreads();
+        for (int i = tid; i < K; i += kSelThreads) {
+            const int b = list[i];
+            unsigned long long P = 0ull, C = kNoComposite;
+            if (b >= 1 && !exact_at_budget(sm, m, b, bin_of_budget(sm, b), P, C, a.status)) continue;
+            evaluate(b, P, C);
+        }
+        if (tid == 0 && b_forced >= 1) {
+            unsigned long long P, C;
+            if (exact_at_budget(sm, m, b_forced, bin_of_budget(sm, b_forced), P, C, a.status)) {
+                sm.d_fP = P;
+                sm.d_fC = C;
+            }
+        }
+    } else {
+        // (4) crowded bins: the budgets left (then the forced budget) take
+        // the threshold slots 32 at a time
+        const int T = K + (b_forced >= 1 ? 1 : 0);
+        for (int base = 0; base < T; base += 32) {  // uniform
+            const int nc = min(32, T - base);
+            if (tid < kHistBins / 32) sm.binmask[tid] = 0u;
+            if (tid == 0) sm.n_gather = 0;
+            __syncthreads();
+            if (warp < nc) {
+                const int item = base + warp;
+                slot_setup(sm, warp, lane, item < K ? list[item] : b_forced, a.status);
+                if (lane == 0) sm.d_item[warp] = item < K ? 0 : -1;
+            }
+            __syncthreads();
+            slot_thresholds<IPT>(a, sm, key, r0, k0, nc);
+            if (warp == 0 && lane < nc) {
+                const int b = sm.cand_b[lane];
+                const unsigned long long P = b >= 1 ? sm.P[lane] : 0ull;
+                const unsigned long long C = b >= 1 ? sm.cthr[lane] : kNoComposite;
+                if (sm.d_item[lane] >= 0) {
+                    evaluate(b, P, C);
+                } else {
+                    sm.d_fP = P;
+                    sm.d_fC = C;
+                }
+            }
+            __syncthreads();
+        }
+    }
+
+    // the first maximiser over the block, in warp 0
+    const bool any_bad_cost = block_first_max(sm, my_key, my_b, my_P, my_C, my_bad_cost);
+    if (warp == 0 && lane == 0) {
+        int st = (any_bad_cost || bad_table) ? DSPARK_STATUS_BAD_COST : 0;
+        int budget = 0;
+        unsigned long long Pbud = 0ull, cstar = kNoComposite;
+        double theta_out = 0.0;
+        if (forced < 0) {
+            if (bad_table || my_b == 0x7FFFFFFF) {
+                st |= DSPARK_STATUS_INFEASIBLE;
+            } else {
+                budget = my_b;
+                theta_out = __longlong_as_double(my_key);
+                if (budget > 0) {
+                    Pbud = my_P;
+                    cstar = my_C;
+                }
+            }
+        } else if (!has_forced) {
+            st |= DSPARK_STATUS_INFEASIBLE;
+        } else {
+            budget = b_forced;
+            if (budget > 0) {
+                Pbud = sm.d_fP;
+                cstar = sm.d_fC;
+            }
+            // theta at the forced budget: the cost interpolated at M = B + budget
+            double Ti;
+            if (interp_cost_staged(sM, c.val, n, (long long)B + budget, fixed_cost, Ti))
+                theta_out = __ddiv_rn(tau_of(B, (long long)Pbud), Ti);
+        }
+        if (st) flag(a.status, st);
+        sm.cstar = cstar;
+        sm.budget_s = budget;
+        a.budget[0] = budget;
+        a.tau_theta[0] = tau_of(B, (long long)Pbud);
+        a.tau_theta[1] = theta_out;
+    }
+    __syncthreads();
+
+    // (5) lengths, tier-filled budget, pack (its inputs from global memory)
+    select_finish<IPT>(a, sm, key, b_top, false);
+}
+
 // The select kernels launch with the largest dynamic shared memory a CTA
 // may have, more than SelSmem needs, so that their one CTA has an SM to
 // itself: with 56 registers a thread, 1024 threads leave room for one CTA of
@@ -2479,24 +2779,30 @@ static_assert(sizeof(SelSmem) <= kSelLaunchSmem, "SelSmem fits the launch");
 size_t select_smem_bytes() { return kSelLaunchSmem; }
 
 
+// Which planner kernel takes a cost table: select_kernel for at most
+// kMaxSelect entries, dense_select_kernel for more (at most
+// kDenseMaxEntries), interp_select_kernel for interpolated tables of at most
+// kInterpMaxSamples samples, rank_kernel for the rest.
+enum class PlanPath { kSelect, kDense, kInterp, kRank };
+
+PlanPath plan_path(const dspark_cost_table *cost) {
+    if (cost->kind == DSPARK_COST_ADDITIVE_INTERP)
+        return cost->n <= kInterpMaxSamples ? PlanPath::kInterp : PlanPath::kRank;
+    if (cost->n <= kMaxSelect) return PlanPath::kSelect;
+    return cost->n <= kDenseMaxEntries ? PlanPath::kDense : PlanPath::kRank;
+}
+
 template <int IPT>
-cudaError_t launch_select(const PlanArgs &a, bool dense, cudaStream_t s) {
-    const int slot = (IPT == 1 ? 1 : IPT == 2 ? 2 : IPT == 4 ? 3 : IPT == 8 ? 4 : 5) + (dense ? 9 : 0);
-    void (*kernel)(PlanArgs) = dense ? dense_select_kernel<IPT> : select_kernel<IPT>;
+cudaError_t launch_select(const PlanArgs &a, PlanPath path, cudaStream_t s) {
+    // shared-memory attribute slots: 1-5 select, 10-14 dense, 15-19 interp
+    const int slot = (IPT == 1 ? 1 : IPT == 2 ? 2 : IPT == 4 ? 3 : IPT == 8 ? 4 : 5) +
+                     (path == PlanPath::kDense ? 9 : path == PlanPath::kInterp ? 14 : 0);
+    void (*kernel)(PlanArgs) = path == PlanPath::kDense    ? dense_select_kernel<IPT>
+                               : path == PlanPath::kInterp ? interp_select_kernel<IPT>
+                                                           : select_kernel<IPT>;
     cudaError_t e = ensure_smem(reinterpret_cast<const void *>(kernel), (int)select_smem_bytes(), slot);
     if (e != cudaSuccess) return e;
     return launch_pdl(kernel, dim3(1), dim3(kSelThreads), select_smem_bytes(), s, a);
-}
-
-// Which planner kernel takes a cost table: select_kernel for at most
-// kMaxSelect entries, dense_select_kernel for more (at most
-// kDenseMaxEntries), rank_kernel for larger and interpolated tables.
-enum class PlanPath { kSelect, kDense, kRank };
-
-PlanPath plan_path(const dspark_cost_table *cost) {
-    if (cost->kind == DSPARK_COST_ADDITIVE_INTERP) return PlanPath::kRank;
-    if (cost->n <= kMaxSelect) return PlanPath::kSelect;
-    return cost->n <= kDenseMaxEntries ? PlanPath::kDense : PlanPath::kRank;
 }
 
 }  // namespace dspark
@@ -2541,14 +2847,13 @@ int check_plan(const float *conf_logits, const float *sts_temps, const dspark_pl
 // chose.
 int launch_pass(PlanArgs a, PlanPath path, cudaStream_t s) {
     if (path != PlanPath::kRank) {
-        const bool dense = path == PlanPath::kDense;
         const int ipt = (a.N + kSelThreads - 1) / kSelThreads;
         cudaError_t e;
-        if (ipt <= 1) e = launch_select<1>(a, dense, s);
-        else if (ipt <= 2) e = launch_select<2>(a, dense, s);
-        else if (ipt <= 4) e = launch_select<4>(a, dense, s);
-        else if (ipt <= 8) e = launch_select<8>(a, dense, s);
-        else e = launch_select<16>(a, dense, s);
+        if (ipt <= 1) e = launch_select<1>(a, path, s);
+        else if (ipt <= 2) e = launch_select<2>(a, path, s);
+        else if (ipt <= 4) e = launch_select<4>(a, path, s);
+        else if (ipt <= 8) e = launch_select<8>(a, path, s);
+        else e = launch_select<16>(a, path, s);
         if (e == cudaSuccess) return DSPARK_OK;
         // the bins survival_kernel filled must not reach the next call
         cudaMemsetAsync(&a.scratch->hcount[0], 0,
@@ -2585,9 +2890,8 @@ int run_plan(const float *conf_logits, const float *sts_temps, const dspark_plan
     PassScratch *ps = scratch_at<PassScratch>(scratch, plan_pass_offset(B, N));
     int32_t *pass_lens = scratch_at<int32_t>(scratch, plan_pass_lens_offset(B, N));
     float *lagged_surv = scratch_at<float>(scratch, plan_pass_surv_offset(B, N));
-    // one-CTA select (few candidate budgets, or a dense table bounded per
-    // entry); an interpolated table makes every budget a candidate and takes
-    // the rank path
+    // one-CTA select (few candidate budgets, a dense table bounded per
+    // entry, an interpolated table bounded per budget), else the rank path
     const PlanPath path = plan_path(cost);
     const bool select = path != PlanPath::kRank;  // the survival kernel bins the keys
     const int32_t *conf_gen = opt ? opt->conf_generation : nullptr;

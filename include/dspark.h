@@ -234,10 +234,10 @@ DSPARK_API int dspark_pack_verify(const int32_t *anchor, const int32_t *draft, c
                        int32_t *status, void *stream);
 
 /* dspark_plan followed by dspark_pack_verify on the planner's verify_lens,
- * in fewer launches: for cost tables of at most 6143 entries (not
- * interpolated) the planner's last kernel, which runs on one CTA, also packs
+ * in fewer launches: for cost tables of at most 6143 entries (interpolated:
+ * 2048 samples) the planner's last kernel, which runs on one CTA, also packs
  * the window (one launch and one dependency wait fewer per step); larger
- * and interpolated tables run the two calls' kernels back to back.
+ * tables run the two calls' kernels back to back.
  * Arguments and outputs are those of the two calls (the planner's
  * workspace, which must be zero-filled once, serves both); the pages'
  * planner and pack are the same two steps ([AVS] §一, §五-§六; [ROUND]

@@ -139,7 +139,7 @@ def _planner_cases(dev, out) -> None:
         Mt = np.unique(Mt)
         _plan(dev, out, f"additive_{n}", z, T, kind=api.COST_ADDITIVE, M=Mt,
               val=0.002 * Mt + 0.5, bias=1.0, alpha=0.2, **base)
-    for n in (8, 100):
+    for n in (8, 100, 2100):  # 2100 samples: the rank path
         Mi = np.unique(np.linspace(B, B * (g + 1) + 8, n).astype(np.int32))
         _plan(dev, out, f"interp_{n}", z, T, kind=api.COST_ADDITIVE_INTERP, M=Mi,
               val=0.0025 * Mi + 0.3 * np.sin(Mi / 97.0) ** 2, bias=0.8, alpha=0.1, **base)

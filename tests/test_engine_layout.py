@@ -50,6 +50,8 @@ def test_select_path_limit_matches_kernel():
     stage = re.search(r"constexpr int kStage = (\d+);", text)
     assert "constexpr int kDenseMaxEntries = (kStage * 4 - 16) / 16;" in text
     assert api.DENSE_MAX_ENTRIES == (int(stage.group(1)) * 4 - 16) // 16
+    interp = re.search(r"constexpr int kInterpMaxSamples = (\d+);", text)
+    assert api.INTERP_MAX_SAMPLES == int(interp.group(1))
 
 
 def test_binding_planner_paths():
@@ -62,4 +64,6 @@ def test_binding_planner_paths():
     assert api.planner_path(4096, api.COST_SPS_1D, 4097) == "dense"
     assert api.planner_path(4096, api.COST_ADDITIVE, api.DENSE_MAX_ENTRIES) == "dense"
     assert api.planner_path(16384, api.COST_SPS_1D, api.DENSE_MAX_ENTRIES + 1) == "rank"
-    assert api.planner_path(64, api.COST_ADDITIVE_INTERP, 5) == "rank"
+    assert api.planner_path(64, api.COST_ADDITIVE_INTERP, 5) == "interp"
+    assert api.planner_path(4096, api.COST_ADDITIVE_INTERP, api.INTERP_MAX_SAMPLES) == "interp"
+    assert api.planner_path(4096, api.COST_ADDITIVE_INTERP, api.INTERP_MAX_SAMPLES + 1) == "rank"

@@ -124,7 +124,8 @@ def test_plan_random(dev, orc, seed):
 
 @pytest.mark.parametrize("seed", range(80))
 def test_plan_random_interpolated_table(dev, orc, seed):
-    """The interpolated additive table (every budget its own cost; rank path),
+    """The interpolated additive table (every budget its own cost; the
+    single-CTA interp path),
     with sparse and dense tables, forced budgets and invalid entries."""
     rng = np.random.default_rng(91000 + seed)
     P = _random_problem(rng)
@@ -143,6 +144,27 @@ def test_plan_random_interpolated_table(dev, orc, seed):
     ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"], 2,
                    P["M"], P["val"], P["bias"], P["alpha"])
     exp = compare_plan(f"interp/{seed}", gres, ref, B, g, P["min_len"], _restage(orc, P))
+    assert int(gres["status"][0]) == exp.status
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_plan_interpolated_table_on_the_rank_path(dev, orc, seed):
+    """Interpolated tables of more than 2048 samples keep the multi-CTA rank
+    path; against the oracle."""
+    from confidence_scheduled_speculative_gb300 import api
+    rng = np.random.default_rng(93000 + seed)
+    B, g = 300, 16
+    z = rng.normal(1.2, 1.4, (B, g)).astype(np.float32)
+    hi = B + B * g + 6
+    M = np.sort(rng.choice(np.arange(1, hi + 1), size=api.INTERP_MAX_SAMPLES + 1 + 300 * seed,
+                           replace=False)).astype(np.int32)
+    val = 0.002 * M + 0.2 * np.sin(M / 53.0) ** 2
+    P = dict(B=B, gamma=g, z=z, T=np.ones(g, np.float32), eps=1e-4, min_len=1, max_len=g + 1,
+             kind=2, M=M, val=val, forced=-1 if seed < 3 else 1500, bias=1.0, alpha=0.4)
+    assert api.planner_path(B * g, 2, M.size) == "rank"
+    gres = _gpu_plan(dev, P)
+    ref = orc.plan(z, P["T"], 1e-4, 1, g + 1, P["forced"], 2, M, val, 1.0, 0.4)
+    exp = compare_plan(f"interp_rank/{seed}", gres, ref, B, g, 1, _restage(orc, P))
     assert int(gres["status"][0]) == exp.status
 
 
@@ -214,6 +236,8 @@ def _crowded_problem(B, g, p, kind, flat, forced=-1, eps=1e-4):
     maximum."""
     z = np.full((B, g), np.log(p / (1 - p)), np.float32)
     M = np.arange(B, B + B * g + 1, dtype=np.int32)
+    if kind == 2:  # interpolated: a few samples, every budget a candidate
+        M = np.unique(np.linspace(B, B + B * g, 9).astype(np.int32))
     if kind == 0:
         val = np.full(M.size, 500.0) if flat else 1.0 / (2e-3 + 3e-6 * M)
     else:
@@ -230,14 +254,18 @@ def _crowded_problem(B, g, p, kind, flat, forced=-1, eps=1e-4):
     dict(B=600, g=8, p=0.3, kind=0, flat=True, forced=1234),
     dict(B=600, g=8, p=0.999, kind=0, flat=True, eps=2.0 ** -14),
     dict(B=64, g=8, p=0.3, kind=0, flat=True),
+    dict(B=600, g=8, p=0.3, kind=2, flat=True),
+    dict(B=600, g=8, p=0.3, kind=2, flat=False, forced=777),
+    dict(B=520, g=11, p=0.6, kind=2, flat=False),
 ])
 def test_plan_dense_path_crowded_bins(dev, orc, case):
-    """Dense tables (more than 31 entries: the single-CTA dense path) over
-    crowded bins and flat tables, against the oracle's fp64 evaluation of
-    every budget."""
+    """Dense tables (more than 31 entries: the single-CTA dense path) and
+    interpolated tables (the single-CTA interp path) over crowded bins and
+    flat tables, against the oracle's fp64 evaluation of every budget."""
     P = _crowded_problem(**case)
     from confidence_scheduled_speculative_gb300 import api
-    assert api.planner_path(P["B"] * P["gamma"], P["kind"], P["M"].size) == "dense"
+    assert api.planner_path(P["B"] * P["gamma"], P["kind"], P["M"].size) == (
+        "interp" if P["kind"] == 2 else "dense")
     g = _gpu_plan(dev, P)
     ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"], P["kind"],
                    P["M"], P["val"], P["bias"], P["alpha"])
