@@ -56,11 +56,19 @@ def _i32(dev, a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
 
 
-def _step_guarded(dev, name, fused):
+def _interpolated(step):
+    """The step with its additive tier table read as interpolation samples."""
+    import dataclasses
+    return dataclasses.replace(step, cost=dataclasses.replace(step.cost, kind=2))
+
+
+def _step_guarded(dev, name, fused, interp=False):
     """One plan + pack + greedy accept + cap-accept of a workload through the
     binding, every output and workspace guarded."""
     from confidence_scheduled_speculative_gb300 import api
     step = wl.make_step(wl.WORKLOADS[name], seed=2)
+    if interp:
+        step = _interpolated(step)
     w, c = step.workload, step.cost
     B, g, cap = step.B, step.gamma, step.capacity
     i32, f32, f64 = torch.int32, torch.float32, torch.float64
@@ -127,14 +135,16 @@ def _step_guarded(dev, name, fused):
     return step, gb, res
 
 
-@pytest.mark.parametrize("name,fused", [("dsv4_like", True), ("mixed", False),
-                                        ("qwen_like", True), ("tiny", False)])
-def test_step_outputs_stay_inside_their_buffers(dev, name, fused):
-    """Planner (select or rank path), pack (fused or its own kernel), greedy
-    accept and cap-accept write nothing outside the buffers they are given,
-    and give the outputs of the same step on plain buffers."""
+@pytest.mark.parametrize("name,fused,interp", [("dsv4_like", True, False), ("mixed", False, False),
+                                               ("dsv4_like", True, True), ("qwen_like", True, False),
+                                               ("tiny", False, False)])
+def test_step_outputs_stay_inside_their_buffers(dev, name, fused, interp):
+    """Planner (select, dense select or interp select path), pack (fused or
+    its own kernel), greedy accept and cap-accept write nothing outside the
+    buffers they are given, and give the outputs of the same step on plain
+    buffers."""
     from confidence_scheduled_speculative_gb300.engine import StepConfig, VerifyStep
-    step, gb, res = _step_guarded(dev, name, fused)
+    step, gb, res = _step_guarded(dev, name, fused, interp)
     _all_intact(gb)
     vs = VerifyStep(StepConfig.from_step(step), dev)
     vs.load_inputs(step)
