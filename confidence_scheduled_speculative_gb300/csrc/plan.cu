@@ -2505,9 +2505,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
 //   (1) bins, keys, their scan;
 //   (2) each thread holds a contiguous run of the budgets 0..b_top; tau's
 //       interval at the run's last budget (the run's largest tau) and the
-//       cost walked along the run in fp32 (InterpWalk: T with its error
-//       bound, a reciprocal with margins) bound theta over the run; the last
-//       budget's lower bound feeds the floor;
+//       cost in fp32 (InterpWalk: T with its error bound, a reciprocal with
+//       margins) at the run's ends and at the samples inside it (where the
+//       piecewise-linear cost takes its minimum) bound theta over the run;
+//       the last budget's lower bound feeds the floor;
 //   (3) the runs reaching the floor are listed and each of their budgets is
 //       bounded by a thread of its own; the budgets left (or that fp32
 //       cannot bound, whose cost is checked in fp64) mark their bins;
@@ -2601,14 +2602,25 @@ __global__ void __launch_bounds__(kSelThreads, 1) interp_select_kernel(PlanArgs 
             const int bl = b1 - 1;
             float t_lo, t_hi;
             tau_interval(sm, B, bl, bl >= 1 ? bin_of_budget(sm, bl) : 0, t_lo, t_hi, a.status);
+            // theta <= tau(bl) / T over the run, and T (linear between the
+            // samples, constant below the first) is smallest at an end of
+            // the run or at a sample inside it: bounded at those only
             InterpWalk wk(sM, c.val, sV, n);
             wk.init((long long)B + b0);
             bool bounded = true;
             float lo, hi;
-            for (int b = b0; b < b1; ++b) {
+            auto at = [&](int b) {
                 if (wk.bounds(B, b, t_hi, fixed32, lo, hi)) run_hi = fmaxf(run_hi, hi);
                 else bounded = false;
+            };
+            at(b0);
+            // the samples after b0's segment up to bl, in order (the table is
+            // ascending here); at most n steps
+            for (int q = wk.seg + 1; q < n && (long long)sM[q] <= (long long)B + bl; ++q) {
+                const int bs = sM[q] - B;
+                if (bs > b0) at(bs);
             }
+            if (bl > b0) at(bl);
             if (!bounded) run_hi = __int_as_float(0x7fffffff);
             if (wk.bounds(B, bl, t_lo, fixed32, lo, hi)) my_floor = lo;
         }
