@@ -728,15 +728,20 @@ def _oracle_plan_ex(orc, P, opt):
 @pytest.mark.parametrize("seed", range(80))
 def test_plan_options_random(dev, orc, seed):
     """dspark_plan_ex with a random mix of the generation mask, a lagged
-    budget and tier alignment, on both planner paths, against the oracle's
-    composition of the plain planner."""
+    budget and tier alignment, on every single-CTA planner path, against the
+    oracle's composition of the plain planner."""
     rng = np.random.default_rng(61000 + seed)
     P = _random_problem(rng)
-    if seed % 4 == 3:  # a dense 1-D table: the rank path
+    if seed % 4 == 3:  # a 1-D table at every M: the dense select path
         B, g = P["B"], P["gamma"]
         P["kind"] = 0
         P["M"] = np.arange(B, B + max(B * g + 2, 40), dtype=np.int32)
         P["val"] = 1.0 / (1e-3 + 2e-6 * P["M"])
+    elif seed % 4 == 2:  # an interpolated table: the interp select path
+        B, g = P["B"], P["gamma"]
+        P["kind"] = 2
+        P["M"] = np.unique(np.linspace(max(1, B - 3), B + B * g + 4, int(rng.integers(2, 9))).astype(np.int32))
+        P["val"] = np.sort(rng.uniform(0.05, 3.0, P["M"].size))
     opt = _options(rng, P)
     g = _gpu_plan_ex(dev, P, opt)
     ref = _oracle_plan_ex(orc, P, opt)
@@ -745,14 +750,19 @@ def test_plan_options_random(dev, orc, seed):
     assert int(g["status"][0]) == exp.status
 
 
-@pytest.mark.parametrize("name", ["dsv4_like", "stress", "mixed"])
-def test_plan_pack_options_workloads(dev, orc, name):
+@pytest.mark.parametrize("name,interp", [("dsv4_like", False), ("stress", False),
+                                         ("mixed", False), ("dsv4_like", True)])
+def test_plan_pack_options_workloads(dev, orc, name, interp):
     """The fused call with every option on a workload: lagged confidences
     from another seed, a third of the slots stale, alignment to the pack's
-    tiers (the workload's, or powers of two where it has none)."""
+    tiers (the workload's, or powers of two where it has none); the
+    dsv4_like tier table also read as interpolation samples."""
+    import dataclasses
     from confidence_scheduled_speculative_gb300 import api
     from confidence_scheduled_speculative_gb300.engine import StepConfig, VerifyStep
     step = wl.make_step(wl.WORKLOADS[name], seed=2)
+    if interp:
+        step = dataclasses.replace(step, cost=dataclasses.replace(step.cost, kind=2))
     lag = wl.make_step(wl.WORKLOADS[name], seed=3)
     B, g = step.B, step.gamma
     rng = np.random.default_rng(9)
