@@ -205,7 +205,8 @@ def _dense_problem(rng, seed):
     forced = -1 if rng.random() < 0.7 else int(rng.integers(0, B * g + 3))
     eps = float(np.float32(rng.choice([2.0 ** -14, 1e-4, 0.01])))
     max_len = int(rng.integers(2, g + 2))
-    return dict(B=B, gamma=g, z=z, T=T, eps=eps, min_len=1, max_len=max_len, kind=kind, M=M,
+    min_len = int(rng.integers(1, max_len + 1)) if rng.random() < 0.25 else 1
+    return dict(B=B, gamma=g, z=z, T=T, eps=eps, min_len=min_len, max_len=max_len, kind=kind, M=M,
                 val=val, forced=forced, bias=float(rng.uniform(0, 2)),
                 alpha=float(rng.uniform(0, 1)))
 
