@@ -2151,6 +2151,88 @@ __device__ __forceinline__ bool block_first_max(SelSmem &sm, long long &key, int
 }
 
 
+// Crowded bins (step (4) of the dense and interp paths): the K items left
+// (item i's budget from budget_of(i)), then the forced budget b_forced when
+// it is >= 1, take select_kernel's threshold slots 32 at a time; eval(i, b,
+// P, C) runs in warp 0's lane of item i's slot, and the forced budget's P and
+// C* go to sm.d_fP / sm.d_fC.  Every thread of the block calls it.
+template <int IPT, class BudgetOf, class Eval>
+__device__ __forceinline__ void threshold_rounds(const PlanArgs &a, SelSmem &sm,
+                                                 const uint32_t (&key)[IPT], int r0, int k0,
+                                                 int K, int b_forced, BudgetOf budget_of,
+                                                 Eval eval) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T = K + (b_forced >= 1 ? 1 : 0);
+    for (int base = 0; base < T; base += 32) {  // uniform
+        const int nc = min(32, T - base);
+        if (tid < kHistBins / 32) sm.binmask[tid] = 0u;
+        if (tid == 0) sm.n_gather = 0;
+        __syncthreads();
+        if (warp < nc) {
+            const int item = base + warp;
+            slot_setup(sm, warp, lane, item < K ? budget_of(item) : b_forced, a.status);
+            if (lane == 0) sm.d_item[warp] = item < K ? item : -1;
+        }
+        __syncthreads();
+        slot_thresholds<IPT>(a, sm, key, r0, k0, nc);
+        if (warp == 0 && lane < nc) {
+            const int b = sm.cand_b[lane], item = sm.d_item[lane];
+            const unsigned long long P = b >= 1 ? sm.P[lane] : 0ull;
+            const unsigned long long C = b >= 1 ? sm.cthr[lane] : kNoComposite;
+            if (item >= 0) {
+                eval(item, b, P, C);
+            } else {
+                sm.d_fP = P;
+                sm.d_fC = C;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// The plan's decision and scalar outputs on the dense and interp paths, in
+// lane 0 of warp 0 after block_first_max: the first maximiser (key, b, P,
+// C), or the forced budget (its P and C* in sm.d_fP / sm.d_fC, theta from
+// forced_theta(budget, tau)); sets sm.cstar and sm.budget_s for the lengths.
+template <class ForcedTheta>
+__device__ __forceinline__ void write_decision(const PlanArgs &a, SelSmem &sm, long long key,
+                                               int b, unsigned long long P, unsigned long long C,
+                                               bool any_bad_cost, bool bad_table, int forced,
+                                               int b_forced, ForcedTheta forced_theta) {
+    int st = (any_bad_cost || bad_table) ? DSPARK_STATUS_BAD_COST : 0;
+    int budget = 0;
+    unsigned long long Pbud = 0ull, cstar = kNoComposite;
+    double theta_out = 0.0;
+    if (forced < 0) {
+        if (bad_table || b == 0x7FFFFFFF) {
+            st |= DSPARK_STATUS_INFEASIBLE;
+        } else {
+            budget = b;
+            theta_out = __longlong_as_double(key);
+            if (budget > 0) {
+                Pbud = P;
+                cstar = C;
+            }
+        }
+    } else if (b_forced < 0) {
+        st |= DSPARK_STATUS_INFEASIBLE;
+    } else {
+        budget = b_forced;
+        if (budget > 0) {
+            Pbud = sm.d_fP;
+            cstar = sm.d_fC;
+        }
+        theta_out = forced_theta(budget, tau_of(a.B, (long long)Pbud));
+    }
+    if (st) flag(a.status, st);
+    sm.cstar = cstar;
+    sm.budget_s = budget;
+    a.budget[0] = budget;
+    a.tau_theta[0] = tau_of(a.B, (long long)Pbud);
+    a.tau_theta[1] = theta_out;
+}
+
+
 template <int IPT>
 __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -2397,98 +2479,38 @@ __global__ void __launch_bounds__(kSelThreads, 1) dense_select_kernel(PlanArgs a
             }
         }
     } else {
-        // (4) crowded bins: the entries left (then the forced budget) take
-        // the threshold slots 32 at a time
-        const int T = K + (b_forced >= 1 ? 1 : 0);
-        for (int base = 0; base < T; base += 32) {  // uniform
-            const int nc = min(32, T - base);
-            if (tid < kHistBins / 32) sm.binmask[tid] = 0u;
-            if (tid == 0) sm.n_gather = 0;
-            __syncthreads();
-            if (warp < nc) {
-                const int item = base + warp;
-                int b = b_forced, j = -1;
-                if (item < K) {
-                    j = ds.list[item];
-                    b = ds.range[j].x;
-                }
-                slot_setup(sm, warp, lane, b, a.status);
-                if (lane == 0) sm.d_item[warp] = j;
-            }
-            __syncthreads();
-            slot_thresholds<IPT>(a, sm, key, r0, k0, nc);
-            if (warp == 0 && lane < nc) {
-                const int b = sm.cand_b[lane], j = sm.d_item[lane];
-                const unsigned long long P = b >= 1 ? sm.P[lane] : 0ull;
-                const unsigned long long C = b >= 1 ? sm.cthr[lane] : kNoComposite;
-                if (j >= 0) {
-                    evaluate(j, __ldg(c.val + j), b, P, C);
-                } else {
-                    sm.d_fP = P;
-                    sm.d_fC = C;
-                }
-            }
-            __syncthreads();
-        }
+        // (4) crowded bins: the entries left, then the forced budget
+        threshold_rounds<IPT>(
+            a, sm, key, r0, k0, K, b_forced, [&](int i) { return ds.range[ds.list[i]].x; },
+            [&](int i, int b, unsigned long long P, unsigned long long C) {
+                const int j = ds.list[i];
+                evaluate(j, __ldg(c.val + j), b, P, C);
+            });
     }
 
-    // the first maximiser over the block, in warp 0
+    // the first maximiser over the block (in warp 0), the decision
     const bool any_bad_cost = block_first_max(sm, my_key, my_b, my_P, my_C, my_bad_cost);
-    if (warp == 0) {
-        const long long bk = my_key;
-        const int bb = my_b;
-        const unsigned long long bP = my_P, bC = my_C;
-        if (lane == 0) {
-            int st = (any_bad_cost || bad_table) ? DSPARK_STATUS_BAD_COST : 0;
-            int budget = 0;
-            unsigned long long Pbud = 0ull, cstar = kNoComposite;
-            double theta_out = 0.0;
-            if (forced < 0) {
-                if (bad_table || bb == 0x7FFFFFFF) {
-                    st |= DSPARK_STATUS_INFEASIBLE;
-                } else {
-                    budget = bb;
-                    theta_out = __longlong_as_double(bk);
-                    if (budget > 0) {
-                        Pbud = bP;
-                        cstar = bC;
-                    }
-                }
-            } else if (!has_forced) {
-                st |= DSPARK_STATUS_INFEASIBLE;
-            } else {
-                budget = b_forced;
-                if (budget > 0) {
-                    Pbud = sm.d_fP;
-                    cstar = sm.d_fC;
-                }
-                // theta at the forced budget: the entry covering M = B + budget
-                const long long Mv = (long long)B + budget;
-                int lo = 0, hi = n;  // first index with M > Mv (1-D) / M >= Mv (additive)
-                while (lo < hi) {
-                    const int mid = (lo + hi) >> 1;
-                    const long long Mm = __ldg(c.M + mid);
-                    const bool right = (c.kind == DSPARK_COST_SPS_1D) ? (Mm > Mv) : (Mm >= Mv);
-                    if (right) hi = mid;
-                    else lo = mid + 1;
-                }
-                const double tau = tau_of(B, (long long)Pbud);
-                if (c.kind == DSPARK_COST_SPS_1D) {
-                    const double sps = __ldg(c.val + (lo > 0 ? lo - 1 : 0));
-                    if (sps > 0.0 && isfinite(sps)) theta_out = __dmul_rn(tau, sps);
-                } else if (lo < n) {
-                    const double Tm = __dadd_rn(fixed_cost, __ldg(c.val + lo));
-                    if (Tm > 0.0 && isfinite(Tm)) theta_out = __ddiv_rn(tau, Tm);
-                }
-            }
-            if (st) flag(a.status, st);
-            sm.cstar = cstar;
-            sm.budget_s = budget;
-            a.budget[0] = budget;
-            a.tau_theta[0] = tau_of(B, (long long)Pbud);
-            a.tau_theta[1] = theta_out;
-        }
-    }
+    if (warp == 0 && lane == 0)
+        write_decision(a, sm, my_key, my_b, my_P, my_C, any_bad_cost, bad_table, forced,
+                       b_forced, [&](int budget, double tau) -> double {
+                           // theta at the forced budget: the entry covering M = B + budget
+                           const long long Mv = (long long)B + budget;
+                           int lo = 0, hi = n;  // first M > Mv (1-D) / M >= Mv (additive)
+                           while (lo < hi) {
+                               const int mid = (lo + hi) >> 1;
+                               const long long Mm = __ldg(c.M + mid);
+                               const bool right = (c.kind == DSPARK_COST_SPS_1D) ? (Mm > Mv) : (Mm >= Mv);
+                               if (right) hi = mid;
+                               else lo = mid + 1;
+                           }
+                           if (c.kind == DSPARK_COST_SPS_1D) {
+                               const double sps = __ldg(c.val + (lo > 0 ? lo - 1 : 0));
+                               return sps > 0.0 && isfinite(sps) ? __dmul_rn(tau, sps) : 0.0;
+                           }
+                           if (lo >= n) return 0.0;
+                           const double Tm = __dadd_rn(fixed_cost, __ldg(c.val + lo));
+                           return Tm > 0.0 && isfinite(Tm) ? __ddiv_rn(tau, Tm) : 0.0;
+                       });
     __syncthreads();
 
     // (5) lengths, tier-filled budget, pack (its inputs from global memory)
@@ -2706,74 +2728,23 @@ __global__ void __launch_bounds__(kSelThreads, 1) interp_select_kernel(PlanArgs 
             }
         }
     } else {
-        // (4) crowded bins: the budgets left (then the forced budget) take
-        // the threshold slots 32 at a time
-        const int T = K + (b_forced >= 1 ? 1 : 0);
-        for (int base = 0; base < T; base += 32) {  // uniform
-            const int nc = min(32, T - base);
-            if (tid < kHistBins / 32) sm.binmask[tid] = 0u;
-            if (tid == 0) sm.n_gather = 0;
-            __syncthreads();
-            if (warp < nc) {
-                const int item = base + warp;
-                slot_setup(sm, warp, lane, item < K ? list[item] : b_forced, a.status);
-                if (lane == 0) sm.d_item[warp] = item < K ? 0 : -1;
-            }
-            __syncthreads();
-            slot_thresholds<IPT>(a, sm, key, r0, k0, nc);
-            if (warp == 0 && lane < nc) {
-                const int b = sm.cand_b[lane];
-                const unsigned long long P = b >= 1 ? sm.P[lane] : 0ull;
-                const unsigned long long C = b >= 1 ? sm.cthr[lane] : kNoComposite;
-                if (sm.d_item[lane] >= 0) {
-                    evaluate(b, P, C);
-                } else {
-                    sm.d_fP = P;
-                    sm.d_fC = C;
-                }
-            }
-            __syncthreads();
-        }
+        // (4) crowded bins: the budgets left, then the forced budget
+        threshold_rounds<IPT>(
+            a, sm, key, r0, k0, K, b_forced, [&](int i) { return list[i]; },
+            [&](int, int b, unsigned long long P, unsigned long long C) { evaluate(b, P, C); });
     }
 
-    // the first maximiser over the block, in warp 0
+    // the first maximiser over the block (in warp 0), the decision
     const bool any_bad_cost = block_first_max(sm, my_key, my_b, my_P, my_C, my_bad_cost);
-    if (warp == 0 && lane == 0) {
-        int st = (any_bad_cost || bad_table) ? DSPARK_STATUS_BAD_COST : 0;
-        int budget = 0;
-        unsigned long long Pbud = 0ull, cstar = kNoComposite;
-        double theta_out = 0.0;
-        if (forced < 0) {
-            if (bad_table || my_b == 0x7FFFFFFF) {
-                st |= DSPARK_STATUS_INFEASIBLE;
-            } else {
-                budget = my_b;
-                theta_out = __longlong_as_double(my_key);
-                if (budget > 0) {
-                    Pbud = my_P;
-                    cstar = my_C;
-                }
-            }
-        } else if (!has_forced) {
-            st |= DSPARK_STATUS_INFEASIBLE;
-        } else {
-            budget = b_forced;
-            if (budget > 0) {
-                Pbud = sm.d_fP;
-                cstar = sm.d_fC;
-            }
-            // theta at the forced budget: the cost interpolated at M = B + budget
-            double Ti;
-            if (interp_cost_staged(sM, c.val, n, (long long)B + budget, fixed_cost, Ti))
-                theta_out = __ddiv_rn(tau_of(B, (long long)Pbud), Ti);
-        }
-        if (st) flag(a.status, st);
-        sm.cstar = cstar;
-        sm.budget_s = budget;
-        a.budget[0] = budget;
-        a.tau_theta[0] = tau_of(B, (long long)Pbud);
-        a.tau_theta[1] = theta_out;
-    }
+    if (warp == 0 && lane == 0)
+        write_decision(a, sm, my_key, my_b, my_P, my_C, any_bad_cost, bad_table, forced,
+                       b_forced, [&](int budget, double tau) -> double {
+                           // theta at the forced budget: the cost interpolated at M = B + budget
+                           double Ti;
+                           return interp_cost_staged(sM, c.val, n, (long long)B + budget,
+                                                     fixed_cost, Ti)
+                                      ? __ddiv_rn(tau, Ti) : 0.0;
+                       });
     __syncthreads();
 
     // (5) lengths, tier-filled budget, pack (its inputs from global memory)
