@@ -266,15 +266,16 @@ __device__ __forceinline__ void write_argmax(const FinalArgs &a, int rows, long 
         a.argmax[row] = row_argmax(a.partial, row, cpr, per, a.max_rows, a.status);
 }
 
-// BuildOutTokens and FinalizeAcceptLens for request r (lane 0 writes the scalars)
+// BuildOutTokens and FinalizeAcceptLens for request r (lane 0 writes the
+// scalars; pre = prefix_lens[r], fetched by lane 0 before the dependency wait)
 __device__ __forceinline__ void finish(const FinalArgs &a, int r, int lane, int correct, int bon,
-                                       int dj) {
+                                       int dj, int pre) {
     const int g = a.gamma;
     if (lane == 0) {
         a.num_acc[r] = correct;
         a.bonus[r] = bon;
         a.commit[r] = correct + 1;
-        if (a.new_seq) a.new_seq[r] = a.prefix[r] + correct + 1;
+        if (a.new_seq) a.new_seq[r] = pre + correct + 1;
     }
     if (lane < g) a.out[(size_t)r * (g + 1) + lane] = (lane == correct) ? bon : dj;
     else if (lane == g) a.out[(size_t)r * (g + 1) + g] = (g == correct) ? bon : -1;
@@ -286,10 +287,11 @@ __global__ void __launch_bounds__(kFinalWarps * 32) greedy_finalize_kernel(Final
     pdl_trigger();
     const int rq = blockIdx.x * kFinalWarps + (threadIdx.x >> 5);
     const int ln = threadIdx.x & 31;
-    // drafts are step inputs, and cu_seqlens was written before any argmax
-    // CTA passed its wait (which precedes this grid's launch): fetch them
-    // while the argmax finishes, from L2
+    // drafts and prefix lengths are step inputs, and cu_seqlens was written
+    // before any argmax CTA passed its wait (which precedes this grid's
+    // launch): fetch them while the argmax finishes, from L2
     const int dj = (rq < a.B && ln < a.gamma) ? __ldg(a.draft + (size_t)rq * a.gamma + ln) : -1;
+    const int pre = (a.new_seq && rq < a.B && ln == 0) ? __ldg(a.prefix + rq) : 0;
     const int rows = a.rows_dev ? min(max(__ldcg(a.rows_dev), 0), a.max_rows) : a.rows_host;
     const int lo = rq < a.B ? __ldcg(a.cu + rq) : 0, hi = rq < a.B ? __ldcg(a.cu + rq + 1) : 0;
     pdl_wait();
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(kFinalWarps * 32) greedy_finalize_kernel(Final
             a.num_acc[r] = 0;
             a.bonus[r] = -1;
             a.commit[r] = 0;
-            if (a.new_seq) a.new_seq[r] = a.prefix[r];
+            if (a.new_seq) a.new_seq[r] = pre;
             flag(a.status, DSPARK_STATUS_BAD_LEN);
         }
         if (lane < g) a.out[(size_t)r * (g + 1) + lane] = dj;
@@ -324,7 +326,7 @@ __global__ void __launch_bounds__(kFinalWarps * 32) greedy_finalize_kernel(Final
     const unsigned mism = __ballot_sync(kFullMask, lane < L - 1 && am != dj);
     const int correct = mism ? __ffs(mism) - 1 : L - 1;
     const int bon = __shfl_sync(kFullMask, am, correct);
-    finish(a, r, lane, correct, bon, dj);
+    finish(a, r, lane, correct, bon, dj, pre);
 }
 
 __global__ void __launch_bounds__(kFinalWarps * 32) cap_finalize_kernel(FinalArgs a) {
@@ -333,6 +335,7 @@ __global__ void __launch_bounds__(kFinalWarps * 32) cap_finalize_kernel(FinalArg
     const int rq = blockIdx.x * kFinalWarps + (threadIdx.x >> 5);
     const int ln = threadIdx.x & 31;
     const int dj0 = (rq < a.B && ln < a.gamma) ? __ldg(a.draft + (size_t)rq * a.gamma + ln) : -1;
+    const int pre = (a.new_seq && rq < a.B && ln == 0) ? __ldg(a.prefix + rq) : 0;
     const int len0 = rq < a.B ? __ldcg(a.lens + rq) : 0;  // written before the argmax's wait
     pdl_wait();
     const int rows = a.rows_host;
@@ -365,7 +368,7 @@ __global__ void __launch_bounds__(kFinalWarps * 32) cap_finalize_kernel(FinalArg
         }
         const int capped = min(raw, len - 1);
         const int bon = __shfl_sync(kFullMask, am, capped);
-        finish(a, r, lane, capped, bon, dj);
+        finish(a, r, lane, capped, bon, dj, pre);
         if (lane == 0) {
             a.ceiling[r] = raw;
             atomicAdd(&sums[0], capped + 1);
