@@ -1523,93 +1523,69 @@ __device__ __forceinline__ void select_pack(const PlanArgs &a, SelSmem &sm, bool
 
 // Step (3) of select_kernel, run by warp 0: theta at every candidate budget,
 // the first maximiser (or the forced budget) and the plan's scalar outputs.
-// Kept out of line so that the compiler schedules it on its own.
-__device__ __noinline__ void select_theta(const PlanArgs &a, SelSmem &sm, long long b_top,
-                                         int forced) {
-    // arguments into registers first (the output stores could alias them)
+// Lane j < n holds entry j's candidate and lane n the forced budget's slot;
+// every choice is a warp vote or a shuffle, so lane 0 only stores.
+__device__ __forceinline__ void select_theta(const PlanArgs &a, SelSmem &sm, long long b_top,
+                                             int forced) {
     const int lane = threadIdx.x & 31;
-    const int B = a.B, n = a.cost.n, kind = a.cost.kind;
-    const double bias = a.cost.bias, alpha = a.cost.alpha;
-    int32_t *budget_out = a.budget, *status = a.status;
-    double *tau_theta = a.tau_theta;
-    long long my_key = -1;
-    int my_b = 0x7FFFFFFF;
-    bool bad_cost = false;
-    if (lane < n) {
-        const int b = sm.cand_b[lane];
-        if (b >= 0) {
-            if (!sm.ok_s[lane]) {
-                bad_cost = true;
-            } else {
-                const double tau = tau_of(B, b == 0 ? 0 : (long long)sm.P[lane]);
-                const double theta = kind == DSPARK_COST_SPS_1D
-                                         ? __dmul_rn(tau, sm.val_s[lane])
-                                         : __ddiv_rn(tau, sm.div_s[lane]);
-                my_key = __double_as_longlong(theta);
-                my_b = b;
-            }
-        }
+    const int B = a.B, n = a.cost.n;
+    const bool sps = a.cost.kind == DSPARK_COST_SPS_1D;
+    const int b = lane <= n ? sm.cand_b[lane] : -1;  // slot n: -1 unless forced
+    const double tau = tau_of(B, b > 0 ? (long long)sm.P[lane] : 0);
+    const unsigned long long cthr = (lane <= n && b > 0) ? sm.cthr[lane] : kNoComposite;
+    // the entry whose theta the lane evaluates; for the forced budget the
+    // entry covering M = B + budget (1-D: the last M_j <= M, else the first
+    // entry; additive: the first M_j >= M, else none)
+    int e = lane < n ? lane : -1;
+    if (forced >= 0) {
+        const long long Mv = (long long)B + __shfl_sync(kFullMask, b, n);
+        const long long Mi = lane < n ? (long long)sm.M_s[lane] : 0;
+        const unsigned m = __ballot_sync(kFullMask, lane < n && (sps ? Mi <= Mv : Mi >= Mv));
+        const int jf = sps ? (m ? 31 - __clz((int)m) : 0) : __ffs((int)m) - 1;
+        if (lane == n) e = jf;
     }
+    const bool ok = e >= 0 && sm.ok_s[e] != 0;
+    double theta = 0.0;
+    if (b >= 0 && ok) theta = sps ? __dmul_rn(tau, sm.val_s[e]) : __ddiv_rn(tau, sm.div_s[e]);
+    const bool cand = lane < n && b >= 0 && ok;
+    const bool bad_cost = lane < n && b >= 0 && !ok;
     // first maximiser: theta >= 0, so its bits order like the values;
     // +1 leaves 0 for "no candidate"; ties go to the smaller budget
+    int my_b;
+    long long my_key;
     {
-        const unsigned long long uk = my_key >= 0 ? (unsigned long long)my_key + 1ull : 0ull;
+        const unsigned long long uk = cand ? (unsigned long long)__double_as_longlong(theta) + 1ull : 0ull;
         const unsigned hi = (unsigned)(uk >> 32), lo = (unsigned)uk;
         const unsigned mhi = __reduce_max_sync(kFullMask, hi);
         const unsigned mlo = __reduce_max_sync(kFullMask, hi == mhi ? lo : 0u);
-        const bool top = hi == mhi && lo == mlo;
-        my_b = (int)__reduce_min_sync(kFullMask, top ? (unsigned)my_b : 0x7FFFFFFFu);
+        const bool top = cand && hi == mhi && lo == mlo;
+        my_b = (int)__reduce_min_sync(kFullMask, top ? (unsigned)b : 0x7FFFFFFFu);
         my_key = (long long)((((unsigned long long)mhi << 32) | mlo) - 1ull);
     }
     const bool any_bad_cost = __any_sync(kFullMask, bad_cost);
+    const bool bad_table = sm.bad_table != 0;
+    int slot = -1;  // -1: infeasible
+    if (forced < 0) {
+        if (!bad_table && my_b != 0x7FFFFFFF)  // the first entry with the chosen budget
+            slot = __ffs((int)__ballot_sync(kFullMask, lane < n && b == my_b)) - 1;
+    } else if (!bad_table && b_top >= 0) {
+        slot = n;
+    }
+    const int src = slot < 0 ? 0 : slot;
+    const int budget = slot < 0 ? 0 : __shfl_sync(kFullMask, b, src);
+    const double tau_s = __shfl_sync(kFullMask, tau, src);
+    const unsigned long long cthr_s = __shfl_sync(kFullMask, cthr, src);
+    const double theta_f = __shfl_sync(kFullMask, theta, n);
     if (lane == 0) {
-        const bool bad_table = sm.bad_table != 0;
         int st = (any_bad_cost || bad_table) ? DSPARK_STATUS_BAD_COST : 0;
-        int budget = 0, slot = -1;
-        double theta_out = 0.0;
-        if (forced < 0) {
-            if (bad_table || my_b == 0x7FFFFFFF) {
-                st |= DSPARK_STATUS_INFEASIBLE;
-            } else {
-                budget = my_b;
-                theta_out = __longlong_as_double(my_key);
-                for (int j = 0; j < n; ++j)
-                    if (sm.cand_b[j] == budget) {
-                        slot = j;
-                        break;
-                    }
-            }
-        } else if (bad_table || b_top < 0) {
-            st |= DSPARK_STATUS_INFEASIBLE;
-        } else {
-            budget = sm.cand_b[n];
-            slot = n;
-            const double tau = tau_of(B, budget == 0 ? 0 : (long long)sm.P[slot]);
-            // theta at the forced budget: the entry covering M = B + budget
-            const long long Mv = (long long)B + budget;
-            int j = -1;
-            if (kind == DSPARK_COST_SPS_1D) {
-                for (int i = 0; i < n; ++i)
-                    if ((long long)sm.M_s[i] <= Mv) j = i;
-                if (j < 0) j = 0;
-                const double sps = sm.val_s[j];
-                if (sps > 0.0 && isfinite(sps)) theta_out = __dmul_rn(tau, sps);
-            } else {
-                for (int i = n - 1; i >= 0; --i)
-                    if ((long long)sm.M_s[i] >= Mv) j = i;
-                if (j >= 0) {
-                    const double Tm = __dadd_rn(__dadd_rn(bias, alpha), sm.val_s[j]);
-                    if (Tm > 0.0 && isfinite(Tm)) theta_out = __ddiv_rn(tau, Tm);
-                }
-            }
-        }
-        const bool chosen = budget > 0 && slot >= 0;
-        if (st) flag(status, st);
-        sm.cstar = chosen ? sm.cthr[slot] : kNoComposite;
+        if (slot < 0) st |= DSPARK_STATUS_INFEASIBLE;
+        if (st) flag(a.status, st);
+        const bool chosen = budget > 0;  // and slot >= 0
+        sm.cstar = chosen ? cthr_s : kNoComposite;
         sm.budget_s = budget;
-        budget_out[0] = budget;
-        tau_theta[0] = tau_of(B, chosen ? (long long)sm.P[slot] : 0);
-        tau_theta[1] = theta_out;
+        a.budget[0] = budget;
+        a.tau_theta[0] = slot < 0 ? tau_of(B, 0) : tau_s;
+        a.tau_theta[1] = slot < 0 ? 0.0 : (forced < 0 ? __longlong_as_double(my_key) : theta_f);
     }
 }
 
