@@ -1450,9 +1450,21 @@ __device__ void radix_thresholds(const PlanArgs &a, SelSmem &sm, const uint32_t 
 // prefix[r]+j, rounded up to the smallest graph tier with pad rows
 // (id 0, position 0, request -1, source -1).  A block scan gives each
 // request its first row; then each thread writes whole packed rows (stores
-// coalesced across the warp), reading anchor / prefix / draft from the copy
-// staged in shared memory before the dependency wait (when B*(gamma+2) <=
-// kStage).  The planner's lengths are always in [1, gamma+1].
+// coalesced across the warp), reading anchor / prefix / draft from their
+// copy in shared memory, started before the dependency wait (when
+// B*(gamma+2) <= kStage).  The planner's lengths are always in [1, gamma+1].
+//
+// The staging copies (stage_async) are 4-byte cp.async copies global ->
+// shared: issuing one does not hold the thread, so the staging's loads run
+// past the dependency wait instead of in front of it; each thread waits for
+// its own copies (stage_wait) before the barrier that precedes the pack.
+__device__ __forceinline__ void stage_async(int32_t *dst, const int32_t *src) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void stage_wait() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ void select_pack(const PlanArgs &a, SelSmem &sm, bool staged) {
     const int tid = threadIdx.x;
     const int B = a.B, G = a.gamma, capacity = a.pk.capacity;
@@ -1855,6 +1867,7 @@ __device__ __forceinline__ void select_finish(const PlanArgs &a, SelSmem &sm,
         if (tid == 0) *a.exec_budget = aligned_budget(a.align, sm.budget_s, total, b_top);
     }
     if (a.pk.on) {
+        if (staged) stage_wait();
         __syncthreads();
         select_pack(a, sm, staged);
     }
@@ -1906,16 +1919,16 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(PlanArgs a) {
     }
     if (tid < kHistBins / 32) sm.binmask[tid] = 0u;
     if (tid == 0) sm.n_gather = 0;
-    // the fused pack's step inputs are not written by the planner: stage
-    // them now, while the survivals are computed
+    // the fused pack's step inputs are not written by the planner: start
+    // their copies now, while the survivals are computed
     const bool staged = a.pk.on && (long long)B * (G + 2) <= kStage;
     if (staged) {
         for (int i = tid; i < B; i += kSelThreads) {
-            sm.stage[i] = __ldg(a.pk.anchor + i);
-            sm.stage[B + i] = __ldg(a.pk.prefix + i);
+            stage_async(sm.stage + i, a.pk.anchor + i);
+            stage_async(sm.stage + B + i, a.pk.prefix + i);
         }
         for (int i = tid; i < N; i += kSelThreads)
-            if (in_bounds(2 * B + i, kStage, a.status)) sm.stage[2 * B + i] = __ldg(a.pk.draft + i);
+            if (in_bounds(2 * B + i, kStage, a.status)) stage_async(sm.stage + 2 * B + i, a.pk.draft + i);
     }
     pdl_wait();  // survivals and bins come from survival_kernel
     const int forced = resolve_forced(a);
