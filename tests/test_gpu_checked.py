@@ -28,7 +28,9 @@ def test_checked_build_matches_and_flags_nothing(tmp_path):
     from confidence_scheduled_speculative_gb300 import build as _b
     import checked_scenarios
 
-    assert not api.dspark_checked_build()
+    if api.dspark_checked_build():
+        pytest.skip("this process already runs the checked library (DSPARK_CHECKED=1): "
+                    "there is no normal build to compare with")
     _b.build(checked=True)
     path = str(tmp_path / "checked.npz")
     env = dict(os.environ, DSPARK_CHECKED="1")
