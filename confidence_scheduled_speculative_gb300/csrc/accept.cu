@@ -233,10 +233,19 @@ struct FinalArgs {
     int32_t *argmax, *num_acc, *bonus, *commit, *new_seq, *out, *ceiling, *totals, *status;
 };
 
-__device__ __forceinline__ int row_argmax(const Partial *partial, int row, long long cpr,
-                                          long long per, int max_rows, int32_t *status) {
+// The argmax CTAs [c_lo, c_hi] whose ranges hold a piece of row `row`
+// (integer divisions only: the finalize kernels take them before their
+// dependency wait).
+__device__ __forceinline__ void row_ctas(int row, long long cpr, long long per, int &c_lo,
+                                         int &c_hi) {
     const long long q_first = (long long)row * cpr;
-    const int c_lo = (int)div_nonneg(q_first, per), c_hi = (int)div_nonneg(q_first + cpr - 1, per);
+    c_lo = (int)div_nonneg(q_first, per);
+    c_hi = (int)div_nonneg(q_first + cpr - 1, per);
+}
+
+// The argmax of row `row` from the partials of CTAs [c_lo, c_hi].
+__device__ __forceinline__ int row_argmax_in(const Partial *partial, int row, int c_lo, int c_hi,
+                                             int max_rows, int32_t *status) {
     if (!in_bounds(c_hi + row, partial_slots(max_rows), status)) return 0;
     // the first two partials (a row usually spans one or two CTAs) are
     // loaded together
@@ -256,6 +265,13 @@ __device__ __forceinline__ int row_argmax(const Partial *partial, int row, long 
         }
     }
     return bi;
+}
+
+__device__ __forceinline__ int row_argmax(const Partial *partial, int row, long long cpr,
+                                          long long per, int max_rows, int32_t *status) {
+    int c_lo, c_hi;
+    row_ctas(row, cpr, per, c_lo, c_hi);
+    return row_argmax_in(partial, row, c_lo, c_hi, max_rows, status);
 }
 
 // per-row argmax output (every row < rows), grid-stride over all threads
@@ -294,7 +310,6 @@ __global__ void __launch_bounds__(kFinalWarps * 32) greedy_finalize_kernel(Final
     const int pre = (a.new_seq && rq < a.B && ln == 0) ? __ldg(a.prefix + rq) : 0;
     const int rows = a.rows_dev ? min(max(__ldcg(a.rows_dev), 0), a.max_rows) : a.rows_host;
     const int lo = rq < a.B ? __ldcg(a.cu + rq) : 0, hi = rq < a.B ? __ldcg(a.cu + rq + 1) : 0;
-    pdl_wait();
     const long long cpr = (a.V + a.epc - 1) / a.epc;
     const long long W = (long long)rows * cpr;
     const long long per = div_nonneg(W + a.grid - 1, a.grid);
@@ -303,9 +318,13 @@ __global__ void __launch_bounds__(kFinalWarps * 32) greedy_finalize_kernel(Final
     const int g = a.gamma;
     const int L = hi - lo;
     const bool valid = r < a.B && lo >= 0 && hi <= rows && L >= 1 && L <= g + 1;
+    const bool mine = valid && lane < L;  // this lane's row: lo + lane
+    int c_lo = 0, c_hi = 0;
+    if (mine) row_ctas(lo + lane, cpr, per, c_lo, c_hi);
+    pdl_wait();
     // the request's row argmaxes first, so that their partial loads and the
     // argmax output pass's are in flight together
-    const int am = valid && lane < L ? row_argmax(a.partial, lo + lane, cpr, per, a.max_rows, a.status) : 0;
+    const int am = mine ? row_argmax_in(a.partial, lo + lane, c_lo, c_hi, a.max_rows, a.status) : 0;
     write_argmax(a, rows, cpr, per);
 
     if (r >= a.B) return;  // warp-uniform
@@ -337,7 +356,6 @@ __global__ void __launch_bounds__(kFinalWarps * 32) cap_finalize_kernel(FinalArg
     const int dj0 = (rq < a.B && ln < a.gamma) ? __ldg(a.draft + (size_t)rq * a.gamma + ln) : -1;
     const int pre = (a.new_seq && rq < a.B && ln == 0) ? __ldg(a.prefix + rq) : 0;
     const int len0 = rq < a.B ? __ldcg(a.lens + rq) : 0;  // written before the argmax's wait
-    pdl_wait();
     const int rows = a.rows_host;
     const long long cpr = (a.V + a.epc - 1) / a.epc;
     const long long W = (long long)rows * cpr;
@@ -345,11 +363,15 @@ __global__ void __launch_bounds__(kFinalWarps * 32) cap_finalize_kernel(FinalArg
     const int lane = ln;
     const int r = rq;
     const int g = a.gamma;
+    const bool mine = r < a.B && lane <= g;  // this lane's row: r*(gamma+1) + lane
+    int c_lo = 0, c_hi = 0;
+    if (mine) row_ctas(r * (g + 1) + lane, cpr, per, c_lo, c_hi);
+    pdl_wait();
     // the request's row argmaxes first (their loads in flight with the
     // argmax output pass's)
-    const int am0 = r < a.B && lane <= g
-                        ? row_argmax(a.partial, r * (g + 1) + lane, cpr, per, a.max_rows, a.status)
-                        : 0;
+    const int am0 = mine ? row_argmax_in(a.partial, r * (g + 1) + lane, c_lo, c_hi, a.max_rows,
+                                         a.status)
+                         : 0;
     write_argmax(a, rows, cpr, per);
     if (threadIdx.x == 0) sums[0] = sums[1] = 0;
     __syncthreads();

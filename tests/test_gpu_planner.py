@@ -384,13 +384,28 @@ def _select_case(name):
         z = np.tile(rng.normal(2.0, 1.0, 16).astype(np.float32), (1000, 1))
         M = np.linspace(1000, 16000, 31).astype(np.int32)
         return dict(base, B=1000, gamma=16, z=z, M=M, val=2e-4 * M, forced=4321)
+    # the forced budget's theta from the entry covering M = B + budget
+    z = rng.normal(1.5, 1.0, (256, 16)).astype(np.float32)
+    if name == "forced_below_first_sample":  # 1-D: every sample above B + 100 (entry 0)
+        return dict(base, B=256, gamma=16, z=z, kind=0,
+                    M=np.array([3256, 3756, 4256], np.int32), val=np.array([500.0, 400.0, 300.0]),
+                    forced=100)
+    if name == "forced_invalid_sps":  # 1-D: the covering entry's SPS is 0 (theta 0, BAD_COST)
+        return dict(base, B=256, gamma=16, z=z, kind=0,
+                    M=np.array([256, 1000, 3000], np.int32), val=np.array([500.0, 0.0, 300.0]),
+                    forced=1500)
+    if name == "forced_invalid_additive":  # additive: the covering tier's cost is negative
+        return dict(base, B=256, gamma=16, z=z,
+                    val=np.array([0.512, -10.0, 2.048, 4.096, 8.192]), forced=200)
     raise KeyError(name)
 
 
 @pytest.mark.parametrize("name", ["all_ones", "all_ones_forced", "half_saturated",
                                   "identical_requests", "identical_forced", "large_spread",
                                   "sixteen_entries", "thirty_one_entries",
-                                  "thirty_one_entries_forced", "thirty_one_entries_ties"])
+                                  "thirty_one_entries_forced", "thirty_one_entries_ties",
+                                  "forced_below_first_sample", "forced_invalid_sps",
+                                  "forced_invalid_additive"])
 def test_plan_select_bins(dev, orc, name):
     P = _select_case(name)
     g = _gpu_plan(dev, P)
