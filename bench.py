@@ -1027,7 +1027,7 @@ def run_ours(args):
         from confidence_scheduled_speculative_gb300 import api as _api
         vs.status.zero_()
         # the same tier costs at every 128 rows: 31 entries, the select
-        # path's largest table; at every 64 rows: 61 entries, the rank path
+        # path's largest table; at every 64 rows: 61 entries, the dense path
         dM = torch.arange(256, 4097, 128, dtype=torch.int32, device=dev)
         dense = (dM, 0.002 * dM.to(torch.float64))
         dM2 = torch.arange(256, 4097, 64, dtype=torch.int32, device=dev)

@@ -69,18 +69,6 @@ constexpr uint32_t kDroppedKey = 0x07FFFFFFu;
 constexpr int kMinExpBiased = 113;          // 2^-14: the smallest allowed eps
 constexpr int kNoRank = 0x7FFFFFFF;
 
-// Cost tables with at most this many entries take the sparse path: every
-// CTA adds the survivals ranked below each candidate budget into one
-// accumulator per candidate, so no prefix scan is needed.
-constexpr int kMaxSparse = 64;
-
-// Dense cost tables (more than kMaxSparse entries, not interpolated) of at
-// most this many entries are staged in the rank kernel's shared memory
-// before its dependency wait (the 1-D SPS table sampled at every M of a
-// B=256, gamma=16 batch has 4097 entries), and the last CTA keeps the prefix
-// sums there too.
-constexpr int kTabStage = 4608;
-
 // The select path ranks candidates inside the top-11-bit bins of their keys:
 // survival_kernel counts the kept keys (and adds their fixed-point
 // survivals) per bin, select_kernel reads and clears the bins.
@@ -90,16 +78,14 @@ constexpr int kHistBins = 2048;              // kept keys use bins 0..1792
 // Planner scratch in the caller's workspace.
 struct PlanScratch {
     unsigned int ticket;  // CTAs of rank_kernel done
-    unsigned int pad0;
-    unsigned long long acc[kMaxSparse + 1];  // sparse path: P at each candidate (+ forced budget)
-    unsigned int pad1[124];
-    // select path: kept keys per top bin and their fixed-point survival sums;
-    // zero between calls (select_kernel clears what survival_kernel added)
+    unsigned int pad[3];
+    // single-CTA paths: kept keys per top bin and their fixed-point survival
+    // sums; zero between calls (the planner kernel clears what
+    // survival_kernel added)
     unsigned int hcount[kHistBins];
     unsigned long long hsum[kHistBins];
-    // followed by: int32 rank[N] | int64 sorted[N] | int64 prefix[N+1] |
-    // int32 count[B][kMaxSparse+1] (sparse path: selected candidates of
-    // request r at each candidate budget)
+    // followed by the rank path's int32 rank[N] | int64 sorted[N] |
+    // int64 prefix[N+1]
 };
 static_assert(offsetof(PlanScratch, hcount) % 16 == 0 && offsetof(PlanScratch, hsum) % 16 == 0,
               "histogram rows are read as 16-byte vectors");
@@ -111,9 +97,6 @@ __host__ __device__ inline size_t plan_sorted_offset(int N) {
 __host__ __device__ inline size_t plan_prefix_offset(int N) {
     return plan_sorted_offset(N) + (size_t)N * 8;
 }
-__host__ __device__ inline size_t plan_count_offset(int N) {
-    return (plan_prefix_offset(N) + (size_t)(N + 1) * 8 + 15) & ~size_t(15);
-}
 // Between the passes of one call (dspark_plan_ex): the lagged pass's
 // budget, the tier-filled budget, and the lengths / tau-theta / survivals a
 // pass computes that the caller does not receive.
@@ -122,7 +105,7 @@ struct PassScratch {
     double pass_tau_theta[2];
 };
 __host__ __device__ inline size_t plan_pass_offset(int B, int N) {
-    return (plan_count_offset(N) + (size_t)B * (kMaxSparse + 1) * 4 + 255) & ~size_t(255);
+    return (plan_prefix_offset(N) + (size_t)(N + 1) * 8 + 255) & ~size_t(255);
 }
 __host__ __device__ inline size_t plan_pass_lens_offset(int B, int N) {
     return plan_pass_offset(B, N) + 256;
@@ -167,17 +150,11 @@ survival_kernel(const float *__restrict__ z, const float *__restrict__ T, int B,
     // table then run after every earlier kernel has completed)
     pdl_wait();
     pdl_trigger();
-    if (blockIdx.x == 0) {  // reset the rank kernel's ticket and accumulators
-        for (int j = threadIdx.x; j <= kMaxSparse; j += blockDim.x) scratch->acc[j] = 0ull;
-        if (threadIdx.x == 0) scratch->ticket = 0u;
-    }
+    // the rank kernel's ticket starts at zero (only that kernel uses it)
+    if (!bin_keys && blockIdx.x == 0 && threadIdx.x == 0) scratch->ticket = 0u;
     const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (r >= B) return;  // warp-uniform
-    {   // reset this request's per-candidate counts (sparse path of rank_kernel)
-        int32_t *cnt = scratch_at<int32_t>(scratch, plan_count_offset(B * gamma)) + (size_t)r * (kMaxSparse + 1);
-        for (int j = lane; j <= kMaxSparse; j += 32) cnt[j] = 0;
-    }
     const bool active = lane < gamma;
     // a request whose pool slot was reused since its confidences were
     // recorded falls back to survivals of 1 ([AVS] §三, req_generation)
@@ -333,15 +310,10 @@ struct RankSmem {
     long long best_key[kRankWarps];
     int best_b[kRankWarps];
     long long best_P[kRankWarps];                // P at each warp's best budget
-    int cand_b[kMaxSparse + 1];                 // candidate budget of each table entry (-1: none)
-    unsigned long long acc_s[kMaxSparse + 1];   // this CTA's part of each candidate's prefix
-    double val_s[kMaxSparse];                   // sparse path and small interpolated tables: values
-    int M_s[kMaxSparse];                        // small interpolated tables: samples
-    float v32_s[kMaxSparse];                    // small interpolated tables: values as floats
     float fixed32;                              // bias + alpha as a float
     double fixed_cost;                          // bias + alpha
-    int itab_bad;                               // interpolated table: samples out of order
-    int budget, last, n_kept, sparse, forced;
+    int order_bad;                              // interpolated table: samples out of order
+    int budget, last, n_kept, forced;
     unsigned int theta_floor;  // interpolated table: a lower bound of the largest theta (float bits)
     int n_icand;               // interpolated table: budgets left for the fp64 definition
     int icand_b[kRankThreads], icand_seg[kRankThreads];
@@ -355,41 +327,15 @@ __host__ __device__ inline int run_stride(int P2) { return P2 + 1; }
 
 __device__ void finish_plan(const PlanArgs &a, RankSmem &sm);
 
-// Dynamic shared memory of rank_kernel: RankSmem | region R | table stage.
-// R holds the keys while the CTAs rank; the last CTA then reuses it for the
-// prefix sums P[0..N] of a dense table (int64) or, for an interpolated
-// table, for the float tau of every budget.  The stage holds a dense
-// table's samples, values and values as floats (kTabStage entries at most).
+// Dynamic shared memory of rank_kernel: RankSmem | region R.  R holds the
+// keys while the CTAs rank; the last CTA then reuses it for the prefix sums
+// P[0..N] (int64) of a table that is not interpolated or, for an
+// interpolated table, for the float tau of every budget.
 __host__ __device__ inline size_t rank_head_bytes() { return (sizeof(RankSmem) + 15) & ~size_t(15); }
-__host__ __device__ inline bool dense_table(int kind, int n) {
-    return kind != DSPARK_COST_ADDITIVE_INTERP && n > kMaxSparse;
-}
-__host__ __device__ inline bool staged_table(int kind, int n) {
-    return dense_table(kind, n) && n <= kTabStage;
-}
-__host__ __device__ inline size_t rank_region_bytes(int B, int S, int N, int kind, int n) {
+__host__ __device__ inline size_t rank_region_bytes(int B, int S, int N, int kind) {
     size_t r = (size_t)4 * B * S;
-    if (dense_table(kind, n) && (size_t)8 * (N + 1) > r) r = (size_t)8 * (N + 1);
+    if (kind != DSPARK_COST_ADDITIVE_INTERP && (size_t)8 * (N + 1) > r) r = (size_t)8 * (N + 1);
     return (r + 15) & ~size_t(15);
-}
-// stage: each entry's range of budgets [lo, hi] (int2; before the clip to
-// the largest in-range budget) | its value as a float
-__host__ __device__ inline size_t stage_f32_offset(int n) { return (size_t)8 * n; }
-__host__ __device__ inline size_t rank_stage_bytes(int kind, int n) {
-    return staged_table(kind, n) ? ((stage_f32_offset(n) + (size_t)4 * n + 15) & ~size_t(15)) : 0;
-}
-
-struct TableStage {
-    int2 *range;
-    float *f32;
-};
-
-// The staged dense table (see rank_kernel's prologue) of a CTA.
-__device__ __forceinline__ TableStage table_stage(unsigned char *smem, const PlanArgs &a) {
-    unsigned char *st = smem + rank_head_bytes() +
-                        rank_region_bytes(a.B, run_stride(a.P2), a.N, a.cost.kind, a.cost.n);
-    return TableStage{reinterpret_cast<int2 *>(st),
-                      reinterpret_cast<float *>(st + stage_f32_offset(a.cost.n))};
 }
 
 __device__ __forceinline__ int sat_int(long long x) {
@@ -431,15 +377,6 @@ __device__ __forceinline__ int2 entry_range_from(int kind, int n, int j, long lo
     return make_int2(sat_int(lo), sat_int(hi));
 }
 
-// The same with M_{j-1}, M_j, M_{j+1} loaded here.
-__device__ __forceinline__ int2 entry_range(const CostArgs &c, int j, long long Bl, bool &order_bad) {
-    const long long Mj = __ldg(c.M + j);
-    const long long Mp = j > 0 ? __ldg(c.M + j - 1) : 0;
-    const long long Mn = j < c.n - 1 ? __ldg(c.M + j + 1) : 0;
-    return entry_range_from(c.kind, c.n, j, Mp, Mj, Mn, Bl, order_bad);
-}
-
-
 __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     RankSmem &sm = *reinterpret_cast<RankSmem *>(smem_raw);
@@ -448,36 +385,12 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
     const int B = a.B, G = a.gamma, N = a.N, P2 = a.P2, S = run_stride(P2);
     const CostArgs &c = a.cost;
     bool order_bad = false;
-    if (staged_table(c.kind, c.n)) {
-        // a dense table into shared memory while the survivals are on the
-        // way (only the last CTA reads it): each entry's range of budgets b
-        // whose M = B + b looks the entry up (as entry_last_budget, before
-        // the clip to the in-range budgets) and its value as a float; the
-        // 64-bit range arithmetic and the fp64 -> fp32 conversions run here,
-        // off the critical path
-        const TableStage ts = table_stage(smem_raw, a);
-        for (int j = tid; j < c.n; j += kRankThreads) {
-            if (!in_bounds(j, kTabStage, a.status)) break;
-            ts.range[j] = entry_range(c, j, B, order_bad);
-            ts.f32[j] = (float)__ldg(c.val + j);
-        }
-    }
     int32_t *rank_out = scratch_at<int32_t>(a.scratch, plan_rank_offset());
     long long *sorted = scratch_at<long long>(a.scratch, plan_sorted_offset(N));
 
     pdl_trigger();
     // the cost table is written before the step: fetch it while waiting
-    int Mj = 0, Mprev = 0, Mnext = 0;
     const bool interp = c.kind == DSPARK_COST_ADDITIVE_INTERP;
-    const bool sparse = c.n <= kMaxSparse && !interp;
-    const bool itab = interp && c.n <= kMaxSparse;  // staged in shared memory
-    double vj = 0.0;
-    if ((sparse || itab) && tid < c.n) {
-        Mj = __ldg(c.M + tid);
-        Mprev = tid > 0 ? __ldg(c.M + tid - 1) : 0;
-        Mnext = tid < c.n - 1 ? __ldg(c.M + tid + 1) : 0;
-        vj = __ldg(c.val + tid);
-    }
     const int Mlast = __ldg(c.M + c.n - 1);
     // interpolated table: its order, checked while the survivals are on the way
     if (interp)
@@ -518,36 +431,18 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
     const int any_order_bad = __syncthreads_or(order_bad);
     long long b_top = n_kept;  // largest in-range budget
     if (c.kind != DSPARK_COST_SPS_1D) b_top = min(b_top, (long long)Mlast - (long long)B);
-    // (conversions from fp64 run on the fp64 unit: done once per entry here)
-    if (itab && tid < c.n) {
-        sm.M_s[tid] = Mj;
-        sm.val_s[tid] = vj;
-        sm.v32_s[tid] = (float)vj;
-    }
     // fp64 operations and conversions share GB300's small fp64 unit: once per CTA
     if (tid == 0) {
         sm.fixed_cost = __dadd_rn(c.bias, c.alpha);
         sm.fixed32 = (float)sm.fixed_cost;
-    }
-    if (sparse) {
-        if (tid < c.n) {
-            sm.cand_b[tid] = entry_last_budget(c, tid, Mj, Mprev, Mnext, B, b_top);
-            sm.val_s[tid] = vj;
-        }
-        if (tid == c.n) sm.cand_b[tid] = (forced >= 0 && b_top >= 0) ? (int)min((long long)forced, b_top) : -1;
-        if (tid <= c.n) sm.acc_s[tid] = 0ull;
-    }
-    if (tid == 0) {
-        sm.itab_bad = any_order_bad;
+        sm.order_bad = any_order_bad;
         sm.n_kept = n_kept;
         sm.b_top = b_top;
-        sm.sparse = sparse ? 1 : 0;
         sm.forced = forced;
     }
     __syncthreads();
 
     // ranks: one warp per candidate, lanes over the other requests' runs
-    unsigned long long my_acc[3] = {0ull, 0ull, 0ull};  // candidates lane, lane+32, lane+64
     // candidate x goes to CTA x mod grid (warps 0, 1, ... in turn), so every
     // SM of the grid gets its share even when there are few candidates
     const int nwarps = gridDim.x * kRankWarps;
@@ -586,30 +481,10 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
             rank_out[x] = rk;
             if (in_bounds(rk, N, a.status)) sorted[rk] = m;
         }
-        if (sparse) {
-            int32_t *cnt_r = scratch_at<int32_t>(a.scratch, plan_count_offset(N)) + (size_t)r * (kMaxSparse + 1);
-#pragma unroll
-            for (int t = 0; t < 3; ++t) {
-                const int j = lane + 32 * t;
-                if (j <= c.n && rk < sm.cand_b[j] && in_bounds(j, kMaxSparse + 1, a.status)) {
-                    my_acc[t] += (unsigned long long)m;
-                    atomicAdd(cnt_r + j, 1);
-                }
-            }
-        }
-    }
-    if (sparse) {
-#pragma unroll
-        for (int t = 0; t < 3; ++t) {
-            const int j = lane + 32 * t;
-            if (j <= c.n && my_acc[t] != 0ull) atomicAdd(&sm.acc_s[j], my_acc[t]);
-        }
-        __syncthreads();
-        if (tid <= c.n && sm.acc_s[tid] != 0ull) atomicAdd(&a.scratch->acc[tid], sm.acc_s[tid]);
     }
 
-    // the last CTA to finish completes the plan: the ranks, sorted values,
-    // counts and accumulator adds are made visible before the ticket
+    // the last CTA to finish completes the plan: the ranks and sorted values
+    // are made visible before the ticket
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -620,15 +495,7 @@ __global__ void __launch_bounds__(kRankThreads, 1) rank_kernel(PlanArgs a) {
     if (!sm.last) return;
     __threadfence();
     finish_plan(a, sm);
-    if (a.more_passes) {  // leave the ticket and accumulators at zero for the next pass
-        __syncthreads();
-        if (tid == 0) a.scratch->ticket = 0u;
-        for (int j = tid; j <= kMaxSparse; j += kRankThreads) a.scratch->acc[j] = 0ull;
-        if (c.n <= kMaxSparse) {
-            int32_t *cnt = scratch_at<int32_t>(a.scratch, plan_count_offset(N));
-            for (int i = tid; i < B * (kMaxSparse + 1); i += kRankThreads) cnt[i] = 0;
-        }
-    }
+    if (a.more_passes && tid == 0) a.scratch->ticket = 0u;  // zero for the next pass
 }
 
 // T(B, M) of the interpolated additive table at M = Mv <= M_{n-1}
@@ -810,14 +677,14 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
     const CostArgs &c = a.cost;
     const int n_kept = sm.n_kept;
     const long long b_top = sm.b_top;
-    const bool sparse = sm.sparse != 0;
     const int forced = sm.forced;
     const int32_t *rank_in = scratch_at<int32_t>(a.scratch, plan_rank_offset());
     const long long *sorted = scratch_at<long long>(a.scratch, plan_sorted_offset(a.N));
-    // the prefix sums: in shared memory (the key region) for a dense table,
-    // in the workspace for an interpolated one
+    // the prefix sums: in shared memory (the key region) for a table that
+    // is not interpolated, in the workspace for an interpolated one
     unsigned char *smem = reinterpret_cast<unsigned char *>(&sm);
-    const bool dense = dense_table(c.kind, c.n);
+    const bool interp = c.kind == DSPARK_COST_ADDITIVE_INTERP;
+    const bool dense = !interp;
     long long *P = dense ? reinterpret_cast<long long *>(smem + rank_head_bytes())
                          : scratch_at<long long>(a.scratch, plan_prefix_offset(a.N));
     // P holds N + 1 sums; the float taus of an interpolated table fill the
@@ -827,13 +694,13 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
         if (!in_bounds(b, nP, a.status)) return 0;
         return dense ? P[b] : __ldcg(P + b);
     };
-    auto dense_P = [&](long long b) -> long long {  // a dense table's P (shared memory)
+    auto dense_P = [&](long long b) -> long long {  // P in shared memory
         return in_bounds(b, nP, a.status) ? P[b] : 0;
     };
 
-    // (a) dense tables: P[i] = sum of the i largest survivals in units of
-    // 2^-37 (P[0] = 0), a blocked scan written to the workspace
-    if (!sparse) {
+    // (a) P[i] = sum of the i largest survivals in units of 2^-37 (P[0] =
+    // 0), a blocked scan
+    {
         const int per = (n_kept + kRankThreads - 1) / kRankThreads;  // <= kScanPer
         const int lo = tid * per, hi = min(lo + per, n_kept);
         // the thread's chunk (up to kScanReg in registers, all in flight at once)
@@ -850,7 +717,7 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
         // key region of shared memory (free once the ranks are out; it holds
         // B * (gamma + 1) >= n_kept + 1 words)
         float *tauf = interp_tau_smem(sm);
-        const bool want_f = c.kind == DSPARK_COST_ADDITIVE_INTERP;
+        const bool want_f = interp;
 #pragma unroll
         for (int u = 0; u < kScanReg; ++u) {
             if (lo + u < hi) {
@@ -871,25 +738,22 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
         __syncthreads();
     }
 
-    // (b) theta at the last budget of every table entry's range of M = B + b
-    if (sparse && tid <= c.n) sm.acc_s[tid] = __ldcg(&a.scratch->acc[tid]);
-    if (sparse) __syncthreads();
+    // (b) theta: at every budget of an interpolated table, else at the last
+    // budget of every table entry's range of M = B + b
     const double fixed_cost = sm.fixed_cost;
     long long my_key = -1, my_P = 0;
     int my_b = 0x7FFFFFFF;
     bool my_bad_cost = false, my_bad_table = false;
-    const bool interp = c.kind == DSPARK_COST_ADDITIVE_INTERP;
     if (interp) {
         // The cost changes with every budget.  fp32 bounds of theta at every
         // in-range budget first; the fp64 definition is then evaluated only
         // where the bounds cannot exclude the maximum (or cannot show T > 0):
         // a budget whose upper bound is below the largest lower bound cannot
         // be the first maximiser.
-        if (sm.itab_bad) my_bad_table = true;  // checked in the prologue
-        const bool itab = c.n <= kMaxSparse;      // staged in shared memory
-        const int32_t *tM = itab ? sm.M_s : c.M;
-        const double *tV = itab ? sm.val_s : c.val;
-        const float *tV32 = itab ? sm.v32_s : nullptr;
+        if (sm.order_bad) my_bad_table = true;  // checked in the prologue
+        const int32_t *tM = c.M;
+        const double *tV = c.val;
+        const float *tV32 = nullptr;  // values converted as the walk reads them
         const float fixed32 = sm.fixed32;
         if (tid == 0) {
             sm.theta_floor = 0u;
@@ -966,18 +830,8 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
         // runs only where the bounds cannot exclude the first maximiser (a
         // budget whose upper bound is below the largest lower bound cannot
         // be it), or cannot bound theta at all
-        const bool staged = staged_table(c.kind, c.n);
-        const TableStage ts = staged ? table_stage(smem, a) : TableStage{nullptr, nullptr};
-        const int b_top32 = (int)max(min(b_top, (long long)INT_MAX), -1LL);
-        if (staged && sm.itab_bad) my_bad_table = true;  // order checked in the prologue
         // entry j's last budget b (false when its range holds none) and value
         auto entry = [&](int j, int &b, float &v32) -> bool {
-            if (staged) {
-                const int2 r = ts.range[j];
-                b = min(r.y, b_top32);
-                v32 = ts.f32[j];
-                return b >= r.x;
-            }
             const int Mj = __ldg(c.M + j);
             const int Mprev = j > 0 ? __ldg(c.M + j - 1) : 0;
             const int Mnext = j < c.n - 1 ? __ldg(c.M + j + 1) : 0;
@@ -1040,33 +894,6 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
             }
         }
     }
-    for (int j = tid; j < (interp || dense ? 0 : c.n); j += kRankThreads) {
-        const int Mj = __ldg(c.M + j);
-        const double vj = sparse ? sm.val_s[j] : __ldg(c.val + j);
-        const int Mprev = j > 0 ? __ldg(c.M + j - 1) : 0;
-        const int Mnext = j < c.n - 1 ? __ldg(c.M + j + 1) : 0;
-        if (j > 0 && !(Mj > Mprev)) my_bad_table = true;
-        const int b = sparse ? sm.cand_b[j] : entry_last_budget(c, j, Mj, Mprev, Mnext, B, b_top);
-        if (b < 0) continue;
-        const long long Pb = sparse ? (long long)sm.acc_s[j] : load_P(b);
-        const double tau = tau_of(B, Pb);
-        double theta;
-        if (c.kind == DSPARK_COST_SPS_1D) {
-            if (!(vj > 0.0) || !isfinite(vj)) { my_bad_cost = true; continue; }
-            theta = __dmul_rn(tau, vj);
-        } else {
-            const double Tm = __dadd_rn(fixed_cost, vj);
-            if (!(Tm > 0.0) || !isfinite(Tm)) { my_bad_cost = true; continue; }
-            theta = __ddiv_rn(tau, Tm);
-        }
-        // positive finite doubles order like their bit patterns
-        const long long kk = __double_as_longlong(theta);
-        if (cand_better(kk, b, my_key, my_b)) {
-            my_key = kk;
-            my_b = b;
-            my_P = Pb;
-        }
-    }
     {
         unsigned long long P = (unsigned long long)my_P, unused = 0ull;
         warp_first_max(my_key, my_b, P, unused);
@@ -1110,22 +937,8 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
                     budget = (int)min((long long)forced, bh);
                 }
             }
-            // P at the budget: the candidate's accumulator (sparse) or the scan
-            if (budget > 0) {
-                if (!sparse && forced < 0) {
-                    Pbud = bP;  // carried with the best candidate
-                } else if (!sparse) {
-                    Pbud = load_P(budget);
-                } else if (forced >= 0) {
-                    Pbud = (long long)sm.acc_s[c.n];
-                } else {
-                    for (int j = 0; j < c.n; ++j)
-                        if (sm.cand_b[j] == budget) {
-                            Pbud = (long long)sm.acc_s[j];
-                            break;
-                        }
-                }
-            }
+            // P at the budget: carried with the best candidate, or the scan's
+            if (budget > 0) Pbud = forced < 0 ? bP : load_P(budget);
             if (forced >= 0 && budget == (int)min((long long)forced, b_top) && b_top >= 0 &&
                 !any_bad_table) {
                 // theta at the forced budget: the entry covering M = B + budget
@@ -1152,18 +965,6 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
             }
             if (st) flag(a.status, st);
             sm.budget = budget;
-            // sparse path: the entry whose counts hold the selection
-            int slot = -1;
-            if (sparse && budget > 0) {
-                if (forced >= 0) slot = c.n;
-                else
-                    for (int j = 0; j < c.n; ++j)
-                        if (sm.cand_b[j] == budget) {
-                            slot = j;
-                            break;
-                        }
-            }
-            sm.last = slot;
             a.budget[0] = budget;
             a.tau_theta[0] = tau_of(B, Pbud);
             a.tau_theta[1] = theta_out;
@@ -1173,19 +974,12 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
 
     // (d) a request's selected candidates are its ranks below the budget
     const int budget = sm.budget;
-    const int slot = sm.last;
     const int kmax = min(G, a.max_len - 1);
-    const int32_t *counts = scratch_at<int32_t>(a.scratch, plan_count_offset(a.N));
     int lens_sum = 0;
     for (int r = tid; r < B; r += kRankThreads) {
         int cnt = 0;
-        if (sparse) {
-            cnt = slot >= 0 && in_bounds(slot, kMaxSparse + 1, a.status)
-                      ? __ldcg(counts + (size_t)r * (kMaxSparse + 1) + slot) : 0;
-        } else {
 #pragma unroll 8
-            for (int k = 0; k < kmax; ++k) cnt += __ldcg(rank_in + r * G + k) < budget ? 1 : 0;
-        }
+        for (int k = 0; k < kmax; ++k) cnt += __ldcg(rank_in + r * G + k) < budget ? 1 : 0;
         const int L = min(max(1 + cnt, a.min_len), a.max_len);
         a.verify_lens[r] = L;
         lens_sum += L;
@@ -1196,9 +990,8 @@ __device__ void finish_plan(const PlanArgs &a, RankSmem &sm) {
     }
 }
 
-size_t rank_smem_bytes(int B, int P2, int N, int kind, int n) {
-    return rank_head_bytes() + rank_region_bytes(B, run_stride(P2), N, kind, n) +
-           rank_stage_bytes(kind, n);
+size_t rank_smem_bytes(int B, int P2, int N, int kind) {
+    return rank_head_bytes() + rank_region_bytes(B, run_stride(P2), N, kind);
 }
 
 int pow2_at_least(int g) {
@@ -1212,7 +1005,7 @@ size_t rank_smem_max() {
     size_t m = 0;
     for (int g = 1; g <= 31; ++g) {
         const int B = kMaxCandidates / g;
-        const size_t v = rank_smem_bytes(B, pow2_at_least(g), B * g, DSPARK_COST_SPS_1D, kTabStage);
+        const size_t v = rank_smem_bytes(B, pow2_at_least(g), B * g, DSPARK_COST_SPS_1D);
         m = v > m ? v : m;
     }
     return m;
@@ -2833,7 +2626,7 @@ int launch_pass(PlanArgs a, PlanPath path, cudaStream_t s) {
         return DSPARK_ERR_CUDA;
     }
     a.pk.on = false;
-    const size_t smem = rank_smem_bytes(a.B, a.P2, a.N, a.cost.kind, a.cost.n);
+    const size_t smem = rank_smem_bytes(a.B, a.P2, a.N, a.cost.kind);
     if (ensure_smem(reinterpret_cast<const void *>(rank_kernel), (int)rank_smem_max(), 0) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     // ranking is issue-bound: at least a few candidates per CTA, else every

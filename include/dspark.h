@@ -128,9 +128,10 @@ typedef struct {
     double alpha_ms;       /* additive only */
 } dspark_cost_table;
 
-/* Device scratch of one planner call: about 16 * B * gamma + 26 KB
- * (candidate ranks, the sorted survivals, a completion counter, a 2048-bin
- * histogram of the survivals, and what passes of one call hand over).  The workspace must be zero-filled
+/* Device scratch of one planner call: about 24 * B * gamma + 4 * B + 25 KB
+ * (a completion counter, a 2048-bin histogram of the survivals, candidate
+ * ranks, the sorted survivals and their prefix sums, and what passes of one
+ * call hand over).  The workspace must be zero-filled
  * once before its first dspark_plan call (cudaMemset); every call that
  * returns DSPARK_OK leaves the histogram zero again, and a call that
  * returns DSPARK_ERR_CUDA after launching clears it on the stream, so the

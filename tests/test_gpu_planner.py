@@ -125,8 +125,8 @@ def test_plan_random(dev, orc, seed):
 @pytest.mark.parametrize("seed", range(80))
 def test_plan_random_interpolated_table(dev, orc, seed):
     """The interpolated additive table (every budget its own cost; the
-    single-CTA interp path),
-    with sparse and dense tables, forced budgets and invalid entries."""
+    single-CTA interp path), with few and many samples, forced budgets and
+    invalid entries."""
     rng = np.random.default_rng(91000 + seed)
     P = _random_problem(rng)
     P["kind"] = 2
@@ -170,9 +170,9 @@ def test_plan_interpolated_table_on_the_rank_path(dev, orc, seed):
 
 def _dense_problem(rng, seed):
     """A cost table of more than 64 entries read as given (1-D floor lookup or
-    additive ceil-to-tier): the rank path's dense tables, staged in shared
-    memory up to 4608 entries and read from global memory beyond."""
-    if seed % 4 == 3:  # large: more than 4608 entries
+    additive ceil-to-tier): the single-CTA dense path up to 6143 entries,
+    the rank path beyond."""
+    if seed % 4 == 3:  # large: a table at every M can pass 6143 entries
         while True:
             B, g = int(rng.integers(200, 700)), int(rng.integers(8, 32))
             if B * g <= 16380 and B * (g + 1) <= 65536 and B * g > 4700:
@@ -313,6 +313,49 @@ def test_plan_dense_and_rank_paths_meet(dev, orc):
         ref = orc.plan(P["z"], P["T"], P["eps"], 1, g + 1, -1, 1, M, P["val"], 1.0, 0.3)
         exp = compare_plan(f"meet/{n}", gres, ref, B, g, 1, _restage(orc, P))
         assert int(gres["status"][0]) == exp.status
+
+
+def _rank_case(name):
+    """Tables that are not interpolated and have more than 6143 entries:
+    the multi-CTA rank path (prefix sums in the last CTA's shared memory,
+    every entry bounded in fp32, fp64 where the bounds cannot decide)."""
+    rng = np.random.default_rng(zlib.crc32(name.encode()))
+    B, g = 512, 16
+    z = rng.normal(1.2, 1.4, (B, g)).astype(np.float32)
+    every_M = np.arange(B, B + B * g + 1, dtype=np.int32)  # 8193 entries
+    base = dict(B=B, gamma=g, z=z, T=np.ones(g, np.float32), eps=1e-4, min_len=1, max_len=g + 1,
+                forced=-1, bias=1.0, alpha=0.3)
+    sps = 1.0 / (3e-3 + 3e-6 * every_M)
+    if name == "sps_every_M":
+        return dict(base, kind=0, M=every_M, val=sps)
+    if name == "sps_every_M_forced":
+        return dict(base, kind=0, M=every_M, val=sps, forced=3000)
+    add_M = np.arange(1, 8001, dtype=np.int32)
+    if name == "additive_8000":
+        return dict(base, kind=1, M=add_M, val=0.0025 * add_M)
+    if name == "additive_forced_bad_value":  # T < 0 at one entry: BAD_COST
+        val = 0.0025 * add_M
+        val[1000] = -50.0
+        return dict(base, kind=1, M=add_M, val=val, forced=777)
+    if name == "sps_unordered":  # M not increasing at one entry: infeasible
+        M = every_M.copy()
+        M[4000] = M[3999]
+        return dict(base, kind=0, M=M, val=sps)
+    raise KeyError(name)
+
+
+@pytest.mark.parametrize("name", ["sps_every_M", "sps_every_M_forced", "additive_8000",
+                                  "additive_forced_bad_value", "sps_unordered"])
+def test_plan_rank_path_large_tables(dev, orc, name):
+    from confidence_scheduled_speculative_gb300 import api
+    P = _rank_case(name)
+    assert api.planner_path(P["B"] * P["gamma"], P["kind"], P["M"].size) == "rank"
+    g = _gpu_plan(dev, P)
+    ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"], P["kind"],
+                   P["M"], P["val"], P["bias"], P["alpha"])
+    exp = compare_plan(f"rank/{name}", g, ref, P["B"], P["gamma"], P["min_len"],
+                       _restage(orc, P))
+    assert int(g["status"][0]) == exp.status
 
 
 @pytest.mark.parametrize("name", ["dsv4_like", "stress", "qwen_like"])
