@@ -42,10 +42,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     }
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 // Announce `bytes` of transaction on the barrier (with this thread's arrival)
 // and start a bulk copy of `bytes` from global `src` to shared `dst` that
 // completes them.  dst, src and bytes are multiples of 16.

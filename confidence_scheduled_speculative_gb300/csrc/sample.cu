@@ -346,11 +346,6 @@ __device__ __forceinline__ void row_stats(const SampArgs &a, long long cpr, long
         }
 }
 
-// p(y) of a row with statistics (M, S) from its logit z.
-__device__ __forceinline__ double row_prob(float z, float M, double S) {
-    return (z == z && S > 0.0) ? (double)__expf(z - M) / S : 0.0;
-}
-
 // Weights of the bonus draw are summed exactly as integers in units of 2^-40:
 // q = w * 2^40 rounded to the nearest integer, ties to even, from the bits of
 // the (exact) float product -- the value a round-to-nearest conversion

@@ -85,14 +85,8 @@ __global__ void __launch_bounds__(32) scatter_bulk_kernel(ScatterArgs a) {
         bulk_segment(a, spr, t0 + i, r, off, bytes);
         const int s = (int)(i % kBulkStages);
         inflight |= 1u << s;
-        const uint32_t b = smem_addr(&bar[s]);
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes)
-                     : "memory");
-        asm volatile(
-            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-            ::"r"(smem_addr(stage_buf + (size_t)s * kBulkSeg)),
-            "l"(a.src + (long long)r * a.ld_src + off), "r"(bytes), "r"(b)
-            : "memory");
+        bulk_load(smem_addr(stage_buf + (size_t)s * kBulkSeg), a.src + (long long)r * a.ld_src + off,
+                  (uint32_t)bytes, smem_addr(&bar[s]));
     };
     bool bad = false, timeout = false;
     uint32_t phase = 0;  // bit s: the parity stage s waits for next

@@ -284,16 +284,29 @@ def test_step_workloads_full_size(dev, orc, name):
 
 
 def test_step_is_deterministic(dev):
+    """The same step twice gives the same bits; the second time the plan,
+    pack and accept run again through VerifyStep.compact_step."""
     step = wl.make_step(wl.DSV4, seed=1)
     strided_dev = to_dev_logits(wl.strided_logits(step), dev)
     outs = []
-    for _ in range(2):
+    for it in range(2):
         vs, _ = run_plan_pack(dev, step)
         compact, _ = _compact_from_gpu(vs, strided_dev)
-        vs.greedy_accept(compact)
+        if it == 0:
+            vs.greedy_accept(compact)
+        else:
+            for t in (vs.survivals, vs.verify_lens, vs.packed_ids, vs.num_accepted, vs.bonus,
+                      vs.commit_lens, vs.new_seq_lens, vs.out_tokens):
+                t.fill_(-9)
+            vs.compact_step(compact)
         outs.append(vs.result())
-    for k in ("survivals", "verify_lens", "tau_theta", "packed_ids", "argmax", "out_tokens"):
+    for k in ("survivals", "verify_lens", "tau_theta") + OUT_KEYS:
         np.testing.assert_array_equal(outs[0][k], outs[1][k], err_msg=k)
+    padded = int(outs[0]["totals"][1])
+    assert int(outs[1]["totals"][1]) == padded
+    np.testing.assert_array_equal(outs[0]["packed_ids"][:padded], outs[1]["packed_ids"][:padded])
+    assert np.all(outs[1]["packed_ids"][padded:] == -9)  # rows past the padded total untouched
+    assert int(outs[1]["status"][0]) == 0
 
 
 def test_stress_full_size_sampled(dev, orc):
