@@ -212,9 +212,10 @@ class VerifyStep:
         self.pad_to_tier(None, stream)
 
     def kernels_per_step(self, separate_plan_pack: bool = False) -> int:
-        """Kernels one compact step launches: survival + select (the pack
-        inside) on the select path, else survival + rank + pack
-        (separate calls add the pack kernel); then argmax + finalize."""
+        """Kernels one compact step launches: survival + one single-CTA
+        planner kernel (select, dense or interp; the pack inside), else
+        survival + rank + pack (separate plan and pack calls add the pack
+        kernel); then argmax + finalize."""
         c = self.cfg
         select = api.planner_path(c.B * c.gamma, c.cost_kind, len(c.cost_M)) != "rank"
         return (3 if (separate_plan_pack or not select) else 2) + 2
