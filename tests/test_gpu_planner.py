@@ -654,11 +654,12 @@ def _pack_inputs(rng, B, g, total_hint):
 def test_plan_pack_fused_random(dev, orc, seed):
     """dspark_plan_pack equals the oracle's planner followed by its pack,
     including untouched rows past the window, capacity overflow and tier
-    lists with no tier above the total; tables of more than 31 entries take
-    the separate kernels."""
+    lists with no tier above the total; the single-CTA planner kernels pack
+    in the same launch, tables beyond them take the rank kernel and then the
+    pack kernel."""
     rng = np.random.default_rng(90000 + seed)
     P = _random_problem(rng)
-    if seed % 5 == 4:  # a dense 1-D table: rank path, then the pack kernel
+    if seed % 5 == 4:  # a 1-D table at every M: the dense path
         B, g = P["B"], P["gamma"]
         P["kind"] = 0
         P["M"] = np.arange(B, B + max(B * g + 2, 40), dtype=np.int32)
@@ -669,6 +670,32 @@ def test_plan_pack_fused_random(dev, orc, seed):
     ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"], P["kind"],
                    P["M"], P["val"], P["bias"], P["alpha"])
     exp = compare_plan(f"fused/{seed}", got, ref, B, g, P["min_len"], _restage(orc, P))
+    pr = orc.pack(anchor, draft, prefix, exp.verify_lens, tiers, cap, sentinel=-9)
+    np.testing.assert_array_equal(got["cu_seqlens"], pr.cu_seqlens)
+    assert list(got["totals"]) == [pr.total, pr.padded]
+    for k in ("ids", "pos", "req", "src"):
+        np.testing.assert_array_equal(got[k], pr[k][:cap], err_msg=k)
+    assert int(got["status"][0]) == (exp.status | pr.status)
+
+
+@pytest.mark.parametrize("B,g,forced", [(9000, 1, 5000), (5000, 3, -1), (5000, 3, 4000)])
+def test_plan_pack_fused_unstaged(dev, orc, B, g, forced):
+    """Batches whose pack inputs (B*(gamma+2) words) do not fit the select
+    kernel's shared-memory stage: its fused pack reads anchor / prefix /
+    drafts from global memory."""
+    rng = np.random.default_rng(B * 100 + g)
+    z = rng.normal(1.5, 1.2, (B, g)).astype(np.float32)
+    M = np.array([B // 2, B, 2 * B, 4 * B, 8 * B], np.int32)
+    P = dict(B=B, gamma=g, z=z, T=np.ones(g, np.float32), eps=1e-4, min_len=1, max_len=g + 1,
+             kind=1, M=M, val=1e-4 * M, forced=forced, bias=1.5, alpha=0.5)
+    assert B * (g + 2) > 24576
+    anchor, prefix, draft, _, _ = _pack_inputs(rng, B, g, B * (g + 1))
+    tiers, cap = [B, 2 * B, 4 * B], B * (g + 1)
+    got = _fused(dev, P, anchor, prefix, draft, tiers, cap)
+    ref = orc.plan(P["z"], P["T"], P["eps"], P["min_len"], P["max_len"], P["forced"], P["kind"],
+                   P["M"], P["val"], P["bias"], P["alpha"])
+    exp = compare_plan(f"unstaged/{B}/{g}/{forced}", got, ref, B, g, P["min_len"],
+                       _restage(orc, P))
     pr = orc.pack(anchor, draft, prefix, exp.verify_lens, tiers, cap, sentinel=-9)
     np.testing.assert_array_equal(got["cu_seqlens"], pr.cu_seqlens)
     assert list(got["totals"]) == [pr.total, pr.padded]
