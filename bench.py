@@ -20,8 +20,9 @@ host buffer over the link, results read back; ``e2e.copy_then_accept`` is
 the variant that reads the packed total back first and copies that many
 rows in before the accept.
 
---impl reference times the CPU oracle (the reference arm of this build) on
-the host cores with the same metric and workload.
+--impl reference times the CPU oracle (the reference arm: the pages print
+no runnable implementation) on the host cores with the same metric and
+workload.
 """
 
 from __future__ import annotations
